@@ -1,0 +1,5 @@
+"""f64 CPU oracle for MLA split-KV decode (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The product path never does.
+"""

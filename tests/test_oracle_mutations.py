@@ -1,0 +1,78 @@
+"""Plant plausible slips in the oracle (on the CPU) and check a pin catches each.
+
+Each mutation monkeypatches one oracle function with a version carrying a
+typical mistake; the listed pin tests must then fail. This guards the pins
+themselves: a pin that cannot see a dropped term is not a pin.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import mla_oracle as orc
+import tests.test_oracle_pins as pins
+
+
+def _drop_rope(q_abs, q_pe, ckv_rows, kpe_rows, scale):
+    return scale * (ckv_rows @ q_abs)
+
+
+def _scale_latent_only(q_abs, q_pe, ckv_rows, kpe_rows, scale):
+    return scale * (ckv_rows @ q_abs) + (kpe_rows @ q_pe)
+
+
+def _natural_log_lse(s, values):
+    if s.size == 0:
+        return np.zeros(values.shape[1]), -math.inf
+    m = float(np.max(s))
+    w = np.exp(s - m)
+    l = float(np.sum(w))
+    return (w @ values) / l, m + math.log(l)
+
+
+def _causal_off_by_one(n_tokens, q_len, i, causal):
+    t = np.arange(n_tokens)
+    if not causal:
+        return np.ones(n_tokens, dtype=bool)
+    return t < (n_tokens - q_len + i)
+
+
+def _page_slip(block_table_row, n_tokens, block_size):
+    t = np.arange(n_tokens, dtype=np.int64)
+    pages = np.asarray(block_table_row, dtype=np.int64)[t // block_size]
+    return pages * block_size + (t % block_size) + (t // block_size) % 2  # shifts odd pages by one row
+
+
+def _merge_natural(part, lse2, o_indptr):
+    B = len(o_indptr) - 1
+    out = np.zeros((B,) + part.shape[1:])
+    out_lse = np.full((B,) + part.shape[1:-1], -math.inf)
+    for b in range(B):
+        lo, hi = o_indptr[b], o_indptr[b + 1]
+        ls = lse2[lo:hi]
+        M = ls.max(axis=0)
+        w = np.exp(ls - M)  # e-base weights on log2 values
+        out[b] = np.einsum("p...,p...d->...d", w, part[lo:hi]) / w.sum(axis=0)[..., None]
+        out_lse[b] = M + np.log2(w.sum(axis=0))
+    return out, out_lse
+
+
+MUTATIONS = [
+    ("scores", _drop_rope, [pins.test_rope_score_is_additive,
+                            lambda: pins.test_matches_torch_sdpa_on_concatenated_keys("f16", 1, False)]),
+    ("scores", _scale_latent_only, [lambda: pins.test_matches_torch_sdpa_on_concatenated_keys("f16", 1, False)]),
+    ("attend", _natural_log_lse, [pins.test_zero_query_gives_uniform_mean_and_log2_count]),
+    ("visible", _causal_off_by_one, [pins.test_visible_rule_small_window,
+                                     pins.test_brute_force_pure_python_tiny]),
+    ("physical_rows", _page_slip, [pins.test_physical_rows_hand_table,
+                                   lambda: pins.test_matches_torch_sdpa_on_concatenated_keys("f16", 1, False)]),
+    ("merge", _merge_natural, [pins.test_merge_weights_are_base_two]),
+]
+
+
+@pytest.mark.parametrize("name,fn,tests", MUTATIONS, ids=[m[1].__name__ for m in MUTATIONS])
+def test_planted_mistake_is_caught(monkeypatch, name, fn, tests):
+    monkeypatch.setattr(orc, name, fn)
+    for t in tests:
+        with pytest.raises((AssertionError, ValueError, IndexError)):
+            t()
