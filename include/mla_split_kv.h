@@ -1,0 +1,255 @@
+/*
+ * mla_split_kv.h -- C ABI of the GB300 (sm_103a) MLA split-KV decode library.
+ *
+ * Matrix-absorbed MLA decode over a paged compressed-latent KV cache. Every
+ * cached token holds a 512-wide latent `ckv` (the key *and* the value of
+ * absorbed attention) and a 64-wide rotary key `kpe`. A decode call is
+ *
+ *     mla_plan            (host)   pick partitions per request, cut each
+ *                                  request's tokens into block-aligned chunks
+ *     mla_decode_partial  (device) one normalized fp32 partial + base-2 LSE
+ *                                  per (chunk, query row, head)
+ *     mla_merge_states    (device) LSE-weighted merge of a request's partials,
+ *                                  rounded once to the output dtype
+ *
+ * Sources of the operation (web pages; cited by title and section):
+ *  - "feat(core): matrix-absorbed MLA decode over a compressed-latent KV cache"
+ *    (mlxcel PR #995), *What changed*: absorbed decode is
+ *    SDPA(q_absorbed, ckv, ckv, scale, mask = scale * q_pe @ kpe^T + causal);
+ *    Stage 2 cuts the latent range into chunks, each producing a normalized
+ *    partial and its log2 LSE; *How #898's merge kernel is reused*: the merge
+ *    contract H = num_heads, D = kv_lora_rank, M = batch, N = batch * chunks,
+ *    o_indptr request-major, LSE in base 2.
+ *  - "[kernel] Wire MLA split-KV decode" (vllm-metal PR #601), *What changed*:
+ *    the decode kernel runs over a slice of the context; a reduce kernel
+ *    combines slices by their LSE; host dispatch picks the split only for
+ *    conservative cases (pure decode, long context, small launch, 2 to 8
+ *    partitions, bounded temporary memory). Review: thresholds belong in a
+ *    device-aware split-plan helper, and tests must assert the chosen plan.
+ *  - MTPLX PR #639, commit log: segments of a non-contiguous history are
+ *    attended separately and merged by LSE; a row with no visible key has
+ *    LSE = -inf, weight 0 and merges to zeros; fp32 per-segment outputs are
+ *    rounded once, after the merge; unsupported shapes bail without a launch.
+ *
+ * Conventions for every call:
+ *  - All device buffers are caller-owned and stay owned by the caller. The
+ *    library never allocates device memory in these calls and never
+ *    synchronizes the stream; work is enqueued on `stream` (a cudaStream_t
+ *    passed as void*, NULL = the legacy default stream).
+ *  - Argument and shape errors are detected on the host and returned before
+ *    anything is launched (the launch counters do not move).
+ *  - Layouts are dense row-major with the innermost dimension last.
+ *  - Supported: num_heads in {16, 64, 128}; kv_lora_rank 512; rope dim 64;
+ *    block_size in {16, 32, 64}; q_len in [1, 32]; fp16 or bf16 inputs.
+ *    Anything else returns MLA_ERR_UNSUPPORTED.
+ */
+#ifndef MLA_SPLIT_KV_H
+#define MLA_SPLIT_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_KV_LORA_RANK 512
+#define MLA_ROPE_DIM 64
+#define MLA_MAX_Q_LEN 32
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned buffer       */
+  MLA_ERR_UNSUPPORTED = 2,  /* shape or dtype outside the supported set       */
+  MLA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed     */
+  MLA_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out              */
+  MLA_ERR_DEVICE_CHECK = 5, /* the device flagged bad data (e.g. page id)      */
+  MLA_ERR_CAPACITY = 6      /* caller-provided plan arrays are too small       */
+} mla_status_t;
+
+typedef enum { MLA_F16 = 0, MLA_BF16 = 1, MLA_F32 = 2 } mla_dtype_t;
+
+/* Which partial-decode kernel runs. AUTO picks the tensor-core kernel. */
+typedef enum {
+  MLA_KERNEL_AUTO = 0,
+  MLA_KERNEL_SIMT = 1, /* CUDA-core fp32 FMA kernel                          */
+  MLA_KERNEL_TC = 2    /* tcgen05/TMEM tensor-core kernel                     */
+} mla_kernel_t;
+
+/* One partition: logical tokens [t0, t1) of request b; its partial and LSE go
+ * to row `out_slot` of the partials/lse buffers. */
+typedef struct {
+  int32_t b, t0, t1, out_slot;
+} mla_chunk_t;
+
+/* Device facts the planner sizes the launch by (mla_device_query fills it;
+ * tests may fill it by hand). max_clusters[k] = co-resident clusters of 2^k
+ * CTAs of the partial kernel (k = 0..4), 0 when that size cannot launch. */
+typedef struct {
+  int32_t num_sms;
+  int32_t max_clusters[5];
+} mla_device_info_t;
+
+/*
+ * mla_device_query -- fill *info for CUDA device `device` (-1 = current).
+ * Returns MLA_ERR_CUDA when no device is usable.
+ */
+mla_status_t mla_device_query(int32_t device, mla_device_info_t* info);
+
+/* Planner input/output. The caller sets the inputs and provides the host
+ * arrays; mla_plan fills the outputs. */
+typedef struct {
+  /* inputs */
+  int32_t max_partitions;   /* per-request cap; 0 = 8 (the pages' 2..8 gate)  */
+  int32_t min_partitions;   /* floor for a request that is split; 0 = 2       */
+  int32_t split_min_tokens; /* contexts shorter than this are not split;
+                               0 = 4096                                        */
+  int32_t dtype;            /* MLA_F16 or MLA_BF16 (sets rows per CTA)         */
+  int32_t capacity;         /* entries available in `chunks`                   */
+  mla_chunk_t* chunks;      /* host, caller-owned, >= capacity entries         */
+  int32_t* o_indptr;        /* host, caller-owned, >= B+1 entries              */
+  /* outputs */
+  int32_t num_chunks;       /* N = sum_b P_b                                   */
+  int32_t cluster_ctas;     /* CTAs that share one partition (1,2,4,8,16)      */
+  int32_t kernel;           /* mla_kernel_t the plan was sized for             */
+} mla_plan_t;
+
+/*
+ * mla_plan -- choose P_b partitions per request and cut [0, L_b) into P_b
+ * contiguous block-aligned chunks (vllm-metal PR #601 *What changed*: host
+ * dispatch picks the split; mlxcel PR #995 `MlaSplitPlan` cuts the latent
+ * range). Chunk p of request b covers [min(p*C, L), min((p+1)*C, L)) with
+ * C = ceil(ceil(L/P)/bs)*bs. Chunks are emitted request-major, out_slot = the
+ * chunk's index, o_indptr[b] = first chunk of request b, o_indptr[B] = N.
+ *
+ * Rule (device-aware): a request shorter than split_min_tokens gets P = 1;
+ * otherwise P_b is proportional to L_b so that all partitions fill one wave
+ * of the device's co-resident clusters, clamped to [min, max] partitions and
+ * so that no chunk is empty. cluster_ctas is the cluster size that keeps the
+ * most CTAs busy in that wave with at least one 64-token tile per CTA.
+ *
+ * context_lens_host: host [B] int32, each >= 0. dev: from mla_device_query or
+ * hand-filled. Returns MLA_ERR_CAPACITY when N > plan->capacity (num_chunks
+ * then holds the size needed), MLA_ERR_INVALID_ARG / MLA_ERR_UNSUPPORTED for
+ * bad arguments. Pure host code; touches no GPU.
+ */
+mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, int32_t num_heads,
+                      int32_t q_len, int32_t block_size, const mla_device_info_t* dev,
+                      mla_plan_t* plan);
+
+/* Shapes and launch options of mla_decode_partial. */
+typedef struct {
+  int32_t num_requests;       /* B                                            */
+  int32_t num_heads;          /* H in {16, 64, 128}                           */
+  int32_t q_len;              /* query rows per request, 1..32                */
+  int32_t block_size;         /* tokens per page: 16, 32 or 64                */
+  int32_t num_blocks;         /* pages in the cache pool                      */
+  int32_t max_blocks_per_req; /* row stride of block_table, in entries        */
+  int32_t dtype;              /* MLA_F16 or MLA_BF16 (q, ckv, kpe)            */
+  int32_t causal;             /* 1: the q_len rows are the last q_len tokens
+                                 of each request; row i sees t <= L-q_len+i    */
+  const mla_chunk_t* chunks;  /* DEVICE array of num_chunks records, or NULL
+                                 for a uniform split into num_partitions       */
+  int32_t num_chunks;         /* records in `chunks` (ignored when NULL)      */
+  int32_t cluster_ctas;       /* CTAs per partition: 1,2,4,8,16; 0 = auto     */
+  int32_t kernel;             /* mla_kernel_t                                 */
+  void* stream;               /* cudaStream_t                                 */
+} mla_decode_desc_t;
+
+/*
+ * mla_decode_partial -- attention of every query row over one chunk of its
+ * request's cached tokens, as a normalized partial and a base-2 LSE
+ * (mlxcel PR #995 *What changed*, `mla/decode.rs` and `mla/split_kv.rs`;
+ * vllm-metal PR #601 *What changed*, slice-capable `paged_mla_attention`).
+ *
+ * For request b, query row i (0 <= i < q_len), head h and chunk [t0, t1):
+ *   s_t   = scale * (q_absorbed[b,i,h,:] . ckv[t,:]) + scale * (q_pe[b,i,h,:] . kpe[t,:])
+ *           over the visible tokens t in [t0, t1) (all of them, or
+ *           t <= L_b - q_len + i when causal)
+ *   partial[slot,i,h,:] = sum_t softmax(s)_t * ckv[t,:]      (fp32)
+ *   lse[slot,i,h]       = log2 sum_t exp(s_t)                (fp32)
+ * An empty chunk (or a row with no visible token) gives partial = 0 and
+ * lse = -inf. The token t of request b lives in cache row
+ * block_table[b, t / bs] * bs + t % bs.
+ *
+ * q_absorbed : device [B, q_len, H, 512] dtype, 16-byte aligned
+ * q_pe       : device [B, q_len, H, 64]  dtype, 16-byte aligned
+ * ckv_cache  : device [num_blocks, bs, 512] dtype, 16-byte aligned
+ * kpe_cache  : device [num_blocks, bs, 64]  dtype, 16-byte aligned
+ * block_table: device [B, max_blocks_per_req] int32; entries past a request's
+ *              last page are never read. An entry outside [0, num_blocks)
+ *              reads zeros and raises MLA_ERR_DEVICE_CHECK at the next
+ *              mla_check_device_errors.
+ * context_lens: device [B] int32
+ * scale      : softmax scale applied to both score terms
+ * num_partitions: with desc->chunks == NULL, every request is split into this
+ *              many chunks by the planner's chunk rule and chunk n = b*P + p
+ *              writes slot n; ignored otherwise.
+ * partials   : device [num_slots, q_len, H, 512] fp32 (written)
+ * lse        : device [num_slots, q_len, H] fp32 (written)
+ * Returns MLA_OK once the kernel is enqueued.
+ */
+mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const void* ckv_cache,
+                                const void* kpe_cache, const int32_t* block_table,
+                                const int32_t* context_lens, float scale, int32_t num_partitions,
+                                float* partials, float* lse, const mla_decode_desc_t* desc);
+
+/*
+ * mla_merge_states -- merge each request's partials by their base-2 LSE
+ * (mlxcel PR #995 *How #898's merge kernel is reused*: the contract of
+ * paged_attention_merge_states; vllm-metal PR #601: paged_mla_attention_reduce;
+ * MTPLX PR #639: -inf rows and a single rounding after the merge).
+ *
+ * For request b (partials o_indptr[b] .. o_indptr[b+1]-1), row i, head h:
+ *   M = max_p lse_p; if M = -inf: out = 0, out_lse = -inf;
+ *   else w_p = 2^(lse_p - M), out = sum_p w_p partial_p / sum_p w_p,
+ *        out_lse = M + log2 sum_p w_p.
+ * The sum runs in fixed p order (bitwise reproducible) and `out` is rounded
+ * once, to nearest-even, to out_dtype.
+ *
+ * partials : device [N, q_len, H, 512] fp32;  lse: device [N, q_len, H] fp32
+ * o_indptr : device [B+1] int32, non-decreasing, o_indptr[0] = 0
+ * out      : device [B, q_len, H, 512] of out_dtype (MLA_F16/BF16/F32)
+ * out_lse  : device [B, q_len, H] fp32, or NULL
+ */
+mla_status_t mla_merge_states(const float* partials, const float* lse, const int32_t* o_indptr,
+                              int32_t B, int32_t q_len, int32_t num_heads, void* out,
+                              int32_t out_dtype, float* out_lse, void* stream);
+
+/*
+ * mla_check_device_errors -- synchronize `stream`, read and clear the device
+ * error word the kernels set (bounded-wait timeout, out-of-range page id).
+ * *code_out (nullable) receives the raw word. Returns MLA_OK when it was 0,
+ * MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_CHECK otherwise.
+ */
+mla_status_t mla_check_device_errors(void* stream, uint32_t* code_out);
+
+/* Launch counters proving which kernel ran (mlxcel PR #995 `mla/stats.rs`:
+ * per-path counters read around a measured region). Indices: */
+#define MLA_CTR_PARTIAL_SIMT 0
+#define MLA_CTR_PARTIAL_TC 1
+#define MLA_CTR_MERGE 2
+#define MLA_CTR_REJECTED 3
+#define MLA_CTR_CTAS 4 /* CTAs launched by partial kernels */
+#define MLA_NUM_COUNTERS 5
+/* mla_get_counters -- copy min(n, MLA_NUM_COUNTERS) counters to out (host). */
+void mla_get_counters(uint64_t* out, int32_t n);
+void mla_reset_counters(void);
+
+/* The bounded device waits give up after this many nanoseconds (default
+ * 2e9), flag MLA_ERR_TIMEOUT and let the kernel exit. Host state; applies to
+ * launches issued after the call. */
+void mla_set_wait_timeout_ns(uint64_t ns);
+
+/* Bytes of the partials and lse buffers for N slots. */
+size_t mla_partials_bytes(int32_t num_slots, int32_t q_len, int32_t num_heads);
+size_t mla_lse_bytes(int32_t num_slots, int32_t q_len, int32_t num_heads);
+
+const char* mla_status_string(mla_status_t status);
+int32_t mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_SPLIT_KV_H */

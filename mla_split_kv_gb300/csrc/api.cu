@@ -1,0 +1,278 @@
+// C ABI entry points: argument checks (before any launch), TMA tensor-map
+// setup, kernel dispatch, launch counters and the device error word.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "mla_split_kv.h"
+
+namespace {
+
+std::atomic<uint64_t> g_counters[MLA_NUM_COUNTERS];
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, fetched through the runtime so that the
+// library itself does not link the driver library.
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2D map over a [rows, cols] 16-bit matrix, boxes of 64 columns x box_rows
+// rows, 128-byte swizzle (the layout both partial kernels read).
+struct MapKey {
+  const void* base;
+  uint64_t rows, cols;
+  uint32_t box_rows;
+  int dtype;
+  int device;
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool valid;
+};
+std::mutex g_map_mu;
+MapEntry g_maps[32];
+int g_map_next = 0;
+
+bool same(const MapKey& a, const MapKey& b) {
+  return a.base == b.base && a.rows == b.rows && a.cols == b.cols && a.box_rows == b.box_rows && a.dtype == b.dtype &&
+         a.device == b.device;
+}
+
+bool tensor_map(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, int dtype) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const MapKey key{base, rows, cols, box_rows, dtype, dev};
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  for (auto& e : g_maps)
+    if (e.valid && same(e.key, key)) {
+      *out = e.map;
+      return true;
+    }
+  EncodeTiledFn enc = encoder();
+  if (enc == nullptr) return false;
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof(m));
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(mla::kBoxCols), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(&m, dtype == MLA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  g_maps[g_map_next] = MapEntry{key, m, true};
+  g_map_next = (g_map_next + 1) % 32;
+  *out = m;
+  return true;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+mla_status_t reject(mla_status_t s) {
+  g_counters[MLA_CTR_REJECTED].fetch_add(1, std::memory_order_relaxed);
+  return s;
+}
+
+bool valid_heads(int32_t H) { return H == 16 || H == 64 || H == 128; }
+
+// Cluster size when the caller leaves it to the library: enough CTAs to cover
+// the SMs once, at most 16.
+int default_cluster(int64_t grid_yz) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  int C = 1;
+  while (C < 16 && static_cast<int64_t>(C) * 2 * grid_yz <= sms) C *= 2;
+  return C;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_device_query(int32_t device, mla_device_info_t* info) {
+  if (info == nullptr) return MLA_ERR_INVALID_ARG;
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return MLA_ERR_CUDA;
+  const int dev = device < 0 ? prev : device;
+  if (cudaSetDevice(dev) != cudaSuccess) return MLA_ERR_CUDA;
+  int sms = 0;
+  mla_status_t st = MLA_OK;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) st = MLA_ERR_CUDA;
+  info->num_sms = sms;
+  for (int k = 0; k < 5; ++k)
+    info->max_clusters[k] = (st == MLA_OK) ? mla::tc_max_active_clusters(1 << k, 16, false) : 0;
+  cudaGetLastError();
+  cudaSetDevice(prev);
+  return st;
+}
+
+mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const void* ckv_cache,
+                                const void* kpe_cache, const int32_t* block_table, const int32_t* context_lens,
+                                float scale, int32_t num_partitions, float* partials, float* lse,
+                                const mla_decode_desc_t* d) {
+  if (d == nullptr || q_absorbed == nullptr || q_pe == nullptr || ckv_cache == nullptr || kpe_cache == nullptr ||
+      block_table == nullptr || context_lens == nullptr || partials == nullptr || lse == nullptr)
+    return reject(MLA_ERR_INVALID_ARG);
+  if (d->num_requests < 1 || d->num_blocks < 1 || d->max_blocks_per_req < 1) return reject(MLA_ERR_INVALID_ARG);
+  if (!valid_heads(d->num_heads) || d->q_len < 1 || d->q_len > MLA_MAX_Q_LEN) return reject(MLA_ERR_UNSUPPORTED);
+  if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64) return reject(MLA_ERR_UNSUPPORTED);
+  if (d->dtype != MLA_F16 && d->dtype != MLA_BF16) return reject(MLA_ERR_UNSUPPORTED);
+  if (d->causal != 0 && d->causal != 1) return reject(MLA_ERR_INVALID_ARG);
+  if (d->kernel < MLA_KERNEL_AUTO || d->kernel > MLA_KERNEL_TC) return reject(MLA_ERR_INVALID_ARG);
+  const int32_t C0 = d->cluster_ctas;
+  if (C0 != 0 && C0 != 1 && C0 != 2 && C0 != 4 && C0 != 8 && C0 != 16) return reject(MLA_ERR_INVALID_ARG);
+  if (!std::isfinite(scale)) return reject(MLA_ERR_INVALID_ARG);
+  int64_t N;
+  if (d->chunks == nullptr) {
+    if (num_partitions < 1 || num_partitions > 1024) return reject(MLA_ERR_INVALID_ARG);
+    N = static_cast<int64_t>(d->num_requests) * num_partitions;
+  } else {
+    if (d->num_chunks < 1 || !aligned(d->chunks, 16)) return reject(MLA_ERR_INVALID_ARG);
+    N = d->num_chunks;
+  }
+  if (N > 65535) return reject(MLA_ERR_UNSUPPORTED);
+  if (!aligned(q_absorbed, 16) || !aligned(q_pe, 16) || !aligned(ckv_cache, 16) || !aligned(kpe_cache, 16) ||
+      !aligned(partials, 16) || !aligned(lse, 4) || !aligned(block_table, 4) || !aligned(context_lens, 4))
+    return reject(MLA_ERR_INVALID_ARG);
+  const uint64_t rows = static_cast<uint64_t>(d->num_blocks) * static_cast<uint64_t>(d->block_size);
+  if (rows > 0x7fffffffull) return reject(MLA_ERR_UNSUPPORTED);
+
+  CUtensorMap tm_ckv, tm_kpe;
+  if (!tensor_map(&tm_ckv, ckv_cache, rows, mla::kRank, d->block_size, d->dtype) ||
+      !tensor_map(&tm_kpe, kpe_cache, rows, mla::kRope, d->block_size, d->dtype))
+    return reject(MLA_ERR_CUDA);
+
+  mla::PartialParams p;
+  p.q_abs = static_cast<const uint16_t*>(q_absorbed);
+  p.q_pe = static_cast<const uint16_t*>(q_pe);
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.chunks = d->chunks;
+  p.partials = partials;
+  p.lse = lse;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.B = d->num_requests;
+  p.H = d->num_heads;
+  p.q_len = d->q_len;
+  p.bs = d->block_size;
+  p.max_blocks = d->max_blocks_per_req;
+  p.num_blocks = d->num_blocks;
+  p.num_parts = (d->chunks == nullptr) ? num_partitions : 1;
+  p.causal = d->causal;
+  p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+
+  const bool use_simt = (d->kernel == MLA_KERNEL_SIMT);
+  const bool bf16 = (d->dtype == MLA_BF16);
+  const int rows_total = d->num_heads * d->q_len;
+  const int nr = use_simt ? mla::simt_rows_per_cta() : mla::tc_rows_per_cta(rows_total, bf16);
+  const int64_t groups = (rows_total + nr - 1) / nr;
+  const int C = C0 ? C0 : default_cluster(N * groups);
+  cudaStream_t stream = static_cast<cudaStream_t>(d->stream);
+  const cudaError_t e = use_simt ? mla::launch_partial_simt(tm_ckv, tm_kpe, p, static_cast<int>(N), C, bf16, stream)
+                                 : mla::launch_partial_tc(tm_ckv, tm_kpe, p, static_cast<int>(N), C, bf16, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  g_counters[use_simt ? MLA_CTR_PARTIAL_SIMT : MLA_CTR_PARTIAL_TC].fetch_add(1, std::memory_order_relaxed);
+  g_counters[MLA_CTR_CTAS].fetch_add(static_cast<uint64_t>(N * groups * C), std::memory_order_relaxed);
+  return MLA_OK;
+}
+
+mla_status_t mla_merge_states(const float* partials, const float* lse, const int32_t* o_indptr, int32_t B,
+                              int32_t q_len, int32_t num_heads, void* out, int32_t out_dtype, float* out_lse,
+                              void* stream) {
+  if (partials == nullptr || lse == nullptr || o_indptr == nullptr || out == nullptr) return reject(MLA_ERR_INVALID_ARG);
+  if (B < 1 || B > (1 << 24)) return reject(MLA_ERR_INVALID_ARG);
+  if (!valid_heads(num_heads) || q_len < 1 || q_len > MLA_MAX_Q_LEN) return reject(MLA_ERR_UNSUPPORTED);
+  if (out_dtype != MLA_F16 && out_dtype != MLA_BF16 && out_dtype != MLA_F32) return reject(MLA_ERR_UNSUPPORTED);
+  if (!aligned(partials, 16) || !aligned(lse, 4) || !aligned(o_indptr, 4) || !aligned(out, 16) ||
+      (out_lse != nullptr && !aligned(out_lse, 4)))
+    return reject(MLA_ERR_INVALID_ARG);
+  mla::MergeParams p;
+  p.partials = partials;
+  p.lse = lse;
+  p.o_indptr = o_indptr;
+  p.out = out;
+  p.out_lse = out_lse;
+  p.B = B;
+  p.rows = q_len * num_heads;
+  p.out_dtype = out_dtype;
+  const cudaError_t e = mla::launch_merge(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  g_counters[MLA_CTR_MERGE].fetch_add(1, std::memory_order_relaxed);
+  return MLA_OK;
+}
+
+mla_status_t mla_check_device_errors(void* stream, uint32_t* code_out) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+  uint32_t a = 0, b = 0;
+  if (mla::simt_read_clear_error(&a) != cudaSuccess || mla::tc_read_clear_error(&b) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  const uint32_t code = a | b;
+  if (code_out != nullptr) *code_out = code;
+  if (code & mla::MLA_DEVERR_TIMEOUT) return MLA_ERR_TIMEOUT;
+  if (code != 0) return MLA_ERR_DEVICE_CHECK;
+  return MLA_OK;
+}
+
+void mla_get_counters(uint64_t* out, int32_t n) {
+  if (out == nullptr) return;
+  for (int32_t i = 0; i < n && i < MLA_NUM_COUNTERS; ++i) out[i] = g_counters[i].load(std::memory_order_relaxed);
+}
+
+void mla_reset_counters(void) {
+  for (auto& c : g_counters) c.store(0, std::memory_order_relaxed);
+}
+
+void mla_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns, std::memory_order_relaxed); }
+
+size_t mla_partials_bytes(int32_t num_slots, int32_t q_len, int32_t num_heads) {
+  if (num_slots < 0 || q_len < 0 || num_heads < 0) return 0;
+  return static_cast<size_t>(num_slots) * q_len * num_heads * mla::kRank * sizeof(float);
+}
+
+size_t mla_lse_bytes(int32_t num_slots, int32_t q_len, int32_t num_heads) {
+  if (num_slots < 0 || q_len < 0 || num_heads < 0) return 0;
+  return static_cast<size_t>(num_slots) * q_len * num_heads * sizeof(float);
+}
+
+const char* mla_status_string(mla_status_t s) {
+  switch (s) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_TIMEOUT: return "device wait timed out";
+    case MLA_ERR_DEVICE_CHECK: return "device data check failed";
+    case MLA_ERR_CAPACITY: return "plan capacity too small";
+  }
+  return "unknown status";
+}
+
+int32_t mla_version(void) { return 1; }
+
+}  // extern "C"

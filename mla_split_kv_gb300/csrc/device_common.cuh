@@ -1,0 +1,384 @@
+// Device helpers shared by the sm_103a kernels: mbarriers with bounded waits,
+// TMA tile loads, tcgen05 (MMA, TMEM load/store/alloc), cluster barriers and
+// distributed shared memory. Inline PTX only; no third-party headers.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+
+namespace mla {
+
+// Device error word of this translation unit (each kernel file has its own),
+// read and cleared by mla_check_device_errors.
+static __device__ uint32_t g_device_error;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void flag_error(uint32_t bits) { atomicOr(&g_device_error, bits); }
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase with the given parity to complete. Gives up after
+// `timeout_ns` of wall time, flags MLA_DEVERR_TIMEOUT and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      flag_error(MLA_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA (tensor tile loads into shared memory, completion on an mbarrier)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+// 2D tile load: box origin (x = innermost element index, y = row).
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Named barrier over `count` threads (multiple of 32), id 1..15.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Thread-block cluster and distributed shared memory
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(local)), "r"(rank));
+  return out;
+}
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05: tensor memory and the 5th-generation MMA
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
+__device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Warp loads 32 lanes x 16 consecutive 32-bit columns (lane = thread).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle.
+// start/lbo/sbo in bytes; the fixed "version" field (bits 46-47) is 1.
+// K-major operands: sbo = stride between 8-row groups (lbo unused).
+// MN-major operands: lbo = stride between 64-element MN blocks, sbo = stride
+// between 8-row K groups.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t start, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((start >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;  // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16 with an fp32 accumulator.
+// a_mn / b_mn: operand stored MN-major (1) or K-major (0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool bf16, bool a_mn, bool b_mn) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Byte offset of element (row, col) inside a [rows x 64] 16-bit tile stored
+// with the 128-byte swizzle (rows of 128 bytes; the 16-byte chunk index is
+// XORed with row % 8). The tile base must be 1024-byte aligned.
+__device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
+  return row * 128u + ((((col >> 3) ^ row) & 7u) << 4) + ((col & 7u) << 1);
+}
+
+// ---------------------------------------------------------------------------
+// 16-bit conversions
+// ---------------------------------------------------------------------------
+template <bool BF16>
+__device__ __forceinline__ float h2f(uint16_t v) {
+  if constexpr (BF16) {
+    return __uint_as_float(static_cast<uint32_t>(v) << 16);
+  } else {
+    return __half2float(__ushort_as_half(v));
+  }
+}
+template <bool BF16>
+__device__ __forceinline__ uint16_t f2h(float v) {
+  if constexpr (BF16) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  } else {
+    return __half_as_ushort(__float2half_rn(v));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Work of one CTA: request, chunk bounds, output slot, token sub-range.
+// ---------------------------------------------------------------------------
+struct CtaWork {
+  int32_t b, t0, t1, slot;  // chunk
+  int32_t L;                // context length of request b
+  int32_t sub0, sub1;       // this CTA's tokens [sub0, sub1)
+  int32_t row0, nrows;      // query rows [row0, row0 + nrows) of this CTA
+};
+
+// Chunk rule shared with the planner: C = ceil(ceil(L/P)/bs)*bs.
+__device__ __forceinline__ void uniform_chunk(int32_t L, int32_t P, int32_t p, int32_t bs, int32_t* t0,
+                                              int32_t* t1) {
+  int32_t per = (L + P - 1) / P;
+  int32_t C = ((per + bs - 1) / bs) * bs;
+  if (C < bs) C = bs;
+  long long a = static_cast<long long>(p) * C, e = static_cast<long long>(p + 1) * C;
+  *t0 = static_cast<int32_t>(a < L ? a : L);
+  *t1 = static_cast<int32_t>(e < L ? e : L);
+}
+
+// Fill the chunk, the CTA's token sub-range (64-token units split evenly over
+// the cluster) and its query rows. Tokens are trimmed to the last one any row
+// of this CTA can see under the causal rule.
+__device__ __forceinline__ CtaWork cta_work(const PartialParams& p, int32_t rows_per_cta) {
+  CtaWork w;
+  const int32_t n = blockIdx.y;
+  if (p.chunks != nullptr) {
+    const int4 c = reinterpret_cast<const int4*>(p.chunks)[n];
+    w.b = c.x;
+    w.t0 = c.y;
+    w.t1 = c.z;
+    w.slot = c.w;
+  } else {
+    w.b = n / p.num_parts;
+    w.slot = n;
+    w.t0 = 0;
+    w.t1 = 0;
+  }
+  w.L = 0;
+  if (w.b >= 0 && w.b < p.B) w.L = p.context_lens[w.b];
+  if (w.L < 0) w.L = 0;
+  if (p.chunks == nullptr) uniform_chunk(w.L, p.num_parts, n % p.num_parts, p.bs, &w.t0, &w.t1);
+  if (w.t1 > w.L) w.t1 = w.L;
+  if (w.t0 < 0) w.t0 = 0;
+  if (w.t0 > w.t1) w.t0 = w.t1;
+  w.row0 = blockIdx.z * rows_per_cta;
+  const int32_t total_rows = p.q_len * p.H;
+  w.nrows = total_rows - w.row0;
+  if (w.nrows > rows_per_cta) w.nrows = rows_per_cta;
+  if (w.nrows < 0) w.nrows = 0;
+  int32_t tend = w.t1;
+  if (p.causal && w.nrows > 0) {
+    const int32_t i_last = (w.row0 + w.nrows - 1) / p.H;
+    const int32_t lim = w.L - p.q_len + i_last + 1;  // exclusive bound of visible tokens
+    if (tend > lim) tend = lim;
+    if (tend < w.t0) tend = w.t0;
+  }
+  const int32_t units = (tend - w.t0 + kTileTokens - 1) / kTileTokens;
+  const int32_t C = static_cast<int32_t>(cluster_nctarank());
+  const int32_t k = static_cast<int32_t>(cluster_ctarank());
+  const int32_t u0 = static_cast<int32_t>((static_cast<long long>(units) * k) / C);
+  const int32_t u1 = static_cast<int32_t>((static_cast<long long>(units) * (k + 1)) / C);
+  w.sub0 = w.t0 + u0 * kTileTokens;
+  w.sub1 = w.t0 + u1 * kTileTokens;
+  if (w.sub1 > tend) w.sub1 = tend;
+  if (w.sub0 > w.sub1) w.sub0 = w.sub1;
+  return w;
+}
+
+// Page id of logical page `pg` of request b, with a range check: an entry
+// outside [0, num_blocks) is flagged and mapped to -1 (TMA then reads zeros).
+__device__ __forceinline__ int32_t checked_page(const PartialParams& p, int32_t b, int32_t pg) {
+  int32_t pid = __ldg(p.block_table + static_cast<long long>(b) * p.max_blocks + pg);
+  if (pid < 0 || pid >= p.num_blocks) {
+    flag_error(MLA_DEVERR_BAD_PAGE);
+    pid = -1;
+  }
+  return pid;
+}
+
+// Combine the (max, sum, O) staged by the CTAs of this cluster: this CTA
+// writes columns [rank*512/C, (rank+1)*512/C) of each of its rows, rank 0
+// also the LSE. Fixed rank order, so the result is bitwise reproducible.
+// `ostage` is [rows][512] fp32, `mst`/`lst` [rows] fp32, same offsets in every CTA.
+__device__ __forceinline__ void cluster_combine(const PartialParams& p, const CtaWork& w, const float* ostage,
+                                                const float* mst, const float* lst, int tid, int nthreads) {
+  const int rows_total = p.q_len * p.H;
+  const uint32_t C = cluster_nctarank(), kr = cluster_ctarank();
+  const int dcols = kRank / static_cast<int>(C);
+  const int dbeg = static_cast<int>(kr) * dcols;
+  const int n4 = dcols / 4;
+  for (int idx = tid; idx < w.nrows * n4; idx += nthreads) {
+    const int r = idx / n4, d = dbeg + (idx % n4) * 4;
+    float M = -INFINITY;
+    for (uint32_t j = 0; j < C; ++j) M = fmaxf(M, dsmem_ld_f32(dsmem_addr(mst + r, j)));
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+    if (M != -INFINITY) {
+      for (uint32_t j = 0; j < C; ++j) {
+        const float mj = dsmem_ld_f32(dsmem_addr(mst + r, j));
+        const float wj = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
+        den = fmaf(wj, dsmem_ld_f32(dsmem_addr(lst + r, j)), den);
+        const float4 v = dsmem_ld_f32x4(dsmem_addr(ostage + r * kRank + d, j));
+        num.x = fmaf(wj, v.x, num.x);
+        num.y = fmaf(wj, v.y, num.y);
+        num.z = fmaf(wj, v.z, num.z);
+        num.w = fmaf(wj, v.w, num.w);
+      }
+    }
+    float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) out = make_float4(num.x / den, num.y / den, num.z / den, num.w / den);
+    const long long base = (static_cast<long long>(w.slot) * rows_total + w.row0 + r) * kRank + d;
+    *reinterpret_cast<float4*>(p.partials + base) = out;
+  }
+  if (kr == 0) {
+    for (int r = tid; r < w.nrows; r += nthreads) {
+      float M = -INFINITY;
+      for (uint32_t j = 0; j < C; ++j) M = fmaxf(M, dsmem_ld_f32(dsmem_addr(mst + r, j)));
+      float den = 0.f;
+      if (M != -INFINITY)
+        for (uint32_t j = 0; j < C; ++j) {
+          const float mj = dsmem_ld_f32(dsmem_addr(mst + r, j));
+          const float wj = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
+          den = fmaf(wj, dsmem_ld_f32(dsmem_addr(lst + r, j)), den);
+        }
+      p.lse[static_cast<long long>(w.slot) * rows_total + w.row0 + r] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
+    }
+  }
+}
+
+}  // namespace mla

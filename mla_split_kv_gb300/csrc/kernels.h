@@ -1,0 +1,65 @@
+// Internal interface between the C-ABI layer and the kernels (not installed).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mla {
+
+constexpr int kRank = 512;        // kv_lora_rank: width of ckv
+constexpr int kRope = 64;         // rope dim: width of kpe
+constexpr int kQkDim = kRank + kRope;
+constexpr int kTileTokens = 64;   // tokens per pipeline tile
+constexpr int kBoxCols = 64;      // 16-bit columns per TMA box (128 bytes)
+constexpr int kBoxesPerTile = kQkDim / kBoxCols;  // 8 ckv boxes + 1 kpe box
+constexpr int kBoxBytes = kTileTokens * kBoxCols * 2;  // 8 KB
+constexpr int kTileBytes = kBoxesPerTile * kBoxBytes;  // 72 KB
+
+// Device error bits (the per-file g_device_error words).
+constexpr uint32_t MLA_DEVERR_TIMEOUT = 1u;
+constexpr uint32_t MLA_DEVERR_BAD_PAGE = 2u;
+
+struct PartialParams {
+  const uint16_t* q_abs;       // [B, q_len, H, 512]
+  const uint16_t* q_pe;        // [B, q_len, H, 64]
+  const int32_t* block_table;  // [B, max_blocks]
+  const int32_t* context_lens; // [B]
+  const void* chunks;          // device int4 {b, t0, t1, slot} per chunk, or null
+  float* partials;             // [slots, q_len, H, 512]
+  float* lse;                  // [slots, q_len, H]
+  float scale_log2;            // softmax scale * log2(e)
+  int32_t B, H, q_len, bs, max_blocks, num_blocks;
+  int32_t num_parts;           // uniform split when chunks == null
+  int32_t causal;
+  uint64_t timeout_ns;
+};
+
+struct MergeParams {
+  const float* partials;
+  const float* lse;
+  const int32_t* o_indptr;
+  void* out;
+  float* out_lse;
+  int32_t B, rows;  // rows = q_len * H
+  int32_t out_dtype;
+};
+
+// Launchers return cudaSuccess or the launch error. grid.x = cluster of
+// `cluster` CTAs, grid.y = chunks, grid.z = row groups.
+cudaError_t launch_partial_simt(const CUtensorMap& tm_ckv, const CUtensorMap& tm_kpe, const PartialParams& p,
+                                int num_chunks, int cluster, bool bf16, cudaStream_t stream);
+cudaError_t launch_partial_tc(const CUtensorMap& tm_ckv, const CUtensorMap& tm_kpe, const PartialParams& p,
+                              int num_chunks, int cluster, bool bf16, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+
+// Query rows per CTA for q_len x H rows (SIMT: always 16).
+int simt_rows_per_cta();
+int tc_rows_per_cta(int total_rows, bool bf16);
+// Occupancy: co-resident clusters of `cluster` CTAs of the tensor-core kernel.
+int tc_max_active_clusters(int cluster, int rows_per_cta, bool bf16);
+
+cudaError_t simt_read_clear_error(uint32_t* out);
+cudaError_t tc_read_clear_error(uint32_t* out);
+
+}  // namespace mla

@@ -1,0 +1,91 @@
+// LSE-weighted merge of request-major partials (base-2 LSE).
+//
+// "feat(core): matrix-absorbed MLA decode over a compressed-latent KV cache",
+// *How #898's merge kernel is reused*: partials of request b are rows
+// o_indptr[b] .. o_indptr[b+1]-1, their LSE is base 2. "[kernel] Wire MLA
+// split-KV decode", *What changed*: the reduce combines slices by their LSE so
+// the result equals ordinary attention. MTPLX PR #639 commit log: a partial with
+// LSE = -inf has weight 0, an all -inf row merges to zeros, and the fp32
+// result is rounded once to the output dtype.
+//
+// One warp per (request, row, 128-column quarter); each lane owns 4 columns.
+// The weights are computed lane-parallel (lane s holds partial s), the sum over
+// partials runs in fixed order, so the result is bitwise reproducible.
+#include "device_common.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kWarps = 8;
+
+__global__ void __launch_bounds__(kWarps * 32) mla_merge_kernel(const MergeParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long gw = static_cast<long long>(blockIdx.x) * kWarps + warp;
+  const long long total = static_cast<long long>(p.B) * p.rows * 4;
+  if (gw >= total) return;
+  const int quarter = static_cast<int>(gw & 3);
+  const long long br = gw >> 2;  // b * rows + row
+  const int b = static_cast<int>(br / p.rows);
+  const int row = static_cast<int>(br % p.rows);
+  const int lo = p.o_indptr[b], hi = p.o_indptr[b + 1];
+  const int n = hi - lo;
+
+  // maximum LSE over this row's partials
+  float M = -INFINITY;
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, p.lse[static_cast<long long>(lo + s) * p.rows + row]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  if (M != -INFINITY) {
+    for (int s0 = 0; s0 < n; s0 += 32) {
+      const int cnt = min(32, n - s0);
+      float wl = 0.f;
+      if (lane < cnt) {
+        const float l = p.lse[static_cast<long long>(lo + s0 + lane) * p.rows + row];
+        wl = (l == -INFINITY) ? 0.f : exp2f(l - M);
+      }
+      for (int j = 0; j < cnt; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, wl, j);
+        const float4 v = *reinterpret_cast<const float4*>(
+            p.partials + (static_cast<long long>(lo + s0 + j) * p.rows + row) * kRank + quarter * 128 + lane * 4);
+        den += wj;
+        acc.x = fmaf(wj, v.x, acc.x);
+        acc.y = fmaf(wj, v.y, acc.y);
+        acc.z = fmaf(wj, v.z, acc.z);
+        acc.w = fmaf(wj, v.w, acc.w);
+      }
+    }
+    acc = make_float4(acc.x / den, acc.y / den, acc.z / den, acc.w / den);
+  }
+  const long long o_off = br * kRank + quarter * 128 + lane * 4;
+  if (p.out_dtype == 2) {
+    *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o_off) = acc;
+  } else {
+    uint16_t h[4];
+    const bool bf = (p.out_dtype == 1);
+    const float f[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = bf ? f2h<true>(f[j]) : f2h<false>(f[j]);
+    uint2 packed;
+    packed.x = static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16);
+    packed.y = static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[3]) << 16);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + o_off) = packed;
+  }
+  if (p.out_lse != nullptr && quarter == 0 && lane == 0)
+    p.out_lse[br] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
+  const long long warps = static_cast<long long>(p.B) * p.rows * 4;
+  const long long blocks = (warps + kWarps - 1) / kWarps;
+  if (blocks <= 0) return cudaSuccess;
+  mla_merge_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,150 @@
+// Partition planner (host only, no GPU access).
+//
+// "[kernel] Wire MLA split-KV decode" (vllm-metal PR #601), *What changed*:
+// host dispatch takes the split path only in conservative cases -- long enough
+// context, 2 to 8 partitions, bounded temporary memory -- and the review asks
+// for these thresholds to live in a device-aware split-plan helper. "feat(core):
+// matrix-absorbed MLA decode over a compressed-latent KV cache", *What
+// changed*: `MlaSplitPlan` cuts the latent range into chunks.
+//
+// Here a partition is one thread-block cluster of C CTAs (the CTAs split the
+// partition's tokens and combine on chip), so the plan is sized against the
+// number of co-resident clusters of the partial kernel: partitions are shared
+// out over requests in proportion to their lengths so that one wave of
+// clusters covers all of them.
+#include <algorithm>
+#include <cstdint>
+#include <vector>
+
+#include "kernels.h"
+#include "mla_split_kv.h"
+
+namespace {
+
+int64_t chunk_len(int64_t L, int64_t P, int64_t bs) {
+  const int64_t per = (L + P - 1) / P;
+  int64_t C = ((per + bs - 1) / bs) * bs;
+  return C < bs ? bs : C;
+}
+
+// Largest P' <= P whose chunks are all non-empty under the chunk rule.
+int64_t no_empty_chunks(int64_t L, int64_t P, int64_t bs) {
+  while (P > 1 && (P - 1) * chunk_len(L, P, bs) >= L) --P;
+  return P;
+}
+
+struct Candidate {
+  int cluster = 1;
+  std::vector<int64_t> parts;
+  int64_t active = -1;  // CTAs busy in the first wave
+};
+
+}  // namespace
+
+extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, int32_t num_heads, int32_t q_len,
+                                 int32_t block_size, const mla_device_info_t* dev, mla_plan_t* plan) {
+  if (context_lens_host == nullptr || dev == nullptr || plan == nullptr) return MLA_ERR_INVALID_ARG;
+  if (B < 1 || B > 65535) return MLA_ERR_INVALID_ARG;
+  if (num_heads != 16 && num_heads != 64 && num_heads != 128) return MLA_ERR_UNSUPPORTED;
+  if (q_len < 1 || q_len > MLA_MAX_Q_LEN) return MLA_ERR_UNSUPPORTED;
+  if (block_size != 16 && block_size != 32 && block_size != 64) return MLA_ERR_UNSUPPORTED;
+  if (plan->dtype != MLA_F16 && plan->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (plan->capacity < 0 || plan->max_partitions < 0 || plan->min_partitions < 0 || plan->split_min_tokens < 0)
+    return MLA_ERR_INVALID_ARG;
+  if (dev->num_sms < 1) return MLA_ERR_INVALID_ARG;
+  for (int32_t b = 0; b < B; ++b)
+    if (context_lens_host[b] < 0) return MLA_ERR_INVALID_ARG;
+
+  const int64_t maxP = plan->max_partitions ? plan->max_partitions : 8;
+  const int64_t minP = std::min<int64_t>(plan->min_partitions ? plan->min_partitions : 2, maxP);
+  const int64_t split_min = plan->split_min_tokens ? plan->split_min_tokens : 4096;
+  if (maxP < 1 || maxP > 1024) return MLA_ERR_INVALID_ARG;
+
+  const int rows = num_heads * q_len;
+  const int nr = mla::tc_rows_per_cta(rows, plan->dtype == MLA_BF16);
+  const int64_t row_groups = (rows + nr - 1) / nr;
+
+  int64_t split_tokens = 0, n_split = 0;
+  for (int32_t b = 0; b < B; ++b)
+    if (context_lens_host[b] >= split_min) {
+      split_tokens += context_lens_host[b];
+      ++n_split;
+    }
+
+  Candidate best;
+  for (int k = 0; k < 5; ++k) {
+    const int C = 1 << k;
+    const int64_t slots = dev->max_clusters[k];
+    if (slots <= 0) continue;
+    Candidate cand;
+    cand.cluster = C;
+    cand.parts.assign(B, 1);
+    const int64_t budget = std::max<int64_t>(B, slots / row_groups);
+    const int64_t spare = budget - (B - n_split);  // partitions left for the split requests
+    bool ok = true;
+    if (n_split > 0) {
+      // proportional share, floor, then largest remainder, all clamped
+      std::vector<std::pair<double, int32_t>> rem;
+      int64_t used = 0;
+      for (int32_t b = 0; b < B; ++b) {
+        const int64_t L = context_lens_host[b];
+        if (L < split_min) continue;
+        const double share = static_cast<double>(spare) * static_cast<double>(L) / static_cast<double>(split_tokens);
+        int64_t P = static_cast<int64_t>(share);
+        P = std::max(minP, std::min(maxP, std::max<int64_t>(P, 1)));
+        cand.parts[b] = P;
+        used += P;
+        rem.push_back({share - static_cast<double>(static_cast<int64_t>(share)), b});
+      }
+      std::stable_sort(rem.begin(), rem.end(), [](const auto& a, const auto& c) { return a.first > c.first; });
+      for (size_t j = 0; j < rem.size() && used < spare; ++j) {
+        const int32_t b = rem[j].second;
+        if (cand.parts[b] < maxP) {
+          ++cand.parts[b];
+          ++used;
+        }
+      }
+      for (int32_t b = 0; b < B; ++b) {
+        const int64_t L = context_lens_host[b];
+        if (L < split_min) continue;
+        cand.parts[b] = no_empty_chunks(L, cand.parts[b], block_size);
+        // every CTA of the cluster should get at least one 64-token tile
+        if (C > 1 && chunk_len(L, cand.parts[b], block_size) < static_cast<int64_t>(C) * mla::kTileTokens) ok = false;
+      }
+    }
+    if (!ok) continue;
+    int64_t N = 0;
+    for (int32_t b = 0; b < B; ++b) N += cand.parts[b];
+    cand.active = std::min<int64_t>(N * row_groups, slots) * C;
+    if (cand.active > best.active) best = cand;  // ties keep the smaller cluster
+  }
+  if (best.active < 0) {  // no cluster size usable: one CTA per partition, no split
+    best = Candidate();
+    best.cluster = 1;
+    best.parts.assign(B, 1);
+  }
+
+  int64_t N = 0;
+  for (int32_t b = 0; b < B; ++b) N += best.parts[b];
+  if (N > 65535) return MLA_ERR_UNSUPPORTED;
+  plan->num_chunks = static_cast<int32_t>(N);
+  plan->cluster_ctas = best.cluster;
+  plan->kernel = MLA_KERNEL_TC;
+  if (N > plan->capacity) return MLA_ERR_CAPACITY;
+  if (plan->chunks == nullptr || plan->o_indptr == nullptr) return MLA_ERR_INVALID_ARG;
+
+  int32_t n = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    plan->o_indptr[b] = n;
+    const int64_t L = context_lens_host[b];
+    const int64_t P = best.parts[b];
+    const int64_t Cl = chunk_len(L, P, block_size);
+    for (int64_t p = 0; p < P; ++p) {
+      const int64_t t0 = std::min(p * Cl, L), t1 = std::min((p + 1) * Cl, L);
+      plan->chunks[n] = mla_chunk_t{b, static_cast<int32_t>(t0), static_cast<int32_t>(t1), n};
+      ++n;
+    }
+  }
+  plan->o_indptr[B] = n;
+  return MLA_OK;
+}

@@ -1,0 +1,105 @@
+"""Device buffers and one decode layer call through the C ABI.
+
+torch supplies device memory and streams; the binding passes raw pointers;
+all computation happens in the CUDA library.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import binding as nb
+from .inputs import DecodeCase
+
+TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def to_device_16(bits: np.ndarray, dtype: str, device) -> torch.Tensor:
+    """uint16 bit patterns -> a 16-bit float tensor on `device` (bit-exact)."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.to(device).view(TORCH_DTYPE[dtype])
+
+
+@dataclasses.dataclass
+class DeviceCase:
+    q_abs: torch.Tensor
+    q_pe: torch.Tensor
+    ckv: torch.Tensor
+    kpe: torch.Tensor
+    block_table: torch.Tensor
+    context_lens: torch.Tensor
+    case: DecodeCase
+
+
+def upload(case: DecodeCase, device="cuda", ckv: torch.Tensor = None, kpe: torch.Tensor = None) -> DeviceCase:
+    """Copy a case to the device. A resident cache (ckv/kpe) can be shared."""
+    return DeviceCase(
+        q_abs=to_device_16(case.q_abs, case.dtype, device),
+        q_pe=to_device_16(case.q_pe, case.dtype, device),
+        ckv=ckv if ckv is not None else to_device_16(case.ckv, case.dtype, device),
+        kpe=kpe if kpe is not None else to_device_16(case.kpe, case.dtype, device),
+        block_table=torch.from_numpy(np.ascontiguousarray(case.block_table)).to(device),
+        context_lens=torch.from_numpy(np.ascontiguousarray(case.context_lens)).to(device),
+        case=case,
+    )
+
+
+def chunks_to_device(chunks: Sequence[Sequence[int]], device="cuda") -> torch.Tensor:
+    arr = np.asarray(chunks, dtype=np.int32).reshape(-1, 4)
+    return torch.from_numpy(arr).to(device)
+
+
+def make_desc(dc: DeviceCase, chunks_dev: Optional[torch.Tensor], kernel: int, cluster: int,
+              stream: Optional[torch.cuda.Stream] = None) -> nb.mla_decode_desc_t:
+    c = dc.case
+    d = nb.mla_decode_desc_t()
+    d.num_requests = c.num_requests
+    d.num_heads = c.num_heads
+    d.q_len = c.q_len
+    d.block_size = c.block_size
+    d.num_blocks = int(dc.ckv.shape[0])
+    d.max_blocks_per_req = int(dc.block_table.shape[1])
+    d.dtype = nb.DTYPE_CODES[c.dtype]
+    d.causal = 1 if c.causal else 0
+    d.chunks = chunks_dev.data_ptr() if chunks_dev is not None else None
+    d.num_chunks = int(chunks_dev.shape[0]) if chunks_dev is not None else 0
+    d.cluster_ctas = cluster
+    d.kernel = kernel
+    s = stream if stream is not None else torch.cuda.current_stream()
+    d.stream = s.cuda_stream
+    return d
+
+
+def alloc_partials(num_slots: int, q_len: int, H: int, device="cuda"):
+    part = torch.empty((num_slots, q_len, H, 512), dtype=torch.float32, device=device)
+    lse = torch.empty((num_slots, q_len, H), dtype=torch.float32, device=device)
+    return part, lse
+
+
+def decode_partial(dc: DeviceCase, part: torch.Tensor, lse: torch.Tensor, num_partitions: int = 1,
+                   chunks_dev: Optional[torch.Tensor] = None, kernel: int = nb.MLA_KERNEL_AUTO,
+                   cluster: int = 0, stream=None, desc: Optional[nb.mla_decode_desc_t] = None) -> None:
+    d = desc if desc is not None else make_desc(dc, chunks_dev, kernel, cluster, stream)
+    nb.mla_decode_partial(dc.q_abs.data_ptr(), dc.q_pe.data_ptr(), dc.ckv.data_ptr(), dc.kpe.data_ptr(),
+                          dc.block_table.data_ptr(), dc.context_lens.data_ptr(), float(dc.case.scale),
+                          num_partitions, part.data_ptr(), lse.data_ptr(), d)
+
+
+def merge_states(part: torch.Tensor, lse: torch.Tensor, o_indptr_dev: torch.Tensor, B: int, q_len: int, H: int,
+                 out_dtype: str = "f32", out: Optional[torch.Tensor] = None, out_lse: Optional[torch.Tensor] = None,
+                 stream=None):
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[out_dtype]
+    if out is None:
+        out = torch.empty((B, q_len, H, 512), dtype=tdt, device=part.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    nb.mla_merge_states(part.data_ptr(), lse.data_ptr(), o_indptr_dev.data_ptr(), B, q_len, H, out.data_ptr(),
+                        nb.DTYPE_CODES[out_dtype], out_lse.data_ptr() if out_lse is not None else None,
+                        s.cuda_stream)
+    return out
+
+
+def uniform_indptr(B: int, P: int, device="cuda") -> torch.Tensor:
+    return torch.arange(0, (B + 1) * P, P, dtype=torch.int32, device=device)

@@ -1,0 +1,208 @@
+"""C-ABI library on the CPU: it loads, exports what the header declares, plans
+correctly, and rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from mla_split_kv_gb300 import binding as nb
+from mla_split_kv_gb300 import build as nbuild
+from mla_split_kv_gb300 import inputs as gen
+from oracle import mla_oracle as orc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nbuild.build()
+    return nb.load()
+
+
+def header_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?!typedef)[A-Za-z_][\w\s\*]*?\b(mla_\w+)\s*\(", text, flags=re.M):
+            names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_header_declares_the_core_calls():
+    names = header_functions()
+    for must in ("mla_plan", "mla_decode_partial", "mla_merge_states", "mla_device_query",
+                 "mla_check_device_errors", "mla_get_counters"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+# --- planner ------------------------------------------------------------------------
+
+def fake_gb300():
+    """Occupancy figures of the tensor-core kernel as measured on a GB300."""
+    dev = nb.mla_device_info_t()
+    dev.num_sms = 152
+    for k, v in enumerate([152, 76, 36, 15, 7]):
+        dev.max_clusters[k] = v
+    return dev
+
+
+def check_plan_tiles(plan, lens, bs):
+    assert plan.o_indptr[0] == 0 and plan.o_indptr[-1] == plan.num_chunks
+    for b, L in enumerate(lens):
+        lo, hi = plan.o_indptr[b], plan.o_indptr[b + 1]
+        ch = plan.chunks[lo:hi]
+        assert all(c[0] == b for c in ch)
+        assert ch[0][1] == 0 and ch[-1][2] == L
+        for c0, c1 in zip(ch, ch[1:]):
+            assert c0[2] == c1[1]
+        for (bb, t0, t1, slot) in ch:
+            assert t0 % bs == 0 and t0 <= t1
+        # the chunk table is exactly the oracle's chunk rule for that P
+        assert [(t0, t1) for (_, t0, t1, _) in ch] == orc.chunk_bounds(L, hi - lo, bs)
+    assert [c[3] for c in plan.chunks] == list(range(plan.num_chunks))
+
+
+@pytest.mark.parametrize("L", [32768, 49152, 65536, 81920, 98304, 131072])
+def test_plan_long_context_single_request(lib, L):
+    plan = nb.mla_plan([L], 16, 1, 32, fake_gb300())
+    assert 2 <= plan.num_chunks <= 8
+    assert plan.num_chunks * plan.cluster_ctas >= 100  # most of the 152 SMs busy
+    check_plan_tiles(plan, [L], 32)
+
+
+def test_plan_mixed_batch_two_to_four(lib):
+    lens = [32768, 20000]
+    plan = nb.mla_plan(lens, 16, 1, 32, fake_gb300(), max_partitions=4)
+    assert all(2 <= p <= 4 for p in plan.parts())
+    check_plan_tiles(plan, lens, 32)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_plan_many_heads_batch(lib, dtype):
+    lens = gen.uniform_lengths(4, 8, 4096, 65536)
+    plan = nb.mla_plan(lens, 128, 1, 64, fake_gb300(), max_partitions=64, dtype=dtype)
+    check_plan_tiles(plan, lens, 64)
+    parts = plan.parts()
+    assert all(1 <= p <= 64 for p in parts)
+    order = np.argsort(lens)
+    assert parts[order[-1]] >= parts[order[0]]
+
+
+def test_plan_short_and_empty_requests_are_not_split(lib):
+    lens = [0, 1, 100, 4095, 40000]
+    plan = nb.mla_plan(lens, 16, 1, 16, fake_gb300())
+    parts = plan.parts()
+    assert parts[:4] == [1, 1, 1, 1] and parts[4] >= 2
+    check_plan_tiles(plan, lens, 16)
+
+
+def test_plan_is_deterministic(lib):
+    lens = gen.uniform_lengths(9, 5, 1000, 90000)
+    a = nb.mla_plan(lens, 16, 4, 32, fake_gb300())
+    b = nb.mla_plan(lens, 16, 4, 32, fake_gb300())
+    assert a.chunks == b.chunks and a.o_indptr == b.o_indptr and a.cluster_ctas == b.cluster_ctas
+
+
+def test_plan_capacity_and_argument_errors(lib):
+    dev = fake_gb300()
+    lens = (ctypes.c_int32 * 1)(65536)
+    plan = nb.mla_plan_t()
+    plan.capacity = 1
+    chunks = (nb.mla_chunk_t * 1)()
+    ind = (ctypes.c_int32 * 2)()
+    plan.chunks = ctypes.cast(chunks, ctypes.POINTER(nb.mla_chunk_t))
+    plan.o_indptr = ctypes.cast(ind, ctypes.POINTER(ctypes.c_int32))
+    assert lib.mla_plan(lens, 1, 16, 1, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_CAPACITY
+    assert plan.num_chunks > 1
+    assert lib.mla_plan(lens, 1, 24, 1, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_UNSUPPORTED
+    assert lib.mla_plan(lens, 1, 16, 33, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_UNSUPPORTED
+    assert lib.mla_plan(lens, 1, 16, 1, 48, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_UNSUPPORTED
+    assert lib.mla_plan(lens, 0, 16, 1, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_INVALID_ARG
+    plan.dtype = 2
+    assert lib.mla_plan(lens, 1, 16, 1, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_UNSUPPORTED
+    plan.dtype = 0
+    neg = (ctypes.c_int32 * 1)(-5)
+    assert lib.mla_plan(neg, 1, 16, 1, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_INVALID_ARG
+
+
+# --- argument checks before any launch ------------------------------------------------
+
+FAKE = 0x10000  # 64 KiB-aligned fake device address: never dereferenced on a rejected call
+
+
+def desc(**kw):
+    d = nb.mla_decode_desc_t()
+    d.num_requests, d.num_heads, d.q_len, d.block_size = 1, 16, 1, 32
+    d.num_blocks, d.max_blocks_per_req, d.dtype, d.causal = 8, 8, nb.MLA_F16, 0
+    d.chunks, d.num_chunks, d.cluster_ctas, d.kernel, d.stream = None, 0, 1, nb.MLA_KERNEL_TC, None
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def call_partial(lib, d, P=2, ptrs=None):
+    p = [FAKE] * 8 if ptrs is None else ptrs
+    return lib.mla_decode_partial(p[0], p[1], p[2], p[3], p[4], p[5], ctypes.c_float(0.07), P, p[6], p[7],
+                                  ctypes.byref(d))
+
+
+@pytest.mark.parametrize("kw,P,want", [
+    (dict(num_heads=32), 2, nb.MLA_ERR_UNSUPPORTED),
+    (dict(q_len=0), 2, nb.MLA_ERR_UNSUPPORTED),
+    (dict(q_len=33), 2, nb.MLA_ERR_UNSUPPORTED),
+    (dict(block_size=128), 2, nb.MLA_ERR_UNSUPPORTED),
+    (dict(dtype=2), 2, nb.MLA_ERR_UNSUPPORTED),
+    (dict(num_requests=0), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(cluster_ctas=3), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(kernel=7), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(causal=2), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(), 0, nb.MLA_ERR_INVALID_ARG),
+    (dict(num_requests=40000), 2, nb.MLA_ERR_UNSUPPORTED),
+])
+def test_decode_partial_rejects_before_launch(lib, kw, P, want):
+    nb.mla_reset_counters()
+    assert call_partial(lib, desc(**kw), P) == want
+    ctr = nb.mla_get_counters()
+    assert ctr[nb.CTR_PARTIAL_TC] == 0 and ctr[nb.CTR_PARTIAL_SIMT] == 0 and ctr[nb.CTR_REJECTED] == 1
+
+
+def test_decode_partial_rejects_null_and_misaligned(lib):
+    nb.mla_reset_counters()
+    ptrs = [FAKE] * 8
+    ptrs[2] = 0
+    assert call_partial(lib, desc(), 2, ptrs) == nb.MLA_ERR_INVALID_ARG
+    ptrs = [FAKE] * 8
+    ptrs[2] = FAKE + 8  # ckv not 16-byte aligned
+    assert call_partial(lib, desc(), 2, ptrs) == nb.MLA_ERR_INVALID_ARG
+    ptrs = [FAKE] * 8
+    ptrs[6] = FAKE + 4  # partials not 16-byte aligned
+    assert call_partial(lib, desc(), 2, ptrs) == nb.MLA_ERR_INVALID_ARG
+    assert nb.mla_get_counters()[nb.CTR_PARTIAL_TC] == 0
+
+
+def test_merge_rejects_before_launch(lib):
+    nb.mla_reset_counters()
+    f = lib.mla_merge_states
+    assert f(FAKE, FAKE, FAKE, 1, 1, 24, FAKE, 0, None, None) == nb.MLA_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, 1, 1, 16, FAKE, 5, None, None) == nb.MLA_ERR_UNSUPPORTED
+    assert f(None, FAKE, FAKE, 1, 1, 16, FAKE, 0, None, None) == nb.MLA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, 0, 1, 16, FAKE, 0, None, None) == nb.MLA_ERR_INVALID_ARG
+    assert f(FAKE + 4, FAKE, FAKE, 1, 1, 16, FAKE, 0, None, None) == nb.MLA_ERR_INVALID_ARG
+    assert nb.mla_get_counters()[nb.CTR_MERGE] == 0
+
+
+def test_sizes_and_strings(lib):
+    assert nb.mla_partials_bytes(8, 1, 16) == 8 * 16 * 512 * 4
+    assert lib.mla_lse_bytes(8, 2, 16) == 8 * 2 * 16 * 4
+    assert nb.status_string(nb.MLA_ERR_TIMEOUT) == "device wait timed out"
+    assert nb.mla_version() >= 1
