@@ -1,0 +1,493 @@
+"""Benchmark: MLA split-KV decode layer calls on one GB300 (or N replicas).
+
+Workload: B=1, H=16, kv_lora_rank 512, rope 64, fp16, block 32, contexts
+32768 / 49152 / 65536 / 81920 / 98304 / 131072 tokens (N(0,1) latents, random
+block permutation), partitions chosen by the planner. One step = one layer
+call (partial kernel + merge kernel) at each of the six contexts; the six
+caches live in disjoint memory (528 MB together, > L2), so every call streams
+its latent from HBM.
+
+Printed: one JSON line. `value` = mean microseconds per layer call over the
+sweep (device time, inputs resident, each kernel replayed from a CUDA graph);
+`e2e` = the same through the C-ABI calls with host buffers (queries, block
+tables and plan copied in, output copied out, every step); `roofline` = the
+partial kernel's algorithmic HBM bytes / its CUDA-event time against the
+measured copy bandwidth; `cpu_baseline` = the f64 oracle on the host cores.
+`--impl reference` times the oracle itself on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+CONTEXTS = [32768, 49152, 65536, 81920, 98304, 131072]
+H, BS, DTYPE, SEED = 16, 32, "f16", 2
+LATENT_BYTES_PER_TOKEN = (512 + 64) * 2
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "partial_tc_ctx_sweep.json")
+WORKLOAD = "mla_decode_ctx_sweep_B1_H16_r512_rope64_fp16_bs32"
+METRIC = "us per MLA decode layer call (mean over ctx 32K-131K), HBM GB/s as fraction of peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--kernel", default="tc", choices=["tc", "simt"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (bounded sample), run in a spawned pool over shared memory
+# ---------------------------------------------------------------------------
+
+def _oracle_worker(args):
+    import numpy as np
+    from multiprocessing import shared_memory
+
+    from mla_split_kv_gb300.inputs import DecodeCase
+    from oracle import mla_oracle as orc
+
+    meta, heads = args
+    shms, arrays = [], {}
+    for key, (name, shape, dt) in meta["arrays"].items():
+        shm = shared_memory.SharedMemory(name=name)
+        shms.append(shm)
+        arrays[key] = np.ndarray(shape, dtype=np.dtype(dt), buffer=shm.buf)
+    case = DecodeCase(dtype=meta["dtype"], num_heads=meta["H"], q_len=1, block_size=meta["bs"],
+                      scale=meta["scale"], causal=False, **arrays)
+    out, _ = orc.unsplit(case, heads=heads)
+    s = float(np.nansum(out))
+    del arrays, case, out
+    for shm in shms:
+        shm.close()
+    return s
+
+
+class OraclePool:
+    """Process pool (spawn) that runs the oracle, one head group per worker."""
+
+    def __init__(self, cores):
+        import multiprocessing as mp
+
+        os.environ["OPENBLAS_NUM_THREADS"] = "1"
+        os.environ["OMP_NUM_THREADS"] = "1"
+        self.cores = cores
+        self.pool = mp.get_context("spawn").Pool(cores)
+
+    def share(self, case):
+        import numpy as np
+        from multiprocessing import shared_memory
+
+        meta = {"dtype": case.dtype, "H": case.num_heads, "bs": case.block_size, "scale": case.scale, "arrays": {}}
+        shms = []
+        for key in ("q_abs", "q_pe", "ckv", "kpe", "block_table", "context_lens"):
+            a = np.ascontiguousarray(getattr(case, key))
+            shm = shared_memory.SharedMemory(create=True, size=max(1, a.nbytes))
+            np.ndarray(a.shape, dtype=a.dtype, buffer=shm.buf)[...] = a
+            meta["arrays"][key] = (shm.name, a.shape, a.dtype.str)
+            shms.append(shm)
+        return meta, shms
+
+    def layer_call(self, meta, num_heads):
+        groups = [list(range(h, num_heads, self.cores)) for h in range(min(self.cores, num_heads))]
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_worker, [(meta, g) for g in groups])
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def make_cases():
+    from mla_split_kv_gb300 import inputs as gen
+
+    cases = []
+    for i, L in enumerate(CONTEXTS):
+        pages = gen.pages_for(L, BS)
+        cases.append(gen.make_decode_case(SEED * 100 + i, [L], num_heads=H, block_size=BS, dtype=DTYPE,
+                                          pool_blocks=pages + pages // 4))
+    return cases
+
+
+def oracle_timing(cases, steps, cores, budget_s=30.0):
+    """Seconds per layer call of the oracle: every context once per step, bounded by budget_s."""
+    pool = OraclePool(cores)
+    shared = [pool.share(c) for c in cases]
+    try:
+        pool.layer_call(shared[0][0], H)  # worker start-up, imports
+        per_call, t_start, done_steps = [], time.perf_counter(), 0
+        for _ in range(max(1, steps)):
+            for meta, _ in shared:
+                per_call.append(pool.layer_call(meta, H))
+            done_steps += 1
+            if time.perf_counter() - t_start > budget_s:
+                break
+    finally:
+        pool.close()
+        for _, shms in shared:
+            for s in shms:
+                s.close()
+                s.unlink()
+    return per_call, done_steps
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(L, n_chunks):
+    """(partial kernel bytes, merge kernel bytes) one layer call must move."""
+    pages = (L + BS - 1) // BS
+    latent = L * LATENT_BYTES_PER_TOKEN
+    table = pages * 4
+    queries = H * 576 * 2
+    partial_io = n_chunks * H * 513 * 4  # partials + lse written
+    merge = n_chunks * H * 513 * 4 + H * 512 * 2  # read back, output written
+    return latent + table + queries + partial_io, merge
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return None
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("partial_tc.cu", "device_common.cuh", "kernels.h"):
+        h.update(open(os.path.join(ROOT, "mla_split_kv_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(tokens_per_launch):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel."""
+    try:
+        prof = json.load(open(PROFILE_TRAFFIC))
+    except (OSError, ValueError):
+        return None
+    if prof.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    bpt = prof.get("dram_bytes_per_token")
+    return None if bpt is None else round(bpt * tokens_per_launch)
+
+
+def run_ours(args, rank, world):
+    import numpy as np
+    import torch
+
+    from mla_split_kv_gb300 import binding as nb
+    from mla_split_kv_gb300 import build as nbuild
+    from mla_split_kv_gb300 import runtime as rt
+
+    nbuild.build()
+    nb.load()
+    dev_index = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev_index)
+    kernel = nb.MLA_KERNEL_TC if args.kernel == "tc" else nb.MLA_KERNEL_SIMT
+
+    cases = make_cases()
+    dev = nb.mla_device_query()
+    stream = torch.cuda.Stream()
+    calls = []
+    with torch.cuda.stream(stream):
+        for case in cases:
+            L = int(case.context_lens[0])
+            plan = nb.mla_plan([L], H, 1, BS, dev)
+            dc = rt.upload(case)
+            chunks_dev = rt.chunks_to_device(plan.chunks)
+            part, lse = rt.alloc_partials(plan.num_chunks, 1, H)
+            ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
+            out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
+            desc = rt.make_desc(dc, chunks_dev, kernel, plan.cluster_ctas, stream)
+            calls.append(dict(L=L, plan=plan, dc=dc, chunks=chunks_dev, part=part, lse=lse, ind=ind, out=out,
+                              desc=desc))
+    torch.cuda.synchronize()
+
+    def partial(c):
+        rt.decode_partial(c["dc"], c["part"], c["lse"], desc=c["desc"])
+
+    def merge(c):
+        rt.merge_states(c["part"], c["lse"], c["ind"], 1, 1, H, "f16", out=c["out"], stream=stream)
+
+    # warm-up through the plain calls (also sets kernel attributes before capture)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            for c in calls:
+                partial(c)
+                merge(c)
+    stream.synchronize()
+    st, code = nb.mla_check_device_errors(stream.cuda_stream)
+    if st != nb.MLA_OK:
+        raise RuntimeError(f"device error word {code:#x} after warm-up")
+
+    # one CUDA graph per kernel so events can bracket each launch
+    for c in calls:
+        gp, gm = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gp, stream=stream):
+            partial(c)
+        with torch.cuda.graph(gm, stream=stream):
+            merge(c)
+        c["gp"], c["gm"] = gp, gm
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            for c in calls:
+                c["gp"].replay()
+                c["gm"].replay()
+    stream.synchronize()
+
+    K = args.steps
+    evs = [[tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in calls] for _ in range(K)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev_index) as clocks:
+        time.sleep(0.3)
+        with torch.cuda.stream(stream):
+            t_begin.record(stream)
+            for k in range(K):
+                for j, c in enumerate(calls):
+                    e0, e1, e2 = evs[k][j]
+                    e0.record(stream)
+                    c["gp"].replay()
+                    e1.record(stream)
+                    c["gm"].replay()
+                    e2.record(stream)
+            t_end.record(stream)
+        stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t_begin.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    st, code = nb.mla_check_device_errors(stream.cuda_stream)
+    if st != nb.MLA_OK:
+        raise RuntimeError(f"device error word {code:#x} in the timed region")
+
+    per_ctx = []
+    part_bytes_all, part_ms_all = 0, 0.0
+    for j, c in enumerate(calls):
+        p_ms = [evs[k][j][0].elapsed_time(evs[k][j][1]) for k in range(K)]
+        l_ms = [evs[k][j][0].elapsed_time(evs[k][j][2]) for k in range(K)]
+        pb, mb = algorithmic_bytes(c["L"], c["plan"].num_chunks)
+        part_bytes_all += pb * K
+        part_ms_all += sum(p_ms)
+        us = statistics.median(l_ms) * 1e3
+        pus = statistics.median(p_ms) * 1e3
+        per_ctx.append({"ctx": c["L"], "partitions": c["plan"].num_chunks, "cluster": c["plan"].cluster_ctas,
+                        "us_per_call": round(us, 3), "partial_us": round(pus, 3),
+                        "layer_gbs": round((pb + mb) / (us * 1e-6) / 1e9, 1),
+                        "partial_gbs": round(pb / (pus * 1e-6) / 1e9, 1)})
+
+    # end to end through the C ABI with host buffers (pinned), every step
+    e2e_steps = max(1, args.e2e_steps)
+    host = []
+    for c in calls:
+        cs = c["dc"].case
+        host.append(dict(q_abs=torch.from_numpy(cs.q_abs.view(np.int16)).pin_memory(),
+                         q_pe=torch.from_numpy(cs.q_pe.view(np.int16)).pin_memory(),
+                         bt=torch.from_numpy(cs.block_table).pin_memory(),
+                         lens=torch.from_numpy(cs.context_lens).pin_memory(),
+                         chunks=torch.from_numpy(c["plan"].chunk_array()).pin_memory(),
+                         ind=torch.tensor(c["plan"].o_indptr, dtype=torch.int32).pin_memory(),
+                         out=torch.empty((1, 1, H, 512), dtype=torch.float16).pin_memory()))
+    h2d = sum(h["q_abs"].numel() * 2 + h["q_pe"].numel() * 2 + h["bt"].numel() * 4 + h["lens"].numel() * 4
+              + h["chunks"].numel() * 4 + h["ind"].numel() * 4 for h in host)
+    d2h = sum(h["out"].numel() * 2 for h in host)
+    nb.mla_reset_counters()
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for c, h in zip(calls, host):
+                dc = c["dc"]
+                dc.q_abs.view(torch.int16).copy_(h["q_abs"], non_blocking=True)
+                dc.q_pe.view(torch.int16).copy_(h["q_pe"], non_blocking=True)
+                dc.block_table.copy_(h["bt"], non_blocking=True)
+                dc.context_lens.copy_(h["lens"], non_blocking=True)
+                c["chunks"].copy_(h["chunks"], non_blocking=True)
+                c["ind"].copy_(h["ind"], non_blocking=True)
+                partial(c)
+                merge(c)
+                h["out"].copy_(c["out"], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = time.perf_counter() - t0
+    ctr = nb.mla_get_counters()
+    expect = (3 + e2e_steps) * len(calls)
+    ctr_key = nb.CTR_PARTIAL_TC if kernel == nb.MLA_KERNEL_TC else nb.CTR_PARTIAL_SIMT
+    if ctr[ctr_key] != expect or ctr[nb.CTR_MERGE] != expect:
+        print(f"WARNING: path counters {ctr} disagree with {expect} launches of the {args.kernel} kernel",
+              file=sys.stderr)
+
+    n_calls = K * len(calls)
+    value_us = total_ms * 1e3 / (n_calls * world)
+    achieved = part_bytes_all / (part_ms_all * 1e-3) / 1e9
+    peaks = measured_peaks()
+    if peaks and peaks.get("hbm_gbs"):
+        peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    else:
+        peak, peak_src = 6800.0, "fallback"
+    result = {
+        "metric": METRIC,
+        "value": round(value_us, 3),
+        "unit": "us/layer-call",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 4),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "contexts": CONTEXTS, "B": 1, "H": H, "kv_lora_rank": 512, "rope_dim": 64,
+                   "block_size": BS, "partitions": "planner", "kernel": args.kernel,
+                   "l2": "inputs larger than L2: each step streams six disjoint caches, 528 MB",
+                   "timing": "one CUDA graph per kernel launch, CUDA events on the launching stream"},
+        "per_ctx": per_ctx,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(sum(CONTEXTS) / len(CONTEXTS)),
+                     "peak_source": peak_src, "kernel": f"mla_partial_{args.kernel}"},
+        "e2e": {"value": round(e2e_s * 1e6 / (e2e_steps * len(calls)), 3), "unit": "us/layer-call",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * n_calls,
+        "clocks": clocks.summary(),
+    }
+    return result, cases
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    cases = make_cases()
+    cores = os.cpu_count() or 1
+    per_call, steps = oracle_timing(cases, max(1, args.steps), cores, budget_s=90.0)
+    us = statistics.mean(per_call) * 1e6
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(us, 1),
+        "unit": "us/layer-call",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": 1,
+        "ms_per_step": round(us * len(CONTEXTS) / 1e3, 3),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "contexts": CONTEXTS, "B": 1, "H": H, "block_size": BS},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us/layer-call", "cores": cores, "kind": "oracle",
+                         "sample": f"{steps} sweep(s) of the six contexts, all 16 heads, f64 numpy oracle, "
+                                   f"{cores} spawned single-threaded workers (heads split across them)"},
+        "e2e": {"value": round(us, 1), "unit": "us/layer-call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res))
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        torch.distributed.init_process_group("nccl")
+    res, cases = run_ours(args, rank, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        per_call, steps = oracle_timing(cases, 1, cores, budget_s=30.0)
+        res["cpu_baseline"] = {"value": round(statistics.mean(per_call) * 1e6, 1), "unit": "us/layer-call",
+                               "cores": cores, "kind": "oracle",
+                               "sample": f"{steps} sweep of the six contexts (one layer call each, all 16 heads), "
+                                         f"f64 numpy oracle in {cores} spawned single-threaded workers"}
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

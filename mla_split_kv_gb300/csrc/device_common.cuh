@@ -58,6 +58,10 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+// Limit of the waits that let copies / MMAs already in flight finish before a
+// CTA that gave up leaves (they always complete; this only bounds the wait).
+constexpr uint64_t kDrainTimeoutNs = 2000000000ull;
+
 // Wait for the phase with the given parity to complete. Gives up after
 // `timeout_ns` of wall time, flags MLA_DEVERR_TIMEOUT and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
@@ -101,6 +105,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Named barrier that also ORs a predicate over the participating threads:
+// every thread gets the same answer (a uniform decision, e.g. to abort).
+__device__ __forceinline__ bool named_bar_sync_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(out)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return out != 0;
+}
 
 // ---------------------------------------------------------------------------
 // Thread-block cluster and distributed shared memory
@@ -121,20 +136,19 @@ __device__ __forceinline__ void cluster_sync() {
 // Address of the same shared variable in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
   uint32_t out;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(local)), "r"(rank));
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(local)), "r"(rank));
   return out;
 }
+// Loads from another CTA's shared memory. Only used on data published before
+// a cluster barrier, so they carry no ordering of their own and can overlap.
 __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
   float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
   return v;
 }
 __device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr) {
   float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
+  asm("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
   return v;
 }
 
@@ -334,7 +348,8 @@ __device__ __forceinline__ int32_t checked_page(const PartialParams& p, int32_t 
 // Combine the (max, sum, O) staged by the CTAs of this cluster: this CTA
 // writes columns [rank*512/C, (rank+1)*512/C) of each of its rows, rank 0
 // also the LSE. Fixed rank order, so the result is bitwise reproducible.
-// `ostage` is [rows][512] fp32, `mst`/`lst` [rows] fp32, same offsets in every CTA.
+// `ostage` is [rows][512] fp32, `mst`/`lst` [rows] fp32, same offsets in every
+// CTA. The per-rank loads are independent (unrolled over the 16 possible ranks).
 __device__ __forceinline__ void cluster_combine(const PartialParams& p, const CtaWork& w, const float* ostage,
                                                 const float* mst, const float* lst, int tid, int nthreads) {
   const int rows_total = p.q_len * p.H;
@@ -342,41 +357,44 @@ __device__ __forceinline__ void cluster_combine(const PartialParams& p, const Ct
   const int dcols = kRank / static_cast<int>(C);
   const int dbeg = static_cast<int>(kr) * dcols;
   const int n4 = dcols / 4;
-  for (int idx = tid; idx < w.nrows * n4; idx += nthreads) {
-    const int r = idx / n4, d = dbeg + (idx % n4) * 4;
+  const int items = w.nrows * n4 + ((kr == 0) ? w.nrows : 0);  // column groups, then LSE rows
+  for (int idx = tid; idx < items; idx += nthreads) {
+    const bool is_lse = idx >= w.nrows * n4;
+    const int r = is_lse ? idx - w.nrows * n4 : idx / n4;
+    const int d = is_lse ? 0 : dbeg + (idx % n4) * 4;
+    float mj[16], wj[16];
     float M = -INFINITY;
-    for (uint32_t j = 0; j < C; ++j) M = fmaxf(M, dsmem_ld_f32(dsmem_addr(mst + r, j)));
-    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      mj[j] = (j < static_cast<int>(C)) ? dsmem_ld_f32(dsmem_addr(mst + r, j)) : -INFINITY;
+      M = fmaxf(M, mj[j]);
+    }
     float den = 0.f;
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
-      for (uint32_t j = 0; j < C; ++j) {
-        const float mj = dsmem_ld_f32(dsmem_addr(mst + r, j));
-        const float wj = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
-        den = fmaf(wj, dsmem_ld_f32(dsmem_addr(lst + r, j)), den);
-        const float4 v = dsmem_ld_f32x4(dsmem_addr(ostage + r * kRank + d, j));
-        num.x = fmaf(wj, v.x, num.x);
-        num.y = fmaf(wj, v.y, num.y);
-        num.z = fmaf(wj, v.z, num.z);
-        num.w = fmaf(wj, v.w, num.w);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) wj[j] = (mj[j] == -INFINITY) ? 0.f : exp2f(mj[j] - M);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (j < static_cast<int>(C)) {
+          den = fmaf(wj[j], dsmem_ld_f32(dsmem_addr(lst + r, j)), den);
+          if (!is_lse) {
+            const float4 v = dsmem_ld_f32x4(dsmem_addr(ostage + r * kRank + d, j));
+            num.x = fmaf(wj[j], v.x, num.x);
+            num.y = fmaf(wj[j], v.y, num.y);
+            num.z = fmaf(wj[j], v.z, num.z);
+            num.w = fmaf(wj[j], v.w, num.w);
+          }
+        }
       }
     }
-    float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) out = make_float4(num.x / den, num.y / den, num.z / den, num.w / den);
-    const long long base = (static_cast<long long>(w.slot) * rows_total + w.row0 + r) * kRank + d;
-    *reinterpret_cast<float4*>(p.partials + base) = out;
-  }
-  if (kr == 0) {
-    for (int r = tid; r < w.nrows; r += nthreads) {
-      float M = -INFINITY;
-      for (uint32_t j = 0; j < C; ++j) M = fmaxf(M, dsmem_ld_f32(dsmem_addr(mst + r, j)));
-      float den = 0.f;
-      if (M != -INFINITY)
-        for (uint32_t j = 0; j < C; ++j) {
-          const float mj = dsmem_ld_f32(dsmem_addr(mst + r, j));
-          const float wj = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
-          den = fmaf(wj, dsmem_ld_f32(dsmem_addr(lst + r, j)), den);
-        }
+    if (is_lse) {
       p.lse[static_cast<long long>(w.slot) * rows_total + w.row0 + r] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
+    } else {
+      float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (M != -INFINITY) out = make_float4(num.x / den, num.y / den, num.z / den, num.w / den);
+      const long long base = (static_cast<long long>(w.slot) * rows_total + w.row0 + r) * kRank + d;
+      *reinterpret_cast<float4*>(p.partials + base) = out;
     }
   }
 }

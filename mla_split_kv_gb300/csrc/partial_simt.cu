@@ -119,9 +119,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int buf = i & 1;
     bool ok = true;
     if (tid == 0) ok = mbar_wait(&full[buf], (i >> 1) & 1, p.timeout_ns);
-    if (!ok) *abort_flag = 1;
-    __syncthreads();
-    if (*abort_flag) break;
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) *abort_flag = 1;
+      break;
+    }
     const uint8_t* tb = tiles + buf * kTileBytes;
     const int tok0 = w.sub0 + i * kTileTokens;
     const int nvalid = min(kTileTokens, w.sub1 - tok0);
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // after an abort, let the loads already in flight land before the buffers go away
   if (tid == 0 && *abort_flag) {
-    for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) mbar_wait(&full[i & 1], (i >> 1) & 1, p.timeout_ns);
+    for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) mbar_wait(&full[i & 1], (i >> 1) & 1, kDrainTimeoutNs);
   }
   __syncthreads();
 

@@ -137,10 +137,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = i & 1;
       if (i >= 2) {
         int ok = 1;
-        if (lane == 0) ok = mbar_wait(&sm->empty[buf], ((i >> 1) - 1) & 1, p.timeout_ns);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) *abort_flag = 1;
-        if (*abort_flag) break;
+        if (lane == 0) {
+          ok = mbar_wait(&sm->empty[buf], ((i >> 1) - 1) & 1, p.timeout_ns) && !*abort_flag;
+          if (!ok) *abort_flag = 1;
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;  // lane 0 decides for the warp
       }
       const int tok0 = w.sub0 + i * kTileTokens;
       const int ntok = min(kTileTokens, w.sub1 - tok0);
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0 && *abort_flag) {  // let loads in flight land before smem is released
       for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
-        mbar_wait(&sm->full[i & 1], (i >> 1) & 1, p.timeout_ns);
+        mbar_wait(&sm->full[i & 1], (i >> 1) & 1, kDrainTimeoutNs);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer
@@ -215,10 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < ntiles; ++i) {
       const int buf = i & 1;
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&sm->full[buf], (i >> 1) & 1, p.timeout_ns);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) *abort_flag = 1;
-      if (*abort_flag) {
+      if (lane == 0) {
+        ok = mbar_wait(&sm->full[buf], (i >> 1) & 1, p.timeout_ns) && !*abort_flag;
+        if (!ok) *abort_flag = 1;
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {  // lane 0 decides for the warp
         alive = false;
         break;
       }
@@ -262,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (alive && ntiles >= 1) issue_pv(ntiles - 1);
     if (lane == 0) {  // every MMA issued so far has completed before TMEM is read or freed
       umma_commit(&sm->drain);
-      mbar_wait(&sm->drain, 0, p.timeout_ns);
+      mbar_wait(&sm->drain, 0, kDrainTimeoutNs);
     }
     __syncwarp();
   } else {
@@ -313,8 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) *abort_flag = 1;
       }
-      named_bar_sync(1, 128);
-      if (*abort_flag) break;
+      if (named_bar_sync_or(1, 128, *abort_flag != 0)) break;
       // per-column reference max (lazy): one thread per column
       if (tid < NR) {
         const int r = tid;
@@ -374,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&sm->pfull);
     }
     // wait for the last PV, then reduce the row sums over the 64 token lanes
-    if (ntiles > 0 && !*abort_flag) {
+    const bool aborted = named_bar_sync_or(1, 128, *abort_flag != 0);  // same answer in all 4 warps
+    if (ntiles > 0 && !aborted) {
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&sm->odone, (ntiles - 1) & 1, p.timeout_ns);
       ok = __shfl_sync(0xffffffffu, ok, 0);

@@ -1,0 +1,269 @@
+"""GPU parity: the CUDA path through the C ABI against the f64 oracle.
+
+Tolerance (the stated target for fp16/bf16 inputs with fp32 accumulation):
+max-abs error <= 2e-3 and relative L2 error <= 1e-3 on fp32 results (partials
+and the fp32 merge output). A 16-bit merge output must equal the fp32 merge
+output rounded once; its distance to the exact result rounded once is then
+at most one unit in the last place plus the fp32 result's own error.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from mla_split_kv_gb300 import binding as nb
+from mla_split_kv_gb300 import build as nbuild
+from mla_split_kv_gb300 import inputs as gen
+from mla_split_kv_gb300 import runtime as rt
+from oracle import mla_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 2e-3
+REL_L2 = 1e-3
+KERNELS = {"tc": nb.MLA_KERNEL_TC, "simt": nb.MLA_KERNEL_SIMT}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    nbuild.build()
+    nb.load()
+    yield
+    st, code = nb.mla_check_device_errors(None)
+    assert st == nb.MLA_OK, f"device error word {code:#x}"
+
+
+def assert_close(got, ref, what, mask=None):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if mask is not None:
+        got, ref = got[mask], ref[mask]
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    err = np.abs(got - ref).max() if got.size else 0.0
+    nrm = np.linalg.norm(ref)
+    rel = np.linalg.norm(got - ref) / nrm if nrm > 0 else np.linalg.norm(got - ref)
+    assert err <= MAX_ABS and rel <= REL_L2, f"{what}: max-abs {err:.3e} rel-L2 {rel:.3e}"
+
+
+def assert_lse_close(got, ref, what):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    inf = np.isneginf(ref)
+    assert np.array_equal(np.isneginf(got), inf), f"{what}: -inf pattern differs"
+    if (~inf).any():
+        err = np.abs(got[~inf] - ref[~inf]).max()
+        assert err <= MAX_ABS * 4, f"{what}: lse max-abs {err:.3e}"
+
+
+def run_uniform(case, P, kernel, cluster, dc=None):
+    dc = dc or rt.upload(case)
+    B, q, H = case.num_requests, case.q_len, case.num_heads
+    part, lse = rt.alloc_partials(B * P, q, H)
+    part.fill_(float("nan"))
+    rt.decode_partial(dc, part, lse, num_partitions=P, kernel=kernel, cluster=cluster)
+    ind = rt.uniform_indptr(B, P)
+    out = rt.merge_states(part, lse, ind, B, q, H, "f32")
+    return part, lse, out, ind, dc
+
+
+def oracle_uniform_chunks(case, P):
+    return orc.plan_chunks(case.context_lens, [P] * case.num_requests, case.block_size)
+
+
+@pytest.mark.parametrize("kernel", ["tc", "simt"])
+@pytest.mark.parametrize("P", [1, 2, 4])
+def test_tiny_config_partials_and_merge(kernel, P):
+    """B=1, H=16, ctx 4096, block 32, shuffled table, fp16, partitions {1,2,4}."""
+    case = gen.make_decode_case(1, [4096], num_heads=16, block_size=32, dtype="f16")
+    nb.mla_reset_counters()
+    part, lse, out, ind, dc = run_uniform(case, P, KERNELS[kernel], cluster=4)
+    ctr = nb.mla_get_counters()
+    assert ctr[nb.CTR_PARTIAL_TC if kernel == "tc" else nb.CTR_PARTIAL_SIMT] == 1 and ctr[nb.CTR_MERGE] == 1
+    chunks, indptr = oracle_uniform_chunks(case, P)
+    ref_part, ref_lse = orc.partials(case, chunks)
+    assert_close(part.cpu().numpy(), ref_part, f"partials {kernel} P={P}")
+    assert_lse_close(lse.cpu().numpy(), ref_lse, f"lse {kernel} P={P}")
+    ref, _ = orc.unsplit(case)
+    out32 = out.cpu().numpy().astype(np.float64)
+    assert_close(out32, ref, f"merged {kernel} P={P}")
+    # 16-bit output: the fp32 result rounded once ...
+    out16 = rt.merge_states(part, lse, ind, 1, 1, 16, "f16")
+    assert torch.equal(out16, out.to(torch.float16))
+    # ... so within one ulp (plus the fp32 error) of the exact result rounded once
+    exact16 = torch.from_numpy(ref).to(torch.float16)
+    ulp = np.abs(np.spacing(exact16.numpy()).astype(np.float64))
+    dist = np.abs(out16.cpu().double().numpy() - exact16.double().numpy())
+    assert np.all(dist <= ulp + np.abs(out32 - ref) + 1e-12)
+
+
+@pytest.mark.parametrize("kernel", ["tc", "simt"])
+def test_bitwise_reproducible_for_one_plan(kernel):
+    case = gen.make_decode_case(2, [9000, 3001], num_heads=16, block_size=32, dtype="f16")
+    outs = []
+    dc = rt.upload(case)
+    for _ in range(3):
+        _, _, out, _, _ = run_uniform(case, 3, KERNELS[kernel], cluster=4, dc=dc)
+        outs.append(out.clone())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+@pytest.mark.parametrize("kernel", ["tc", "simt"])
+def test_paging_invariance_bitwise(kernel):
+    case = gen.make_decode_case(3, [5000, 777], num_heads=16, block_size=16, dtype="f16")
+    _, _, a, _, _ = run_uniform(case, 2, KERNELS[kernel], cluster=2)
+    _, _, b, _, _ = run_uniform(gen.permute_pool(case, 11), 2, KERNELS[kernel], cluster=2)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("kernel", ["tc", "simt"])
+@pytest.mark.parametrize("bs", [16, 32, 64])
+def test_ragged_lengths_and_empty_requests(kernel, bs):
+    lens = [0, 1, 31, 33, 64, 65, 100, 1000]
+    case = gen.make_decode_case(4, lens, num_heads=16, block_size=bs, dtype="f16")
+    part, lse, out, _, _ = run_uniform(case, 3, KERNELS[kernel], cluster=2)
+    chunks, _ = oracle_uniform_chunks(case, 3)
+    ref_part, ref_lse = orc.partials(case, chunks)
+    assert_close(part.cpu().numpy(), ref_part, "partials")
+    assert_lse_close(lse.cpu().numpy(), ref_lse, "lse")
+    ref, _ = orc.unsplit(case)
+    got = out.cpu().numpy()
+    assert np.all(got[0] == 0)  # empty request merges to zeros
+    assert_close(got[1:], ref[1:], "merged")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("H", [16, 64, 128])
+def test_heads_and_dtypes(dtype, H):
+    case = gen.make_decode_case(5, [2500, 700], num_heads=H, block_size=64 if dtype == "bf16" else 32,
+                                dtype=dtype, latent_std=0.5 if dtype == "bf16" else 1.0)
+    ref, _ = orc.unsplit(case)
+    for kernel in ("tc", "simt"):
+        part, lse, out, _, _ = run_uniform(case, 2, KERNELS[kernel], cluster=2)
+        assert_close(out.cpu().numpy(), ref, f"{kernel} H={H} {dtype}")
+
+
+def test_out_lse_and_hierarchical_merge_is_associative():
+    case = gen.make_decode_case(6, [6000], num_heads=16, block_size=32, dtype="f16")
+    part, lse, out, _, _ = run_uniform(case, 4, nb.MLA_KERNEL_TC, cluster=2)
+    # merge (0,1) and (2,3) separately, then merge the two results by their LSE
+    ind2 = torch.tensor([0, 2, 4], dtype=torch.int32, device="cuda")
+    lse2 = torch.empty((2, 1, 16), dtype=torch.float32, device="cuda")
+    half = rt.merge_states(part, lse, ind2, 2, 1, 16, "f32", out_lse=lse2)
+    ind1 = torch.tensor([0, 2], dtype=torch.int32, device="cuda")
+    top = rt.merge_states(half.contiguous(), lse2, ind1, 1, 1, 16, "f32")
+    assert_close(top.cpu().numpy(), out.cpu().numpy(), "hierarchical vs flat")
+    lse1 = torch.empty((1, 1, 16), dtype=torch.float32, device="cuda")
+    rt.merge_states(part, lse, rt.uniform_indptr(1, 4), 1, 1, 16, "f32", out_lse=lse1)
+    _, ref_lse = orc.unsplit(case)
+    assert_lse_close(lse1.cpu().numpy(), ref_lse, "merged lse")
+
+
+def test_natural_log_lse_fails_parity_on_the_gpu_merge():
+    """Negative control: natural-log LSE fed to the base-2 merge gives a wrong answer."""
+    case = gen.make_decode_case(7, [4096], num_heads=16, block_size=32, dtype="f16")
+    part, lse, out, ind, _ = run_uniform(case, 4, nb.MLA_KERNEL_TC, cluster=2)
+    ref, _ = orc.unsplit(case)
+    assert_close(out.cpu().numpy(), ref, "log2 merge")
+    bad = rt.merge_states(part, lse * math.log(2.0), ind, 1, 1, 16, "f32").cpu().numpy()
+    err = np.abs(bad - ref).max()
+    rel = np.linalg.norm(bad - ref) / np.linalg.norm(ref)
+    assert err > MAX_ABS or rel > REL_L2, "natural-log LSE should not pass parity"
+
+
+def plan_and_run(case, max_partitions=0, kernel=nb.MLA_KERNEL_TC, dc=None):
+    dev = nb.mla_device_query()
+    plan = nb.mla_plan(case.context_lens.tolist(), case.num_heads, case.q_len, case.block_size, dev,
+                       max_partitions=max_partitions, dtype=case.dtype)
+    dc = dc or rt.upload(case)
+    chunks_dev = rt.chunks_to_device(plan.chunks)
+    part, lse = rt.alloc_partials(plan.num_chunks, case.q_len, case.num_heads)
+    rt.decode_partial(dc, part, lse, chunks_dev=chunks_dev, kernel=kernel, cluster=plan.cluster_ctas)
+    ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
+    out = rt.merge_states(part, lse, ind, case.num_requests, case.q_len, case.num_heads, "f32")
+    return plan, part, lse, out
+
+
+@pytest.mark.parametrize("L", [32768, 131072])
+def test_long_context_planned_full_size_sampled_heads(L):
+    case = gen.make_decode_case(2, [L], num_heads=16, block_size=32, dtype="f16")
+    nb.mla_reset_counters()
+    plan, part, lse, out = plan_and_run(case)
+    assert 2 <= plan.num_chunks <= 8, plan.parts()
+    assert nb.mla_get_counters()[nb.CTR_PARTIAL_TC] == 1
+    heads = [0, 7, 15]
+    ref, _ = orc.unsplit(case, heads=heads)
+    assert_close(out.cpu().numpy()[:, :, heads], ref[:, :, heads], f"L={L}")
+
+
+def test_mixed_batch_request_major():
+    case = gen.make_decode_case(3, [32768, 20000], num_heads=16, block_size=32, dtype="f16")
+    plan, part, lse, out = plan_and_run(case, max_partitions=4)
+    assert all(2 <= p <= 4 for p in plan.parts()), plan.parts()
+    heads = [0, 5, 10, 15]
+    ref, _ = orc.unsplit(case, heads=heads)
+    assert_close(out.cpu().numpy()[:, :, heads], ref[:, :, heads], "mixed batch")
+
+
+def test_many_heads_bf16_planned_sampled():
+    lens = gen.uniform_lengths(4, 8, 4096, 65536)
+    case = gen.make_decode_case(4, lens, num_heads=128, block_size=64, dtype="bf16", latent_std=0.5)
+    plan, part, lse, out = plan_and_run(case, max_partitions=64)
+    heads = [0, 47, 48, 95, 96, 127]
+    ref, _ = orc.unsplit(case, heads=heads)
+    assert_close(out.cpu().numpy()[:, :, heads], ref[:, :, heads], "H=128 bf16")
+
+
+def run_segments(seg, q_len, cluster=2):
+    B, H = seg.base.num_requests, seg.base.num_heads
+    nseg = len(seg.segments)
+    part, lse = rt.alloc_partials(B * nseg, q_len, H)
+    dc0 = rt.upload(seg.segments[0])
+    for k, s in enumerate(seg.segments):
+        dc = rt.upload(s, ckv=dc0.ckv, kpe=dc0.kpe)
+        # one partition per (request, segment); slot = b * nseg + k (request-major)
+        chunks = [(b, 0, int(s.context_lens[b]), b * nseg + k) for b in range(B)]
+        rt.decode_partial(dc, part, lse, chunks_dev=rt.chunks_to_device(chunks), kernel=nb.MLA_KERNEL_TC,
+                          cluster=cluster)
+    ind = rt.uniform_indptr(B, nseg)
+    out = rt.merge_states(part, lse, ind, B, q_len, H, "f32")
+    return out, part, lse, ind, dc0
+
+
+@pytest.mark.parametrize("q_len", [4, 9, 16, 32])
+def test_verify_windows_over_segments(q_len):
+    seg = gen.make_segmented_case(5, B=4, q_len=q_len, segment_tokens=(4096, 2048, 1024), num_heads=16,
+                                  block_size=32)
+    ref, _ = orc.unsplit(gen.concat_segments(seg))
+    out, part, lse, ind, dc0 = run_segments(seg, q_len)
+    assert_close(out.cpu().numpy(), ref, f"q_len={q_len}")
+    # positive control: the tail without its causal mask gives a different answer
+    B, nseg = 4, len(seg.segments)
+    tail = seg.segments[-1]
+    tail.causal = False
+    dc = rt.upload(tail, ckv=dc0.ckv, kpe=dc0.kpe)
+    chunks = [(b, 0, int(tail.context_lens[b]), b * nseg + nseg - 1) for b in range(B)]
+    rt.decode_partial(dc, part, lse, chunks_dev=rt.chunks_to_device(chunks), kernel=nb.MLA_KERNEL_TC, cluster=1)
+    bad = rt.merge_states(part, lse, ind, B, q_len, 16, "f32").cpu().numpy()
+    assert np.abs(bad - ref).max() > 3 * MAX_ABS
+
+
+def test_verify_window_full_prefix_sampled_heads():
+    """Prefix 81920 tokens in 3 segments, window of 16 rows, B=4, sampled heads."""
+    seg = gen.make_segmented_case(5, B=4, q_len=16, num_heads=16, block_size=32)
+    heads = [0, 9]
+    ref, _ = orc.unsplit(gen.concat_segments(seg), heads=heads)
+    out, *_ = run_segments(seg, 16, cluster=4)
+    assert_close(out.cpu().numpy()[:, :, heads], ref[:, :, heads], "full prefix")
+
+
+def test_out_of_range_page_reads_zeros_and_is_flagged():
+    case = gen.make_decode_case(8, [300], num_heads=16, block_size=32, dtype="f16")
+    case.block_table[0, 2] = case.num_blocks + 5  # a bad page id inside the context
+    nb.mla_check_device_errors(None)
+    part, lse, out, _, _ = run_uniform(case, 1, nb.MLA_KERNEL_TC, cluster=1)
+    st, code = nb.mla_check_device_errors(None)
+    assert st == nb.MLA_ERR_DEVICE_CHECK and code & 2
+    assert np.all(np.isfinite(out.cpu().numpy()))
