@@ -123,7 +123,7 @@ mla_status_t mla_device_query(int32_t device, mla_device_info_t* info) {
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) st = MLA_ERR_CUDA;
   info->num_sms = sms;
   for (int k = 0; k < 5; ++k)
-    info->max_clusters[k] = (st == MLA_OK) ? mla::tc_max_active_clusters(1 << k, 16, false) : 0;
+    info->max_clusters[k] = (st == MLA_OK) ? mla::tc128_max_active_clusters(1 << k) : 0;
   cudaGetLastError();
   cudaSetDevice(prev);
   return st;
@@ -229,10 +229,11 @@ mla_status_t mla_merge_states(const float* partials, const float* lse, const int
 
 mla_status_t mla_check_device_errors(void* stream, uint32_t* code_out) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
-  uint32_t a = 0, b = 0;
-  if (mla::simt_read_clear_error(&a) != cudaSuccess || mla::tc_read_clear_error(&b) != cudaSuccess)
+  uint32_t a = 0, b = 0, c = 0;
+  if (mla::simt_read_clear_error(&a) != cudaSuccess || mla::tc_read_clear_error(&b) != cudaSuccess ||
+      mla::tc128_read_clear_error(&c) != cudaSuccess)
     return MLA_ERR_CUDA;
-  const uint32_t code = a | b;
+  const uint32_t code = a | b | c;
   if (code_out != nullptr) *code_out = code;
   if (code & mla::MLA_DEVERR_TIMEOUT) return MLA_ERR_TIMEOUT;
   if (code != 0) return MLA_ERR_DEVICE_CHECK;

@@ -43,13 +43,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// Test the phase; if it is not complete the thread is suspended in hardware
+// until it completes or about `hint_ns` pass, so waiting warps do not take
+// issue slots from the warps doing work.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns = 1000000u) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -95,6 +98,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
       "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+
+// Prefetch a 2D tile into L2 (no shared-memory destination, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+               : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -285,10 +294,11 @@ __device__ __forceinline__ void uniform_chunk(int32_t L, int32_t P, int32_t p, i
   *t1 = static_cast<int32_t>(e < L ? e : L);
 }
 
-// Fill the chunk, the CTA's token sub-range (64-token units split evenly over
-// the cluster) and its query rows. Tokens are trimmed to the last one any row
+// Fill the chunk, the CTA's token sub-range (runs of `unit`-token tiles split
+// evenly over the cluster) and its query rows. Tokens are trimmed to the last one any row
 // of this CTA can see under the causal rule.
-__device__ __forceinline__ CtaWork cta_work(const PartialParams& p, int32_t rows_per_cta) {
+__device__ __forceinline__ CtaWork cta_work(const PartialParams& p, int32_t rows_per_cta,
+                                            int32_t unit = kTileTokens) {
   CtaWork w;
   const int32_t n = blockIdx.y;
   if (p.chunks != nullptr) {
@@ -322,13 +332,13 @@ __device__ __forceinline__ CtaWork cta_work(const PartialParams& p, int32_t rows
     if (tend > lim) tend = lim;
     if (tend < w.t0) tend = w.t0;
   }
-  const int32_t units = (tend - w.t0 + kTileTokens - 1) / kTileTokens;
+  const int32_t units = (tend - w.t0 + unit - 1) / unit;
   const int32_t C = static_cast<int32_t>(cluster_nctarank());
   const int32_t k = static_cast<int32_t>(cluster_ctarank());
   const int32_t u0 = static_cast<int32_t>((static_cast<long long>(units) * k) / C);
   const int32_t u1 = static_cast<int32_t>((static_cast<long long>(units) * (k + 1)) / C);
-  w.sub0 = w.t0 + u0 * kTileTokens;
-  w.sub1 = w.t0 + u1 * kTileTokens;
+  w.sub0 = w.t0 + u0 * unit;
+  w.sub1 = w.t0 + u1 * unit;
   if (w.sub1 > tend) w.sub1 = tend;
   if (w.sub0 > w.sub1) w.sub0 = w.sub1;
   return w;

@@ -52,6 +52,11 @@ cudaError_t launch_partial_simt(const CUtensorMap& tm_ckv, const CUtensorMap& tm
 cudaError_t launch_partial_tc(const CUtensorMap& tm_ckv, const CUtensorMap& tm_kpe, const PartialParams& p,
                               int num_chunks, int cluster, bool bf16, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+// 128-token-tile tensor-core kernel for CTAs of at most 16 rows (fp16 only).
+bool tc128_supports(int total_rows, bool bf16);
+cudaError_t launch_partial_tc128(const CUtensorMap& tm_ckv, const CUtensorMap& tm_kpe, const PartialParams& p,
+                                 int num_chunks, int cluster, cudaStream_t stream);
+int tc128_max_active_clusters(int cluster);
 
 // Query rows per CTA for q_len x H rows (SIMT: always 16).
 int simt_rows_per_cta();
@@ -61,5 +66,6 @@ int tc_max_active_clusters(int cluster, int rows_per_cta, bool bf16);
 
 cudaError_t simt_read_clear_error(uint32_t* out);
 cudaError_t tc_read_clear_error(uint32_t* out);
+cudaError_t tc128_read_clear_error(uint32_t* out);
 
 }  // namespace mla

@@ -5,22 +5,30 @@
 // matrix-absorbed MLA decode over a compressed-latent KV cache", *What
 // changed*: SDPA(q_absorbed, ckv, ckv, scale, mask = scale * q_pe @ kpe^T)).
 //
-// Both contractions are issued with tokens / latent columns on the MMA's M
-// side and the CTA's NR query rows (heads x window rows) on N, so one 128-row
-// MMA serves all heads that share a latent tile:
-//   S^T[tok, row]  = [ckv | kpe][tok, 0:576] . Q^T          M=128, N=NR, K=576
-//   O^T[d, row]   += ckv^T[d, tok] . P^T[tok, row]          M=128 (x4), N=NR, K=64
-// The tile of 64 tokens (8 ckv boxes + 1 kpe box of 64x64, 128-byte swizzle)
-// is the K-major A operand of the first product (rows 64..127 of that M=128
-// operand are ignored) and, read MN-major, the A operand of the second: every
-// latent byte leaves HBM once and is used twice from shared memory. S^T
-// (double-buffered) and O^T live in tensor memory.
+// Both contractions put tokens / latent columns on the MMA's M side and the
+// CTA's NR query rows (heads x window rows) on N, so one MMA serves every
+// head that shares a latent tile:
+//   S^T[tok, row]  = [ckv | kpe][tok, 0:576] . Q^T        M=64 tokens, N=NR, K=576
+//   O^T[d, row]   += ckv^T[d, tok] . P^T[tok, row]        M=128 (x4), N=NR, K=64
+// A tile of 64 tokens (8 ckv boxes + 1 kpe box of 64x64, 128-byte swizzle) is
+// the K-major A operand of the first product and, read MN-major, the A operand
+// of the second: every latent byte leaves HBM once and is used twice from
+// shared memory. S^T (double-buffered, M=64 layout: token t in TMEM lane
+// 32*(t/16) + t%16) and O^T (M=128 layout) live in tensor memory.
 //
-// Warp roles (192 threads): warps 0-3 softmax / O rescale / epilogue (TMEM
-// lanes 0..127), warp 4 TMA producer, warp 5 TMEM owner + MMA issuer.
-// Online softmax in base 2 with a lazy rescale: a column's reference max only
-// moves when the tile max exceeds it by more than 2^8, so P stays <= 256 and
-// the O rescale pass over TMEM is rare.
+// A tcgen05.mma with N <= 48 costs the same ~45 cycles whatever its size, so
+// the pipeline is built to keep the single MMA-issuing thread busy: two 72 KB
+// tile buffers fed by TMA with an L2 prefetch two tiles ahead, S^T and P^T
+// double-buffered, and a softmax that normally needs no cross-warp exchange.
+//
+// Warp roles (192 threads): warps 0-3 softmax / O rescale / epilogue, warp 4
+// TMA producer, warp 5 TMEM owner + MMA issuer.
+//
+// Online softmax in base 2 with a lazy reference max: P = 2^(s - m_ref) is
+// formed against the current reference; only when some score exceeds it by
+// more than 2^8 (always on the first tile) do the warps reduce the tile maxima,
+// move the reference and rescale O^T and the row sums. P therefore stays
+// <= 256 and the rescale pass is rare.
 //
 // With bf16 inputs P is carried as two bf16 terms (hi + lo, two MMAs per
 // step): a single bf16 rounding of P (8-bit mantissa) would by itself leave a
@@ -38,9 +46,10 @@ template <int NR, bool SPLIT>
 struct TcLayout {
   static constexpr uint32_t kQChunk = NR * 128;  // [NR x 64] 16-bit, swizzled
   static constexpr uint32_t kPBuf = NR * 128;    // P^T [NR x 64 tokens]
+  static constexpr uint32_t kPStage = (SPLIT ? 2 : 1) * kPBuf;
   static constexpr uint32_t kOffQ = 2 * kTileBytes;
   static constexpr uint32_t kOffP = kOffQ + 9 * kQChunk;
-  static constexpr uint32_t kOffSmall = kOffP + (SPLIT ? 2 : 1) * kPBuf;
+  static constexpr uint32_t kOffSmall = kOffP + 2 * kPStage;  // P^T double-buffered
   static constexpr uint32_t kSmallBytes = 2048;
   static constexpr uint32_t kSmem = kOffSmall + kSmallBytes + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = (6 * NR <= 32)    ? 32
@@ -52,17 +61,19 @@ struct TcLayout {
 };
 
 struct TcSmall {
-  uint64_t full[2], empty[2], sfull[2], sfree[2], pfull, odone, drain;
+  uint64_t full[2], empty[2], sfull[2], sfree[2], pfull[2], drain;
   uint32_t tmem_base;
   int32_t abort_flag;
-  int32_t need[2];
-  float red[2][64];    // per-warp column maxima / column sums
-  float mref[2][64];   // reference max per column, double-buffered by tile parity
-  float alpha[64];     // rescale factor per column of the current tile
+  float red[4][64];   // per-warp column maxima (rescale path) / row sums (epilogue)
+  float mref[64];     // reference max per column (log2 units of the scaled score)
+  float alpha[64];    // rescale factor per column
 };
 static_assert(sizeof(TcSmall) <= 2048, "small smem region");
 
 __device__ __forceinline__ uint32_t tmem_lane_base(int warp) { return static_cast<uint32_t>(32 * (warp & 3)) << 16; }
+
+// Descriptor advanced by a byte offset (start-address field, 16-byte units).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 template <int NR, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -88,19 +99,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm->full[b], 1);
       mbar_init(&sm->empty[b], 1);
       mbar_init(&sm->sfull[b], 1);
-      mbar_init(&sm->sfree[b], 2);
-      sm->need[b] = 0;
+      mbar_init(&sm->sfree[b], 4);
+      mbar_init(&sm->pfull[b], 4);
     }
-    mbar_init(&sm->pfull, 4);
-    mbar_init(&sm->odone, 1);
     mbar_init(&sm->drain, 1);
     sm->abort_flag = 0;
     fence_mbar_init();
   }
-  if (tid < 64) {
-    sm->mref[0][tid] = -INFINITY;
-    sm->mref[1][tid] = -INFINITY;
-  }
+  if (tid < 64) sm->mref[tid] = -INFINITY;
   if (warp == 5) {
     tmem_alloc(&sm->tmem_base, Lay::kTmemCols);
     tmem_relinquish();
@@ -133,6 +139,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int npages_req = (w.L + p.bs - 1) / p.bs;
     int win_base = -1, win_pid = -1, issued = 0;
+    // physical page of logical page pg (warp-uniform pg), through a 32-entry window
+    auto page_of = [&](int pg) -> int {
+      const int base = pg & ~31;
+      if (base != win_base) {
+        win_base = base;
+        const int q = base + lane;
+        win_pid = (q < npages_req && q < p.max_blocks) ? checked_page(p, w.b, q) : -1;
+      }
+      return __shfl_sync(0xffffffffu, win_pid, pg & 31);
+    };
+    auto l2_prefetch = [&](int i) {  // tile i into L2 (no smem, no barrier)
+      const int tok0 = w.sub0 + i * kTileTokens;
+      const int npg = (min(kTileTokens, w.sub1 - tok0) + p.bs - 1) / p.bs;
+      for (int k = 0; k < npg; ++k) {
+        const int pid = page_of(tok0 / p.bs + k);
+        if (lane == 0 && pid >= 0) {
+          for (int c = 0; c < kBoxesPerTile - 1; ++c) tma_prefetch_l2_2d(&tm_ckv, c * kBoxCols, pid * p.bs);
+          tma_prefetch_l2_2d(&tm_kpe, 0, pid * p.bs);
+        }
+      }
+    };
     for (int i = 0; i < ntiles; ++i) {
       const int buf = i & 1;
       if (i >= 2) {
@@ -149,19 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int npg = (ntok + p.bs - 1) / p.bs;
       int pids[kTileTokens / 16];
 #pragma unroll
-      for (int k = 0; k < kTileTokens / 16; ++k) {
-        pids[k] = -1;
-        if (k < npg) {
-          const int pg = pg0 + k;
-          const int base = pg & ~31;
-          if (base != win_base) {  // warp-uniform: refill the 32-entry page window
-            win_base = base;
-            const int q = base + lane;
-            win_pid = (q < npages_req && q < p.max_blocks) ? checked_page(p, w.b, q) : -1;
-          }
-          pids[k] = __shfl_sync(0xffffffffu, win_pid, pg & 31);
-        }
-      }
+      for (int k = 0; k < kTileTokens / 16; ++k) pids[k] = (k < npg) ? page_of(pg0 + k) : -1;
       if (lane == 0) {
         uint8_t* tb = tiles + buf * kTileBytes;
         mbar_arrive_expect_tx(&sm->full[buf], static_cast<uint32_t>(npg * p.bs * 128 * kBoxesPerTile));
@@ -173,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       issued = i + 1;
+      if (i + 2 < ntiles) l2_prefetch(i + 2);
     }
     if (lane == 0 && *abort_flag) {  // let loads in flight land before smem is released
       for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
@@ -180,34 +196,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer
-    const uint32_t idesc_s = idesc_f16_f32(128, NR, BF16, false, false);
+    const uint32_t idesc_s = idesc_f16_f32(64, NR, BF16, false, false);
     const uint32_t idesc_o = idesc_f16_f32(128, NR, BF16, true, false);
-    const uint32_t q_addr = smem_u32(qs), p_addr = smem_u32(ps), t_addr = smem_u32(tiles);
+    const uint32_t t_addr = smem_u32(tiles);
+    const uint64_t q_desc = smem_desc_sw128(smem_u32(qs), 16, 1024);
+    const uint64_t p_desc = smem_desc_sw128(smem_u32(ps), 16, 1024);
     auto issue_pv = [&](int j) -> bool {
+      const int b = j & 1;
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&sm->pfull, j & 1, p.timeout_ns);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        *abort_flag = 1;
+      if (lane == 0) ok = mbar_wait(&sm->pfull[b], (j >> 1) & 1, p.timeout_ns);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        if (lane == 0) *abort_flag = 1;
         return false;
       }
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t tb = t_addr + (j & 1) * kTileBytes;
+        const uint64_t a0 = smem_desc_sw128(t_addr + b * kTileBytes, kBoxBytes, 1024);
+        const uint64_t pb = desc_add(p_desc, b * Lay::kPStage);
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t adesc = smem_desc_sw128(tb + 2 * blk * kBoxBytes + ks * 16 * 128, kBoxBytes, 1024);
-            umma_f16_ss(tmem + 2 * NR + blk * NR, adesc, smem_desc_sw128(p_addr + ks * 32, 16, 1024), idesc_o,
-                        (j > 0 || ks > 0) ? 1u : 0u);
+            const uint64_t adesc = desc_add(a0, 2 * blk * kBoxBytes + ks * 16 * 128);
+            umma_f16_ss(tmem + 2 * NR + blk * NR, adesc, desc_add(pb, ks * 32), idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
             if constexpr (SPLIT)
-              umma_f16_ss(tmem + 2 * NR + blk * NR, adesc, smem_desc_sw128(p_addr + Lay::kPBuf + ks * 32, 16, 1024),
-                          idesc_o, 1u);
+              umma_f16_ss(tmem + 2 * NR + blk * NR, adesc, desc_add(pb, Lay::kPBuf + ks * 32), idesc_o, 1u);
           }
         }
-        umma_commit(&sm->empty[j & 1]);
-        umma_commit(&sm->odone);
+        umma_commit(&sm->empty[b]);  // tile buffer b and P^T buffer b are free again
       }
       __syncwarp();
       return true;
@@ -236,23 +252,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (i >= 2) {
         if (lane == 0) ok = mbar_wait(&sm->sfree[buf], ((i >> 1) - 1) & 1, p.timeout_ns);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          *abort_flag = 1;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          if (lane == 0) *abort_flag = 1;
           alive = false;
           break;
         }
       }
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t tb = t_addr + buf * kTileBytes;
+        const uint64_t a0 = smem_desc_sw128(t_addr + buf * kTileBytes, 16, 1024);
 #pragma unroll
         for (int c = 0; c < kBoxesPerTile; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_f16_ss(tmem + buf * NR, smem_desc_sw128(tb + c * kBoxBytes + kk * 32, 16, 1024),
-                        smem_desc_sw128(q_addr + c * Lay::kQChunk + kk * 32, 16, 1024), idesc_s,
-                        (c | kk) != 0 ? 1u : 0u);
+            umma_f16_ss(tmem + buf * NR, desc_add(a0, c * kBoxBytes + kk * 32),
+                        desc_add(q_desc, c * Lay::kQChunk + kk * 32), idesc_s, (c | kk) != 0 ? 1u : 0u);
         umma_commit(&sm->sfull[buf]);
       }
       __syncwarp();
@@ -269,102 +283,116 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ softmax (warps 0-3)
+    // Thread (warp, lane < 16) owns token 16*warp + lane of each tile (M=64 layout of S^T).
     float lsum[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) lsum[r] = 0.f;
-    const int tl = warp * 32 + lane;  // TMEM lane: token (S^T) or latent column within a block (O^T)
+    const bool owns_token = lane < 16;
+    const int tl = 16 * warp + lane;
+    // smallest causal limit over this CTA's rows: tiles below it need no causal mask
+    const int causal_floor = p.causal ? w.L - p.q_len + w.row0 / p.H : 0x7fffffff;
     for (int i = 0; i < ntiles; ++i) {
       const int buf = i & 1;
       const int tok0 = w.sub0 + i * kTileTokens;
       const int nvalid = min(kTileTokens, w.sub1 - tok0);
+      const bool masked_tile = (nvalid < kTileTokens) || (tok0 + kTileTokens - 1 > causal_floor) ||
+                               (w.nrows < NR);
       float x[NR];
-      if (warp < 2) {
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(&sm->sfull[buf], (i >> 1) & 1, p.timeout_ns);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          *abort_flag = 1;
-        } else {
-          tc_fence_after();
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&sm->sfull[buf], (i >> 1) & 1, p.timeout_ns);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      bool need_local = false;
+      if (ok) {
+        tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < NR; c += 16) tmem_ld16(tmem + tmem_lane_base(warp) + buf * NR + c, x + c);
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm->sfree[buf]);
-          const int t = tok0 + tl;
-#pragma unroll
-          for (int r = 0; r < NR; ++r) {
-            const int row = w.row0 + r;
-            bool vis = (tl < nvalid) && (r < w.nrows);
-            if (p.causal) vis = vis && (t <= w.L - p.q_len + row / p.H);
-            x[r] = vis ? x[r] * p.scale_log2 : -INFINITY;
-            float v = x[r];
-            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-            if (lane == 0) sm->red[warp][r] = v;
-          }
-        }
-      }
-      if (i >= 1) {  // PV(i-1) finished: P^T may be overwritten, O may be rescaled
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(&sm->odone, (i - 1) & 1, p.timeout_ns);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) *abort_flag = 1;
-      }
-      if (named_bar_sync_or(1, 128, *abort_flag != 0)) break;
-      // per-column reference max (lazy): one thread per column
-      if (tid < NR) {
-        const int r = tid;
-        const float mprev = sm->mref[buf ^ 1][r];
-        const float tmax = fmaxf(sm->red[0][r], sm->red[1][r]);
-        const bool need = tmax > mprev + kRescaleTau;
-        const float mnew = need ? fmaxf(mprev, tmax) : mprev;
-        sm->mref[buf][r] = mnew;
-        sm->alpha[r] = (need && mnew != -INFINITY) ? exp2f(mprev - mnew) : 1.f;
-        if (need) sm->need[buf] = 1;
-      }
-      if (tid == 0) sm->need[buf ^ 1] = 0;
-      named_bar_sync(1, 128);
-      const bool rescale = sm->need[buf] != 0;
-      if (rescale) {
-        if (i >= 1) {  // O^T columns *= alpha (lanes = latent columns of each 128-block)
-          tc_fence_after();
-#pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
-#pragma unroll
-            for (int c = 0; c < NR; c += 16) {
-              float v[16];
-              const uint32_t a = tmem + tmem_lane_base(warp) + 2 * NR + blk * NR + c;
-              tmem_ld16(a, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] *= sm->alpha[c + j];
-              tmem_st16(a, v);
-            }
-          }
-          tmem_wait_st();
-        }
-        if (warp < 2) {
-#pragma unroll
-          for (int r = 0; r < NR; ++r) lsum[r] *= sm->alpha[r];
-        }
-      }
-      if (warp < 2) {  // probabilities -> P^T (16-bit, K-major, swizzled) and row sums
+        for (int c = 0; c < NR; c += 16) tmem_ld16(tmem + tmem_lane_base(warp) + buf * NR + c, x + c);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->sfree[buf]);
+        const int t = tok0 + tl;
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
-          const float m = sm->mref[buf][r];
-          const float pr = (x[r] == -INFINITY) ? 0.f : exp2f(x[r] - m);
+          bool vis = owns_token;
+          if (masked_tile) {
+            vis = vis && (tl < nvalid) && (r < w.nrows);
+            if (p.causal) vis = vis && (t <= w.L - p.q_len + (w.row0 + r) / p.H);
+          }
+          x[r] = vis ? x[r] * p.scale_log2 : -INFINITY;
+          need_local |= x[r] > sm->mref[r] + kRescaleTau;
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < NR; ++r) x[r] = -INFINITY;
+        if (lane == 0) *abort_flag = 1;
+      }
+      // one barrier per tile; it is also where an abort becomes a uniform decision
+      if (named_bar_sync_or(1, 128, need_local || *abort_flag != 0)) {
+        if (named_bar_sync_or(1, 128, *abort_flag != 0)) break;
+        // rare path: move the reference max, rescale O^T and the row sums
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          float v = x[r];
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+          if (lane == 0) sm->red[warp][r] = v;
+        }
+        named_bar_sync(1, 128);
+        if (tid < NR) {
+          const float mprev = sm->mref[tid];
+          const float tmax = fmaxf(fmaxf(sm->red[0][tid], sm->red[1][tid]), fmaxf(sm->red[2][tid], sm->red[3][tid]));
+          const float mnew = fmaxf(mprev, tmax);
+          sm->alpha[tid] = (mnew == -INFINITY) ? 1.f : exp2f(mprev - mnew);
+          sm->mref[tid] = mnew;
+        }
+        named_bar_sync(1, 128);
+        if (i >= 1) {  // PV(i-1) must be complete before O^T is rescaled
+          int ok2 = 1;
+          if (lane == 0) ok2 = mbar_wait(&sm->empty[(i - 1) & 1], ((i - 1) >> 1) & 1, p.timeout_ns);
+          if (__shfl_sync(0xffffffffu, ok2, 0)) {
+            tc_fence_after();
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+              for (int c = 0; c < NR; c += 16) {
+                float v[16];
+                const uint32_t a = tmem + tmem_lane_base(warp) + 2 * NR + blk * NR + c;
+                tmem_ld16(a, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] *= sm->alpha[c + j];
+                tmem_st16(a, v);
+              }
+            }
+            tmem_wait_st();
+          } else if (lane == 0) {
+            *abort_flag = 1;
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r) lsum[r] *= sm->alpha[r];
+      }
+      // P^T buffer `buf` was last read by PV(i-2)
+      if (i >= 2) {
+        int ok3 = 1;
+        if (lane == 0) ok3 = mbar_wait(&sm->empty[buf], ((i >> 1) - 1) & 1, p.timeout_ns);
+        if (!__shfl_sync(0xffffffffu, ok3, 0) && lane == 0) *abort_flag = 1;
+      }
+      if (owns_token) {  // probabilities -> P^T (16-bit, K-major, swizzled) and row sums
+        uint8_t* pb = ps + buf * Lay::kPStage;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          const float pr = (x[r] == -INFINITY) ? 0.f : exp2f(x[r] - sm->mref[r]);
           const uint16_t hv = f2h<BF16>(pr);
           float used = h2f<BF16>(hv);
-          *reinterpret_cast<uint16_t*>(ps + sw128_offset(r, tl)) = hv;
+          *reinterpret_cast<uint16_t*>(pb + sw128_offset(r, tl)) = hv;
           if constexpr (SPLIT) {
             const uint16_t lv = f2h<BF16>(pr - used);
             used += h2f<BF16>(lv);
-            *reinterpret_cast<uint16_t*>(ps + Lay::kPBuf + sw128_offset(r, tl)) = lv;
+            *reinterpret_cast<uint16_t*>(pb + Lay::kPBuf + sw128_offset(r, tl)) = lv;
           }
           lsum[r] += used;
         }
@@ -372,27 +400,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm->pfull);
+      if (lane == 0) mbar_arrive(&sm->pfull[buf]);
     }
-    // wait for the last PV, then reduce the row sums over the 64 token lanes
+    // after the last PV: reduce the row sums over the 64 token lanes
     const bool aborted = named_bar_sync_or(1, 128, *abort_flag != 0);  // same answer in all 4 warps
     if (ntiles > 0 && !aborted) {
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&sm->odone, (ntiles - 1) & 1, p.timeout_ns);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) *abort_flag = 1;
+      if (lane == 0) ok = mbar_wait(&sm->empty[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, p.timeout_ns);
+      if (!__shfl_sync(0xffffffffu, ok, 0) && lane == 0) *abort_flag = 1;
     }
-    if (warp < 2) {
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        float v = lsum[r];
-        v += __shfl_xor_sync(0xffffffffu, v, 16);
-        v += __shfl_xor_sync(0xffffffffu, v, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        if (lane == 0) sm->red[warp][r] = v;
-      }
+    for (int r = 0; r < NR; ++r) {
+      float v = owns_token ? lsum[r] : 0.f;
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      if (lane == 0) sm->red[warp][r] = v;
     }
     named_bar_sync(1, 128);
   }
@@ -420,9 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int idx = tid; idx < NR * kRank; idx += 128) ostage[idx] = 0.f;
     }
     if (tid < NR) {
-      const int buf_last = (ntiles - 1) & 1;
-      mst[tid] = have ? sm->mref[buf_last][tid] : -INFINITY;
-      lst[tid] = have ? sm->red[0][tid] + sm->red[1][tid] : 0.f;
+      mst[tid] = have ? sm->mref[tid] : -INFINITY;
+      lst[tid] = have ? (sm->red[0][tid] + sm->red[1][tid]) + (sm->red[2][tid] + sm->red[3][tid]) : 0.f;
     }
   }
   tc_fence_before();
@@ -441,35 +465,21 @@ const void* tc_fn() {
   return reinterpret_cast<const void*>(&mla_partial_tc_kernel<NR, BF16>);
 }
 
-// Instantiated variants: fp16 {16, 32, 64} rows; bf16 {16, 32, 48} rows (its
-// second P buffer leaves no room for 64 rows next to two 72 KB tiles).
+// Instantiated variants: {16, 32, 48} rows for fp16 and bf16 (64 rows would not
+// fit next to two 72 KB tiles once P^T is double-buffered).
 const void* tc_kernel_ptr(int nr, bool bf16) {
-  if (bf16) {
-    switch (nr) {
-      case 16: return tc_fn<16, true>();
-      case 32: return tc_fn<32, true>();
-      default: return tc_fn<48, true>();
-    }
-  }
   switch (nr) {
-    case 16: return tc_fn<16, false>();
-    case 32: return tc_fn<32, false>();
-    default: return tc_fn<64, false>();
+    case 16: return bf16 ? tc_fn<16, true>() : tc_fn<16, false>();
+    case 32: return bf16 ? tc_fn<32, true>() : tc_fn<32, false>();
+    default: return bf16 ? tc_fn<48, true>() : tc_fn<48, false>();
   }
 }
 
 uint32_t tc_smem(int nr, bool bf16) {
-  if (bf16) {
-    switch (nr) {
-      case 16: return TcLayout<16, true>::kSmem;
-      case 32: return TcLayout<32, true>::kSmem;
-      default: return TcLayout<48, true>::kSmem;
-    }
-  }
   switch (nr) {
-    case 16: return TcLayout<16, false>::kSmem;
-    case 32: return TcLayout<32, false>::kSmem;
-    default: return TcLayout<64, false>::kSmem;
+    case 16: return bf16 ? TcLayout<16, true>::kSmem : TcLayout<16, false>::kSmem;
+    case 32: return bf16 ? TcLayout<32, true>::kSmem : TcLayout<32, false>::kSmem;
+    default: return bf16 ? TcLayout<48, true>::kSmem : TcLayout<48, false>::kSmem;
   }
 }
 
@@ -496,15 +506,17 @@ cudaError_t prepare(const void* fn, int nr, bool bf16, int cluster) {
 
 }  // namespace
 
-int tc_rows_per_cta(int total_rows, bool bf16) {
-  if (total_rows <= 16) return 16;
-  if (total_rows <= 32) return 32;
-  return bf16 ? 48 : 64;
+// Rows per CTA: the fewest groups of at most 48 rows, balanced, rounded up to 16.
+int tc_rows_per_cta(int total_rows, bool) {
+  const int groups = (total_rows + 47) / 48;
+  const int per = (total_rows + groups - 1) / groups;
+  return per <= 16 ? 16 : (per <= 32 ? 32 : 48);
 }
 
 cudaError_t launch_partial_tc(const CUtensorMap& tm_ckv, const CUtensorMap& tm_kpe, const PartialParams& p,
                               int num_chunks, int cluster, bool bf16, cudaStream_t stream) {
   const int rows = p.q_len * p.H;
+  if (tc128_supports(rows, bf16)) return launch_partial_tc128(tm_ckv, tm_kpe, p, num_chunks, cluster, stream);
   const int nr = tc_rows_per_cta(rows, bf16);
   const void* fn = tc_kernel_ptr(nr, bf16);
   cudaError_t e = prepare(fn, nr, bf16, cluster);
@@ -531,7 +543,7 @@ cudaError_t launch_partial_tc(const CUtensorMap& tm_ckv, const CUtensorMap& tm_k
   switch (nr) {
     case 16: return cudaLaunchKernelEx(&cfg, mla_partial_tc_kernel<16, false>, tm_ckv, tm_kpe, p);
     case 32: return cudaLaunchKernelEx(&cfg, mla_partial_tc_kernel<32, false>, tm_ckv, tm_kpe, p);
-    default: return cudaLaunchKernelEx(&cfg, mla_partial_tc_kernel<64, false>, tm_ckv, tm_kpe, p);
+    default: return cudaLaunchKernelEx(&cfg, mla_partial_tc_kernel<48, false>, tm_ckv, tm_kpe, p);
   }
 }
 
