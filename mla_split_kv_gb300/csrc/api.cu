@@ -44,6 +44,7 @@ struct MapKey {
   uint32_t box_rows;
   int dtype;
   int device;
+  int kind;  // 0: the 2D map; 1: the page map of the ckv cache (see page_map)
 };
 struct MapEntry {
   MapKey key;
@@ -56,13 +57,28 @@ int g_map_next = 0;
 
 bool same(const MapKey& a, const MapKey& b) {
   return a.base == b.base && a.rows == b.rows && a.cols == b.cols && a.box_rows == b.box_rows && a.dtype == b.dtype &&
-         a.device == b.device;
+         a.device == b.device && a.kind == b.kind;
 }
+
+bool encode_map(CUtensorMap* out, const MapKey& key);
 
 bool tensor_map(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, int dtype) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  const MapKey key{base, rows, cols, box_rows, dtype, dev};
+  return encode_map(out, MapKey{base, rows, cols, box_rows, dtype, dev, 0});
+}
+
+// 4D map over the [rows, 512] ckv cache seen as (64 columns, 8 rows, 8 column
+// blocks, rows / 8 row groups), boxes of (64, 8, 4, box_rows / 8): one box is
+// the 256 columns of one half of a page, landing as row groups of four
+// swizzled [8 x 64] atoms (the layout the paired tensor-core kernel reads).
+bool page_map(CUtensorMap* out, const void* base, uint64_t rows, uint32_t box_rows, int dtype) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  return encode_map(out, MapKey{base, rows, static_cast<uint64_t>(mla::kRank), box_rows, dtype, dev, 1});
+}
+
+bool encode_map(CUtensorMap* out, const MapKey& key) {
   std::lock_guard<std::mutex> lock(g_map_mu);
   for (auto& e : g_maps)
     if (e.valid && same(e.key, key)) {
@@ -73,14 +89,25 @@ bool tensor_map(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols
   if (enc == nullptr) return false;
   CUtensorMap m;
   std::memset(&m, 0, sizeof(m));
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(mla::kBoxCols), box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(&m, dtype == MLA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUtensorMapDataType dt =
+      key.dtype == MLA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r;
+  if (key.kind == 0) {
+    cuuint64_t dims[2] = {key.cols, key.rows};
+    cuuint64_t strides[1] = {key.cols * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(mla::kBoxCols), key.box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    r = enc(&m, dt, 2, const_cast<void*>(key.base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    if (key.rows % 8 != 0 || key.box_rows % 8 != 0) return false;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(mla::kBoxCols), 8, key.cols / mla::kBoxCols, key.rows / 8};
+    cuuint64_t strides[3] = {key.cols * 2, mla::kBoxCols * 2, key.cols * 2 * 8};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(mla::kBoxCols), 8, 4, key.box_rows / 8};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    r = enc(&m, dt, 4, const_cast<void*>(key.base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) return false;
   g_maps[g_map_next] = MapEntry{key, m, true};
   g_map_next = (g_map_next + 1) % 32;
@@ -160,9 +187,10 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   const uint64_t rows = static_cast<uint64_t>(d->num_blocks) * static_cast<uint64_t>(d->block_size);
   if (rows > 0x7fffffffull) return reject(MLA_ERR_UNSUPPORTED);
 
-  CUtensorMap tm_ckv, tm_kpe;
+  CUtensorMap tm_ckv, tm_kpe, tm_pages;
   if (!tensor_map(&tm_ckv, ckv_cache, rows, mla::kRank, d->block_size, d->dtype) ||
-      !tensor_map(&tm_kpe, kpe_cache, rows, mla::kRope, d->block_size, d->dtype))
+      !tensor_map(&tm_kpe, kpe_cache, rows, mla::kRope, d->block_size, d->dtype) ||
+      !page_map(&tm_pages, ckv_cache, rows, d->block_size, d->dtype))
     return reject(MLA_ERR_CUDA);
 
   mla::PartialParams p;
@@ -170,6 +198,8 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   p.q_pe = static_cast<const uint16_t*>(q_pe);
   p.block_table = block_table;
   p.context_lens = context_lens;
+  p.ckv = static_cast<const uint8_t*>(ckv_cache);
+  p.kpe = static_cast<const uint8_t*>(kpe_cache);
   p.chunks = d->chunks;
   p.partials = partials;
   p.lse = lse;
@@ -192,7 +222,7 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   const int C = C0 ? C0 : default_cluster(N * groups);
   cudaStream_t stream = static_cast<cudaStream_t>(d->stream);
   const cudaError_t e = use_simt ? mla::launch_partial_simt(tm_ckv, tm_kpe, p, static_cast<int>(N), C, bf16, stream)
-                                 : mla::launch_partial_tc(tm_ckv, tm_kpe, p, static_cast<int>(N), C, bf16, stream);
+                                 : mla::launch_partial_tc(tm_ckv, tm_kpe, tm_pages, p, static_cast<int>(N), C, bf16, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;

@@ -87,6 +87,15 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// Prefetch `bytes` contiguous bytes into L2 (address and size multiples of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
@@ -97,6 +106,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
       "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// 4D tile load (coordinates innermost first).
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2,
+                                            int32_t c3, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 
@@ -113,6 +132,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // Named barrier over `count` threads (multiple of 32), id 1..15.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Arrive on a named barrier without waiting (the consumer side calls named_bar_sync).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 // Named barrier that also ORs a predicate over the participating threads:
 // every thread gets the same answer (a uniform decision, e.g. to abort).
@@ -142,6 +165,12 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Split cluster barrier: arrive (release) now, wait (acquire) later. Every
+// thread that arrives must wait before it arrives again.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 // Address of the same shared variable in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
   uint32_t out;
@@ -159,6 +188,54 @@ __device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr) {
   float4 v;
   asm("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
   return v;
+}
+
+// Store to another CTA's shared memory; published by a release arrive on that
+// CTA's mbarrier (mbar_remote_arrive) issued after it.
+__device__ __forceinline__ void dsmem_st_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// Asynchronous 16-byte store to another CTA's shared memory; its bytes count
+// as completed transactions on that CTA's mbarrier `remote_bar` (both
+// addresses from dsmem_addr). The sender does not wait for it.
+__device__ __forceinline__ void dsmem_st_async_f32x4(uint32_t addr, float4 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+               : "memory");
+}
+// Arrive, with release semantics at cluster scope, on an mbarrier of another
+// CTA (address from dsmem_addr).
+__device__ __forceinline__ void mbar_remote_arrive(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+// Arrive without memory ordering on an mbarrier of another CTA: a pure signal,
+// for use only where every access it must follow has completed (values
+// consumed and a CTA barrier passed since).
+__device__ __forceinline__ void mbar_remote_arrive_relaxed(uint32_t addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+// Bounded wait on a local mbarrier whose arrivals come from other CTAs of the
+// cluster: acquire at cluster scope, so their stores before the arrive are visible.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  auto test = [&]() -> bool {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+        : "memory");
+    return ok != 0;
+  };
+  if (test()) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (test()) return true;
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      flag_error(MLA_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -295,10 +372,11 @@ __device__ __forceinline__ void uniform_chunk(int32_t L, int32_t P, int32_t p, i
 }
 
 // Fill the chunk, the CTA's token sub-range (runs of `unit`-token tiles split
-// evenly over the cluster) and its query rows. Tokens are trimmed to the last one any row
+// evenly over the cluster, or over `nparts` groups of it, this CTA in group
+// `part`) and its query rows. Tokens are trimmed to the last one any row
 // of this CTA can see under the causal rule.
 __device__ __forceinline__ CtaWork cta_work(const PartialParams& p, int32_t rows_per_cta,
-                                            int32_t unit = kTileTokens) {
+                                            int32_t unit = kTileTokens, int32_t part = -1, int32_t nparts = 0) {
   CtaWork w;
   const int32_t n = blockIdx.y;
   if (p.chunks != nullptr) {
@@ -333,8 +411,8 @@ __device__ __forceinline__ CtaWork cta_work(const PartialParams& p, int32_t rows
     if (tend < w.t0) tend = w.t0;
   }
   const int32_t units = (tend - w.t0 + unit - 1) / unit;
-  const int32_t C = static_cast<int32_t>(cluster_nctarank());
-  const int32_t k = static_cast<int32_t>(cluster_ctarank());
+  const int32_t C = (nparts > 0) ? nparts : static_cast<int32_t>(cluster_nctarank());
+  const int32_t k = (nparts > 0) ? part : static_cast<int32_t>(cluster_ctarank());
   const int32_t u0 = static_cast<int32_t>((static_cast<long long>(units) * k) / C);
   const int32_t u1 = static_cast<int32_t>((static_cast<long long>(units) * (k + 1)) / C);
   w.sub0 = w.t0 + u0 * unit;

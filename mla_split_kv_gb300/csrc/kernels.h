@@ -25,6 +25,8 @@ struct PartialParams {
   const uint16_t* q_pe;        // [B, q_len, H, 64]
   const int32_t* block_table;  // [B, max_blocks]
   const int32_t* context_lens; // [B]
+  const uint8_t* ckv;          // ckv cache base: page g at g * bs * 1024 bytes
+  const uint8_t* kpe;          // kpe cache base: page g at g * bs * 128 bytes
   const void* chunks;          // device int4 {b, t0, t1, slot} per chunk, or null
   float* partials;             // [slots, q_len, H, 512]
   float* lse;                  // [slots, q_len, H]
@@ -49,12 +51,14 @@ struct MergeParams {
 // `cluster` CTAs, grid.y = chunks, grid.z = row groups.
 cudaError_t launch_partial_simt(const CUtensorMap& tm_ckv, const CUtensorMap& tm_kpe, const PartialParams& p,
                                 int num_chunks, int cluster, bool bf16, cudaStream_t stream);
-cudaError_t launch_partial_tc(const CUtensorMap& tm_ckv, const CUtensorMap& tm_kpe, const PartialParams& p,
-                              int num_chunks, int cluster, bool bf16, cudaStream_t stream);
+// tm_pages: 4D map of the ckv cache whose box is one half (256 columns) of a page.
+cudaError_t launch_partial_tc(const CUtensorMap& tm_ckv, const CUtensorMap& tm_kpe, const CUtensorMap& tm_pages,
+                              const PartialParams& p, int num_chunks, int cluster, bool bf16, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
-// 128-token-tile tensor-core kernel for CTAs of at most 16 rows (fp16 only).
-bool tc128_supports(int total_rows, bool bf16);
-cudaError_t launch_partial_tc128(const CUtensorMap& tm_ckv, const CUtensorMap& tm_kpe, const PartialParams& p,
+// 128-token-tile tensor-core kernel for CTAs of at most 16 rows (fp16 only),
+// CTAs in pairs that split the latent columns (cluster of 2..16 CTAs).
+bool tc128_supports(int total_rows, bool bf16, int cluster);
+cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe, const PartialParams& p,
                                  int num_chunks, int cluster, cudaStream_t stream);
 int tc128_max_active_clusters(int cluster);
 

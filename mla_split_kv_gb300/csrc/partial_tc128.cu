@@ -1,4 +1,5 @@
-// Tensor-core partial-decode kernel for CTAs of 16 query rows (fp16), sm_103a.
+// Tensor-core partial-decode kernel for CTAs of 16 query rows (fp16) working
+// in pairs, sm_103a.
 //
 // The operation is the one of the other partial kernels ("feat(core):
 // matrix-absorbed MLA decode over a compressed-latent KV cache", *What
@@ -8,54 +9,76 @@
 // 16 query rows (the heads of a one-token decode) are too few for the tensor
 // core's M side, so both products put tokens / latent columns on M=128 and the
 // 16 rows on N:
-//   S^T[tok, row] = [ckv | kpe][tok, 0:576] . Q^T      M=128 tokens, N=16, K=576
-//   O^T[d, row]  += ckv^T[d, tok] . P^T[tok, row]      M=128 (x4), N=16, K=128
-// At N=16 every tcgen05.mma costs about the same fixed time, so a tile of 128
-// tokens (68 MMAs) is used rather than 64 (52 MMAs for half the tokens). A
-// 128-token tile is 144 KB, more than half of shared memory, so the latent is
-// staged in a ring of five 32 KB "pair slots" (a pair = two 64-column ckv boxes
-// = one 128-column block of the latent for 128 tokens) plus two 16 KB kpe
-// slots. A pair slot is released as soon as the PV block that reads it is
-// done, and the MMA warp issues, per tile i: the head of the score product of
-// tile i (kpe and pair 0), the PV product of tile i-1, then the tail of the
-// score product of tile i (pairs 1..3). Reloads of released slots then overlap
-// MMA work, and the softmax of tile i-1 overlaps the head of tile i.
+//   S^T[tok, row] = [ckv | kpe][tok, :] . Q^T          M=128 tokens, N=16
+//   O^T[d, row]  += ckv^T[d, tok] . P^T[tok, row]      M=128 columns, N=16, K=128
+// At N=16 every tcgen05.mma costs about the same fixed time, so tiles are 128
+// tokens (the most one M=128 instruction covers).
 //
-// TMA issue costs about the same per instruction whatever the box size, so the
-// loads are spread over eleven producer warps: warps 5+2s and 6+2s own the two
-// 64-column boxes of pair slot s (every use of a slot is issued by the same two
-// warps, in order) and warp 15 loads kpe. Each producer also prefetches its
-// boxes of the tile after next into L2.
+// A 128-token tile of the whole latent is 144 KB; it has to stay in shared
+// memory from the score product until the PV product (after the softmax), and
+// the next tile has to be loading meanwhile, which does not fit in one SM. So
+// the two CTAs of a pair (cluster ranks 2k, 2k+1) take the same tokens and
+// split the latent columns: CTA `half` holds ckv columns [256 half, 256 half +
+// 256) and the kpe box, of whose 64 columns it uses [32 half, 32 half + 32).
+// Each computes a partial S^T over its columns, the two exchange them through
+// distributed shared memory and add them (both get the same sum, in the same
+// order), run the same softmax, and each accumulates O^T for its own 256
+// columns. A tile slot is then 80 KB (64 KB of ckv + 16 KB of kpe) and two
+// fit, so tile i+2 loads while tiles i and i+1 are computed. Pairs of a
+// cluster split the chunk's tiles; the cluster combines at the end, in rank
+// order.
 //
-// Warp roles (512 threads): warps 0-3 softmax / O rescale / epilogue, warp 4
-// TMEM owner + MMA issuer, warps 5-14 pair-slot producers, warp 15 kpe producer.
+// The ckv half of a tile arrives as one 4D TMA box per page (64 columns x 8
+// rows x 4 column blocks x page/8 row groups): it lands as row groups of four
+// swizzled [8 x 64] atoms, atom (g, c) at 4096 g + 1024 c. For the score MMAs
+// (K-major, column block c) the 8-row groups are then 4 KB apart (SBO), and
+// for the PV MMAs (MN-major, latent columns on M) the two 64-column blocks of
+// an M=128 block are 1 KB apart (LBO) and the 8-token groups 4 KB (SBO). One
+// TMA instruction per page and cache keeps the issue cost low.
+//
+// MMA order: S(0) S(1) PV(0) PV(1) S(2) S(3) PV(2) PV(3) ...: the softmax of
+// a tile overlaps the MMAs of the other tile of its pair of tiles, and the
+// load of tile i+2 (issued when PV(i) releases its slot) overlaps PV(i+1).
+//
+// Warp roles (288 threads): warps 0-3 softmax / O rescale / epilogue (thread
+// = token of the M=128 layout), warp 4 TMEM owner + MMA issuer, warps 5-8
+// producers (warp 5+k loads pages k, k+4, ... of each tile, both caches, and
+// prefetches the same pages of tile i+2 into L2).
 #include "device_common.cuh"
 
 namespace mla {
 
 namespace {
 
-constexpr int kT = 128;                    // tokens per tile
-constexpr int kNR = 16;                    // query rows per CTA
-constexpr int kSlots = 5;                  // pair slots
-constexpr int kBox128 = kT * 128;          // one 64-column box of 128 rows: 16 KB
-constexpr int kPairBytes = 2 * kBox128;    // 32 KB
-constexpr int kThreads = 16 * 32;
+constexpr int kT = 128;                          // tokens per tile
+constexpr int kNR = 16;                          // query rows per CTA
+constexpr int kHalfBoxes = 4;                    // ckv column blocks per CTA: 256 columns
+constexpr int kSlotBoxes = kHalfBoxes + 1;       // + the kpe box (Q^T chunks)
+constexpr int kHalfCols = kHalfBoxes * kBoxCols; // 256
+constexpr int kCkvBytes = kT * kHalfCols * 2;    // 64 KB: row group g, block c at 4096 g + 1024 c
+constexpr int kKpeBytes = kT * 128;              // 16 KB: [128 rows x 64 columns], swizzled
+constexpr int kTileSlot = kCkvBytes + kKpeBytes; // 80 KB
+constexpr int kGroupBytes = 8 * kHalfCols * 2;   // 4 KB: one 8-row group of the four blocks
+constexpr int kPageWarps = 4;                    // producer warps
+constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = (5 + kPageWarps) * 32;  // 288
 constexpr float kRescaleTau = 8.0f;
 
-constexpr uint32_t kOffPair = 0;
-constexpr uint32_t kOffKpe = kSlots * kPairBytes;               // 160 KB
-constexpr uint32_t kOffQ = kOffKpe + 2 * kBox128;               // 192 KB
-constexpr uint32_t kQChunk = kNR * 128;                         // 2 KB
-constexpr uint32_t kOffP = kOffQ + 9 * kQChunk;                 // 210 KB
-constexpr uint32_t kPBuf = 2 * kNR * 128;                       // P^T [16 x 128 tokens]: two 64-token atoms
-constexpr uint32_t kOffSmall = kOffP + 2 * kPBuf;               // 218 KB
-constexpr uint32_t kSmem = kOffSmall + 2048 + 1024;             // + alignment slack
-constexpr uint32_t kTmemCols = 128;                             // S^T 2x16 + O^T 4x16
+constexpr uint32_t kOffTile = 0;                            // 2 tile slots
+constexpr uint32_t kOffQ = 2 * kTileSlot;                   // 160 KB: Q^T, 5 chunks
+constexpr uint32_t kQChunk = kNR * 128;                     // [16 x 64] fp16, swizzled: 2 KB
+constexpr uint32_t kOffP = kOffQ + kSlotBoxes * kQChunk;    // 170 KB: P^T, 2 buffers
+constexpr uint32_t kPBuf = 2 * kNR * 128;                   // [16 x 128 tokens]: two 64-token atoms
+constexpr uint32_t kOffX = kOffP + 2 * kPBuf;               // 178 KB: the peer's partial S, 2 buffers
+constexpr uint32_t kXBuf = kNR * kT * 4;                    // [128 tokens][16 rows] fp32: 8 KB
+constexpr uint32_t kOffSmall = kOffX + 2 * kXBuf;           // 194 KB
+constexpr uint32_t kSmem = kOffSmall + 2048 + 1024;         // + alignment slack
+constexpr uint32_t kTmemCols = 64;                          // S^T 2 x 16 + O^T 2 x 16
 static_assert(kSmem <= 232448, "shared memory per CTA");
+static_assert(kNR * kHalfCols * 4 + 2 * kNR * 4 <= 2 * kTileSlot, "epilogue staging fits the tile slots");
 
 struct Small {
-  uint64_t pfull[kSlots], pempty[kSlots], kfull[2], kempty[2], sfull[2], sfree[2], ppfull[2], pvdone[2], drain;
+  uint64_t full[2], empty[2], sfull[2], sfree[2], ppfull[2], pvdone[2], xfull[2], xempty[2], drain;
   uint32_t tmem_base;
   int32_t abort_flag;
   float red[4][kNR];
@@ -67,39 +90,37 @@ static_assert(sizeof(Small) <= 2048, "small smem region");
 __device__ __forceinline__ uint32_t tmem_lane_base(int warp) { return static_cast<uint32_t>(32 * (warp & 3)) << 16; }
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
-// Pair j of tile i lives in slot (4i + j) % 5; it is that slot's use number (4i + j) / 5.
-__device__ __forceinline__ int slot_of(int i, int j) { return (4 * i + j) % kSlots; }
-__device__ __forceinline__ int use_of(int i, int j) { return (4 * i + j) / kSlots; }
-
 __global__ void __launch_bounds__(kThreads, 1)
-    mla_partial_tc128_kernel(const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
+    mla_partial_tc128_kernel(const __grid_constant__ CUtensorMap tm_pages, const __grid_constant__ CUtensorMap tm_kpe,
                              const PartialParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* qs = smem + kOffQ;
   uint8_t* ps = smem + kOffP;
+  float* xs = reinterpret_cast<float*>(smem + kOffX);
   Small* sm = reinterpret_cast<Small*>(smem + kOffSmall);
   volatile int32_t* abort_flag = &sm->abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const CtaWork w = cta_work(p, kNR, kT);
+  const uint32_t rank = cluster_ctarank(), nranks = cluster_nctarank(), peer = rank ^ 1u;
+  const int half = static_cast<int>(rank & 1u);
+  const CtaWork w = cta_work(p, kNR, kT, static_cast<int>(rank >> 1), static_cast<int>(nranks >> 1));
   const int ntiles = (w.sub1 - w.sub0 + kT - 1) / kT;
   const int rows_total = p.q_len * p.H;
 
   if (tid == 0) {
-    for (int s = 0; s < kSlots; ++s) {
-      mbar_init(&sm->pfull[s], 2);  // one arrival per box-half producer
-      mbar_init(&sm->pempty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm->kfull[b], 1);
-      mbar_init(&sm->kempty[b], 1);
-      mbar_init(&sm->sfull[b], 1);
-      mbar_init(&sm->sfree[b], 4);
-      mbar_init(&sm->ppfull[b], 4);
-      mbar_init(&sm->pvdone[b], 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm->full[t], kPageWarps);  // one expect_tx arrival per producer warp
+      mbar_init(&sm->empty[t], 1);
+      mbar_init(&sm->sfull[t], 1);
+      mbar_init(&sm->sfree[t], 4);
+      mbar_init(&sm->ppfull[t], 4);
+      mbar_init(&sm->pvdone[t], 1);
+      mbar_init(&sm->xfull[t], 1);   // local expect_tx arrival + the peer's st.async bytes
+      mbar_init(&sm->xempty[t], 4);  // one remote arrival per peer softmax warp
     }
     mbar_init(&sm->drain, 1);
+    for (int t = 0; t < 2; ++t) mbar_arrive_expect_tx(&sm->xfull[t], kXBuf);  // tiles 0 and 1
     sm->abort_flag = 0;
     fence_mbar_init();
   }
@@ -108,26 +129,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&sm->tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp < 4) {  // Q^T: 16 rows x 576, K-major, 9 swizzled [16 x 64] chunks
-    for (int idx = tid; idx < kNR * (kQkDim / 8); idx += 128) {
-      const int r = idx / (kQkDim / 8), k = (idx % (kQkDim / 8)) * 8;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (r < w.nrows) {
-        const long long row = static_cast<long long>(w.b) * rows_total + w.row0 + r;
-        v = (k < kRank) ? *reinterpret_cast<const uint4*>(p.q_abs + row * kRank + k)
-                        : *reinterpret_cast<const uint4*>(p.q_pe + row * kRope + (k - kRank));
-      }
-      *reinterpret_cast<uint4*>(qs + (k / kBoxCols) * kQChunk + sw128_offset(r, k % kBoxCols)) = v;
-    }
-    fence_proxy_async_smem();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_arrive_release();  // the peer touches this CTA's barriers only after this cluster phase
   const uint32_t tmem = sm->tmem_base;
 
   if (warp >= 5) {
     // ------------------------------------------------------------------ producers
+    const int k0 = warp - 5;  // this warp loads pages k0, k0 + 4, ... of each tile
     const uint64_t pol = l2_policy_evict_first();
     const int npages_req = (w.L + p.bs - 1) / p.bs;
     int win_base = -1, win_pid = -1;
@@ -145,83 +155,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       *pg0 = tok0 / p.bs;
       *npg = (min(kT, w.sub1 - tok0) + p.bs - 1) / p.bs;
     };
-    const bool kpe_warp = (warp == 15);
-    const int s = (warp - 5) >> 1;  // pair slot owned by this warp
-    const int half = (warp - 5) & 1;  // which 64-column box of the pair
-    int issued_q = -1;       // last (tile, pair) index this warp loaded
+    int issued = -1;
     for (int i = 0; i < ntiles; ++i) {
+      const int t = i & 1;
+      if (i >= 2) {  // tile i-2 released the slot
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait(&sm->empty[t], ((i >> 1) - 1) & 1, p.timeout_ns) && !*abort_flag;
+          if (!ok) *abort_flag = 1;
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
       int pg0, npg;
       tile_pages(i, &pg0, &npg);
-      int j = -1;
-      if (kpe_warp) {
-        j = 8;  // kpe box
-      } else {
-        const int jj = ((s - 4 * i) % kSlots + kSlots) % kSlots;
-        if (jj < 4) j = jj;
-      }
-      if (j < 0) continue;  // this slot is not used by tile i
-      // wait until the previous use of the destination is released
-      int ok = 1;
-      if (lane == 0) {
-        if (kpe_warp) {
-          if (i >= 2) ok = mbar_wait(&sm->kempty[i & 1], ((i >> 1) - 1) & 1, p.timeout_ns);
-        } else {
-          const int u = use_of(i, j);
-          if (u >= 1) ok = mbar_wait(&sm->pempty[s], (u - 1) & 1, p.timeout_ns);
-        }
-        ok = ok && !*abort_flag;
-        if (!ok) *abort_flag = 1;
-      }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      int pids[kT / 16];
+      const int mine = (npg > k0) ? (npg - k0 + kPageWarps - 1) / kPageWarps : 0;
+      int pids[kT / 16 / kPageWarps];
 #pragma unroll
-      for (int k = 0; k < kT / 16; ++k) pids[k] = (k < npg) ? page_of(pg0 + k) : -1;
+      for (int m = 0; m < kT / 16 / kPageWarps; ++m) pids[m] = (m < mine) ? page_of(pg0 + k0 + m * kPageWarps) : -1;
       if (lane == 0) {
-        if (kpe_warp) {
-          uint8_t* dst = smem + kOffKpe + (i & 1) * kBox128;
-          mbar_arrive_expect_tx(&sm->kfull[i & 1], static_cast<uint32_t>(npg * p.bs * 128));
-          for (int k = 0; k < npg; ++k) tma_load_2d(dst + k * p.bs * 128, &tm_kpe, 0, pids[k] * p.bs, &sm->kfull[i & 1], pol);
-        } else {
-          uint8_t* dst = smem + kOffPair + s * kPairBytes + half * kBox128;
-          mbar_arrive_expect_tx(&sm->pfull[s], static_cast<uint32_t>(npg * p.bs * 128));
-          for (int k = 0; k < npg; ++k)
-            tma_load_2d(dst + k * p.bs * 128, &tm_ckv, (2 * j + half) * kBoxCols, pids[k] * p.bs, &sm->pfull[s], pol);
+        uint8_t* slot = smem + kOffTile + t * kTileSlot;
+        mbar_arrive_expect_tx(&sm->full[t], static_cast<uint32_t>(mine * p.bs * (kHalfCols * 2 + 128)));
+        for (int m = 0; m < mine; ++m) {
+          const int j = k0 + m * kPageWarps;  // page of the tile
+          tma_load_4d(slot + j * p.bs * (kHalfCols * 2), &tm_pages, 0, 0, kHalfBoxes * half, pids[m] * (p.bs / 8),
+                      &sm->full[t], pol);
+          tma_load_2d(slot + kCkvBytes + j * p.bs * 128, &tm_kpe, 0, pids[m] * p.bs, &sm->full[t], pol);
         }
       }
-      issued_q = i;
-      // the same boxes of the tile after next, into L2
-      if (i + 2 < ntiles) {
+      issued = i;
+      if (i + 2 < ntiles) {  // the same pages of tile i+2 into L2: ckv by the even CTA, kpe by the odd one
         int qg0, qn;
         tile_pages(i + 2, &qg0, &qn);
-        for (int k = 0; k < qn; ++k) {
-          const int pid = page_of(qg0 + k);
+        for (int j = k0; j < qn; j += kPageWarps) {
+          const int pid = page_of(qg0 + j);
           if (lane == 0 && pid >= 0) {
-            if (kpe_warp) {
-              tma_prefetch_l2_2d(&tm_kpe, 0, pid * p.bs);
-            } else {
-              tma_prefetch_l2_2d(&tm_ckv, (2 * j + half) * kBoxCols, pid * p.bs);
-            }
+            const long long row = static_cast<long long>(pid) * p.bs;
+            if (half == 0)
+              bulk_prefetch_l2(p.ckv + row * (kRank * 2), static_cast<uint32_t>(p.bs * kRank * 2));
+            else
+              bulk_prefetch_l2(p.kpe + row * (kRope * 2), static_cast<uint32_t>(p.bs * kRope * 2));
           }
         }
       }
     }
-    // after an abort, let this warp's last load land before shared memory is released
-    if (lane == 0 && *abort_flag && issued_q >= 0) {
-      if (kpe_warp) {
-        mbar_wait(&sm->kfull[issued_q & 1], (issued_q >> 1) & 1, kDrainTimeoutNs);
-      } else {
-        const int jj = ((s - 4 * issued_q) % kSlots + kSlots) % kSlots;
-        mbar_wait(&sm->pfull[s], use_of(issued_q, jj) & 1, kDrainTimeoutNs);
-      }
-    }
+    // after an abort, let this warp's last loads land before shared memory is released
+    if (lane == 0 && *abort_flag && issued >= 0) mbar_wait(&sm->full[issued & 1], (issued >> 1) & 1, kDrainTimeoutNs);
+    cluster_wait_acquire();
   } else if (warp == 4) {
     // ------------------------------------------------------------------ MMA issuer
     const uint32_t idesc_s = idesc_f16_f32(128, kNR, false, false, false);
     const uint32_t idesc_o = idesc_f16_f32(128, kNR, false, true, false);
     const uint64_t q_desc = smem_desc_sw128(smem_u32(qs), 16, 1024);
     const uint64_t p_desc = smem_desc_sw128(smem_u32(ps), 16, 1024);
-    const uint32_t pair_base = smem_u32(smem + kOffPair), kpe_base = smem_u32(smem + kOffKpe);
-    bool alive = true;
+    const uint32_t tile_base = smem_u32(smem + kOffTile);
     auto wait_lane0 = [&](uint64_t* bar, uint32_t parity) -> bool {
       int ok = 1;
       if (lane == 0) {
@@ -230,102 +216,112 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
-    // rows >= nvalid of a 128-row box: zero them so the A operand stays finite
-    auto zero_tail = [&](uint8_t* box, int nvalid) {
-      for (int x = lane; x < (kT - nvalid) * 8; x += 32)
-        *reinterpret_cast<uint4*>(box + nvalid * 128 + x * 16) = make_uint4(0u, 0u, 0u, 0u);
-    };
-    // score MMAs over box c (c < 8: ckv column block c, c = 8: kpe) of tile i
-    auto score_box = [&](int i, int c, bool first) {
-      const uint32_t a = (c < 8) ? pair_base + slot_of(i, c >> 1) * kPairBytes + (c & 1) * kBox128
-                                 : kpe_base + (i & 1) * kBox128;
-      const uint64_t ad = smem_desc_sw128(a, 16, 1024);
+    // score product of tile i into S buffer i&1: this CTA's 4 ckv column blocks, then its half of kpe
+    auto score = [&](int i) -> bool {
+      const int t = i & 1;
+      if (i >= 2 && !wait_lane0(&sm->sfree[t], ((i >> 1) - 1) & 1)) return false;
+      if (!wait_lane0(&sm->full[t], (i >> 1) & 1)) return false;
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t slot = tile_base + t * kTileSlot;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        umma_f16_ss(tmem + (i & 1) * kNR, desc_add(ad, kk * 32), desc_add(q_desc, c * kQChunk + kk * 32), idesc_s,
-                    (first && kk == 0) ? 0u : 1u);
+        for (int c = 0; c < kHalfBoxes; ++c) {
+          const uint64_t ad = smem_desc_sw128(slot + c * 1024, 16, kGroupBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_f16_ss(tmem + t * kNR, desc_add(ad, kk * 32), desc_add(q_desc, c * kQChunk + kk * 32), idesc_s,
+                        (c == 0 && kk == 0) ? 0u : 1u);
+        }
+        const uint64_t ak = smem_desc_sw128(slot + kCkvBytes, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const uint32_t ks = 2 * half + kk;  // 16-column step of the kpe box
+          umma_f16_ss(tmem + t * kNR, desc_add(ak, ks * 32), desc_add(q_desc, kHalfBoxes * kQChunk + ks * 32), idesc_s,
+                      1u);
+        }
+        umma_commit(&sm->sfull[t]);
+      }
+      __syncwarp();
+      return true;
     };
-    auto pair_ready = [&](int i, int j, int nvalid) -> bool {
-      if (!wait_lane0(&sm->pfull[slot_of(i, j)], use_of(i, j) & 1)) return false;
-      if (nvalid < kT) {
-        uint8_t* pr = smem + kOffPair + slot_of(i, j) * kPairBytes;
-        zero_tail(pr, nvalid);
-        zero_tail(pr + kBox128, nvalid);
+    // rows >= nvalid of the ckv part of a slot: zero them so the PV operand stays finite
+    auto zero_tail = [&](uint8_t* ckv, int nvalid) {
+      for (int x = lane; x < (kT - nvalid) * kHalfBoxes * 8; x += 32) {
+        const int rc = x >> 3, tok = nvalid + rc / kHalfBoxes, c = rc % kHalfBoxes;
+        *reinterpret_cast<uint4*>(ckv + (tok >> 3) * kGroupBytes + c * 1024 + (tok & 7) * 128 + (x & 7) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    // PV product of tile i: O^T rows [128 blk, 128 blk + 128) of this CTA's columns = boxes 2 blk, 2 blk + 1
+    auto pv = [&](int i) -> bool {
+      const int t = i & 1;
+      const int nvalid = min(kT, w.sub1 - (w.sub0 + i * kT));
+      if (!wait_lane0(&sm->ppfull[t], (i >> 1) & 1)) return false;
+      if (nvalid < kT) {  // the score product of tile i is complete (its softmax ran)
+        zero_tail(smem + kOffTile + t * kTileSlot, nvalid);
         fence_proxy_async_smem();
         __syncwarp();
       }
+      if (lane == 0) {
+        tc_fence_after();
+        const uint64_t pb = desc_add(p_desc, t * kPBuf);
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          const uint64_t a0 = smem_desc_sw128(tile_base + t * kTileSlot + 2 * blk * 1024, 1024, kGroupBytes);
+#pragma unroll
+          for (int ks = 0; ks < kT / 16; ++ks)
+            umma_f16_ss(tmem + 2 * kNR + blk * kNR, desc_add(a0, ks * 2 * kGroupBytes),
+                        desc_add(pb, (ks >> 2) * (kNR * 128) + (ks & 3) * 32), idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
+        }
+        umma_commit(&sm->empty[t]);
+        umma_commit(&sm->pvdone[t]);
+      }
+      __syncwarp();
       return true;
     };
-    for (int i = 0; i <= ntiles && alive; ++i) {
-      const int nvalid = (i < ntiles) ? min(kT, w.sub1 - (w.sub0 + i * kT)) : 0;
-      if (i < ntiles) {  // head of the score product: kpe, pair 0
-        if (!wait_lane0(&sm->kfull[i & 1], (i >> 1) & 1)) break;
-        if (nvalid < kT) {
-          zero_tail(smem + kOffKpe + (i & 1) * kBox128, nvalid);
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        if (i >= 2 && !wait_lane0(&sm->sfree[i & 1], ((i >> 1) - 1) & 1)) break;
-        if (!pair_ready(i, 0, nvalid)) break;
-        if (lane == 0) {
-          tc_fence_after();
-          score_box(i, 8, true);
-          score_box(i, 0, false);
-          score_box(i, 1, false);
-        }
-        __syncwarp();
-      }
-      if (i >= 1) {  // PV of the previous tile, releasing its pair slots block by block
-        const int j = i - 1;
-        if (!wait_lane0(&sm->ppfull[j & 1], (j >> 1) & 1)) break;
-        if (lane == 0) {
-          tc_fence_after();
-          const uint64_t pb = desc_add(p_desc, (j & 1) * kPBuf);
-#pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
-            const uint64_t a0 = smem_desc_sw128(pair_base + slot_of(j, blk) * kPairBytes, kBox128, 1024);
-#pragma unroll
-            for (int ks = 0; ks < kT / 16; ++ks)
-              umma_f16_ss(tmem + 2 * kNR + blk * kNR, desc_add(a0, ks * 16 * 128),
-                          desc_add(pb, (ks >> 2) * (kNR * 128) + (ks & 3) * 32), idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
-            umma_commit(&sm->pempty[slot_of(j, blk)]);
-          }
-          umma_commit(&sm->pvdone[j & 1]);
-        }
-        __syncwarp();
-      }
-      if (i < ntiles) {  // tail of the score product: pairs 1..3
-        bool ok = true;
-        for (int jp = 1; jp < 4 && ok; ++jp) {
-          ok = pair_ready(i, jp, nvalid);
-          if (ok && lane == 0) {
-            tc_fence_after();
-            score_box(i, 2 * jp, false);
-            score_box(i, 2 * jp + 1, false);
-          }
-          __syncwarp();
-        }
-        if (!ok) break;
-        if (lane == 0) {
-          umma_commit(&sm->sfull[i & 1]);
-          umma_commit(&sm->kempty[i & 1]);
-        }
-        __syncwarp();
-      }
+    named_bar_sync(2, 160);  // Q^T staged by the softmax warps
+    bool alive = true;
+    for (int i0 = 0; i0 < ntiles && alive; i0 += 2) {
+      const int i1 = min(i0 + 2, ntiles);
+      for (int i = i0; i < i1 && alive; ++i) alive = score(i);
+      for (int i = i0; i < i1 && alive; ++i) alive = pv(i);
     }
     if (lane == 0) {  // every MMA issued so far has completed before TMEM is read or freed
       umma_commit(&sm->drain);
       mbar_wait(&sm->drain, 0, kDrainTimeoutNs);
     }
     __syncwarp();
+    cluster_wait_acquire();
   } else {
     // ------------------------------------------------------------------ softmax (warps 0-3)
+    // Q^T: this CTA's 256 latent columns, then the 64 kpe columns; 16 rows, K-major, 5 swizzled chunks
+    for (int idx = tid; idx < kNR * kSlotBoxes * 8; idx += kSoftmaxThreads) {
+      const int r = idx / (kSlotBoxes * 8), k = (idx % (kSlotBoxes * 8)) * 8;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (r < w.nrows) {
+        const long long row = static_cast<long long>(w.b) * rows_total + w.row0 + r;
+        v = (k < kHalfCols) ? *reinterpret_cast<const uint4*>(p.q_abs + row * kRank + kHalfCols * half + k)
+                            : *reinterpret_cast<const uint4*>(p.q_pe + row * kRope + (k - kHalfCols));
+      }
+      *reinterpret_cast<uint4*>(qs + (k / kBoxCols) * kQChunk + sw128_offset(r, k % kBoxCols)) = v;
+    }
+    fence_proxy_async_smem();
+    named_bar_arrive(2, 160);
+    cluster_wait_acquire();  // the peer's barriers are initialised
+
     // Thread (warp, lane) owns token 32*warp + lane of each tile (M=128 layout of S^T).
     float lsum[kNR];
 #pragma unroll
     for (int r = 0; r < kNR; ++r) lsum[r] = 0.f;
     const int tl = 32 * warp + lane;
     const int causal_floor = p.causal ? w.L - p.q_len + w.row0 / p.H : 0x7fffffff;
+    const uint32_t peer_x = dsmem_addr(xs, peer);
+    // the peer's partial S: thread tl's 16 values are 4 float4 chunks of row tl, chunk c at
+    // position c ^ ((tl >> 1) & 3) (conflict-free 16-byte accesses for the reader)
+    const uint32_t xsw = static_cast<uint32_t>((tl >> 1) & 3);
+    float mr[kNR];  // reference max of each row (the same in every softmax thread)
+#pragma unroll
+    for (int r = 0; r < kNR; ++r) mr[r] = -INFINITY;
     for (int i = 0; i < ntiles; ++i) {
       const int buf = i & 1;
       const int tok0 = w.sub0 + i * kT;
@@ -335,14 +331,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&sm->sfull[buf], (i >> 1) & 1, p.timeout_ns);
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      bool need_local = false;
       if (ok) {
         tc_fence_after();
         tmem_ld16(tmem + tmem_lane_base(warp) + buf * kNR, x);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->sfree[buf]);
+        if (lane == 0) {
+          mbar_arrive(&sm->sfree[buf]);
+          if (i >= 1) {
+            // tile i-1's buffer was read in the previous iteration (the values are consumed and the
+            // softmax warps have passed named barriers since): expect the peer's tile i+1 in it, then
+            // free it with a plain signal (a release arrive here costs a cluster round trip)
+            if (tid == 0) mbar_arrive_expect_tx(&sm->xfull[buf ^ 1], kXBuf);
+            mbar_remote_arrive_relaxed(dsmem_addr(&sm->xempty[buf ^ 1], peer));
+          }
+        }
+        // this CTA's partial scores to the peer (once it has read the previous use of the buffer)
+        if (i >= 2) ok = mbar_wait_cluster(&sm->xempty[buf], ((i >> 1) - 1) & 1, p.timeout_ns);
+      }
+      ok = __all_sync(0xffffffffu, ok);  // per-thread waits: one decision per warp
+      if (ok) {
+        const uint32_t dst = peer_x + buf * kXBuf + tl * 64;
+        const uint32_t rbar = dsmem_addr(&sm->xfull[buf], peer);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          dsmem_st_async_f32x4(dst + ((c ^ xsw) << 4), make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]),
+                               rbar);
+        ok = mbar_wait_cluster(&sm->xfull[buf], (i >> 1) & 1, p.timeout_ns);
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      bool need_local = false;
+      if (ok) {
+        const float4* xb = reinterpret_cast<const float4*>(xs + buf * (kXBuf / 4) + tl * 16);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float4 y = xb[c ^ xsw];
+          // rank-0 part + rank-1 part, the same sum in both CTAs
+          x[4 * c] = half ? (y.x + x[4 * c]) : (x[4 * c] + y.x);
+          x[4 * c + 1] = half ? (y.y + x[4 * c + 1]) : (x[4 * c + 1] + y.y);
+          x[4 * c + 2] = half ? (y.z + x[4 * c + 2]) : (x[4 * c + 2] + y.z);
+          x[4 * c + 3] = half ? (y.w + x[4 * c + 3]) : (x[4 * c + 3] + y.w);
+        }
         const int t = tok0 + tl;
 #pragma unroll
         for (int r = 0; r < kNR; ++r) {
@@ -352,14 +382,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.causal) vis = vis && (t <= w.L - p.q_len + (w.row0 + r) / p.H);
           }
           x[r] = vis ? x[r] * p.scale_log2 : -INFINITY;
-          need_local |= x[r] > sm->mref[r] + kRescaleTau;
+          need_local |= x[r] > mr[r] + kRescaleTau;
         }
       } else {
 #pragma unroll
         for (int r = 0; r < kNR; ++r) x[r] = -INFINITY;
-        if (lane == 0) *abort_flag = 1;
+        *abort_flag = 1;
       }
-      if (named_bar_sync_or(1, 128, need_local || *abort_flag != 0)) {
+      if (named_bar_sync_or(1, 128, need_local || !ok || *abort_flag != 0)) {
         if (named_bar_sync_or(1, 128, *abort_flag != 0)) break;
         // rare path: move the reference max, rescale O^T and the row sums
 #pragma unroll
@@ -381,13 +411,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           sm->mref[tid] = mnew;
         }
         named_bar_sync(1, 128);
+#pragma unroll
+        for (int r = 0; r < kNR; ++r) mr[r] = sm->mref[r];
         if (i >= 1) {  // PV(i-1) must be complete before O^T is rescaled
           int ok2 = 1;
           if (lane == 0) ok2 = mbar_wait(&sm->pvdone[(i - 1) & 1], ((i - 1) >> 1) & 1, p.timeout_ns);
           if (__shfl_sync(0xffffffffu, ok2, 0)) {
             tc_fence_after();
 #pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
+            for (int blk = 0; blk < 2; ++blk) {
               float v[16];
               const uint32_t a = tmem + tmem_lane_base(warp) + 2 * kNR + blk * kNR;
               tmem_ld16(a, v);
@@ -413,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* pb = ps + buf * kPBuf + (tl >> 6) * (kNR * 128);
 #pragma unroll
         for (int r = 0; r < kNR; ++r) {
-          const float pr = (x[r] == -INFINITY) ? 0.f : exp2f(x[r] - sm->mref[r]);
+          const float pr = (x[r] == -INFINITY) ? 0.f : exp2f(x[r] - mr[r]);
           const uint16_t hv = f2h<false>(pr);
           lsum[r] += h2f<false>(hv);
           *reinterpret_cast<uint16_t*>(pb + sw128_offset(r, tl & 63)) = hv;
@@ -442,25 +474,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     named_bar_sync(1, 128);
   }
-  __syncthreads();  // all roles done: the pair slots are free for staging
+  __syncthreads();  // all roles done: the tile slots are free for staging
   const bool have = (ntiles > 0) && !*abort_flag;
-  float* ostage = reinterpret_cast<float*>(smem + kOffPair);  // [16][512]
-  float* mst = ostage + kNR * kRank;
+  float* ostage = reinterpret_cast<float*>(smem + kOffTile);  // [16][256]: this CTA's columns
+  float* mst = ostage + kNR * kHalfCols;
   float* lst = mst + kNR;
   if (warp < 4) {
     if (have) {
       tc_fence_after();
 #pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
+      for (int blk = 0; blk < 2; ++blk) {
         float v[16];
         tmem_ld16(tmem + tmem_lane_base(warp) + 2 * kNR + blk * kNR, v);
         tmem_wait_ld();
         const int d = blk * 128 + warp * 32 + lane;
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) ostage[jj * kRank + d] = v[jj];
+        for (int jj = 0; jj < 16; ++jj) ostage[jj * kHalfCols + d] = v[jj];
       }
     } else {
-      for (int idx = tid; idx < kNR * kRank; idx += 128) ostage[idx] = 0.f;
+      for (int idx = tid; idx < kNR * kHalfCols; idx += kSoftmaxThreads) ostage[idx] = 0.f;
     }
     if (tid < kNR) {
       mst[tid] = have ? sm->mref[tid] : -INFINITY;
@@ -470,7 +502,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();
-  cluster_combine(p, w, ostage, mst, lst, tid, kThreads);
+  {
+    // Combine the pairs of the cluster in rank order: this CTA writes output
+    // columns [rank * 512 / n, (rank + 1) * 512 / n), held by the CTAs of
+    // half h = those columns / 256; rank 0 also writes the LSE.
+    const int npairs = static_cast<int>(nranks >> 1);
+    const int dcols = kRank / static_cast<int>(nranks);
+    const int dbeg = static_cast<int>(rank) * dcols;
+    const uint32_t h = static_cast<uint32_t>(dbeg / kHalfCols);
+    const int n4 = dcols / 4;
+    const int items = w.nrows * n4 + ((rank == 0) ? w.nrows : 0);
+    for (int idx = tid; idx < items; idx += kThreads) {
+      const bool is_lse = idx >= w.nrows * n4;
+      const int r = is_lse ? idx - w.nrows * n4 : idx / n4;
+      const int d = is_lse ? 0 : dbeg + (idx % n4) * 4;
+      float mj[8], wj[8];
+      float M = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        mj[j] = (j < npairs) ? dsmem_ld_f32(dsmem_addr(mst + r, 2 * j + h)) : -INFINITY;
+        M = fmaxf(M, mj[j]);
+      }
+      float den = 0.f;
+      float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) wj[j] = (mj[j] == -INFINITY) ? 0.f : exp2f(mj[j] - M);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j < npairs) {
+            den = fmaf(wj[j], dsmem_ld_f32(dsmem_addr(lst + r, 2 * j + h)), den);
+            if (!is_lse) {
+              const float4 v = dsmem_ld_f32x4(dsmem_addr(ostage + r * kHalfCols + (d - kHalfCols * h), 2 * j + h));
+              num.x = fmaf(wj[j], v.x, num.x);
+              num.y = fmaf(wj[j], v.y, num.y);
+              num.z = fmaf(wj[j], v.z, num.z);
+              num.w = fmaf(wj[j], v.w, num.w);
+            }
+          }
+        }
+      }
+      if (is_lse) {
+        p.lse[static_cast<long long>(w.slot) * rows_total + w.row0 + r] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
+      } else {
+        float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) out = make_float4(num.x / den, num.y / den, num.z / den, num.w / den);
+        const long long base = (static_cast<long long>(w.slot) * rows_total + w.row0 + r) * kRank + d;
+        *reinterpret_cast<float4*>(p.partials + base) = out;
+      }
+    }
+  }
   cluster_sync();
   if (warp == 4) {
     tc_fence_after();
@@ -497,9 +578,11 @@ cudaError_t prepare(int cluster) {
 
 }  // namespace
 
-bool tc128_supports(int total_rows, bool bf16) { return total_rows <= kNR && !bf16; }
+bool tc128_supports(int total_rows, bool bf16, int cluster) {
+  return total_rows <= kNR && !bf16 && cluster >= 2 && cluster <= 16 && (cluster & (cluster - 1)) == 0;
+}
 
-cudaError_t launch_partial_tc128(const CUtensorMap& tm_ckv, const CUtensorMap& tm_kpe, const PartialParams& p,
+cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe, const PartialParams& p,
                                  int num_chunks, int cluster, cudaStream_t stream) {
   cudaError_t e = prepare(cluster);
   if (e != cudaSuccess) return e;
@@ -515,7 +598,7 @@ cudaError_t launch_partial_tc128(const CUtensorMap& tm_ckv, const CUtensorMap& t
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_partial_tc128_kernel, tm_ckv, tm_kpe, p);
+  return cudaLaunchKernelEx(&cfg, mla_partial_tc128_kernel, tm_pages, tm_kpe, p);
 }
 
 int tc128_max_active_clusters(int cluster) {
