@@ -68,7 +68,7 @@ constexpr uint64_t kDrainTimeoutNs = 2000000000ull;
 // Wait for the phase with the given parity to complete. Gives up after
 // `timeout_ns` of wall time, flags MLA_DEVERR_TIMEOUT and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (__builtin_expect(mbar_try_wait(bar, parity), 1)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -227,7 +227,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
         : "memory");
     return ok != 0;
   };
-  if (test()) return true;
+  if (__builtin_expect(test(), 1)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (test()) return true;

@@ -208,10 +208,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t q_desc = smem_desc_sw128(smem_u32(qs), 16, 1024);
     const uint64_t p_desc = smem_desc_sw128(smem_u32(ps), 16, 1024);
     const uint32_t tile_base = smem_u32(smem + kOffTile);
+    uint64_t tmo = p.timeout_ns;
+    asm volatile("" : "+l"(tmo));
     auto wait_lane0 = [&](uint64_t* bar, uint32_t parity) -> bool {
       int ok = 1;
       if (lane == 0) {
-        ok = mbar_wait(bar, parity, p.timeout_ns) && !*abort_flag;
+        ok = mbar_wait(bar, parity, tmo) && !*abort_flag;
         if (!ok) *abort_flag = 1;
       }
       return __shfl_sync(0xffffffffu, ok, 0) != 0;
@@ -244,9 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
-    // rows >= nvalid of the ckv part of a slot: zero them so the PV operand stays finite
-    auto zero_tail = [&](uint8_t* ckv, int nvalid) {
-      for (int x = lane; x < (kT - nvalid) * kHalfBoxes * 8; x += 32) {
+    // rows [nvalid, nend) of the ckv part of a slot: zero them so the PV operand stays finite
+    // (the probabilities there are 0, but stale or unwritten rows may hold non-finite values)
+    auto zero_rows = [&](uint8_t* ckv, int nvalid, int nend) {
+      for (int x = lane; x < (nend - nvalid) * kHalfBoxes * 8; x += 32) {
         const int rc = x >> 3, tok = nvalid + rc / kHalfBoxes, c = rc % kHalfBoxes;
         *reinterpret_cast<uint4*>(ckv + (tok >> 3) * kGroupBytes + c * 1024 + (tok & 7) * 128 + (x & 7) * 16) =
             make_uint4(0u, 0u, 0u, 0u);
@@ -257,8 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = i & 1;
       const int nvalid = min(kT, w.sub1 - (w.sub0 + i * kT));
       if (!wait_lane0(&sm->ppfull[t], (i >> 1) & 1)) return false;
-      if (nvalid < kT) {  // the score product of tile i is complete (its softmax ran)
-        zero_tail(smem + kOffTile + t * kTileSlot, nvalid);
+      // K steps of 16 tokens that hold valid tokens; in a partial tile only the rows up to the
+      // next multiple of 16 are read, and those past the end are zeroed (the score product of
+      // tile i is complete: its softmax ran)
+      const int ksteps = (nvalid + 15) >> 4;
+      if (nvalid < (ksteps << 4)) {
+        zero_rows(smem + kOffTile + t * kTileSlot, nvalid, ksteps << 4);
         fence_proxy_async_smem();
         __syncwarp();
       }
@@ -268,8 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int blk = 0; blk < 2; ++blk) {
           const uint64_t a0 = smem_desc_sw128(tile_base + t * kTileSlot + 2 * blk * 1024, 1024, kGroupBytes);
-#pragma unroll
-          for (int ks = 0; ks < kT / 16; ++ks)
+          for (int ks = 0; ks < ksteps; ++ks)
             umma_f16_ss(tmem + 2 * kNR + blk * kNR, desc_add(a0, ks * 2 * kGroupBytes),
                         desc_add(pb, (ks >> 2) * (kNR * 128) + (ks & 3) * 32), idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
         }
@@ -294,6 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_wait_acquire();
   } else {
     // ------------------------------------------------------------------ softmax (warps 0-3)
+    // kernel parameters used every tile, held in registers (not re-read from the parameter bank)
+    float scale_log2 = p.scale_log2;
+    uint64_t tmo = p.timeout_ns;
+    asm volatile("" : "+f"(scale_log2), "+l"(tmo));
     // Q^T: this CTA's 256 latent columns, then the 64 kpe columns; 16 rows, K-major, 5 swizzled chunks
     for (int idx = tid; idx < kNR * kSlotBoxes * 8; idx += kSoftmaxThreads) {
       const int r = idx / (kSlotBoxes * 8), k = (idx % (kSlotBoxes * 8)) * 8;
@@ -329,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool masked_tile = (nvalid < kT) || (tok0 + kT - 1 > causal_floor) || (w.nrows < kNR);
       float x[kNR];
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&sm->sfull[buf], (i >> 1) & 1, p.timeout_ns);
+      if (lane == 0) ok = mbar_wait(&sm->sfull[buf], (i >> 1) & 1, tmo);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (ok) {
         tc_fence_after();
@@ -348,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // this CTA's partial scores to the peer (once it has read the previous use of the buffer)
-        if (i >= 2) ok = mbar_wait_cluster(&sm->xempty[buf], ((i >> 1) - 1) & 1, p.timeout_ns);
+        if (i >= 2) ok = mbar_wait_cluster(&sm->xempty[buf], ((i >> 1) - 1) & 1, tmo);
       }
       ok = __all_sync(0xffffffffu, ok);  // per-thread waits: one decision per warp
       if (ok) {
@@ -358,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c)
           dsmem_st_async_f32x4(dst + ((c ^ xsw) << 4), make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]),
                                rbar);
-        ok = mbar_wait_cluster(&sm->xfull[buf], (i >> 1) & 1, p.timeout_ns);
+        ok = mbar_wait_cluster(&sm->xfull[buf], (i >> 1) & 1, tmo);
       }
       ok = __all_sync(0xffffffffu, ok);
       bool need_local = false;
@@ -373,23 +383,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           x[4 * c + 2] = half ? (y.z + x[4 * c + 2]) : (x[4 * c + 2] + y.z);
           x[4 * c + 3] = half ? (y.w + x[4 * c + 3]) : (x[4 * c + 3] + y.w);
         }
-        const int t = tok0 + tl;
+        if (__builtin_expect(masked_tile, 0)) {  // tail of the chunk, causal edge, or fewer than 16 rows
+          const int t = tok0 + tl;
 #pragma unroll
-        for (int r = 0; r < kNR; ++r) {
-          bool vis = true;
-          if (masked_tile) {
-            vis = (tl < nvalid) && (r < w.nrows);
+          for (int r = 0; r < kNR; ++r) {
+            bool vis = (tl < nvalid) && (r < w.nrows);
             if (p.causal) vis = vis && (t <= w.L - p.q_len + (w.row0 + r) / p.H);
+            x[r] = vis ? x[r] * scale_log2 : -INFINITY;
           }
-          x[r] = vis ? x[r] * p.scale_log2 : -INFINITY;
-          need_local |= x[r] > mr[r] + kRescaleTau;
+        } else {
+#pragma unroll
+          for (int r = 0; r < kNR; ++r) x[r] *= scale_log2;
         }
+#pragma unroll
+        for (int r = 0; r < kNR; ++r) need_local |= x[r] > mr[r] + kRescaleTau;
       } else {
 #pragma unroll
         for (int r = 0; r < kNR; ++r) x[r] = -INFINITY;
         *abort_flag = 1;
       }
-      if (named_bar_sync_or(1, 128, need_local || !ok || *abort_flag != 0)) {
+      if (__builtin_expect(named_bar_sync_or(1, 128, need_local || !ok || *abort_flag != 0), 0)) {
         if (named_bar_sync_or(1, 128, *abort_flag != 0)) break;
         // rare path: move the reference max, rescale O^T and the row sums
 #pragma unroll
@@ -415,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < kNR; ++r) mr[r] = sm->mref[r];
         if (i >= 1) {  // PV(i-1) must be complete before O^T is rescaled
           int ok2 = 1;
-          if (lane == 0) ok2 = mbar_wait(&sm->pvdone[(i - 1) & 1], ((i - 1) >> 1) & 1, p.timeout_ns);
+          if (lane == 0) ok2 = mbar_wait(&sm->pvdone[(i - 1) & 1], ((i - 1) >> 1) & 1, tmo);
           if (__shfl_sync(0xffffffffu, ok2, 0)) {
             tc_fence_after();
 #pragma unroll
@@ -438,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (i >= 2) {  // P^T buffer `buf` was last read by PV(i-2)
         int ok3 = 1;
-        if (lane == 0) ok3 = mbar_wait(&sm->pvdone[buf], ((i >> 1) - 1) & 1, p.timeout_ns);
+        if (lane == 0) ok3 = mbar_wait(&sm->pvdone[buf], ((i >> 1) - 1) & 1, tmo);
         if (!__shfl_sync(0xffffffffu, ok3, 0) && lane == 0) *abort_flag = 1;
       }
       {  // probabilities -> P^T (fp16, K-major, two swizzled 64-token atoms) and row sums
@@ -459,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool aborted = named_bar_sync_or(1, 128, *abort_flag != 0);
     if (ntiles > 0 && !aborted) {
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&sm->pvdone[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, p.timeout_ns);
+      if (lane == 0) ok = mbar_wait(&sm->pvdone[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, tmo);
       if (!__shfl_sync(0xffffffffu, ok, 0) && lane == 0) *abort_flag = 1;
     }
 #pragma unroll
@@ -516,30 +529,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool is_lse = idx >= w.nrows * n4;
       const int r = is_lse ? idx - w.nrows * n4 : idx / n4;
       const int d = is_lse ? 0 : dbeg + (idx % n4) * 4;
-      float mj[8], wj[8];
-      float M = -INFINITY;
+      // every load of this item at once (one round trip), then the fixed-order reduction
+      float mj[8], lj[8];
+      float4 vj[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        mj[j] = (j < npairs) ? dsmem_ld_f32(dsmem_addr(mst + r, 2 * j + h)) : -INFINITY;
-        M = fmaxf(M, mj[j]);
+        mj[j] = -INFINITY;
+        lj[j] = 0.f;
+        vj[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < npairs) {
+          const uint32_t src = 2 * j + h;
+          mj[j] = dsmem_ld_f32(dsmem_addr(mst + r, src));
+          lj[j] = dsmem_ld_f32(dsmem_addr(lst + r, src));
+          if (!is_lse) vj[j] = dsmem_ld_f32x4(dsmem_addr(ostage + r * kHalfCols + (d - kHalfCols * h), src));
+        }
       }
+      float M = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) M = fmaxf(M, mj[j]);
       float den = 0.f;
       float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
       if (M != -INFINITY) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) wj[j] = (mj[j] == -INFINITY) ? 0.f : exp2f(mj[j] - M);
-#pragma unroll
         for (int j = 0; j < 8; ++j) {
-          if (j < npairs) {
-            den = fmaf(wj[j], dsmem_ld_f32(dsmem_addr(lst + r, 2 * j + h)), den);
-            if (!is_lse) {
-              const float4 v = dsmem_ld_f32x4(dsmem_addr(ostage + r * kHalfCols + (d - kHalfCols * h), 2 * j + h));
-              num.x = fmaf(wj[j], v.x, num.x);
-              num.y = fmaf(wj[j], v.y, num.y);
-              num.z = fmaf(wj[j], v.z, num.z);
-              num.w = fmaf(wj[j], v.w, num.w);
-            }
-          }
+          const float wj = (mj[j] == -INFINITY) ? 0.f : exp2f(mj[j] - M);
+          den = fmaf(wj, lj[j], den);
+          num.x = fmaf(wj, vj[j].x, num.x);
+          num.y = fmaf(wj, vj[j].y, num.y);
+          num.z = fmaf(wj, vj[j].z, num.z);
+          num.w = fmaf(wj, vj[j].w, num.w);
         }
       }
       if (is_lse) {
