@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 CONTEXTS = [32768, 49152, 65536, 81920, 98304, 131072]
 H, BS, DTYPE, SEED = 16, 32, "f16", 2
 LATENT_BYTES_PER_TOKEN = (512 + 64) * 2
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "partial_tc_ctx_sweep.json")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "mla_partial_tc128_kernel_dram_traffic.json")
 WORKLOAD = "mla_decode_ctx_sweep_B1_H16_r512_rope64_fp16_bs32"
 METRIC = "us per MLA decode layer call (mean over ctx 32K-131K), HBM GB/s as fraction of peak"
 
@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--kernel", default="tc", choices=["tc", "simt"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-ctx", type=int, default=0,
+                    help="profiling case: only --launches plain layer calls at this context (of the sweep), then exit")
+    ap.add_argument("--launches", type=int, default=5)
     return ap.parse_args()
 
 
@@ -112,15 +115,17 @@ class OraclePool:
         self.pool.join()
 
 
-def make_cases():
+def make_case(i, L):
+    """Context i of the sweep: seeded latents, a pool 25% larger than needed, random page order."""
     from mla_split_kv_gb300 import inputs as gen
 
-    cases = []
-    for i, L in enumerate(CONTEXTS):
-        pages = gen.pages_for(L, BS)
-        cases.append(gen.make_decode_case(SEED * 100 + i, [L], num_heads=H, block_size=BS, dtype=DTYPE,
-                                          pool_blocks=pages + pages // 4))
-    return cases
+    pages = gen.pages_for(L, BS)
+    return gen.make_decode_case(SEED * 100 + i, [L], num_heads=H, block_size=BS, dtype=DTYPE,
+                                pool_blocks=pages + pages // 4)
+
+
+def make_cases():
+    return [make_case(i, L) for i, L in enumerate(CONTEXTS)]
 
 
 def oracle_timing(cases, steps, cores, budget_s=30.0):
@@ -222,7 +227,7 @@ def measured_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("partial_tc.cu", "device_common.cuh", "kernels.h"):
+    for f in ("partial_tc.cu", "partial_tc128.cu", "device_common.cuh", "kernels.h"):
         h.update(open(os.path.join(ROOT, "mla_split_kv_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -237,6 +242,48 @@ def profiled_traffic(tokens_per_launch):
         return None
     bpt = prof.get("dram_bytes_per_token")
     return None if bpt is None else round(bpt * tokens_per_launch)
+
+
+def partial_kernel_name(kernel, plans):
+    """The partial kernel the library dispatches for this workload (16 fp16 rows per CTA)."""
+    if kernel == "simt":
+        return "mla_partial_simt_kernel"
+    if all(2 <= p.cluster_ctas <= 16 for p in plans):
+        return "mla_partial_tc128_kernel"
+    return "mla_partial_tc_kernel"
+
+
+def run_profile_case(args):
+    """A few plain layer calls at one context: the workload of the ncu captures in profiles/."""
+    import torch
+
+    from mla_split_kv_gb300 import binding as nb
+    from mla_split_kv_gb300 import build as nbuild
+    from mla_split_kv_gb300 import runtime as rt
+
+    nbuild.build()
+    nb.load()
+    L = args.profile_ctx
+    i = CONTEXTS.index(L) if L in CONTEXTS else 0
+    case = make_case(i, L)
+    dev = nb.mla_device_query()
+    plan = nb.mla_plan([L], H, 1, BS, dev)
+    kernel = nb.MLA_KERNEL_TC if args.kernel == "tc" else nb.MLA_KERNEL_SIMT
+    dc = rt.upload(case)
+    chunks_dev = rt.chunks_to_device(plan.chunks)
+    part, lse = rt.alloc_partials(plan.num_chunks, 1, H)
+    ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
+    out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
+    for _ in range(args.launches):
+        rt.decode_partial(dc, part, lse, chunks_dev=chunks_dev, kernel=kernel, cluster=plan.cluster_ctas)
+        rt.merge_states(part, lse, ind, 1, 1, H, "f16", out=out)
+    torch.cuda.synchronize()
+    st, code = nb.mla_check_device_errors(None)
+    print(json.dumps({"profile_ctx": L, "launches": args.launches, "partitions": plan.num_chunks,
+                      "cluster": plan.cluster_ctas, "kernel": partial_kernel_name(args.kernel, [plan]),
+                      "device_status": st, "device_error": code}))
+    if st != nb.MLA_OK:
+        raise SystemExit(1)
 
 
 def run_ours(args, rank, world):
@@ -450,7 +497,7 @@ def run_ours(args, rank, world):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(sum(CONTEXTS) / len(CONTEXTS)),
-                     "peak_source": peak_src, "kernel": f"mla_partial_{args.kernel}"},
+                     "peak_source": peak_src, "kernel": partial_kernel_name(args.kernel, [c["plan"] for c in calls])},
         "e2e": {"value": round(e2e_s * 1e6 / (e2e_steps * len(calls)), 3), "unit": "us/layer-call",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": (2 + 1) * n_calls * reps,  # step graphs (partial + merge) and partial-only graphs
@@ -491,6 +538,9 @@ def run_reference(args, rank, world):
 
 def main():
     args = parse()
+    if args.profile_ctx:
+        run_profile_case(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
