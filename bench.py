@@ -274,13 +274,17 @@ def run_profile_case(args):
     part, lse = rt.alloc_partials(plan.num_chunks, 1, H)
     ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
     out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
+    k = plan.clusters_per_chunk if kernel == nb.MLA_KERNEL_TC else 1
+    ws = rt.alloc_workspace(plan.num_chunks, k, 1, H)
     for _ in range(args.launches):
-        rt.decode_partial(dc, part, lse, chunks_dev=chunks_dev, kernel=kernel, cluster=plan.cluster_ctas)
+        rt.decode_partial(dc, part, lse, chunks_dev=chunks_dev, kernel=kernel, cluster=plan.cluster_ctas, subs=k,
+                          workspace=ws)
         rt.merge_states(part, lse, ind, 1, 1, H, "f16", out=out)
     torch.cuda.synchronize()
     st, code = nb.mla_check_device_errors(None)
     print(json.dumps({"profile_ctx": L, "launches": args.launches, "partitions": plan.num_chunks,
-                      "cluster": plan.cluster_ctas, "kernel": partial_kernel_name(args.kernel, [plan]),
+                      "cluster": plan.cluster_ctas, "clusters_per_partition": k,
+                      "kernel": partial_kernel_name(args.kernel, [plan]),
                       "device_status": st, "device_error": code}))
     if st != nb.MLA_OK:
         raise SystemExit(1)
@@ -313,9 +317,11 @@ def run_ours(args, rank, world):
             part, lse = rt.alloc_partials(plan.num_chunks, 1, H)
             ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
             out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
-            desc = rt.make_desc(dc, chunks_dev, kernel, plan.cluster_ctas, stream)
+            k = plan.clusters_per_chunk if kernel == nb.MLA_KERNEL_TC else 1
+            ws = rt.alloc_workspace(plan.num_chunks, k, 1, H)
+            desc = rt.make_desc(dc, chunks_dev, kernel, plan.cluster_ctas, stream, k, ws)
             calls.append(dict(L=L, plan=plan, dc=dc, chunks=chunks_dev, part=part, lse=lse, ind=ind, out=out,
-                              desc=desc))
+                              desc=desc, ws=ws))
     torch.cuda.synchronize()
 
     def partial(c):
@@ -417,6 +423,7 @@ def run_ours(args, rank, world):
         us = e[0].elapsed_time(e[1]) * 1e3 / 4
         pus = e[1].elapsed_time(e[2]) * 1e3 / 4
         per_ctx.append({"ctx": c["L"], "partitions": c["plan"].num_chunks, "cluster": c["plan"].cluster_ctas,
+                        "clusters_per_partition": c["desc"].clusters_per_chunk,
                         "us_per_call": round(us, 3), "partial_us": round(pus, 3),
                         "layer_gbs": round((pb + mb) / (us * 1e-6) / 1e9, 1),
                         "partial_gbs": round(pb / (pus * 1e-6) / 1e9, 1),

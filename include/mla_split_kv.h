@@ -110,8 +110,10 @@ typedef struct {
   int32_t* o_indptr;        /* host, caller-owned, >= B+1 entries              */
   /* outputs */
   int32_t num_chunks;       /* N = sum_b P_b                                   */
-  int32_t cluster_ctas;     /* CTAs that share one partition (1,2,4,8,16)      */
+  int32_t cluster_ctas;     /* CTAs per cluster (1,2,4,8,16)                    */
   int32_t kernel;           /* mla_kernel_t the plan was sized for             */
+  int32_t clusters_per_chunk; /* k >= 1 clusters share one partition; k > 1
+                               needs a workspace (mla_workspace_bytes)         */
 } mla_plan_t;
 
 /*
@@ -126,7 +128,11 @@ typedef struct {
  * otherwise P_b is proportional to L_b so that all partitions fill one wave
  * of the device's co-resident clusters, clamped to [min, max] partitions and
  * so that no chunk is empty. cluster_ctas is the cluster size that keeps the
- * most CTAs busy in that wave with at least one 64-token tile per CTA.
+ * most CTAs busy in that wave with at least one 64-token tile per CTA. When
+ * the paired 16-row kernel applies (q_len*H <= 16, fp16, clusters of >= 2)
+ * and one wave holds more clusters than partitions, each partition is spread
+ * over clusters_per_chunk = k clusters (k <= 16, every CTA pair keeping at
+ * least one 128-token tile); the partition count itself is not raised.
  *
  * context_lens_host: host [B] int32, each >= 0. dev: from mla_device_query or
  * hand-filled. Returns MLA_ERR_CAPACITY when N > plan->capacity (num_chunks
@@ -151,10 +157,39 @@ typedef struct {
   const mla_chunk_t* chunks;  /* DEVICE array of num_chunks records, or NULL
                                  for a uniform split into num_partitions       */
   int32_t num_chunks;         /* records in `chunks` (ignored when NULL)      */
-  int32_t cluster_ctas;       /* CTAs per partition: 1,2,4,8,16; 0 = auto     */
+  int32_t cluster_ctas;       /* CTAs per cluster: 1,2,4,8,16; 0 = auto       */
   int32_t kernel;             /* mla_kernel_t                                 */
   void* stream;               /* cudaStream_t                                 */
+  int32_t clusters_per_chunk; /* k: clusters per partition; 0 or 1 = one.
+                                 k > 1 (1..16): the chunk's tokens are split
+                                 over k clusters; each writes a sub-partial
+                                 (normalized partial + log2 LSE) to the
+                                 workspace and the cluster that finishes last
+                                 merges the k of them in index order into the
+                                 partition's slot. Only for the paired 16-row
+                                 fp16 tensor-core kernel (q_len*H <= 16,
+                                 cluster_ctas set to 2..16, not 0 = auto);
+                                 otherwise MLA_ERR_UNSUPPORTED (INVALID_ARG for
+                                 cluster_ctas 0 or a missing / short workspace;
+                                 k > 16 is INVALID_ARG).                         */
+  void* workspace;            /* DEVICE, >= mla_workspace_bytes(...) bytes,
+                                 16-byte aligned, ZEROED by the caller before
+                                 its first use; every call leaves its counters
+                                 at zero again (after a device error, zero it
+                                 again). Calls sharing a workspace must not
+                                 overlap in time. Unused when k <= 1.           */
+  uint64_t workspace_bytes;   /* size of `workspace`                          */
 } mla_decode_desc_t;
+
+/*
+ * mla_workspace_bytes -- device bytes a mla_decode_partial call with
+ * clusters_per_chunk = k > 1 needs: one uint32 ticket per chunk (256-byte
+ * aligned block), then N*k sub-partials [q_len, H, 512] fp32 and their LSEs
+ * [q_len, H] fp32. 0 when k <= 1. No counterpart on the pages: the split of a
+ * partition over several clusters is this library's way to fill the GPU at
+ * the pages' 2..8 partitions.
+ */
+uint64_t mla_workspace_bytes(int32_t num_chunks, int32_t clusters_per_chunk, int32_t q_len, int32_t num_heads);
 
 /*
  * mla_decode_partial -- attention of every query row over one chunk of its

@@ -58,6 +58,7 @@ class mla_plan_t(ctypes.Structure):
         ("num_chunks", ctypes.c_int32),
         ("cluster_ctas", ctypes.c_int32),
         ("kernel", ctypes.c_int32),
+        ("clusters_per_chunk", ctypes.c_int32),
     ]
 
 
@@ -76,6 +77,9 @@ class mla_decode_desc_t(ctypes.Structure):
         ("cluster_ctas", ctypes.c_int32),
         ("kernel", ctypes.c_int32),
         ("stream", ctypes.c_void_p),
+        ("clusters_per_chunk", ctypes.c_int32),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_uint64),
     ]
 
 
@@ -113,6 +117,8 @@ def load() -> ctypes.CDLL:
     lib.mla_partials_bytes.restype = ctypes.c_size_t
     lib.mla_lse_bytes.argtypes = [i32, i32, i32]
     lib.mla_lse_bytes.restype = ctypes.c_size_t
+    lib.mla_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.mla_workspace_bytes.restype = u64
     lib.mla_status_string.argtypes = [i32]
     lib.mla_status_string.restype = ctypes.c_char_p
     lib.mla_version.argtypes = []
@@ -144,11 +150,12 @@ def mla_device_query(device: int = -1) -> mla_device_info_t:
 class Plan:
     """Host result of :func:`mla_plan`."""
 
-    def __init__(self, chunks, o_indptr, cluster_ctas, kernel):
+    def __init__(self, chunks, o_indptr, cluster_ctas, kernel, clusters_per_chunk=1):
         self.chunks = chunks  # list of (b, t0, t1, out_slot)
         self.o_indptr = o_indptr  # list of B+1 ints
         self.cluster_ctas = cluster_ctas
         self.kernel = kernel
+        self.clusters_per_chunk = clusters_per_chunk
 
     @property
     def num_chunks(self) -> int:
@@ -185,7 +192,7 @@ def mla_plan(context_lens: Sequence[int], num_heads: int, q_len: int, block_size
     plan.o_indptr = ctypes.cast(indptr, ctypes.POINTER(ctypes.c_int32))
     _check(lib.mla_plan(lens, B, num_heads, q_len, block_size, ctypes.byref(dev), ctypes.byref(plan)), "mla_plan")
     out = [(c.b, c.t0, c.t1, c.out_slot) for c in chunks[: plan.num_chunks]]
-    return Plan(out, list(indptr), plan.cluster_ctas, plan.kernel)
+    return Plan(out, list(indptr), plan.cluster_ctas, plan.kernel, plan.clusters_per_chunk)
 
 
 def mla_decode_partial(q_absorbed: int, q_pe: int, ckv_cache: int, kpe_cache: int, block_table: int,
@@ -220,6 +227,10 @@ def mla_reset_counters() -> None:
 
 def mla_set_wait_timeout_ns(ns: int) -> None:
     load().mla_set_wait_timeout_ns(ns)
+
+
+def mla_workspace_bytes(num_chunks: int, clusters_per_chunk: int, q_len: int, num_heads: int) -> int:
+    return int(load().mla_workspace_bytes(num_chunks, clusters_per_chunk, q_len, num_heads))
 
 
 def mla_partials_bytes(num_slots: int, q_len: int, num_heads: int) -> int:

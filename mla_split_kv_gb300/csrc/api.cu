@@ -172,6 +172,7 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   const int32_t C0 = d->cluster_ctas;
   if (C0 != 0 && C0 != 1 && C0 != 2 && C0 != 4 && C0 != 8 && C0 != 16) return reject(MLA_ERR_INVALID_ARG);
   if (!std::isfinite(scale)) return reject(MLA_ERR_INVALID_ARG);
+  if (d->clusters_per_chunk < 0 || d->clusters_per_chunk > 16) return reject(MLA_ERR_INVALID_ARG);
   int64_t N;
   if (d->chunks == nullptr) {
     if (num_partitions < 1 || num_partitions > 1024) return reject(MLA_ERR_INVALID_ARG);
@@ -186,6 +187,22 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
     return reject(MLA_ERR_INVALID_ARG);
   const uint64_t rows = static_cast<uint64_t>(d->num_blocks) * static_cast<uint64_t>(d->block_size);
   if (rows > 0x7fffffffull) return reject(MLA_ERR_UNSUPPORTED);
+
+  const bool use_simt = (d->kernel == MLA_KERNEL_SIMT);
+  const bool bf16 = (d->dtype == MLA_BF16);
+  const int rows_total = d->num_heads * d->q_len;
+  const int nr = use_simt ? mla::simt_rows_per_cta() : mla::tc_rows_per_cta(rows_total, bf16);
+  const int64_t groups = (rows_total + nr - 1) / nr;
+  const int32_t subs = (d->clusters_per_chunk > 1) ? d->clusters_per_chunk : 1;
+  if (subs > 1) {  // a partition spread over several clusters: the paired kernel with a workspace
+    if (C0 == 0) return reject(MLA_ERR_INVALID_ARG);  // the cluster size is part of that plan
+    if (use_simt || !mla::tc128_supports(rows_total, bf16, C0)) return reject(MLA_ERR_UNSUPPORTED);
+    const uint64_t need = mla_workspace_bytes(static_cast<int32_t>(N), subs, d->q_len, d->num_heads);
+    if (d->workspace == nullptr || !aligned(d->workspace, 16) || d->workspace_bytes < need)
+      return reject(MLA_ERR_INVALID_ARG);
+    if (N * subs > 65535) return reject(MLA_ERR_UNSUPPORTED);
+  }
+  const int C = C0 ? C0 : default_cluster(N * groups);
 
   CUtensorMap tm_ckv, tm_kpe, tm_pages;
   if (!tensor_map(&tm_ckv, ckv_cache, rows, mla::kRank, d->block_size, d->dtype) ||
@@ -214,12 +231,17 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   p.causal = d->causal;
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
 
-  const bool use_simt = (d->kernel == MLA_KERNEL_SIMT);
-  const bool bf16 = (d->dtype == MLA_BF16);
-  const int rows_total = d->num_heads * d->q_len;
-  const int nr = use_simt ? mla::simt_rows_per_cta() : mla::tc_rows_per_cta(rows_total, bf16);
-  const int64_t groups = (rows_total + nr - 1) / nr;
-  const int C = C0 ? C0 : default_cluster(N * groups);
+  p.subs = subs;
+  p.ws_partials = nullptr;
+  p.ws_lse = nullptr;
+  p.ws_tickets = nullptr;
+  if (subs > 1) {
+    uint8_t* ws = static_cast<uint8_t*>(d->workspace);
+    const uint64_t tickets = (static_cast<uint64_t>(N) * 4 + 255) / 256 * 256;
+    p.ws_tickets = reinterpret_cast<uint32_t*>(ws);
+    p.ws_partials = reinterpret_cast<float*>(ws + tickets);
+    p.ws_lse = p.ws_partials + static_cast<uint64_t>(N) * subs * rows_total * mla::kRank;
+  }
   cudaStream_t stream = static_cast<cudaStream_t>(d->stream);
   const cudaError_t e = use_simt ? mla::launch_partial_simt(tm_ckv, tm_kpe, p, static_cast<int>(N), C, bf16, stream)
                                  : mla::launch_partial_tc(tm_ckv, tm_kpe, tm_pages, p, static_cast<int>(N), C, bf16, stream);
@@ -228,8 +250,16 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
     return MLA_ERR_CUDA;
   }
   g_counters[use_simt ? MLA_CTR_PARTIAL_SIMT : MLA_CTR_PARTIAL_TC].fetch_add(1, std::memory_order_relaxed);
-  g_counters[MLA_CTR_CTAS].fetch_add(static_cast<uint64_t>(N * groups * C), std::memory_order_relaxed);
+  g_counters[MLA_CTR_CTAS].fetch_add(static_cast<uint64_t>(N * groups * C * subs), std::memory_order_relaxed);
   return MLA_OK;
+}
+
+uint64_t mla_workspace_bytes(int32_t num_chunks, int32_t clusters_per_chunk, int32_t q_len, int32_t num_heads) {
+  if (clusters_per_chunk <= 1 || num_chunks < 1 || q_len < 1 || num_heads < 1) return 0;
+  const uint64_t n = static_cast<uint64_t>(num_chunks), k = static_cast<uint64_t>(clusters_per_chunk);
+  const uint64_t rows = static_cast<uint64_t>(q_len) * static_cast<uint64_t>(num_heads);
+  const uint64_t tickets = (n * 4 + 255) / 256 * 256;
+  return tickets + n * k * rows * mla::kRank * 4 + n * k * rows * 4;
 }
 
 mla_status_t mla_merge_states(const float* partials, const float* lse, const int32_t* o_indptr, int32_t B,

@@ -184,6 +184,11 @@ __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
   asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
   return v;
 }
+__device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr) {
   float4 v;
   asm("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
@@ -371,14 +376,15 @@ __device__ __forceinline__ void uniform_chunk(int32_t L, int32_t P, int32_t p, i
   *t1 = static_cast<int32_t>(e < L ? e : L);
 }
 
-// Fill the chunk, the CTA's token sub-range (runs of `unit`-token tiles split
-// evenly over the cluster, or over `nparts` groups of it, this CTA in group
-// `part`) and its query rows. Tokens are trimmed to the last one any row
+// Fill the chunk (blockIdx.y, or `chunk`), the CTA's token sub-range (runs of
+// `unit`-token tiles split evenly over the cluster, or over `nparts` groups,
+// this CTA in group `part`) and its query rows. Tokens are trimmed to the last one any row
 // of this CTA can see under the causal rule.
 __device__ __forceinline__ CtaWork cta_work(const PartialParams& p, int32_t rows_per_cta,
-                                            int32_t unit = kTileTokens, int32_t part = -1, int32_t nparts = 0) {
+                                            int32_t unit = kTileTokens, int32_t part = -1, int32_t nparts = 0,
+                                            int32_t chunk = -1) {
   CtaWork w;
-  const int32_t n = blockIdx.y;
+  const int32_t n = (chunk >= 0) ? chunk : static_cast<int32_t>(blockIdx.y);
   if (p.chunks != nullptr) {
     const int4 c = reinterpret_cast<const int4*>(p.chunks)[n];
     w.b = c.x;

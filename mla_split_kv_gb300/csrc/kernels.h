@@ -35,6 +35,13 @@ struct PartialParams {
   int32_t num_parts;           // uniform split when chunks == null
   int32_t causal;
   uint64_t timeout_ns;
+  // a chunk spread over `subs` clusters (paired 16-row kernel only): grid.y =
+  // chunks * subs; the sub-partials and their LSEs go to ws_partials / ws_lse
+  // (slot = grid.y index), one ticket per chunk in ws_tickets (zero between calls)
+  int32_t subs;
+  float* ws_partials;          // [chunks * subs, q_len, H, 512]
+  float* ws_lse;               // [chunks * subs, q_len, H]
+  uint32_t* ws_tickets;        // [chunks]
 };
 
 struct MergeParams {

@@ -81,6 +81,7 @@ struct Small {
   uint64_t full[2], empty[2], sfull[2], sfree[2], ppfull[2], pvdone[2], xfull[2], xempty[2], drain;
   uint32_t tmem_base;
   int32_t abort_flag;
+  int32_t last_cluster;  // this cluster took the chunk's last ticket
   float red[4][kNR];
   float mref[kNR];
   float alpha[kNR];
@@ -104,7 +105,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank(), nranks = cluster_nctarank(), peer = rank ^ 1u;
   const int half = static_cast<int>(rank & 1u);
-  const CtaWork w = cta_work(p, kNR, kT, static_cast<int>(rank >> 1), static_cast<int>(nranks >> 1));
+  // a chunk may be spread over `subs` clusters (grid.y = chunk * subs + sub); its tiles are
+  // split over all their pairs
+  const int subs = (p.subs > 1) ? p.subs : 1;
+  const int chunk = static_cast<int>(blockIdx.y) / subs, sub = static_cast<int>(blockIdx.y) % subs;
+  const int cluster_pairs = static_cast<int>(nranks >> 1);
+  const CtaWork w =
+      cta_work(p, kNR, kT, sub * cluster_pairs + static_cast<int>(rank >> 1), subs * cluster_pairs, chunk);
   const int ntiles = (w.sub1 - w.sub0 + kT - 1) / kT;
   const int rows_total = p.q_len * p.H;
 
@@ -515,11 +522,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();
+  // the cluster's result goes to the chunk's slot, or, when the chunk is spread over several
+  // clusters, to this cluster's sub-partial slot of the workspace
+  float* const dst_partials = (subs > 1) ? p.ws_partials : p.partials;
+  float* const dst_lse = (subs > 1) ? p.ws_lse : p.lse;
+  const long long dst_slot = (subs > 1) ? static_cast<long long>(blockIdx.y) : static_cast<long long>(w.slot);
   {
     // Combine the pairs of the cluster in rank order: this CTA writes output
     // columns [rank * 512 / n, (rank + 1) * 512 / n), held by the CTAs of
     // half h = those columns / 256; rank 0 also writes the LSE.
-    const int npairs = static_cast<int>(nranks >> 1);
+    const int npairs = cluster_pairs;
     const int dcols = kRank / static_cast<int>(nranks);
     const int dbeg = static_cast<int>(rank) * dcols;
     const uint32_t h = static_cast<uint32_t>(dbeg / kHalfCols);
@@ -561,12 +573,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (is_lse) {
-        p.lse[static_cast<long long>(w.slot) * rows_total + w.row0 + r] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
+        dst_lse[dst_slot * rows_total + w.row0 + r] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
       } else {
         float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
         if (M != -INFINITY) out = make_float4(num.x / den, num.y / den, num.z / den, num.w / den);
-        const long long base = (static_cast<long long>(w.slot) * rows_total + w.row0 + r) * kRank + d;
-        *reinterpret_cast<float4*>(p.partials + base) = out;
+        const long long base = (dst_slot * rows_total + w.row0 + r) * kRank + d;
+        *reinterpret_cast<float4*>(dst_partials + base) = out;
+      }
+    }
+  }
+  if (subs > 1) __threadfence();  // this thread's share of the sub-partial, visible before the ticket
+  cluster_sync();
+  if (subs > 1) {
+    // Take the chunk's ticket; the cluster that takes the last one merges the chunk's sub-partials
+    // (normalized partials with log2 LSEs, like the partitions of a request) in sub order, so the
+    // result does not depend on which cluster finishes last. It also resets the ticket.
+    if (rank == 0 && tid == 0) {
+      const uint32_t t = atomicAdd(p.ws_tickets + chunk, 1u);
+      const int last = (t == static_cast<uint32_t>(subs - 1)) ? 1 : 0;
+      if (last) atomicExch(p.ws_tickets + chunk, 0u);
+      sm->last_cluster = last;
+    }
+    cluster_sync();
+    const bool last = dsmem_ld_u32(dsmem_addr(&sm->last_cluster, 0)) != 0;
+    if (last) {
+      __threadfence();
+      const int dcols = kRank / static_cast<int>(nranks);
+      const int dbeg = static_cast<int>(rank) * dcols;
+      const int n4 = dcols / 4;
+      const int items = w.nrows * n4 + ((rank == 0) ? w.nrows : 0);
+      const long long sub0 = static_cast<long long>(chunk) * subs;
+      for (int idx = tid; idx < items; idx += kThreads) {
+        const bool is_lse = idx >= w.nrows * n4;
+        const int r = is_lse ? idx - w.nrows * n4 : idx / n4;
+        const int d = is_lse ? 0 : dbeg + (idx % n4) * 4;
+        float lj[16];
+        float4 vj[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          lj[j] = -INFINITY;
+          vj[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (j < subs) {
+            const long long row = (sub0 + j) * rows_total + w.row0 + r;
+            lj[j] = __ldcg(p.ws_lse + row);
+            if (!is_lse) vj[j] = __ldcg(reinterpret_cast<const float4*>(p.ws_partials + row * kRank + d));
+          }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) M = fmaxf(M, lj[j]);
+        float den = 0.f;
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float wj = (lj[j] == -INFINITY) ? 0.f : exp2f(lj[j] - M);
+            den += wj;
+            num.x = fmaf(wj, vj[j].x, num.x);
+            num.y = fmaf(wj, vj[j].y, num.y);
+            num.z = fmaf(wj, vj[j].z, num.z);
+            num.w = fmaf(wj, vj[j].w, num.w);
+          }
+        }
+        if (is_lse) {
+          p.lse[static_cast<long long>(w.slot) * rows_total + w.row0 + r] =
+              (M == -INFINITY) ? -INFINITY : M + log2f(den);
+        } else {
+          float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (M != -INFINITY) out = make_float4(num.x / den, num.y / den, num.z / den, num.w / den);
+          *reinterpret_cast<float4*>(p.partials + (static_cast<long long>(w.slot) * rows_total + w.row0 + r) * kRank +
+                                     d) = out;
+        }
       }
     }
   }
@@ -605,7 +682,7 @@ cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap&
   cudaError_t e = prepare(cluster);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cluster, num_chunks, 1);
+  cfg.gridDim = dim3(cluster, num_chunks * (p.subs > 1 ? p.subs : 1), 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;

@@ -11,7 +11,9 @@
 // partition's tokens and combine on chip), so the plan is sized against the
 // number of co-resident clusters of the partial kernel: partitions are shared
 // out over requests in proportion to their lengths so that one wave of
-// clusters covers all of them.
+// clusters covers all of them. With the paired 16-row kernel a partition may
+// also span k clusters (combined through a workspace), so that the 2..8
+// partitions of one request still fill the device.
 #include <algorithm>
 #include <cstdint>
 #include <vector>
@@ -35,9 +37,27 @@ int64_t no_empty_chunks(int64_t L, int64_t P, int64_t bs) {
 
 struct Candidate {
   int cluster = 1;
+  int64_t subs = 1;     // clusters per partition
   std::vector<int64_t> parts;
   int64_t active = -1;  // CTAs busy in the first wave
+  double cost_us = 0;   // modelled time (single request on the paired kernel)
 };
+
+constexpr int64_t kMaxSubs = 16;       // clusters per partition (the kernel's final merge reads at most 16)
+constexpr int64_t kPairTileTokens = 128;
+// Time model of the paired kernel for one request (measured on GB300): a CTA pair takes ~2.6 us per
+// 128-token tile; spreading a partition over k > 1 clusters adds a ticket + final-merge tail of
+// ~3 us plus ~0.3 us per sub-partial for a 2-CTA cluster (the merge work per CTA scales with k / C).
+constexpr double kTileUs = 2.6, kSpreadTailUs = 3.0, kMergeUsPerSub = 0.3;
+
+double paired_cost_us(int64_t L, int64_t P, int64_t k, int C) {
+  const int64_t pairs = P * k * (C / 2);
+  const int64_t tiles = (L + kPairTileTokens - 1) / kPairTileTokens;
+  const int64_t per_pair = (tiles + pairs - 1) / pairs;
+  double t = static_cast<double>(per_pair) * kTileUs;
+  if (k > 1) t += kSpreadTailUs + kMergeUsPerSub * static_cast<double>(k) * 2.0 / static_cast<double>(C);
+  return t;
+}
 
 }  // namespace
 
@@ -72,10 +92,13 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
     }
 
   Candidate best;
+  // one long request on the paired kernel: candidates compared by the time model
+  const bool paired_single = (B == 1 && n_split == 1 && mla::tc128_supports(rows, plan->dtype == MLA_BF16, 2));
   for (int k = 0; k < 5; ++k) {
     const int C = 1 << k;
     const int64_t slots = dev->max_clusters[k];
     if (slots <= 0) continue;
+    if (paired_single && C == 1) continue;  // the paired kernel needs a pair of CTAs
     Candidate cand;
     cand.cluster = C;
     cand.parts.assign(B, 1);
@@ -115,8 +138,53 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
     if (!ok) continue;
     int64_t N = 0;
     for (int32_t b = 0; b < B; ++b) N += cand.parts[b];
-    cand.active = std::min<int64_t>(N * row_groups, slots) * C;
-    if (cand.active > best.active) best = cand;  // ties keep the smaller cluster
+    // spread each partition over k clusters when the paired kernel runs and a wave has room,
+    // every CTA pair keeping at least one 128-token tile of its partition
+    auto largest_k = [&](const std::vector<int64_t>& parts, int64_t n) -> int64_t {
+      int64_t k = std::min<int64_t>(kMaxSubs, slots / (n * row_groups));
+      for (; k > 1; --k) {
+        bool fits = true;
+        for (int32_t b = 0; b < B && fits; ++b) {
+          const int64_t L = context_lens_host[b];
+          const int64_t len = (parts[b] > 1) ? chunk_len(L, parts[b], block_size) : L;
+          if (len < k * (C / 2) * kPairTileTokens) fits = false;
+        }
+        if (fits) break;
+      }
+      return std::max<int64_t>(1, k);
+    };
+    if (mla::tc128_supports(rows, plan->dtype == MLA_BF16, C) && N * row_groups < slots) {
+      cand.subs = largest_k(cand.parts, N);
+      if (paired_single) {
+        // one long request: among the allowed partition counts and spreads take the fastest by the
+        // time model (ties: fewer clusters per partition)
+        const int64_t L = context_lens_host[0];
+        double best_cost = paired_cost_us(L, N, cand.subs, C);
+        std::vector<int64_t> parts1(1);
+        for (int64_t P1 = minP; P1 <= maxP; ++P1) {
+          parts1[0] = no_empty_chunks(L, P1, block_size);
+          if (parts1[0] != P1 || P1 * row_groups > slots) continue;
+          for (int64_t k1 = largest_k(parts1, P1); k1 >= 1; --k1) {
+            const double c1 = paired_cost_us(L, P1, k1, C);
+            if (c1 < best_cost - 1e-9 || (c1 < best_cost + 1e-9 && k1 < cand.subs)) {
+              best_cost = c1;
+              cand.parts[0] = P1;
+              cand.subs = k1;
+            }
+          }
+        }
+        N = cand.parts[0];
+      }
+    }
+    if (paired_single) cand.cost_us = paired_cost_us(context_lens_host[0], N, cand.subs, C);
+    cand.active = std::min<int64_t>(N * row_groups * cand.subs, slots) * C;
+    if (paired_single) {
+      // the modelled fastest; on a tie the smaller cluster (visited first)
+      if (best.active < 0 || cand.cost_us < best.cost_us - 1e-9) best = cand;
+    } else if (cand.active > best.active || (cand.active == best.active && cand.subs < best.subs)) {
+      // more busy CTAs wins; on a tie, fewer clusters per partition, then the smaller cluster
+      best = cand;
+    }
   }
   if (best.active < 0) {  // no cluster size usable: one CTA per partition, no split
     best = Candidate();
@@ -130,6 +198,7 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
   plan->num_chunks = static_cast<int32_t>(N);
   plan->cluster_ctas = best.cluster;
   plan->kernel = MLA_KERNEL_TC;
+  plan->clusters_per_chunk = static_cast<int32_t>(best.subs);
   if (N > plan->capacity) return MLA_ERR_CAPACITY;
   if (plan->chunks == nullptr || plan->o_indptr == nullptr) return MLA_ERR_INVALID_ARG;
 

@@ -53,7 +53,8 @@ def chunks_to_device(chunks: Sequence[Sequence[int]], device="cuda") -> torch.Te
 
 
 def make_desc(dc: DeviceCase, chunks_dev: Optional[torch.Tensor], kernel: int, cluster: int,
-              stream: Optional[torch.cuda.Stream] = None) -> nb.mla_decode_desc_t:
+              stream: Optional[torch.cuda.Stream] = None, subs: int = 1,
+              workspace: Optional[torch.Tensor] = None) -> nb.mla_decode_desc_t:
     c = dc.case
     d = nb.mla_decode_desc_t()
     d.num_requests = c.num_requests
@@ -70,7 +71,16 @@ def make_desc(dc: DeviceCase, chunks_dev: Optional[torch.Tensor], kernel: int, c
     d.kernel = kernel
     s = stream if stream is not None else torch.cuda.current_stream()
     d.stream = s.cuda_stream
+    d.clusters_per_chunk = subs
+    d.workspace = workspace.data_ptr() if workspace is not None else None
+    d.workspace_bytes = workspace.numel() if workspace is not None else 0
     return d
+
+
+def alloc_workspace(num_chunks: int, subs: int, q_len: int, H: int, device="cuda") -> Optional[torch.Tensor]:
+    """Zeroed workspace for partitions spread over `subs` clusters (None when subs <= 1)."""
+    n = nb.mla_workspace_bytes(num_chunks, subs, q_len, H)
+    return torch.zeros(n, dtype=torch.uint8, device=device) if n else None
 
 
 def alloc_partials(num_slots: int, q_len: int, H: int, device="cuda"):
@@ -81,8 +91,9 @@ def alloc_partials(num_slots: int, q_len: int, H: int, device="cuda"):
 
 def decode_partial(dc: DeviceCase, part: torch.Tensor, lse: torch.Tensor, num_partitions: int = 1,
                    chunks_dev: Optional[torch.Tensor] = None, kernel: int = nb.MLA_KERNEL_AUTO,
-                   cluster: int = 0, stream=None, desc: Optional[nb.mla_decode_desc_t] = None) -> None:
-    d = desc if desc is not None else make_desc(dc, chunks_dev, kernel, cluster, stream)
+                   cluster: int = 0, stream=None, desc: Optional[nb.mla_decode_desc_t] = None, subs: int = 1,
+                   workspace: Optional[torch.Tensor] = None) -> None:
+    d = desc if desc is not None else make_desc(dc, chunks_dev, kernel, cluster, stream, subs, workspace)
     nb.mla_decode_partial(dc.q_abs.data_ptr(), dc.q_pe.data_ptr(), dc.ckv.data_ptr(), dc.kpe.data_ptr(),
                           dc.block_table.data_ptr(), dc.context_lens.data_ptr(), float(dc.case.scale),
                           num_partitions, part.data_ptr(), lse.data_ptr(), d)

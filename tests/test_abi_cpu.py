@@ -76,8 +76,40 @@ def check_plan_tiles(plan, lens, bs):
 def test_plan_long_context_single_request(lib, L):
     plan = nb.mla_plan([L], 16, 1, 32, fake_gb300())
     assert 2 <= plan.num_chunks <= 8
-    assert plan.num_chunks * plan.cluster_ctas >= 100  # most of the 152 SMs busy
+    busy = plan.num_chunks * plan.cluster_ctas * plan.clusters_per_chunk
+    assert 100 <= busy <= 152  # most of the 152 SMs busy, with at most 8 partitions
+    if L >= 81920:  # long enough that spreading partitions over clusters pays for its merge tail
+        assert plan.clusters_per_chunk > 1 and busy >= 140
     check_plan_tiles(plan, [L], 32)
+    # every CTA pair of every cluster keeps at least one 128-token tile of its partition
+    k, C = plan.clusters_per_chunk, plan.cluster_ctas
+    assert 1 <= k <= 16
+    for (_, t0, t1, _) in plan.chunks:
+        assert t1 - t0 >= k * (C // 2) * 128
+
+
+def test_plan_spreads_partitions_only_for_the_paired_kernel(lib):
+    # the paired kernel runs for 16 fp16 rows per CTA only: bf16 or 128 heads keep one cluster per partition
+    p16 = nb.mla_plan([131072], 16, 1, 32, fake_gb300())
+    assert p16.clusters_per_chunk > 1 and p16.cluster_ctas >= 2
+    pb = nb.mla_plan([131072], 16, 1, 32, fake_gb300(), dtype="bf16")
+    assert pb.clusters_per_chunk == 1
+    p128 = nb.mla_plan([131072], 128, 1, 32, fake_gb300())
+    assert p128.clusters_per_chunk == 1
+    # a short request in the batch caps k so that, when a partition is spread, every pair still gets a tile
+    pmix = nb.mla_plan([131072, 700], 16, 1, 32, fake_gb300())
+    k, C = pmix.clusters_per_chunk, pmix.cluster_ctas
+    if k > 1:
+        for (_, t0, t1, _) in pmix.chunks:
+            assert t1 - t0 >= k * (C // 2) * 128
+
+
+def test_workspace_bytes(lib):
+    assert nb.mla_workspace_bytes(8, 1, 1, 16) == 0
+    n, k, rows = 8, 9, 16
+    expect = 256 + n * k * rows * 512 * 4 + n * k * rows * 4
+    assert nb.mla_workspace_bytes(n, k, 1, 16) == expect
+    assert nb.mla_workspace_bytes(100, 2, 2, 16) == 512 + 100 * 2 * 32 * 512 * 4 + 100 * 2 * 32 * 4
 
 
 def test_plan_mixed_batch_two_to_four(lib):
@@ -174,6 +206,30 @@ def test_decode_partial_rejects_before_launch(lib, kw, P, want):
     assert call_partial(lib, desc(**kw), P) == want
     ctr = nb.mla_get_counters()
     assert ctr[nb.CTR_PARTIAL_TC] == 0 and ctr[nb.CTR_PARTIAL_SIMT] == 0 and ctr[nb.CTR_REJECTED] == 1
+
+
+BIG = 1 << 40
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(clusters_per_chunk=17, cluster_ctas=2, workspace=FAKE, workspace_bytes=BIG), nb.MLA_ERR_INVALID_ARG),
+    (dict(clusters_per_chunk=-1), nb.MLA_ERR_INVALID_ARG),
+    (dict(clusters_per_chunk=4, cluster_ctas=2), nb.MLA_ERR_INVALID_ARG),  # no workspace
+    (dict(clusters_per_chunk=4, cluster_ctas=2, workspace=FAKE, workspace_bytes=1024), nb.MLA_ERR_INVALID_ARG),
+    (dict(clusters_per_chunk=4, cluster_ctas=2, workspace=FAKE + 8, workspace_bytes=BIG), nb.MLA_ERR_INVALID_ARG),
+    (dict(clusters_per_chunk=4, cluster_ctas=0, workspace=FAKE, workspace_bytes=BIG), nb.MLA_ERR_INVALID_ARG),
+    (dict(clusters_per_chunk=4, cluster_ctas=1, workspace=FAKE, workspace_bytes=BIG), nb.MLA_ERR_UNSUPPORTED),
+    (dict(clusters_per_chunk=4, cluster_ctas=2, dtype=nb.MLA_BF16, workspace=FAKE, workspace_bytes=BIG),
+     nb.MLA_ERR_UNSUPPORTED),
+    (dict(clusters_per_chunk=4, cluster_ctas=2, num_heads=64, workspace=FAKE, workspace_bytes=BIG),
+     nb.MLA_ERR_UNSUPPORTED),
+    (dict(clusters_per_chunk=4, cluster_ctas=2, kernel=nb.MLA_KERNEL_SIMT, workspace=FAKE, workspace_bytes=BIG),
+     nb.MLA_ERR_UNSUPPORTED),
+])
+def test_decode_partial_rejects_bad_spread_partitions(lib, kw, want):
+    nb.mla_reset_counters()
+    assert call_partial(lib, desc(**kw), 2) == want
+    assert nb.mla_get_counters()[nb.CTR_REJECTED] == 1
 
 
 def test_decode_partial_rejects_null_and_misaligned(lib):

@@ -58,12 +58,14 @@ def assert_lse_close(got, ref, what):
         assert err <= MAX_ABS * 4, f"{what}: lse max-abs {err:.3e}"
 
 
-def run_uniform(case, P, kernel, cluster, dc=None):
+def run_uniform(case, P, kernel, cluster, dc=None, subs=1, ws=None):
     dc = dc or rt.upload(case)
     B, q, H = case.num_requests, case.q_len, case.num_heads
     part, lse = rt.alloc_partials(B * P, q, H)
     part.fill_(float("nan"))
-    rt.decode_partial(dc, part, lse, num_partitions=P, kernel=kernel, cluster=cluster)
+    if subs > 1 and ws is None:
+        ws = rt.alloc_workspace(B * P, subs, q, H)
+    rt.decode_partial(dc, part, lse, num_partitions=P, kernel=kernel, cluster=cluster, subs=subs, workspace=ws)
     ind = rt.uniform_indptr(B, P)
     out = rt.merge_states(part, lse, ind, B, q, H, "f32")
     return part, lse, out, ind, dc
@@ -173,14 +175,19 @@ def test_natural_log_lse_fails_parity_on_the_gpu_merge():
     assert err > MAX_ABS or rel > REL_L2, "natural-log LSE should not pass parity"
 
 
-def plan_and_run(case, max_partitions=0, kernel=nb.MLA_KERNEL_TC, dc=None):
+def plan_and_run(case, max_partitions=0, kernel=nb.MLA_KERNEL_TC, dc=None, ws=None):
+    """The planner's plan as the bench runs it: its cluster size and clusters per partition."""
     dev = nb.mla_device_query()
     plan = nb.mla_plan(case.context_lens.tolist(), case.num_heads, case.q_len, case.block_size, dev,
                        max_partitions=max_partitions, dtype=case.dtype)
     dc = dc or rt.upload(case)
     chunks_dev = rt.chunks_to_device(plan.chunks)
     part, lse = rt.alloc_partials(plan.num_chunks, case.q_len, case.num_heads)
-    rt.decode_partial(dc, part, lse, chunks_dev=chunks_dev, kernel=kernel, cluster=plan.cluster_ctas)
+    k = plan.clusters_per_chunk if kernel == nb.MLA_KERNEL_TC else 1
+    if k > 1 and ws is None:
+        ws = rt.alloc_workspace(plan.num_chunks, k, case.q_len, case.num_heads)
+    rt.decode_partial(dc, part, lse, chunks_dev=chunks_dev, kernel=kernel, cluster=plan.cluster_ctas, subs=k,
+                      workspace=ws)
     ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
     out = rt.merge_states(part, lse, ind, case.num_requests, case.q_len, case.num_heads, "f32")
     return plan, part, lse, out
@@ -192,10 +199,50 @@ def test_long_context_planned_full_size_sampled_heads(L):
     nb.mla_reset_counters()
     plan, part, lse, out = plan_and_run(case)
     assert 2 <= plan.num_chunks <= 8, plan.parts()
-    assert nb.mla_get_counters()[nb.CTR_PARTIAL_TC] == 1
+    if L == 131072:
+        assert plan.clusters_per_chunk > 1  # the partitions are spread over clusters to fill the GPU
+    ctr = nb.mla_get_counters()
+    assert ctr[nb.CTR_PARTIAL_TC] == 1
+    assert ctr[nb.CTR_CTAS] == plan.num_chunks * plan.cluster_ctas * plan.clusters_per_chunk
     heads = [0, 7, 15]
     ref, _ = orc.unsplit(case, heads=heads)
     assert_close(out.cpu().numpy()[:, :, heads], ref[:, :, heads], f"L={L}")
+
+
+@pytest.mark.parametrize("L,P,C,k,bs", [(4096, 2, 2, 4, 32), (4096, 1, 4, 2, 32), (20017, 3, 2, 5, 16),
+                                         (20017, 2, 4, 3, 64), (9000, 2, 16, 2, 32)])
+def test_spread_partitions_partials_match_oracle(L, P, C, k, bs):
+    """Each partition over k clusters (sub-partials merged by the last cluster) gives the partition's partial."""
+    case = gen.make_decode_case(5, [L], num_heads=16, block_size=bs, dtype="f16")
+    nb.mla_reset_counters()
+    part, lse, out, ind, dc = run_uniform(case, P, nb.MLA_KERNEL_TC, cluster=C, subs=k)
+    assert nb.mla_get_counters()[nb.CTR_CTAS] == P * C * k
+    chunks, _ = oracle_uniform_chunks(case, P)
+    ref_part, ref_lse = orc.partials(case, chunks)
+    assert_close(part.cpu().numpy(), ref_part, f"partials L={L} P={P} C={C} k={k}")
+    assert_lse_close(lse.cpu().numpy(), ref_lse, f"lse L={L} P={P} C={C} k={k}")
+    ref, _ = orc.unsplit(case)
+    assert_close(out.cpu().numpy(), ref, f"merged L={L} P={P} C={C} k={k}")
+
+
+def test_spread_partitions_bitwise_reproducible_and_workspace_reused():
+    """Same plan, same workspace, several calls: identical bits (the merge order does not depend on which
+    cluster finishes last, and every call leaves its tickets at zero)."""
+    case = gen.make_decode_case(6, [65536], num_heads=16, block_size=32, dtype="f16")
+    dc = rt.upload(case)
+    dev = nb.mla_device_query()
+    plan = nb.mla_plan([65536], 16, 1, 32, dev)
+    assert plan.clusters_per_chunk > 1
+    ws = rt.alloc_workspace(plan.num_chunks, plan.clusters_per_chunk, 1, 16)
+    outs = []
+    for _ in range(3):
+        _, part, lse, out = plan_and_run(case, dc=dc, ws=ws)
+        outs.append((part.clone(), lse.clone(), out.clone()))
+    for other in outs[1:]:
+        for a, b in zip(outs[0], other):
+            assert torch.equal(a, b)
+    tickets = ws[: 4 * plan.num_chunks].view(torch.int32)
+    assert int(tickets.abs().sum()) == 0
 
 
 def test_mixed_batch_request_major():
