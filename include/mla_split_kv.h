@@ -191,6 +191,34 @@ typedef struct {
  */
 uint64_t mla_workspace_bytes(int32_t num_chunks, int32_t clusters_per_chunk, int32_t q_len, int32_t num_heads);
 
+/* Size of the library's own scratch used by mla_decode_partial_static. */
+#define MLA_STATIC_WORKSPACE_BYTES (4u * 1024u * 1024u)
+
+/*
+ * mla_decode_partial_static -- mla_decode_partial for callers that cannot
+ * provide a workspace: the same arguments and results, but a partition
+ * spread over clusters (desc->clusters_per_chunk > 1) uses a scratch buffer
+ * that lives in the library itself (a statically sized device array of
+ * MLA_STATIC_WORKSPACE_BYTES bytes per device) instead of desc->workspace,
+ * which is ignored. The call allocates nothing. The pages have no
+ * counterpart: they split a partition over one thread group and need no
+ * scratch.
+ *
+ * Set-up happens on the first call for a device (with that device
+ * current): the scratch address is looked up and the scratch is cleared,
+ * synchronously. Make that first call before any stream capture. Calls on
+ * one device share the scratch: calls that may overlap in time (other
+ * streams, other threads) race and give undefined results; calls in one
+ * stream are fine. Returns MLA_ERR_CAPACITY (before any launch) when
+ * mla_workspace_bytes(...) of the call exceeds MLA_STATIC_WORKSPACE_BYTES,
+ * MLA_ERR_CUDA when the set-up fails, otherwise what mla_decode_partial
+ * returns. With clusters_per_chunk <= 1 it is mla_decode_partial.
+ */
+mla_status_t mla_decode_partial_static(const void* q_absorbed, const void* q_pe, const void* ckv_cache,
+                                       const void* kpe_cache, const int32_t* block_table,
+                                       const int32_t* context_lens, float scale, int32_t num_partitions,
+                                       float* partials, float* lse, const mla_decode_desc_t* desc);
+
 /*
  * mla_decode_partial -- attention of every query row over one chunk of its
  * request's cached tokens, as a normalized partial and a base-2 LSE

@@ -24,6 +24,7 @@ MLA_ERR_DEVICE_CHECK = 5
 MLA_ERR_CAPACITY = 6
 
 MLA_F16, MLA_BF16, MLA_F32 = 0, 1, 2
+MLA_STATIC_WORKSPACE_BYTES = 4 * 1024 * 1024
 MLA_KERNEL_AUTO, MLA_KERNEL_SIMT, MLA_KERNEL_TC = 0, 1, 2
 
 CTR_PARTIAL_SIMT, CTR_PARTIAL_TC, CTR_MERGE, CTR_REJECTED, CTR_CTAS = range(5)
@@ -103,6 +104,9 @@ def load() -> ctypes.CDLL:
     lib.mla_plan.restype = i32
     lib.mla_decode_partial.argtypes = [vp, vp, vp, vp, vp, vp, f32, i32, vp, vp, ctypes.POINTER(mla_decode_desc_t)]
     lib.mla_decode_partial.restype = i32
+    lib.mla_decode_partial_static.argtypes = [vp, vp, vp, vp, vp, vp, f32, i32, vp, vp,
+                                              ctypes.POINTER(mla_decode_desc_t)]
+    lib.mla_decode_partial_static.restype = i32
     lib.mla_merge_states.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32, vp, vp]
     lib.mla_merge_states.restype = i32
     lib.mla_check_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -201,6 +205,14 @@ def mla_decode_partial(q_absorbed: int, q_pe: int, ckv_cache: int, kpe_cache: in
     _check(load().mla_decode_partial(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens,
                                      ctypes.c_float(scale), num_partitions, partials, lse, ctypes.byref(desc)),
            "mla_decode_partial")
+
+
+def mla_decode_partial_static(q_absorbed: int, q_pe: int, ckv_cache: int, kpe_cache: int, block_table: int,
+                              context_lens: int, scale: float, num_partitions: int, partials: int, lse: int,
+                              desc: mla_decode_desc_t) -> None:
+    _check(load().mla_decode_partial_static(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens,
+                                            ctypes.c_float(scale), num_partitions, partials, lse, ctypes.byref(desc)),
+           "mla_decode_partial_static")
 
 
 def mla_merge_states(partials: int, lse: int, o_indptr: int, B: int, q_len: int, num_heads: int, out: int,

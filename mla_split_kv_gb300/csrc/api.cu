@@ -254,6 +254,71 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   return MLA_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Scratch of mla_decode_partial_static: one statically sized array per device
+// (the module is loaded on each device that uses it). Its address is looked up
+// once per device; it is cleared then, since the chunk tickets must start at
+// zero (every call leaves them at zero again).
+static __device__ __align__(256) uint8_t g_static_workspace[MLA_STATIC_WORKSPACE_BYTES];
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_addr[kMaxDevices] = {};
+
+mla_status_t static_workspace(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_addr[dev] == nullptr) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_static_workspace) != cudaSuccess || addr == nullptr) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+    if (cudaMemset(addr, 0, MLA_STATIC_WORKSPACE_BYTES) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+    g_static_addr[dev] = addr;
+  }
+  *out = g_static_addr[dev];
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_decode_partial_static(const void* q_absorbed, const void* q_pe, const void* ckv_cache,
+                                       const void* kpe_cache, const int32_t* block_table,
+                                       const int32_t* context_lens, float scale, int32_t num_partitions,
+                                       float* partials, float* lse, const mla_decode_desc_t* d) {
+  if (d == nullptr) return reject(MLA_ERR_INVALID_ARG);
+  mla_decode_desc_t dd = *d;
+  dd.workspace = nullptr;
+  dd.workspace_bytes = 0;
+  if (dd.clusters_per_chunk > 1) {
+    const int64_t N = (dd.chunks == nullptr) ? static_cast<int64_t>(dd.num_requests) * num_partitions
+                                             : static_cast<int64_t>(dd.num_chunks);
+    if (N < 1 || N > 65535) return reject(MLA_ERR_INVALID_ARG);
+    const uint64_t need = mla_workspace_bytes(static_cast<int32_t>(N), dd.clusters_per_chunk, dd.q_len, dd.num_heads);
+    if (need == 0 || need > MLA_STATIC_WORKSPACE_BYTES) return reject(MLA_ERR_CAPACITY);
+    void* ws = nullptr;
+    const mla_status_t st = static_workspace(&ws);
+    if (st != MLA_OK) return st;
+    dd.workspace = ws;
+    dd.workspace_bytes = MLA_STATIC_WORKSPACE_BYTES;
+  }
+  return mla_decode_partial(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale, num_partitions,
+                            partials, lse, &dd);
+}
+
 uint64_t mla_workspace_bytes(int32_t num_chunks, int32_t clusters_per_chunk, int32_t q_len, int32_t num_heads) {
   if (clusters_per_chunk <= 1 || num_chunks < 1 || q_len < 1 || num_heads < 1) return 0;
   const uint64_t n = static_cast<uint64_t>(num_chunks), k = static_cast<uint64_t>(clusters_per_chunk);
