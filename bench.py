@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-ctx", type=int, default=0,
                     help="profiling case: only --launches plain layer calls at this context (of the sweep), then exit")
+    ap.add_argument("--profile-many-heads", action="store_true",
+                    help="profiling case: only --launches plain layer calls of the many-head workload, then exit")
     ap.add_argument("--launches", type=int, default=5)
     return ap.parse_args()
 
@@ -126,6 +128,39 @@ def make_case(i, L):
 
 def make_cases():
     return [make_case(i, L) for i, L in enumerate(CONTEXTS)]
+
+
+# many-head decode (the tensor-core-bound shape): B=8, H=128, bf16, block 64, contexts uniform in
+# [4096, 65536] from the seed, latents N(0, 0.5), partitions planned per request
+MH_B, MH_H, MH_BS, MH_SEED = 8, 128, 64, 4
+MANY_HEADS = "mla_decode_B8_H128_bf16_bs64_ctx_U4K_64K"
+
+
+def make_many_heads_case():
+    from mla_split_kv_gb300 import inputs as gen
+
+    lens = gen.uniform_lengths(MH_SEED, MH_B, 4096, 65536)
+    return gen.make_decode_case(MH_SEED, lens, num_heads=MH_H, block_size=MH_BS, dtype="bf16", latent_std=0.5)
+
+
+def many_heads_call(nb, rt, torch, stream=None):
+    """Upload the many-head case, plan it, and return a closure doing one layer call (partial + merge)."""
+    case = make_many_heads_case()
+    dev = nb.mla_device_query()
+    plan = nb.mla_plan(case.context_lens.tolist(), MH_H, 1, MH_BS, dev, max_partitions=64, dtype="bf16")
+    dc = rt.upload(case)
+    chunks_dev = rt.chunks_to_device(plan.chunks)
+    part, lse = rt.alloc_partials(plan.num_chunks, 1, MH_H)
+    ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
+    out = torch.empty((MH_B, 1, MH_H, 512), dtype=torch.bfloat16, device="cuda")
+    desc = rt.make_desc(dc, chunks_dev, nb.MLA_KERNEL_TC, plan.cluster_ctas, stream)
+
+    def call():
+        rt.decode_partial(dc, part, lse, desc=desc)
+        rt.merge_states(part, lse, ind, MH_B, 1, MH_H, "bf16", out=out, stream=stream)
+
+    tokens = int(case.context_lens.sum())
+    return call, plan, tokens
 
 
 def oracle_timing(cases, steps, cores, budget_s=30.0):
@@ -244,6 +279,21 @@ def profiled_traffic(tokens_per_launch):
     return None if bpt is None else round(bpt * tokens_per_launch)
 
 
+def max_over_ranks(value, device):
+    """The largest of one float over all ranks (the job's time is its slowest rank's)."""
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_call(max_ms, calls_per_rank, world):
+    """Whole-job figure: every rank replays the same calls (replicas), so the job did world x calls in the
+    slowest rank's time."""
+    return max_ms * 1e3 / (calls_per_rank * world)
+
+
 def partial_kernel_name(kernel, plans):
     """The partial kernel the library dispatches for this workload (16 fp16 rows per CTA)."""
     if kernel == "simt":
@@ -288,6 +338,52 @@ def run_profile_case(args):
                       "device_status": st, "device_error": code}))
     if st != nb.MLA_OK:
         raise SystemExit(1)
+
+
+def run_profile_many_heads(args):
+    import torch
+
+    from mla_split_kv_gb300 import binding as nb
+    from mla_split_kv_gb300 import build as nbuild
+    from mla_split_kv_gb300 import runtime as rt
+
+    nbuild.build()
+    nb.load()
+    call, plan, tokens = many_heads_call(nb, rt, torch)
+    for _ in range(args.launches):
+        call()
+    torch.cuda.synchronize()
+    st, code = nb.mla_check_device_errors(None)
+    print(json.dumps({"profile": MANY_HEADS, "launches": args.launches, "partitions": plan.num_chunks,
+                      "cluster": plan.cluster_ctas, "tokens": tokens, "device_status": st, "device_error": code}))
+    if st != nb.MLA_OK:
+        raise SystemExit(1)
+
+
+def time_many_heads(nb, rt, torch, stream, reps=20):
+    """Device time of one many-head layer call (graph of `reps` calls, CUDA events), and its flop rate."""
+    with torch.cuda.stream(stream):
+        call, plan, tokens = many_heads_call(nb, rt, torch, stream)
+        for _ in range(3):
+            call()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(reps):
+            call()
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(stream):
+        g.replay()
+        e[0].record(stream)
+        g.replay()
+        e[1].record(stream)
+    stream.synchronize()
+    us = e[0].elapsed_time(e[1]) * 1e3 / reps
+    flops = tokens * MH_H * 2 * (576 + 512)
+    return {"workload": MANY_HEADS, "us_per_call": round(us, 3), "partitions": plan.num_chunks,
+            "cluster": plan.cluster_ctas, "tokens": tokens, "tflops": round(flops / (us * 1e-6) / 1e12, 1),
+            "hbm_gbs": round(tokens * LATENT_BYTES_PER_TOKEN / (us * 1e-6) / 1e9, 1),
+            "note": "a parity workload timed beside the headline one; repeats of one cache (323 MB, > L2)"}
 
 
 def run_ours(args, rank, world):
@@ -389,9 +485,7 @@ def run_ours(args, rank, world):
     total_ms = ev[0].elapsed_time(ev[1]) / reps  # per K steps
     part_ms_all = ev[1].elapsed_time(ev[2]) / reps
     if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, "cuda")
     st, code = nb.mla_check_device_errors(stream.cuda_stream)
     if st != nb.MLA_OK:
         raise RuntimeError(f"device error word {code:#x} in the timed region")
@@ -474,8 +568,13 @@ def run_ours(args, rank, world):
         print(f"WARNING: path counters {ctr} disagree with {expect} launches of the {args.kernel} kernel",
               file=sys.stderr)
 
+    many_heads = time_many_heads(nb, rt, torch, stream)
+    st, code = nb.mla_check_device_errors(stream.cuda_stream)
+    if st != nb.MLA_OK:
+        raise RuntimeError(f"device error word {code:#x} in the many-head timing")
+
     n_calls = K * len(calls)
-    value_us = total_ms * 1e3 / (n_calls * world)
+    value_us = job_us_per_call(total_ms, n_calls, world)
     achieved = part_bytes_all / (part_ms_all * 1e-3) / 1e9
     peaks = measured_peaks()
     if peaks and peaks.get("hbm_gbs"):
@@ -501,6 +600,7 @@ def run_ours(args, rank, world):
                    "timing": "CUDA graph per step (6 layer calls), CUDA events on the launching stream; "
                              "roofline from a graph of the 6 partial launches"},
         "per_ctx": per_ctx,
+        "many_heads": many_heads,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(sum(CONTEXTS) / len(CONTEXTS)),
@@ -547,6 +647,9 @@ def main():
     args = parse()
     if args.profile_ctx:
         run_profile_case(args)
+        return
+    if args.profile_many_heads:
+        run_profile_many_heads(args)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
