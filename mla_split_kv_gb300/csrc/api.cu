@@ -191,7 +191,9 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   const bool use_simt = (d->kernel == MLA_KERNEL_SIMT);
   const bool bf16 = (d->dtype == MLA_BF16);
   const int rows_total = d->num_heads * d->q_len;
-  const int nr = use_simt ? mla::simt_rows_per_cta() : mla::tc_rows_per_cta(rows_total, bf16);
+  // 128 rows on the tensor-core path: one CTA pair holds all of them (a cluster of 2 by default)
+  const bool mh = !use_simt && mla::mh_supports(rows_total, C0 ? C0 : 2);
+  const int nr = use_simt ? mla::simt_rows_per_cta() : (mh ? rows_total : mla::tc_rows_per_cta(rows_total, bf16));
   const int64_t groups = (rows_total + nr - 1) / nr;
   const int32_t subs = (d->clusters_per_chunk > 1) ? d->clusters_per_chunk : 1;
   if (subs > 1) {  // a partition spread over several clusters: the paired kernel with a workspace
@@ -202,7 +204,7 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
       return reject(MLA_ERR_INVALID_ARG);
     if (N * subs > 65535) return reject(MLA_ERR_UNSUPPORTED);
   }
-  const int C = C0 ? C0 : default_cluster(N * groups);
+  const int C = C0 ? C0 : (mh ? 2 : default_cluster(N * groups));
 
   CUtensorMap tm_ckv, tm_kpe, tm_pages;
   if (!tensor_map(&tm_ckv, ckv_cache, rows, mla::kRank, d->block_size, d->dtype) ||
@@ -354,11 +356,11 @@ mla_status_t mla_merge_states(const float* partials, const float* lse, const int
 
 mla_status_t mla_check_device_errors(void* stream, uint32_t* code_out) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
-  uint32_t a = 0, b = 0, c = 0;
+  uint32_t a = 0, b = 0, c = 0, e = 0;
   if (mla::simt_read_clear_error(&a) != cudaSuccess || mla::tc_read_clear_error(&b) != cudaSuccess ||
-      mla::tc128_read_clear_error(&c) != cudaSuccess)
+      mla::tc128_read_clear_error(&c) != cudaSuccess || mla::mh_read_clear_error(&e) != cudaSuccess)
     return MLA_ERR_CUDA;
-  const uint32_t code = a | b | c;
+  const uint32_t code = a | b | c | e;
   if (code_out != nullptr) *code_out = code;
   if (code & mla::MLA_DEVERR_TIMEOUT) return MLA_ERR_TIMEOUT;
   if (code != 0) return MLA_ERR_DEVICE_CHECK;

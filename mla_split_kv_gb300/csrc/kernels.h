@@ -68,6 +68,11 @@ bool tc128_supports(int total_rows, bool bf16, int cluster);
 cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe, const PartialParams& p,
                                  int num_chunks, int cluster, cudaStream_t stream);
 int tc128_max_active_clusters(int cluster);
+// 64-token-tile tensor-core kernel for 128 rows (q_len * H == 128), fp16 or bf16,
+// on clusters of one CTA pair that split the latent columns.
+bool mh_supports(int total_rows, int cluster);
+cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe, const PartialParams& p,
+                              int num_chunks, bool bf16, cudaStream_t stream);
 
 // Query rows per CTA for q_len x H rows (SIMT: always 16).
 int simt_rows_per_cta();
@@ -78,5 +83,6 @@ int tc_max_active_clusters(int cluster, int rows_per_cta, bool bf16);
 cudaError_t simt_read_clear_error(uint32_t* out);
 cudaError_t tc_read_clear_error(uint32_t* out);
 cudaError_t tc128_read_clear_error(uint32_t* out);
+cudaError_t mh_read_clear_error(uint32_t* out);
 
 }  // namespace mla

@@ -1,0 +1,581 @@
+// Tensor-core partial-decode kernel for 128 query rows (the heads of a
+// many-head decode, e.g. H=128 with one query token), on a pair of CTAs,
+// sm_103a.
+//
+// The operation is the one of the other partial kernels ("feat(core):
+// matrix-absorbed MLA decode over a compressed-latent KV cache", *What
+// changed*: SDPA(q_absorbed, ckv, ckv, scale, mask = scale * q_pe @ kpe^T),
+// each chunk yielding a normalized partial and its log2 LSE).
+//
+// With 128 rows sharing each latent tile the two products are dense enough to
+// keep the rows on the MMA's M side:
+//   S[row, tok]  = Q[row, :] . [ckv | kpe][tok, :]        M=128 rows, N=64 tokens
+//   O[row, d]   += P[row, tok] . ckv[tok, d]              M=128 rows, N=256 columns, K=64
+// O for 128 rows x 512 columns would fill all of tensor memory, so the two
+// CTAs of a cluster pair split the latent columns: CTA `half` holds ckv
+// columns [256 half, 256 half + 256) (and the kpe box, of whose 4 16-column
+// K steps it uses 2) and accumulates O for those columns. Each computes S
+// over its columns, stages it (128 x 64 fp32, 32 KB) in its shared memory
+// and sends it into the peer's with one bulk copy completing on the peer's
+// mbarrier (one copy instead of 2048 16-byte remote stores), and adds the
+// peer's part in a fixed order, so both hold the same scores and take the
+// same decisions.
+//
+// S lands in TMEM with row r in lane r, so softmax thread r owns row r: its
+// running max and sum are thread-local (no cross-thread reduction). It writes
+// the probabilities back into TMEM in the same lane, packed two 16-bit values
+// per column, where the PV MMA reads them as its A operand; V (B operand) is
+// the same shared-memory tile read N-major. With bf16 inputs P is carried as
+// two bf16 terms (hi + lo, two MMAs per step), as in the other kernels.
+//
+// TMEM: O 256 columns, S 2 x 64, P 2 x (32 + 32) = 512. Shared memory: Q (5
+// swizzled [128 x 64] chunks, 80 KB), two 64-token tile slots of 40 KB (the
+// ckv half as one 4D TMA box per page: row groups of four [8 x 64] atoms,
+// group g and block c at 4096 g + 1024 c; the kpe box), this CTA's and the
+// peer's partial S (32 KB each): 226 KB.
+//
+// Warp roles (256 threads): warps 0-3 softmax (thread = row) and epilogue,
+// warp 4 TMEM owner + MMA issuer, warps 5-7 page producers.
+#include "device_common.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kT = 64;                            // tokens per tile
+constexpr int kRows = 128;                        // query rows (M)
+constexpr int kHalfBoxes = 4;                     // ckv column blocks per CTA: 256 columns
+constexpr int kHalfCols = kHalfBoxes * kBoxCols;  // 256
+constexpr int kGroupBytes = 8 * kHalfCols * 2;    // 4 KB: one 8-token group of the four blocks
+constexpr int kCkvBytes = kT * kHalfCols * 2;     // 32 KB
+constexpr int kKpeBytes = kT * 128;               // 8 KB
+constexpr int kTileSlot = kCkvBytes + kKpeBytes;  // 40 KB
+constexpr int kQChunk = kRows * 128;              // 16 KB: [128 rows x 64 columns], swizzled
+constexpr int kPageWarps = 3;                     // 8 warps in all: two per scheduler, so up to 255 registers
+constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = (5 + kPageWarps) * 32;   // 256
+constexpr float kRescaleTau = 8.0f;
+
+constexpr uint32_t kOffQ = 0;                             // 80 KB
+constexpr uint32_t kOffTile = 5 * kQChunk;                // 80 KB: 2 tile slots
+constexpr uint32_t kOffX = kOffTile + 2 * kTileSlot;      // 160 KB: the peer's partial S
+constexpr uint32_t kXBytes = kRows * kT * 4;              // [128 rows][64 tokens] fp32: 32 KB
+constexpr uint32_t kOffXS = kOffX + kXBytes;              // 192 KB: this CTA's partial S, sent as one copy
+constexpr uint32_t kOffSmall = kOffXS + kXBytes;          // 224 KB
+constexpr uint32_t kSmem = kOffSmall + 1024 + 1024;       // + alignment slack
+static_assert(kSmem <= 232448, "shared memory per CTA");
+
+constexpr uint32_t kTmemO = 0;      // O [128 x 256] fp32
+constexpr uint32_t kTmemS = 256;    // S [128 x 64] fp32, 2 buffers
+constexpr uint32_t kTmemP = 384;    // P [128 x 64] 16-bit, hi and lo (32 columns each), 2 buffers
+constexpr uint32_t kTmemCols = 512;
+
+struct Small {
+  uint64_t full[2], empty[2], sfull[2], sfree[2], ppfull[2], pvdone[2], xfull, xempty, drain;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+static_assert(sizeof(Small) <= 1024, "small smem region");
+
+__device__ __forceinline__ uint32_t tmem_lane_base(int warp) { return static_cast<uint32_t>(32 * (warp & 3)) << 16; }
+
+// two values rounded to 16 bits in one conversion: a in the low half, b in the high half
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (BF16) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  } else {
+    const __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
+}
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_partial_mh_kernel(const __grid_constant__ CUtensorMap tm_pages, const __grid_constant__ CUtensorMap tm_kpe,
+                          const PartialParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* qs = smem + kOffQ;
+  float* xs = reinterpret_cast<float*>(smem + kOffX);
+  float* xsend = reinterpret_cast<float*>(smem + kOffXS);
+  Small* sm = reinterpret_cast<Small*>(smem + kOffSmall);
+  volatile int32_t* abort_flag = &sm->abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
+  const int half = static_cast<int>(rank & 1u);
+  const CtaWork w = cta_work(p, kRows, kT, 0, 1);  // both CTAs of the pair take the whole chunk
+  const int ntiles = (w.sub1 - w.sub0 + kT - 1) / kT;
+  const int rows_total = p.q_len * p.H;
+
+  if (tid == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm->full[t], kPageWarps);  // one expect_tx arrival per producer warp
+      mbar_init(&sm->empty[t], 1);
+      mbar_init(&sm->sfull[t], 1);
+      mbar_init(&sm->sfree[t], 4);
+      mbar_init(&sm->ppfull[t], 4);
+      mbar_init(&sm->pvdone[t], 1);
+    }
+    mbar_init(&sm->xfull, 1);   // local expect_tx arrival + the peer's st.async bytes
+    mbar_init(&sm->xempty, 4);  // one remote arrival per peer softmax warp
+    mbar_init(&sm->drain, 1);
+    mbar_arrive_expect_tx(&sm->xfull, kXBytes);  // tile 0
+    sm->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(&sm->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_arrive_release();  // the peer touches this CTA's barriers only after this cluster phase
+  const uint32_t tmem = sm->tmem_base;
+
+  if (warp >= 5) {
+    // ------------------------------------------------------------------ producers
+    const int k0 = warp - 5;  // this warp loads pages k0, k0 + 3, ... of each tile (at most 2: 4 pages of 16)
+    const uint64_t pol = l2_policy_evict_first();
+    uint64_t tmo = p.timeout_ns;
+    asm volatile("" : "+l"(tmo));
+    const int npages_req = (w.L + p.bs - 1) / p.bs;
+    int win_base = -1, win_pid = -1;
+    auto page_of = [&](int pg) -> int {  // warp-uniform pg
+      const int base = pg & ~31;
+      if (base != win_base) {
+        win_base = base;
+        const int q = base + lane;
+        win_pid = (q < npages_req && q < p.max_blocks) ? checked_page(p, w.b, q) : -1;
+      }
+      return __shfl_sync(0xffffffffu, win_pid, pg & 31);
+    };
+    auto tile_pages = [&](int i, int* pg0, int* npg) {
+      const int tok0 = w.sub0 + i * kT;
+      *pg0 = tok0 / p.bs;
+      *npg = (min(kT, w.sub1 - tok0) + p.bs - 1) / p.bs;
+    };
+    int issued = -1;
+    for (int i = 0; i < ntiles; ++i) {
+      const int t = i & 1;
+      if (i >= 2) {  // PV(i-2) released the slot
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait(&sm->empty[t], ((i >> 1) - 1) & 1, tmo) && !*abort_flag;
+          if (!ok) *abort_flag = 1;
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
+      int pg0, npg;
+      tile_pages(i, &pg0, &npg);
+      const int mine = (npg > k0) ? (npg - k0 + kPageWarps - 1) / kPageWarps : 0;  // at most 2 (bs >= 16)
+      int pids[2];
+#pragma unroll
+      for (int m = 0; m < 2; ++m) pids[m] = (m < mine) ? page_of(pg0 + k0 + m * kPageWarps) : -1;
+      if (lane == 0) {
+        uint8_t* slot = smem + kOffTile + t * kTileSlot;
+        mbar_arrive_expect_tx(&sm->full[t], static_cast<uint32_t>(mine * p.bs * (kHalfCols * 2 + 128)));
+        for (int m = 0; m < mine; ++m) {
+          const int j = k0 + m * kPageWarps;
+          tma_load_4d(slot + j * p.bs * (kHalfCols * 2), &tm_pages, 0, 0, kHalfBoxes * half, pids[m] * (p.bs / 8),
+                      &sm->full[t], pol);
+          tma_load_2d(slot + kCkvBytes + j * p.bs * 128, &tm_kpe, 0, pids[m] * p.bs, &sm->full[t], pol);
+        }
+      }
+      issued = i;
+      if (i + 2 < ntiles) {  // the same page of tile i+2 into L2: ckv by the even CTA, kpe by the odd one
+        int qg0, qn;
+        tile_pages(i + 2, &qg0, &qn);
+        for (int j = k0; j < qn; j += kPageWarps) {
+          const int qpid = page_of(qg0 + j);
+          if (lane == 0 && qpid >= 0) {
+            const long long row = static_cast<long long>(qpid) * p.bs;
+            if (half == 0)
+              bulk_prefetch_l2(p.ckv + row * (kRank * 2), static_cast<uint32_t>(p.bs * kRank * 2));
+            else
+              bulk_prefetch_l2(p.kpe + row * (kRope * 2), static_cast<uint32_t>(p.bs * kRope * 2));
+          }
+        }
+      }
+    }
+    if (lane == 0 && *abort_flag && issued >= 0) mbar_wait(&sm->full[issued & 1], (issued >> 1) & 1, kDrainTimeoutNs);
+    cluster_wait_acquire();
+  } else if (warp == 4) {
+    // ------------------------------------------------------------------ MMA issuer
+    const uint32_t idesc_s = idesc_f16_f32(kRows, kT, BF16, false, false);         // A = Q, B = K tile
+    const uint32_t idesc_o = idesc_f16_f32(kRows, kHalfCols, BF16, false, true);   // A = P (TMEM), B = V N-major
+    const uint32_t q_base = smem_u32(qs);
+    const uint32_t tile_base = smem_u32(smem + kOffTile);
+    uint64_t tmo = p.timeout_ns;
+    asm volatile("" : "+l"(tmo));
+    auto wait_lane0 = [&](uint64_t* bar, uint32_t parity) -> bool {
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait(bar, parity, tmo) && !*abort_flag;
+        if (!ok) *abort_flag = 1;
+      }
+      return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    };
+    auto score = [&](int i) -> bool {
+      const int t = i & 1;
+      if (i >= 2 && !wait_lane0(&sm->sfree[t], ((i >> 1) - 1) & 1)) return false;
+      if (!wait_lane0(&sm->full[t], (i >> 1) & 1)) return false;
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t slot = tile_base + t * kTileSlot;
+        const uint32_t d = tmem + kTmemS + t * kT;
+#pragma unroll
+        for (int c = 0; c < kHalfBoxes; ++c) {
+          const uint64_t qd = smem_desc_sw128(q_base + c * kQChunk, 16, 1024);
+          const uint64_t kd = smem_desc_sw128(slot + c * 1024, 16, kGroupBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_f16_ss(d, desc_add(qd, kk * 32), desc_add(kd, kk * 32), idesc_s, (c == 0 && kk == 0) ? 0u : 1u);
+        }
+        const uint64_t qd = smem_desc_sw128(q_base + kHalfBoxes * kQChunk, 16, 1024);
+        const uint64_t kd = smem_desc_sw128(slot + kCkvBytes, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const uint32_t ks = 2 * half + kk;  // 16-column step of the kpe box
+          umma_f16_ss(d, desc_add(qd, ks * 32), desc_add(kd, ks * 32), idesc_s, 1u);
+        }
+        umma_commit(&sm->sfull[t]);
+      }
+      __syncwarp();
+      return true;
+    };
+    // rows [nvalid, nend) of the ckv part of a slot: zeroed so the V operand stays finite
+    auto zero_rows = [&](uint8_t* ckv, int nvalid, int nend) {
+      for (int x = lane; x < (nend - nvalid) * kHalfBoxes * 8; x += 32) {
+        const int rc = x >> 3, tok = nvalid + rc / kHalfBoxes, c = rc % kHalfBoxes;
+        *reinterpret_cast<uint4*>(ckv + (tok >> 3) * kGroupBytes + c * 1024 + (tok & 7) * 128 + (x & 7) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    auto pv = [&](int i) -> bool {
+      const int t = i & 1;
+      const int nvalid = min(kT, w.sub1 - (w.sub0 + i * kT));
+      if (!wait_lane0(&sm->ppfull[t], (i >> 1) & 1)) return false;
+      const int ksteps = (nvalid + 15) >> 4;
+      if (nvalid < (ksteps << 4)) {
+        zero_rows(smem + kOffTile + t * kTileSlot, nvalid, ksteps << 4);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t slot = tile_base + t * kTileSlot;
+        const uint32_t pa = tmem + kTmemP + t * 64;
+        for (int ks = 0; ks < ksteps; ++ks) {
+          const uint64_t vd = smem_desc_sw128(slot + ks * 2 * kGroupBytes, 1024, kGroupBytes);
+          umma_f16_ts(tmem + kTmemO, pa + ks * 8, vd, idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
+          if (BF16) umma_f16_ts(tmem + kTmemO, pa + 32 + ks * 8, vd, idesc_o, 1u);
+        }
+        umma_commit(&sm->empty[t]);
+        umma_commit(&sm->pvdone[t]);
+      }
+      __syncwarp();
+      return true;
+    };
+    named_bar_sync(2, 160);  // Q staged by the softmax warps
+    bool alive = true;
+    for (int i0 = 0; i0 < ntiles && alive; i0 += 2) {
+      const int i1 = min(i0 + 2, ntiles);
+      for (int i = i0; i < i1 && alive; ++i) alive = score(i);
+      for (int i = i0; i < i1 && alive; ++i) alive = pv(i);
+    }
+    if (lane == 0) {  // every MMA issued so far has completed before TMEM is read or freed
+      umma_commit(&sm->drain);
+      mbar_wait(&sm->drain, 0, kDrainTimeoutNs);
+    }
+    __syncwarp();
+    cluster_wait_acquire();
+  } else {
+    // ------------------------------------------------------------------ softmax (warps 0-3): thread = row
+    // Q: this CTA's 256 latent columns, then the 64 kpe columns; 128 rows, K-major, 5 swizzled chunks
+    // (all the 16-byte copies in flight at once; rows past the request's zero-filled)
+    for (int idx = tid; idx < kRows * 40; idx += kSoftmaxThreads) {
+      const int r = idx / 40, k = (idx % 40) * 8;
+      const bool in = r < w.nrows;
+      const long long row = static_cast<long long>(w.b) * rows_total + w.row0 + (in ? r : 0);
+      const uint16_t* src = (k < kHalfCols) ? p.q_abs + row * kRank + kHalfCols * half + k
+                                            : p.q_pe + row * kRope + (k - kHalfCols);
+      cp_async16(qs + (k / kBoxCols) * kQChunk + sw128_offset(r, k % kBoxCols), src, in ? 16u : 0u);
+    }
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    named_bar_arrive(2, 160);
+    cluster_wait_acquire();  // the peer's barriers are initialised
+
+    float scale_log2 = p.scale_log2;
+    uint64_t tmo = p.timeout_ns;
+    asm volatile("" : "+f"(scale_log2), "+l"(tmo));
+    const int r = tid;  // query row of this thread (TMEM lane r)
+    const uint32_t lane_base = tmem_lane_base(warp);
+    // visible tokens of this row: t < L, and t <= L - q_len + i under the causal rule
+    const int row_q = (w.row0 + r) / p.H;
+    // end of the tokens this row sees in this CTA's range: the chunk end, and the causal limit
+    const int tlim = min(w.sub1, p.causal ? (w.L - p.q_len + row_q + 1) : w.L);
+    const uint32_t xsw = static_cast<uint32_t>(r & 15);
+    const uint32_t peer_x = dsmem_addr(xs, peer);
+    const uint32_t peer_xfull = dsmem_addr(&sm->xfull, peer);
+    const uint32_t peer_xempty = dsmem_addr(&sm->xempty, peer);
+    const float4* xrow = reinterpret_cast<const float4*>(xs + r * kT);
+    float4* srow = reinterpret_cast<float4*>(xsend + r * kT);
+    float m_r = -INFINITY, l_r = 0.f;
+    const float4* srow_c = srow;
+    // C(j): probabilities of tile j (its scaled scores wait in its P buffer) -> the same buffer (hi, and lo
+    // for bf16), 32 tokens at a time; then PV(j) may run
+    auto probabilities = [&](int j) {
+        const uint32_t pa = tmem + lane_base + kTmemP + (j & 1) * 64;
+        float y[kT];
+        tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < kT / 16; ++q) tmem_ld16(pa + q * 16, y + 16 * q);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          float hw[16], lw[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = 32 * q + 2 * j;
+            const float p0 = (y[t] == -INFINITY) ? 0.f : exp2f(y[t] - m_r);
+            const float p1 = (y[t + 1] == -INFINITY) ? 0.f : exp2f(y[t + 1] - m_r);
+            const uint32_t h = pack2<BF16>(p0, p1);  // one paired conversion, element t in the low half
+            hw[j] = __uint_as_float(h);
+            const float h0 = h2f<BF16>(static_cast<uint16_t>(h & 0xffffu));
+            const float h1 = h2f<BF16>(static_cast<uint16_t>(h >> 16));
+            if (BF16) {
+              const uint32_t l = pack2<BF16>(p0 - h0, p1 - h1);
+              lw[j] = __uint_as_float(l);
+              l_r += (h0 + h2f<BF16>(static_cast<uint16_t>(l & 0xffffu))) +
+                     (h1 + h2f<BF16>(static_cast<uint16_t>(l >> 16)));
+            } else {
+              l_r += h0 + h1;
+            }
+          }
+          tmem_st16(pa + q * 16, hw);
+          if (BF16) tmem_st16(pa + 32 + q * 16, lw);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->ppfull[j & 1]);
+    };
+    // Software pipeline over tiles: iteration i sends tile i's partial scores (A), computes the
+    // probabilities of tile i-1 while that copy is in flight (C), then finishes tile i's scores (B).
+    // Between B(i) and C(i) the scaled scores of tile i wait in tile i's P buffer in tensor memory
+    // (64 fp32 columns), which C(i) then overwrites with the packed probabilities.
+    for (int i = 0; i <= ntiles; ++i) {
+      const bool cur = i < ntiles;
+      const int buf = i & 1;
+      int ok = 1;
+      // C(i-1) is done while tile i's copy is in flight; but first, if tile i's scores are not ready
+      // (the MMA warp may be waiting for PV(i-1), which needs C(i-1)), right away
+      bool c_done = (i == 0);
+      if (!c_done) {
+        int ready = 0;
+        if (cur && lane == 0) ready = mbar_test(&sm->sfull[buf], (i >> 1) & 1) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, ready, 0)) {
+          probabilities(i - 1);
+          c_done = true;
+        }
+      }
+      // ---- A(i): this CTA's partial S of tile i -> send buffer -> one copy into the peer
+      if (cur) {
+        if (lane == 0) ok = mbar_wait(&sm->sfull[buf], (i >> 1) & 1, tmo);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        float x[kT];
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < kT / 16; ++q) tmem_ld16(tmem + lane_base + kTmemS + buf * kT + q * 16, x + 16 * q);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm->sfree[buf]);
+          // the peer has read tile i-1's scores (so the copy out of the send buffer is finished too)
+          if (i >= 1) ok = mbar_wait_cluster(&sm->xempty, (i - 1) & 1, tmo);
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+#pragma unroll
+          for (int c = 0; c < kT / 4; ++c)
+            srow[c ^ xsw] = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+          fence_proxy_async_smem();
+        }
+      }
+      if (named_bar_sync_or(1, 128, !ok || *abort_flag != 0)) {
+        *abort_flag = 1;
+        break;
+      }
+      if (cur && tid == 0) dsmem_bulk_copy(peer_x, xsend, kXBytes, peer_xfull);
+      // ---- C(i-1), when tile i's scores are not ready yet (so it cannot wait on them)
+      if (!c_done) {
+        probabilities(i - 1);
+        c_done = true;
+      }
+      if (!cur) break;
+      // ---- B(i): add the peer's part, scale and mask, lazy rescale, scores -> tile i's P buffer
+      const int tok0 = w.sub0 + i * kT;
+      ok = mbar_wait_cluster(&sm->xfull, i & 1, tmo);
+      ok = __all_sync(0xffffffffu, ok);
+      float x[kT];
+      float mx = -INFINITY;
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < kT / 4; ++c) {
+          const float4 o = srow_c[c ^ xsw];
+          const float4 y = xrow[c ^ xsw];
+          // rank-0 part + rank-1 part, the same sum in both CTAs
+          x[4 * c] = half ? (y.x + o.x) : (o.x + y.x);
+          x[4 * c + 1] = half ? (y.y + o.y) : (o.y + y.y);
+          x[4 * c + 2] = half ? (y.z + o.z) : (o.z + y.z);
+          x[4 * c + 3] = half ? (y.w + o.w) : (o.w + y.w);
+        }
+        __syncwarp();
+        if (lane == 0) {
+          // expect the peer's next tile before letting it send, then free the buffer (the values are
+          // consumed above; a plain signal)
+          if (tid == 0) mbar_arrive_expect_tx(&sm->xfull, kXBytes);
+          mbar_remote_arrive_relaxed(peer_xempty);
+        }
+        const int nvis = min(kT, tlim - tok0);  // tokens of this tile the row can see
+        if (__builtin_expect(nvis < kT, 0)) {
+#pragma unroll
+          for (int t = 0; t < kT; ++t) x[t] = (t < nvis) ? x[t] * scale_log2 : -INFINITY;
+        } else {
+#pragma unroll
+          for (int t = 0; t < kT; ++t) x[t] *= scale_log2;
+        }
+#pragma unroll
+        for (int t = 0; t < kT; ++t) mx = fmaxf(mx, x[t]);
+      }
+      if (named_bar_sync_or(1, 128, !ok || *abort_flag != 0)) {
+        *abort_flag = 1;
+        break;
+      }
+      // lazy rescale of this row (rare): move the reference max and scale O and the sum; PV(i-1)
+      // (its probabilities were written in C(i-1) above) must be complete before O is rescaled
+      const bool need = mx > m_r + kRescaleTau;
+      if (__builtin_expect(__any_sync(0xffffffffu, need), 0)) {
+        const float m_new = need ? fmaxf(m_r, mx) : m_r;
+        const float alpha = need ? ((m_r == -INFINITY) ? 0.f : exp2f(m_r - m_new)) : 1.f;
+        if (i >= 1) {
+          int ok2 = 1;
+          if (lane == 0) ok2 = mbar_wait(&sm->pvdone[(i - 1) & 1], ((i - 1) >> 1) & 1, tmo);
+          if (__shfl_sync(0xffffffffu, ok2, 0)) {
+            tc_fence_after();
+            for (int q = 0; q < kHalfCols / 16; ++q) {
+              float v[16];
+              const uint32_t a = tmem + lane_base + kTmemO + q * 16;
+              tmem_ld16(a, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) v[jj] *= alpha;
+              tmem_st16(a, v);
+            }
+            tmem_wait_st();
+          } else if (lane == 0) {
+            *abort_flag = 1;
+          }
+        }
+        l_r *= alpha;
+        m_r = m_new;
+      }
+      // tile i's P buffer was last read by PV(i-2)
+      if (i >= 2) {
+        int ok3 = 1;
+        if (lane == 0) ok3 = mbar_wait(&sm->pvdone[buf], ((i >> 1) - 1) & 1, tmo);
+        if (!__shfl_sync(0xffffffffu, ok3, 0) && lane == 0) *abort_flag = 1;
+      }
+      {
+        const uint32_t pa = tmem + lane_base + kTmemP + buf * 64;
+#pragma unroll
+        for (int q = 0; q < kT / 16; ++q) tmem_st16(pa + q * 16, x + 16 * q);
+        tmem_wait_st();
+      }
+    }
+    const bool aborted = named_bar_sync_or(1, 128, *abort_flag != 0);
+    if (ntiles > 0 && !aborted) {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&sm->pvdone[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, tmo);
+      if (!__shfl_sync(0xffffffffu, ok, 0) && lane == 0) *abort_flag = 1;
+    }
+    const bool read_o = (ntiles > 0) && !named_bar_sync_or(1, 128, *abort_flag != 0);  // uniform
+    // epilogue: the normalized partial of this row over this CTA's 256 columns, and the LSE (rank 0)
+    const bool has_mass = read_o && (r < w.nrows) && (m_r != -INFINITY) && (l_r > 0.f);
+    const float inv = has_mass ? 1.f / l_r : 0.f;
+    const long long orow = static_cast<long long>(w.slot) * rows_total + w.row0 + r;
+    if (read_o) tc_fence_after();
+    for (int q = 0; q < kHalfCols / 16; ++q) {
+      float v[16];
+      if (read_o) {
+        tmem_ld16(tmem + lane_base + kTmemO + q * 16, v);
+        tmem_wait_ld();
+      }
+      if (r < w.nrows) {
+        float4* dst = reinterpret_cast<float4*>(p.partials + orow * kRank + kHalfCols * half + q * 16);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dst[j] = has_mass ? make_float4(v[4 * j] * inv, v[4 * j + 1] * inv, v[4 * j + 2] * inv, v[4 * j + 3] * inv)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    if (rank == 0 && r < w.nrows) p.lse[orow] = has_mass ? m_r + log2f(l_r) : -INFINITY;
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer is done with this CTA's shared memory
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <bool BF16>
+cudaError_t prepare_mh() {
+  static bool done = false;
+  if (done) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&mla_partial_mh_kernel<BF16>),
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
+}  // namespace
+
+bool mh_supports(int total_rows, int cluster) { return total_rows == kRows && cluster == 2; }
+
+cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe, const PartialParams& p,
+                              int num_chunks, bool bf16, cudaStream_t stream) {
+  cudaError_t e = bf16 ? prepare_mh<true>() : prepare_mh<false>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, num_chunks, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return bf16 ? cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<true>, tm_pages, tm_kpe, p)
+              : cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<false>, tm_pages, tm_kpe, p);
+}
+
+cudaError_t mh_read_clear_error(uint32_t* out) {
+  uint32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_device_error, sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(uint32_t));
+}
+
+}  // namespace mla

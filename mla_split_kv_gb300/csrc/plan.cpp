@@ -81,7 +81,9 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
   if (maxP < 1 || maxP > 1024) return MLA_ERR_INVALID_ARG;
 
   const int rows = num_heads * q_len;
-  const int nr = mla::tc_rows_per_cta(rows, plan->dtype == MLA_BF16);
+  // 128 rows: one CTA pair (a cluster of 2) holds all of them
+  const bool many_rows = mla::mh_supports(rows, 2);
+  const int nr = many_rows ? rows : mla::tc_rows_per_cta(rows, plan->dtype == MLA_BF16);
   const int64_t row_groups = (rows + nr - 1) / nr;
 
   int64_t split_tokens = 0, n_split = 0;
@@ -99,6 +101,7 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
     const int64_t slots = dev->max_clusters[k];
     if (slots <= 0) continue;
     if (paired_single && C == 1) continue;  // the paired kernel needs a pair of CTAs
+    if (many_rows && C != 2) continue;      // the 128-row kernel runs on one pair
     Candidate cand;
     cand.cluster = C;
     cand.parts.assign(B, 1);

@@ -245,6 +245,28 @@ def test_spread_partitions_bitwise_reproducible_and_workspace_reused():
     assert int(tickets.abs().sum()) == 0
 
 
+@pytest.mark.parametrize("H,q_len,dtype,bs,lens,causal", [
+    (128, 1, "bf16", 64, [5000, 777], False),
+    (128, 1, "f16", 32, [4096], False),
+    (128, 1, "bf16", 16, [2049, 130], False),
+    (64, 2, "bf16", 32, [3000, 1500], True),
+])
+def test_many_rows_pair_kernel_partials(H, q_len, dtype, bs, lens, causal):
+    """128 rows per CTA pair (rows on M, P in tensor memory): per-chunk partials against the oracle."""
+    case = gen.make_decode_case(9, lens, num_heads=H, q_len=q_len, block_size=bs, dtype=dtype, latent_std=0.5,
+                                causal=causal)
+    P = 3
+    nb.mla_reset_counters()
+    part, lse, out, ind, dc = run_uniform(case, P, nb.MLA_KERNEL_TC, cluster=2)
+    assert nb.mla_get_counters()[nb.CTR_CTAS] == len(lens) * P * 2  # one pair per chunk, all rows
+    chunks, _ = oracle_uniform_chunks(case, P)
+    ref_part, ref_lse = orc.partials(case, chunks)
+    assert_close(part.cpu().numpy(), ref_part, f"partials H={H} q={q_len} {dtype} bs={bs}")
+    assert_lse_close(lse.cpu().numpy(), ref_lse, f"lse H={H} q={q_len} {dtype} bs={bs}")
+    ref, _ = orc.unsplit(case)
+    assert_close(out.cpu().numpy(), ref, f"merged H={H} q={q_len} {dtype} bs={bs}")
+
+
 def test_mixed_batch_request_major():
     case = gen.make_decode_case(3, [32768, 20000], num_heads=16, block_size=32, dtype="f16")
     plan, part, lse, out = plan_and_run(case, max_partitions=4)
