@@ -384,6 +384,13 @@ __device__ __forceinline__ float h2f(uint16_t v) {
     return __half2float(__ushort_as_half(v));
   }
 }
+// 2^x with the hardware approximation (PTX ex2.approx.ftz.f32: relative error
+// below 2^-22 per the PTX ISA); 2^-inf = +0, so masked scores need no test.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 template <bool BF16>
 __device__ __forceinline__ uint16_t f2h(float v) {
   if constexpr (BF16) {

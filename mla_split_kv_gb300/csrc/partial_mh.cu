@@ -332,6 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // for bf16), 32 tokens at a time; then PV(j) may run
     auto probabilities = [&](int j) {
         const uint32_t pa = tmem + lane_base + kTmemP + (j & 1) * 64;
+        // a row that has seen no visible token yet has only -inf scores: subtract a finite stand-in
+        const float m_sub = (m_r == -INFINITY) ? 0.f : m_r;
         float y[kT];
         tc_fence_after();
 #pragma unroll
@@ -343,8 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int t = 32 * q + 2 * j;
-            const float p0 = (y[t] == -INFINITY) ? 0.f : exp2f(y[t] - m_r);
-            const float p1 = (y[t + 1] == -INFINITY) ? 0.f : exp2f(y[t + 1] - m_r);
+            const float p0 = fast_exp2(y[t] - m_sub);  // masked scores (-inf) give 0
+            const float p1 = fast_exp2(y[t + 1] - m_sub);
             const uint32_t h = pack2<BF16>(p0, p1);  // one paired conversion, element t in the low half
             hw[j] = __uint_as_float(h);
             const float h0 = h2f<BF16>(static_cast<uint16_t>(h & 0xffffu));

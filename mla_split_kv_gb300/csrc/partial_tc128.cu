@@ -465,7 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* pb = ps + buf * kPBuf + (tl >> 6) * (kNR * 128);
 #pragma unroll
         for (int r = 0; r < kNR; ++r) {
-          const float pr = (x[r] == -INFINITY) ? 0.f : exp2f(x[r] - mr[r]);
+          // masked scores (-inf) give 0; a row with no visible token yet subtracts a finite stand-in
+          const float pr = fast_exp2(x[r] - ((mr[r] == -INFINITY) ? 0.f : mr[r]));
           const uint16_t hv = f2h<false>(pr);
           lsum[r] += h2f<false>(hv);
           *reinterpret_cast<uint16_t*>(pb + sw128_offset(r, tl & 63)) = hv;
