@@ -384,6 +384,14 @@ __device__ __forceinline__ float h2f(uint16_t v) {
     return __half2float(__ushort_as_half(v));
   }
 }
+// Programmatic dependent launch. A grid that calls pdl_launch_dependents lets the
+// next kernel of its stream, when that one is launched with programmatic stream
+// serialization, start before this grid ends; the dependent must call pdl_wait
+// before it touches memory this grid writes: the wait returns once every
+// prerequisite grid has completed and its writes are visible. Without the
+// launch attribute both are no-ops in effect (the dependent starts after the end).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // 2^x with the hardware approximation (PTX ex2.approx.ftz.f32: relative error
 // below 2^-22 per the PTX ISA); 2^-inf = +0, so masked scores need no test.
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -9,6 +9,9 @@
 // result is rounded once to the output dtype.
 //
 // One warp per (request, row, 128-column quarter); each lane owns 4 columns.
+// The kernel is a programmatic dependent launch: it may be scheduled while the
+// partial kernel that precedes it still runs, and waits for that grid before
+// its first read, so its launch latency hides behind the partial kernel's end.
 // The weights are computed lane-parallel (lane s holds partial s), the sum over
 // partials runs in fixed order, so the result is bitwise reproducible.
 #include "device_common.cuh"
@@ -20,6 +23,9 @@ namespace {
 constexpr int kWarps = 8;
 
 __global__ void __launch_bounds__(kWarps * 32) mla_merge_kernel(const MergeParams p) {
+  // Launched as a programmatic dependent of the partial kernel: everything this
+  // kernel reads may still be in flight until the wait returns.
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long gw = static_cast<long long>(blockIdx.x) * kWarps + warp;
   const long long total = static_cast<long long>(p.B) * p.rows * 4;
@@ -31,31 +37,44 @@ __global__ void __launch_bounds__(kWarps * 32) mla_merge_kernel(const MergeParam
   const int lo = p.o_indptr[b], hi = p.o_indptr[b + 1];
   const int n = hi - lo;
 
-  // maximum LSE over this row's partials
-  float M = -INFINITY;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, p.lse[static_cast<long long>(lo + s) * p.rows + row]);
+  // maximum LSE over this row's partials; lane s keeps the LSE of partial s (s < 32)
+  const float l0 = (lane < n) ? p.lse[static_cast<long long>(lo + lane) * p.rows + row] : -INFINITY;
+  float M = l0;
+  for (int s = lane + 32; s < n; s += 32) M = fmaxf(M, p.lse[static_cast<long long>(lo + s) * p.rows + row]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
   if (M != -INFINITY) {
+    const float* col = p.partials + static_cast<long long>(row) * kRank + quarter * 128 + lane * 4;
+    const long long stride = static_cast<long long>(p.rows) * kRank;  // one partial slot
     for (int s0 = 0; s0 < n; s0 += 32) {
       const int cnt = min(32, n - s0);
       float wl = 0.f;
       if (lane < cnt) {
-        const float l = p.lse[static_cast<long long>(lo + s0 + lane) * p.rows + row];
+        const float l = (s0 == 0) ? l0 : p.lse[static_cast<long long>(lo + s0 + lane) * p.rows + row];
         wl = (l == -INFINITY) ? 0.f : exp2f(l - M);
       }
-      for (int j = 0; j < cnt; ++j) {
-        const float wj = __shfl_sync(0xffffffffu, wl, j);
-        const float4 v = *reinterpret_cast<const float4*>(
-            p.partials + (static_cast<long long>(lo + s0 + j) * p.rows + row) * kRank + quarter * 128 + lane * 4);
-        den += wj;
-        acc.x = fmaf(wj, v.x, acc.x);
-        acc.y = fmaf(wj, v.y, acc.y);
-        acc.z = fmaf(wj, v.z, acc.z);
-        acc.w = fmaf(wj, v.w, acc.w);
+      // batches of 8 partials: all loads of a batch in flight at once, then the
+      // weighted sum in partial order
+      for (int j0 = 0; j0 < cnt; j0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+          v[jj] = (j0 + jj < cnt) ? *reinterpret_cast<const float4*>(col + (lo + s0 + j0 + jj) * stride)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const float wj = __shfl_sync(0xffffffffu, wl, (j0 + jj) & 31);
+          if (j0 + jj < cnt) {
+            den += wj;
+            acc.x = fmaf(wj, v[jj].x, acc.x);
+            acc.y = fmaf(wj, v[jj].y, acc.y);
+            acc.z = fmaf(wj, v[jj].z, acc.z);
+            acc.w = fmaf(wj, v[jj].w, acc.w);
+          }
+        }
       }
     }
     acc = make_float4(acc.x / den, acc.y / den, acc.z / den, acc.w / den);
@@ -84,8 +103,17 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   const long long warps = static_cast<long long>(p.B) * p.rows * 4;
   const long long blocks = (warps + kWarps - 1) / kWarps;
   if (blocks <= 0) return cudaSuccess;
-  mla_merge_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_merge_kernel, p);
 }
 
 }  // namespace mla

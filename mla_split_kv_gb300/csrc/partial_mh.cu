@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mla_partial_mh_kernel(const __grid_constant__ CUtensorMap tm_pages, const __grid_constant__ CUtensorMap tm_kpe,
                           const PartialParams p) {
   extern __shared__ uint8_t smem_raw[];
+  pdl_launch_dependents();  // the merge of these partials may be scheduled now; it waits for this grid
   uint8_t* smem = align1024(smem_raw);
   uint8_t* qs = smem + kOffQ;
   float* xs = reinterpret_cast<float*>(smem + kOffX);

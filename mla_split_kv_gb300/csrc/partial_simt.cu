@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mla_partial_simt_kernel(const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
                             const PartialParams p) {
   extern __shared__ uint8_t smem_raw[];
+  pdl_launch_dependents();  // the merge of these partials may be scheduled now; it waits for this grid
   uint8_t* smem = align1024(smem_raw);
   uint8_t* tiles = smem;
   float* qs = reinterpret_cast<float*>(smem + kOffQ);

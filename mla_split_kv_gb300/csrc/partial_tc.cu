@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mla_partial_tc_kernel(const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
                           const PartialParams p) {
   constexpr bool SPLIT = BF16;
+  pdl_launch_dependents();  // the merge of these partials may be scheduled now; it waits for this grid
   using Lay = TcLayout<NR, SPLIT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
