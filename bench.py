@@ -32,7 +32,6 @@ sys.path.insert(0, ROOT)
 CONTEXTS = [32768, 49152, 65536, 81920, 98304, 131072]
 H, BS, DTYPE, SEED = 16, 32, "f16", 2
 LATENT_BYTES_PER_TOKEN = (512 + 64) * 2
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "mla_partial_tc128_kernel_dram_traffic.json")
 WORKLOAD = "mla_decode_ctx_sweep_B1_H16_r512_rope64_fp16_bs32"
 METRIC = "us per MLA decode layer call (mean over ctx 32K-131K), HBM GB/s as fraction of peak"
 
@@ -43,7 +42,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--kernel", default="tc", choices=["tc", "simt"])
+    ap.add_argument("--kernel", default="tc", choices=["tc", "tc_quad", "simt"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-ctx", type=int, default=0,
@@ -262,18 +261,18 @@ def measured_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("partial_tc.cu", "partial_tc128.cu", "device_common.cuh", "kernels.h"):
+    for f in ("partial_tc.cu", "partial_tc128.cu", "partial_quad.cu", "device_common.cuh", "kernels.h"):
         h.update(open(os.path.join(ROOT, "mla_split_kv_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(tokens_per_launch):
+def profiled_traffic(kernel_name, tokens_per_launch):
     """DRAM bytes per launch from the committed ncu summary, if it matches this kernel."""
     try:
-        prof = json.load(open(PROFILE_TRAFFIC))
+        prof = json.load(open(os.path.join(ROOT, "profiles", f"{kernel_name}_dram_traffic.json")))
     except (OSError, ValueError):
         return None
-    if prof.get("kernel_source_hash") != kernel_source_hash():
+    if prof.get("kernel") != kernel_name or prof.get("kernel_source_hash") != kernel_source_hash():
         return None
     bpt = prof.get("dram_bytes_per_token")
     return None if bpt is None else round(bpt * tokens_per_launch)
@@ -298,6 +297,8 @@ def partial_kernel_name(kernel, plans):
     """The partial kernel the library dispatches for this workload (16 fp16 rows per CTA)."""
     if kernel == "simt":
         return "mla_partial_simt_kernel"
+    if kernel == "tc_quad" and all(p.cluster_ctas in (4, 8, 16) for p in plans):
+        return "mla_partial_quad_kernel"
     if all(2 <= p.cluster_ctas <= 16 for p in plans):
         return "mla_partial_tc128_kernel"
     return "mla_partial_tc_kernel"
@@ -318,13 +319,13 @@ def run_profile_case(args):
     case = make_case(i, L)
     dev = nb.mla_device_query()
     plan = nb.mla_plan([L], H, 1, BS, dev)
-    kernel = nb.MLA_KERNEL_TC if args.kernel == "tc" else nb.MLA_KERNEL_SIMT
+    kernel = {"tc": nb.MLA_KERNEL_TC, "tc_quad": nb.MLA_KERNEL_TC_QUAD, "simt": nb.MLA_KERNEL_SIMT}[args.kernel]
     dc = rt.upload(case)
     chunks_dev = rt.chunks_to_device(plan.chunks)
     part, lse = rt.alloc_partials(plan.num_chunks, 1, H)
     ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
     out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
-    k = plan.clusters_per_chunk if kernel == nb.MLA_KERNEL_TC else 1
+    k = plan.clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
     ws = rt.alloc_workspace(plan.num_chunks, k, 1, H)
     for _ in range(args.launches):
         rt.decode_partial(dc, part, lse, chunks_dev=chunks_dev, kernel=kernel, cluster=plan.cluster_ctas, subs=k,
@@ -398,7 +399,7 @@ def run_ours(args, rank, world):
     nb.load()
     dev_index = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(dev_index)
-    kernel = nb.MLA_KERNEL_TC if args.kernel == "tc" else nb.MLA_KERNEL_SIMT
+    kernel = {"tc": nb.MLA_KERNEL_TC, "tc_quad": nb.MLA_KERNEL_TC_QUAD, "simt": nb.MLA_KERNEL_SIMT}[args.kernel]
 
     cases = make_cases()
     dev = nb.mla_device_query()
@@ -413,7 +414,7 @@ def run_ours(args, rank, world):
             part, lse = rt.alloc_partials(plan.num_chunks, 1, H)
             ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
             out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
-            k = plan.clusters_per_chunk if kernel == nb.MLA_KERNEL_TC else 1
+            k = plan.clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
             ws = rt.alloc_workspace(plan.num_chunks, k, 1, H)
             desc = rt.make_desc(dc, chunks_dev, kernel, plan.cluster_ctas, stream, k, ws)
             calls.append(dict(L=L, plan=plan, dc=dc, chunks=chunks_dev, part=part, lse=lse, ind=ind, out=out,
@@ -563,7 +564,7 @@ def run_ours(args, rank, world):
     e2e_s = time.perf_counter() - t0
     ctr = nb.mla_get_counters()
     expect = (3 + e2e_steps) * len(calls)
-    ctr_key = nb.CTR_PARTIAL_TC if kernel == nb.MLA_KERNEL_TC else nb.CTR_PARTIAL_SIMT
+    ctr_key = nb.CTR_PARTIAL_SIMT if kernel == nb.MLA_KERNEL_SIMT else nb.CTR_PARTIAL_TC
     if ctr[ctr_key] != expect or ctr[nb.CTR_MERGE] != expect:
         print(f"WARNING: path counters {ctr} disagree with {expect} launches of the {args.kernel} kernel",
               file=sys.stderr)
@@ -581,6 +582,7 @@ def run_ours(args, rank, world):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured"
     else:
         peak, peak_src = 6800.0, "fallback"
+    kname = partial_kernel_name(args.kernel, [c["plan"] for c in calls])
     result = {
         "metric": METRIC,
         "value": round(value_us, 3),
@@ -603,8 +605,8 @@ def run_ours(args, rank, world):
         "many_heads": many_heads,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": profiled_traffic(sum(CONTEXTS) / len(CONTEXTS)),
-                     "peak_source": peak_src, "kernel": partial_kernel_name(args.kernel, [c["plan"] for c in calls])},
+                     "traffic": profiled_traffic(kname, sum(CONTEXTS) / len(CONTEXTS)),
+                     "peak_source": peak_src, "kernel": kname},
         "e2e": {"value": round(e2e_s * 1e6 / (e2e_steps * len(calls)), 3), "unit": "us/layer-call",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": (2 + 1) * n_calls * reps,  # step graphs (partial + merge) and partial-only graphs

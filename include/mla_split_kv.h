@@ -72,8 +72,14 @@ typedef enum { MLA_F16 = 0, MLA_BF16 = 1, MLA_F32 = 2 } mla_dtype_t;
 /* Which partial-decode kernel runs. AUTO picks the tensor-core kernel. */
 typedef enum {
   MLA_KERNEL_AUTO = 0,
-  MLA_KERNEL_SIMT = 1, /* CUDA-core fp32 FMA kernel                          */
-  MLA_KERNEL_TC = 2    /* tcgen05/TMEM tensor-core kernel                     */
+  MLA_KERNEL_SIMT = 1,   /* CUDA-core fp32 FMA kernel                        */
+  MLA_KERNEL_TC = 2,     /* tcgen05/TMEM tensor-core kernel                  */
+  MLA_KERNEL_TC_QUAD = 3 /* at q_len*H <= 16 in fp16 with clusters of 4, 8 or
+                            16 CTAs: the tensor-core variant whose CTAs share
+                            each tile in quads (scores split by columns, PV
+                            by tokens) instead of pairs; same results within
+                            rounding, slower on the long-context decode; kept
+                            to compare the two designs. Elsewhere like TC.   */
 } mla_kernel_t;
 
 /* One partition: logical tokens [t0, t1) of request b; its partial and LSE go
@@ -166,9 +172,10 @@ typedef struct {
                                  (normalized partial + log2 LSE) to the
                                  workspace and the cluster that finishes last
                                  merges the k of them in index order into the
-                                 partition's slot. Only for the paired 16-row
-                                 fp16 tensor-core kernel (q_len*H <= 16,
-                                 cluster_ctas set to 2..16, not 0 = auto);
+                                 partition's slot. Only for the 16-row fp16
+                                 tensor-core kernels whose CTAs share tiles in
+                                 pairs or quads (q_len*H <= 16, cluster_ctas
+                                 set to 2..16, not 0 = auto);
                                  otherwise MLA_ERR_UNSUPPORTED (INVALID_ARG for
                                  cluster_ctas 0 or a missing / short workspace;
                                  k > 16 is INVALID_ARG).                         */

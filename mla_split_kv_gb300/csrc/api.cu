@@ -44,7 +44,7 @@ struct MapKey {
   uint32_t box_rows;
   int dtype;
   int device;
-  int kind;  // 0: the 2D map; 1: the page map of the ckv cache (see page_map)
+  int kind;  // 0: the 2D map; 1, 2: page maps of the ckv cache (see page_map); 3: kpe quarter map
 };
 struct MapEntry {
   MapKey key;
@@ -77,6 +77,22 @@ bool page_map(CUtensorMap* out, const void* base, uint64_t rows, uint32_t box_ro
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   return encode_map(out, MapKey{base, rows, static_cast<uint64_t>(mla::kRank), box_rows, dtype, dev, 1});
 }
+// The same view with boxes of two column blocks, (64, 8, 2, box_rows / 8): the
+// 128 columns of one quarter of a page, row group g and block c landing at
+// 2048 g + 1024 c (the layout of the kernel whose CTAs share tiles in quads).
+bool quarter_page_map(CUtensorMap* out, const void* base, uint64_t rows, uint32_t box_rows, int dtype) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  return encode_map(out, MapKey{base, rows, static_cast<uint64_t>(mla::kRank), box_rows, dtype, dev, 2});
+}
+// 2D map over the [rows, 64] kpe cache with boxes of 16 columns x box_rows rows
+// and the 32-byte swizzle: one quarter of the rope columns of a page, rows of
+// 32 bytes (one K=16 step of a K-major tensor-core operand).
+bool kpe_quarter_map(CUtensorMap* out, const void* base, uint64_t rows, uint32_t box_rows, int dtype) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  return encode_map(out, MapKey{base, rows, static_cast<uint64_t>(mla::kRope), box_rows, dtype, dev, 3});
+}
 
 bool encode_map(CUtensorMap* out, const MapKey& key) {
   std::lock_guard<std::mutex> lock(g_map_mu);
@@ -99,11 +115,18 @@ bool encode_map(CUtensorMap* out, const MapKey& key) {
     cuuint32_t estr[2] = {1, 1};
     r = enc(&m, dt, 2, const_cast<void*>(key.base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else if (key.kind == 3) {
+    cuuint64_t dims[2] = {key.cols, key.rows};
+    cuuint64_t strides[1] = {key.cols * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(mla::kRope / 4), key.box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    r = enc(&m, dt, 2, const_cast<void*>(key.base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
     if (key.rows % 8 != 0 || key.box_rows % 8 != 0) return false;
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(mla::kBoxCols), 8, key.cols / mla::kBoxCols, key.rows / 8};
     cuuint64_t strides[3] = {key.cols * 2, mla::kBoxCols * 2, key.cols * 2 * 8};
-    cuuint32_t box[4] = {static_cast<cuuint32_t>(mla::kBoxCols), 8, 4, key.box_rows / 8};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(mla::kBoxCols), 8, key.kind == 2 ? 2u : 4u, key.box_rows / 8};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     r = enc(&m, dt, 4, const_cast<void*>(key.base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -168,7 +191,7 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64) return reject(MLA_ERR_UNSUPPORTED);
   if (d->dtype != MLA_F16 && d->dtype != MLA_BF16) return reject(MLA_ERR_UNSUPPORTED);
   if (d->causal != 0 && d->causal != 1) return reject(MLA_ERR_INVALID_ARG);
-  if (d->kernel < MLA_KERNEL_AUTO || d->kernel > MLA_KERNEL_TC) return reject(MLA_ERR_INVALID_ARG);
+  if (d->kernel < MLA_KERNEL_AUTO || d->kernel > MLA_KERNEL_TC_QUAD) return reject(MLA_ERR_INVALID_ARG);
   const int32_t C0 = d->cluster_ctas;
   if (C0 != 0 && C0 != 1 && C0 != 2 && C0 != 4 && C0 != 8 && C0 != 16) return reject(MLA_ERR_INVALID_ARG);
   if (!std::isfinite(scale)) return reject(MLA_ERR_INVALID_ARG);
@@ -196,7 +219,7 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   const int nr = use_simt ? mla::simt_rows_per_cta() : (mh ? rows_total : mla::tc_rows_per_cta(rows_total, bf16));
   const int64_t groups = (rows_total + nr - 1) / nr;
   const int32_t subs = (d->clusters_per_chunk > 1) ? d->clusters_per_chunk : 1;
-  if (subs > 1) {  // a partition spread over several clusters: the paired kernel with a workspace
+  if (subs > 1) {  // a partition spread over several clusters: the pair or quad kernel with a workspace
     if (C0 == 0) return reject(MLA_ERR_INVALID_ARG);  // the cluster size is part of that plan
     if (use_simt || !mla::tc128_supports(rows_total, bf16, C0)) return reject(MLA_ERR_UNSUPPORTED);
     const uint64_t need = mla_workspace_bytes(static_cast<int32_t>(N), subs, d->q_len, d->num_heads);
@@ -205,12 +228,19 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
     if (N * subs > 65535) return reject(MLA_ERR_UNSUPPORTED);
   }
   const int C = C0 ? C0 : (mh ? 2 : default_cluster(N * groups));
+  // 16 rows or fewer in fp16 with clusters of 4..16: CTAs share tiles in quads when asked for
+  const bool quad = d->kernel == MLA_KERNEL_TC_QUAD && mla::quad_supports(rows_total, bf16, C);
 
   CUtensorMap tm_ckv, tm_kpe, tm_pages;
-  if (!tensor_map(&tm_ckv, ckv_cache, rows, mla::kRank, d->block_size, d->dtype) ||
-      !tensor_map(&tm_kpe, kpe_cache, rows, mla::kRope, d->block_size, d->dtype) ||
-      !page_map(&tm_pages, ckv_cache, rows, d->block_size, d->dtype))
+  if (quad) {
+    if (!quarter_page_map(&tm_pages, ckv_cache, rows, d->block_size, d->dtype) ||
+        !kpe_quarter_map(&tm_kpe, kpe_cache, rows, d->block_size, d->dtype))
+      return reject(MLA_ERR_CUDA);
+  } else if (!tensor_map(&tm_ckv, ckv_cache, rows, mla::kRank, d->block_size, d->dtype) ||
+             !tensor_map(&tm_kpe, kpe_cache, rows, mla::kRope, d->block_size, d->dtype) ||
+             !page_map(&tm_pages, ckv_cache, rows, d->block_size, d->dtype)) {
     return reject(MLA_ERR_CUDA);
+  }
 
   mla::PartialParams p;
   p.q_abs = static_cast<const uint16_t*>(q_absorbed);
@@ -245,8 +275,10 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
     p.ws_lse = p.ws_partials + static_cast<uint64_t>(N) * subs * rows_total * mla::kRank;
   }
   cudaStream_t stream = static_cast<cudaStream_t>(d->stream);
-  const cudaError_t e = use_simt ? mla::launch_partial_simt(tm_ckv, tm_kpe, p, static_cast<int>(N), C, bf16, stream)
-                                 : mla::launch_partial_tc(tm_ckv, tm_kpe, tm_pages, p, static_cast<int>(N), C, bf16, stream);
+  const cudaError_t e =
+      use_simt ? mla::launch_partial_simt(tm_ckv, tm_kpe, p, static_cast<int>(N), C, bf16, stream)
+      : quad   ? mla::launch_partial_quad(tm_pages, tm_kpe, p, static_cast<int>(N), C, stream)
+               : mla::launch_partial_tc(tm_ckv, tm_kpe, tm_pages, p, static_cast<int>(N), C, bf16, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;
@@ -356,11 +388,12 @@ mla_status_t mla_merge_states(const float* partials, const float* lse, const int
 
 mla_status_t mla_check_device_errors(void* stream, uint32_t* code_out) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
-  uint32_t a = 0, b = 0, c = 0, e = 0;
+  uint32_t a = 0, b = 0, c = 0, e = 0, f = 0;
   if (mla::simt_read_clear_error(&a) != cudaSuccess || mla::tc_read_clear_error(&b) != cudaSuccess ||
-      mla::tc128_read_clear_error(&c) != cudaSuccess || mla::mh_read_clear_error(&e) != cudaSuccess)
+      mla::tc128_read_clear_error(&c) != cudaSuccess || mla::mh_read_clear_error(&e) != cudaSuccess ||
+      mla::quad_read_clear_error(&f) != cudaSuccess)
     return MLA_ERR_CUDA;
-  const uint32_t code = a | b | c | e;
+  const uint32_t code = a | b | c | e | f;
   if (code_out != nullptr) *code_out = code;
   if (code & mla::MLA_DEVERR_TIMEOUT) return MLA_ERR_TIMEOUT;
   if (code != 0) return MLA_ERR_DEVICE_CHECK;

@@ -310,11 +310,43 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// A shared-memory matrix descriptor as its two 32-bit halves. The start
+// address field (address / 16) is in the low half, and an offset inside one
+// CTA's shared memory never carries out of it, so advancing a descriptor is a
+// single 32-bit add. The MMA issue loops use this form: per instruction they
+// do one add per operand, so back-to-back MMAs keep the tensor core busy
+// (64-bit descriptor arithmetic between them left it idle about half the time).
+struct Desc2 {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ Desc2 desc2(uint64_t d) {
+  return Desc2{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+// The descriptor advanced by `bytes` (a multiple of 16).
+__device__ __forceinline__ Desc2 desc2_add(Desc2 d, uint32_t bytes) { return Desc2{d.lo + (bytes >> 4), d.hi}; }
+// D[tmem] (+)= A[smem] * B[smem]; a and b advanced by a16 / b16 units of 16 bytes.
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, Desc2 a, uint32_t a16, Desc2 b, uint32_t b16, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 da, db;\n setp.ne.b32 p, %6, 0;\n mov.b64 da, {%1, %2};\n"
+      " mov.b64 db, {%3, %4};\n tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d_tmem),
+      "r"(a.lo + a16), "r"(a.hi), "r"(b.lo + b16), "r"(b.hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive on `bar` once every MMA this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+// Arrive on the mbarrier at `bar`'s offset in every CTA of the cluster whose
+// rank bit is set in `cta_mask`, once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -355,6 +387,21 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t start, uint32_t lbo
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;  // SWIZZLE_128B
+  return d;
+}
+
+// The same for a K-major operand whose rows are 32 bytes (one K=16 step of
+// 16-bit elements) stored with the 32-byte swizzle (the 16-byte half of each
+// row is swapped on rows 4-7 of every 8-row group, as a TMA box with
+// CU_TENSOR_MAP_SWIZZLE_32B lands): sbo = stride between 8-row groups (256 B
+// when the rows are packed).
+__device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t start, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((start >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;  // leading byte offset: unused within one swizzle atom
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(6) << 61;  // SWIZZLE_32B
   return d;
 }
 
@@ -497,8 +544,11 @@ __device__ __forceinline__ int32_t checked_page(const PartialParams& p, int32_t 
 // also the LSE. Fixed rank order, so the result is bitwise reproducible.
 // `ostage` is [rows][512] fp32, `mst`/`lst` [rows] fp32, same offsets in every
 // CTA. The per-rank loads are independent (unrolled over the 16 possible ranks).
-__device__ __forceinline__ void cluster_combine(const PartialParams& p, const CtaWork& w, const float* ostage,
-                                                const float* mst, const float* lst, int tid, int nthreads) {
+// The result goes to slot `dst_slot` of `dst_partials` / `dst_lse` (the chunk's
+// own slot, or a sub-partial slot of the workspace).
+__device__ __forceinline__ void cluster_combine_to(const PartialParams& p, const CtaWork& w, const float* ostage,
+                                                   const float* mst, const float* lst, int tid, int nthreads,
+                                                   float* dst_partials, float* dst_lse, long long dst_slot) {
   const int rows_total = p.q_len * p.H;
   const uint32_t C = cluster_nctarank(), kr = cluster_ctarank();
   const int dcols = kRank / static_cast<int>(C);
@@ -536,12 +586,87 @@ __device__ __forceinline__ void cluster_combine(const PartialParams& p, const Ct
       }
     }
     if (is_lse) {
+      dst_lse[dst_slot * rows_total + w.row0 + r] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
+    } else {
+      float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (M != -INFINITY) out = make_float4(num.x / den, num.y / den, num.z / den, num.w / den);
+      const long long base = (dst_slot * rows_total + w.row0 + r) * kRank + d;
+      *reinterpret_cast<float4*>(dst_partials + base) = out;
+    }
+  }
+}
+__device__ __forceinline__ void cluster_combine(const PartialParams& p, const CtaWork& w, const float* ostage,
+                                                const float* mst, const float* lst, int tid, int nthreads) {
+  cluster_combine_to(p, w, ostage, mst, lst, tid, nthreads, p.partials, p.lse, static_cast<long long>(w.slot));
+}
+
+// A chunk spread over `subs` clusters (grid.y = chunk * subs + sub): each
+// cluster has written its sub-partial (normalized, with its log2 LSE) to slot
+// chunk * subs + sub of the workspace. Every CTA of the cluster calls this
+// after writing its share. The cluster that takes the chunk's last ticket
+// merges the chunk's sub-partials, in sub order (so the result does not depend
+// on which cluster finished last), into the chunk's slot of the partials, and
+// resets the ticket for the next call. CTA `rank` of the cluster merges columns
+// [rank * 512 / C, (rank + 1) * 512 / C), rank 0 also the LSE.
+__device__ __forceinline__ void merge_sub_partials(const PartialParams& p, const CtaWork& w, int chunk, int subs,
+                                                   int32_t* last_flag, int tid, int nthreads) {
+  const int rows_total = p.q_len * p.H;
+  const uint32_t rank = cluster_ctarank(), nranks = cluster_nctarank();
+  __threadfence();  // this thread's share of the sub-partial, visible before the ticket
+  cluster_sync();
+  if (rank == 0 && tid == 0) {
+    const uint32_t t = atomicAdd(p.ws_tickets + chunk, 1u);
+    const int last = (t == static_cast<uint32_t>(subs - 1)) ? 1 : 0;
+    if (last) atomicExch(p.ws_tickets + chunk, 0u);
+    *last_flag = last;
+  }
+  cluster_sync();
+  if (dsmem_ld_u32(dsmem_addr(last_flag, 0)) == 0) return;
+  __threadfence();
+  const int dcols = kRank / static_cast<int>(nranks);
+  const int dbeg = static_cast<int>(rank) * dcols;
+  const int n4 = dcols / 4;
+  const int items = w.nrows * n4 + ((rank == 0) ? w.nrows : 0);
+  const long long sub0 = static_cast<long long>(chunk) * subs;
+  for (int idx = tid; idx < items; idx += nthreads) {
+    const bool is_lse = idx >= w.nrows * n4;
+    const int r = is_lse ? idx - w.nrows * n4 : idx / n4;
+    const int d = is_lse ? 0 : dbeg + (idx % n4) * 4;
+    float lj[16];
+    float4 vj[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      lj[j] = -INFINITY;
+      vj[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j < subs) {
+        const long long row = (sub0 + j) * rows_total + w.row0 + r;
+        lj[j] = __ldcg(p.ws_lse + row);
+        if (!is_lse) vj[j] = __ldcg(reinterpret_cast<const float4*>(p.ws_partials + row * kRank + d));
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) M = fmaxf(M, lj[j]);
+    float den = 0.f;
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float wj = (lj[j] == -INFINITY) ? 0.f : exp2f(lj[j] - M);
+        den += wj;
+        num.x = fmaf(wj, vj[j].x, num.x);
+        num.y = fmaf(wj, vj[j].y, num.y);
+        num.z = fmaf(wj, vj[j].z, num.z);
+        num.w = fmaf(wj, vj[j].w, num.w);
+      }
+    }
+    if (is_lse) {
       p.lse[static_cast<long long>(w.slot) * rows_total + w.row0 + r] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
     } else {
       float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
       if (M != -INFINITY) out = make_float4(num.x / den, num.y / den, num.z / den, num.w / den);
-      const long long base = (static_cast<long long>(w.slot) * rows_total + w.row0 + r) * kRank + d;
-      *reinterpret_cast<float4*>(p.partials + base) = out;
+      *reinterpret_cast<float4*>(p.partials + (static_cast<long long>(w.slot) * rows_total + w.row0 + r) * kRank +
+                                 d) = out;
     }
   }
 }

@@ -89,7 +89,6 @@ struct Small {
 static_assert(sizeof(Small) <= 2048, "small smem region");
 
 __device__ __forceinline__ uint32_t tmem_lane_base(int warp) { return static_cast<uint32_t>(32 * (warp & 3)) << 16; }
-__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 __global__ void __launch_bounds__(kThreads, 1)
     mla_partial_tc128_kernel(const __grid_constant__ CUtensorMap tm_pages, const __grid_constant__ CUtensorMap tm_kpe,
@@ -213,9 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ MMA issuer
     const uint32_t idesc_s = idesc_f16_f32(128, kNR, false, false, false);
     const uint32_t idesc_o = idesc_f16_f32(128, kNR, false, true, false);
-    const uint64_t q_desc = smem_desc_sw128(smem_u32(qs), 16, 1024);
-    const uint64_t p_desc = smem_desc_sw128(smem_u32(ps), 16, 1024);
+    const Desc2 qd = desc2(smem_desc_sw128(smem_u32(qs), 16, 1024));
+    const Desc2 pd = desc2(smem_desc_sw128(smem_u32(ps), 16, 1024));
     const uint32_t tile_base = smem_u32(smem + kOffTile);
+    const uint32_t kpe16 = static_cast<uint32_t>(2 * half * 32) >> 4;  // this CTA's first kpe step, 16-byte units
     uint64_t tmo = p.timeout_ns;
     asm volatile("" : "+l"(tmo));
     auto wait_lane0 = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -234,21 +234,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         tc_fence_after();
         const uint32_t slot = tile_base + t * kTileSlot;
+        const Desc2 ad = desc2(smem_desc_sw128(slot, 16, kGroupBytes));
+        const Desc2 ak = desc2(smem_desc_sw128(slot + kCkvBytes, 16, 1024));
+        const uint32_t d = tmem + t * kNR;
 #pragma unroll
-        for (int c = 0; c < kHalfBoxes; ++c) {
-          const uint64_t ad = smem_desc_sw128(slot + c * 1024, 16, kGroupBytes);
+        for (int c = 0; c < kHalfBoxes; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_f16_ss(tmem + t * kNR, desc_add(ad, kk * 32), desc_add(q_desc, c * kQChunk + kk * 32), idesc_s,
-                        (c == 0 && kk == 0) ? 0u : 1u);
-        }
-        const uint64_t ak = smem_desc_sw128(slot + kCkvBytes, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const uint32_t ks = 2 * half + kk;  // 16-column step of the kpe box
-          umma_f16_ss(tmem + t * kNR, desc_add(ak, ks * 32), desc_add(q_desc, kHalfBoxes * kQChunk + ks * 32), idesc_s,
-                      1u);
-        }
+            umma_ss(d, ad, (c * 1024 + kk * 32) >> 4, qd, (c * kQChunk + kk * 32) >> 4, idesc_s,
+                    (c == 0 && kk == 0) ? 0u : 1u);
+        // this CTA's two 16-column steps of the kpe box
+        umma_ss(d, ak, kpe16, qd, (kHalfBoxes * kQChunk) / 16 + kpe16, idesc_s, 1u);
+        umma_ss(d, ak, kpe16 + 2, qd, (kHalfBoxes * kQChunk) / 16 + kpe16 + 2, idesc_s, 1u);
         umma_commit(&sm->sfull[t]);
       }
       __syncwarp();
@@ -279,13 +276,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (lane == 0) {
         tc_fence_after();
-        const uint64_t pb = desc_add(p_desc, t * kPBuf);
+        const Desc2 pb = desc2_add(pd, t * kPBuf);
+        const uint32_t acc0 = (i > 0) ? 1u : 0u;
+        // K step ks: tokens [16 ks, 16 ks + 16): two 8-token groups of the slot, and 16 tokens of the
+        // P^T atom (ks / 4) at 32-byte step ks % 4
 #pragma unroll
         for (int blk = 0; blk < 2; ++blk) {
-          const uint64_t a0 = smem_desc_sw128(tile_base + t * kTileSlot + 2 * blk * 1024, 1024, kGroupBytes);
-          for (int ks = 0; ks < ksteps; ++ks)
-            umma_f16_ss(tmem + 2 * kNR + blk * kNR, desc_add(a0, ks * 2 * kGroupBytes),
-                        desc_add(pb, (ks >> 2) * (kNR * 128) + (ks & 3) * 32), idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
+          const Desc2 a0 = desc2(smem_desc_sw128(tile_base + t * kTileSlot + 2 * blk * 1024, 1024, kGroupBytes));
+          const uint32_t d = tmem + 2 * kNR + blk * kNR;
+          if (ksteps == kT / 16) {
+#pragma unroll
+            for (int ks = 0; ks < kT / 16; ++ks)
+              umma_ss(d, a0, (ks * 2 * kGroupBytes) >> 4, pb, ((ks >> 2) * (kNR * 128) + (ks & 3) * 32) >> 4, idesc_o,
+                      ks > 0 ? 1u : acc0);
+          } else {
+            for (int ks = 0; ks < ksteps; ++ks)
+              umma_ss(d, a0, (ks * 2 * kGroupBytes) >> 4, pb, ((ks >> 2) * (kNR * 128) + (ks & 3) * 32) >> 4, idesc_o,
+                      ks > 0 ? 1u : acc0);
+          }
         }
         umma_commit(&sm->empty[t]);
         umma_commit(&sm->pvdone[t]);
@@ -584,71 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  if (subs > 1) __threadfence();  // this thread's share of the sub-partial, visible before the ticket
-  cluster_sync();
-  if (subs > 1) {
-    // Take the chunk's ticket; the cluster that takes the last one merges the chunk's sub-partials
-    // (normalized partials with log2 LSEs, like the partitions of a request) in sub order, so the
-    // result does not depend on which cluster finishes last. It also resets the ticket.
-    if (rank == 0 && tid == 0) {
-      const uint32_t t = atomicAdd(p.ws_tickets + chunk, 1u);
-      const int last = (t == static_cast<uint32_t>(subs - 1)) ? 1 : 0;
-      if (last) atomicExch(p.ws_tickets + chunk, 0u);
-      sm->last_cluster = last;
-    }
-    cluster_sync();
-    const bool last = dsmem_ld_u32(dsmem_addr(&sm->last_cluster, 0)) != 0;
-    if (last) {
-      __threadfence();
-      const int dcols = kRank / static_cast<int>(nranks);
-      const int dbeg = static_cast<int>(rank) * dcols;
-      const int n4 = dcols / 4;
-      const int items = w.nrows * n4 + ((rank == 0) ? w.nrows : 0);
-      const long long sub0 = static_cast<long long>(chunk) * subs;
-      for (int idx = tid; idx < items; idx += kThreads) {
-        const bool is_lse = idx >= w.nrows * n4;
-        const int r = is_lse ? idx - w.nrows * n4 : idx / n4;
-        const int d = is_lse ? 0 : dbeg + (idx % n4) * 4;
-        float lj[16];
-        float4 vj[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          lj[j] = -INFINITY;
-          vj[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (j < subs) {
-            const long long row = (sub0 + j) * rows_total + w.row0 + r;
-            lj[j] = __ldcg(p.ws_lse + row);
-            if (!is_lse) vj[j] = __ldcg(reinterpret_cast<const float4*>(p.ws_partials + row * kRank + d));
-          }
-        }
-        float M = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) M = fmaxf(M, lj[j]);
-        float den = 0.f;
-        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float wj = (lj[j] == -INFINITY) ? 0.f : exp2f(lj[j] - M);
-            den += wj;
-            num.x = fmaf(wj, vj[j].x, num.x);
-            num.y = fmaf(wj, vj[j].y, num.y);
-            num.z = fmaf(wj, vj[j].z, num.z);
-            num.w = fmaf(wj, vj[j].w, num.w);
-          }
-        }
-        if (is_lse) {
-          p.lse[static_cast<long long>(w.slot) * rows_total + w.row0 + r] =
-              (M == -INFINITY) ? -INFINITY : M + log2f(den);
-        } else {
-          float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (M != -INFINITY) out = make_float4(num.x / den, num.y / den, num.z / den, num.w / den);
-          *reinterpret_cast<float4*>(p.partials + (static_cast<long long>(w.slot) * rows_total + w.row0 + r) * kRank +
-                                     d) = out;
-        }
-      }
-    }
-  }
+  if (subs > 1) merge_sub_partials(p, w, chunk, subs, &sm->last_cluster, tid, kThreads);
   cluster_sync();
   if (warp == 4) {
     tc_fence_after();

@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 
 MAX_ABS = 2e-3
 REL_L2 = 1e-3
-KERNELS = {"tc": nb.MLA_KERNEL_TC, "simt": nb.MLA_KERNEL_SIMT}
+KERNELS = {"tc": nb.MLA_KERNEL_TC, "tc_quad": nb.MLA_KERNEL_TC_QUAD, "simt": nb.MLA_KERNEL_SIMT}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -175,6 +175,36 @@ def test_natural_log_lse_fails_parity_on_the_gpu_merge():
     assert err > MAX_ABS or rel > REL_L2, "natural-log LSE should not pass parity"
 
 
+@pytest.mark.parametrize("kernel", ["tc", "tc_quad"])
+@pytest.mark.parametrize("C", [4, 8, 16])
+@pytest.mark.parametrize("bs", [16, 32, 64])
+def test_shared_tile_kernels_ragged(kernel, C, bs):
+    """16 fp16 rows, clusters of 4..16: CTAs share each 128-token tile in pairs (tc) or quads (tc_quad).
+    The lengths end chunks at every kind of place in a tile's 32-token quarters (empty, partial, full)."""
+    lens = [0, 1, 17, 31, 32, 33, 64, 95, 96, 97, 127, 128, 129, 1000, 4133]
+    case = gen.make_decode_case(12, lens, num_heads=16, block_size=bs, dtype="f16")
+    P = 3
+    nb.mla_reset_counters()
+    part, lse, out, _, _ = run_uniform(case, P, KERNELS[kernel], cluster=C)
+    assert nb.mla_get_counters()[nb.CTR_CTAS] == len(lens) * P * C
+    chunks, _ = oracle_uniform_chunks(case, P)
+    ref_part, ref_lse = orc.partials(case, chunks)
+    assert_close(part.cpu().numpy(), ref_part, f"partials {kernel} C={C} bs={bs}")
+    assert_lse_close(lse.cpu().numpy(), ref_lse, f"lse {kernel} C={C} bs={bs}")
+    ref, _ = orc.unsplit(case)
+    assert_close(out.cpu().numpy(), ref, f"merged {kernel} C={C} bs={bs}")
+
+
+def test_quad_kernel_paging_invariance_and_reproducibility():
+    """The quad kernel's result depends only on the logical cache (not on which pages hold it) and is
+    the same bits on every call."""
+    case = gen.make_decode_case(13, [7777, 300, 4096], num_heads=16, block_size=32, dtype="f16")
+    _, _, a, _, dc = run_uniform(case, 2, nb.MLA_KERNEL_TC_QUAD, cluster=4)
+    _, _, a2, _, _ = run_uniform(case, 2, nb.MLA_KERNEL_TC_QUAD, cluster=4, dc=dc)
+    _, _, b, _, _ = run_uniform(gen.permute_pool(case, 5), 2, nb.MLA_KERNEL_TC_QUAD, cluster=4)
+    assert torch.equal(a, a2) and torch.equal(a, b)
+
+
 def plan_and_run(case, max_partitions=0, kernel=nb.MLA_KERNEL_TC, dc=None, ws=None):
     """The planner's plan as the bench runs it: its cluster size and clusters per partition."""
     dev = nb.mla_device_query()
@@ -183,7 +213,7 @@ def plan_and_run(case, max_partitions=0, kernel=nb.MLA_KERNEL_TC, dc=None, ws=No
     dc = dc or rt.upload(case)
     chunks_dev = rt.chunks_to_device(plan.chunks)
     part, lse = rt.alloc_partials(plan.num_chunks, case.q_len, case.num_heads)
-    k = plan.clusters_per_chunk if kernel == nb.MLA_KERNEL_TC else 1
+    k = plan.clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
     if k > 1 and ws is None:
         ws = rt.alloc_workspace(plan.num_chunks, k, case.q_len, case.num_heads)
     rt.decode_partial(dc, part, lse, chunks_dev=chunks_dev, kernel=kernel, cluster=plan.cluster_ctas, subs=k,
@@ -223,6 +253,17 @@ def test_spread_partitions_partials_match_oracle(L, P, C, k, bs):
     assert_lse_close(lse.cpu().numpy(), ref_lse, f"lse L={L} P={P} C={C} k={k}")
     ref, _ = orc.unsplit(case)
     assert_close(out.cpu().numpy(), ref, f"merged L={L} P={P} C={C} k={k}")
+
+
+@pytest.mark.parametrize("L,P,C,k", [(20017, 2, 4, 3), (9000, 1, 16, 2)])
+def test_quad_kernel_spread_partitions(L, P, C, k):
+    """The quad variant with each partition over k clusters: sub-partials merged by the last cluster."""
+    case = gen.make_decode_case(14, [L], num_heads=16, block_size=32, dtype="f16")
+    part, lse, out, ind, dc = run_uniform(case, P, nb.MLA_KERNEL_TC_QUAD, cluster=C, subs=k)
+    chunks, _ = oracle_uniform_chunks(case, P)
+    ref_part, ref_lse = orc.partials(case, chunks)
+    assert_close(part.cpu().numpy(), ref_part, f"quad partials L={L} P={P} C={C} k={k}")
+    assert_lse_close(lse.cpu().numpy(), ref_lse, f"quad lse L={L} P={P} C={C} k={k}")
 
 
 def test_spread_partitions_bitwise_reproducible_and_workspace_reused():
