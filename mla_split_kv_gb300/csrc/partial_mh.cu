@@ -34,8 +34,11 @@
 // group g and block c at 4096 g + 1024 c; the kpe box), this CTA's and the
 // peer's partial S (32 KB each): 226 KB.
 //
-// Warp roles (256 threads): warps 0-3 softmax (thread = row) and epilogue,
-// warp 4 TMEM owner + MMA issuer, warps 5-7 page producers.
+// Warp roles (384 threads): warps 0-7 softmax and epilogue (thread = row r =
+// TMEM lane 32 (w % 4) + lane; warps w and w + 4 share the rows and take the
+// two 32-token halves of each tile, which halves each thread's exponentials
+// and conversions and puts two softmax warps on every scheduler), warp 8 TMEM
+// owner + MMA issuer, warps 9-11 page producers.
 #include "device_common.cuh"
 
 namespace mla {
@@ -51,9 +54,12 @@ constexpr int kCkvBytes = kT * kHalfCols * 2;     // 32 KB
 constexpr int kKpeBytes = kT * 128;               // 8 KB
 constexpr int kTileSlot = kCkvBytes + kKpeBytes;  // 40 KB
 constexpr int kQChunk = kRows * 128;              // 16 KB: [128 rows x 64 columns], swizzled
-constexpr int kPageWarps = 3;                     // 8 warps in all: two per scheduler, so up to 255 registers
-constexpr int kSoftmaxThreads = 128;
-constexpr int kThreads = (5 + kPageWarps) * 32;   // 256
+constexpr int kPageWarps = 3;
+constexpr int kSoftmaxWarps = 8;                  // two per TMEM lane quadrant: each takes half of a tile's tokens
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kMmaWarp = kSoftmaxWarps;
+constexpr int kThreads = (kSoftmaxWarps + 1 + kPageWarps) * 32;  // 384: three warps per scheduler
+constexpr int kHalfT = kT / 2;                    // tokens of a tile per softmax thread
 constexpr float kRescaleTau = 8.0f;
 
 constexpr uint32_t kOffQ = 0;                             // 80 KB
@@ -62,7 +68,7 @@ constexpr uint32_t kOffX = kOffTile + 2 * kTileSlot;      // 160 KB: the peer's 
 constexpr uint32_t kXBytes = kRows * kT * 4;              // [128 rows][64 tokens] fp32: 32 KB
 constexpr uint32_t kOffXS = kOffX + kXBytes;              // 192 KB: this CTA's partial S, sent as one copy
 constexpr uint32_t kOffSmall = kOffXS + kXBytes;          // 224 KB
-constexpr uint32_t kSmem = kOffSmall + 1024 + 1024;       // + alignment slack
+constexpr uint32_t kSmem = kOffSmall + 2048 + 1024;       // + alignment slack
 static_assert(kSmem <= 232448, "shared memory per CTA");
 
 constexpr uint32_t kTmemO = 0;      // O [128 x 256] fp32
@@ -74,8 +80,9 @@ struct Small {
   uint64_t full[2], empty[2], sfull[2], sfree[2], ppfull[2], pvdone[2], xfull, xempty, drain;
   uint32_t tmem_base;
   int32_t abort_flag;
+  float half_val[2][kRows];  // per row, the two token halves' tile maximum (then their sums)
 };
-static_assert(sizeof(Small) <= 1024, "small smem region");
+static_assert(sizeof(Small) <= 2048, "small smem region");
 
 __device__ __forceinline__ uint32_t tmem_lane_base(int warp) { return static_cast<uint32_t>(32 * (warp & 3)) << 16; }
 
@@ -117,18 +124,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm->full[t], kPageWarps);  // one expect_tx arrival per producer warp
       mbar_init(&sm->empty[t], 1);
       mbar_init(&sm->sfull[t], 1);
-      mbar_init(&sm->sfree[t], 4);
-      mbar_init(&sm->ppfull[t], 4);
+      mbar_init(&sm->sfree[t], kSoftmaxWarps);
+      mbar_init(&sm->ppfull[t], kSoftmaxWarps);
       mbar_init(&sm->pvdone[t], 1);
     }
     mbar_init(&sm->xfull, 1);   // local expect_tx arrival + the peer's st.async bytes
-    mbar_init(&sm->xempty, 4);  // one remote arrival per peer softmax warp
+    mbar_init(&sm->xempty, kSoftmaxWarps);  // one remote arrival per peer softmax warp
     mbar_init(&sm->drain, 1);
     mbar_arrive_expect_tx(&sm->xfull, kXBytes);  // tile 0
     sm->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&sm->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -138,9 +145,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_arrive_release();  // the peer touches this CTA's barriers only after this cluster phase
   const uint32_t tmem = sm->tmem_base;
 
-  if (warp >= 5) {
+  if (warp > kMmaWarp) {
     // ------------------------------------------------------------------ producers
-    const int k0 = warp - 5;  // this warp loads pages k0, k0 + 3, ... of each tile (at most 2: 4 pages of 16)
+    const int k0 = warp - kMmaWarp - 1;  // this warp loads pages k0, k0 + 3, ... of each tile (at most 2: 4 pages of 16)
     const uint64_t pol = l2_policy_evict_first();
     uint64_t tmo = p.timeout_ns;
     asm volatile("" : "+l"(tmo));
@@ -205,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0 && *abort_flag && issued >= 0) mbar_wait(&sm->full[issued & 1], (issued >> 1) & 1, kDrainTimeoutNs);
     cluster_wait_acquire();
-  } else if (warp == 4) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     const uint32_t idesc_s = idesc_f16_f32(kRows, kT, BF16, false, false);         // A = Q, B = K tile
     const uint32_t idesc_o = idesc_f16_f32(kRows, kHalfCols, BF16, false, true);   // A = P (TMEM), B = V N-major
@@ -273,8 +280,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t pa = tmem + kTmemP + t * 64;
         for (int ks = 0; ks < ksteps; ++ks) {
           const uint64_t vd = smem_desc_sw128(slot + ks * 2 * kGroupBytes, 1024, kGroupBytes);
-          umma_f16_ts(tmem + kTmemO, pa + ks * 8, vd, idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
-          if (BF16) umma_f16_ts(tmem + kTmemO, pa + 32 + ks * 8, vd, idesc_o, 1u);
+          // K step ks: tokens [16 ks, 16 ks + 16) of token half ks / 2, whose P (hi, then lo) fills
+          // that half's 32 columns of the buffer
+          const uint32_t pk = pa + 32 * (ks >> 1) + 8 * (ks & 1);
+          umma_f16_ts(tmem + kTmemO, pk, vd, idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
+          if (BF16) umma_f16_ts(tmem + kTmemO, pk + 16, vd, idesc_o, 1u);
         }
         umma_commit(&sm->empty[t]);
         umma_commit(&sm->pvdone[t]);
@@ -282,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
-    named_bar_sync(2, 160);  // Q staged by the softmax warps
+    named_bar_sync(2, kSoftmaxThreads + 32);  // Q staged by the softmax warps
     bool alive = true;
     for (int i0 = 0; i0 < ntiles && alive; i0 += 2) {
       const int i1 = min(i0 + 2, ntiles);
@@ -309,13 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cp_async_wait_all();
     fence_proxy_async_smem();
-    named_bar_arrive(2, 160);
+    named_bar_arrive(2, kSoftmaxThreads + 32);
     cluster_wait_acquire();  // the peer's barriers are initialised
 
     float scale_log2 = p.scale_log2;
     uint64_t tmo = p.timeout_ns;
     asm volatile("" : "+f"(scale_log2), "+l"(tmo));
-    const int r = tid;  // query row of this thread (TMEM lane r)
+    const int r = 32 * (warp & 3) + lane;  // query row of this thread (TMEM lane r)
+    const int hf = warp >> 2;               // its token half of each tile: tokens [32 hf, 32 hf + 32)
     const uint32_t lane_base = tmem_lane_base(warp);
     // visible tokens of this row: t < L, and t <= L - q_len + i under the causal rule
     const int row_q = (w.row0 + r) / p.H;
@@ -332,38 +343,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     // C(j): probabilities of tile j (its scaled scores wait in its P buffer) -> the same buffer (hi, and lo
     // for bf16), 32 tokens at a time; then PV(j) may run
     auto probabilities = [&](int j) {
-        const uint32_t pa = tmem + lane_base + kTmemP + (j & 1) * 64;
+        // this thread's half of the buffer: its 32 scaled scores, overwritten by P hi (16 columns)
+        // and, for bf16, P lo (16 columns)
+        const uint32_t pa = tmem + lane_base + kTmemP + (j & 1) * 64 + 32 * hf;
         // a row that has seen no visible token yet has only -inf scores: subtract a finite stand-in
         const float m_sub = (m_r == -INFINITY) ? 0.f : m_r;
-        float y[kT];
+        float y[kHalfT];
         tc_fence_after();
-#pragma unroll
-        for (int q = 0; q < kT / 16; ++q) tmem_ld16(pa + q * 16, y + 16 * q);
+        tmem_ld16(pa, y);
+        tmem_ld16(pa + 16, y + 16);
         tmem_wait_ld();
+        float hw[16], lw[16];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          float hw[16], lw[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = 32 * q + 2 * j;
-            const float p0 = fast_exp2(y[t] - m_sub);  // masked scores (-inf) give 0
-            const float p1 = fast_exp2(y[t + 1] - m_sub);
-            const uint32_t h = pack2<BF16>(p0, p1);  // one paired conversion, element t in the low half
-            hw[j] = __uint_as_float(h);
-            const float h0 = h2f<BF16>(static_cast<uint16_t>(h & 0xffffu));
-            const float h1 = h2f<BF16>(static_cast<uint16_t>(h >> 16));
-            if (BF16) {
-              const uint32_t l = pack2<BF16>(p0 - h0, p1 - h1);
-              lw[j] = __uint_as_float(l);
-              l_r += (h0 + h2f<BF16>(static_cast<uint16_t>(l & 0xffffu))) +
-                     (h1 + h2f<BF16>(static_cast<uint16_t>(l >> 16)));
-            } else {
-              l_r += h0 + h1;
-            }
+        for (int u = 0; u < 16; ++u) {
+          const float p0 = fast_exp2(y[2 * u] - m_sub);  // masked scores (-inf) give 0
+          const float p1 = fast_exp2(y[2 * u + 1] - m_sub);
+          const uint32_t h = pack2<BF16>(p0, p1);  // one paired conversion, element 2u in the low half
+          hw[u] = __uint_as_float(h);
+          const float h0 = h2f<BF16>(static_cast<uint16_t>(h & 0xffffu));
+          const float h1 = h2f<BF16>(static_cast<uint16_t>(h >> 16));
+          if (BF16) {
+            const uint32_t l = pack2<BF16>(p0 - h0, p1 - h1);
+            lw[u] = __uint_as_float(l);
+            l_r += (h0 + h2f<BF16>(static_cast<uint16_t>(l & 0xffffu))) + (h1 + h2f<BF16>(static_cast<uint16_t>(l >> 16)));
+          } else {
+            l_r += h0 + h1;
           }
-          tmem_st16(pa + q * 16, hw);
-          if (BF16) tmem_st16(pa + 32 + q * 16, lw);
         }
+        tmem_st16(pa, hw);
+        if (BF16) tmem_st16(pa + 16, lw);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -392,11 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (cur) {
         if (lane == 0) ok = mbar_wait(&sm->sfull[buf], (i >> 1) & 1, tmo);
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        float x[kT];
+        float x[kHalfT];
         if (ok) {
           tc_fence_after();
-#pragma unroll
-          for (int q = 0; q < kT / 16; ++q) tmem_ld16(tmem + lane_base + kTmemS + buf * kT + q * 16, x + 16 * q);
+          tmem_ld16(tmem + lane_base + kTmemS + buf * kT + 32 * hf, x);
+          tmem_ld16(tmem + lane_base + kTmemS + buf * kT + 32 * hf + 16, x + 16);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
@@ -407,12 +415,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
 #pragma unroll
-          for (int c = 0; c < kT / 4; ++c)
-            srow[c ^ xsw] = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+          for (int c = 0; c < kHalfT / 4; ++c)
+            srow[(8 * hf + c) ^ xsw] = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
           fence_proxy_async_smem();
         }
       }
-      if (named_bar_sync_or(1, 128, !ok || *abort_flag != 0)) {
+      if (named_bar_sync_or(1, kSoftmaxThreads, !ok || *abort_flag != 0)) {
         *abort_flag = 1;
         break;
       }
@@ -427,13 +435,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tok0 = w.sub0 + i * kT;
       ok = mbar_wait_cluster(&sm->xfull, i & 1, tmo);
       ok = __all_sync(0xffffffffu, ok);
-      float x[kT];
+      float x[kHalfT];
       float mx = -INFINITY;
       if (ok) {
 #pragma unroll
-        for (int c = 0; c < kT / 4; ++c) {
-          const float4 o = srow_c[c ^ xsw];
-          const float4 y = xrow[c ^ xsw];
+        for (int c = 0; c < kHalfT / 4; ++c) {
+          const float4 o = srow_c[(8 * hf + c) ^ xsw];
+          const float4 y = xrow[(8 * hf + c) ^ xsw];
           // rank-0 part + rank-1 part, the same sum in both CTAs
           x[4 * c] = half ? (y.x + o.x) : (o.x + y.x);
           x[4 * c + 1] = half ? (y.y + o.y) : (o.y + y.y);
@@ -447,21 +455,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (tid == 0) mbar_arrive_expect_tx(&sm->xfull, kXBytes);
           mbar_remote_arrive_relaxed(peer_xempty);
         }
-        const int nvis = min(kT, tlim - tok0);  // tokens of this tile the row can see
-        if (__builtin_expect(nvis < kT, 0)) {
+        const int nvis = min(kT, tlim - tok0) - kHalfT * hf;  // tokens of this half the row can see
+        if (__builtin_expect(nvis < kHalfT, 0)) {
 #pragma unroll
-          for (int t = 0; t < kT; ++t) x[t] = (t < nvis) ? x[t] * scale_log2 : -INFINITY;
+          for (int t = 0; t < kHalfT; ++t) x[t] = (t < nvis) ? x[t] * scale_log2 : -INFINITY;
         } else {
 #pragma unroll
-          for (int t = 0; t < kT; ++t) x[t] *= scale_log2;
+          for (int t = 0; t < kHalfT; ++t) x[t] *= scale_log2;
         }
 #pragma unroll
-        for (int t = 0; t < kT; ++t) mx = fmaxf(mx, x[t]);
+        for (int t = 0; t < kHalfT; ++t) mx = fmaxf(mx, x[t]);
       }
-      if (named_bar_sync_or(1, 128, !ok || *abort_flag != 0)) {
+      sm->half_val[hf][r] = mx;
+      if (named_bar_sync_or(1, kSoftmaxThreads, !ok || *abort_flag != 0)) {
         *abort_flag = 1;
         break;
       }
+      mx = fmaxf(mx, sm->half_val[hf ^ 1][r]);  // the row's maximum over the tile: the same in both halves
       // lazy rescale of this row (rare): move the reference max and scale O and the sum; PV(i-1)
       // (its probabilities were written in C(i-1) above) must be complete before O is rescaled
       const bool need = mx > m_r + kRescaleTau;
@@ -473,9 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) ok2 = mbar_wait(&sm->pvdone[(i - 1) & 1], ((i - 1) >> 1) & 1, tmo);
           if (__shfl_sync(0xffffffffu, ok2, 0)) {
             tc_fence_after();
-            for (int q = 0; q < kHalfCols / 16; ++q) {
+            for (int q = 0; q < kHalfCols / 32; ++q) {  // this thread's half of the row's O columns
               float v[16];
-              const uint32_t a = tmem + lane_base + kTmemO + q * 16;
+              const uint32_t a = tmem + lane_base + kTmemO + (kHalfCols / 2) * hf + q * 16;
               tmem_ld16(a, v);
               tmem_wait_ld();
 #pragma unroll
@@ -497,44 +507,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!__shfl_sync(0xffffffffu, ok3, 0) && lane == 0) *abort_flag = 1;
       }
       {
-        const uint32_t pa = tmem + lane_base + kTmemP + buf * 64;
-#pragma unroll
-        for (int q = 0; q < kT / 16; ++q) tmem_st16(pa + q * 16, x + 16 * q);
+        const uint32_t pa = tmem + lane_base + kTmemP + buf * 64 + 32 * hf;
+        tmem_st16(pa, x);
+        tmem_st16(pa + 16, x + 16);
         tmem_wait_st();
       }
     }
-    const bool aborted = named_bar_sync_or(1, 128, *abort_flag != 0);
+    const bool aborted = named_bar_sync_or(1, kSoftmaxThreads, *abort_flag != 0);
     if (ntiles > 0 && !aborted) {
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&sm->pvdone[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, tmo);
       if (!__shfl_sync(0xffffffffu, ok, 0) && lane == 0) *abort_flag = 1;
     }
-    const bool read_o = (ntiles > 0) && !named_bar_sync_or(1, 128, *abort_flag != 0);  // uniform
-    // epilogue: the normalized partial of this row over this CTA's 256 columns, and the LSE (rank 0)
-    const bool has_mass = read_o && (r < w.nrows) && (m_r != -INFINITY) && (l_r > 0.f);
-    const float inv = has_mass ? 1.f / l_r : 0.f;
+    sm->half_val[hf][r] = l_r;
+    const bool read_o = (ntiles > 0) && !named_bar_sync_or(1, kSoftmaxThreads, *abort_flag != 0);  // uniform
+    const float l_row = sm->half_val[0][r] + sm->half_val[1][r];  // the row's sum, the same in both halves
+    // epilogue: the normalized partial of this row over this thread's half of the CTA's 256 columns,
+    // and the LSE (rank 0)
+    const bool has_mass = read_o && (r < w.nrows) && (m_r != -INFINITY) && (l_row > 0.f);
+    const float inv = has_mass ? 1.f / l_row : 0.f;
     const long long orow = static_cast<long long>(w.slot) * rows_total + w.row0 + r;
     if (read_o) tc_fence_after();
-    for (int q = 0; q < kHalfCols / 16; ++q) {
+    for (int q = 0; q < kHalfCols / 32; ++q) {
       float v[16];
+      const int col = (kHalfCols / 2) * hf + q * 16;
       if (read_o) {
-        tmem_ld16(tmem + lane_base + kTmemO + q * 16, v);
+        tmem_ld16(tmem + lane_base + kTmemO + col, v);
         tmem_wait_ld();
       }
       if (r < w.nrows) {
-        float4* dst = reinterpret_cast<float4*>(p.partials + orow * kRank + kHalfCols * half + q * 16);
+        float4* dst = reinterpret_cast<float4*>(p.partials + orow * kRank + kHalfCols * half + col);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           dst[j] = has_mass ? make_float4(v[4 * j] * inv, v[4 * j + 1] * inv, v[4 * j + 2] * inv, v[4 * j + 3] * inv)
                             : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-    if (rank == 0 && r < w.nrows) p.lse[orow] = has_mass ? m_r + log2f(l_r) : -INFINITY;
+    if (rank == 0 && hf == 0 && r < w.nrows) p.lse[orow] = has_mass ? m_r + log2f(l_row) : -INFINITY;
   }
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the peer is done with this CTA's shared memory
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
