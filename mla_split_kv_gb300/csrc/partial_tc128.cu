@@ -59,9 +59,13 @@ constexpr int kCkvBytes = kT * kHalfCols * 2;    // 64 KB: row group g, block c 
 constexpr int kKpeBytes = kT * 128;              // 16 KB: [128 rows x 64 columns], swizzled
 constexpr int kTileSlot = kCkvBytes + kKpeBytes; // 80 KB
 constexpr int kGroupBytes = 8 * kHalfCols * 2;   // 4 KB: one 8-row group of the four blocks
-constexpr int kPageWarps = 4;                    // producer warps
-constexpr int kSoftmaxThreads = 128;
-constexpr int kThreads = (5 + kPageWarps) * 32;  // 288
+constexpr int kPageWarps = 3;                    // producer warps
+constexpr int kSoftmaxWarps = 8;                 // two per TMEM lane quadrant: rows 0-7 and 8-15
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kMmaWarp = kSoftmaxWarps;
+constexpr int kThreads = (kSoftmaxWarps + 1 + kPageWarps) * 32;  // 384: three warps per scheduler
+constexpr int kRH = kNR / 2;                     // rows per softmax thread
+constexpr int kMaxPagesPerWarp = (kT / 16 + kPageWarps - 1) / kPageWarps;  // pages of 16 tokens or more
 constexpr float kRescaleTau = 8.0f;
 
 constexpr uint32_t kOffTile = 0;                            // 2 tile slots
@@ -120,11 +124,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm->full[t], kPageWarps);  // one expect_tx arrival per producer warp
       mbar_init(&sm->empty[t], 1);
       mbar_init(&sm->sfull[t], 1);
-      mbar_init(&sm->sfree[t], 4);
-      mbar_init(&sm->ppfull[t], 4);
+      mbar_init(&sm->sfree[t], kSoftmaxWarps);
+      mbar_init(&sm->ppfull[t], kSoftmaxWarps);
       mbar_init(&sm->pvdone[t], 1);
-      mbar_init(&sm->xfull[t], 1);   // local expect_tx arrival + the peer's st.async bytes
-      mbar_init(&sm->xempty[t], 4);  // one remote arrival per peer softmax warp
+      mbar_init(&sm->xfull[t], 1);                // local expect_tx arrival + the peer's st.async bytes
+      mbar_init(&sm->xempty[t], kSoftmaxWarps);   // one remote arrival per peer softmax warp
     }
     mbar_init(&sm->drain, 1);
     for (int t = 0; t < 2; ++t) mbar_arrive_expect_tx(&sm->xfull[t], kXBuf);  // tiles 0 and 1
@@ -132,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (tid < kNR) sm->mref[tid] = -INFINITY;
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&sm->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -142,9 +146,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_arrive_release();  // the peer touches this CTA's barriers only after this cluster phase
   const uint32_t tmem = sm->tmem_base;
 
-  if (warp >= 5) {
+  if (warp > kMmaWarp) {
     // ------------------------------------------------------------------ producers
-    const int k0 = warp - 5;  // this warp loads pages k0, k0 + 4, ... of each tile
+    const int k0 = warp - kMmaWarp - 1;  // this warp loads pages k0, k0 + kPageWarps, ... of each tile
     const uint64_t pol = l2_policy_evict_first();
     const int npages_req = (w.L + p.bs - 1) / p.bs;
     int win_base = -1, win_pid = -1;
@@ -176,13 +180,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       int pg0, npg;
       tile_pages(i, &pg0, &npg);
       const int mine = (npg > k0) ? (npg - k0 + kPageWarps - 1) / kPageWarps : 0;
-      int pids[kT / 16 / kPageWarps];
+      int pids[kMaxPagesPerWarp];
 #pragma unroll
-      for (int m = 0; m < kT / 16 / kPageWarps; ++m) pids[m] = (m < mine) ? page_of(pg0 + k0 + m * kPageWarps) : -1;
-      if (lane == 0) {
-        uint8_t* slot = smem + kOffTile + t * kTileSlot;
-        mbar_arrive_expect_tx(&sm->full[t], static_cast<uint32_t>(mine * p.bs * (kHalfCols * 2 + 128)));
-        for (int m = 0; m < mine; ++m) {
+      for (int m = 0; m < kMaxPagesPerWarp; ++m) pids[m] = (m < mine) ? page_of(pg0 + k0 + m * kPageWarps) : -1;
+      uint8_t* slot = smem + kOffTile + t * kTileSlot;
+      if (lane == 0) mbar_arrive_expect_tx(&sm->full[t], static_cast<uint32_t>(mine * p.bs * (kHalfCols * 2 + 128)));
+      __syncwarp();
+      // lane m issues this warp's page m (TMA issue from several lanes overlaps)
+#pragma unroll
+      for (int m = 0; m < kMaxPagesPerWarp; ++m) {
+        if (lane == m && m < mine) {
           const int j = k0 + m * kPageWarps;  // page of the tile
           tma_load_4d(slot + j * p.bs * (kHalfCols * 2), &tm_pages, 0, 0, kHalfBoxes * half, pids[m] * (p.bs / 8),
                       &sm->full[t], pol);
@@ -208,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // after an abort, let this warp's last loads land before shared memory is released
     if (lane == 0 && *abort_flag && issued >= 0) mbar_wait(&sm->full[issued & 1], (issued >> 1) & 1, kDrainTimeoutNs);
     cluster_wait_acquire();
-  } else if (warp == 4) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     const uint32_t idesc_s = idesc_f16_f32(128, kNR, false, false, false);
     const uint32_t idesc_o = idesc_f16_f32(128, kNR, false, true, false);
@@ -301,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
-    named_bar_sync(2, 160);  // Q^T staged by the softmax warps
+    named_bar_sync(2, kSoftmaxThreads + 32);  // Q^T staged by the softmax warps
     bool alive = true;
     for (int i0 = 0; i0 < ntiles && alive; i0 += 2) {
       const int i1 = min(i0 + 2, ntiles);
@@ -315,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     cluster_wait_acquire();
   } else {
-    // ------------------------------------------------------------------ softmax (warps 0-3)
+    // ------------------------------------------------------------------ softmax (warps 0-7)
     // kernel parameters used every tile, held in registers (not re-read from the parameter bank)
     float scale_log2 = p.scale_log2;
     uint64_t tmo = p.timeout_ns;
@@ -332,67 +339,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<uint4*>(qs + (k / kBoxCols) * kQChunk + sw128_offset(r, k % kBoxCols)) = v;
     }
     fence_proxy_async_smem();
-    named_bar_arrive(2, 160);
+    named_bar_arrive(2, kSoftmaxThreads + 32);
     cluster_wait_acquire();  // the peer's barriers are initialised
 
-    // Thread (warp, lane) owns token 32*warp + lane of each tile (M=128 layout of S^T).
-    float lsum[kNR];
+    // Thread (warp, lane) owns token tl = 32 (warp % 4) + lane of each tile (M=128 layout of S^T)
+    // and rows [8 h, 8 h + 8), h = warp / 4 (the two warps of a TMEM lane quadrant split the rows).
+    const int q4 = warp & 3, h = warp >> 2;
+    const int tl = 32 * q4 + lane;
+    const uint32_t lane_base = tmem_lane_base(q4);
+    float lsum[kRH], mr[kRH];  // running row sums over this thread's tokens; reference max per row
 #pragma unroll
-    for (int r = 0; r < kNR; ++r) lsum[r] = 0.f;
-    const int tl = 32 * warp + lane;
+    for (int k = 0; k < kRH; ++k) {
+      lsum[k] = 0.f;
+      mr[k] = -INFINITY;
+    }
     const int causal_floor = p.causal ? w.L - p.q_len + w.row0 / p.H : 0x7fffffff;
-    const uint32_t peer_x = dsmem_addr(xs, peer);
-    // the peer's partial S: thread tl's 16 values are 4 float4 chunks of row tl, chunk c at
-    // position c ^ ((tl >> 1) & 3) (conflict-free 16-byte accesses for the reader)
+    // the peer's partial S, [token][16 rows] fp32: row tl's 16 values are 4 float4 chunks, chunk c at
+    // position c ^ ((tl >> 1) & 3) (conflict-free 16-byte accesses); this thread's rows are chunks 2h, 2h+1
     const uint32_t xsw = static_cast<uint32_t>((tl >> 1) & 3);
-    float mr[kNR];  // reference max of each row (the same in every softmax thread)
+    const uint32_t peer_x = dsmem_addr(xs, peer) + tl * 64;
+    bool ok_all = true;
+    // A(i): this CTA's partial scores of tile i to the peer (after it has read tile i-2's), and the
+    // signal that this CTA's buffer of tile i-2 is free for the peer's tile i.
+    auto send = [&](int i, float* x) -> bool {
+      const int b = i & 1;
+      if (i >= 2) {
+        // tile i-2's buffer was read in B(i-2) (its values are consumed and the softmax warps have
+        // passed named barriers since): expect the peer's tile i in it, then free it with a plain signal
+        if (tid == 0) mbar_arrive_expect_tx(&sm->xfull[b], kXBuf);
+        if (lane == 0) mbar_remote_arrive_relaxed(dsmem_addr(&sm->xempty[b], peer));
+      }
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&sm->sfull[b], (i >> 1) & 1, tmo);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      tc_fence_after();
+      tmem_ld8(tmem + lane_base + b * kNR + kRH * h, x);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->sfree[b]);
+      if (i >= 2) ok = mbar_wait_cluster(&sm->xempty[b], ((i >> 1) - 1) & 1, tmo);
+      if (!__all_sync(0xffffffffu, ok)) return false;
+      const uint32_t dst = peer_x + b * kXBuf;
+      const uint32_t rbar = dsmem_addr(&sm->xfull[b], peer);
 #pragma unroll
-    for (int r = 0; r < kNR; ++r) mr[r] = -INFINITY;
-    for (int i = 0; i < ntiles; ++i) {
-      const int buf = i & 1;
+      for (int c = 0; c < 2; ++c)
+        dsmem_st_async_f32x4(dst + (((2 * h + c) ^ xsw) << 4),
+                             make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]), rbar);
+      return true;
+    };
+    // B(i): add the peer's part, scale and mask, lazy rescale, probabilities -> P^T. Every softmax
+    // warp calls it for every tile it reaches, also after a failed send (sent = false), so all of
+    // them pass the same named barriers; a failure anywhere ends the loop in all of them.
+    auto finish = [&](int i, float* x, bool sent) -> bool {
+      const int b = i & 1;
       const int tok0 = w.sub0 + i * kT;
       const int nvalid = min(kT, w.sub1 - tok0);
       const bool masked_tile = (nvalid < kT) || (tok0 + kT - 1 > causal_floor) || (w.nrows < kNR);
-      float x[kNR];
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(&sm->sfull[buf], (i >> 1) & 1, tmo);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (ok) {
-        tc_fence_after();
-        tmem_ld16(tmem + tmem_lane_base(warp) + buf * kNR, x);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sm->sfree[buf]);
-          if (i >= 1) {
-            // tile i-1's buffer was read in the previous iteration (the values are consumed and the
-            // softmax warps have passed named barriers since): expect the peer's tile i+1 in it, then
-            // free it with a plain signal (a release arrive here costs a cluster round trip)
-            if (tid == 0) mbar_arrive_expect_tx(&sm->xfull[buf ^ 1], kXBuf);
-            mbar_remote_arrive_relaxed(dsmem_addr(&sm->xempty[buf ^ 1], peer));
-          }
-        }
-        // this CTA's partial scores to the peer (once it has read the previous use of the buffer)
-        if (i >= 2) ok = mbar_wait_cluster(&sm->xempty[buf], ((i >> 1) - 1) & 1, tmo);
-      }
-      ok = __all_sync(0xffffffffu, ok);  // per-thread waits: one decision per warp
-      if (ok) {
-        const uint32_t dst = peer_x + buf * kXBuf + tl * 64;
-        const uint32_t rbar = dsmem_addr(&sm->xfull[buf], peer);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          dsmem_st_async_f32x4(dst + ((c ^ xsw) << 4), make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]),
-                               rbar);
-        ok = mbar_wait_cluster(&sm->xfull[buf], (i >> 1) & 1, tmo);
-      }
+      int ok = sent ? mbar_wait_cluster(&sm->xfull[b], (i >> 1) & 1, tmo) : 0;
       ok = __all_sync(0xffffffffu, ok);
       bool need_local = false;
       if (ok) {
-        const float4* xb = reinterpret_cast<const float4*>(xs + buf * (kXBuf / 4) + tl * 16);
+        const float4* xb = reinterpret_cast<const float4*>(xs + b * (kXBuf / 4) + tl * 16);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float4 y = xb[c ^ xsw];
+        for (int c = 0; c < 2; ++c) {
+          const float4 y = xb[(2 * h + c) ^ xsw];
           // rank-0 part + rank-1 part, the same sum in both CTAs
           x[4 * c] = half ? (y.x + x[4 * c]) : (x[4 * c] + y.x);
           x[4 * c + 1] = half ? (y.y + x[4 * c + 1]) : (x[4 * c + 1] + y.y);
@@ -402,36 +413,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__builtin_expect(masked_tile, 0)) {  // tail of the chunk, causal edge, or fewer than 16 rows
           const int t = tok0 + tl;
 #pragma unroll
-          for (int r = 0; r < kNR; ++r) {
+          for (int k = 0; k < kRH; ++k) {
+            const int r = kRH * h + k;
             bool vis = (tl < nvalid) && (r < w.nrows);
             if (p.causal) vis = vis && (t <= w.L - p.q_len + (w.row0 + r) / p.H);
-            x[r] = vis ? x[r] * scale_log2 : -INFINITY;
+            x[k] = vis ? x[k] * scale_log2 : -INFINITY;
           }
         } else {
 #pragma unroll
-          for (int r = 0; r < kNR; ++r) x[r] *= scale_log2;
+          for (int k = 0; k < kRH; ++k) x[k] *= scale_log2;
         }
 #pragma unroll
-        for (int r = 0; r < kNR; ++r) need_local |= x[r] > mr[r] + kRescaleTau;
+        for (int k = 0; k < kRH; ++k) need_local |= x[k] > mr[k] + kRescaleTau;
       } else {
 #pragma unroll
-        for (int r = 0; r < kNR; ++r) x[r] = -INFINITY;
+        for (int k = 0; k < kRH; ++k) x[k] = -INFINITY;
         *abort_flag = 1;
       }
-      if (__builtin_expect(named_bar_sync_or(1, 128, need_local || !ok || *abort_flag != 0), 0)) {
-        if (named_bar_sync_or(1, 128, *abort_flag != 0)) break;
+      if (__builtin_expect(named_bar_sync_or(1, kSoftmaxThreads, need_local || !ok || *abort_flag != 0), 0)) {
+        if (named_bar_sync_or(1, kSoftmaxThreads, *abort_flag != 0)) return false;
         // rare path: move the reference max, rescale O^T and the row sums
 #pragma unroll
-        for (int r = 0; r < kNR; ++r) {
-          float v = x[r];
+        for (int k = 0; k < kRH; ++k) {
+          float v = x[k];
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-          if (lane == 0) sm->red[warp][r] = v;
+          if (lane == 0) sm->red[q4][kRH * h + k] = v;
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kSoftmaxThreads);
         if (tid < kNR) {
           const float mprev = sm->mref[tid];
           const float tmax = fmaxf(fmaxf(sm->red[0][tid], sm->red[1][tid]), fmaxf(sm->red[2][tid], sm->red[3][tid]));
@@ -439,9 +451,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           sm->alpha[tid] = (mnew == -INFINITY) ? 1.f : exp2f(mprev - mnew);
           sm->mref[tid] = mnew;
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kSoftmaxThreads);
 #pragma unroll
-        for (int r = 0; r < kNR; ++r) mr[r] = sm->mref[r];
+        for (int k = 0; k < kRH; ++k) mr[k] = sm->mref[kRH * h + k];
         if (i >= 1) {  // PV(i-1) must be complete before O^T is rescaled
           int ok2 = 1;
           if (lane == 0) ok2 = mbar_wait(&sm->pvdone[(i - 1) & 1], ((i - 1) >> 1) & 1, tmo);
@@ -449,13 +461,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
 #pragma unroll
             for (int blk = 0; blk < 2; ++blk) {
-              float v[16];
-              const uint32_t a = tmem + tmem_lane_base(warp) + 2 * kNR + blk * kNR;
-              tmem_ld16(a, v);
+              float v[kRH];
+              const uint32_t a = tmem + lane_base + 2 * kNR + blk * kNR + kRH * h;
+              tmem_ld8(a, v);
               tmem_wait_ld();
 #pragma unroll
-              for (int jj = 0; jj < 16; ++jj) v[jj] *= sm->alpha[jj];
-              tmem_st16(a, v);
+              for (int k = 0; k < kRH; ++k) v[k] *= sm->alpha[kRH * h + k];
+              tmem_st8(a, v);
             }
             tmem_wait_st();
           } else if (lane == 0) {
@@ -463,63 +475,86 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 #pragma unroll
-        for (int r = 0; r < kNR; ++r) lsum[r] *= sm->alpha[r];
+        for (int k = 0; k < kRH; ++k) lsum[k] *= sm->alpha[kRH * h + k];
       }
-      if (i >= 2) {  // P^T buffer `buf` was last read by PV(i-2)
+      if (i >= 2) {  // P^T buffer b was last read by PV(i-2)
         int ok3 = 1;
-        if (lane == 0) ok3 = mbar_wait(&sm->pvdone[buf], ((i >> 1) - 1) & 1, tmo);
+        if (lane == 0) ok3 = mbar_wait(&sm->pvdone[b], ((i >> 1) - 1) & 1, tmo);
         if (!__shfl_sync(0xffffffffu, ok3, 0) && lane == 0) *abort_flag = 1;
       }
       {  // probabilities -> P^T (fp16, K-major, two swizzled 64-token atoms) and row sums
-        uint8_t* pb = ps + buf * kPBuf + (tl >> 6) * (kNR * 128);
+        uint8_t* pb = ps + b * kPBuf + (tl >> 6) * (kNR * 128);
 #pragma unroll
-        for (int r = 0; r < kNR; ++r) {
+        for (int k = 0; k < kRH; ++k) {
           // masked scores (-inf) give 0; a row with no visible token yet subtracts a finite stand-in
-          const float pr = fast_exp2(x[r] - ((mr[r] == -INFINITY) ? 0.f : mr[r]));
+          const float pr = fast_exp2(x[k] - ((mr[k] == -INFINITY) ? 0.f : mr[k]));
           const uint16_t hv = f2h<false>(pr);
-          lsum[r] += h2f<false>(hv);
-          *reinterpret_cast<uint16_t*>(pb + sw128_offset(r, tl & 63)) = hv;
+          lsum[k] += h2f<false>(hv);
+          *reinterpret_cast<uint16_t*>(pb + sw128_offset(kRH * h + k, tl & 63)) = hv;
         }
         fence_proxy_async_smem();
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm->ppfull[buf]);
+      if (lane == 0) mbar_arrive(&sm->ppfull[b]);
+      return true;
+    };
+    // Tiles in pairs, as the MMA warp issues them (S(i) S(i+1) PV(i) PV(i+1)): when tile i+1's scores
+    // are already there, they go to the peer before tile i is finished (the exchange of one overlaps
+    // the work on the other); otherwise tile i is finished first, so PV(i) is not held back.
+    for (int i0 = 0; i0 < ntiles && ok_all; i0 += 2) {
+      const bool two = i0 + 1 < ntiles;
+      float x0[kRH], x1[kRH];
+      const bool sent0 = send(i0, x0);
+      bool early = false, sent1 = false;
+      if (two && sent0) {
+        int ready = 0;
+        if (lane == 0) ready = mbar_test(&sm->sfull[(i0 + 1) & 1], ((i0 + 1) >> 1) & 1) ? 1 : 0;
+        early = __shfl_sync(0xffffffffu, ready, 0) != 0;
+        if (early) sent1 = send(i0 + 1, x1);
+      }
+      ok_all = finish(i0, x0, sent0);
+      if (ok_all && two) {
+        if (!early) sent1 = sent0 && send(i0 + 1, x1);
+        ok_all = finish(i0 + 1, x1, sent1);
+      }
     }
-    const bool aborted = named_bar_sync_or(1, 128, *abort_flag != 0);
+    if (!ok_all && lane == 0) *abort_flag = 1;
+    const bool aborted = named_bar_sync_or(1, kSoftmaxThreads, *abort_flag != 0);
     if (ntiles > 0 && !aborted) {
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&sm->pvdone[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, tmo);
       if (!__shfl_sync(0xffffffffu, ok, 0) && lane == 0) *abort_flag = 1;
     }
 #pragma unroll
-    for (int r = 0; r < kNR; ++r) {
-      float v = lsum[r];
+    for (int k = 0; k < kRH; ++k) {
+      float v = lsum[k];
       v += __shfl_xor_sync(0xffffffffu, v, 16);
       v += __shfl_xor_sync(0xffffffffu, v, 8);
       v += __shfl_xor_sync(0xffffffffu, v, 4);
       v += __shfl_xor_sync(0xffffffffu, v, 2);
       v += __shfl_xor_sync(0xffffffffu, v, 1);
-      if (lane == 0) sm->red[warp][r] = v;
+      if (lane == 0) sm->red[q4][kRH * h + k] = v;
     }
-    named_bar_sync(1, 128);
+    named_bar_sync(1, kSoftmaxThreads);
   }
   __syncthreads();  // all roles done: the tile slots are free for staging
   const bool have = (ntiles > 0) && !*abort_flag;
   float* ostage = reinterpret_cast<float*>(smem + kOffTile);  // [16][256]: this CTA's columns
   float* mst = ostage + kNR * kHalfCols;
   float* lst = mst + kNR;
-  if (warp < 4) {
+  if (warp < kSoftmaxWarps) {
+    const int q4 = warp & 3, h = warp >> 2;
     if (have) {
       tc_fence_after();
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
-        float v[16];
-        tmem_ld16(tmem + tmem_lane_base(warp) + 2 * kNR + blk * kNR, v);
+        float v[kRH];
+        tmem_ld8(tmem + tmem_lane_base(q4) + 2 * kNR + blk * kNR + kRH * h, v);
         tmem_wait_ld();
-        const int d = blk * 128 + warp * 32 + lane;
+        const int d = blk * 128 + q4 * 32 + lane;
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) ostage[jj * kHalfCols + d] = v[jj];
+        for (int k = 0; k < kRH; ++k) ostage[(kRH * h + k) * kHalfCols + d] = v[k];
       }
     } else {
       for (int idx = tid; idx < kNR * kHalfCols; idx += kSoftmaxThreads) ostage[idx] = 0.f;
@@ -594,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (subs > 1) merge_sub_partials(p, w, chunk, subs, &sm->last_cluster, tid, kThreads);
   cluster_sync();
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
