@@ -24,7 +24,9 @@ constexpr int kWarps = 8;
 
 __global__ void __launch_bounds__(kWarps * 32) mla_merge_kernel(const MergeParams p) {
   // Launched as a programmatic dependent of the partial kernel: everything this
-  // kernel reads may still be in flight until the wait returns.
+  // kernel reads may still be in flight until the wait returns. The next kernel
+  // (the next layer's partial kernel) may start its set-up meanwhile.
+  pdl_launch_dependents();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long gw = static_cast<long long>(blockIdx.x) * kWarps + warp;

@@ -40,10 +40,13 @@
 // a tile overlaps the MMAs of the other tile of its pair of tiles, and the
 // load of tile i+2 (issued when PV(i) releases its slot) overlaps PV(i+1).
 //
-// Warp roles (288 threads): warps 0-3 softmax / O rescale / epilogue (thread
-// = token of the M=128 layout), warp 4 TMEM owner + MMA issuer, warps 5-8
-// producers (warp 5+k loads pages k, k+4, ... of each tile, both caches, and
-// prefetches the same pages of tile i+2 into L2).
+// Warp roles (384 threads, three warps per scheduler): warps 0-7 softmax / O
+// rescale / epilogue (thread = token of the M=128 layout; the two warps of a
+// TMEM lane quadrant take rows 0-7 and 8-15), warp 8 TMEM owner + MMA issuer,
+// warps 9-11 producers (warp 9+k loads pages k, k+3, ... of each tile, both
+// caches, one page per lane, and prefetches the same pages of tile i+1 into
+// L2). The kernel is a programmatic dependent launch: its set-up overlaps the
+// end of the previous kernel in the stream.
 #include "device_common.cuh"
 
 namespace mla {
@@ -114,9 +117,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int subs = (p.subs > 1) ? p.subs : 1;
   const int chunk = static_cast<int>(blockIdx.y) / subs, sub = static_cast<int>(blockIdx.y) % subs;
   const int cluster_pairs = static_cast<int>(nranks >> 1);
-  const CtaWork w =
-      cta_work(p, kNR, kT, sub * cluster_pairs + static_cast<int>(rank >> 1), subs * cluster_pairs, chunk);
-  const int ntiles = (w.sub1 - w.sub0 + kT - 1) / kT;
   const int rows_total = p.q_len * p.H;
 
   if (tid == 0) {
@@ -145,6 +145,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   cluster_arrive_release();  // the peer touches this CTA's barriers only after this cluster phase
   const uint32_t tmem = sm->tmem_base;
+  // Launched as a programmatic dependent of the previous kernel in the stream: the set-up above
+  // overlaps its end; every input this kernel reads (chunk table, lengths, block table, queries,
+  // caches) is read after this wait.
+  pdl_wait();
+  const CtaWork w =
+      cta_work(p, kNR, kT, sub * cluster_pairs + static_cast<int>(rank >> 1), subs * cluster_pairs, chunk);
+  const int ntiles = (w.sub1 - w.sub0 + kT - 1) / kT;
 
   if (warp > kMmaWarp) {
     // ------------------------------------------------------------------ producers
@@ -197,9 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       issued = i;
-      if (i + 2 < ntiles) {  // the same pages of tile i+2 into L2: ckv by the even CTA, kpe by the odd one
+      if (i + 1 < ntiles) {  // the same pages of tile i+1 into L2: ckv by the even CTA, kpe by the odd one
         int qg0, qn;
-        tile_pages(i + 2, &qg0, &qn);
+        tile_pages(i + 1, &qg0, &qn);
         for (int j = k0; j < qn; j += kPageWarps) {
           const int pid = page_of(qg0 + j);
           if (lane == 0 && pid >= 0) {
@@ -667,13 +674,15 @@ cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap&
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, mla_partial_tc128_kernel, tm_pages, tm_kpe, p);
 }
 
