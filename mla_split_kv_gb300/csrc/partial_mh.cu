@@ -115,8 +115,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   const int half = static_cast<int>(rank & 1u);
-  const CtaWork w = cta_work(p, kRows, kT, 0, 1);  // both CTAs of the pair take the whole chunk
-  const int ntiles = (w.sub1 - w.sub0 + kT - 1) / kT;
   const int rows_total = p.q_len * p.H;
 
   if (tid == 0) {
@@ -144,6 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   cluster_arrive_release();  // the peer touches this CTA's barriers only after this cluster phase
   const uint32_t tmem = sm->tmem_base;
+  const CtaWork w = cta_work(p, kRows, kT, 0, 1);  // both CTAs of the pair take the whole chunk
+  const int ntiles = (w.sub1 - w.sub0 + kT - 1) / kT;
 
   if (warp > kMmaWarp) {
     // ------------------------------------------------------------------ producers
@@ -184,10 +184,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int pids[2];
 #pragma unroll
       for (int m = 0; m < 2; ++m) pids[m] = (m < mine) ? page_of(pg0 + k0 + m * kPageWarps) : -1;
-      if (lane == 0) {
-        uint8_t* slot = smem + kOffTile + t * kTileSlot;
-        mbar_arrive_expect_tx(&sm->full[t], static_cast<uint32_t>(mine * p.bs * (kHalfCols * 2 + 128)));
-        for (int m = 0; m < mine; ++m) {
+      uint8_t* slot = smem + kOffTile + t * kTileSlot;
+      if (lane == 0) mbar_arrive_expect_tx(&sm->full[t], static_cast<uint32_t>(mine * p.bs * (kHalfCols * 2 + 128)));
+      __syncwarp();
+      // lane m issues this warp's page m (TMA issue from several lanes overlaps)
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        if (lane == m && m < mine) {
           const int j = k0 + m * kPageWarps;
           tma_load_4d(slot + j * p.bs * (kHalfCols * 2), &tm_pages, 0, 0, kHalfBoxes * half, pids[m] * (p.bs / 8),
                       &sm->full[t], pol);
@@ -577,6 +580,8 @@ cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
+  // (not a programmatic dependent launch: with all SMs taken by one wave, launching early made the
+  // many-head decode about 6 us per call slower)
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
