@@ -39,6 +39,13 @@ __global__ void __launch_bounds__(kWarps * 32) mla_merge_kernel(const MergeParam
   const int lo = p.o_indptr[b], hi = p.o_indptr[b + 1];
   const int n = hi - lo;
 
+  const float* col = p.partials + static_cast<long long>(row) * kRank + quarter * 128 + lane * 4;
+  const long long stride = static_cast<long long>(p.rows) * kRank;  // one partial slot
+  // the first 8 partials' values do not depend on the weights: their loads go out with the LSE loads
+  float4 v0[8];
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj)
+    v0[jj] = (jj < n) ? *reinterpret_cast<const float4*>(col + (lo + jj) * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
   // maximum LSE over this row's partials; lane s keeps the LSE of partial s (s < 32)
   const float l0 = (lane < n) ? p.lse[static_cast<long long>(lo + lane) * p.rows + row] : -INFINITY;
   float M = l0;
@@ -49,8 +56,6 @@ __global__ void __launch_bounds__(kWarps * 32) mla_merge_kernel(const MergeParam
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
   if (M != -INFINITY) {
-    const float* col = p.partials + static_cast<long long>(row) * kRank + quarter * 128 + lane * 4;
-    const long long stride = static_cast<long long>(p.rows) * kRank;  // one partial slot
     for (int s0 = 0; s0 < n; s0 += 32) {
       const int cnt = min(32, n - s0);
       float wl = 0.f;
@@ -64,8 +69,9 @@ __global__ void __launch_bounds__(kWarps * 32) mla_merge_kernel(const MergeParam
         float4 v[8];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj)
-          v[jj] = (j0 + jj < cnt) ? *reinterpret_cast<const float4*>(col + (lo + s0 + j0 + jj) * stride)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[jj] = (s0 + j0 == 0) ? v0[jj]
+                  : (j0 + jj < cnt) ? *reinterpret_cast<const float4*>(col + (lo + s0 + j0 + jj) * stride)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
           const float wj = __shfl_sync(0xffffffffu, wl, (j0 + jj) & 31);

@@ -366,9 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t xsw = static_cast<uint32_t>((tl >> 1) & 3);
     const uint32_t peer_x = dsmem_addr(xs, peer) + tl * 64;
     bool ok_all = true;
-    // A(i): this CTA's partial scores of tile i to the peer (after it has read tile i-2's), and the
-    // signal that this CTA's buffer of tile i-2 is free for the peer's tile i.
-    auto send = [&](int i, float* x) -> bool {
+    // A(i), first part, which never waits on the peer: the signal that this CTA's buffer of tile
+    // i-2 is free for the peer's tile i, then this warp's partial scores of tile i (and its S
+    // buffer freed).
+    auto prep = [&](int i, float* x) -> bool {
       const int b = i & 1;
       if (i >= 2) {
         // tile i-2's buffer was read in B(i-2) (its values are consumed and the softmax warps have
@@ -385,6 +386,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->sfree[b]);
+      return true;
+    };
+    // the peer has read its buffer of tile i-2, so tile i's scores may go there (non-blocking test)
+    auto peer_free = [&](int i) -> bool {
+      if (i < 2) return true;
+      int ready = 0;
+      if (lane == 0) ready = mbar_test(&sm->xempty[i & 1], ((i >> 1) - 1) & 1) ? 1 : 0;
+      return __shfl_sync(0xffffffffu, ready, 0) != 0;
+    };
+    // A(i), second part: once the peer has read its buffer of tile i-2, this warp's partial scores
+    // of tile i go there
+    auto push = [&](int i, const float* x) -> bool {
+      const int b = i & 1;
+      int ok = 1;
       if (i >= 2) ok = mbar_wait_cluster(&sm->xempty[b], ((i >> 1) - 1) & 1, tmo);
       if (!__all_sync(0xffffffffu, ok)) return false;
       const uint32_t dst = peer_x + b * kXBuf;
@@ -507,22 +522,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     // Tiles in pairs, as the MMA warp issues them (S(i) S(i+1) PV(i) PV(i+1)): when tile i+1's scores
-    // are already there, they go to the peer before tile i is finished (the exchange of one overlaps
-    // the work on the other); otherwise tile i is finished first, so PV(i) is not held back.
+    // are already there, they are loaded (and, if the peer's buffer is already free, sent) before
+    // tile i is finished, so the exchange of one overlaps the work on the other; otherwise tile i is
+    // finished first, so PV(i) is not held back. Each warp decides for itself, so no warp may wait
+    // on the peer between the two: the peer's warps that would release it may be held at their own
+    // barrier in B(i) by their warps that are waiting on this CTA the same way.
     for (int i0 = 0; i0 < ntiles && ok_all; i0 += 2) {
       const bool two = i0 + 1 < ntiles;
       float x0[kRH], x1[kRH];
-      const bool sent0 = send(i0, x0);
-      bool early = false, sent1 = false;
+      const bool sent0 = prep(i0, x0) && push(i0, x0);
+      bool prepped1 = false, sent1 = false;
       if (two && sent0) {
         int ready = 0;
         if (lane == 0) ready = mbar_test(&sm->sfull[(i0 + 1) & 1], ((i0 + 1) >> 1) & 1) ? 1 : 0;
-        early = __shfl_sync(0xffffffffu, ready, 0) != 0;
-        if (early) sent1 = send(i0 + 1, x1);
+        if (__shfl_sync(0xffffffffu, ready, 0) != 0) {
+          prepped1 = prep(i0 + 1, x1);
+          if (prepped1 && peer_free(i0 + 1)) sent1 = push(i0 + 1, x1);
+        }
       }
       ok_all = finish(i0, x0, sent0);
       if (ok_all && two) {
-        if (!early) sent1 = sent0 && send(i0 + 1, x1);
+        if (!prepped1) prepped1 = sent0 && prep(i0 + 1, x1);
+        if (prepped1 && !sent1) sent1 = push(i0 + 1, x1);
         ok_all = finish(i0 + 1, x1, sent1);
       }
     }
@@ -574,6 +595,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();
+  if (!have && ntiles > 0) {
+    // after an abort: the remote stores the peer issued before it reached this barrier (it issues
+    // none after it) may still be in flight; give them time to land before this CTA can leave
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 20000ull) {
+    }
+  }
   // the cluster's result goes to the chunk's slot, or, when the chunk is spread over several
   // clusters, to this cluster's sub-partial slot of the workspace
   float* const dst_partials = (subs > 1) ? p.ws_partials : p.partials;

@@ -74,6 +74,8 @@ def make_desc(dc: DeviceCase, chunks_dev: Optional[torch.Tensor], kernel: int, c
     d.clusters_per_chunk = subs
     d.workspace = workspace.data_ptr() if workspace is not None else None
     d.workspace_bytes = workspace.numel() if workspace is not None else 0
+    # the descriptor holds raw device pointers: keep their tensors alive as long as it lives
+    d._keep = (chunks_dev, workspace)
     return d
 
 

@@ -262,3 +262,26 @@ def test_sizes_and_strings(lib):
     assert lib.mla_lse_bytes(8, 2, 16) == 8 * 2 * 16 * 4
     assert nb.status_string(nb.MLA_ERR_TIMEOUT) == "device wait timed out"
     assert nb.mla_version() >= 1
+
+
+def test_descriptor_keeps_its_tensors_alive():
+    # a descriptor stores raw pointers to the partition table and the workspace: the tensors behind
+    # them must live as long as the descriptor, whatever the caller keeps
+    import gc
+    import types
+    import weakref
+    import torch
+    from mla_split_kv_gb300 import runtime as rt
+    case = types.SimpleNamespace(num_requests=1, num_heads=16, q_len=1, block_size=32, dtype="f16", causal=False)
+    dc = types.SimpleNamespace(case=case, ckv=torch.zeros(4, 1), block_table=torch.zeros(1, 4, dtype=torch.int32))
+    chunks = torch.zeros(3, 4, dtype=torch.int32)
+    ws = torch.zeros(256, dtype=torch.uint8)
+    refs = (weakref.ref(chunks), weakref.ref(ws))
+    desc = rt.make_desc(dc, chunks, nb.MLA_KERNEL_TC, 4, types.SimpleNamespace(cuda_stream=0), 2, ws)
+    assert desc.chunks == chunks.data_ptr() and desc.workspace == ws.data_ptr()
+    del chunks, ws
+    gc.collect()
+    assert all(r() is not None for r in refs)
+    del desc
+    gc.collect()
+    assert all(r() is None for r in refs)
