@@ -44,7 +44,7 @@ struct MapKey {
   uint32_t box_rows;
   int dtype;
   int device;
-  int kind;  // 0: the 2D map; 1, 2: page maps of the ckv cache (see page_map); 3: kpe quarter map
+  int kind;  // 0: the 2D map; 1, 2: page maps of the ckv cache (see page_map); 3, 4: kpe quarter / half maps
 };
 struct MapEntry {
   MapKey key;
@@ -52,7 +52,7 @@ struct MapEntry {
   bool valid;
 };
 std::mutex g_map_mu;
-MapEntry g_maps[32];
+MapEntry g_maps[64];
 int g_map_next = 0;
 
 bool same(const MapKey& a, const MapKey& b) {
@@ -94,6 +94,15 @@ bool kpe_quarter_map(CUtensorMap* out, const void* base, uint64_t rows, uint32_t
   return encode_map(out, MapKey{base, rows, static_cast<uint64_t>(mla::kRope), box_rows, dtype, dev, 3});
 }
 
+// 2D map over the [rows, 64] kpe cache with boxes of 32 columns x box_rows rows
+// and the 64-byte swizzle: one half of the rope columns of a page, rows of 64
+// bytes (two K=16 steps of a K-major tensor-core operand).
+bool kpe_half_map(CUtensorMap* out, const void* base, uint64_t rows, uint32_t box_rows, int dtype) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  return encode_map(out, MapKey{base, rows, static_cast<uint64_t>(mla::kRope), box_rows, dtype, dev, 4});
+}
+
 bool encode_map(CUtensorMap* out, const MapKey& key) {
   std::lock_guard<std::mutex> lock(g_map_mu);
   for (auto& e : g_maps)
@@ -115,13 +124,14 @@ bool encode_map(CUtensorMap* out, const MapKey& key) {
     cuuint32_t estr[2] = {1, 1};
     r = enc(&m, dt, 2, const_cast<void*>(key.base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  } else if (key.kind == 3) {
+  } else if (key.kind == 3 || key.kind == 4) {
     cuuint64_t dims[2] = {key.cols, key.rows};
     cuuint64_t strides[1] = {key.cols * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(mla::kRope / 4), key.box_rows};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(key.kind == 3 ? mla::kRope / 4 : mla::kRope / 2), key.box_rows};
     cuuint32_t estr[2] = {1, 1};
     r = enc(&m, dt, 2, const_cast<void*>(key.base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            key.kind == 3 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
     if (key.rows % 8 != 0 || key.box_rows % 8 != 0) return false;
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(mla::kBoxCols), 8, key.cols / mla::kBoxCols, key.rows / 8};
@@ -133,7 +143,7 @@ bool encode_map(CUtensorMap* out, const MapKey& key) {
   }
   if (r != CUDA_SUCCESS) return false;
   g_maps[g_map_next] = MapEntry{key, m, true};
-  g_map_next = (g_map_next + 1) % 32;
+  g_map_next = (g_map_next + 1) % 64;
   *out = m;
   return true;
 }
@@ -231,14 +241,15 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   // 16 rows or fewer in fp16 with clusters of 4..16: CTAs share tiles in quads when asked for
   const bool quad = d->kernel == MLA_KERNEL_TC_QUAD && mla::quad_supports(rows_total, bf16, C);
 
-  CUtensorMap tm_ckv, tm_kpe, tm_pages;
+  CUtensorMap tm_ckv, tm_kpe, tm_pages, tm_kpe_half;
   if (quad) {
     if (!quarter_page_map(&tm_pages, ckv_cache, rows, d->block_size, d->dtype) ||
         !kpe_quarter_map(&tm_kpe, kpe_cache, rows, d->block_size, d->dtype))
       return reject(MLA_ERR_CUDA);
   } else if (!tensor_map(&tm_ckv, ckv_cache, rows, mla::kRank, d->block_size, d->dtype) ||
              !tensor_map(&tm_kpe, kpe_cache, rows, mla::kRope, d->block_size, d->dtype) ||
-             !page_map(&tm_pages, ckv_cache, rows, d->block_size, d->dtype)) {
+             !page_map(&tm_pages, ckv_cache, rows, d->block_size, d->dtype) ||
+             !kpe_half_map(&tm_kpe_half, kpe_cache, rows, d->block_size, d->dtype)) {
     return reject(MLA_ERR_CUDA);
   }
 
@@ -278,7 +289,7 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   const cudaError_t e =
       use_simt ? mla::launch_partial_simt(tm_ckv, tm_kpe, p, static_cast<int>(N), C, bf16, stream)
       : quad   ? mla::launch_partial_quad(tm_pages, tm_kpe, p, static_cast<int>(N), C, stream)
-               : mla::launch_partial_tc(tm_ckv, tm_kpe, tm_pages, p, static_cast<int>(N), C, bf16, stream);
+               : mla::launch_partial_tc(tm_ckv, tm_kpe, tm_pages, tm_kpe_half, p, static_cast<int>(N), C, bf16, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;

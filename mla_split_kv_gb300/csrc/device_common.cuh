@@ -421,6 +421,21 @@ __device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t start, uint32_t sbo)
   return d;
 }
 
+// The same for a K-major operand whose rows are 64 bytes (two K=16 steps of
+// 16-bit elements) stored with the 64-byte swizzle (16-byte chunk c of row r
+// at position c ^ ((r / 2) % 4), as a TMA box with CU_TENSOR_MAP_SWIZZLE_64B
+// lands): sbo = stride between 8-row groups (512 B when the rows are packed);
+// the second K step starts 32 bytes in.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t start, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((start >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;  // leading byte offset: unused within one swizzle atom
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(4) << 61;  // SWIZZLE_64B
+  return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with an fp32 accumulator.
 // a_mn / b_mn: operand stored MN-major (1) or K-major (0).
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool bf16, bool a_mn, bool b_mn) {
@@ -434,6 +449,12 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool bf16, bo
 // XORed with row % 8). The tile base must be 1024-byte aligned.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
   return row * 128u + ((((col >> 3) ^ row) & 7u) << 4) + ((col & 7u) << 1);
+}
+
+// Byte offset of 16-bit element (row, col) in rows of 64 bytes stored with the
+// 64-byte swizzle (the layout smem_desc_sw64 describes).
+__device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t col) {
+  return row * 64u + ((((col >> 3) ^ (row >> 1)) & 3u) << 4) + ((col & 7u) << 1);
 }
 
 // ---------------------------------------------------------------------------

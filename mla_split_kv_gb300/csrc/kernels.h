@@ -58,14 +58,17 @@ struct MergeParams {
 // `cluster` CTAs, grid.y = chunks, grid.z = row groups.
 cudaError_t launch_partial_simt(const CUtensorMap& tm_ckv, const CUtensorMap& tm_kpe, const PartialParams& p,
                                 int num_chunks, int cluster, bool bf16, cudaStream_t stream);
-// tm_pages: 4D map of the ckv cache whose box is one half (256 columns) of a page.
+// tm_pages: 4D map of the ckv cache whose box is one half (256 columns) of a page;
+// tm_kpe_half: kpe boxes of 32 columns with the 64-byte swizzle.
 cudaError_t launch_partial_tc(const CUtensorMap& tm_ckv, const CUtensorMap& tm_kpe, const CUtensorMap& tm_pages,
-                              const PartialParams& p, int num_chunks, int cluster, bool bf16, cudaStream_t stream);
+                              const CUtensorMap& tm_kpe_half, const PartialParams& p, int num_chunks, int cluster,
+                              bool bf16, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 // 128-token-tile tensor-core kernel for CTAs of at most 16 rows (fp16 only),
 // CTAs in pairs that split the latent columns (cluster of 2..16 CTAs).
+// tm_kpe_half: kpe boxes of 32 columns with the 64-byte swizzle.
 bool tc128_supports(int total_rows, bool bf16, int cluster);
-cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe, const PartialParams& p,
+cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe_half, const PartialParams& p,
                                  int num_chunks, int cluster, cudaStream_t stream);
 int tc128_max_active_clusters(int cluster);
 // The same tiles shared by CTA quads (score product split by columns, PV by

@@ -515,9 +515,11 @@ int tc_rows_per_cta(int total_rows, bool) {
 }
 
 cudaError_t launch_partial_tc(const CUtensorMap& tm_ckv, const CUtensorMap& tm_kpe, const CUtensorMap& tm_pages,
-                              const PartialParams& p, int num_chunks, int cluster, bool bf16, cudaStream_t stream) {
+                              const CUtensorMap& tm_kpe_half, const PartialParams& p, int num_chunks, int cluster,
+                              bool bf16, cudaStream_t stream) {
   const int rows = p.q_len * p.H;
-  if (tc128_supports(rows, bf16, cluster)) return launch_partial_tc128(tm_pages, tm_kpe, p, num_chunks, cluster, stream);
+  if (tc128_supports(rows, bf16, cluster))
+    return launch_partial_tc128(tm_pages, tm_kpe_half, p, num_chunks, cluster, stream);
   if (mh_supports(rows, cluster)) return launch_partial_mh(tm_pages, tm_kpe, p, num_chunks, bf16, stream);
   const int nr = tc_rows_per_cta(rows, bf16);
   const void* fn = tc_kernel_ptr(nr, bf16);

@@ -16,15 +16,19 @@
 //
 // A 128-token tile of the whole latent is 144 KB; it has to stay in shared
 // memory from the score product until the PV product (after the softmax), and
-// the next tile has to be loading meanwhile, which does not fit in one SM. So
-// the two CTAs of a pair (cluster ranks 2k, 2k+1) take the same tokens and
+// the next tiles have to be loading meanwhile, which does not fit in one SM.
+// So the two CTAs of a pair (cluster ranks 2k, 2k+1) take the same tokens and
 // split the latent columns: CTA `half` holds ckv columns [256 half, 256 half +
-// 256) and the kpe box, of whose 64 columns it uses [32 half, 32 half + 32).
-// Each computes a partial S^T over its columns, the two exchange them through
-// distributed shared memory and add them (both get the same sum, in the same
-// order), run the same softmax, and each accumulates O^T for its own 256
-// columns. A tile slot is then 80 KB (64 KB of ckv + 16 KB of kpe) and two
-// fit, so tile i+2 loads while tiles i and i+1 are computed. Pairs of a
+// 256) and kpe columns [32 half, 32 half + 32). Each computes a partial S^T
+// over its columns, the two exchange them through distributed shared memory
+// and add them (both get the same sum, in the same order), run the same
+// softmax, and each accumulates O^T for its own 256 columns. A tile slot is
+// then 72 KB (64 KB of ckv + 8 KB of kpe) and three fit, so tiles i+1 and i+2
+// load while tile i is computed (a slot is held from its load through the
+// score product, the exchange, the softmax and the PV product; with two slots
+// the loads would wait on that whole chain). The kpe part of a slot is free
+// once the tile's score product is done; it then takes the peer's partial
+// scores of the tile, and after those are read, the tile's P^T. Pairs of a
 // cluster split the chunk's tiles; the cluster combines at the end, in rank
 // order.
 //
@@ -36,16 +40,15 @@
 // an M=128 block are 1 KB apart (LBO) and the 8-token groups 4 KB (SBO). One
 // TMA instruction per page and cache keeps the issue cost low.
 //
-// MMA order: S(0) S(1) PV(0) PV(1) S(2) S(3) PV(2) PV(3) ...: the softmax of
-// a tile overlaps the MMAs of the other tile of its pair of tiles, and the
-// load of tile i+2 (issued when PV(i) releases its slot) overlaps PV(i+1).
+// MMA order: as the inputs get ready, PV(j) first (it releases a slot), else
+// S(i) (its tile landed and its TMEM buffer is free), each in tile order.
 //
 // Warp roles (384 threads, three warps per scheduler): warps 0-7 softmax / O
 // rescale / epilogue (thread = token of the M=128 layout; the two warps of a
 // TMEM lane quadrant take rows 0-7 and 8-15), warp 8 TMEM owner + MMA issuer,
 // warps 9-11 producers (warp 9+k loads pages k, k+3, ... of each tile, both
 // caches, one page per lane, and prefetches the same pages of tile i+1 into
-// L2). The kernel is a programmatic dependent launch: its set-up overlaps the
+// L2; the kpe box is this CTA's 32 columns, with the 64-byte swizzle). The kernel is a programmatic dependent launch: its set-up overlaps the
 // end of the previous kernel in the stream.
 #include "device_common.cuh"
 
@@ -56,11 +59,12 @@ namespace {
 constexpr int kT = 128;                          // tokens per tile
 constexpr int kNR = 16;                          // query rows per CTA
 constexpr int kHalfBoxes = 4;                    // ckv column blocks per CTA: 256 columns
-constexpr int kSlotBoxes = kHalfBoxes + 1;       // + the kpe box (Q^T chunks)
 constexpr int kHalfCols = kHalfBoxes * kBoxCols; // 256
+constexpr int kKpeCols = kRope / 2;              // 32 rope columns per CTA
 constexpr int kCkvBytes = kT * kHalfCols * 2;    // 64 KB: row group g, block c at 4096 g + 1024 c
-constexpr int kKpeBytes = kT * 128;              // 16 KB: [128 rows x 64 columns], swizzled
-constexpr int kTileSlot = kCkvBytes + kKpeBytes; // 80 KB
+constexpr int kKpeBytes = kT * kKpeCols * 2;     // 8 KB: [128 rows x 32 columns], 64-byte swizzle
+constexpr int kTileSlot = kCkvBytes + kKpeBytes; // 72 KB
+constexpr int kSlots = 3;
 constexpr int kGroupBytes = 8 * kHalfCols * 2;   // 4 KB: one 8-row group of the four blocks
 constexpr int kPageWarps = 3;                    // producer warps
 constexpr int kSoftmaxWarps = 8;                 // two per TMEM lane quadrant: rows 0-7 and 8-15
@@ -71,21 +75,28 @@ constexpr int kRH = kNR / 2;                     // rows per softmax thread
 constexpr int kMaxPagesPerWarp = (kT / 16 + kPageWarps - 1) / kPageWarps;  // pages of 16 tokens or more
 constexpr float kRescaleTau = 8.0f;
 
-constexpr uint32_t kOffTile = 0;                            // 2 tile slots
-constexpr uint32_t kOffQ = 2 * kTileSlot;                   // 160 KB: Q^T, 5 chunks
-constexpr uint32_t kQChunk = kNR * 128;                     // [16 x 64] fp16, swizzled: 2 KB
-constexpr uint32_t kOffP = kOffQ + kSlotBoxes * kQChunk;    // 170 KB: P^T, 2 buffers
-constexpr uint32_t kPBuf = 2 * kNR * 128;                   // [16 x 128 tokens]: two 64-token atoms
-constexpr uint32_t kOffX = kOffP + 2 * kPBuf;               // 178 KB: the peer's partial S, 2 buffers
+constexpr uint32_t kOffTile = 0;                            // 3 tile slots
+constexpr uint32_t kOffQ = kSlots * kTileSlot;              // 216 KB: Q^T
+constexpr uint32_t kQChunk = kNR * 128;                     // [16 x 64] fp16, 128-byte swizzle: 2 KB
+constexpr uint32_t kQKpe = kNR * kKpeCols * 2;              // [16 x 32] fp16, 64-byte swizzle: 1 KB
+constexpr uint32_t kOffSmall = kOffQ + kHalfBoxes * kQChunk + kQKpe;  // 225 KB
+constexpr uint32_t kSmallBytes = 1024;
+constexpr uint32_t kSmem = kOffSmall + kSmallBytes + 1024;  // + alignment slack
+// in the kpe part of a slot, after the tile's score product: the peer's partial S, then P^T
 constexpr uint32_t kXBuf = kNR * kT * 4;                    // [128 tokens][16 rows] fp32: 8 KB
-constexpr uint32_t kOffSmall = kOffX + 2 * kXBuf;           // 194 KB
-constexpr uint32_t kSmem = kOffSmall + 2048 + 1024;         // + alignment slack
+constexpr uint32_t kPBytes = 2 * kNR * 128;                 // P^T [16 x 128 tokens]: two 64-token atoms
 constexpr uint32_t kTmemCols = 64;                          // S^T 2 x 16 + O^T 2 x 16
 static_assert(kSmem <= 232448, "shared memory per CTA");
-static_assert(kNR * kHalfCols * 4 + 2 * kNR * 4 <= 2 * kTileSlot, "epilogue staging fits the tile slots");
+static_assert(kXBuf <= kKpeBytes && kPBytes <= kKpeBytes, "exchange and P^T fit the kpe part of a slot");
+static_assert(kCkvBytes % 1024 == 0 && kTileSlot % 1024 == 0, "swizzle atoms stay aligned");
+static_assert(kNR * kHalfCols * 4 + 2 * kNR * 4 <= kSlots * kTileSlot, "epilogue staging fits the tile slots");
 
 struct Small {
-  uint64_t full[2], empty[2], sfull[2], sfree[2], ppfull[2], pvdone[2], xfull[2], xempty[2], drain;
+  // slot ring: full / empty; TMEM S buffers (tile parity): sfull / sfree; per slot: ppfull (P^T
+  // written), xfull (the peer's partial S landed), xready (the peer's kpe part of the slot is free
+  // for this CTA's partial S); pvdone per tile parity
+  uint64_t full[kSlots], empty[kSlots], sfull[2], sfree[2], ppfull[kSlots], pvdone[2], xfull[kSlots],
+      xready[kSlots], drain;
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t last_cluster;  // this cluster took the chunk's last ticket
@@ -93,19 +104,17 @@ struct Small {
   float mref[kNR];
   float alpha[kNR];
 };
-static_assert(sizeof(Small) <= 2048, "small smem region");
+static_assert(sizeof(Small) <= kSmallBytes, "small smem region");
 
 __device__ __forceinline__ uint32_t tmem_lane_base(int warp) { return static_cast<uint32_t>(32 * (warp & 3)) << 16; }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    mla_partial_tc128_kernel(const __grid_constant__ CUtensorMap tm_pages, const __grid_constant__ CUtensorMap tm_kpe,
+    mla_partial_tc128_kernel(const __grid_constant__ CUtensorMap tm_pages, const __grid_constant__ CUtensorMap tm_kpe_half,
                              const PartialParams p) {
   extern __shared__ uint8_t smem_raw[];
   pdl_launch_dependents();  // the merge of these partials may be scheduled now; it waits for this grid
   uint8_t* smem = align1024(smem_raw);
   uint8_t* qs = smem + kOffQ;
-  uint8_t* ps = smem + kOffP;
-  float* xs = reinterpret_cast<float*>(smem + kOffX);
   Small* sm = reinterpret_cast<Small*>(smem + kOffSmall);
   volatile int32_t* abort_flag = &sm->abort_flag;
 
@@ -120,18 +129,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rows_total = p.q_len * p.H;
 
   if (tid == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&sm->full[s], kPageWarps);  // one expect_tx arrival per producer warp
+      mbar_init(&sm->empty[s], 1);
+      mbar_init(&sm->ppfull[s], kSoftmaxWarps);
+      mbar_init(&sm->xfull[s], 1);   // local expect_tx arrival + the peer's st.async bytes
+      mbar_init(&sm->xready[s], 1);  // one remote arrival from the peer
+    }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&sm->full[t], kPageWarps);  // one expect_tx arrival per producer warp
-      mbar_init(&sm->empty[t], 1);
       mbar_init(&sm->sfull[t], 1);
       mbar_init(&sm->sfree[t], kSoftmaxWarps);
-      mbar_init(&sm->ppfull[t], kSoftmaxWarps);
       mbar_init(&sm->pvdone[t], 1);
-      mbar_init(&sm->xfull[t], 1);                // local expect_tx arrival + the peer's st.async bytes
-      mbar_init(&sm->xempty[t], kSoftmaxWarps);   // one remote arrival per peer softmax warp
     }
     mbar_init(&sm->drain, 1);
-    for (int t = 0; t < 2; ++t) mbar_arrive_expect_tx(&sm->xfull[t], kXBuf);  // tiles 0 and 1
     sm->abort_flag = 0;
     fence_mbar_init();
   }
@@ -175,23 +185,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int issued = -1;
     for (int i = 0; i < ntiles; ++i) {
-      const int t = i & 1;
-      if (i >= 2) {  // tile i-2 released the slot
-        int ok = 1;
-        if (lane == 0) {
-          ok = mbar_wait(&sm->empty[t], ((i >> 1) - 1) & 1, p.timeout_ns) && !*abort_flag;
-          if (!ok) *abort_flag = 1;
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      }
+      const int s = i % kSlots;
+      // the pages of tile i first: their block-table reads overlap the wait for the slot
       int pg0, npg;
       tile_pages(i, &pg0, &npg);
       const int mine = (npg > k0) ? (npg - k0 + kPageWarps - 1) / kPageWarps : 0;
       int pids[kMaxPagesPerWarp];
 #pragma unroll
       for (int m = 0; m < kMaxPagesPerWarp; ++m) pids[m] = (m < mine) ? page_of(pg0 + k0 + m * kPageWarps) : -1;
-      uint8_t* slot = smem + kOffTile + t * kTileSlot;
-      if (lane == 0) mbar_arrive_expect_tx(&sm->full[t], static_cast<uint32_t>(mine * p.bs * (kHalfCols * 2 + 128)));
+      if (i >= kSlots) {  // tile i-3 released the slot
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait(&sm->empty[s], ((i / kSlots) - 1) & 1, p.timeout_ns) && !*abort_flag;
+          if (!ok) *abort_flag = 1;
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
+      uint8_t* slot = smem + kOffTile + s * kTileSlot;
+      if (lane == 0)
+        mbar_arrive_expect_tx(&sm->full[s], static_cast<uint32_t>(mine * p.bs * (kHalfCols + kKpeCols) * 2));
       __syncwarp();
       // lane m issues this warp's page m (TMA issue from several lanes overlaps)
 #pragma unroll
@@ -199,8 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == m && m < mine) {
           const int j = k0 + m * kPageWarps;  // page of the tile
           tma_load_4d(slot + j * p.bs * (kHalfCols * 2), &tm_pages, 0, 0, kHalfBoxes * half, pids[m] * (p.bs / 8),
-                      &sm->full[t], pol);
-          tma_load_2d(slot + kCkvBytes + j * p.bs * 128, &tm_kpe, 0, pids[m] * p.bs, &sm->full[t], pol);
+                      &sm->full[s], pol);
+          tma_load_2d(slot + kCkvBytes + j * p.bs * (kKpeCols * 2), &tm_kpe_half, kKpeCols * half, pids[m] * p.bs,
+                      &sm->full[s], pol);
         }
       }
       issued = i;
@@ -220,36 +233,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // after an abort, let this warp's last loads land before shared memory is released
-    if (lane == 0 && *abort_flag && issued >= 0) mbar_wait(&sm->full[issued & 1], (issued >> 1) & 1, kDrainTimeoutNs);
+    if (lane == 0 && *abort_flag && issued >= 0)
+      mbar_wait(&sm->full[issued % kSlots], (issued / kSlots) & 1, kDrainTimeoutNs);
     cluster_wait_acquire();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     const uint32_t idesc_s = idesc_f16_f32(128, kNR, false, false, false);
     const uint32_t idesc_o = idesc_f16_f32(128, kNR, false, true, false);
     const Desc2 qd = desc2(smem_desc_sw128(smem_u32(qs), 16, 1024));
-    const Desc2 pd = desc2(smem_desc_sw128(smem_u32(ps), 16, 1024));
+    const Desc2 qk = desc2(smem_desc_sw64(smem_u32(qs + kHalfBoxes * kQChunk), 512));
     const uint32_t tile_base = smem_u32(smem + kOffTile);
-    const uint32_t kpe16 = static_cast<uint32_t>(2 * half * 32) >> 4;  // this CTA's first kpe step, 16-byte units
     uint64_t tmo = p.timeout_ns;
     asm volatile("" : "+l"(tmo));
-    auto wait_lane0 = [&](uint64_t* bar, uint32_t parity) -> bool {
-      int ok = 1;
-      if (lane == 0) {
-        ok = mbar_wait(bar, parity, tmo) && !*abort_flag;
-        if (!ok) *abort_flag = 1;
-      }
-      return __shfl_sync(0xffffffffu, ok, 0) != 0;
-    };
-    // score product of tile i into S buffer i&1: this CTA's 4 ckv column blocks, then its half of kpe
-    auto score = [&](int i) -> bool {
+    // score product of tile i (slot i % 3) into S buffer i & 1: this CTA's 4 ckv column blocks,
+    // then its 32 kpe columns (two K steps of the 64-byte-swizzled box)
+    auto score = [&](int i) {
       const int t = i & 1;
-      if (i >= 2 && !wait_lane0(&sm->sfree[t], ((i >> 1) - 1) & 1)) return false;
-      if (!wait_lane0(&sm->full[t], (i >> 1) & 1)) return false;
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t slot = tile_base + t * kTileSlot;
+        const uint32_t slot = tile_base + (i % kSlots) * kTileSlot;
         const Desc2 ad = desc2(smem_desc_sw128(slot, 16, kGroupBytes));
-        const Desc2 ak = desc2(smem_desc_sw128(slot + kCkvBytes, 16, 1024));
+        const Desc2 ak = desc2(smem_desc_sw64(slot + kCkvBytes, 512));
         const uint32_t d = tmem + t * kNR;
 #pragma unroll
         for (int c = 0; c < kHalfBoxes; ++c)
@@ -257,13 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 4; ++kk)
             umma_ss(d, ad, (c * 1024 + kk * 32) >> 4, qd, (c * kQChunk + kk * 32) >> 4, idesc_s,
                     (c == 0 && kk == 0) ? 0u : 1u);
-        // this CTA's two 16-column steps of the kpe box
-        umma_ss(d, ak, kpe16, qd, (kHalfBoxes * kQChunk) / 16 + kpe16, idesc_s, 1u);
-        umma_ss(d, ak, kpe16 + 2, qd, (kHalfBoxes * kQChunk) / 16 + kpe16 + 2, idesc_s, 1u);
+        umma_ss(d, ak, 0, qk, 0, idesc_s, 1u);
+        umma_ss(d, ak, 32 >> 4, qk, 32 >> 4, idesc_s, 1u);
         umma_commit(&sm->sfull[t]);
       }
       __syncwarp();
-      return true;
     };
     // rows [nvalid, nend) of the ckv part of a slot: zero them so the PV operand stays finite
     // (the probabilities there are 0, but stale or unwritten rows may hold non-finite values)
@@ -274,29 +276,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             make_uint4(0u, 0u, 0u, 0u);
       }
     };
-    // PV product of tile i: O^T rows [128 blk, 128 blk + 128) of this CTA's columns = boxes 2 blk, 2 blk + 1
-    auto pv = [&](int i) -> bool {
-      const int t = i & 1;
+    // PV product of tile i: O^T rows [128 blk, 128 blk + 128) of this CTA's columns = boxes 2 blk,
+    // 2 blk + 1; P^T is in the kpe part of the tile's slot
+    auto pv = [&](int i) {
+      const int s = i % kSlots, t = i & 1;
       const int nvalid = min(kT, w.sub1 - (w.sub0 + i * kT));
-      if (!wait_lane0(&sm->ppfull[t], (i >> 1) & 1)) return false;
       // K steps of 16 tokens that hold valid tokens; in a partial tile only the rows up to the
       // next multiple of 16 are read, and those past the end are zeroed (the score product of
       // tile i is complete: its softmax ran)
       const int ksteps = (nvalid + 15) >> 4;
       if (nvalid < (ksteps << 4)) {
-        zero_rows(smem + kOffTile + t * kTileSlot, nvalid, ksteps << 4);
+        zero_rows(smem + kOffTile + s * kTileSlot, nvalid, ksteps << 4);
         fence_proxy_async_smem();
         __syncwarp();
       }
       if (lane == 0) {
         tc_fence_after();
-        const Desc2 pb = desc2_add(pd, t * kPBuf);
+        const uint32_t slot = tile_base + s * kTileSlot;
+        const Desc2 pb = desc2(smem_desc_sw128(slot + kCkvBytes, 16, 1024));
         const uint32_t acc0 = (i > 0) ? 1u : 0u;
         // K step ks: tokens [16 ks, 16 ks + 16): two 8-token groups of the slot, and 16 tokens of the
         // P^T atom (ks / 4) at 32-byte step ks % 4
 #pragma unroll
         for (int blk = 0; blk < 2; ++blk) {
-          const Desc2 a0 = desc2(smem_desc_sw128(tile_base + t * kTileSlot + 2 * blk * 1024, 1024, kGroupBytes));
+          const Desc2 a0 = desc2(smem_desc_sw128(slot + 2 * blk * 1024, 1024, kGroupBytes));
           const uint32_t d = tmem + 2 * kNR + blk * kNR;
           if (ksteps == kT / 16) {
 #pragma unroll
@@ -309,18 +312,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                       ks > 0 ? 1u : acc0);
           }
         }
-        umma_commit(&sm->empty[t]);
+        umma_commit(&sm->empty[s]);
         umma_commit(&sm->pvdone[t]);
       }
       __syncwarp();
-      return true;
     };
     named_bar_sync(2, kSoftmaxThreads + 32);  // Q^T staged by the softmax warps
-    bool alive = true;
-    for (int i0 = 0; i0 < ntiles && alive; i0 += 2) {
-      const int i1 = min(i0 + 2, ntiles);
-      for (int i = i0; i < i1 && alive; ++i) alive = score(i);
-      for (int i = i0; i < i1 && alive; ++i) alive = pv(i);
+    // Issue as the inputs get ready, each product in tile order: PV(np) once P^T(np) is written
+    // (first: it releases a slot for the next load), else S(ns) once tile ns has landed and its S
+    // buffer is free. Nothing ready for longer than the wait limit (or an abort elsewhere) ends it.
+    int ns = 0, np = 0;
+    bool idle = false;
+    uint64_t idle_t0 = 0;
+    while (np < ntiles) {
+      int act = 0;
+      if (lane == 0) {
+        if (np < ns && mbar_test(&sm->ppfull[np % kSlots], (np / kSlots) & 1)) {
+          act = 2;
+        } else if (ns < ntiles && (ns < 2 || mbar_test(&sm->sfree[ns & 1], ((ns >> 1) - 1) & 1)) &&
+                   mbar_test(&sm->full[ns % kSlots], (ns / kSlots) & 1)) {
+          act = 1;
+        } else if (*abort_flag) {
+          act = -1;
+        } else {
+          const uint64_t now = globaltimer_ns();
+          if (!idle) {
+            idle = true;
+            idle_t0 = now;
+          } else if (now - idle_t0 > tmo) {
+            act = -1;
+            *abort_flag = 1;
+          }
+        }
+        if (act > 0) idle = false;
+      }
+      act = __shfl_sync(0xffffffffu, act, 0);
+      if (act == 2) {
+        pv(np);
+        ++np;
+      } else if (act == 1) {
+        score(ns);
+        ++ns;
+      } else if (act < 0) {
+        break;
+      }
     }
     if (lane == 0) {  // every MMA issued so far has completed before TMEM is read or freed
       umma_commit(&sm->drain);
@@ -334,16 +369,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     float scale_log2 = p.scale_log2;
     uint64_t tmo = p.timeout_ns;
     asm volatile("" : "+f"(scale_log2), "+l"(tmo));
-    // Q^T: this CTA's 256 latent columns, then the 64 kpe columns; 16 rows, K-major, 5 swizzled chunks
-    for (int idx = tid; idx < kNR * kSlotBoxes * 8; idx += kSoftmaxThreads) {
-      const int r = idx / (kSlotBoxes * 8), k = (idx % (kSlotBoxes * 8)) * 8;
+    // Q^T: this CTA's 256 latent columns (4 chunks, 128-byte swizzle), then its 32 kpe columns
+    // (one chunk, 64-byte swizzle); 16 rows, K-major
+    constexpr int kQPieces = (kHalfCols + kKpeCols) / 8;  // 16-byte pieces per row
+    for (int idx = tid; idx < kNR * kQPieces; idx += kSoftmaxThreads) {
+      const int r = idx / kQPieces, k = (idx % kQPieces) * 8;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (r < w.nrows) {
         const long long row = static_cast<long long>(w.b) * rows_total + w.row0 + r;
-        v = (k < kHalfCols) ? *reinterpret_cast<const uint4*>(p.q_abs + row * kRank + kHalfCols * half + k)
-                            : *reinterpret_cast<const uint4*>(p.q_pe + row * kRope + (k - kHalfCols));
+        v = (k < kHalfCols)
+                ? *reinterpret_cast<const uint4*>(p.q_abs + row * kRank + kHalfCols * half + k)
+                : *reinterpret_cast<const uint4*>(p.q_pe + row * kRope + kKpeCols * half + (k - kHalfCols));
       }
-      *reinterpret_cast<uint4*>(qs + (k / kBoxCols) * kQChunk + sw128_offset(r, k % kBoxCols)) = v;
+      uint8_t* dst = (k < kHalfCols) ? qs + (k / kBoxCols) * kQChunk + sw128_offset(r, k % kBoxCols)
+                                     : qs + kHalfBoxes * kQChunk + sw64_offset(r, k - kHalfCols);
+      *reinterpret_cast<uint4*>(dst) = v;
     }
     fence_proxy_async_smem();
     named_bar_arrive(2, kSoftmaxThreads + 32);
@@ -361,26 +401,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       mr[k] = -INFINITY;
     }
     const int causal_floor = p.causal ? w.L - p.q_len + w.row0 / p.H : 0x7fffffff;
-    // the peer's partial S, [token][16 rows] fp32: row tl's 16 values are 4 float4 chunks, chunk c at
-    // position c ^ ((tl >> 1) & 3) (conflict-free 16-byte accesses); this thread's rows are chunks 2h, 2h+1
+    // the peer's partial S of a tile, in the kpe part of the tile's slot, [token][16 rows] fp32: row
+    // tl's 16 values are 4 float4 chunks, chunk c at position c ^ ((tl >> 1) & 3) (conflict-free
+    // 16-byte accesses); this thread's rows are chunks 2h, 2h+1
     const uint32_t xsw = static_cast<uint32_t>((tl >> 1) & 3);
-    const uint32_t peer_x = dsmem_addr(xs, peer) + tl * 64;
+    const uint32_t peer_x = dsmem_addr(smem + kOffTile + kCkvBytes, peer) + tl * 64;  // + slot * kTileSlot
     bool ok_all = true;
-    // A(i), first part, which never waits on the peer: the signal that this CTA's buffer of tile
-    // i-2 is free for the peer's tile i, then this warp's partial scores of tile i (and its S
-    // buffer freed).
+    // A(i), first part, which never waits on the peer: once the score product of tile i is done
+    // (it has read the kpe part of the slot), the expectation of the peer's partial scores there
+    // and the signal that the peer may send them; then this warp's partial scores of tile i (and
+    // its S buffer freed).
     auto prep = [&](int i, float* x) -> bool {
-      const int b = i & 1;
-      if (i >= 2) {
-        // tile i-2's buffer was read in B(i-2) (its values are consumed and the softmax warps have
-        // passed named barriers since): expect the peer's tile i in it, then free it with a plain signal
-        if (tid == 0) mbar_arrive_expect_tx(&sm->xfull[b], kXBuf);
-        if (lane == 0) mbar_remote_arrive_relaxed(dsmem_addr(&sm->xempty[b], peer));
-      }
+      const int b = i & 1, s = i % kSlots;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&sm->sfull[b], (i >> 1) & 1, tmo);
       if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
       tc_fence_after();
+      if (warp == 0 && lane == 0) {
+        mbar_arrive_expect_tx(&sm->xfull[s], kXBuf);
+        mbar_remote_arrive(dsmem_addr(&sm->xready[s], peer));
+      }
       tmem_ld8(tmem + lane_base + b * kNR + kRH * h, x);
       tmem_wait_ld();
       tc_fence_before();
@@ -388,22 +428,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&sm->sfree[b]);
       return true;
     };
-    // the peer has read its buffer of tile i-2, so tile i's scores may go there (non-blocking test)
+    // the peer's score product of tile i is done, so tile i's scores may go to its slot
+    // (non-blocking test)
     auto peer_free = [&](int i) -> bool {
-      if (i < 2) return true;
       int ready = 0;
-      if (lane == 0) ready = mbar_test(&sm->xempty[i & 1], ((i >> 1) - 1) & 1) ? 1 : 0;
+      if (lane == 0) ready = mbar_test(&sm->xready[i % kSlots], (i / kSlots) & 1) ? 1 : 0;
       return __shfl_sync(0xffffffffu, ready, 0) != 0;
     };
-    // A(i), second part: once the peer has read its buffer of tile i-2, this warp's partial scores
-    // of tile i go there
+    // A(i), second part: once the peer's score product of tile i is done, this warp's partial scores
+    // of tile i go to the kpe part of the peer's slot
     auto push = [&](int i, const float* x) -> bool {
-      const int b = i & 1;
-      int ok = 1;
-      if (i >= 2) ok = mbar_wait_cluster(&sm->xempty[b], ((i >> 1) - 1) & 1, tmo);
+      const int s = i % kSlots;
+      const int ok = mbar_wait_cluster(&sm->xready[s], (i / kSlots) & 1, tmo);
       if (!__all_sync(0xffffffffu, ok)) return false;
-      const uint32_t dst = peer_x + b * kXBuf;
-      const uint32_t rbar = dsmem_addr(&sm->xfull[b], peer);
+      const uint32_t dst = peer_x + s * kTileSlot;
+      const uint32_t rbar = dsmem_addr(&sm->xfull[s], peer);
 #pragma unroll
       for (int c = 0; c < 2; ++c)
         dsmem_st_async_f32x4(dst + (((2 * h + c) ^ xsw) << 4),
@@ -414,15 +453,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warp calls it for every tile it reaches, also after a failed send (sent = false), so all of
     // them pass the same named barriers; a failure anywhere ends the loop in all of them.
     auto finish = [&](int i, float* x, bool sent) -> bool {
-      const int b = i & 1;
+      const int s = i % kSlots;
+      uint8_t* region = smem + kOffTile + s * kTileSlot + kCkvBytes;  // the peer's partial S, then P^T
       const int tok0 = w.sub0 + i * kT;
       const int nvalid = min(kT, w.sub1 - tok0);
       const bool masked_tile = (nvalid < kT) || (tok0 + kT - 1 > causal_floor) || (w.nrows < kNR);
-      int ok = sent ? mbar_wait_cluster(&sm->xfull[b], (i >> 1) & 1, tmo) : 0;
+      int ok = sent ? mbar_wait_cluster(&sm->xfull[s], (i / kSlots) & 1, tmo) : 0;
       ok = __all_sync(0xffffffffu, ok);
       bool need_local = false;
       if (ok) {
-        const float4* xb = reinterpret_cast<const float4*>(xs + b * (kXBuf / 4) + tl * 16);
+        const float4* xb = reinterpret_cast<const float4*>(region) + tl * 4;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const float4 y = xb[(2 * h + c) ^ xsw];
@@ -499,13 +539,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < kRH; ++k) lsum[k] *= sm->alpha[kRH * h + k];
       }
-      if (i >= 2) {  // P^T buffer b was last read by PV(i-2)
-        int ok3 = 1;
-        if (lane == 0) ok3 = mbar_wait(&sm->pvdone[b], ((i >> 1) - 1) & 1, tmo);
-        if (!__shfl_sync(0xffffffffu, ok3, 0) && lane == 0) *abort_flag = 1;
-      }
-      {  // probabilities -> P^T (fp16, K-major, two swizzled 64-token atoms) and row sums
-        uint8_t* pb = ps + b * kPBuf + (tl >> 6) * (kNR * 128);
+      {  // probabilities -> P^T (fp16, K-major, two swizzled 64-token atoms) and row sums, over the
+         // peer's partial S (every softmax warp has read its part: the barrier above)
+        uint8_t* pb = region + (tl >> 6) * (kNR * 128);
 #pragma unroll
         for (int k = 0; k < kRH; ++k) {
           // masked scores (-inf) give 0; a row with no visible token yet subtracts a finite stand-in
@@ -518,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm->ppfull[b]);
+      if (lane == 0) mbar_arrive(&sm->ppfull[s]);
       return true;
     };
     // Tiles in pairs, as the MMA warp issues them (S(i) S(i+1) PV(i) PV(i+1)): when tile i+1's scores
@@ -693,7 +729,7 @@ bool tc128_supports(int total_rows, bool bf16, int cluster) {
   return total_rows <= kNR && !bf16 && cluster >= 2 && cluster <= 16 && (cluster & (cluster - 1)) == 0;
 }
 
-cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe, const PartialParams& p,
+cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe_half, const PartialParams& p,
                                  int num_chunks, int cluster, cudaStream_t stream) {
   cudaError_t e = prepare(cluster);
   if (e != cudaSuccess) return e;
@@ -711,7 +747,7 @@ cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap&
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, mla_partial_tc128_kernel, tm_pages, tm_kpe, p);
+  return cudaLaunchKernelEx(&cfg, mla_partial_tc128_kernel, tm_pages, tm_kpe_half, p);
 }
 
 int tc128_max_active_clusters(int cluster) {
