@@ -93,8 +93,8 @@ static_assert(kNR * kHalfCols * 4 + 2 * kNR * 4 <= kSlots * kTileSlot, "epilogue
 
 struct Small {
   // slot ring: full / empty; TMEM S buffers (tile parity): sfull / sfree; per slot: ppfull (P^T
-  // written), xfull (the peer's partial S landed), xready (the peer's kpe part of the slot is free
-  // for this CTA's partial S); pvdone per tile parity
+  // written), xfull (the peer's partial S landed), xready (the peer's score product of the slot's
+  // tile is done: its kpe part is free for this CTA's partial S); pvdone per tile parity
   uint64_t full[kSlots], empty[kSlots], sfull[2], sfree[2], ppfull[kSlots], pvdone[2], xfull[kSlots],
       xready[kSlots], drain;
   uint32_t tmem_base;
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm->empty[s], 1);
       mbar_init(&sm->ppfull[s], kSoftmaxWarps);
       mbar_init(&sm->xfull[s], 1);   // local expect_tx arrival + the peer's st.async bytes
-      mbar_init(&sm->xready[s], 1);  // one remote arrival from the peer
+      mbar_init(&sm->xready[s], 1);  // the peer's MMA commit
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm->sfull[t], 1);
@@ -264,6 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_ss(d, ak, 0, qk, 0, idesc_s, 1u);
         umma_ss(d, ak, 32 >> 4, qk, 32 >> 4, idesc_s, 1u);
         umma_commit(&sm->sfull[t]);
+        // once these MMAs have read the kpe part of the slot, the peer may send its partial scores there
+        umma_commit_multicast(&sm->xready[i % kSlots], static_cast<uint16_t>(1u << peer));
       }
       __syncwarp();
     };
@@ -318,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     };
     named_bar_sync(2, kSoftmaxThreads + 32);  // Q^T staged by the softmax warps
+    cluster_wait_acquire();                   // the peer's barriers are initialised (commits reach them)
     // Issue as the inputs get ready, each product in tile order: PV(np) once P^T(np) is written
     // (first: it releases a slot for the next load), else S(ns) once tile ns has landed and its S
     // buffer is free. Nothing ready for longer than the wait limit (or an abort elsewhere) ends it.
@@ -362,7 +365,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&sm->drain, 0, kDrainTimeoutNs);
     }
     __syncwarp();
-    cluster_wait_acquire();
   } else {
     // ------------------------------------------------------------------ softmax (warps 0-7)
     // kernel parameters used every tile, held in registers (not re-read from the parameter bank)
@@ -407,20 +409,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t xsw = static_cast<uint32_t>((tl >> 1) & 3);
     const uint32_t peer_x = dsmem_addr(smem + kOffTile + kCkvBytes, peer) + tl * 64;  // + slot * kTileSlot
     bool ok_all = true;
-    // A(i), first part, which never waits on the peer: once the score product of tile i is done
-    // (it has read the kpe part of the slot), the expectation of the peer's partial scores there
-    // and the signal that the peer may send them; then this warp's partial scores of tile i (and
-    // its S buffer freed).
+    // A(i), first part, which never waits on the peer: the expectation of the peer's partial scores
+    // of tile i in the kpe part of the slot (the completion of this CTA's score product tells the
+    // peer that it may send them; the bytes may land before this), then this warp's partial scores
+    // of tile i (and its S buffer freed).
     auto prep = [&](int i, float* x) -> bool {
       const int b = i & 1, s = i % kSlots;
+      if (warp == 0 && lane == 0) mbar_arrive_expect_tx(&sm->xfull[s], kXBuf);
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&sm->sfull[b], (i >> 1) & 1, tmo);
       if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
       tc_fence_after();
-      if (warp == 0 && lane == 0) {
-        mbar_arrive_expect_tx(&sm->xfull[s], kXBuf);
-        mbar_remote_arrive(dsmem_addr(&sm->xready[s], peer));
-      }
       tmem_ld8(tmem + lane_base + b * kNR + kRH * h, x);
       tmem_wait_ld();
       tc_fence_before();
