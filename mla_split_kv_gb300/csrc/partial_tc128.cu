@@ -47,8 +47,10 @@
 // rescale / epilogue (thread = token of the M=128 layout; the two warps of a
 // TMEM lane quadrant take rows 0-7 and 8-15), warp 8 TMEM owner + MMA issuer,
 // warps 9-11 producers (warp 9+k loads pages k, k+3, ... of each tile, both
-// caches, one page per lane, and prefetches the same pages of tile i+1 into
-// L2; the kpe box is this CTA's 32 columns, with the 64-byte swizzle). The kernel is a programmatic dependent launch: its set-up overlaps the
+// caches, one page per lane; the kpe box is this CTA's 32 columns, with the
+// 64-byte swizzle). With three slots in flight an L2 prefetch of the next
+// tile's pages measured slower over a sweep of caches larger than L2, so
+// there is none. The kernel is a programmatic dependent launch: its set-up overlaps the
 // end of the previous kernel in the stream.
 #include "device_common.cuh"
 
@@ -217,20 +219,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       issued = i;
-      if (i + 1 < ntiles) {  // the same pages of tile i+1 into L2: ckv by the even CTA, kpe by the odd one
-        int qg0, qn;
-        tile_pages(i + 1, &qg0, &qn);
-        for (int j = k0; j < qn; j += kPageWarps) {
-          const int pid = page_of(qg0 + j);
-          if (lane == 0 && pid >= 0) {
-            const long long row = static_cast<long long>(pid) * p.bs;
-            if (half == 0)
-              bulk_prefetch_l2(p.ckv + row * (kRank * 2), static_cast<uint32_t>(p.bs * kRank * 2));
-            else
-              bulk_prefetch_l2(p.kpe + row * (kRope * 2), static_cast<uint32_t>(p.bs * kRope * 2));
-          }
-        }
-      }
     }
     // after an abort, let this warp's last loads land before shared memory is released
     if (lane == 0 && *abort_flag && issued >= 0)

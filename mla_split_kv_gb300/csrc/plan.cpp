@@ -46,10 +46,10 @@ struct Candidate {
 constexpr int64_t kMaxSubs = 16;       // clusters per partition (the kernel's final merge reads at most 16)
 constexpr int64_t kPairTileTokens = 128;
 // Time model of the paired kernel for one request, fitted to layer-call times measured on GB300 over
-// partition counts, cluster sizes and spreads at 32K-128K tokens: a CTA pair takes ~2.33 us per
+// partition counts, cluster sizes and spreads at 32K-128K tokens: a CTA pair takes ~1.75 us per
 // 128-token tile; spreading a partition over k > 1 clusters adds a ticket + final-merge tail of
-// ~4.2 us plus ~0.3 us per sub-partial for a 2-CTA cluster (the merge work per CTA scales with k / C).
-constexpr double kTileUs = 2.33, kSpreadTailUs = 4.2, kMergeUsPerSub = 0.3;
+// ~6 us plus ~0.3 us per sub-partial for a 2-CTA cluster (the merge work per CTA scales with k / C).
+constexpr double kTileUs = 1.75, kSpreadTailUs = 6.0, kMergeUsPerSub = 0.3;
 
 double paired_cost_us(int64_t L, int64_t P, int64_t k, int C) {
   const int64_t pairs = P * k * (C / 2);

@@ -78,8 +78,10 @@ def test_plan_long_context_single_request(lib, L):
     assert 2 <= plan.num_chunks <= 8
     busy = plan.num_chunks * plan.cluster_ctas * plan.clusters_per_chunk
     assert 100 <= busy <= 152  # most of the 152 SMs busy, with at most 8 partitions
-    if L >= 81920:  # long enough that spreading partitions over clusters pays for its merge tail
+    if L >= 131072:  # long enough that spreading partitions over clusters pays for its merge tail
         assert plan.clusters_per_chunk > 1 and busy >= 140
+    if L <= 65536:  # too short for that: one cluster of 16 per partition
+        assert plan.clusters_per_chunk == 1 and plan.cluster_ctas == 16
     check_plan_tiles(plan, [L], 32)
     # every CTA pair of every cluster keeps at least one 128-token tile of its partition
     k, C = plan.clusters_per_chunk, plan.cluster_ctas

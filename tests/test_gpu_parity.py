@@ -269,10 +269,10 @@ def test_quad_kernel_spread_partitions(L, P, C, k):
 def test_spread_partitions_bitwise_reproducible_and_workspace_reused():
     """Same plan, same workspace, several calls: identical bits (the merge order does not depend on which
     cluster finishes last, and every call leaves its tickets at zero)."""
-    case = gen.make_decode_case(6, [98304], num_heads=16, block_size=32, dtype="f16")
+    case = gen.make_decode_case(6, [131072], num_heads=16, block_size=32, dtype="f16")
     dc = rt.upload(case)
     dev = nb.mla_device_query()
-    plan = nb.mla_plan([98304], 16, 1, 32, dev)
+    plan = nb.mla_plan([131072], 16, 1, 32, dev)
     assert plan.clusters_per_chunk > 1
     ws = rt.alloc_workspace(plan.num_chunks, plan.clusters_per_chunk, 1, 16)
     outs = []
