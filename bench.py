@@ -416,7 +416,8 @@ def run_ours(args, rank, world):
             out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
             k = plan.clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
             ws = rt.alloc_workspace(plan.num_chunks, k, 1, H)
-            desc = rt.make_desc(dc, chunks_dev, kernel, plan.cluster_ctas, stream, k, ws)
+            # the tables are uploaded before the step and no kernel of the step writes them
+            desc = rt.make_desc(dc, chunks_dev, kernel, plan.cluster_ctas, stream, k, ws, tables_ready=True)
             calls.append(dict(L=L, plan=plan, dc=dc, chunks=chunks_dev, part=part, lse=lse, ind=ind, out=out,
                               desc=desc, ws=ws))
     torch.cuda.synchronize()

@@ -81,6 +81,7 @@ class mla_decode_desc_t(ctypes.Structure):
         ("clusters_per_chunk", ctypes.c_int32),
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_uint64),
+        ("tables_ready", ctypes.c_int32),
     ]
 
 

@@ -201,6 +201,7 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64) return reject(MLA_ERR_UNSUPPORTED);
   if (d->dtype != MLA_F16 && d->dtype != MLA_BF16) return reject(MLA_ERR_UNSUPPORTED);
   if (d->causal != 0 && d->causal != 1) return reject(MLA_ERR_INVALID_ARG);
+  if (d->tables_ready != 0 && d->tables_ready != 1) return reject(MLA_ERR_INVALID_ARG);
   if (d->kernel < MLA_KERNEL_AUTO || d->kernel > MLA_KERNEL_TC_QUAD) return reject(MLA_ERR_INVALID_ARG);
   const int32_t C0 = d->cluster_ctas;
   if (C0 != 0 && C0 != 1 && C0 != 2 && C0 != 4 && C0 != 8 && C0 != 16) return reject(MLA_ERR_INVALID_ARG);
@@ -272,6 +273,7 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   p.num_blocks = d->num_blocks;
   p.num_parts = (d->chunks == nullptr) ? num_partitions : 1;
   p.causal = d->causal;
+  p.tables_ready = d->tables_ready;
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
 
   p.subs = subs;

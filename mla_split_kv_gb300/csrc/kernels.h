@@ -34,6 +34,7 @@ struct PartialParams {
   int32_t B, H, q_len, bs, max_blocks, num_blocks;
   int32_t num_parts;           // uniform split when chunks == null
   int32_t causal;
+  int32_t tables_ready;        // chunks / context_lens / block_table may be read before the dependency wait
   uint64_t timeout_ns;
   // a chunk spread over `subs` clusters (paired 16-row kernel only): grid.y =
   // chunks * subs; the sub-partials and their LSEs go to ws_partials / ws_lse

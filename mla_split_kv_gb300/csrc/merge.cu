@@ -25,9 +25,10 @@ constexpr int kWarps = 8;
 __global__ void __launch_bounds__(kWarps * 32) mla_merge_kernel(const MergeParams p) {
   // Launched as a programmatic dependent of the partial kernel: everything this
   // kernel reads may still be in flight until the wait returns. The next kernel
-  // (the next layer's partial kernel) may start its set-up meanwhile.
-  pdl_launch_dependents();
+  // (the next layer's partial kernel) is released after the wait and may start
+  // its set-up while this one works.
   pdl_wait();
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long gw = static_cast<long long>(blockIdx.x) * kWarps + warp;
   const long long total = static_cast<long long>(p.B) * p.rows * 4;

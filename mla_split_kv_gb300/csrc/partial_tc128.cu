@@ -114,7 +114,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mla_partial_tc128_kernel(const __grid_constant__ CUtensorMap tm_pages, const __grid_constant__ CUtensorMap tm_kpe_half,
                              const PartialParams p) {
   extern __shared__ uint8_t smem_raw[];
-  pdl_launch_dependents();  // the merge of these partials may be scheduled now; it waits for this grid
   uint8_t* smem = align1024(smem_raw);
   uint8_t* qs = smem + kOffQ;
   Small* sm = reinterpret_cast<Small*>(smem + kOffSmall);
@@ -158,26 +157,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_arrive_release();  // the peer touches this CTA's barriers only after this cluster phase
   const uint32_t tmem = sm->tmem_base;
   // Launched as a programmatic dependent of the previous kernel in the stream: the set-up above
-  // overlaps its end; every input this kernel reads (chunk table, lengths, block table, queries,
-  // caches) is read after this wait.
+  // overlaps its end. The queries and the caches are read after the wait below; so are the chunk
+  // table, the lengths and the block table, unless the caller declared them complete before that
+  // kernel started (tables_ready): then they are read while it finishes (producers: the first
+  // block-table window too). The next kernel (the merge) is released only after the wait, so a
+  // kernel launched after this one starts once everything before this one has finished.
+  CtaWork w{};
+  const int pair_index = sub * cluster_pairs + static_cast<int>(rank >> 1);
+  int win_base = -1, win_pid = -1;  // producers: a window of 32 block-table entries (page ids)
+  auto load_window = [&](int pg) {   // warp-uniform page index
+    win_base = pg & ~31;
+    const int q = win_base + lane;
+    const int npages_req = (w.L + p.bs - 1) / p.bs;
+    win_pid = (q < npages_req && q < p.max_blocks) ? checked_page(p, w.b, q) : -1;
+  };
+  if (p.tables_ready) {
+    w = cta_work(p, kNR, kT, pair_index, subs * cluster_pairs, chunk);
+    if (warp > kMmaWarp && w.sub1 > w.sub0) load_window(w.sub0 / p.bs);
+  }
   pdl_wait();
-  const CtaWork w =
-      cta_work(p, kNR, kT, sub * cluster_pairs + static_cast<int>(rank >> 1), subs * cluster_pairs, chunk);
+  pdl_launch_dependents();  // the merge of these partials may be scheduled now; it waits for this grid
+  if (!p.tables_ready) w = cta_work(p, kNR, kT, pair_index, subs * cluster_pairs, chunk);
   const int ntiles = (w.sub1 - w.sub0 + kT - 1) / kT;
 
   if (warp > kMmaWarp) {
     // ------------------------------------------------------------------ producers
     const int k0 = warp - kMmaWarp - 1;  // this warp loads pages k0, k0 + kPageWarps, ... of each tile
     const uint64_t pol = l2_policy_evict_first();
-    const int npages_req = (w.L + p.bs - 1) / p.bs;
-    int win_base = -1, win_pid = -1;
     auto page_of = [&](int pg) -> int {  // warp-uniform pg
-      const int base = pg & ~31;
-      if (base != win_base) {
-        win_base = base;
-        const int q = base + lane;
-        win_pid = (q < npages_req && q < p.max_blocks) ? checked_page(p, w.b, q) : -1;
-      }
+      if ((pg & ~31) != win_base) load_window(pg);
       return __shfl_sync(0xffffffffu, win_pid, pg & 31);
     };
     auto tile_pages = [&](int i, int* pg0, int* npg) {

@@ -54,7 +54,7 @@ def chunks_to_device(chunks: Sequence[Sequence[int]], device="cuda") -> torch.Te
 
 def make_desc(dc: DeviceCase, chunks_dev: Optional[torch.Tensor], kernel: int, cluster: int,
               stream: Optional[torch.cuda.Stream] = None, subs: int = 1,
-              workspace: Optional[torch.Tensor] = None) -> nb.mla_decode_desc_t:
+              workspace: Optional[torch.Tensor] = None, tables_ready: bool = False) -> nb.mla_decode_desc_t:
     c = dc.case
     d = nb.mla_decode_desc_t()
     d.num_requests = c.num_requests
@@ -74,6 +74,7 @@ def make_desc(dc: DeviceCase, chunks_dev: Optional[torch.Tensor], kernel: int, c
     d.clusters_per_chunk = subs
     d.workspace = workspace.data_ptr() if workspace is not None else None
     d.workspace_bytes = workspace.numel() if workspace is not None else 0
+    d.tables_ready = 1 if tables_ready else 0
     # the descriptor holds raw device pointers: keep their tensors alive as long as it lives
     d._keep = (chunks_dev, workspace)
     return d
@@ -94,8 +95,9 @@ def alloc_partials(num_slots: int, q_len: int, H: int, device="cuda"):
 def decode_partial(dc: DeviceCase, part: torch.Tensor, lse: torch.Tensor, num_partitions: int = 1,
                    chunks_dev: Optional[torch.Tensor] = None, kernel: int = nb.MLA_KERNEL_AUTO,
                    cluster: int = 0, stream=None, desc: Optional[nb.mla_decode_desc_t] = None, subs: int = 1,
-                   workspace: Optional[torch.Tensor] = None) -> None:
-    d = desc if desc is not None else make_desc(dc, chunks_dev, kernel, cluster, stream, subs, workspace)
+                   workspace: Optional[torch.Tensor] = None, tables_ready: bool = False) -> None:
+    d = desc if desc is not None else make_desc(dc, chunks_dev, kernel, cluster, stream, subs, workspace,
+                                                tables_ready)
     nb.mla_decode_partial(dc.q_abs.data_ptr(), dc.q_pe.data_ptr(), dc.ckv.data_ptr(), dc.kpe.data_ptr(),
                           dc.block_table.data_ptr(), dc.context_lens.data_ptr(), float(dc.case.scale),
                           num_partitions, part.data_ptr(), lse.data_ptr(), d)

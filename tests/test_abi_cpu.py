@@ -200,6 +200,7 @@ def call_partial(lib, d, P=2, ptrs=None):
     (dict(cluster_ctas=3), 2, nb.MLA_ERR_INVALID_ARG),
     (dict(kernel=7), 2, nb.MLA_ERR_INVALID_ARG),
     (dict(causal=2), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(tables_ready=2), 2, nb.MLA_ERR_INVALID_ARG),
     (dict(), 0, nb.MLA_ERR_INVALID_ARG),
     (dict(num_requests=40000), 2, nb.MLA_ERR_UNSUPPORTED),
 ])

@@ -205,7 +205,7 @@ def test_quad_kernel_paging_invariance_and_reproducibility():
     assert torch.equal(a, a2) and torch.equal(a, b)
 
 
-def plan_and_run(case, max_partitions=0, kernel=nb.MLA_KERNEL_TC, dc=None, ws=None):
+def plan_and_run(case, max_partitions=0, kernel=nb.MLA_KERNEL_TC, dc=None, ws=None, tables_ready=False):
     """The planner's plan as the bench runs it: its cluster size and clusters per partition."""
     dev = nb.mla_device_query()
     plan = nb.mla_plan(case.context_lens.tolist(), case.num_heads, case.q_len, case.block_size, dev,
@@ -217,7 +217,7 @@ def plan_and_run(case, max_partitions=0, kernel=nb.MLA_KERNEL_TC, dc=None, ws=No
     if k > 1 and ws is None:
         ws = rt.alloc_workspace(plan.num_chunks, k, case.q_len, case.num_heads)
     rt.decode_partial(dc, part, lse, chunks_dev=chunks_dev, kernel=kernel, cluster=plan.cluster_ctas, subs=k,
-                      workspace=ws)
+                      workspace=ws, tables_ready=tables_ready)
     ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
     out = rt.merge_states(part, lse, ind, case.num_requests, case.q_len, case.num_heads, "f32")
     return plan, part, lse, out
@@ -264,6 +264,22 @@ def test_quad_kernel_spread_partitions(L, P, C, k):
     ref_part, ref_lse = orc.partials(case, chunks)
     assert_close(part.cpu().numpy(), ref_part, f"quad partials L={L} P={P} C={C} k={k}")
     assert_lse_close(lse.cpu().numpy(), ref_lse, f"quad lse L={L} P={P} C={C} k={k}")
+
+
+@pytest.mark.parametrize("L", [32768, 131072])
+def test_tables_read_before_the_dependency_wait_give_the_same_bits(L):
+    """tables_ready only moves the reads of the chunk table, the lengths and the block table before the
+    wait for the preceding kernel: the same plan gives the same bits either way, also right behind
+    another decode call (a merge, then this call's kernel as its programmatic dependent)."""
+    case = gen.make_decode_case(7, [L], num_heads=16, block_size=32, dtype="f16")
+    dc = rt.upload(case)
+    ref = plan_and_run(case, dc=dc)[1:]
+    for _ in range(2):  # the second time behind the first call's merge in the stream
+        got = plan_and_run(case, dc=dc, tables_ready=True)[1:]
+        for a, b in zip(ref, got):
+            assert torch.equal(a, b)
+    st, code = nb.mla_check_device_errors(None)
+    assert st == nb.MLA_OK, code
 
 
 def test_spread_partitions_bitwise_reproducible_and_workspace_reused():
