@@ -10,7 +10,8 @@ its latent from HBM.
 Printed: one JSON line. `value` = mean microseconds per layer call over the
 sweep (device time, inputs resident, each step replayed from one CUDA graph);
 `e2e` = the same through the C-ABI calls with host buffers (queries, block
-tables and plan copied in, output copied out, every step); `roofline` = the
+tables and plan of the six calls copied in with one copy from one pinned
+buffer, the six outputs copied out with one copy, every step); `roofline` = the
 partial kernel's algorithmic HBM bytes / its CUDA-event time against the
 measured copy bandwidth; `cpu_baseline` = the f64 oracle on the host cores.
 `--impl reference` times the oracle itself on the same workload.
@@ -525,36 +526,62 @@ def run_ours(args, rank, world):
                         "partial_gbs": round(pb / (pus * 1e-6) / 1e9, 1),
                         "note": "repeats of one cache; caches <= 113 MB may be partly L2-resident"})
 
-    # end to end through the C ABI with host buffers (pinned), every step
+    # end to end through the C ABI with host buffers (pinned), every step: the inputs of the six calls
+    # (queries, block tables, lengths, partition tables, merge offsets) sit in one pinned host buffer
+    # that mirrors one device buffer, so a step uploads them with one copy; the six outputs come back
+    # with one copy as well
     e2e_steps = max(1, args.e2e_steps)
-    host = []
+    segs, off = [], 0
+
+    def seg(arr):
+        nonlocal off
+        a = np.ascontiguousarray(arr)
+        segs.append((off, a))
+        off += (a.nbytes + 15) // 16 * 16  # every device input 16-byte aligned
+        return len(segs) - 1
+
+    layout = []
     for c in calls:
         cs = c["dc"].case
-        host.append(dict(q_abs=torch.from_numpy(cs.q_abs.view(np.int16)).pin_memory(),
-                         q_pe=torch.from_numpy(cs.q_pe.view(np.int16)).pin_memory(),
-                         bt=torch.from_numpy(cs.block_table).pin_memory(),
-                         lens=torch.from_numpy(cs.context_lens).pin_memory(),
-                         chunks=torch.from_numpy(c["plan"].chunk_array()).pin_memory(),
-                         ind=torch.tensor(c["plan"].o_indptr, dtype=torch.int32).pin_memory(),
-                         out=torch.empty((1, 1, H, 512), dtype=torch.float16).pin_memory()))
-    h2d = sum(h["q_abs"].numel() * 2 + h["q_pe"].numel() * 2 + h["bt"].numel() * 4 + h["lens"].numel() * 4
-              + h["chunks"].numel() * 4 + h["ind"].numel() * 4 for h in host)
-    d2h = sum(h["out"].numel() * 2 for h in host)
+        layout.append(dict(q_abs=seg(cs.q_abs.view(np.int16)), q_pe=seg(cs.q_pe.view(np.int16)),
+                           bt=seg(cs.block_table), lens=seg(cs.context_lens),
+                           chunks=seg(c["plan"].chunk_array()),
+                           ind=seg(np.asarray(c["plan"].o_indptr, dtype=np.int32))))
+    hbuf = torch.empty(off, dtype=torch.uint8).pin_memory()
+    hview = hbuf.numpy()
+    for o, a in segs:
+        hview[o:o + a.nbytes] = a.view(np.uint8).reshape(-1)
+    dbuf = torch.empty(off, dtype=torch.uint8, device="cuda")
+
+    def dview(i, dtype):
+        o, a = segs[i]
+        return dbuf[o:o + a.nbytes].view(dtype).view(a.shape)
+
+    dout = torch.empty((len(calls), 1, 1, H, 512), dtype=torch.float16, device="cuda")
+    hout = torch.empty(dout.shape, dtype=torch.float16).pin_memory()
+    e2e_calls = []
+    for j, (c, lay) in enumerate(zip(calls, layout)):
+        dc = c["dc"]
+        edc = rt.DeviceCase(q_abs=dview(lay["q_abs"], torch.int16).view(torch.float16),
+                            q_pe=dview(lay["q_pe"], torch.int16).view(torch.float16),
+                            ckv=dc.ckv, kpe=dc.kpe, block_table=dview(lay["bt"], torch.int32),
+                            context_lens=dview(lay["lens"], torch.int32), case=dc.case)
+        chunks = dview(lay["chunks"], torch.int32)
+        desc = rt.make_desc(edc, chunks, kernel, c["plan"].cluster_ctas, stream, c["desc"].clusters_per_chunk, c["ws"],
+                            tables_ready=True)
+        e2e_calls.append(dict(dc=edc, desc=desc, ind=dview(lay["ind"], torch.int32), out=dout[j],
+                              part=c["part"], lse=c["lse"]))
+    h2d = off
+    d2h = dout.numel() * 2
     nb.mla_reset_counters()
 
     def e2e_step():
         with torch.cuda.stream(stream):
-            for c, h in zip(calls, host):
-                dc = c["dc"]
-                dc.q_abs.view(torch.int16).copy_(h["q_abs"], non_blocking=True)
-                dc.q_pe.view(torch.int16).copy_(h["q_pe"], non_blocking=True)
-                dc.block_table.copy_(h["bt"], non_blocking=True)
-                dc.context_lens.copy_(h["lens"], non_blocking=True)
-                c["chunks"].copy_(h["chunks"], non_blocking=True)
-                c["ind"].copy_(h["ind"], non_blocking=True)
-                partial(c)
-                merge(c)
-                h["out"].copy_(c["out"], non_blocking=True)
+            dbuf.copy_(hbuf, non_blocking=True)
+            for e in e2e_calls:
+                rt.decode_partial(e["dc"], e["part"], e["lse"], desc=e["desc"])
+                rt.merge_states(e["part"], e["lse"], e["ind"], 1, 1, H, "f16", out=e["out"], stream=stream)
+            hout.copy_(dout, non_blocking=True)
         stream.synchronize()
 
     for _ in range(3):
@@ -563,6 +590,10 @@ def run_ours(args, rank, world):
     for _ in range(e2e_steps):
         e2e_step()
     e2e_s = time.perf_counter() - t0
+    # the results of the last step are the graph's results (same inputs)
+    for j, c in enumerate(calls):
+        if not torch.equal(hout[j], c["out"].cpu()):
+            raise RuntimeError(f"end-to-end output of call {j} differs from the timed graph's")
     ctr = nb.mla_get_counters()
     expect = (3 + e2e_steps) * len(calls)
     ctr_key = nb.CTR_PARTIAL_SIMT if kernel == nb.MLA_KERNEL_SIMT else nb.CTR_PARTIAL_TC
