@@ -20,7 +20,7 @@ namespace mla {
 
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 2;
 
 __global__ void __launch_bounds__(kWarps * 32) mla_merge_kernel(const MergeParams p) {
   // Launched as a programmatic dependent of the partial kernel: everything this
