@@ -662,48 +662,72 @@ __device__ __forceinline__ void merge_sub_partials(const PartialParams& p, const
   __threadfence();
   const int dcols = kRank / static_cast<int>(nranks);
   const int dbeg = static_cast<int>(rank) * dcols;
-  const int n4 = dcols / 4;
-  const int items = w.nrows * n4 + ((rank == 0) ? w.nrows : 0);
+  const int n8 = dcols / 8;
+  const int items = w.nrows * n8 + ((rank == 0) ? w.nrows : 0);
   const long long sub0 = static_cast<long long>(chunk) * subs;
+  // item = 8 columns of a row (or a row's LSE): one round of loads for up to 8 sub-partials (every
+  // CTA of the cluster has about one item per thread), then the fixed-order reduction
   for (int idx = tid; idx < items; idx += nthreads) {
-    const bool is_lse = idx >= w.nrows * n4;
-    const int r = is_lse ? idx - w.nrows * n4 : idx / n4;
-    const int d = is_lse ? 0 : dbeg + (idx % n4) * 4;
+    const bool is_lse = idx >= w.nrows * n8;
+    const int r = is_lse ? idx - w.nrows * n8 : idx / n8;
+    const int d = is_lse ? 0 : dbeg + (idx % n8) * 8;
     float lj[16];
-    float4 vj[16];
+    float4 va[8], vb[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      lj[j] = -INFINITY;
-      vj[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (j < subs) {
-        const long long row = (sub0 + j) * rows_total + w.row0 + r;
-        lj[j] = __ldcg(p.ws_lse + row);
-        if (!is_lse) vj[j] = __ldcg(reinterpret_cast<const float4*>(p.ws_partials + row * kRank + d));
+    for (int j = 0; j < 16; ++j)
+      lj[j] = (j < subs) ? __ldcg(p.ws_lse + (sub0 + j) * rows_total + w.row0 + r) : -INFINITY;
+    auto load8 = [&](int j0) {
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        va[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+        vb[jj] = va[jj];
+        if (j0 + jj < subs && !is_lse) {
+          const float* src = p.ws_partials + ((sub0 + j0 + jj) * rows_total + w.row0 + r) * kRank + d;
+          va[jj] = __ldcg(reinterpret_cast<const float4*>(src));
+          vb[jj] = __ldcg(reinterpret_cast<const float4*>(src + 4));
+        }
       }
-    }
+    };
+    load8(0);
     float M = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 16; ++j) M = fmaxf(M, lj[j]);
     float den = 0.f;
-    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 num0 = make_float4(0.f, 0.f, 0.f, 0.f), num1 = num0;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float wj = (lj[j] == -INFINITY) ? 0.f : exp2f(lj[j] - M);
-        den += wj;
-        num.x = fmaf(wj, vj[j].x, num.x);
-        num.y = fmaf(wj, vj[j].y, num.y);
-        num.z = fmaf(wj, vj[j].z, num.z);
-        num.w = fmaf(wj, vj[j].w, num.w);
+      for (int j0 = 0; j0 < 16; j0 += 8) {
+        if (j0 >= subs) break;
+        if (j0 > 0) load8(j0);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj;
+          if (j < subs) {
+            const float wj = (lj[j] == -INFINITY) ? 0.f : exp2f(lj[j] - M);
+            den += wj;
+            num0.x = fmaf(wj, va[jj].x, num0.x);
+            num0.y = fmaf(wj, va[jj].y, num0.y);
+            num0.z = fmaf(wj, va[jj].z, num0.z);
+            num0.w = fmaf(wj, va[jj].w, num0.w);
+            num1.x = fmaf(wj, vb[jj].x, num1.x);
+            num1.y = fmaf(wj, vb[jj].y, num1.y);
+            num1.z = fmaf(wj, vb[jj].z, num1.z);
+            num1.w = fmaf(wj, vb[jj].w, num1.w);
+          }
+        }
       }
     }
     if (is_lse) {
       p.lse[static_cast<long long>(w.slot) * rows_total + w.row0 + r] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
     } else {
-      float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (M != -INFINITY) out = make_float4(num.x / den, num.y / den, num.z / den, num.w / den);
-      *reinterpret_cast<float4*>(p.partials + (static_cast<long long>(w.slot) * rows_total + w.row0 + r) * kRank +
-                                 d) = out;
+      float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0;
+      if (M != -INFINITY) {
+        o0 = make_float4(num0.x / den, num0.y / den, num0.z / den, num0.w / den);
+        o1 = make_float4(num1.x / den, num1.y / den, num1.z / den, num1.w / den);
+      }
+      float* dst = p.partials + (static_cast<long long>(w.slot) * rows_total + w.row0 + r) * kRank + d;
+      *reinterpret_cast<float4*>(dst) = o0;
+      *reinterpret_cast<float4*>(dst + 4) = o1;
     }
   }
 }
