@@ -327,7 +327,7 @@ def run_profile_case(args):
     ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
     out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
     k = plan.clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
-    ws = rt.alloc_workspace(plan.num_chunks, k, 1, H)
+    ws = rt.alloc_workspace(plan.num_chunks, k, plan.cluster_ctas, 1, H)
     for _ in range(args.launches):
         rt.decode_partial(dc, part, lse, chunks_dev=chunks_dev, kernel=kernel, cluster=plan.cluster_ctas, subs=k,
                           workspace=ws)
@@ -416,7 +416,7 @@ def run_ours(args, rank, world):
             ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
             out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
             k = plan.clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
-            ws = rt.alloc_workspace(plan.num_chunks, k, 1, H)
+            ws = rt.alloc_workspace(plan.num_chunks, k, plan.cluster_ctas, 1, H)
             # the tables are uploaded before the step and no kernel of the step writes them
             desc = rt.make_desc(dc, chunks_dev, kernel, plan.cluster_ctas, stream, k, ws, tables_ready=True)
             calls.append(dict(L=L, plan=plan, dc=dc, chunks=chunks_dev, part=part, lse=lse, ind=ind, out=out,

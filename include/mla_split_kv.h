@@ -168,11 +168,12 @@ typedef struct {
   void* stream;               /* cudaStream_t                                 */
   int32_t clusters_per_chunk; /* k: clusters per partition; 0 or 1 = one.
                                  k > 1 (1..16): the chunk's tokens are split
-                                 over k clusters; each writes a sub-partial
-                                 (normalized partial + log2 LSE) to the
-                                 workspace and the cluster that finishes last
-                                 merges the k of them in index order into the
-                                 partition's slot. Only for the 16-row fp16
+                                 over k clusters; each CTA pair writes its part
+                                 (unnormalized O, row maxima and sums; the quad
+                                 kernel: each cluster its normalized sub-partial
+                                 + log2 LSE) to the workspace and the CTA that
+                                 finishes last merges them in index order into
+                                 the partition's slot. Only for the 16-row fp16
                                  tensor-core kernels whose CTAs share tiles in
                                  pairs or quads (q_len*H <= 16, cluster_ctas
                                  set to 2..16, not 0 = auto);
@@ -200,13 +201,16 @@ typedef struct {
 
 /*
  * mla_workspace_bytes -- device bytes a mla_decode_partial call with
- * clusters_per_chunk = k > 1 needs: one uint32 ticket per chunk (256-byte
- * aligned block), then N*k sub-partials [q_len, H, 512] fp32 and their LSEs
- * [q_len, H] fp32. 0 when k <= 1. No counterpart on the pages: the split of a
- * partition over several clusters is this library's way to fill the GPU at
- * the pages' 2..8 partitions.
+ * clusters_per_chunk = k > 1 on clusters of cluster_ctas CTAs needs: two
+ * uint32 tickets per chunk (256-byte aligned block), then E = N*k*cluster_ctas/2
+ * entries (one per CTA pair of a chunk) of [q_len, H, 512] fp32, then E x 2
+ * blocks of [q_len, H, 2] fp32 (each pair's row maxima and sums, one copy per
+ * column half). 0 when k <= 1 or cluster_ctas < 2. No counterpart on the
+ * pages: the split of a partition over several clusters is this library's way
+ * to fill the GPU at the pages' 2..8 partitions.
  */
-uint64_t mla_workspace_bytes(int32_t num_chunks, int32_t clusters_per_chunk, int32_t q_len, int32_t num_heads);
+uint64_t mla_workspace_bytes(int32_t num_chunks, int32_t clusters_per_chunk, int32_t cluster_ctas, int32_t q_len,
+                             int32_t num_heads);
 
 /* Size of the library's own scratch used by mla_decode_partial_static. */
 #define MLA_STATIC_WORKSPACE_BYTES (4u * 1024u * 1024u)

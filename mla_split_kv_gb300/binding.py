@@ -122,7 +122,7 @@ def load() -> ctypes.CDLL:
     lib.mla_partials_bytes.restype = ctypes.c_size_t
     lib.mla_lse_bytes.argtypes = [i32, i32, i32]
     lib.mla_lse_bytes.restype = ctypes.c_size_t
-    lib.mla_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.mla_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     lib.mla_workspace_bytes.restype = u64
     lib.mla_status_string.argtypes = [i32]
     lib.mla_status_string.restype = ctypes.c_char_p
@@ -242,8 +242,8 @@ def mla_set_wait_timeout_ns(ns: int) -> None:
     load().mla_set_wait_timeout_ns(ns)
 
 
-def mla_workspace_bytes(num_chunks: int, clusters_per_chunk: int, q_len: int, num_heads: int) -> int:
-    return int(load().mla_workspace_bytes(num_chunks, clusters_per_chunk, q_len, num_heads))
+def mla_workspace_bytes(num_chunks: int, clusters_per_chunk: int, cluster_ctas: int, q_len: int, num_heads: int) -> int:
+    return int(load().mla_workspace_bytes(num_chunks, clusters_per_chunk, cluster_ctas, q_len, num_heads))
 
 
 def mla_partials_bytes(num_slots: int, q_len: int, num_heads: int) -> int:

@@ -233,7 +233,7 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   if (subs > 1) {  // a partition spread over several clusters: the pair or quad kernel with a workspace
     if (C0 == 0) return reject(MLA_ERR_INVALID_ARG);  // the cluster size is part of that plan
     if (use_simt || !mla::tc128_supports(rows_total, bf16, C0)) return reject(MLA_ERR_UNSUPPORTED);
-    const uint64_t need = mla_workspace_bytes(static_cast<int32_t>(N), subs, d->q_len, d->num_heads);
+    const uint64_t need = mla_workspace_bytes(static_cast<int32_t>(N), subs, C0, d->q_len, d->num_heads);
     if (d->workspace == nullptr || !aligned(d->workspace, 16) || d->workspace_bytes < need)
       return reject(MLA_ERR_INVALID_ARG);
     if (N * subs > 65535) return reject(MLA_ERR_UNSUPPORTED);
@@ -282,10 +282,14 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   p.ws_tickets = nullptr;
   if (subs > 1) {
     uint8_t* ws = static_cast<uint8_t*>(d->workspace);
-    const uint64_t tickets = (static_cast<uint64_t>(N) * 4 + 255) / 256 * 256;
+    // tickets (two per chunk), then per chunk its entries: pairs = subs * cluster_ctas / 2 (the
+    // paired kernel: one entry per CTA pair; the quad kernel uses the first subs of them as its
+    // sub-partial slots), [rows][512] fp32 each, then per entry two [rows][2] fp32 copies
+    const uint64_t tickets = (static_cast<uint64_t>(N) * 2 * 4 + 255) / 256 * 256;
+    const uint64_t entries = static_cast<uint64_t>(N) * subs * static_cast<uint64_t>(C0 / 2);
     p.ws_tickets = reinterpret_cast<uint32_t*>(ws);
     p.ws_partials = reinterpret_cast<float*>(ws + tickets);
-    p.ws_lse = p.ws_partials + static_cast<uint64_t>(N) * subs * rows_total * mla::kRank;
+    p.ws_lse = p.ws_partials + entries * rows_total * mla::kRank;
   }
   cudaStream_t stream = static_cast<cudaStream_t>(d->stream);
   const cudaError_t e =
@@ -354,7 +358,8 @@ mla_status_t mla_decode_partial_static(const void* q_absorbed, const void* q_pe,
     const int64_t N = (dd.chunks == nullptr) ? static_cast<int64_t>(dd.num_requests) * num_partitions
                                              : static_cast<int64_t>(dd.num_chunks);
     if (N < 1 || N > 65535) return reject(MLA_ERR_INVALID_ARG);
-    const uint64_t need = mla_workspace_bytes(static_cast<int32_t>(N), dd.clusters_per_chunk, dd.q_len, dd.num_heads);
+    const uint64_t need =
+        mla_workspace_bytes(static_cast<int32_t>(N), dd.clusters_per_chunk, dd.cluster_ctas, dd.q_len, dd.num_heads);
     if (need == 0 || need > MLA_STATIC_WORKSPACE_BYTES) return reject(MLA_ERR_CAPACITY);
     void* ws = nullptr;
     const mla_status_t st = static_workspace(&ws);
@@ -366,12 +371,14 @@ mla_status_t mla_decode_partial_static(const void* q_absorbed, const void* q_pe,
                             partials, lse, &dd);
 }
 
-uint64_t mla_workspace_bytes(int32_t num_chunks, int32_t clusters_per_chunk, int32_t q_len, int32_t num_heads) {
-  if (clusters_per_chunk <= 1 || num_chunks < 1 || q_len < 1 || num_heads < 1) return 0;
+uint64_t mla_workspace_bytes(int32_t num_chunks, int32_t clusters_per_chunk, int32_t cluster_ctas, int32_t q_len,
+                             int32_t num_heads) {
+  if (clusters_per_chunk <= 1 || num_chunks < 1 || cluster_ctas < 2 || q_len < 1 || num_heads < 1) return 0;
   const uint64_t n = static_cast<uint64_t>(num_chunks), k = static_cast<uint64_t>(clusters_per_chunk);
   const uint64_t rows = static_cast<uint64_t>(q_len) * static_cast<uint64_t>(num_heads);
-  const uint64_t tickets = (n * 4 + 255) / 256 * 256;
-  return tickets + n * k * rows * mla::kRank * 4 + n * k * rows * 4;
+  const uint64_t entries = n * k * static_cast<uint64_t>(cluster_ctas / 2);
+  const uint64_t tickets = (n * 2 * 4 + 255) / 256 * 256;
+  return tickets + entries * rows * mla::kRank * 4 + entries * 2 * rows * 2 * 4;
 }
 
 mla_status_t mla_merge_states(const float* partials, const float* lse, const int32_t* o_indptr, int32_t B,

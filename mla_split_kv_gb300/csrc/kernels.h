@@ -36,13 +36,16 @@ struct PartialParams {
   int32_t causal;
   int32_t tables_ready;        // chunks / context_lens / block_table may be read before the dependency wait
   uint64_t timeout_ns;
-  // a chunk spread over `subs` clusters (paired 16-row kernel only): grid.y =
-  // chunks * subs; the sub-partials and their LSEs go to ws_partials / ws_lse
-  // (slot = grid.y index), one ticket per chunk in ws_tickets (zero between calls)
+  // a chunk spread over `subs` clusters (16-row kernels whose CTAs share tiles): grid.y =
+  // chunks * subs. Paired kernel: one entry per CTA pair of a chunk (subs * cluster / 2
+  // of them), its unnormalized O^T in ws_partials and its row maxima / sums in ws_lse,
+  // two tickets per chunk (one per column half). Quad kernel: the sub-partial of
+  // cluster grid.y in entry slot grid.y, its LSE rows at ws_lse + grid.y * rows, one
+  // ticket per chunk. Tickets are zero between calls.
   int32_t subs;
-  float* ws_partials;          // [chunks * subs, q_len, H, 512]
-  float* ws_lse;               // [chunks * subs, q_len, H]
-  uint32_t* ws_tickets;        // [chunks]
+  float* ws_partials;          // [entries, q_len, H, 512]
+  float* ws_lse;               // [entries, 2, q_len, H, 2]
+  uint32_t* ws_tickets;        // [chunks, 2]
 };
 
 struct MergeParams {

@@ -599,6 +599,130 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();  // all roles done: the tile slots are free for staging
   const bool have = (ntiles > 0) && !*abort_flag;
+  if (subs > 1) {
+    // A chunk spread over several clusters: no in-cluster combine. Every CTA writes its
+    // unnormalized O^T (its 256 columns, the rows it holds) and its row maxima and sums as the
+    // entry of its pair (entry = chunk * pairs + pair, pairs = subs * pairs per cluster) in the
+    // workspace; per chunk and half a ticket counts the CTAs, and the one that takes the last
+    // merges the half's columns over all the chunk's entries, in entry order (the result does not
+    // depend on which pair finished last), into the chunk's slot, half 0 also the LSE; it then
+    // resets the ticket. The cluster barrier split around it keeps every CTA until its peer has
+    // left the tile loop (no remote store or commit reaches a CTA that has left).
+    cluster_arrive_release();
+    const int npairs_tot = subs * cluster_pairs;
+    const long long entry = static_cast<long long>(chunk) * npairs_tot + pair_index;
+    float* const eo = p.ws_partials + entry * rows_total * kRank;                     // [rows][512]
+    float* const eml = p.ws_lse + (entry * 2 + half) * rows_total * 2;               // [rows][m, l]
+    if (warp < kSoftmaxWarps) {
+      const int q4 = warp & 3, h = warp >> 2;
+      if (have) tc_fence_after();
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        float v[kRH];
+        if (have) {
+          tmem_ld8(tmem + tmem_lane_base(q4) + 2 * kNR + blk * kNR + kRH * h, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < kRH; ++k) v[k] = 0.f;
+        }
+        const int col = kHalfCols * half + blk * 128 + q4 * 32 + lane;
+#pragma unroll
+        for (int k = 0; k < kRH; ++k)
+          if (kRH * h + k < w.nrows) eo[static_cast<long long>(w.row0 + kRH * h + k) * kRank + col] = v[k];
+      }
+      if (tid < w.nrows) {
+        eml[(w.row0 + tid) * 2] = have ? sm->mref[tid] : -INFINITY;
+        eml[(w.row0 + tid) * 2 + 1] =
+            have ? (sm->red[0][tid] + sm->red[1][tid]) + (sm->red[2][tid] + sm->red[3][tid]) : 0.f;
+      }
+    }
+    __threadfence();  // this CTA's entry, visible before its ticket
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t* ticket = p.ws_tickets + static_cast<long long>(chunk) * 2 + half;
+      const uint32_t t = atomicAdd(ticket, 1u);
+      const int last = (t == static_cast<uint32_t>(npairs_tot - 1)) ? 1 : 0;
+      if (last) atomicExch(ticket, 0u);
+      sm->last_cluster = last;
+    }
+    __syncthreads();
+    if (sm->last_cluster) {
+      __threadfence();
+      const float* const ebase = p.ws_partials + static_cast<long long>(chunk) * npairs_tot * rows_total * kRank;
+      const float* const mbase = p.ws_lse + static_cast<long long>(chunk) * npairs_tot * 2 * rows_total * 2 +
+                              static_cast<long long>(half) * rows_total * 2;
+      const long long estride = static_cast<long long>(rows_total) * kRank;  // one entry's O
+      const long long mstride = 2LL * rows_total * 2;                        // one entry's two m/l copies
+      // item = 4 columns of a row (or, half 0, a row's LSE): the values, row maximum and sum of
+      // up to 12 entries at once (one round trip), reduced in entry order; more entries take
+      // further rounds, a larger maximum rescaling what earlier rounds summed
+      const int n4 = kHalfCols / 4;
+      const int items = w.nrows * n4 + (half == 0 ? w.nrows : 0);
+      for (int idx = tid; idx < items; idx += kThreads) {
+        const bool is_lse = idx >= w.nrows * n4;
+        const int r = is_lse ? idx - w.nrows * n4 : idx / n4;
+        const int c = kHalfCols * half + (is_lse ? 0 : (idx % n4) * 4);
+        const long long rowoff = static_cast<long long>(w.row0 + r);
+        float M = -INFINITY, den = 0.f;
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e0 = 0; e0 < npairs_tot; e0 += 12) {
+          float2 ml[12];
+          float4 v[12];
+#pragma unroll
+          for (int jj = 0; jj < 12; ++jj) {
+            ml[jj] = make_float2(-INFINITY, 0.f);
+            v[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e0 + jj < npairs_tot) {
+              ml[jj] = __ldcg(reinterpret_cast<const float2*>(mbase + (e0 + jj) * mstride + rowoff * 2));
+              if (!is_lse) v[jj] = __ldcg(reinterpret_cast<const float4*>(ebase + (e0 + jj) * estride + rowoff * kRank + c));
+            }
+          }
+          float Mr = M;
+#pragma unroll
+          for (int jj = 0; jj < 12; ++jj) Mr = fmaxf(Mr, ml[jj].x);
+          if (Mr != -INFINITY) {
+            if (M != Mr) {
+              const float sc = (M == -INFINITY) ? 0.f : exp2f(M - Mr);
+              den *= sc;
+              num = make_float4(num.x * sc, num.y * sc, num.z * sc, num.w * sc);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 12; ++jj) {
+              const float wj = (ml[jj].x == -INFINITY) ? 0.f : exp2f(ml[jj].x - Mr);
+              den = fmaf(wj, ml[jj].y, den);
+              num.x = fmaf(wj, v[jj].x, num.x);
+              num.y = fmaf(wj, v[jj].y, num.y);
+              num.z = fmaf(wj, v[jj].z, num.z);
+              num.w = fmaf(wj, v[jj].w, num.w);
+            }
+          }
+          M = Mr;
+        }
+        if (is_lse) {
+          p.lse[static_cast<long long>(w.slot) * rows_total + rowoff] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
+        } else {
+          float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (M != -INFINITY) o = make_float4(num.x / den, num.y / den, num.z / den, num.w / den);
+          *reinterpret_cast<float4*>(p.partials + (static_cast<long long>(w.slot) * rows_total + rowoff) * kRank + c) = o;
+        }
+      }
+    }
+    cluster_wait_acquire();
+    if (!have && ntiles > 0) {
+      // after an abort: stores the peer issued before it left the tile loop may still be in flight
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 20000ull) {
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+      tc_fence_after();
+      tmem_dealloc(tmem, kTmemCols);
+    }
+    return;
+  }
   float* ostage = reinterpret_cast<float*>(smem + kOffTile);  // [16][256]: this CTA's columns
   float* mst = ostage + kNR * kHalfCols;
   float* lst = mst + kNR;
@@ -633,11 +757,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (globaltimer_ns() - t0 < 20000ull) {
     }
   }
-  // the cluster's result goes to the chunk's slot, or, when the chunk is spread over several
-  // clusters, to this cluster's sub-partial slot of the workspace
-  float* const dst_partials = (subs > 1) ? p.ws_partials : p.partials;
-  float* const dst_lse = (subs > 1) ? p.ws_lse : p.lse;
-  const long long dst_slot = (subs > 1) ? static_cast<long long>(blockIdx.y) : static_cast<long long>(w.slot);
+  // the cluster's result goes to the chunk's slot
+  float* const dst_partials = p.partials;
+  float* const dst_lse = p.lse;
+  const long long dst_slot = static_cast<long long>(w.slot);
   {
     // Combine the pairs of the cluster in rank order: this CTA writes output
     // columns [rank * 512 / n, (rank + 1) * 512 / n), held by the CTAs of
@@ -693,7 +816,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  if (subs > 1) merge_sub_partials(p, w, chunk, subs, &sm->last_cluster, tid, kThreads);
   cluster_sync();
   if (warp == kMmaWarp) {
     tc_fence_after();

@@ -80,9 +80,10 @@ def make_desc(dc: DeviceCase, chunks_dev: Optional[torch.Tensor], kernel: int, c
     return d
 
 
-def alloc_workspace(num_chunks: int, subs: int, q_len: int, H: int, device="cuda") -> Optional[torch.Tensor]:
-    """Zeroed workspace for partitions spread over `subs` clusters (None when subs <= 1)."""
-    n = nb.mla_workspace_bytes(num_chunks, subs, q_len, H)
+def alloc_workspace(num_chunks: int, subs: int, cluster: int, q_len: int, H: int,
+                    device="cuda") -> Optional[torch.Tensor]:
+    """Zeroed workspace for partitions spread over `subs` clusters of `cluster` CTAs (None when subs <= 1)."""
+    n = nb.mla_workspace_bytes(num_chunks, subs, cluster, q_len, H)
     return torch.zeros(n, dtype=torch.uint8, device=device) if n else None
 
 

@@ -107,11 +107,14 @@ def test_plan_spreads_partitions_only_for_the_paired_kernel(lib):
 
 
 def test_workspace_bytes(lib):
-    assert nb.mla_workspace_bytes(8, 1, 1, 16) == 0
-    n, k, rows = 8, 9, 16
-    expect = 256 + n * k * rows * 512 * 4 + n * k * rows * 4
-    assert nb.mla_workspace_bytes(n, k, 1, 16) == expect
-    assert nb.mla_workspace_bytes(100, 2, 2, 16) == 512 + 100 * 2 * 32 * 512 * 4 + 100 * 2 * 32 * 4
+    assert nb.mla_workspace_bytes(8, 1, 4, 1, 16) == 0
+    assert nb.mla_workspace_bytes(8, 4, 1, 1, 16) == 0
+    # two tickets per chunk, one entry per CTA pair: O [rows][512] + two [rows][2] blocks
+    n, k, C, rows = 8, 9, 4, 16
+    e = n * k * (C // 2)
+    assert nb.mla_workspace_bytes(n, k, C, 1, 16) == 256 + e * rows * 512 * 4 + e * 2 * rows * 2 * 4
+    e = 100 * 2 * 8
+    assert nb.mla_workspace_bytes(100, 2, 16, 2, 16) == 1024 + e * 32 * 512 * 4 + e * 2 * 32 * 2 * 4
 
 
 def test_plan_mixed_batch_two_to_four(lib):

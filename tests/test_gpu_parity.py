@@ -64,7 +64,7 @@ def run_uniform(case, P, kernel, cluster, dc=None, subs=1, ws=None):
     part, lse = rt.alloc_partials(B * P, q, H)
     part.fill_(float("nan"))
     if subs > 1 and ws is None:
-        ws = rt.alloc_workspace(B * P, subs, q, H)
+        ws = rt.alloc_workspace(B * P, subs, cluster, q, H)
     rt.decode_partial(dc, part, lse, num_partitions=P, kernel=kernel, cluster=cluster, subs=subs, workspace=ws)
     ind = rt.uniform_indptr(B, P)
     out = rt.merge_states(part, lse, ind, B, q, H, "f32")
@@ -215,7 +215,7 @@ def plan_and_run(case, max_partitions=0, kernel=nb.MLA_KERNEL_TC, dc=None, ws=No
     part, lse = rt.alloc_partials(plan.num_chunks, case.q_len, case.num_heads)
     k = plan.clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
     if k > 1 and ws is None:
-        ws = rt.alloc_workspace(plan.num_chunks, k, case.q_len, case.num_heads)
+        ws = rt.alloc_workspace(plan.num_chunks, k, plan.cluster_ctas, case.q_len, case.num_heads)
     rt.decode_partial(dc, part, lse, chunks_dev=chunks_dev, kernel=kernel, cluster=plan.cluster_ctas, subs=k,
                       workspace=ws, tables_ready=tables_ready)
     ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
@@ -290,7 +290,7 @@ def test_spread_partitions_bitwise_reproducible_and_workspace_reused():
     dev = nb.mla_device_query()
     plan = nb.mla_plan([131072], 16, 1, 32, dev)
     assert plan.clusters_per_chunk > 1
-    ws = rt.alloc_workspace(plan.num_chunks, plan.clusters_per_chunk, 1, 16)
+    ws = rt.alloc_workspace(plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, 16)
     outs = []
     for _ in range(3):
         _, part, lse, out = plan_and_run(case, dc=dc, ws=ws)
@@ -298,7 +298,7 @@ def test_spread_partitions_bitwise_reproducible_and_workspace_reused():
     for other in outs[1:]:
         for a, b in zip(outs[0], other):
             assert torch.equal(a, b)
-    tickets = ws[: 4 * plan.num_chunks].view(torch.int32)
+    tickets = ws[: 8 * plan.num_chunks].view(torch.int32)
     assert int(tickets.abs().sum()) == 0
 
 

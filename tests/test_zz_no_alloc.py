@@ -38,10 +38,10 @@ def call_static(dc, part, lse, desc, P):
 def test_static_entry_matches_workspace_entry_two_calls_in_a_row(L, P, C, k):
     case = gen.make_decode_case(7, [L], num_heads=16, block_size=32, dtype="f16")
     dc = rt.upload(case)
-    assert nb.mla_workspace_bytes(P, k, 1, 16) <= nb.MLA_STATIC_WORKSPACE_BYTES
+    assert nb.mla_workspace_bytes(P, k, C, 1, 16) <= nb.MLA_STATIC_WORKSPACE_BYTES
     # the existing entry point, with a caller workspace
     ref_part, ref_lse = rt.alloc_partials(P, 1, 16)
-    ws = rt.alloc_workspace(P, k, 1, 16)
+    ws = rt.alloc_workspace(P, k, C, 1, 16)
     rt.decode_partial(dc, ref_part, ref_lse, num_partitions=P, kernel=nb.MLA_KERNEL_TC, cluster=C, subs=k,
                       workspace=ws)
     # the static variant, twice in a row on the same stream (its tickets must be back at zero in between)
@@ -62,7 +62,7 @@ def test_static_entry_rejects_plans_beyond_its_scratch():
     case = gen.make_decode_case(8, [4096], num_heads=16, block_size=32, dtype="f16")
     dc = rt.upload(case)
     P, k = 64, 16  # 64 * 16 sub-partials of 16 x 513 floats: more than 4 MiB
-    assert nb.mla_workspace_bytes(P, k, 1, 16) > nb.MLA_STATIC_WORKSPACE_BYTES
+    assert nb.mla_workspace_bytes(P, k, 2, 1, 16) > nb.MLA_STATIC_WORKSPACE_BYTES
     part, lse = rt.alloc_partials(P, 1, 16)
     desc = rt.make_desc(dc, None, nb.MLA_KERNEL_TC, 2, None, k, None)
     nb.mla_reset_counters()
