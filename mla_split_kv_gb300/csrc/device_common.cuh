@@ -205,11 +205,6 @@ __device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr) {
   return v;
 }
 
-// Store to another CTA's shared memory; published by a release arrive on that
-// CTA's mbarrier (mbar_remote_arrive) issued after it.
-__device__ __forceinline__ void dsmem_st_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
 // Asynchronous 16-byte store to another CTA's shared memory; its bytes count
 // as completed transactions on that CTA's mbarrier `remote_bar` (both
 // addresses from dsmem_addr). The sender does not wait for it.
@@ -235,11 +230,6 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t 
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
-// Arrive, with release semantics at cluster scope, on an mbarrier of another
-// CTA (address from dsmem_addr).
-__device__ __forceinline__ void mbar_remote_arrive(uint32_t addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
 // Arrive without memory ordering on an mbarrier of another CTA: a pure signal,
 // for use only where every access it must follow has completed (values

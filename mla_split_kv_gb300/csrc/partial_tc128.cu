@@ -30,7 +30,8 @@
 // once the tile's score product is done; it then takes the peer's partial
 // scores of the tile, and after those are read, the tile's P^T. Pairs of a
 // cluster split the chunk's tiles; the cluster combines at the end, in rank
-// order.
+// order. A chunk spread over several clusters skips that combine: every pair
+// writes its part to the workspace and the last CTA to finish merges them.
 //
 // The ckv half of a tile arrives as one 4D TMA box per page (64 columns x 8
 // rows x 4 column blocks x page/8 row groups): it lands as row groups of four
