@@ -242,7 +242,8 @@ def test_long_context_planned_full_size_sampled_heads(L):
 @pytest.mark.parametrize("L,P,C,k,bs", [(4096, 2, 2, 4, 32), (4096, 1, 4, 2, 32), (20017, 3, 2, 5, 16),
                                          (20017, 2, 4, 3, 64), (9000, 2, 16, 2, 32)])
 def test_spread_partitions_partials_match_oracle(L, P, C, k, bs):
-    """Each partition over k clusters (sub-partials merged by the last cluster) gives the partition's partial."""
+    """Each partition over k clusters (every CTA pair's part merged by the last CTA to finish, up to 16 parts:
+    more than one round of the merge) gives the partition's partial."""
     case = gen.make_decode_case(5, [L], num_heads=16, block_size=bs, dtype="f16")
     nb.mla_reset_counters()
     part, lse, out, ind, dc = run_uniform(case, P, nb.MLA_KERNEL_TC, cluster=C, subs=k)
@@ -284,7 +285,7 @@ def test_tables_read_before_the_dependency_wait_give_the_same_bits(L):
 
 def test_spread_partitions_bitwise_reproducible_and_workspace_reused():
     """Same plan, same workspace, several calls: identical bits (the merge order does not depend on which
-    cluster finishes last, and every call leaves its tickets at zero)."""
+    pair finishes last, and every call leaves its tickets at zero)."""
     case = gen.make_decode_case(6, [131072], num_heads=16, block_size=32, dtype="f16")
     dc = rt.upload(case)
     dev = nb.mla_device_query()
