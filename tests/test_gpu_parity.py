@@ -223,11 +223,13 @@ def plan_and_run(case, max_partitions=0, kernel=nb.MLA_KERNEL_TC, dc=None, ws=No
     return plan, part, lse, out
 
 
-@pytest.mark.parametrize("L", [32768, 131072])
+@pytest.mark.parametrize("L", [32768, 49152, 65536, 81920, 98304, 131072])
 def test_long_context_planned_full_size_sampled_heads(L):
+    """Every context of the bench's sweep, in the bench's launch configuration (the planner's plan, tables
+    read before the dependency wait), against the oracle on sampled heads."""
     case = gen.make_decode_case(2, [L], num_heads=16, block_size=32, dtype="f16")
     nb.mla_reset_counters()
-    plan, part, lse, out = plan_and_run(case)
+    plan, part, lse, out = plan_and_run(case, tables_ready=True)
     assert 2 <= plan.num_chunks <= 8, plan.parts()
     if L == 131072:
         assert plan.clusters_per_chunk > 1  # the partitions are spread over clusters to fill the GPU
