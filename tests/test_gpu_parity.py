@@ -327,9 +327,10 @@ def test_many_rows_pair_kernel_partials(H, q_len, dtype, bs, lens, causal):
     assert_close(out.cpu().numpy(), ref, f"merged H={H} q={q_len} {dtype} bs={bs}")
 
 
-def test_mixed_batch_request_major():
+@pytest.mark.parametrize("tables_ready", [False, True])
+def test_mixed_batch_request_major(tables_ready):
     case = gen.make_decode_case(3, [32768, 20000], num_heads=16, block_size=32, dtype="f16")
-    plan, part, lse, out = plan_and_run(case, max_partitions=4)
+    plan, part, lse, out = plan_and_run(case, max_partitions=4, tables_ready=tables_ready)
     assert all(2 <= p <= 4 for p in plan.parts()), plan.parts()
     heads = [0, 5, 10, 15]
     ref, _ = orc.unsplit(case, heads=heads)
