@@ -308,6 +308,31 @@ mla_status_t mla_merge_states(const float* partials, const float* lse, const int
  */
 mla_status_t mla_check_device_errors(void* stream, uint32_t* code_out);
 
+/*
+ * mla_selfcheck -- run mla_plan, mla_decode_partial and mla_merge_states on
+ * the current device over a built-in case whose answer is known in closed
+ * form, and compare. The case has 2 requests (6000 and 700 tokens, ragged last
+ * pages, pages of 32 tokens scattered over a 256-page pool whose unowned pages
+ * hold 1000.0) and 16 heads: 15 heads whose query picks out one "needle"
+ * token through either the rope key or one latent column (score 64 against
+ * at most 16 elsewhere, so the merged output is that token's latent row and
+ * the LSE is 64 log2 e), and one head with all-zero queries (the mean of the
+ * latent rows, LSE log2 L; softmax of equal scores, mlxcel PR #995 *What
+ * changed*: the partial is normalized, the LSE in base 2). It runs in fp16
+ * and bf16, on the planner's default kernel choice and on the CUDA-core
+ * kernel.
+ *
+ * Unlike the other calls it allocates device memory (about 25 MB), creates
+ * and synchronizes its own stream, and reads and clears the device error
+ * word (as mla_check_device_errors does). Not for a hot path.
+ * *max_abs_err (nullable) receives the largest |output - expected| seen.
+ * Returns MLA_OK when every output row is within 1e-6 (needle rows, exact in
+ * fp32) or 2e-3 (the mean row) and every LSE within 1e-3;
+ * MLA_ERR_DEVICE_CHECK on a mismatch; otherwise the first failing call's
+ * status (MLA_ERR_CUDA without a usable device).
+ */
+mla_status_t mla_selfcheck(float* max_abs_err);
+
 /* Launch counters proving which kernel ran (mlxcel PR #995 `mla/stats.rs`:
  * per-path counters read around a measured region). Indices: */
 #define MLA_CTR_PARTIAL_SIMT 0

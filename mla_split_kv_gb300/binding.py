@@ -112,6 +112,8 @@ def load() -> ctypes.CDLL:
     lib.mla_merge_states.restype = i32
     lib.mla_check_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.mla_check_device_errors.restype = i32
+    lib.mla_selfcheck.argtypes = [ctypes.POINTER(f32)]
+    lib.mla_selfcheck.restype = i32
     lib.mla_get_counters.argtypes = [ctypes.POINTER(u64), i32]
     lib.mla_get_counters.restype = None
     lib.mla_reset_counters.argtypes = []
@@ -226,6 +228,12 @@ def mla_check_device_errors(stream: Optional[int] = None):
     """Synchronize and read/clear the device error word; returns (status, word)."""
     code = ctypes.c_uint32(0)
     return load().mla_check_device_errors(stream or None, ctypes.byref(code)), code.value
+
+
+def mla_selfcheck():
+    """Run the library's closed-form decode check on the current device; returns (status, max-abs error)."""
+    err = ctypes.c_float(0.0)
+    return load().mla_selfcheck(ctypes.byref(err)), err.value
 
 
 def mla_get_counters():

@@ -36,7 +36,7 @@ def header_functions():
 def test_header_declares_the_core_calls():
     names = header_functions()
     for must in ("mla_plan", "mla_decode_partial", "mla_merge_states", "mla_device_query",
-                 "mla_check_device_errors", "mla_get_counters"):
+                 "mla_check_device_errors", "mla_get_counters", "mla_selfcheck"):
         assert must in names
 
 

@@ -397,3 +397,15 @@ def test_out_of_range_page_reads_zeros_and_is_flagged():
     st, code = nb.mla_check_device_errors(None)
     assert st == nb.MLA_ERR_DEVICE_CHECK and code & 2
     assert np.all(np.isfinite(out.cpu().numpy()))
+
+
+def test_selfcheck_closed_form_case():
+    """The library's built-in check (needle heads and a uniform head, fp16 and bf16, default and CUDA-core
+    kernels) passes on this device; its closed form is confirmed by the oracle in the CPU tests."""
+    nb.mla_check_device_errors(None)
+    nb.mla_reset_counters()
+    st, err = nb.mla_selfcheck()
+    assert st == nb.MLA_OK, (st, err)
+    assert err <= 2e-3
+    ctr = nb.mla_get_counters()
+    assert ctr[nb.CTR_PARTIAL_TC] == 2 and ctr[nb.CTR_PARTIAL_SIMT] == 2 and ctr[nb.CTR_MERGE] == 4
