@@ -11,6 +11,7 @@ import pytest
 
 from oracle import mla_oracle as orc
 import tests.test_oracle_pins as pins
+import tests.test_selfcheck_case_cpu as selfcase
 
 
 def _drop_rope(q_abs, q_pe, ckv_rows, kpe_rows, scale):
@@ -57,16 +58,34 @@ def _merge_natural(part, lse2, o_indptr):
     return out, out_lse
 
 
+def _chunks_unaligned(n_tokens, n_parts, block_size):
+    C = -(-n_tokens // n_parts)  # forgets to round the chunk length up to whole pages
+    return [(min(p * C, n_tokens), min((p + 1) * C, n_tokens)) for p in range(n_parts)]
+
+
+def _indptr_slip(context_lens, parts, block_size):
+    chunks, indptr = [], [0]
+    for b, (L, P) in enumerate(zip(context_lens, parts)):
+        indptr.append(len(chunks))  # records the start instead of the end of request b
+        for t0, t1 in orc.chunk_bounds(int(L), int(P), block_size):
+            chunks.append((b, t0, t1))
+    return chunks, indptr
+
+
 MUTATIONS = [
     ("scores", _drop_rope, [pins.test_rope_score_is_additive,
                             lambda: pins.test_matches_torch_sdpa_on_concatenated_keys("f16", 1, False)]),
     ("scores", _scale_latent_only, [lambda: pins.test_matches_torch_sdpa_on_concatenated_keys("f16", 1, False)]),
-    ("attend", _natural_log_lse, [pins.test_zero_query_gives_uniform_mean_and_log2_count]),
+    ("attend", _natural_log_lse, [pins.test_zero_query_gives_uniform_mean_and_log2_count,
+                                  lambda: selfcase.test_selfcheck_case_has_the_closed_form_answer("f16")]),
     ("visible", _causal_off_by_one, [pins.test_visible_rule_small_window,
                                      pins.test_brute_force_pure_python_tiny]),
     ("physical_rows", _page_slip, [pins.test_physical_rows_hand_table,
                                    lambda: pins.test_matches_torch_sdpa_on_concatenated_keys("f16", 1, False)]),
     ("merge", _merge_natural, [pins.test_merge_weights_are_base_two]),
+    ("chunk_bounds", _chunks_unaligned, [pins.test_chunk_bounds_examples_and_invariants,
+                                         pins.test_plan_chunks_covers_every_token_once_request_major]),
+    ("plan_chunks", _indptr_slip, [pins.test_plan_chunks_covers_every_token_once_request_major]),
 ]
 
 

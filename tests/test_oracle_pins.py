@@ -210,6 +210,25 @@ def test_chunk_bounds_examples_and_invariants():
                     assert t0 <= t1 and (t0 % bs == 0 or t0 == L)
 
 
+def test_plan_chunks_covers_every_token_once_request_major():
+    # brute force over tiny batches: each (request, token) lies in exactly one chunk of that
+    # request, the chunks of request b are o_indptr[b]..o_indptr[b+1]-1, P_b of them, and
+    # every chunk starts on a page boundary (or at the end of an exhausted request)
+    lens, parts, bs = [0, 5, 33, 64, 100], [1, 2, 3, 2, 4], 16
+    chunks, indptr = orc.plan_chunks(lens, parts, bs)
+    assert indptr[0] == 0 and indptr[-1] == len(chunks) == sum(parts)
+    for b, (L, P) in enumerate(zip(lens, parts)):
+        mine = chunks[indptr[b]:indptr[b + 1]]
+        assert len(mine) == P and all(c[0] == b for c in mine)
+        hits = np.zeros(L, dtype=int)
+        for _, t0, t1 in mine:
+            assert t0 % bs == 0 or t0 == L
+            hits[t0:t1] += 1
+        assert np.all(hits == 1)
+        starts = [t0 for _, t0, _ in mine]
+        assert starts == sorted(starts)
+
+
 # --- split + merge -----------------------------------------------------------------
 
 @pytest.mark.parametrize("chunk_len", [1, 7, 8, 29, 90])
