@@ -14,6 +14,9 @@ tables and plan of the six calls copied in with one copy from one pinned
 buffer, the six outputs copied out with one copy, every step); `roofline` = the
 partial kernel's algorithmic HBM bytes / its CUDA-event time against the
 measured copy bandwidth; `cpu_baseline` = the f64 oracle on the host cores.
+Outside the timed region: `per_ctx` (each context alone, its planned split, a
+single cold call after an L2 flush and the host planner's time per call) and
+`trials` (median / min / max over five more K-step trials).
 `--impl reference` times the oracle itself on the same workload.
 """
 from __future__ import annotations
@@ -241,6 +244,33 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+
+def planner_host_us(nb, lens, dev, batches=5, reps=400):
+    """Host time of one mla_plan call (median over batches of the per-call mean), with the
+    ctypes arguments built once so that mostly the C planner is timed."""
+    import ctypes
+
+    lib = nb.load()
+    B = len(lens)
+    arr = (ctypes.c_int32 * B)(*[int(x) for x in lens])
+    cap = 8 * B + 64
+    chunks = (nb.mla_chunk_t * cap)()
+    indptr = (ctypes.c_int32 * (B + 1))()
+    plan = nb.mla_plan_t()
+    plan.capacity = cap
+    plan.dtype = nb.DTYPE_CODES[DTYPE]
+    plan.chunks = ctypes.cast(chunks, ctypes.POINTER(nb.mla_chunk_t))
+    plan.o_indptr = ctypes.cast(indptr, ctypes.POINTER(ctypes.c_int32))
+    pdev, pplan = ctypes.byref(dev), ctypes.byref(plan)
+    per = []
+    for _ in range(batches):
+        t0 = time.perf_counter_ns()
+        for _ in range(reps):
+            if lib.mla_plan(arr, B, H, 1, BS, pdev, pplan) != nb.MLA_OK:
+                raise RuntimeError("mla_plan failed")
+        per.append((time.perf_counter_ns() - t0) / reps / 1e3)
+    return statistics.median(per)
+
 
 def algorithmic_bytes(L, n_chunks):
     """(partial kernel bytes, merge kernel bytes) one layer call must move."""
@@ -526,6 +556,41 @@ def run_ours(args, rank, world):
                         "partial_gbs": round(pb / (pus * 1e-6) / 1e9, 1),
                         "note": "repeats of one cache; caches <= 113 MB may be partly L2-resident"})
 
+    # a single cold call per context: L2 flushed by writing 512 MB, then one un-graphed layer call
+    # (host launch included), event-timed; median of three. And the host planner's time per call.
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    for c, row in zip(calls, per_ctx):
+        cold = []
+        for t in range(3):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            with torch.cuda.stream(stream):
+                flush.fill_(t + 1)
+                e[0].record(stream)
+                partial(c)
+                merge(c)
+                e[1].record(stream)
+            stream.synchronize()
+            cold.append(e[0].elapsed_time(e[1]) * 1e3)
+        row["cold_us"] = round(statistics.median(cold), 3)
+        row["planner_host_us"] = round(planner_host_us(nb, [c["L"]], dev), 3)
+    del flush
+    # spread of the step time: five more trials of K graph replays each (outside the timed region)
+    trial_us = []
+    for _ in range(5):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        with torch.cuda.stream(stream):
+            e[0].record(stream)
+            for _ in range(K):
+                g_step.replay()
+            e[1].record(stream)
+        stream.synchronize()
+        trial_us.append(e[0].elapsed_time(e[1]) * 1e3 / (K * len(calls)))
+    trials = {"n": 5, "median_us": round(statistics.median(trial_us), 3), "min_us": round(min(trial_us), 3),
+              "max_us": round(max(trial_us), 3)}
+    st, code = nb.mla_check_device_errors(stream.cuda_stream)
+    if st != nb.MLA_OK:
+        raise RuntimeError(f"device error word {code:#x} in the cold-call timing")
+
     # end to end through the C ABI with host buffers (pinned), every step: the inputs of the six calls
     # (queries, block tables, lengths, partition tables, merge offsets) sit in one pinned host buffer
     # that mirrors one device buffer, so a step uploads them with one copy; the six outputs come back
@@ -634,6 +699,7 @@ def run_ours(args, rank, world):
                    "timing": "CUDA graph per step (6 layer calls), CUDA events on the launching stream; "
                              "roofline from a graph of the 6 partial launches"},
         "per_ctx": per_ctx,
+        "trials": trials,
         "many_heads": many_heads,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),

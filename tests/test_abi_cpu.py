@@ -143,6 +143,12 @@ def test_plan_short_and_empty_requests_are_not_split(lib):
     check_plan_tiles(plan, lens, 16)
 
 
+def test_planner_host_timing_helper(lib):
+    import bench
+    us = bench.planner_host_us(nb, [131072], fake_gb300(), batches=2, reps=20)
+    assert 0 < us < 1e4
+
+
 def test_plan_is_deterministic(lib):
     lens = gen.uniform_lengths(9, 5, 1000, 90000)
     a = nb.mla_plan(lens, 16, 4, 32, fake_gb300())
