@@ -180,6 +180,9 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
         N = cand.parts[0];
       }
     }
+    // the time model assumes one wave: a launch whose clusters cannot all be co-resident (the
+    // partition floor exceeding the device's clusters of this size) is not a candidate
+    if (paired_single && N * cand.subs * row_groups > slots) continue;
     if (paired_single) cand.cost_us = paired_cost_us(context_lens_host[0], N, cand.subs, C);
     cand.active = std::min<int64_t>(N * row_groups * cand.subs, slots) * C;
     if (paired_single) {

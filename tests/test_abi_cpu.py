@@ -149,6 +149,35 @@ def test_planner_host_timing_helper(lib):
     assert 0 < us < 1e4
 
 
+def fake_device(num_sms, max_clusters):
+    dev = nb.mla_device_info_t()
+    dev.num_sms = num_sms
+    for k, v in enumerate(max_clusters):
+        dev.max_clusters[k] = v
+    return dev
+
+
+@pytest.mark.parametrize("sms,clusters", [
+    (132, [132, 66, 33, 16, 8]),   # fewer SMs
+    (148, [148, 74, 36, 18, 0]),   # clusters of 16 unavailable
+    (20, [20, 10, 5, 2, 1]),       # a small part
+    (152, [152, 76, 0, 0, 0]),     # pairs only
+])
+@pytest.mark.parametrize("L", [4096, 32768, 131072])
+def test_plan_follows_the_device(lib, sms, clusters, L):
+    dev = fake_device(sms, clusters)
+    plan = nb.mla_plan([L], 16, 1, 32, dev)
+    C, k, N = plan.cluster_ctas, plan.clusters_per_chunk, plan.num_chunks
+    log2c = C.bit_length() - 1
+    assert C in (1, 2, 4, 8, 16) and clusters[log2c] > 0  # never a size the device cannot launch
+    assert 2 <= N <= 8  # the pages' 2..8 gate for a split request
+    assert N * k <= clusters[log2c]  # every cluster of the launch is co-resident (one wave)
+    assert N * k * C <= sms
+    check_plan_tiles(plan, [L], 32)
+    for (_, t0, t1, _) in plan.chunks:  # every CTA pair keeps at least one 128-token tile
+        assert t1 - t0 >= k * max(1, C // 2) * 128
+
+
 def test_plan_is_deterministic(lib):
     lens = gen.uniform_lengths(9, 5, 1000, 90000)
     a = nb.mla_plan(lens, 16, 4, 32, fake_gb300())
