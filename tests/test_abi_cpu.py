@@ -178,6 +178,25 @@ def test_plan_follows_the_device(lib, sms, clusters, L):
         assert t1 - t0 >= k * max(1, C // 2) * 128
 
 
+@pytest.mark.parametrize("sms,clusters", [
+    (132, [132, 66, 33, 16, 8]),
+    (148, [148, 74, 36, 18, 0]),
+    (20, [20, 10, 5, 2, 1]),
+])
+@pytest.mark.parametrize("H,dtype,bs,maxp", [(128, "bf16", 64, 64), (16, "f16", 32, 4), (16, "bf16", 16, 8)])
+def test_batch_plans_follow_the_device(lib, sms, clusters, H, dtype, bs, maxp):
+    dev = fake_device(sms, clusters)
+    lens = gen.uniform_lengths(4, 8, 4096, 65536) + [0, 1000]
+    plan = nb.mla_plan(lens, H, 1, bs, dev, max_partitions=maxp, dtype=dtype)
+    C = plan.cluster_ctas
+    assert C in (1, 2, 4, 8, 16) and clusters[C.bit_length() - 1] > 0
+    if H == 128:
+        assert C == 2  # the 128-row kernel runs on one CTA pair
+    parts = plan.parts()
+    assert all(1 <= p <= maxp for p in parts) and parts[-2:] == [1, 1]
+    check_plan_tiles(plan, lens, bs)
+
+
 def test_plan_is_deterministic(lib):
     lens = gen.uniform_lengths(9, 5, 1000, 90000)
     a = nb.mla_plan(lens, 16, 4, 32, fake_gb300())
