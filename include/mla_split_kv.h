@@ -292,7 +292,10 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
  * once, to nearest-even, to out_dtype.
  *
  * partials : device [N, q_len, H, 512] fp32;  lse: device [N, q_len, H] fp32
- * o_indptr : device [B+1] int32, non-decreasing, o_indptr[0] = 0
+ * o_indptr : device [B+1] int32, non-decreasing, o_indptr[0] = 0, and
+ *            o_indptr[B] <= the slots held by partials / lse. The offsets are
+ *            device data and are not checked: a table that breaks this reads
+ *            outside the buffers (mla_plan's o_indptr always satisfies it).
  * out      : device [B, q_len, H, 512] of out_dtype (MLA_F16/BF16/F32)
  * out_lse  : device [B, q_len, H] fp32, or NULL
  */
