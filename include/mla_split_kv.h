@@ -138,7 +138,10 @@ typedef struct {
  * the paired 16-row kernel applies (q_len*H <= 16, fp16, clusters of >= 2)
  * and one wave holds more clusters than partitions, each partition is spread
  * over clusters_per_chunk = k clusters (k <= 16, every CTA pair keeping at
- * least one 128-token tile); the partition count itself is not raised.
+ * least one 128-token tile); the partition count itself is not raised. For a
+ * single long request on that kernel, P, the cluster size and k are chosen
+ * by a time model among the plans whose P * k clusters are all co-resident
+ * (one wave).
  *
  * context_lens_host: host [B] int32, each >= 0. dev: from mla_device_query or
  * hand-filled. Returns MLA_ERR_CAPACITY when N > plan->capacity (num_chunks
