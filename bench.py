@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--kernel", default="tc", choices=["tc", "tc_quad", "simt"])
+    ap.add_argument("--kernel", default="tc", choices=["tc", "simt"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-ctx", type=int, default=0,
@@ -292,7 +292,7 @@ def measured_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("partial_tc.cu", "partial_tc128.cu", "partial_quad.cu", "device_common.cuh", "kernels.h"):
+    for f in ("partial_tc.cu", "partial_tc128.cu", "device_common.cuh", "kernels.h"):
         h.update(open(os.path.join(ROOT, "mla_split_kv_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -307,6 +307,52 @@ def profiled_traffic(kernel_name, tokens_per_launch):
         return None
     bpt = prof.get("dram_bytes_per_token")
     return None if bpt is None else round(bpt * tokens_per_launch)
+
+
+def free_port():
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def replica_command(nprocs, script, script_args, port):
+    """One process per GPU on this node: torch's launcher, rendezvous on 127.0.0.1."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={nprocs}",
+            "--master-addr=127.0.0.1", f"--master-port={port}", script, *script_args]
+
+
+def launch_replicas(nprocs, script_args, script=None, stdout=None):
+    """Run `script` (this file by default) as `nprocs` ranks and wait for them; returns the exit status.
+    Each rank reads RANK / LOCAL_RANK / WORLD_SIZE from the environment the launcher sets."""
+    cmd = replica_command(nprocs, script or os.path.abspath(__file__), list(script_args), free_port())
+    return subprocess.run(cmd, stdout=stdout, text=True)
+
+
+def init_ranks():
+    """(rank, world, local rank) of this process. Under a launcher (WORLD_SIZE > 1) it binds the process to GPU
+    LOCAL_RANK and joins the process group (NCCL on GPUs, gloo on a machine without them); the group carries
+    only the barrier around the timed region and the max over ranks."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            torch.distributed.init_process_group("nccl")
+        else:
+            torch.distributed.init_process_group("gloo")
+    return rank, world, local
+
+
+def finish_ranks(world):
+    if world > 1:
+        import torch
+
+        torch.distributed.destroy_process_group()
 
 
 def max_over_ranks(value, device):
@@ -328,8 +374,6 @@ def partial_kernel_name(kernel, plans):
     """The partial kernel the library dispatches for this workload (16 fp16 rows per CTA)."""
     if kernel == "simt":
         return "mla_partial_simt_kernel"
-    if kernel == "tc_quad" and all(p.cluster_ctas in (4, 8, 16) for p in plans):
-        return "mla_partial_quad_kernel"
     if all(2 <= p.cluster_ctas <= 16 for p in plans):
         return "mla_partial_tc128_kernel"
     return "mla_partial_tc_kernel"
@@ -350,7 +394,7 @@ def run_profile_case(args):
     case = make_case(i, L)
     dev = nb.mla_device_query()
     plan = nb.mla_plan([L], H, 1, BS, dev)
-    kernel = {"tc": nb.MLA_KERNEL_TC, "tc_quad": nb.MLA_KERNEL_TC_QUAD, "simt": nb.MLA_KERNEL_SIMT}[args.kernel]
+    kernel = {"tc": nb.MLA_KERNEL_TC, "simt": nb.MLA_KERNEL_SIMT}[args.kernel]
     dc = rt.upload(case)
     chunks_dev = rt.chunks_to_device(plan.chunks)
     part, lse = rt.alloc_partials(plan.num_chunks, 1, H)
@@ -430,7 +474,7 @@ def run_ours(args, rank, world):
     nb.load()
     dev_index = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(dev_index)
-    kernel = {"tc": nb.MLA_KERNEL_TC, "tc_quad": nb.MLA_KERNEL_TC_QUAD, "simt": nb.MLA_KERNEL_SIMT}[args.kernel]
+    kernel = {"tc": nb.MLA_KERNEL_TC, "simt": nb.MLA_KERNEL_SIMT}[args.kernel]
 
     cases = make_cases()
     dev = nb.mla_device_query()
@@ -751,17 +795,18 @@ def main():
     if args.profile_many_heads:
         run_profile_many_heads(args)
         return
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # no launcher around this process: start one rank per GPU (this file again, same arguments)
+        raise SystemExit(launch_replicas(args.gpus, sys.argv[1:]).returncode)
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} does not match the launcher's WORLD_SIZE {world}")
     if args.impl == "reference":
-        res = run_reference(args, rank, world)
+        res = run_reference(args, int(os.environ.get("RANK", "0")), world)
         if res is not None:
             print(json.dumps(res))
         return
-    if world > 1:
-        import torch
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-        torch.distributed.init_process_group("nccl")
+    rank, world, _ = init_ranks()
     res, cases = run_ours(args, rank, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
@@ -770,10 +815,9 @@ def main():
                                "cores": cores, "kind": "oracle",
                                "sample": f"{steps} sweep of the six contexts (one layer call each, all 16 heads), "
                                          f"f64 numpy oracle in {cores} spawned single-threaded workers"}
-    if world > 1:
-        import torch
-        torch.distributed.destroy_process_group()
+    finish_ranks(world)
     if rank == 0:
+        assert res["n_gpus"] == args.gpus
         print(json.dumps(res))
 
 

@@ -73,13 +73,7 @@ typedef enum { MLA_F16 = 0, MLA_BF16 = 1, MLA_F32 = 2 } mla_dtype_t;
 typedef enum {
   MLA_KERNEL_AUTO = 0,
   MLA_KERNEL_SIMT = 1,   /* CUDA-core fp32 FMA kernel                        */
-  MLA_KERNEL_TC = 2,     /* tcgen05/TMEM tensor-core kernel                  */
-  MLA_KERNEL_TC_QUAD = 3 /* at q_len*H <= 16 in fp16 with clusters of 4, 8 or
-                            16 CTAs: the tensor-core variant whose CTAs share
-                            each tile in quads (scores split by columns, PV
-                            by tokens) instead of pairs; same results within
-                            rounding, slower on the long-context decode; kept
-                            to compare the two designs. Elsewhere like TC.   */
+  MLA_KERNEL_TC = 2      /* tcgen05/TMEM tensor-core kernel                  */
 } mla_kernel_t;
 
 /* One partition: logical tokens [t0, t1) of request b; its partial and LSE go
@@ -172,14 +166,13 @@ typedef struct {
   int32_t clusters_per_chunk; /* k: clusters per partition; 0 or 1 = one.
                                  k > 1 (1..16): the chunk's tokens are split
                                  over k clusters; each CTA pair writes its part
-                                 (unnormalized O, row maxima and sums; the quad
-                                 kernel: each cluster its normalized sub-partial
-                                 + log2 LSE) to the workspace and the CTA that
-                                 finishes last merges them in index order into
-                                 the partition's slot. Only for the 16-row fp16
-                                 tensor-core kernels whose CTAs share tiles in
-                                 pairs or quads (q_len*H <= 16, cluster_ctas
-                                 set to 2..16, not 0 = auto);
+                                 (unnormalized O, row maxima and sums) to the
+                                 workspace and the CTA that finishes last
+                                 merges them in index order into the
+                                 partition's slot. Only for the 16-row fp16
+                                 tensor-core kernel whose CTAs share tiles in
+                                 pairs (q_len*H <= 16, cluster_ctas set to
+                                 2..16, not 0 = auto);
                                  otherwise MLA_ERR_UNSUPPORTED (INVALID_ARG for
                                  cluster_ctas 0 or a missing / short workspace;
                                  k > 16 is INVALID_ARG).                         */
@@ -230,13 +223,22 @@ uint64_t mla_workspace_bytes(int32_t num_chunks, int32_t clusters_per_chunk, int
  *
  * Set-up happens on the first call for a device (with that device
  * current): the scratch address is looked up and the scratch is cleared,
- * synchronously. Make that first call before any stream capture. Calls on
- * one device share the scratch: calls that may overlap in time (other
- * streams, other threads) race and give undefined results; calls in one
- * stream are fine. Returns MLA_ERR_CAPACITY (before any launch) when
- * mla_workspace_bytes(...) of the call exceeds MLA_STATIC_WORKSPACE_BYTES,
- * MLA_ERR_CUDA when the set-up fails, otherwise what mla_decode_partial
- * returns. With clusters_per_chunk <= 1 it is mla_decode_partial.
+ * synchronously. Make that first call before any stream capture. The set-up
+ * is kept for the life of the process: after cudaDeviceReset (or anything
+ * else that replaces the device's primary context) this entry point must not
+ * be used again in that process. Calls on one device share the scratch:
+ * calls that may overlap in time (other streams, other threads) race and
+ * give undefined results; calls in one stream are fine. Every call that
+ * completes leaves the scratch's tickets at zero; a call stopped by a device
+ * error may not, so mla_check_device_errors clears the current device's
+ * scratch again whenever it finds the error word set.
+ *
+ * Returns MLA_ERR_CAPACITY (before any launch) when the call's spread plan
+ * needs more than MLA_STATIC_WORKSPACE_BYTES (mla_workspace_bytes(...) of
+ * the call), MLA_ERR_CUDA when the set-up fails, otherwise what
+ * mla_decode_partial returns for the same descriptor without a workspace
+ * (so an invalid or unsupported spread gets the same status from both).
+ * With clusters_per_chunk <= 1 it is mla_decode_partial.
  */
 mla_status_t mla_decode_partial_static(const void* q_absorbed, const void* q_pe, const void* ckv_cache,
                                        const void* kpe_cache, const int32_t* block_table,
@@ -309,8 +311,12 @@ mla_status_t mla_merge_states(const float* partials, const float* lse, const int
 /*
  * mla_check_device_errors -- synchronize `stream`, read and clear the device
  * error word the kernels set (bounded-wait timeout, out-of-range page id).
- * *code_out (nullable) receives the raw word. Returns MLA_OK when it was 0,
- * MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_CHECK otherwise.
+ * *code_out (nullable) receives the raw word. When the word was set it also
+ * zeroes the current device's mla_decode_partial_static scratch (if set up),
+ * since a call that stopped early may have left its tickets counted; a
+ * caller-owned workspace must be zeroed again by its owner. Returns MLA_OK
+ * when the word was 0, MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_CHECK otherwise
+ * (MLA_ERR_CUDA if a CUDA call fails).
  */
 mla_status_t mla_check_device_errors(void* stream, uint32_t* code_out);
 

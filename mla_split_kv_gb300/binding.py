@@ -25,7 +25,7 @@ MLA_ERR_CAPACITY = 6
 
 MLA_F16, MLA_BF16, MLA_F32 = 0, 1, 2
 MLA_STATIC_WORKSPACE_BYTES = 4 * 1024 * 1024
-MLA_KERNEL_AUTO, MLA_KERNEL_SIMT, MLA_KERNEL_TC, MLA_KERNEL_TC_QUAD = 0, 1, 2, 3
+MLA_KERNEL_AUTO, MLA_KERNEL_SIMT, MLA_KERNEL_TC = 0, 1, 2
 
 CTR_PARTIAL_SIMT, CTR_PARTIAL_TC, CTR_MERGE, CTR_REJECTED, CTR_CTAS = range(5)
 NUM_COUNTERS = 5

@@ -44,7 +44,7 @@ struct MapKey {
   uint32_t box_rows;
   int dtype;
   int device;
-  int kind;  // 0: the 2D map; 1, 2: page maps of the ckv cache (see page_map); 3, 4: kpe quarter / half maps
+  int kind;  // 0: the 2D map; 1: the page map of the ckv cache (see page_map); 2: the kpe half map
 };
 struct MapEntry {
   MapKey key;
@@ -77,30 +77,13 @@ bool page_map(CUtensorMap* out, const void* base, uint64_t rows, uint32_t box_ro
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   return encode_map(out, MapKey{base, rows, static_cast<uint64_t>(mla::kRank), box_rows, dtype, dev, 1});
 }
-// The same view with boxes of two column blocks, (64, 8, 2, box_rows / 8): the
-// 128 columns of one quarter of a page, row group g and block c landing at
-// 2048 g + 1024 c (the layout of the kernel whose CTAs share tiles in quads).
-bool quarter_page_map(CUtensorMap* out, const void* base, uint64_t rows, uint32_t box_rows, int dtype) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  return encode_map(out, MapKey{base, rows, static_cast<uint64_t>(mla::kRank), box_rows, dtype, dev, 2});
-}
-// 2D map over the [rows, 64] kpe cache with boxes of 16 columns x box_rows rows
-// and the 32-byte swizzle: one quarter of the rope columns of a page, rows of
-// 32 bytes (one K=16 step of a K-major tensor-core operand).
-bool kpe_quarter_map(CUtensorMap* out, const void* base, uint64_t rows, uint32_t box_rows, int dtype) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  return encode_map(out, MapKey{base, rows, static_cast<uint64_t>(mla::kRope), box_rows, dtype, dev, 3});
-}
-
 // 2D map over the [rows, 64] kpe cache with boxes of 32 columns x box_rows rows
 // and the 64-byte swizzle: one half of the rope columns of a page, rows of 64
 // bytes (two K=16 steps of a K-major tensor-core operand).
 bool kpe_half_map(CUtensorMap* out, const void* base, uint64_t rows, uint32_t box_rows, int dtype) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  return encode_map(out, MapKey{base, rows, static_cast<uint64_t>(mla::kRope), box_rows, dtype, dev, 4});
+  return encode_map(out, MapKey{base, rows, static_cast<uint64_t>(mla::kRope), box_rows, dtype, dev, 2});
 }
 
 bool encode_map(CUtensorMap* out, const MapKey& key) {
@@ -124,19 +107,18 @@ bool encode_map(CUtensorMap* out, const MapKey& key) {
     cuuint32_t estr[2] = {1, 1};
     r = enc(&m, dt, 2, const_cast<void*>(key.base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  } else if (key.kind == 3 || key.kind == 4) {
+  } else if (key.kind == 2) {
     cuuint64_t dims[2] = {key.cols, key.rows};
     cuuint64_t strides[1] = {key.cols * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(key.kind == 3 ? mla::kRope / 4 : mla::kRope / 2), key.box_rows};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(mla::kRope / 2), key.box_rows};
     cuuint32_t estr[2] = {1, 1};
     r = enc(&m, dt, 2, const_cast<void*>(key.base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            key.kind == 3 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
     if (key.rows % 8 != 0 || key.box_rows % 8 != 0) return false;
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(mla::kBoxCols), 8, key.cols / mla::kBoxCols, key.rows / 8};
     cuuint64_t strides[3] = {key.cols * 2, mla::kBoxCols * 2, key.cols * 2 * 8};
-    cuuint32_t box[4] = {static_cast<cuuint32_t>(mla::kBoxCols), 8, key.kind == 2 ? 2u : 4u, key.box_rows / 8};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(mla::kBoxCols), 8, 4u, key.box_rows / 8};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     r = enc(&m, dt, 4, const_cast<void*>(key.base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -189,39 +171,75 @@ mla_status_t mla_device_query(int32_t device, mla_device_info_t* info) {
   return st;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Every argument check of mla_decode_partial, in one place, touching no GPU state. With
+// check_workspace false the workspace fields are not looked at (mla_decode_partial_static
+// supplies its own). Returns MLA_OK and the number of chunks, or the status to return.
+mla_status_t check_decode(const void* q_absorbed, const void* q_pe, const void* ckv_cache, const void* kpe_cache,
+                          const int32_t* block_table, const int32_t* context_lens, float scale,
+                          int32_t num_partitions, const float* partials, const float* lse, const mla_decode_desc_t* d,
+                          bool check_workspace, int64_t* n_chunks) {
+  if (d == nullptr || q_absorbed == nullptr || q_pe == nullptr || ckv_cache == nullptr || kpe_cache == nullptr ||
+      block_table == nullptr || context_lens == nullptr || partials == nullptr || lse == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (d->num_requests < 1 || d->num_blocks < 1 || d->max_blocks_per_req < 1) return MLA_ERR_INVALID_ARG;
+  if (!valid_heads(d->num_heads) || d->q_len < 1 || d->q_len > MLA_MAX_Q_LEN) return MLA_ERR_UNSUPPORTED;
+  if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64) return MLA_ERR_UNSUPPORTED;
+  if (d->dtype != MLA_F16 && d->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (d->causal != 0 && d->causal != 1) return MLA_ERR_INVALID_ARG;
+  if (d->tables_ready != 0 && d->tables_ready != 1) return MLA_ERR_INVALID_ARG;
+  if (d->kernel < MLA_KERNEL_AUTO || d->kernel > MLA_KERNEL_TC) return MLA_ERR_INVALID_ARG;
+  const int32_t C0 = d->cluster_ctas;
+  if (C0 != 0 && C0 != 1 && C0 != 2 && C0 != 4 && C0 != 8 && C0 != 16) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return MLA_ERR_INVALID_ARG;
+  if (d->clusters_per_chunk < 0 || d->clusters_per_chunk > 16) return MLA_ERR_INVALID_ARG;
+  int64_t N;
+  if (d->chunks == nullptr) {
+    if (num_partitions < 1 || num_partitions > 1024) return MLA_ERR_INVALID_ARG;
+    N = static_cast<int64_t>(d->num_requests) * num_partitions;
+  } else {
+    if (d->num_chunks < 1 || !aligned(d->chunks, 16)) return MLA_ERR_INVALID_ARG;
+    N = d->num_chunks;
+  }
+  if (N > 65535) return MLA_ERR_UNSUPPORTED;
+  if (!aligned(q_absorbed, 16) || !aligned(q_pe, 16) || !aligned(ckv_cache, 16) || !aligned(kpe_cache, 16) ||
+      !aligned(partials, 16) || !aligned(lse, 4) || !aligned(block_table, 4) || !aligned(context_lens, 4))
+    return MLA_ERR_INVALID_ARG;
+  const uint64_t rows = static_cast<uint64_t>(d->num_blocks) * static_cast<uint64_t>(d->block_size);
+  if (rows > 0x7fffffffull) return MLA_ERR_UNSUPPORTED;
+  const int32_t subs = (d->clusters_per_chunk > 1) ? d->clusters_per_chunk : 1;
+  if (subs > 1) {  // a partition spread over several clusters: the paired kernel with a workspace
+    if (C0 == 0) return MLA_ERR_INVALID_ARG;  // the cluster size is part of that plan
+    if (d->kernel == MLA_KERNEL_SIMT || !mla::tc128_supports(d->num_heads * d->q_len, d->dtype == MLA_BF16, C0))
+      return MLA_ERR_UNSUPPORTED;
+    if (check_workspace) {
+      const uint64_t need = mla_workspace_bytes(static_cast<int32_t>(N), subs, C0, d->q_len, d->num_heads);
+      if (d->workspace == nullptr || !aligned(d->workspace, 16) || d->workspace_bytes < need)
+        return MLA_ERR_INVALID_ARG;
+    }
+    if (N * subs > 65535) return MLA_ERR_UNSUPPORTED;
+  }
+  *n_chunks = N;
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const void* ckv_cache,
                                 const void* kpe_cache, const int32_t* block_table, const int32_t* context_lens,
                                 float scale, int32_t num_partitions, float* partials, float* lse,
                                 const mla_decode_desc_t* d) {
-  if (d == nullptr || q_absorbed == nullptr || q_pe == nullptr || ckv_cache == nullptr || kpe_cache == nullptr ||
-      block_table == nullptr || context_lens == nullptr || partials == nullptr || lse == nullptr)
-    return reject(MLA_ERR_INVALID_ARG);
-  if (d->num_requests < 1 || d->num_blocks < 1 || d->max_blocks_per_req < 1) return reject(MLA_ERR_INVALID_ARG);
-  if (!valid_heads(d->num_heads) || d->q_len < 1 || d->q_len > MLA_MAX_Q_LEN) return reject(MLA_ERR_UNSUPPORTED);
-  if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64) return reject(MLA_ERR_UNSUPPORTED);
-  if (d->dtype != MLA_F16 && d->dtype != MLA_BF16) return reject(MLA_ERR_UNSUPPORTED);
-  if (d->causal != 0 && d->causal != 1) return reject(MLA_ERR_INVALID_ARG);
-  if (d->tables_ready != 0 && d->tables_ready != 1) return reject(MLA_ERR_INVALID_ARG);
-  if (d->kernel < MLA_KERNEL_AUTO || d->kernel > MLA_KERNEL_TC_QUAD) return reject(MLA_ERR_INVALID_ARG);
+  int64_t N = 0;
+  const mla_status_t chk = check_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
+                                        num_partitions, partials, lse, d, true, &N);
+  if (chk != MLA_OK) return reject(chk);
   const int32_t C0 = d->cluster_ctas;
-  if (C0 != 0 && C0 != 1 && C0 != 2 && C0 != 4 && C0 != 8 && C0 != 16) return reject(MLA_ERR_INVALID_ARG);
-  if (!std::isfinite(scale)) return reject(MLA_ERR_INVALID_ARG);
-  if (d->clusters_per_chunk < 0 || d->clusters_per_chunk > 16) return reject(MLA_ERR_INVALID_ARG);
-  int64_t N;
-  if (d->chunks == nullptr) {
-    if (num_partitions < 1 || num_partitions > 1024) return reject(MLA_ERR_INVALID_ARG);
-    N = static_cast<int64_t>(d->num_requests) * num_partitions;
-  } else {
-    if (d->num_chunks < 1 || !aligned(d->chunks, 16)) return reject(MLA_ERR_INVALID_ARG);
-    N = d->num_chunks;
-  }
-  if (N > 65535) return reject(MLA_ERR_UNSUPPORTED);
-  if (!aligned(q_absorbed, 16) || !aligned(q_pe, 16) || !aligned(ckv_cache, 16) || !aligned(kpe_cache, 16) ||
-      !aligned(partials, 16) || !aligned(lse, 4) || !aligned(block_table, 4) || !aligned(context_lens, 4))
-    return reject(MLA_ERR_INVALID_ARG);
   const uint64_t rows = static_cast<uint64_t>(d->num_blocks) * static_cast<uint64_t>(d->block_size);
-  if (rows > 0x7fffffffull) return reject(MLA_ERR_UNSUPPORTED);
-
   const bool use_simt = (d->kernel == MLA_KERNEL_SIMT);
   const bool bf16 = (d->dtype == MLA_BF16);
   const int rows_total = d->num_heads * d->q_len;
@@ -230,27 +248,13 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   const int nr = use_simt ? mla::simt_rows_per_cta() : (mh ? rows_total : mla::tc_rows_per_cta(rows_total, bf16));
   const int64_t groups = (rows_total + nr - 1) / nr;
   const int32_t subs = (d->clusters_per_chunk > 1) ? d->clusters_per_chunk : 1;
-  if (subs > 1) {  // a partition spread over several clusters: the pair or quad kernel with a workspace
-    if (C0 == 0) return reject(MLA_ERR_INVALID_ARG);  // the cluster size is part of that plan
-    if (use_simt || !mla::tc128_supports(rows_total, bf16, C0)) return reject(MLA_ERR_UNSUPPORTED);
-    const uint64_t need = mla_workspace_bytes(static_cast<int32_t>(N), subs, C0, d->q_len, d->num_heads);
-    if (d->workspace == nullptr || !aligned(d->workspace, 16) || d->workspace_bytes < need)
-      return reject(MLA_ERR_INVALID_ARG);
-    if (N * subs > 65535) return reject(MLA_ERR_UNSUPPORTED);
-  }
   const int C = C0 ? C0 : (mh ? 2 : default_cluster(N * groups));
-  // 16 rows or fewer in fp16 with clusters of 4..16: CTAs share tiles in quads when asked for
-  const bool quad = d->kernel == MLA_KERNEL_TC_QUAD && mla::quad_supports(rows_total, bf16, C);
 
   CUtensorMap tm_ckv, tm_kpe, tm_pages, tm_kpe_half;
-  if (quad) {
-    if (!quarter_page_map(&tm_pages, ckv_cache, rows, d->block_size, d->dtype) ||
-        !kpe_quarter_map(&tm_kpe, kpe_cache, rows, d->block_size, d->dtype))
-      return reject(MLA_ERR_CUDA);
-  } else if (!tensor_map(&tm_ckv, ckv_cache, rows, mla::kRank, d->block_size, d->dtype) ||
-             !tensor_map(&tm_kpe, kpe_cache, rows, mla::kRope, d->block_size, d->dtype) ||
-             !page_map(&tm_pages, ckv_cache, rows, d->block_size, d->dtype) ||
-             !kpe_half_map(&tm_kpe_half, kpe_cache, rows, d->block_size, d->dtype)) {
+  if (!tensor_map(&tm_ckv, ckv_cache, rows, mla::kRank, d->block_size, d->dtype) ||
+      !tensor_map(&tm_kpe, kpe_cache, rows, mla::kRope, d->block_size, d->dtype) ||
+      !page_map(&tm_pages, ckv_cache, rows, d->block_size, d->dtype) ||
+      !kpe_half_map(&tm_kpe_half, kpe_cache, rows, d->block_size, d->dtype)) {
     return reject(MLA_ERR_CUDA);
   }
 
@@ -282,9 +286,8 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   p.ws_tickets = nullptr;
   if (subs > 1) {
     uint8_t* ws = static_cast<uint8_t*>(d->workspace);
-    // tickets (two per chunk), then per chunk its entries: pairs = subs * cluster_ctas / 2 (the
-    // paired kernel: one entry per CTA pair; the quad kernel uses the first subs of them as its
-    // sub-partial slots), [rows][512] fp32 each, then per entry two [rows][2] fp32 copies
+    // tickets (two per chunk), then per chunk its entries, one per CTA pair (subs * cluster_ctas / 2),
+    // [rows][512] fp32 each, then per entry two [rows][2] fp32 copies
     const uint64_t tickets = (static_cast<uint64_t>(N) * 2 * 4 + 255) / 256 * 256;
     const uint64_t entries = static_cast<uint64_t>(N) * subs * static_cast<uint64_t>(C0 / 2);
     p.ws_tickets = reinterpret_cast<uint32_t*>(ws);
@@ -294,7 +297,6 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   cudaStream_t stream = static_cast<cudaStream_t>(d->stream);
   const cudaError_t e =
       use_simt ? mla::launch_partial_simt(tm_ckv, tm_kpe, p, static_cast<int>(N), C, bf16, stream)
-      : quad   ? mla::launch_partial_quad(tm_pages, tm_kpe, p, static_cast<int>(N), C, stream)
                : mla::launch_partial_tc(tm_ckv, tm_kpe, tm_pages, tm_kpe_half, p, static_cast<int>(N), C, bf16, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -311,8 +313,10 @@ namespace {
 
 // Scratch of mla_decode_partial_static: one statically sized array per device
 // (the module is loaded on each device that uses it). Its address is looked up
-// once per device; it is cleared then, since the chunk tickets must start at
-// zero (every call leaves them at zero again).
+// once per device and process; it is cleared then, since the chunk tickets
+// must start at zero (every call that completes leaves them at zero again),
+// and again by mla_check_device_errors when it finds the error word set (an
+// aborted call may leave tickets counted).
 static __device__ __align__(256) uint8_t g_static_workspace[MLA_STATIC_WORKSPACE_BYTES];
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
@@ -342,6 +346,17 @@ mla_status_t static_workspace(void** out) {
   return MLA_OK;
 }
 
+// Zero the current device's static scratch if it has been set up (after a
+// device error, when a call may have stopped with tickets counted).
+bool clear_static_workspace() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_addr[dev] == nullptr) return true;
+  return cudaMemset(g_static_addr[dev], 0, MLA_STATIC_WORKSPACE_BYTES) == cudaSuccess &&
+         cudaDeviceSynchronize() == cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -350,17 +365,17 @@ mla_status_t mla_decode_partial_static(const void* q_absorbed, const void* q_pe,
                                        const void* kpe_cache, const int32_t* block_table,
                                        const int32_t* context_lens, float scale, int32_t num_partitions,
                                        float* partials, float* lse, const mla_decode_desc_t* d) {
-  if (d == nullptr) return reject(MLA_ERR_INVALID_ARG);
+  int64_t N = 0;
+  const mla_status_t chk = check_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
+                                        num_partitions, partials, lse, d, false, &N);
+  if (chk != MLA_OK) return reject(chk);
   mla_decode_desc_t dd = *d;
   dd.workspace = nullptr;
   dd.workspace_bytes = 0;
-  if (dd.clusters_per_chunk > 1) {
-    const int64_t N = (dd.chunks == nullptr) ? static_cast<int64_t>(dd.num_requests) * num_partitions
-                                             : static_cast<int64_t>(dd.num_chunks);
-    if (N < 1 || N > 65535) return reject(MLA_ERR_INVALID_ARG);
+  if (dd.clusters_per_chunk > 1) {  // a valid spread plan: the library's scratch stands in for the workspace
     const uint64_t need =
         mla_workspace_bytes(static_cast<int32_t>(N), dd.clusters_per_chunk, dd.cluster_ctas, dd.q_len, dd.num_heads);
-    if (need == 0 || need > MLA_STATIC_WORKSPACE_BYTES) return reject(MLA_ERR_CAPACITY);
+    if (need > MLA_STATIC_WORKSPACE_BYTES) return reject(MLA_ERR_CAPACITY);
     void* ws = nullptr;
     const mla_status_t st = static_workspace(&ws);
     if (st != MLA_OK) return st;
@@ -408,13 +423,13 @@ mla_status_t mla_merge_states(const float* partials, const float* lse, const int
 
 mla_status_t mla_check_device_errors(void* stream, uint32_t* code_out) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
-  uint32_t a = 0, b = 0, c = 0, e = 0, f = 0;
+  uint32_t a = 0, b = 0, c = 0, e = 0;
   if (mla::simt_read_clear_error(&a) != cudaSuccess || mla::tc_read_clear_error(&b) != cudaSuccess ||
-      mla::tc128_read_clear_error(&c) != cudaSuccess || mla::mh_read_clear_error(&e) != cudaSuccess ||
-      mla::quad_read_clear_error(&f) != cudaSuccess)
+      mla::tc128_read_clear_error(&c) != cudaSuccess || mla::mh_read_clear_error(&e) != cudaSuccess)
     return MLA_ERR_CUDA;
-  const uint32_t code = a | b | c | e | f;
+  const uint32_t code = a | b | c | e;
   if (code_out != nullptr) *code_out = code;
+  if (code != 0 && !clear_static_workspace()) return MLA_ERR_CUDA;
   if (code & mla::MLA_DEVERR_TIMEOUT) return MLA_ERR_TIMEOUT;
   if (code != 0) return MLA_ERR_DEVICE_CHECK;
   return MLA_OK;

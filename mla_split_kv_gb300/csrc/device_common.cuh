@@ -75,13 +75,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // CTA that gave up leaves (they always complete; this only bounds the wait).
 constexpr uint64_t kDrainTimeoutNs = 2000000000ull;
 
+// Suspend-time hint of the waits: at most 1 ms, and no longer than the
+// wait's own limit, so a short limit is checked about that often.
+__device__ __forceinline__ uint32_t wait_hint_ns(uint64_t timeout_ns) {
+  return timeout_ns < 1000000ull ? static_cast<uint32_t>(timeout_ns) : 1000000u;
+}
+
 // Wait for the phase with the given parity to complete. Gives up after
 // `timeout_ns` of wall time, flags MLA_DEVERR_TIMEOUT and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
-  if (__builtin_expect(mbar_try_wait(bar, parity), 1)) return true;
+  const uint32_t hint = wait_hint_ns(timeout_ns);
+  if (__builtin_expect(mbar_try_wait(bar, parity, hint), 1)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, hint)) return true;
     if (globaltimer_ns() - t0 > timeout_ns) {
       flag_error(MLA_DEVERR_TIMEOUT);
       return false;
@@ -205,6 +212,18 @@ __device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr) {
   return v;
 }
 
+// Plain 32-bit store to another CTA's shared memory (address from dsmem_addr);
+// ordered before a following cluster barrier's release.
+__device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// After an abort: spin for `ns` nanoseconds, so that copies and remote stores
+// already issued between the CTAs of a cluster complete before a CTA exits.
+__device__ __forceinline__ void settle_in_flight(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) {
+  }
+}
 // Asynchronous 16-byte store to another CTA's shared memory; its bytes count
 // as completed transactions on that CTA's mbarrier `remote_bar` (both
 // addresses from dsmem_addr). The sender does not wait for it.
@@ -240,13 +259,14 @@ __device__ __forceinline__ void mbar_remote_arrive_relaxed(uint32_t addr) {
 // Bounded wait on a local mbarrier whose arrivals come from other CTAs of the
 // cluster: acquire at cluster scope, so their stores before the arrive are visible.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint32_t hint = wait_hint_ns(timeout_ns);
   auto test = [&]() -> bool {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint)
         : "memory");
     return ok != 0;
   };
@@ -393,21 +413,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t start, uint32_t lbo
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;  // SWIZZLE_128B
-  return d;
-}
-
-// The same for a K-major operand whose rows are 32 bytes (one K=16 step of
-// 16-bit elements) stored with the 32-byte swizzle (the 16-byte half of each
-// row is swapped on rows 4-7 of every 8-row group, as a TMA box with
-// CU_TENSOR_MAP_SWIZZLE_32B lands): sbo = stride between 8-row groups (256 B
-// when the rows are packed).
-__device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t start, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((start >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>(1) << 16;  // leading byte offset: unused within one swizzle atom
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(6) << 61;  // SWIZZLE_32B
   return d;
 }
 
@@ -625,101 +630,6 @@ __device__ __forceinline__ void cluster_combine_to(const PartialParams& p, const
 __device__ __forceinline__ void cluster_combine(const PartialParams& p, const CtaWork& w, const float* ostage,
                                                 const float* mst, const float* lst, int tid, int nthreads) {
   cluster_combine_to(p, w, ostage, mst, lst, tid, nthreads, p.partials, p.lse, static_cast<long long>(w.slot));
-}
-
-// A chunk spread over `subs` clusters (grid.y = chunk * subs + sub): each
-// cluster has written its sub-partial (normalized, with its log2 LSE) to slot
-// chunk * subs + sub of the workspace. Every CTA of the cluster calls this
-// after writing its share. The cluster that takes the chunk's last ticket
-// merges the chunk's sub-partials, in sub order (so the result does not depend
-// on which cluster finished last), into the chunk's slot of the partials, and
-// resets the ticket for the next call. CTA `rank` of the cluster merges columns
-// [rank * 512 / C, (rank + 1) * 512 / C), rank 0 also the LSE.
-__device__ __forceinline__ void merge_sub_partials(const PartialParams& p, const CtaWork& w, int chunk, int subs,
-                                                   int32_t* last_flag, int tid, int nthreads) {
-  const int rows_total = p.q_len * p.H;
-  const uint32_t rank = cluster_ctarank(), nranks = cluster_nctarank();
-  __threadfence();  // this thread's share of the sub-partial, visible before the ticket
-  cluster_sync();
-  if (rank == 0 && tid == 0) {
-    const uint32_t t = atomicAdd(p.ws_tickets + chunk, 1u);
-    const int last = (t == static_cast<uint32_t>(subs - 1)) ? 1 : 0;
-    if (last) atomicExch(p.ws_tickets + chunk, 0u);
-    *last_flag = last;
-  }
-  cluster_sync();
-  if (dsmem_ld_u32(dsmem_addr(last_flag, 0)) == 0) return;
-  __threadfence();
-  const int dcols = kRank / static_cast<int>(nranks);
-  const int dbeg = static_cast<int>(rank) * dcols;
-  const int n8 = dcols / 8;
-  const int items = w.nrows * n8 + ((rank == 0) ? w.nrows : 0);
-  const long long sub0 = static_cast<long long>(chunk) * subs;
-  // item = 8 columns of a row (or a row's LSE): one round of loads for up to 8 sub-partials (every
-  // CTA of the cluster has about one item per thread), then the fixed-order reduction
-  for (int idx = tid; idx < items; idx += nthreads) {
-    const bool is_lse = idx >= w.nrows * n8;
-    const int r = is_lse ? idx - w.nrows * n8 : idx / n8;
-    const int d = is_lse ? 0 : dbeg + (idx % n8) * 8;
-    float lj[16];
-    float4 va[8], vb[8];
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      lj[j] = (j < subs) ? __ldcg(p.ws_lse + (sub0 + j) * rows_total + w.row0 + r) : -INFINITY;
-    auto load8 = [&](int j0) {
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        va[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
-        vb[jj] = va[jj];
-        if (j0 + jj < subs && !is_lse) {
-          const float* src = p.ws_partials + ((sub0 + j0 + jj) * rows_total + w.row0 + r) * kRank + d;
-          va[jj] = __ldcg(reinterpret_cast<const float4*>(src));
-          vb[jj] = __ldcg(reinterpret_cast<const float4*>(src + 4));
-        }
-      }
-    };
-    load8(0);
-    float M = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) M = fmaxf(M, lj[j]);
-    float den = 0.f;
-    float4 num0 = make_float4(0.f, 0.f, 0.f, 0.f), num1 = num0;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int j0 = 0; j0 < 16; j0 += 8) {
-        if (j0 >= subs) break;
-        if (j0 > 0) load8(j0);
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const int j = j0 + jj;
-          if (j < subs) {
-            const float wj = (lj[j] == -INFINITY) ? 0.f : exp2f(lj[j] - M);
-            den += wj;
-            num0.x = fmaf(wj, va[jj].x, num0.x);
-            num0.y = fmaf(wj, va[jj].y, num0.y);
-            num0.z = fmaf(wj, va[jj].z, num0.z);
-            num0.w = fmaf(wj, va[jj].w, num0.w);
-            num1.x = fmaf(wj, vb[jj].x, num1.x);
-            num1.y = fmaf(wj, vb[jj].y, num1.y);
-            num1.z = fmaf(wj, vb[jj].z, num1.z);
-            num1.w = fmaf(wj, vb[jj].w, num1.w);
-          }
-        }
-      }
-    }
-    if (is_lse) {
-      p.lse[static_cast<long long>(w.slot) * rows_total + w.row0 + r] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
-    } else {
-      float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0;
-      if (M != -INFINITY) {
-        o0 = make_float4(num0.x / den, num0.y / den, num0.z / den, num0.w / den);
-        o1 = make_float4(num1.x / den, num1.y / den, num1.z / den, num1.w / den);
-      }
-      float* dst = p.partials + (static_cast<long long>(w.slot) * rows_total + w.row0 + r) * kRank + d;
-      *reinterpret_cast<float4*>(dst) = o0;
-      *reinterpret_cast<float4*>(dst + 4) = o1;
-    }
-  }
 }
 
 }  // namespace mla

@@ -36,12 +36,10 @@ struct PartialParams {
   int32_t causal;
   int32_t tables_ready;        // chunks / context_lens / block_table may be read before the dependency wait
   uint64_t timeout_ns;
-  // a chunk spread over `subs` clusters (16-row kernels whose CTAs share tiles): grid.y =
-  // chunks * subs. Paired kernel: one entry per CTA pair of a chunk (subs * cluster / 2
-  // of them), its unnormalized O^T in ws_partials and its row maxima / sums in ws_lse,
-  // two tickets per chunk (one per column half). Quad kernel: the sub-partial of
-  // cluster grid.y in entry slot grid.y, its LSE rows at ws_lse + grid.y * rows, one
-  // ticket per chunk. Tickets are zero between calls.
+  // a chunk spread over `subs` clusters (the paired 16-row kernel): grid.y = chunks * subs.
+  // One entry per CTA pair of a chunk (subs * cluster / 2 of them): its unnormalized O^T in
+  // ws_partials and its row maxima / sums in ws_lse; two tickets per chunk (one per column
+  // half). Tickets are zero between calls.
   int32_t subs;
   float* ws_partials;          // [entries, q_len, H, 512]
   float* ws_lse;               // [entries, 2, q_len, H, 2]
@@ -75,14 +73,6 @@ bool tc128_supports(int total_rows, bool bf16, int cluster);
 cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe_half, const PartialParams& p,
                                  int num_chunks, int cluster, cudaStream_t stream);
 int tc128_max_active_clusters(int cluster);
-// The same tiles shared by CTA quads (score product split by columns, PV by
-// tokens): q_len*H <= 16, fp16, clusters of 4, 8 or 16 CTAs. tm_pages: the
-// ckv page map with two-column-block boxes; tm_kpe: 16-column kpe boxes with
-// the 32-byte swizzle.
-bool quad_supports(int total_rows, bool bf16, int cluster);
-cudaError_t launch_partial_quad(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe, const PartialParams& p,
-                                int num_chunks, int cluster, cudaStream_t stream);
-int quad_max_active_clusters(int cluster);
 // 64-token-tile tensor-core kernel for 128 rows (q_len * H == 128), fp16 or bf16,
 // on clusters of one CTA pair that split the latent columns.
 bool mh_supports(int total_rows, int cluster);
@@ -98,7 +88,6 @@ int tc_max_active_clusters(int cluster, int rows_per_cta, bool bf16);
 cudaError_t simt_read_clear_error(uint32_t* out);
 cudaError_t tc_read_clear_error(uint32_t* out);
 cudaError_t tc128_read_clear_error(uint32_t* out);
-cudaError_t quad_read_clear_error(uint32_t* out);
 cudaError_t mh_read_clear_error(uint32_t* out);
 
 }  // namespace mla

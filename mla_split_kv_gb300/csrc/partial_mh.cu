@@ -80,6 +80,7 @@ struct Small {
   uint64_t full[2], empty[2], sfull[2], sfree[2], ppfull[2], pvdone[2], xfull, xempty, drain;
   uint32_t tmem_base;
   int32_t abort_flag;
+  int32_t peer_abort;        // set by the peer CTA (remote store) when it gave up
   float half_val[2][kRows];  // per row, the two token halves' tile maximum (then their sums)
 };
 static_assert(sizeof(Small) <= 2048, "small smem region");
@@ -131,6 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm->drain, 1);
     mbar_arrive_expect_tx(&sm->xfull, kXBytes);  // tile 0
     sm->abort_flag = 0;
+    sm->peer_abort = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -213,7 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (lane == 0 && *abort_flag && issued >= 0) mbar_wait(&sm->full[issued & 1], (issued >> 1) & 1, kDrainTimeoutNs);
+    // after an abort, let this warp's loads still in flight (the last two tiles it issued) land before
+    // shared memory is released
+    if (lane == 0 && *abort_flag)
+      for (int t = max(0, issued - 1); t <= issued; ++t) mbar_wait(&sm->full[t & 1], (t >> 1) & 1, kDrainTimeoutNs);
     cluster_wait_acquire();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
@@ -550,7 +555,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // a CTA that gave up tells its peer before the last cluster barrier: the bulk copies of partial
+  // scores that either CTA issued may then still be in flight (reading the sender's shared memory,
+  // writing the receiver's), so after an abort on either side both stay until they have landed
+  if (tid == 0 && *abort_flag) dsmem_st_u32(dsmem_addr(&sm->peer_abort, peer), 1u);
   cluster_sync();  // the peer is done with this CTA's shared memory
+  if (*abort_flag || *reinterpret_cast<volatile int32_t*>(&sm->peer_abort)) settle_in_flight(20000ull);
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

@@ -229,9 +229,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       issued = i;
     }
-    // after an abort, let this warp's last loads land before shared memory is released
-    if (lane == 0 && *abort_flag && issued >= 0)
-      mbar_wait(&sm->full[issued % kSlots], (issued / kSlots) & 1, kDrainTimeoutNs);
+    // after an abort, let this warp's loads still in flight (the last three tiles it issued, one per
+    // slot) land before shared memory is released
+    if (lane == 0 && *abort_flag)
+      for (int t = max(0, issued - (kSlots - 1)); t <= issued; ++t)
+        mbar_wait(&sm->full[t % kSlots], (t / kSlots) & 1, kDrainTimeoutNs);
     cluster_wait_acquire();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
@@ -342,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (now - idle_t0 > tmo) {
             act = -1;
             *abort_flag = 1;
+            flag_error(MLA_DEVERR_TIMEOUT);
           }
         }
         if (act > 0) idle = false;
@@ -710,12 +713,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     cluster_wait_acquire();
-    if (!have && ntiles > 0) {
-      // after an abort: stores the peer issued before it left the tile loop may still be in flight
-      const uint64_t t0 = globaltimer_ns();
-      while (globaltimer_ns() - t0 < 20000ull) {
-      }
-    }
+    // after an abort: stores the peer issued before it left the tile loop may still be in flight
+    if (!have && ntiles > 0) settle_in_flight(20000ull);
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
@@ -751,13 +750,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();
-  if (!have && ntiles > 0) {
-    // after an abort: the remote stores the peer issued before it reached this barrier (it issues
-    // none after it) may still be in flight; give them time to land before this CTA can leave
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 20000ull) {
-    }
-  }
+  // after an abort: the remote stores the peer issued before it reached this barrier (it issues
+  // none after it) may still be in flight; give them time to land before this CTA can leave
+  if (!have && ntiles > 0) settle_in_flight(20000ull);
   // the cluster's result goes to the chunk's slot
   float* const dst_partials = p.partials;
   float* const dst_lse = p.lse;

@@ -345,3 +345,41 @@ def test_descriptor_keeps_its_tensors_alive():
     del desc
     gc.collect()
     assert all(r() is None for r in refs)
+
+
+def call_static(lib, d, P=2, ptrs=None):
+    p = [FAKE] * 8 if ptrs is None else ptrs
+    return lib.mla_decode_partial_static(p[0], p[1], p[2], p[3], p[4], p[5], ctypes.c_float(0.07), P, p[6], p[7],
+                                         ctypes.byref(d))
+
+
+@pytest.mark.parametrize("kw,P", [
+    (dict(clusters_per_chunk=4, cluster_ctas=0), 2),
+    (dict(clusters_per_chunk=4, cluster_ctas=1), 2),
+    (dict(clusters_per_chunk=4, cluster_ctas=2, dtype=nb.MLA_BF16), 2),
+    (dict(clusters_per_chunk=4, cluster_ctas=2, num_heads=64), 2),
+    (dict(clusters_per_chunk=4, cluster_ctas=2, kernel=nb.MLA_KERNEL_SIMT), 2),
+    (dict(clusters_per_chunk=17, cluster_ctas=2), 2),
+    (dict(clusters_per_chunk=4, cluster_ctas=2, num_requests=40000), 2),
+    (dict(clusters_per_chunk=4, cluster_ctas=2, num_heads=32), 2),
+    (dict(clusters_per_chunk=4, cluster_ctas=2), 0),
+])
+def test_static_entry_gives_the_plain_entrys_status_before_any_device_work(lib, kw, P):
+    """The allocation-free variant validates the whole descriptor (all but the workspace, which it supplies)
+    before its device set-up, so a bad descriptor gets the same status as from mla_decode_partial given a
+    workspace, and nothing runs on a device (this machine may have none)."""
+    d = desc(**kw)
+    nb.mla_reset_counters()
+    got = call_static(lib, d, P)
+    plain = call_partial(lib, desc(workspace=FAKE, workspace_bytes=BIG, **kw), P)
+    assert got == plain and got in (nb.MLA_ERR_INVALID_ARG, nb.MLA_ERR_UNSUPPORTED)
+    ctr = nb.mla_get_counters()
+    assert ctr[nb.CTR_REJECTED] == 2 and ctr[nb.CTR_PARTIAL_TC] == 0
+
+
+def test_static_entry_rejects_a_plan_beyond_its_scratch_before_any_device_work(lib):
+    d = desc(clusters_per_chunk=16, cluster_ctas=2, num_requests=64, max_blocks_per_req=8)
+    assert nb.mla_workspace_bytes(64, 16, 2, 1, 16) > nb.MLA_STATIC_WORKSPACE_BYTES
+    nb.mla_reset_counters()
+    assert call_static(lib, d, 1) == nb.MLA_ERR_CAPACITY
+    assert nb.mla_get_counters()[nb.CTR_REJECTED] == 1

@@ -70,3 +70,50 @@ def test_two_cpu_ranks_max_time_identical_plans_reference_on_rank0():
         assert us == pytest.approx(15.0 * 1e3 / (6 * 20 * 2))
         assert same_plans
     assert out[1][3] is None                           # non-zero ranks of the reference arm do nothing
+
+
+PROBE = """
+import json, os, sys
+sys.path.insert(0, {root!r})
+import bench
+rank, world, local = bench.init_ranks()
+job_ms = bench.max_over_ranks(10.0 + 5.0 * rank, "cpu")
+if rank == 0:
+    print(json.dumps({{"n_gpus": world, "job_ms": job_ms, "local_ranks": local,
+                      "backend": __import__("torch").distributed.get_backend()}}))
+bench.finish_ranks(world)
+"""
+
+
+def test_launcher_starts_one_rank_per_gpu_on_cpu_ranks(tmp_path):
+    """bench.py --gpus N with no launcher around it starts N ranks through torch's launcher (rendezvous on
+    127.0.0.1); each binds to its LOCAL_RANK and joins the group (gloo here, no GPU), and rank 0 sees the
+    slowest rank's time. The same launch and rank set-up serve the benchmark."""
+    import json
+    import subprocess
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+
+    probe = tmp_path / "probe.py"
+    probe.write_text(PROBE.format(root=ROOT))
+    res = bench.launch_replicas(2, [], script=str(probe), stdout=subprocess.PIPE)
+    assert res.returncode == 0
+    line = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(line) == 1, res.stdout
+    got = json.loads(line[0])
+    assert got["n_gpus"] == 2 and got["job_ms"] == 15.0 and got["local_ranks"] == 0 and got["backend"] == "gloo"
+    cmd = bench.replica_command(4, "bench.py", ["--gpus", "4"], 29500)
+    assert "--nproc-per-node=4" in cmd and "--master-addr=127.0.0.1" in cmd and cmd[-2:] == ["--gpus", "4"]
+
+
+def test_bench_refuses_a_gpu_count_that_differs_from_the_launcher(monkeypatch):
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--gpus", "4"])
+    with pytest.raises(SystemExit) as e:
+        bench.main()
+    assert "does not match" in str(e.value)

@@ -71,3 +71,32 @@ def test_static_entry_rejects_plans_beyond_its_scratch():
     assert e.value.status == nb.MLA_ERR_CAPACITY
     ctr = nb.mla_get_counters()
     assert ctr[nb.CTR_REJECTED] == 1 and ctr[nb.CTR_PARTIAL_TC] == 0
+
+
+def test_static_entry_is_usable_again_after_a_device_error():
+    """A static call cut short by its bounded waits (a limit of a few microseconds) is reported by
+    mla_check_device_errors, which then clears the library's scratch; the next two calls match the
+    workspace entry point bit for bit."""
+    L, P, C, k = 65536, 6, 4, 6
+    case = gen.make_decode_case(7, [L], num_heads=16, block_size=32, dtype="f16")
+    dc = rt.upload(case)
+    ref_part, ref_lse = rt.alloc_partials(P, 1, 16)
+    ws = rt.alloc_workspace(P, k, C, 1, 16)
+    rt.decode_partial(dc, ref_part, ref_lse, num_partitions=P, kernel=nb.MLA_KERNEL_TC, cluster=C, subs=k,
+                      workspace=ws)
+    desc = rt.make_desc(dc, None, nb.MLA_KERNEL_TC, C, None, k, None)
+    part, lse = rt.alloc_partials(P, 1, 16)
+    nb.mla_check_device_errors(None)
+    try:
+        nb.mla_set_wait_timeout_ns(2_000)
+        call_static(dc, part, lse, desc, P)
+        st, code = nb.mla_check_device_errors(None)
+    finally:
+        nb.mla_set_wait_timeout_ns(2_000_000_000)
+    assert st == nb.MLA_ERR_TIMEOUT and code & 1, (st, code)
+    for _ in range(2):
+        part.fill_(float("nan"))
+        call_static(dc, part, lse, desc, P)
+        torch.cuda.synchronize()
+        assert torch.equal(part, ref_part)
+        assert torch.equal(lse, ref_lse)
