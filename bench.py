@@ -3,21 +3,24 @@
 Workload: B=1, H=16, kv_lora_rank 512, rope 64, fp16, block 32, contexts
 32768 / 49152 / 65536 / 81920 / 98304 / 131072 tokens (N(0,1) latents, random
 block permutation), partitions chosen by the planner. One step = one layer
-call (partial kernel + merge kernel) at each of the six contexts; the six
-caches live in disjoint memory (528 MB together, > L2), so every call streams
-its latent from HBM.
+call at each of the six contexts through mla_decode (with the paired kernel a
+single launch: the partial kernel merges each request's partials itself); the
+six caches live in disjoint memory (528 MB together, > L2), so every call
+streams its latent from HBM.
 
 Printed: one JSON line. `value` = mean microseconds per layer call over the
 sweep (device time, inputs resident, each step replayed from one CUDA graph);
-`e2e` = the same through the C-ABI calls with host buffers (queries, block
-tables and plan of the six calls copied in with one copy from one pinned
-buffer, the six outputs copied out with one copy, every step); `roofline` = the
-partial kernel's algorithmic HBM bytes / its CUDA-event time against the
-measured copy bandwidth; `cpu_baseline` = the f64 oracle on the host cores.
-Outside the timed region: `per_ctx` (each context alone, its planned split, a
-single cold call after an L2 flush and the host planner's time per call) and
-`trials` (median / min / max over five more K-step trials).
-`--impl reference` times the oracle itself on the same workload.
+`e2e` = the same through mla_decode with host buffers (queries, block tables
+and plan of the six calls copied in with one copy from one pinned buffer, the
+six outputs copied out with one copy, every step); `roofline` = the kernel's
+algorithmic HBM bytes / its CUDA-event time against the measured copy
+bandwidth; `cpu_baseline` = the f64 oracle on the host cores. Outside the
+timed region: `two_launch_us` (the same step as partial kernel + merge
+kernel), `per_ctx` (each context alone, its planned split, a single cold call
+after an L2 flush and the host planner's time per call), `trials` (median /
+min / max over five more K-step trials) and `many_heads` (the many-head
+workload). `--impl reference` times the oracle itself on the same workload;
+`--gpus N` without a launcher starts N ranks (one replica per GPU).
 """
 from __future__ import annotations
 
@@ -147,7 +150,7 @@ def make_many_heads_case():
 
 
 def many_heads_call(nb, rt, torch, stream=None):
-    """Upload the many-head case, plan it, and return a closure doing one layer call (partial + merge)."""
+    """Upload the many-head case, plan it, and return a closure doing one layer call (partial + merge kernels)."""
     case = make_many_heads_case()
     dev = nb.mla_device_query()
     plan = nb.mla_plan(case.context_lens.tolist(), MH_H, 1, MH_BS, dev, max_partitions=64, dtype="bf16")
@@ -158,9 +161,8 @@ def many_heads_call(nb, rt, torch, stream=None):
     out = torch.empty((MH_B, 1, MH_H, 512), dtype=torch.bfloat16, device="cuda")
     desc = rt.make_desc(dc, chunks_dev, nb.MLA_KERNEL_TC, plan.cluster_ctas, stream)
 
-    def call():
-        rt.decode_partial(dc, part, lse, desc=desc)
-        rt.merge_states(part, lse, ind, MH_B, 1, MH_H, "bf16", out=out, stream=stream)
+    def call():  # mla_decode: the 128-row kernel, then the merge kernel
+        rt.decode(dc, part, lse, ind, out, desc=desc)
 
     tokens = int(case.context_lens.sum())
     return call, plan, tokens
@@ -401,11 +403,10 @@ def run_profile_case(args):
     ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
     out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
     k = plan.clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
-    ws = rt.alloc_workspace(plan.num_chunks, k, plan.cluster_ctas, 1, H)
-    for _ in range(args.launches):
-        rt.decode_partial(dc, part, lse, chunks_dev=chunks_dev, kernel=kernel, cluster=plan.cluster_ctas, subs=k,
-                          workspace=ws)
-        rt.merge_states(part, lse, ind, 1, 1, H, "f16", out=out)
+    ws = rt.alloc_decode_workspace(1, plan.num_chunks, k, plan.cluster_ctas, 1, H)
+    for _ in range(args.launches):  # the bench's layer call: mla_decode (one launch on the paired kernel)
+        rt.decode(dc, part, lse, ind, out, kernel=kernel, cluster=plan.cluster_ctas, chunks_dev=chunks_dev, subs=k,
+                  workspace=ws, tables_ready=True)
     torch.cuda.synchronize()
     st, code = nb.mla_check_device_errors(None)
     print(json.dumps({"profile_ctx": L, "launches": args.launches, "partitions": plan.num_chunks,
@@ -491,11 +492,16 @@ def run_ours(args, rank, world):
             out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
             k = plan.clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
             ws = rt.alloc_workspace(plan.num_chunks, k, plan.cluster_ctas, 1, H)
+            dws = rt.alloc_decode_workspace(1, plan.num_chunks, k, plan.cluster_ctas, 1, H)
             # the tables are uploaded before the step and no kernel of the step writes them
             desc = rt.make_desc(dc, chunks_dev, kernel, plan.cluster_ctas, stream, k, ws, tables_ready=True)
+            fdesc = rt.make_desc(dc, chunks_dev, kernel, plan.cluster_ctas, stream, k, dws, tables_ready=True)
             calls.append(dict(L=L, plan=plan, dc=dc, chunks=chunks_dev, part=part, lse=lse, ind=ind, out=out,
-                              desc=desc, ws=ws))
+                              desc=desc, fdesc=fdesc, ws=ws, dws=dws))
     torch.cuda.synchronize()
+
+    def layer(c):  # one decode layer call through the library's single entry point
+        rt.decode(c["dc"], c["part"], c["lse"], c["ind"], c["out"], desc=c["fdesc"])
 
     def partial(c):
         rt.decode_partial(c["dc"], c["part"], c["lse"], desc=c["desc"])
@@ -504,32 +510,40 @@ def run_ours(args, rank, world):
         rt.merge_states(c["part"], c["lse"], c["ind"], 1, 1, H, "f16", out=c["out"], stream=stream)
 
     # warm-up through the plain calls (also sets kernel attributes before capture)
+    nb.mla_reset_counters()
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
             for c in calls:
+                layer(c)
                 partial(c)
                 merge(c)
     stream.synchronize()
     st, code = nb.mla_check_device_errors(stream.cuda_stream)
     if st != nb.MLA_OK:
         raise RuntimeError(f"device error word {code:#x} after warm-up")
+    fused = nb.mla_get_counters()[nb.CTR_DECODE_FUSED] == max(3, args.warmup) * len(calls)
 
-    # One CUDA graph per step (all six layer calls, partial + merge): `value`.
-    # One CUDA graph of the six partial launches alone: the partial kernel's
-    # average launch duration for the roofline. Both sweep the six disjoint
-    # caches, so every launch streams its latent from HBM.
-    g_step, g_part = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    # One CUDA graph per step (all six layer calls through mla_decode): `value`. With the paired
+    # kernel each call is one launch (the merge runs inside it), so the step graph is that
+    # kernel's launches alone and also gives its average launch duration for the roofline.
+    # Otherwise a graph of the six partial launches alone gives the partial kernel's. Every
+    # graph sweeps the six disjoint caches, so every launch streams its latent from HBM.
+    g_step, g_part, g_two = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step, stream=stream):
         for c in calls:
-            partial(c)
-            merge(c)
+            layer(c)
     with torch.cuda.graph(g_part, stream=stream):
         for c in calls:
             partial(c)
+    with torch.cuda.graph(g_two, stream=stream):
+        for c in calls:
+            partial(c)
+            merge(c)
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
             g_step.replay()
             g_part.replay()
+            g_two.replay()
     stream.synchronize()
 
     K = args.steps
@@ -542,7 +556,7 @@ def run_ours(args, rank, world):
     stream.synchronize()
     step_s = max(probe[0].elapsed_time(probe[1]) * 1e-3, 1e-6)
     reps = max(1, int(0.6 / (step_s * K)) + 1)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -553,34 +567,46 @@ def run_ours(args, rank, world):
             for _ in range(K * reps):
                 g_step.replay()
             ev[1].record(stream)
-            for _ in range(K * reps):
-                g_part.replay()
-            ev[2].record(stream)
+            if not fused:
+                for _ in range(K * reps):
+                    g_part.replay()
+                ev[2].record(stream)
         stream.synchronize()
     if world > 1:
         torch.distributed.barrier()
     total_ms = ev[0].elapsed_time(ev[1]) / reps  # per K steps
-    part_ms_all = ev[1].elapsed_time(ev[2]) / reps
+    part_ms_all = total_ms if fused else ev[1].elapsed_time(ev[2]) / reps
     if world > 1:
         total_ms = max_over_ranks(total_ms, "cuda")
     st, code = nb.mla_check_device_errors(stream.cuda_stream)
     if st != nb.MLA_OK:
         raise RuntimeError(f"device error word {code:#x} in the timed region")
 
+    # the same step as two launches per layer call (partial kernel, then merge kernel), outside the
+    # timed region, for comparison
+    e2 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(stream):
+        e2[0].record(stream)
+        for _ in range(K):
+            g_two.replay()
+        e2[1].record(stream)
+    stream.synchronize()
+    two_launch_us = e2[0].elapsed_time(e2[1]) * 1e3 / (K * len(calls))
+
     # per-context breakdown (not part of the timed region): one graph per call
     per_ctx = []
-    part_bytes_all = 0
+    kern_bytes_all = 0
     for c in calls:
         pb, mb = algorithmic_bytes(c["L"], c["plan"].num_chunks)
-        part_bytes_all += pb * K
+        kern_bytes_all += (pb + mb if fused else pb) * K
         g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(g1, stream=stream):
             for _ in range(4):  # the other caches sit between repeats in the sweep; here each repeat re-reads
-                partial(c)
-                merge(c)
+                layer(c)
         with torch.cuda.graph(g2, stream=stream):
             for _ in range(4):
                 partial(c)
+                merge(c)
         e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         with torch.cuda.stream(stream):
             g1.replay()
@@ -592,12 +618,11 @@ def run_ours(args, rank, world):
             e[2].record(stream)
         stream.synchronize()
         us = e[0].elapsed_time(e[1]) * 1e3 / 4
-        pus = e[1].elapsed_time(e[2]) * 1e3 / 4
+        tus = e[1].elapsed_time(e[2]) * 1e3 / 4
         per_ctx.append({"ctx": c["L"], "partitions": c["plan"].num_chunks, "cluster": c["plan"].cluster_ctas,
                         "clusters_per_partition": c["desc"].clusters_per_chunk,
-                        "us_per_call": round(us, 3), "partial_us": round(pus, 3),
+                        "us_per_call": round(us, 3), "two_launch_us": round(tus, 3),
                         "layer_gbs": round((pb + mb) / (us * 1e-6) / 1e9, 1),
-                        "partial_gbs": round(pb / (pus * 1e-6) / 1e9, 1),
                         "note": "repeats of one cache; caches <= 113 MB may be partly L2-resident"})
 
     # a single cold call per context: L2 flushed by writing 512 MB, then one un-graphed layer call
@@ -610,8 +635,7 @@ def run_ours(args, rank, world):
             with torch.cuda.stream(stream):
                 flush.fill_(t + 1)
                 e[0].record(stream)
-                partial(c)
-                merge(c)
+                layer(c)
                 e[1].record(stream)
             stream.synchronize()
             cold.append(e[0].elapsed_time(e[1]) * 1e3)
@@ -676,8 +700,8 @@ def run_ours(args, rank, world):
                             ckv=dc.ckv, kpe=dc.kpe, block_table=dview(lay["bt"], torch.int32),
                             context_lens=dview(lay["lens"], torch.int32), case=dc.case)
         chunks = dview(lay["chunks"], torch.int32)
-        desc = rt.make_desc(edc, chunks, kernel, c["plan"].cluster_ctas, stream, c["desc"].clusters_per_chunk, c["ws"],
-                            tables_ready=True)
+        desc = rt.make_desc(edc, chunks, kernel, c["plan"].cluster_ctas, stream, c["desc"].clusters_per_chunk,
+                            c["dws"], tables_ready=True)
         e2e_calls.append(dict(dc=edc, desc=desc, ind=dview(lay["ind"], torch.int32), out=dout[j],
                               part=c["part"], lse=c["lse"]))
     h2d = off
@@ -688,8 +712,7 @@ def run_ours(args, rank, world):
         with torch.cuda.stream(stream):
             dbuf.copy_(hbuf, non_blocking=True)
             for e in e2e_calls:
-                rt.decode_partial(e["dc"], e["part"], e["lse"], desc=e["desc"])
-                rt.merge_states(e["part"], e["lse"], e["ind"], 1, 1, H, "f16", out=e["out"], stream=stream)
+                rt.decode(e["dc"], e["part"], e["lse"], e["ind"], e["out"], desc=e["desc"])
             hout.copy_(dout, non_blocking=True)
         stream.synchronize()
 
@@ -706,9 +729,9 @@ def run_ours(args, rank, world):
     ctr = nb.mla_get_counters()
     expect = (3 + e2e_steps) * len(calls)
     ctr_key = nb.CTR_PARTIAL_SIMT if kernel == nb.MLA_KERNEL_SIMT else nb.CTR_PARTIAL_TC
-    if ctr[ctr_key] != expect or ctr[nb.CTR_MERGE] != expect:
-        print(f"WARNING: path counters {ctr} disagree with {expect} launches of the {args.kernel} kernel",
-              file=sys.stderr)
+    if ctr[ctr_key] != expect or ctr[nb.CTR_DECODE_FUSED if fused else nb.CTR_MERGE] != expect:
+        print(f"WARNING: path counters {ctr} disagree with {expect} layer calls on the {args.kernel} kernel "
+              f"({'one launch' if fused else 'two launches'} each)", file=sys.stderr)
 
     many_heads = time_many_heads(nb, rt, torch, stream)
     st, code = nb.mla_check_device_errors(stream.cuda_stream)
@@ -717,7 +740,7 @@ def run_ours(args, rank, world):
 
     n_calls = K * len(calls)
     value_us = job_us_per_call(total_ms, n_calls, world)
-    achieved = part_bytes_all / (part_ms_all * 1e-3) / 1e9
+    achieved = kern_bytes_all / (part_ms_all * 1e-3) / 1e9
     peaks = measured_peaks()
     if peaks and peaks.get("hbm_gbs"):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured"
@@ -739,19 +762,23 @@ def run_ours(args, rank, world):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "contexts": CONTEXTS, "B": 1, "H": H, "kv_lora_rank": 512, "rope_dim": 64,
                    "block_size": BS, "partitions": "planner", "kernel": args.kernel,
+                   "launches_per_layer_call": 1 if fused else 2,
                    "l2": "inputs larger than L2: each step streams six disjoint caches, 528 MB",
-                   "timing": "CUDA graph per step (6 layer calls), CUDA events on the launching stream; "
-                             "roofline from a graph of the 6 partial launches"},
+                   "timing": "CUDA graph per step (6 layer calls through mla_decode), CUDA events on the launching "
+                             "stream" + ("" if fused else "; roofline from a graph of the 6 partial launches")},
         "per_ctx": per_ctx,
         "trials": trials,
+        "two_launch_us": round(two_launch_us, 3),
         "many_heads": many_heads,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(kname, sum(CONTEXTS) / len(CONTEXTS)),
-                     "peak_source": peak_src, "kernel": kname},
+                     "peak_source": peak_src, "kernel": kname,
+                     "bytes": "latent + block table + queries + partials and LSE written and read back + output"
+                              if fused else "latent + block table + queries + partials and LSE written"},
         "e2e": {"value": round(e2e_s * 1e6 / (e2e_steps * len(calls)), 3), "unit": "us/layer-call",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": (2 + 1) * n_calls * reps,  # step graphs (partial + merge) and partial-only graphs
+        "gpu_launches": (1 if fused else 3) * n_calls * reps,
         "timed_repeats": reps,
         "clocks": clocks.summary(),
     }

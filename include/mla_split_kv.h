@@ -309,6 +309,52 @@ mla_status_t mla_merge_states(const float* partials, const float* lse, const int
                               int32_t out_dtype, float* out_lse, void* stream);
 
 /*
+ * mla_decode -- one whole decode layer call: mla_decode_partial and then
+ * mla_merge_states over the request-major offsets o_indptr, with the same
+ * arguments and the same results (the chunk partials and LSE in
+ * partials / lse, the merged output in out, rounded once to out_dtype, the
+ * merged LSE in out_lse when it is not NULL). "[kernel] Wire MLA split-KV
+ * decode" (vllm-metal PR #601), *What changed*, avoids a temporary by letting
+ * partition 0 write straight into the output; here the reduce itself moves
+ * into the partial kernel: with the paired 16-row fp16 kernel (q_len*H <=
+ * 16, clusters of 2..16 CTAs) the call is ONE launch. Once a chunk's partial
+ * is written, a ticket per (request, column slice) counts it, and the CTA
+ * that counts a request's last chunk merges that slice of all the request's
+ * partials into `out`, with the merge kernel's arithmetic in its order, so
+ * `out` is the same bits as mla_merge_states on the same partials. Other
+ * kernels run the two launches on `stream` (no spread plans there).
+ *
+ * o_indptr : device [B+1] int32, as for mla_merge_states; request b's chunks
+ *            must write exactly the slots o_indptr[b] .. o_indptr[b+1]-1 and
+ *            every request needs at least one chunk (mla_plan's tables do;
+ *            with desc->chunks == NULL, o_indptr[b] = b * num_partitions).
+ *            Device data: not checked.
+ * out      : device [B, q_len, H, 512] of out_dtype (MLA_F16/BF16/F32)
+ * out_lse  : device [B, q_len, H] fp32, or NULL
+ * desc->workspace (one launch only): DEVICE, >= mla_decode_workspace_bytes(...)
+ *            bytes, 16-byte aligned, ZEROED by the caller before its first use;
+ *            every completed call leaves it zeroed again (after a device error,
+ *            zero it again). It holds the request tickets, a copy of each
+ *            chunk's LSE and, for clusters_per_chunk > 1, what
+ *            mla_decode_partial's workspace holds. Calls sharing a workspace
+ *            must not overlap in time.
+ * Returns what mla_decode_partial returns (and MLA_ERR_INVALID_ARG for a
+ * NULL or misaligned o_indptr / out / out_lse or a short workspace,
+ * MLA_ERR_UNSUPPORTED for another out_dtype). No counterpart on the pages as
+ * one call: the pages launch the two kernels.
+ */
+mla_status_t mla_decode(const void* q_absorbed, const void* q_pe, const void* ckv_cache, const void* kpe_cache,
+                        const int32_t* block_table, const int32_t* context_lens, float scale, int32_t num_partitions,
+                        float* partials, float* lse, const int32_t* o_indptr, void* out, int32_t out_dtype,
+                        float* out_lse, const mla_decode_desc_t* desc);
+
+/* Workspace bytes of a single-launch mla_decode: B * 16 uint32 request tickets
+ * and num_chunks * q_len * H fp32 LSE copies (each block 256-byte aligned),
+ * then mla_workspace_bytes(num_chunks, clusters_per_chunk, cluster_ctas, ...). */
+uint64_t mla_decode_workspace_bytes(int32_t num_requests, int32_t num_chunks, int32_t clusters_per_chunk,
+                                    int32_t cluster_ctas, int32_t q_len, int32_t num_heads);
+
+/*
  * mla_check_device_errors -- synchronize `stream`, read and clear the device
  * error word the kernels set (bounded-wait timeout, out-of-range page id).
  * *code_out (nullable) receives the raw word. When the word was set it also
@@ -352,7 +398,8 @@ mla_status_t mla_selfcheck(float* max_abs_err);
 #define MLA_CTR_MERGE 2
 #define MLA_CTR_REJECTED 3
 #define MLA_CTR_CTAS 4 /* CTAs launched by partial kernels */
-#define MLA_NUM_COUNTERS 5
+#define MLA_CTR_DECODE_FUSED 5 /* mla_decode calls that ran as one launch */
+#define MLA_NUM_COUNTERS 6
 /* mla_get_counters -- copy min(n, MLA_NUM_COUNTERS) counters to out (host). */
 void mla_get_counters(uint64_t* out, int32_t n);
 void mla_reset_counters(void);

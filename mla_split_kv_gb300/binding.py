@@ -27,8 +27,8 @@ MLA_F16, MLA_BF16, MLA_F32 = 0, 1, 2
 MLA_STATIC_WORKSPACE_BYTES = 4 * 1024 * 1024
 MLA_KERNEL_AUTO, MLA_KERNEL_SIMT, MLA_KERNEL_TC = 0, 1, 2
 
-CTR_PARTIAL_SIMT, CTR_PARTIAL_TC, CTR_MERGE, CTR_REJECTED, CTR_CTAS = range(5)
-NUM_COUNTERS = 5
+CTR_PARTIAL_SIMT, CTR_PARTIAL_TC, CTR_MERGE, CTR_REJECTED, CTR_CTAS, CTR_DECODE_FUSED = range(6)
+NUM_COUNTERS = 6
 
 DTYPE_CODES = {"f16": MLA_F16, "bf16": MLA_BF16, "f32": MLA_F32}
 
@@ -108,6 +108,11 @@ def load() -> ctypes.CDLL:
     lib.mla_decode_partial_static.argtypes = [vp, vp, vp, vp, vp, vp, f32, i32, vp, vp,
                                               ctypes.POINTER(mla_decode_desc_t)]
     lib.mla_decode_partial_static.restype = i32
+    lib.mla_decode.argtypes = [vp, vp, vp, vp, vp, vp, f32, i32, vp, vp, vp, vp, i32, vp,
+                               ctypes.POINTER(mla_decode_desc_t)]
+    lib.mla_decode.restype = i32
+    lib.mla_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.mla_decode_workspace_bytes.restype = u64
     lib.mla_merge_states.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32, vp, vp]
     lib.mla_merge_states.restype = i32
     lib.mla_check_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -216,6 +221,20 @@ def mla_decode_partial_static(q_absorbed: int, q_pe: int, ckv_cache: int, kpe_ca
     _check(load().mla_decode_partial_static(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens,
                                             ctypes.c_float(scale), num_partitions, partials, lse, ctypes.byref(desc)),
            "mla_decode_partial_static")
+
+
+def mla_decode(q_absorbed: int, q_pe: int, ckv_cache: int, kpe_cache: int, block_table: int, context_lens: int,
+               scale: float, num_partitions: int, partials: int, lse: int, o_indptr: int, out: int, out_dtype: int,
+               out_lse: Optional[int], desc: mla_decode_desc_t) -> None:
+    _check(load().mla_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, ctypes.c_float(scale),
+                             num_partitions, partials, lse, o_indptr, out, out_dtype, out_lse or None,
+                             ctypes.byref(desc)), "mla_decode")
+
+
+def mla_decode_workspace_bytes(num_requests: int, num_chunks: int, clusters_per_chunk: int, cluster_ctas: int,
+                               q_len: int, num_heads: int) -> int:
+    return int(load().mla_decode_workspace_bytes(num_requests, num_chunks, clusters_per_chunk, cluster_ctas, q_len,
+                                                 num_heads))
 
 
 def mla_merge_states(partials: int, lse: int, o_indptr: int, B: int, q_len: int, num_heads: int, out: int,

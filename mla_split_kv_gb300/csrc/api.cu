@@ -226,29 +226,44 @@ mla_status_t check_decode(const void* q_absorbed, const void* q_pe, const void* 
   return MLA_OK;
 }
 
-}  // namespace
+// The fused final merge of mla_decode (all null / 0 for mla_decode_partial).
+struct FusedMerge {
+  const int32_t* o_indptr = nullptr;
+  void* out = nullptr;
+  float* out_lse = nullptr;
+  int32_t out_dtype = 0;
+  uint32_t* req_tickets = nullptr;
+  float* lse_copy = nullptr;
+};
 
-extern "C" {
+// Cluster size the launch will use (the descriptor's, or the library's choice).
+int launch_cluster(const mla_decode_desc_t* d, int64_t N) {
+  const bool use_simt = (d->kernel == MLA_KERNEL_SIMT);
+  const int rows_total = d->num_heads * d->q_len;
+  const bool mh = !use_simt && mla::mh_supports(rows_total, d->cluster_ctas ? d->cluster_ctas : 2);
+  const int nr = use_simt ? mla::simt_rows_per_cta()
+                          : (mh ? 128 : mla::tc_rows_per_cta(rows_total, d->dtype == MLA_BF16));
+  const int64_t groups = (rows_total + nr - 1) / nr;
+  return d->cluster_ctas ? d->cluster_ctas : (mh ? 2 : default_cluster(N * groups));
+}
 
-mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const void* ckv_cache,
-                                const void* kpe_cache, const int32_t* block_table, const int32_t* context_lens,
-                                float scale, int32_t num_partitions, float* partials, float* lse,
-                                const mla_decode_desc_t* d) {
-  int64_t N = 0;
-  const mla_status_t chk = check_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
-                                        num_partitions, partials, lse, d, true, &N);
-  if (chk != MLA_OK) return reject(chk);
+// One launch of the partial kernel the descriptor selects (arguments already checked; N chunks;
+// `spread_ws` the workspace of a spread plan), with the final merge fused when fm.out is set.
+mla_status_t launch_decode(const void* q_absorbed, const void* q_pe, const void* ckv_cache, const void* kpe_cache,
+                           const int32_t* block_table, const int32_t* context_lens, float scale,
+                           int32_t num_partitions, float* partials, float* lse, const mla_decode_desc_t* d,
+                           int64_t N, void* spread_ws, const FusedMerge& fm) {
   const int32_t C0 = d->cluster_ctas;
   const uint64_t rows = static_cast<uint64_t>(d->num_blocks) * static_cast<uint64_t>(d->block_size);
   const bool use_simt = (d->kernel == MLA_KERNEL_SIMT);
   const bool bf16 = (d->dtype == MLA_BF16);
   const int rows_total = d->num_heads * d->q_len;
-  // 128 rows on the tensor-core path: one CTA pair holds all of them (a cluster of 2 by default)
+  // a multiple of 128 rows on the tensor-core path: one CTA pair per 128 rows (a cluster of 2 by default)
   const bool mh = !use_simt && mla::mh_supports(rows_total, C0 ? C0 : 2);
-  const int nr = use_simt ? mla::simt_rows_per_cta() : (mh ? rows_total : mla::tc_rows_per_cta(rows_total, bf16));
+  const int nr = use_simt ? mla::simt_rows_per_cta() : (mh ? 128 : mla::tc_rows_per_cta(rows_total, bf16));
   const int64_t groups = (rows_total + nr - 1) / nr;
   const int32_t subs = (d->clusters_per_chunk > 1) ? d->clusters_per_chunk : 1;
-  const int C = C0 ? C0 : (mh ? 2 : default_cluster(N * groups));
+  const int C = launch_cluster(d, N);
 
   CUtensorMap tm_ckv, tm_kpe, tm_pages, tm_kpe_half;
   if (!tensor_map(&tm_ckv, ckv_cache, rows, mla::kRank, d->block_size, d->dtype) ||
@@ -285,7 +300,7 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   p.ws_lse = nullptr;
   p.ws_tickets = nullptr;
   if (subs > 1) {
-    uint8_t* ws = static_cast<uint8_t*>(d->workspace);
+    uint8_t* ws = static_cast<uint8_t*>(spread_ws);
     // tickets (two per chunk), then per chunk its entries, one per CTA pair (subs * cluster_ctas / 2),
     // [rows][512] fp32 each, then per entry two [rows][2] fp32 copies
     const uint64_t tickets = (static_cast<uint64_t>(N) * 2 * 4 + 255) / 256 * 256;
@@ -294,6 +309,12 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
     p.ws_partials = reinterpret_cast<float*>(ws + tickets);
     p.ws_lse = p.ws_partials + entries * rows_total * mla::kRank;
   }
+  p.o_indptr = fm.o_indptr;
+  p.out = fm.out;
+  p.out_lse = fm.out_lse;
+  p.out_dtype = fm.out_dtype;
+  p.req_tickets = fm.req_tickets;
+  p.lse_copy = fm.lse_copy;
   cudaStream_t stream = static_cast<cudaStream_t>(d->stream);
   const cudaError_t e =
       use_simt ? mla::launch_partial_simt(tm_ckv, tm_kpe, p, static_cast<int>(N), C, bf16, stream)
@@ -304,7 +325,76 @@ mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const 
   }
   g_counters[use_simt ? MLA_CTR_PARTIAL_SIMT : MLA_CTR_PARTIAL_TC].fetch_add(1, std::memory_order_relaxed);
   g_counters[MLA_CTR_CTAS].fetch_add(static_cast<uint64_t>(N * groups * C * subs), std::memory_order_relaxed);
+  if (fm.out != nullptr) g_counters[MLA_CTR_DECODE_FUSED].fetch_add(1, std::memory_order_relaxed);
   return MLA_OK;
+}
+
+uint64_t round256(uint64_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_decode_partial(const void* q_absorbed, const void* q_pe, const void* ckv_cache,
+                                const void* kpe_cache, const int32_t* block_table, const int32_t* context_lens,
+                                float scale, int32_t num_partitions, float* partials, float* lse,
+                                const mla_decode_desc_t* d) {
+  int64_t N = 0;
+  const mla_status_t chk = check_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
+                                        num_partitions, partials, lse, d, true, &N);
+  if (chk != MLA_OK) return reject(chk);
+  return launch_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale, num_partitions,
+                       partials, lse, d, N, d->workspace, FusedMerge{});
+}
+
+uint64_t mla_decode_workspace_bytes(int32_t num_requests, int32_t num_chunks, int32_t clusters_per_chunk,
+                                    int32_t cluster_ctas, int32_t q_len, int32_t num_heads) {
+  if (num_requests < 1 || num_chunks < 1 || q_len < 1 || num_heads < 1) return 0;
+  const uint64_t tickets = round256(static_cast<uint64_t>(num_requests) * mla::kSliceTickets * 4);
+  const uint64_t lse_copy = round256(static_cast<uint64_t>(num_chunks) * q_len * num_heads * 4);
+  return tickets + lse_copy + mla_workspace_bytes(num_chunks, clusters_per_chunk, cluster_ctas, q_len, num_heads);
+}
+
+mla_status_t mla_decode(const void* q_absorbed, const void* q_pe, const void* ckv_cache, const void* kpe_cache,
+                        const int32_t* block_table, const int32_t* context_lens, float scale, int32_t num_partitions,
+                        float* partials, float* lse, const int32_t* o_indptr, void* out, int32_t out_dtype,
+                        float* out_lse, const mla_decode_desc_t* d) {
+  int64_t N = 0;
+  const mla_status_t chk = check_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
+                                        num_partitions, partials, lse, d, false, &N);
+  if (chk != MLA_OK) return reject(chk);
+  if (o_indptr == nullptr || out == nullptr || !aligned(o_indptr, 4) || !aligned(out, 16) ||
+      (out_lse != nullptr && !aligned(out_lse, 4)))
+    return reject(MLA_ERR_INVALID_ARG);
+  if (out_dtype != MLA_F16 && out_dtype != MLA_BF16 && out_dtype != MLA_F32) return reject(MLA_ERR_UNSUPPORTED);
+  const int rows_total = d->num_heads * d->q_len;
+  const bool fused = d->kernel != MLA_KERNEL_SIMT &&
+                     mla::tc128_supports(rows_total, d->dtype == MLA_BF16, launch_cluster(d, N));
+  if (!fused) {
+    // kernels without the fused merge: the partial kernel, then the merge kernel, on the same stream
+    if (d->clusters_per_chunk > 1) return reject(MLA_ERR_UNSUPPORTED);  // spread plans are the paired kernel's
+    mla_status_t st = launch_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
+                                    num_partitions, partials, lse, d, N, nullptr, FusedMerge{});
+    if (st != MLA_OK) return st;
+    return mla_merge_states(partials, lse, o_indptr, d->num_requests, d->q_len, d->num_heads, out, out_dtype, out_lse,
+                            d->stream);
+  }
+  const uint64_t need = mla_decode_workspace_bytes(d->num_requests, static_cast<int32_t>(N), d->clusters_per_chunk,
+                                                   d->cluster_ctas, d->q_len, d->num_heads);
+  if (d->workspace == nullptr || !aligned(d->workspace, 16) || d->workspace_bytes < need)
+    return reject(MLA_ERR_INVALID_ARG);
+  uint8_t* ws = static_cast<uint8_t*>(d->workspace);
+  FusedMerge fm;
+  fm.o_indptr = o_indptr;
+  fm.out = out;
+  fm.out_lse = out_lse;
+  fm.out_dtype = out_dtype;
+  fm.req_tickets = reinterpret_cast<uint32_t*>(ws);
+  const uint64_t tickets = round256(static_cast<uint64_t>(d->num_requests) * mla::kSliceTickets * 4);
+  fm.lse_copy = reinterpret_cast<float*>(ws + tickets);
+  void* spread_ws = ws + tickets + round256(static_cast<uint64_t>(N) * rows_total * 4);
+  return launch_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale, num_partitions,
+                       partials, lse, d, N, spread_ws, fm);
 }
 
 }  // extern "C"

@@ -510,11 +510,12 @@ __device__ __forceinline__ void uniform_chunk(int32_t L, int32_t P, int32_t p, i
 
 // Fill the chunk (blockIdx.y, or `chunk`), the CTA's token sub-range (runs of
 // `unit`-token tiles split evenly over the cluster, or over `nparts` groups,
-// this CTA in group `part`) and its query rows. Tokens are trimmed to the last one any row
+// this CTA in group `part`) and its query rows (row group blockIdx.z, or
+// `row_group`). Tokens are trimmed to the last one any row
 // of this CTA can see under the causal rule.
 __device__ __forceinline__ CtaWork cta_work(const PartialParams& p, int32_t rows_per_cta,
                                             int32_t unit = kTileTokens, int32_t part = -1, int32_t nparts = 0,
-                                            int32_t chunk = -1) {
+                                            int32_t chunk = -1, int32_t row_group = -1) {
   CtaWork w;
   const int32_t n = (chunk >= 0) ? chunk : static_cast<int32_t>(blockIdx.y);
   if (p.chunks != nullptr) {
@@ -536,7 +537,7 @@ __device__ __forceinline__ CtaWork cta_work(const PartialParams& p, int32_t rows
   if (w.t1 > w.L) w.t1 = w.L;
   if (w.t0 < 0) w.t0 = 0;
   if (w.t0 > w.t1) w.t0 = w.t1;
-  w.row0 = blockIdx.z * rows_per_cta;
+  w.row0 = ((row_group >= 0) ? row_group : static_cast<int32_t>(blockIdx.z)) * rows_per_cta;
   const int32_t total_rows = p.q_len * p.H;
   w.nrows = total_rows - w.row0;
   if (w.nrows > rows_per_cta) w.nrows = rows_per_cta;
@@ -630,6 +631,88 @@ __device__ __forceinline__ void cluster_combine_to(const PartialParams& p, const
 __device__ __forceinline__ void cluster_combine(const PartialParams& p, const CtaWork& w, const float* ostage,
                                                 const float* mst, const float* lst, int tid, int nthreads) {
   cluster_combine_to(p, w, ostage, mst, lst, tid, nthreads, p.partials, p.lse, static_cast<long long>(w.slot));
+}
+
+// Single-launch decode: the final merge of request b's chunk partials (slots lo .. hi-1,
+// normalized, base-2 LSE in lse_src) for columns [col0, col0 + ncols) of every row, into
+// p.out (p.out_dtype) and, with write_lse, p.out_lse. It is the merge kernel's arithmetic in
+// the merge kernel's order (maximum LSE, weights 2^(lse - M) with -inf giving 0, the weight
+// sum and the fused multiply-adds in slot order, one division, one rounding), so the output
+// is the same bits as mla_merge_states on the same partials. The partials were written by
+// other CTAs (ordered before this CTA's ticket by their fences), so they are read through L2.
+__device__ __forceinline__ void request_merge(const PartialParams& p, int b, int lo, int hi, int col0, int ncols,
+                                              bool write_lse, const float* lse_src, int tid, int nthreads) {
+  const int rows = p.q_len * p.H;
+  const int n = hi - lo;
+  const int n4 = ncols / 4;
+  const int items = rows * n4 + (write_lse ? rows : 0);
+  const long long stride = static_cast<long long>(rows) * kRank;  // one partial slot
+  for (int idx = tid; idx < items; idx += nthreads) {
+    const bool is_lse = idx >= rows * n4;
+    const int r = is_lse ? idx - rows * n4 : idx / n4;
+    const int c = col0 + (is_lse ? 0 : (idx % n4) * 4);
+    const float* lrow = lse_src + static_cast<long long>(lo) * rows + r;
+    const float* vcol = p.partials + static_cast<long long>(lo) * stride + static_cast<long long>(r) * kRank + c;
+    float M = -INFINITY;
+    for (int j = 0; j < n; ++j) M = fmaxf(M, __ldcg(lrow + static_cast<long long>(j) * rows));
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+      for (int j0 = 0; j0 < n; j0 += 8) {
+        float lj[8];
+        float4 v[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const bool in = j0 + jj < n;
+          lj[jj] = in ? __ldcg(lrow + static_cast<long long>(j0 + jj) * rows) : -INFINITY;
+          v[jj] = (in && !is_lse) ? __ldcg(reinterpret_cast<const float4*>(vcol + (j0 + jj) * stride))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          if (j0 + jj < n) {
+            const float wj = (lj[jj] == -INFINITY) ? 0.f : exp2f(lj[jj] - M);
+            den += wj;
+            acc.x = fmaf(wj, v[jj].x, acc.x);
+            acc.y = fmaf(wj, v[jj].y, acc.y);
+            acc.z = fmaf(wj, v[jj].z, acc.z);
+            acc.w = fmaf(wj, v[jj].w, acc.w);
+          }
+        }
+      }
+      acc = make_float4(acc.x / den, acc.y / den, acc.z / den, acc.w / den);
+    }
+    const long long br = static_cast<long long>(b) * rows + r;
+    if (is_lse) {
+      if (p.out_lse != nullptr) p.out_lse[br] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
+      continue;
+    }
+    const long long o_off = br * kRank + c;
+    if (p.out_dtype == 2) {
+      *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o_off) = acc;
+    } else {
+      const bool bf = (p.out_dtype == 1);
+      const float f[4] = {acc.x, acc.y, acc.z, acc.w};
+      uint16_t h[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) h[j] = bf ? f2h<true>(f[j]) : f2h<false>(f[j]);
+      uint2 packed;
+      packed.x = static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16);
+      packed.y = static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[3]) << 16);
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + o_off) = packed;
+    }
+  }
+}
+
+// Request b's chunk slots [lo, hi): from the offsets, or the uniform split.
+__device__ __forceinline__ void request_slots(const PartialParams& p, int b, int* lo, int* hi) {
+  if (p.o_indptr != nullptr) {
+    *lo = __ldg(p.o_indptr + b);
+    *hi = __ldg(p.o_indptr + b + 1);
+  } else {
+    *lo = b * p.num_parts;
+    *hi = (b + 1) * p.num_parts;
+  }
 }
 
 }  // namespace mla

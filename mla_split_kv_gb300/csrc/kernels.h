@@ -44,7 +44,18 @@ struct PartialParams {
   float* ws_partials;          // [entries, q_len, H, 512]
   float* ws_lse;               // [entries, 2, q_len, H, 2]
   uint32_t* ws_tickets;        // [chunks, 2]
+  // Single-launch decode (out != null): once a request's chunk partials are written, the CTA
+  // that finishes last for a column slice of the request merges that slice of all of them into
+  // `out`, with the merge kernel's arithmetic. Tickets: [B][kSliceTickets], zero between calls.
+  // lse_copy: [slots, q_len, H], the second column half's copy of each chunk's LSE (spread plans).
+  const int32_t* o_indptr;     // [B+1] request-major chunk offsets (device)
+  void* out;                   // [B, q_len, H, 512] of out_dtype, or null
+  float* out_lse;              // [B, q_len, H], or null
+  int32_t out_dtype;           // MLA_F16 / MLA_BF16 / MLA_F32
+  uint32_t* req_tickets;
+  float* lse_copy;
 };
+constexpr int kSliceTickets = 16;  // per request: one per column slice (cluster rank) or column half
 
 struct MergeParams {
   const float* partials;
@@ -73,8 +84,8 @@ bool tc128_supports(int total_rows, bool bf16, int cluster);
 cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe_half, const PartialParams& p,
                                  int num_chunks, int cluster, cudaStream_t stream);
 int tc128_max_active_clusters(int cluster);
-// 64-token-tile tensor-core kernel for 128 rows (q_len * H == 128), fp16 or bf16,
-// on clusters of one CTA pair that split the latent columns.
+// 64-token-tile tensor-core kernel for groups of 128 rows (q_len * H a multiple of 128),
+// fp16 or bf16, each group on a cluster of one CTA pair that split the latent columns.
 bool mh_supports(int total_rows, int cluster);
 cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe, const PartialParams& p,
                               int num_chunks, bool bf16, cudaStream_t stream);

@@ -1,6 +1,6 @@
-// Tensor-core partial-decode kernel for 128 query rows (the heads of a
-// many-head decode, e.g. H=128 with one query token), on a pair of CTAs,
-// sm_103a.
+// Tensor-core partial-decode kernel for groups of 128 query rows (the heads of
+// a many-head decode, e.g. H=128 with one query token, or the rows of a
+// verify window, q_len x H), each group on a pair of CTAs, sm_103a.
 //
 // The operation is the one of the other partial kernels ("feat(core):
 // matrix-absorbed MLA decode over a compressed-latent KV cache", *What
@@ -144,7 +144,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   cluster_arrive_release();  // the peer touches this CTA's barriers only after this cluster phase
   const uint32_t tmem = sm->tmem_base;
-  const CtaWork w = cta_work(p, kRows, kT, 0, 1);  // both CTAs of the pair take the whole chunk
+  // both CTAs of the pair take the whole chunk; pair g = blockIdx.x / 2 takes query rows [128 g, 128 g + 128)
+  // (the row groups of a chunk are adjacent clusters, so they stream the same tiles at about the same time
+  // and the later reads are served by L2)
+  const CtaWork w = cta_work(p, kRows, kT, 0, 1, -1, static_cast<int32_t>(blockIdx.x >> 1));
   const int ntiles = (w.sub1 - w.sub0 + kT - 1) / kT;
 
   if (warp > kMmaWarp) {
@@ -579,14 +582,14 @@ cudaError_t prepare_mh() {
 
 }  // namespace
 
-bool mh_supports(int total_rows, int cluster) { return total_rows == kRows && cluster == 2; }
+bool mh_supports(int total_rows, int cluster) { return total_rows % kRows == 0 && cluster == 2; }
 
 cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe, const PartialParams& p,
                               int num_chunks, bool bf16, cudaStream_t stream) {
   cudaError_t e = bf16 ? prepare_mh<true>() : prepare_mh<false>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2, num_chunks, 1);
+  cfg.gridDim = dim3(2 * (p.q_len * p.H / kRows), num_chunks, 1);  // one CTA pair per 128-row group
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;

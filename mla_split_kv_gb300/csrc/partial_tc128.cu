@@ -102,7 +102,8 @@ struct Small {
       xready[kSlots], drain;
   uint32_t tmem_base;
   int32_t abort_flag;
-  int32_t last_cluster;  // this cluster took the chunk's last ticket
+  int32_t last_cluster;  // this CTA took the last ticket of its chunk half (spread plans)
+  int32_t last_request;  // this CTA took the last ticket of its request slice (single-launch decode)
   float red[4][kNR];
   float mref[kNR];
   float alpha[kNR];
@@ -180,6 +181,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_launch_dependents();  // the merge of these partials may be scheduled now; it waits for this grid
   if (!p.tables_ready) w = cta_work(p, kNR, kT, pair_index, subs * cluster_pairs, chunk);
   const int ntiles = (w.sub1 - w.sub0 + kT - 1) / kT;
+  // single-launch decode: request b's chunk slots, whose partials this launch also merges
+  const bool fused = p.out != nullptr;
+  int req_lo = 0, req_hi = 0;
+  if (fused) request_slots(p, w.b, &req_lo, &req_hi);
 
   if (warp > kMmaWarp) {
     // ------------------------------------------------------------------ producers
@@ -662,7 +667,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // up to 12 entries at once (one round trip), reduced in entry order; more entries take
       // further rounds, a larger maximum rescaling what earlier rounds summed
       const int n4 = kHalfCols / 4;
-      const int items = w.nrows * n4 + (half == 0 ? w.nrows : 0);
+      // (single-launch decode: half 1 writes its own copy of the LSE, for its final merge)
+      const int items = w.nrows * n4 + ((half == 0 || fused) ? w.nrows : 0);
+      float* const lse_dst = half ? p.lse_copy : p.lse;
       for (int idx = tid; idx < items; idx += kThreads) {
         const bool is_lse = idx >= w.nrows * n4;
         const int r = is_lse ? idx - w.nrows * n4 : idx / n4;
@@ -704,11 +711,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           M = Mr;
         }
         if (is_lse) {
-          p.lse[static_cast<long long>(w.slot) * rows_total + rowoff] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
+          lse_dst[static_cast<long long>(w.slot) * rows_total + rowoff] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
         } else {
           float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
           if (M != -INFINITY) o = make_float4(num.x / den, num.y / den, num.z / den, num.w / den);
           *reinterpret_cast<float4*>(p.partials + (static_cast<long long>(w.slot) * rows_total + rowoff) * kRank + c) = o;
+        }
+      }
+      if (fused) {
+        // the chunk's partial (this half) is written: count it for the request; the CTA that
+        // counts the request's last chunk for this half merges the half's columns into the output
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+          __threadfence();
+          uint32_t* ticket = p.req_tickets + static_cast<long long>(w.b) * kSliceTickets + half;
+          const uint32_t t = atomicAdd(ticket, 1u);
+          const int last = (t == static_cast<uint32_t>(req_hi - req_lo - 1)) ? 1 : 0;
+          if (last) atomicExch(ticket, 0u);
+          sm->last_request = last;
+        }
+        __syncthreads();
+        if (sm->last_request) {
+          __threadfence();
+          request_merge(p, w.b, req_lo, req_hi, kHalfCols * half, kHalfCols, half == 0, half ? p.lse_copy : p.lse,
+                        tid, kThreads);
         }
       }
     }
@@ -812,10 +839,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  if (fused) __threadfence();  // this CTA's slice of the chunk partial, visible before any ticket below
   cluster_sync();
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  if (fused) {
+    // Single-launch decode: the cluster's chunk partial is complete (every rank wrote its column
+    // slice, rank 0 the LSE, all before the barrier above). Per request and slice a ticket counts
+    // the chunks; the CTA that counts the last one merges that slice of all the request's
+    // partials into the output (rank 0's slice also the merged LSE).
+    const int dcols = kRank / static_cast<int>(nranks);
+    if (tid == 0) {
+      // the other ranks' slices and rank 0's LSE reached this thread through the cluster barrier; this
+      // fence makes them (and this CTA's slice) visible at device scope before the ticket
+      __threadfence();
+      uint32_t* ticket = p.req_tickets + static_cast<long long>(w.b) * kSliceTickets + rank;
+      const uint32_t t = atomicAdd(ticket, 1u);
+      const int last = (t == static_cast<uint32_t>(req_hi - req_lo - 1)) ? 1 : 0;
+      if (last) atomicExch(ticket, 0u);
+      sm->last_request = last;
+    }
+    __syncthreads();
+    if (sm->last_request) {
+      __threadfence();
+      request_merge(p, w.b, req_lo, req_hi, static_cast<int>(rank) * dcols, dcols, rank == 0, p.lse, tid, kThreads);
+    }
   }
 }
 

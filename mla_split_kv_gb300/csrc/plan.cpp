@@ -82,9 +82,9 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
   if (maxP < 1 || maxP > 1024) return MLA_ERR_INVALID_ARG;
 
   const int rows = num_heads * q_len;
-  // 128 rows: one CTA pair (a cluster of 2) holds all of them
+  // a multiple of 128 rows: one CTA pair (a cluster of 2) per 128 rows
   const bool many_rows = mla::mh_supports(rows, 2);
-  const int nr = many_rows ? rows : mla::tc_rows_per_cta(rows, plan->dtype == MLA_BF16);
+  const int nr = many_rows ? 128 : mla::tc_rows_per_cta(rows, plan->dtype == MLA_BF16);
   const int64_t row_groups = (rows + nr - 1) / nr;
 
   int64_t split_tokens = 0, n_split = 0;
@@ -102,7 +102,7 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
     const int64_t slots = dev->max_clusters[k];
     if (slots <= 0) continue;
     if (paired_single && C == 1) continue;  // the paired kernel needs a pair of CTAs
-    if (many_rows && C != 2) continue;      // the 128-row kernel runs on one pair
+    if (many_rows && C != 2) continue;      // the 128-row kernel runs on CTA pairs
     Candidate cand;
     cand.cluster = C;
     cand.parts.assign(B, 1);

@@ -200,6 +200,22 @@ def make_segmented_case(seed: int, B: int, q_len: int,
     return SegmentedCase(segments=segs)
 
 
+def window_view(case: SegmentedCase, q_len: int) -> SegmentedCase:
+    """The same prefix with a shorter verify window: the first ``q_len`` query rows
+    and the first ``q_len`` tokens of the window segment (its pages and cache are
+    shared with ``case``, nothing is copied but the queries)."""
+    segs = case.segments
+    if not 1 <= q_len <= segs[0].q_len:
+        raise ValueError("q_len must be in [1, the case's window]")
+    q_abs = np.ascontiguousarray(segs[0].q_abs[:, :q_len])
+    q_pe = np.ascontiguousarray(segs[0].q_pe[:, :q_len])
+    out = []
+    for k, s in enumerate(segs):
+        lens = s.context_lens if k < len(segs) - 1 else np.full_like(s.context_lens, q_len)
+        out.append(dataclasses.replace(s, q_len=q_len, q_abs=q_abs, q_pe=q_pe, context_lens=lens))
+    return SegmentedCase(segments=out)
+
+
 def concat_segments(case: SegmentedCase) -> DecodeCase:
     """The same tokens as one logical sequence per request (prefix, then window).
 

@@ -87,6 +87,29 @@ def alloc_workspace(num_chunks: int, subs: int, cluster: int, q_len: int, H: int
     return torch.zeros(n, dtype=torch.uint8, device=device) if n else None
 
 
+def alloc_decode_workspace(B: int, num_chunks: int, subs: int, cluster: int, q_len: int, H: int,
+                           device="cuda") -> torch.Tensor:
+    """Zeroed workspace of a single-launch mla_decode (request tickets, LSE copies, the spread workspace)."""
+    n = nb.mla_decode_workspace_bytes(B, num_chunks, subs, cluster, q_len, H)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def decode(dc: DeviceCase, part: torch.Tensor, lse: torch.Tensor, o_indptr_dev: torch.Tensor, out: torch.Tensor,
+           out_lse: Optional[torch.Tensor] = None, num_partitions: int = 1, desc: Optional[nb.mla_decode_desc_t] = None,
+           **desc_kw) -> torch.Tensor:
+    """One decode layer call through mla_decode (a single launch on the paired kernel)."""
+    d = desc if desc is not None else make_desc(dc, desc_kw.get("chunks_dev"), desc_kw.get("kernel", nb.MLA_KERNEL_AUTO),
+                                                desc_kw.get("cluster", 0), desc_kw.get("stream"),
+                                                desc_kw.get("subs", 1), desc_kw.get("workspace"),
+                                                desc_kw.get("tables_ready", False))
+    out_code = {torch.float32: nb.MLA_F32, torch.float16: nb.MLA_F16, torch.bfloat16: nb.MLA_BF16}[out.dtype]
+    nb.mla_decode(dc.q_abs.data_ptr(), dc.q_pe.data_ptr(), dc.ckv.data_ptr(), dc.kpe.data_ptr(),
+                  dc.block_table.data_ptr(), dc.context_lens.data_ptr(), float(dc.case.scale), num_partitions,
+                  part.data_ptr(), lse.data_ptr(), o_indptr_dev.data_ptr(), out.data_ptr(), out_code,
+                  out_lse.data_ptr() if out_lse is not None else None, d)
+    return out
+
+
 def alloc_partials(num_slots: int, q_len: int, H: int, device="cuda"):
     part = torch.empty((num_slots, q_len, H, 512), dtype=torch.float32, device=device)
     lse = torch.empty((num_slots, q_len, H), dtype=torch.float32, device=device)
@@ -119,3 +142,35 @@ def merge_states(part: torch.Tensor, lse: torch.Tensor, o_indptr_dev: torch.Tens
 
 def uniform_indptr(B: int, P: int, device="cuda") -> torch.Tensor:
     return torch.arange(0, (B + 1) * P, P, dtype=torch.int32, device=device)
+
+
+@dataclasses.dataclass
+class SegmentPlan:
+    """Partitions of a verify window over a segmented prefix: each segment planned on its own,
+    chunk slots request-major over all segments, so one merge of o_indptr combines them."""
+    chunk_tables: list       # per segment, device int32 [n, 4] {b, t0, t1, slot}
+    plans: list              # per segment, the planner's Plan
+    o_indptr: torch.Tensor   # device [B+1]
+    num_slots: int
+
+
+def plan_segments(seg, dev: nb.mla_device_info_t, max_partitions: int = 0, device="cuda") -> SegmentPlan:
+    segs = seg.segments
+    B = segs[0].num_requests
+    plans = [nb.mla_plan(s.context_lens.tolist(), s.num_heads, s.q_len, s.block_size, dev,
+                         max_partitions=max_partitions, dtype=s.dtype) for s in segs]
+    # request b's slots: its chunks of segment 0, then of segment 1, ...
+    per = [[p.o_indptr[b + 1] - p.o_indptr[b] for b in range(B)] for p in plans]
+    indptr = [0]
+    for b in range(B):
+        indptr.append(indptr[-1] + sum(per[k][b] for k in range(len(segs))))
+    tables = []
+    for k, p in enumerate(plans):
+        rows = []
+        for b in range(B):
+            base = indptr[b] + sum(per[j][b] for j in range(k))
+            for i, (cb, t0, t1, _) in enumerate(p.chunks[p.o_indptr[b]:p.o_indptr[b + 1]]):
+                rows.append((cb, t0, t1, base + i))
+        tables.append(chunks_to_device(rows, device))
+    return SegmentPlan(chunk_tables=tables, plans=plans,
+                       o_indptr=torch.tensor(indptr, dtype=torch.int32, device=device), num_slots=indptr[-1])

@@ -383,3 +383,35 @@ def test_static_entry_rejects_a_plan_beyond_its_scratch_before_any_device_work(l
     nb.mla_reset_counters()
     assert call_static(lib, d, 1) == nb.MLA_ERR_CAPACITY
     assert nb.mla_get_counters()[nb.CTR_REJECTED] == 1
+
+
+def call_decode(lib, d, P=2, o_indptr=FAKE, out=FAKE, out_dtype=nb.MLA_F16, out_lse=None):
+    p = [FAKE] * 8
+    return lib.mla_decode(p[0], p[1], p[2], p[3], p[4], p[5], ctypes.c_float(0.07), P, p[6], p[7], o_indptr, out,
+                          out_dtype, out_lse, ctypes.byref(d))
+
+
+@pytest.mark.parametrize("kw,args,want", [
+    (dict(cluster_ctas=2), dict(o_indptr=None), nb.MLA_ERR_INVALID_ARG),
+    (dict(cluster_ctas=2), dict(out=None), nb.MLA_ERR_INVALID_ARG),
+    (dict(cluster_ctas=2), dict(out=FAKE + 8), nb.MLA_ERR_INVALID_ARG),
+    (dict(cluster_ctas=2), dict(out_lse=FAKE + 2), nb.MLA_ERR_INVALID_ARG),
+    (dict(cluster_ctas=2), dict(out_dtype=7), nb.MLA_ERR_UNSUPPORTED),
+    (dict(cluster_ctas=2), dict(), nb.MLA_ERR_INVALID_ARG),                          # no workspace
+    (dict(cluster_ctas=2, workspace=FAKE, workspace_bytes=64), dict(), nb.MLA_ERR_INVALID_ARG),  # too small
+    (dict(cluster_ctas=2, num_heads=24), dict(), nb.MLA_ERR_UNSUPPORTED),
+    (dict(cluster_ctas=4, clusters_per_chunk=4, workspace=FAKE, workspace_bytes=1024), dict(), nb.MLA_ERR_INVALID_ARG),
+])
+def test_decode_rejects_before_launch(lib, kw, args, want):
+    nb.mla_reset_counters()
+    assert call_decode(lib, desc(**kw), 2, **args) == want
+    ctr = nb.mla_get_counters()
+    assert ctr[nb.CTR_REJECTED] == 1 and ctr[nb.CTR_PARTIAL_TC] == 0 and ctr[nb.CTR_DECODE_FUSED] == 0
+
+
+def test_decode_workspace_layout():
+    # request tickets (16 per request), then a copy of each chunk's LSE, each block 256-byte aligned, then the
+    # spread workspace
+    assert nb.mla_decode_workspace_bytes(1, 7, 1, 16, 1, 16) == 256 + 512
+    assert nb.mla_decode_workspace_bytes(3, 7, 5, 4, 1, 16) == 256 + 512 + nb.mla_workspace_bytes(7, 5, 4, 1, 16)
+    assert nb.mla_decode_workspace_bytes(0, 7, 1, 16, 1, 16) == 0

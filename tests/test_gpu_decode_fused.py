@@ -1,0 +1,167 @@
+"""Single-launch decode (mla_decode) against the two-launch path and the oracle.
+
+mla_decode is mla_decode_partial followed by mla_merge_states; on the paired
+16-row fp16 kernel the merge runs inside the partial kernel (one launch). The
+fused merge uses the merge kernel's arithmetic in its order, so the chunk
+partials, the LSE and the merged output must be the same bits as the two
+launches give, and the merged output must match the f64 oracle within the
+stated tolerance (max-abs 2e-3, rel-L2 1e-3 on fp32 results).
+"""
+import numpy as np
+import pytest
+import torch
+
+from mla_split_kv_gb300 import binding as nb
+from mla_split_kv_gb300 import build as nbuild
+from mla_split_kv_gb300 import inputs as gen
+from mla_split_kv_gb300 import runtime as rt
+from oracle import mla_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, REL_L2 = 2e-3, 1e-3
+TDT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    nbuild.build()
+    nb.load()
+    yield
+    st, code = nb.mla_check_device_errors(None)
+    assert st == nb.MLA_OK, f"device error word {code:#x}"
+
+
+def assert_close(got, ref, what):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(got)), what
+    err = np.abs(got - ref).max()
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert err <= MAX_ABS and rel <= REL_L2, f"{what}: max-abs {err:.3e} rel-L2 {rel:.3e}"
+
+
+def both_paths(case, dc, chunks_dev, ind, N, kernel, C, k, out_dtype="f16", tables_ready=False, num_partitions=1,
+               ws_fused=None, with_lse=True):
+    """(partials, lse, out, out_lse) of mla_decode, then of mla_decode_partial + mla_merge_states."""
+    B, q, H = case.num_requests, case.q_len, case.num_heads
+    res = []
+    for fused in (True, False):
+        part, lse = rt.alloc_partials(N, q, H)
+        part.fill_(float("nan"))
+        out = torch.full((B, q, H, 512), float("nan"), dtype=TDT[out_dtype], device="cuda")
+        out_lse = torch.full((B, q, H), float("nan"), device="cuda") if with_lse else None
+        if fused:
+            ws = ws_fused if ws_fused is not None else rt.alloc_decode_workspace(B, N, k, C, q, H)
+            desc = rt.make_desc(dc, chunks_dev, kernel, C, None, k, ws, tables_ready)
+            rt.decode(dc, part, lse, ind, out, out_lse, num_partitions=num_partitions, desc=desc)
+        else:
+            ws = rt.alloc_workspace(N, k, C, q, H)
+            desc = rt.make_desc(dc, chunks_dev, kernel, C, None, k, ws, tables_ready)
+            rt.decode_partial(dc, part, lse, num_partitions=num_partitions, desc=desc)
+            rt.merge_states(part, lse, ind, B, q, H, out_dtype, out=out, out_lse=out_lse)
+        res.append((part, lse, out, out_lse))
+    return res
+
+
+def assert_same_bits(a, b):
+    for x, y in zip(a, b):
+        if x is not None:
+            assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("L", [32768, 49152, 65536, 81920, 98304, 131072])
+def test_single_launch_equals_two_launches_at_every_bench_context(L):
+    """The bench's workload and launch configuration (planner plan, tables read before the dependency wait):
+    one launch, the same bits as the two launches, and the oracle on sampled heads."""
+    case = gen.make_decode_case(2, [L], num_heads=16, block_size=32, dtype="f16")
+    dc = rt.upload(case)
+    plan = nb.mla_plan([L], 16, 1, 32, nb.mla_device_query())
+    chunks = rt.chunks_to_device(plan.chunks)
+    ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
+    nb.mla_reset_counters()
+    fused, plain = both_paths(case, dc, chunks, ind, plan.num_chunks, nb.MLA_KERNEL_TC, plan.cluster_ctas,
+                              plan.clusters_per_chunk, "f16", tables_ready=True)
+    ctr = nb.mla_get_counters()
+    assert ctr[nb.CTR_DECODE_FUSED] == 1 and ctr[nb.CTR_PARTIAL_TC] == 2 and ctr[nb.CTR_MERGE] == 1
+    assert_same_bits(fused, plain)
+    # fp32 output of the fused path against the oracle
+    out32 = torch.empty((1, 1, 16, 512), device="cuda")
+    part, lse = rt.alloc_partials(plan.num_chunks, 1, 16)
+    ws = rt.alloc_decode_workspace(1, plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, 16)
+    rt.decode(dc, part, lse, ind, out32, kernel=nb.MLA_KERNEL_TC, cluster=plan.cluster_ctas, chunks_dev=chunks,
+              subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True)
+    heads = [0, 7, 15]
+    ref, _ = orc.unsplit(case, heads=heads)
+    assert_close(out32.cpu().numpy()[:, :, heads], ref[:, :, heads], f"fused L={L}")
+    assert torch.equal(out32.to(torch.float16), fused[2])
+
+
+@pytest.mark.parametrize("C,bs,out_dtype", [(2, 16, "f32"), (4, 32, "f16"), (8, 64, "bf16"), (16, 32, "f32")])
+def test_single_launch_ragged_batch_with_empty_requests(C, bs, out_dtype):
+    """A batch of ragged requests (empty, one token, partial pages, several tiles) on the uniform split: the
+    same bits as the two launches, the oracle on every head, an empty request merges to zeros."""
+    lens = [0, 1, 31, 33, 127, 129, 1000, 4133]
+    case = gen.make_decode_case(31, lens, num_heads=16, block_size=bs, dtype="f16")
+    dc = rt.upload(case)
+    P, B = 3, len(lens)
+    ind = rt.uniform_indptr(B, P)
+    fused, plain = both_paths(case, dc, None, ind, B * P, nb.MLA_KERNEL_TC, C, 1, out_dtype, num_partitions=P)
+    assert_same_bits(fused, plain)
+    ref, ref_lse = orc.unsplit(case)
+    out = fused[2].float().cpu().numpy()
+    assert np.all(out[0] == 0) and np.all(np.isneginf(fused[3].cpu().numpy()[0]))
+    if out_dtype == "f32":
+        assert_close(out[1:], ref[1:], f"ragged C={C} bs={bs}")
+        got_lse = fused[3].cpu().numpy()[1:]
+        assert np.abs(got_lse - ref_lse[1:]).max() <= MAX_ABS
+
+
+@pytest.mark.parametrize("L,P,C,k,bs", [(20017, 3, 2, 5, 16), (65536, 6, 4, 6, 32), (9000, 2, 16, 2, 32)])
+def test_single_launch_with_partitions_spread_over_clusters(L, P, C, k, bs):
+    """Partitions spread over k clusters (the workspace merge of each chunk, then the request merge, all in
+    one launch), two requests so both request tickets are exercised."""
+    case = gen.make_decode_case(32, [L, L // 3], num_heads=16, block_size=bs, dtype="f16")
+    dc = rt.upload(case)
+    ind = rt.uniform_indptr(2, P)
+    fused, plain = both_paths(case, dc, None, ind, 2 * P, nb.MLA_KERNEL_TC, C, k, "f32", num_partitions=P)
+    assert_same_bits(fused, plain)
+    ref, _ = orc.unsplit(case)
+    assert_close(fused[2].cpu().numpy(), ref, f"spread L={L} P={P} C={C} k={k}")
+
+
+def test_single_launch_bitwise_reproducible_and_workspace_reused():
+    case = gen.make_decode_case(33, [131072], num_heads=16, block_size=32, dtype="f16")
+    dc = rt.upload(case)
+    plan = nb.mla_plan([131072], 16, 1, 32, nb.mla_device_query())
+    chunks = rt.chunks_to_device(plan.chunks)
+    ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
+    ws = rt.alloc_decode_workspace(1, plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, 16)
+    outs = []
+    for _ in range(3):
+        part, lse = rt.alloc_partials(plan.num_chunks, 1, 16)
+        out = torch.empty((1, 1, 16, 512), dtype=torch.float16, device="cuda")
+        rt.decode(dc, part, lse, ind, out, kernel=nb.MLA_KERNEL_TC, cluster=plan.cluster_ctas, chunks_dev=chunks,
+                  subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True)
+        outs.append((part, lse, out))
+    for other in outs[1:]:
+        assert_same_bits(outs[0], other)
+    torch.cuda.synchronize()
+    assert int(ws.view(torch.int32)[: 16].abs().sum()) == 0  # request tickets back at zero
+
+
+@pytest.mark.parametrize("H,dtype,kernel", [(128, "bf16", nb.MLA_KERNEL_TC), (16, "f16", nb.MLA_KERNEL_SIMT),
+                                            (16, "bf16", nb.MLA_KERNEL_TC)])
+def test_decode_without_the_fused_merge_is_the_two_launches(H, dtype, kernel):
+    """Kernels without the fused merge: mla_decode enqueues the partial kernel and the merge kernel."""
+    case = gen.make_decode_case(34, [3000, 700], num_heads=H, block_size=64 if dtype == "bf16" else 32, dtype=dtype,
+                                latent_std=0.5)
+    dc = rt.upload(case)
+    ind = rt.uniform_indptr(2, 2)
+    nb.mla_reset_counters()
+    fused, plain = both_paths(case, dc, None, ind, 4, kernel, 2, 1, "f32", num_partitions=2)
+    ctr = nb.mla_get_counters()
+    assert ctr[nb.CTR_DECODE_FUSED] == 0 and ctr[nb.CTR_MERGE] == 2
+    assert_same_bits(fused, plain)

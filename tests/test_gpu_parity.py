@@ -403,17 +403,39 @@ def test_verify_windows_over_segments(q_len):
     assert np.abs(bad - ref).max() > 3 * MAX_ABS
 
 
+def run_planned_segments(seg):
+    """A verify window as the bench runs it: every segment planned by mla_plan (its own partitions, cluster
+    size and row groups), one partial launch per segment into request-major slots, one merge."""
+    base = seg.base
+    B, q_len, H = base.num_requests, base.q_len, base.num_heads
+    sp = rt.plan_segments(seg, nb.mla_device_query())
+    part, lse = rt.alloc_partials(sp.num_slots, q_len, H)
+    part.fill_(float("nan"))
+    dc0 = rt.upload(base)
+    for s, table, plan in zip(seg.segments, sp.chunk_tables, sp.plans):
+        dc = rt.upload(s, ckv=dc0.ckv, kpe=dc0.kpe)
+        ws = rt.alloc_workspace(plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, q_len, H)
+        rt.decode_partial(dc, part, lse, chunks_dev=table, kernel=nb.MLA_KERNEL_TC, cluster=plan.cluster_ctas,
+                          subs=plan.clusters_per_chunk, workspace=ws)
+    out_lse = torch.empty((B, q_len, H), dtype=torch.float32, device="cuda")
+    out = rt.merge_states(part, lse, sp.o_indptr, B, q_len, H, "f32", out_lse=out_lse)
+    return out, out_lse, sp
+
+
 @pytest.mark.parametrize("q_len", [4, 9, 16, 32])
 def test_verify_window_full_prefix_sampled_heads(q_len):
-    """The verify-window workload at full size: prefix 81920 tokens in 3 segments plus the causal window tail,
-    B=4, every window length, on sampled heads whose rows fall in different TMEM lane quadrants."""
+    """The verify-window workload at full size, in the bench's launch configuration: prefix 81920 tokens in 3
+    segments plus the causal window tail, B=4, every window length (a window of 16 or 32 rows over 16 heads
+    runs on the 128-row pair kernel in 2 or 4 row groups), on sampled heads whose rows fall in different TMEM
+    lane quadrants."""
     seg = gen.make_segmented_case(5, B=4, q_len=q_len, num_heads=16, block_size=32)
     heads = [0, 9] if q_len == 32 else [0, 7, 9, 14]
     ref, ref_lse = orc.unsplit(gen.concat_segments(seg), heads=heads)
-    out, part, lse, ind, _ = run_segments(seg, q_len, cluster=4)
+    nb.mla_reset_counters()
+    out, out_lse, sp = run_planned_segments(seg)
+    assert nb.mla_get_counters()[nb.CTR_PARTIAL_TC] == 4
+    assert all(p.num_chunks >= 4 for p in sp.plans[:3])  # every prefix segment split over the requests
     assert_close(out.cpu().numpy()[:, :, heads], ref[:, :, heads], f"full prefix q_len={q_len}")
-    out_lse = torch.empty((4, q_len, 16), dtype=torch.float32, device="cuda")
-    rt.merge_states(part, lse, ind, 4, q_len, 16, "f32", out_lse=out_lse)
     assert_lse_close(out_lse.cpu().numpy()[:, :, heads], ref_lse[:, :, heads], f"full prefix lse q_len={q_len}")
 
 
