@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--profile-many-heads", action="store_true",
                     help="profiling case: only --launches plain layer calls of the many-head workload, then exit")
     ap.add_argument("--launches", type=int, default=5)
+    ap.add_argument("--skip-extra", action="store_true",
+                    help="leave out the verify-window and batch-grid timings (reported beside the headline)")
     return ap.parse_args()
 
 
@@ -166,6 +168,137 @@ def many_heads_call(nb, rt, torch, stream=None):
 
     tokens = int(case.context_lens.sum())
     return call, plan, tokens
+
+
+# verify windows (the tensor-core-bound shape at 16 and 32 rows): B=4 requests, H=16, fp16, block 32, a
+# prefix of 81920 tokens in 3 non-contiguous segments (40960 / 28672 / 12288) and the window's own q_len
+# tokens as a causal tail segment; every segment planned on its own, all merged per request by LSE
+VW_B, VW_SEED, VW_QLENS = 4, 5, [4, 9, 16, 32]
+VERIFY = "mla_verify_windows_B4_H16_fp16_bs32_prefix81920_in_3_segments"
+
+
+def window_work(seg):
+    """(flops, bytes) one window call must do: every visible (row, token) pair, and the latent stream plus
+    tables, queries, partials written and read back, and the output."""
+    segs = seg.segments
+    B, q, Hh = segs[0].num_requests, segs[0].q_len, segs[0].num_heads
+    prefix = sum(int(s.context_lens[0]) for s in segs[:-1])
+    pairs = B * sum(prefix + i + 1 for i in range(q))  # row i of the window sees the prefix and i + 1 window tokens
+    flops = pairs * Hh * 2 * (576 + 512)
+    tokens = B * (prefix + q)
+    pages = sum(-(-int(L) // s.block_size) for s in segs for L in s.context_lens)
+    return flops, tokens * LATENT_BYTES_PER_TOKEN + pages * 4 + B * q * Hh * (576 * 2 + 512 * 2)
+
+
+def time_verify_windows(nb, rt, torch, stream, peaks, reps=5):
+    from mla_split_kv_gb300 import inputs as gen
+
+    dev = nb.mla_device_query()
+    full = gen.make_segmented_case(VW_SEED, B=VW_B, q_len=max(VW_QLENS), num_heads=H, block_size=BS)
+    dc_base = rt.upload(full.base)  # the cache pool, shared by every window length
+    rows = []
+    for q in VW_QLENS:
+        seg = gen.window_view(full, q)
+        sp = rt.plan_segments(seg, dev)
+        part, lse = rt.alloc_partials(sp.num_slots, q, H)
+        out = torch.empty((VW_B, q, H, 512), dtype=torch.float16, device="cuda")
+        launches = []
+        for s, table, plan in zip(seg.segments, sp.chunk_tables, sp.plans):
+            dc = rt.upload(s, ckv=dc_base.ckv, kpe=dc_base.kpe)
+            ws = rt.alloc_workspace(plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, q, H)
+            desc = rt.make_desc(dc, table, nb.MLA_KERNEL_TC, plan.cluster_ctas, stream, plan.clusters_per_chunk, ws,
+                                tables_ready=True)
+            launches.append((dc, desc))
+
+        def call():
+            for dc, desc in launches:
+                rt.decode_partial(dc, part, lse, desc=desc)
+            rt.merge_states(part, lse, sp.o_indptr, VW_B, q, H, "f16", out=out, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                call()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                call()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        with torch.cuda.stream(stream):
+            g.replay()
+            e[0].record(stream)
+            g.replay()
+            e[1].record(stream)
+        stream.synchronize()
+        us = e[0].elapsed_time(e[1]) * 1e3 / reps
+        flops, nbytes = window_work(seg)
+        tf = flops / (us * 1e-6) / 1e12
+        gbs = nbytes / (us * 1e-6) / 1e9
+        frac_t = tf / peaks["tensor_tflops"]
+        frac_h = gbs / peaks["hbm_gbs"]
+        rows.append({"q_len": q, "us_per_call": round(us, 3), "tflops": round(tf, 1), "hbm_gbs": round(gbs, 1),
+                     "bound": "tensor" if flops / nbytes > peaks["tensor_tflops"] * 1e3 / peaks["hbm_gbs"] else "hbm",
+                     "frac_tensor": round(frac_t, 4), "frac_hbm": round(frac_h, 4),
+                     "flop_per_byte": round(flops / nbytes, 1),
+                     "partitions_per_segment": [p.num_chunks for p in sp.plans],
+                     "launches": len(launches) + 1})
+    return {"workload": VERIFY, "per_q_len": rows,
+            "peaks": {"tensor_tflops": peaks["tensor_tflops"], "hbm_gbs": peaks["hbm_gbs"],
+                      "source": peaks["source"]},
+            "note": "each window call: one partial launch per segment (3 prefix segments + the causal window tail) "
+                    "and one merge; the 377 MB prefix cache is larger than L2; fp16 tensor peak = the measured bf16 "
+                    "dense peak (the same nominal rate)"}
+
+
+# the batch grid of the many-head comparison (heads x batch), at an 8192-token context per request
+GRID_HEADS, GRID_BATCH, GRID_CTX = [16, 64, 128], [1, 8, 32], 8192
+GRID = "mla_decode_grid_H16_64_128_x_B1_8_32_ctx8192"
+
+
+def time_batch_grid(nb, rt, torch, stream, reps=10):
+    from mla_split_kv_gb300 import inputs as gen
+
+    dev = nb.mla_device_query()
+    rows = []
+    for Hh in GRID_HEADS:
+        dtype = "bf16" if Hh == 128 else "f16"
+        for B in GRID_BATCH:
+            case = gen.make_decode_case(40 + Hh + B, [GRID_CTX] * B, num_heads=Hh, block_size=BS if dtype == "f16" else 64,
+                                        dtype=dtype, latent_std=0.5 if dtype == "bf16" else 1.0)
+            plan = nb.mla_plan(case.context_lens.tolist(), Hh, 1, case.block_size, dev, max_partitions=64, dtype=dtype)
+            dc = rt.upload(case)
+            chunks = rt.chunks_to_device(plan.chunks)
+            part, lse = rt.alloc_partials(plan.num_chunks, 1, Hh)
+            ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
+            out = torch.empty((B, 1, Hh, 512), dtype=rt.TORCH_DTYPE[dtype], device="cuda")
+            ws = rt.alloc_decode_workspace(B, plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, Hh)
+            desc = rt.make_desc(dc, chunks, nb.MLA_KERNEL_TC, plan.cluster_ctas, stream, plan.clusters_per_chunk, ws,
+                                tables_ready=True)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    rt.decode(dc, part, lse, ind, out, desc=desc)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(reps):
+                    rt.decode(dc, part, lse, ind, out, desc=desc)
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            with torch.cuda.stream(stream):
+                g.replay()
+                e[0].record(stream)
+                g.replay()
+                e[1].record(stream)
+            stream.synchronize()
+            us = e[0].elapsed_time(e[1]) * 1e3 / reps
+            tokens = B * GRID_CTX
+            rows.append({"H": Hh, "B": B, "dtype": dtype, "us_per_call": round(us, 3),
+                         "hbm_gbs": round(tokens * LATENT_BYTES_PER_TOKEN / (us * 1e-6) / 1e9, 1),
+                         "tflops": round(tokens * Hh * 2 * (576 + 512) / (us * 1e-6) / 1e12, 1),
+                         "partitions": plan.num_chunks, "cluster": plan.cluster_ctas,
+                         "clusters_per_partition": plan.clusters_per_chunk,
+                         "l2_resident": tokens * LATENT_BYTES_PER_TOKEN < 129e6})
+    return {"workload": GRID, "cells": rows,
+            "note": "repeats of one cache per cell; caches smaller than L2 (129 MB) are partly L2-resident"}
 
 
 def oracle_timing(cases, steps, cores, budget_s=30.0):
@@ -737,6 +870,15 @@ def run_ours(args, rank, world):
     st, code = nb.mla_check_device_errors(stream.cuda_stream)
     if st != nb.MLA_OK:
         raise RuntimeError(f"device error word {code:#x} in the many-head timing")
+    peaks = measured_peaks()
+    tpk = {"hbm_gbs": float(peaks["hbm_gbs"]), "tensor_tflops": float(peaks["bf16_tflops"]), "source": "measured"} \
+        if peaks and peaks.get("hbm_gbs") and peaks.get("bf16_tflops") else \
+        {"hbm_gbs": 6800.0, "tensor_tflops": 1900.0, "source": "fallback"}
+    verify = time_verify_windows(nb, rt, torch, stream, tpk) if not args.skip_extra else None
+    grid = time_batch_grid(nb, rt, torch, stream) if not args.skip_extra else None
+    st, code = nb.mla_check_device_errors(stream.cuda_stream)
+    if st != nb.MLA_OK:
+        raise RuntimeError(f"device error word {code:#x} in the verify-window / batch-grid timing")
 
     n_calls = K * len(calls)
     value_us = job_us_per_call(total_ms, n_calls, world)
@@ -770,6 +912,8 @@ def run_ours(args, rank, world):
         "trials": trials,
         "two_launch_us": round(two_launch_us, 3),
         "many_heads": many_heads,
+        "verify_windows": verify,
+        "batch_grid": grid,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(kname, sum(CONTEXTS) / len(CONTEXTS)),

@@ -355,6 +355,49 @@ uint64_t mla_decode_workspace_bytes(int32_t num_requests, int32_t num_chunks, in
                                     int32_t cluster_ctas, int32_t q_len, int32_t num_heads);
 
 /*
+ * mla_cache_append -- write each request's newest tokens into the paged
+ * cache, the step before attention in a decode layer call ("[kernel] Wire MLA
+ * split-KV decode", *Bench*: the wrapper's cache write). Token i of the q_len
+ * new tokens of request b goes to logical position t = context_lens[b] -
+ * q_len + i (context_lens already counts the new tokens, as with a causal
+ * window: its rows are the last q_len tokens), cache row
+ * block_table[b, t / bs] * bs + t % bs. Positions t < 0 are not written. A
+ * page outside the table row or the pool is not written and raises
+ * MLA_ERR_DEVICE_CHECK at the next mla_check_device_errors.
+ *
+ * ckv_new  : device [B, q_len, 512] 16-bit (the caches' dtype), 16-byte aligned
+ * kpe_new  : device [B, q_len, 64]  16-bit, 16-byte aligned
+ * block_table, context_lens: as for mla_decode_partial
+ * ckv_cache, kpe_cache: device, as for mla_decode_partial (written)
+ * Returns MLA_OK once the copy kernel is enqueued.
+ */
+mla_status_t mla_cache_append(const void* ckv_new, const void* kpe_new, const int32_t* block_table,
+                              const int32_t* context_lens, int32_t B, int32_t q_len, int32_t block_size,
+                              int32_t num_blocks, int32_t max_blocks_per_req, void* ckv_cache, void* kpe_cache,
+                              void* stream);
+
+/*
+ * mla_merge_unembed -- mla_merge_states followed by the output side of the
+ * fold, the step after attention ("feat(core): matrix-absorbed MLA decode over
+ * a compressed-latent KV cache", *What changed*: W_UV^T [1, H, r, v_head];
+ * "[kernel] Wire MLA split-KV decode", *Bench*: the wrapper's unembed):
+ *   out_v[b, i, h, :] = merged[b, i, h, :] @ W_UV^T[h]
+ * where merged is what mla_merge_states computes in fp32 (the same bits; it
+ * is never rounded here), the product accumulates in fp32 over d = 0 .. 511
+ * in that order, and the result is rounded once to out_dtype. out_lse (NULL
+ * allowed) receives the merged LSE.
+ *
+ * w_uv_t : device [H, 512, v_head] of w_dtype (MLA_F16 / MLA_BF16), 16-byte
+ *          aligned; v_head a multiple of 32, at most 512
+ * out    : device [B, q_len, H, v_head] of out_dtype (MLA_F16 / BF16 / F32)
+ * partials, lse, o_indptr: as for mla_merge_states
+ * A programmatic dependent launch, like mla_merge_states.
+ */
+mla_status_t mla_merge_unembed(const float* partials, const float* lse, const int32_t* o_indptr, int32_t B,
+                               int32_t q_len, int32_t num_heads, const void* w_uv_t, int32_t w_dtype, int32_t v_head,
+                               void* out, int32_t out_dtype, float* out_lse, void* stream);
+
+/*
  * mla_check_device_errors -- synchronize `stream`, read and clear the device
  * error word the kernels set (bounded-wait timeout, out-of-range page id).
  * *code_out (nullable) receives the raw word. When the word was set it also
@@ -399,7 +442,8 @@ mla_status_t mla_selfcheck(float* max_abs_err);
 #define MLA_CTR_REJECTED 3
 #define MLA_CTR_CTAS 4 /* CTAs launched by partial kernels */
 #define MLA_CTR_DECODE_FUSED 5 /* mla_decode calls that ran as one launch */
-#define MLA_NUM_COUNTERS 6
+#define MLA_CTR_WRAP 6 /* mla_cache_append and mla_merge_unembed launches */
+#define MLA_NUM_COUNTERS 7
 /* mla_get_counters -- copy min(n, MLA_NUM_COUNTERS) counters to out (host). */
 void mla_get_counters(uint64_t* out, int32_t n);
 void mla_reset_counters(void);

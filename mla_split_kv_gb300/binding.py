@@ -27,8 +27,8 @@ MLA_F16, MLA_BF16, MLA_F32 = 0, 1, 2
 MLA_STATIC_WORKSPACE_BYTES = 4 * 1024 * 1024
 MLA_KERNEL_AUTO, MLA_KERNEL_SIMT, MLA_KERNEL_TC = 0, 1, 2
 
-CTR_PARTIAL_SIMT, CTR_PARTIAL_TC, CTR_MERGE, CTR_REJECTED, CTR_CTAS, CTR_DECODE_FUSED = range(6)
-NUM_COUNTERS = 6
+CTR_PARTIAL_SIMT, CTR_PARTIAL_TC, CTR_MERGE, CTR_REJECTED, CTR_CTAS, CTR_DECODE_FUSED, CTR_WRAP = range(7)
+NUM_COUNTERS = 7
 
 DTYPE_CODES = {"f16": MLA_F16, "bf16": MLA_BF16, "f32": MLA_F32}
 
@@ -113,6 +113,10 @@ def load() -> ctypes.CDLL:
     lib.mla_decode.restype = i32
     lib.mla_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.mla_decode_workspace_bytes.restype = u64
+    lib.mla_cache_append.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.mla_cache_append.restype = i32
+    lib.mla_merge_unembed.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32, i32, vp, i32, vp, vp]
+    lib.mla_merge_unembed.restype = i32
     lib.mla_merge_states.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32, vp, vp]
     lib.mla_merge_states.restype = i32
     lib.mla_check_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -241,6 +245,20 @@ def mla_merge_states(partials: int, lse: int, o_indptr: int, B: int, q_len: int,
                      out_dtype: int, out_lse: Optional[int], stream: Optional[int]) -> None:
     _check(load().mla_merge_states(partials, lse, o_indptr, B, q_len, num_heads, out, out_dtype,
                                    out_lse or None, stream or None), "mla_merge_states")
+
+
+def mla_cache_append(ckv_new: int, kpe_new: int, block_table: int, context_lens: int, B: int, q_len: int,
+                     block_size: int, num_blocks: int, max_blocks_per_req: int, ckv_cache: int, kpe_cache: int,
+                     stream: Optional[int]) -> None:
+    _check(load().mla_cache_append(ckv_new, kpe_new, block_table, context_lens, B, q_len, block_size, num_blocks,
+                                   max_blocks_per_req, ckv_cache, kpe_cache, stream or None), "mla_cache_append")
+
+
+def mla_merge_unembed(partials: int, lse: int, o_indptr: int, B: int, q_len: int, num_heads: int, w_uv_t: int,
+                      w_dtype: int, v_head: int, out: int, out_dtype: int, out_lse: Optional[int],
+                      stream: Optional[int]) -> None:
+    _check(load().mla_merge_unembed(partials, lse, o_indptr, B, q_len, num_heads, w_uv_t, w_dtype, v_head, out,
+                                    out_dtype, out_lse or None, stream or None), "mla_merge_unembed")
 
 
 def mla_check_device_errors(stream: Optional[int] = None):

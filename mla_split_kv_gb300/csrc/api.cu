@@ -511,13 +511,78 @@ mla_status_t mla_merge_states(const float* partials, const float* lse, const int
   return MLA_OK;
 }
 
+mla_status_t mla_cache_append(const void* ckv_new, const void* kpe_new, const int32_t* block_table,
+                              const int32_t* context_lens, int32_t B, int32_t q_len, int32_t block_size,
+                              int32_t num_blocks, int32_t max_blocks_per_req, void* ckv_cache, void* kpe_cache,
+                              void* stream) {
+  if (ckv_new == nullptr || kpe_new == nullptr || block_table == nullptr || context_lens == nullptr ||
+      ckv_cache == nullptr || kpe_cache == nullptr)
+    return reject(MLA_ERR_INVALID_ARG);
+  if (B < 1 || B > (1 << 24) || num_blocks < 1 || max_blocks_per_req < 1) return reject(MLA_ERR_INVALID_ARG);
+  if (q_len < 1 || q_len > MLA_MAX_Q_LEN) return reject(MLA_ERR_UNSUPPORTED);
+  if (block_size != 16 && block_size != 32 && block_size != 64) return reject(MLA_ERR_UNSUPPORTED);
+  if (!aligned(ckv_new, 16) || !aligned(kpe_new, 16) || !aligned(ckv_cache, 16) || !aligned(kpe_cache, 16) ||
+      !aligned(block_table, 4) || !aligned(context_lens, 4))
+    return reject(MLA_ERR_INVALID_ARG);
+  mla::AppendParams p;
+  p.ckv_new = static_cast<const uint16_t*>(ckv_new);
+  p.kpe_new = static_cast<const uint16_t*>(kpe_new);
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.ckv = static_cast<uint16_t*>(ckv_cache);
+  p.kpe = static_cast<uint16_t*>(kpe_cache);
+  p.B = B;
+  p.q_len = q_len;
+  p.bs = block_size;
+  p.max_blocks = max_blocks_per_req;
+  p.num_blocks = num_blocks;
+  if (mla::launch_cache_append(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+  g_counters[MLA_CTR_WRAP].fetch_add(1, std::memory_order_relaxed);
+  return MLA_OK;
+}
+
+mla_status_t mla_merge_unembed(const float* partials, const float* lse, const int32_t* o_indptr, int32_t B,
+                               int32_t q_len, int32_t num_heads, const void* w_uv_t, int32_t w_dtype, int32_t v_head,
+                               void* out, int32_t out_dtype, float* out_lse, void* stream) {
+  if (partials == nullptr || lse == nullptr || o_indptr == nullptr || w_uv_t == nullptr || out == nullptr)
+    return reject(MLA_ERR_INVALID_ARG);
+  if (B < 1 || B > (1 << 24)) return reject(MLA_ERR_INVALID_ARG);
+  if (!valid_heads(num_heads) || q_len < 1 || q_len > MLA_MAX_Q_LEN) return reject(MLA_ERR_UNSUPPORTED);
+  if (v_head < 32 || v_head > 512 || v_head % 32 != 0) return reject(MLA_ERR_UNSUPPORTED);
+  if (w_dtype != MLA_F16 && w_dtype != MLA_BF16) return reject(MLA_ERR_UNSUPPORTED);
+  if (out_dtype != MLA_F16 && out_dtype != MLA_BF16 && out_dtype != MLA_F32) return reject(MLA_ERR_UNSUPPORTED);
+  if (static_cast<int64_t>(B) * q_len > 65535LL * 16) return reject(MLA_ERR_UNSUPPORTED);
+  if (!aligned(partials, 16) || !aligned(lse, 4) || !aligned(o_indptr, 4) || !aligned(w_uv_t, 16) ||
+      !aligned(out, 4) || (out_lse != nullptr && !aligned(out_lse, 4)))
+    return reject(MLA_ERR_INVALID_ARG);
+  mla::UnembedParams p;
+  p.partials = partials;
+  p.lse = lse;
+  p.o_indptr = o_indptr;
+  p.w_uv_t = static_cast<const uint16_t*>(w_uv_t);
+  p.out = out;
+  p.out_lse = out_lse;
+  p.B = B;
+  p.q_len = q_len;
+  p.H = num_heads;
+  p.v_head = v_head;
+  p.out_dtype = out_dtype;
+  if (mla::launch_merge_unembed(p, w_dtype == MLA_BF16, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  g_counters[MLA_CTR_WRAP].fetch_add(1, std::memory_order_relaxed);
+  return MLA_OK;
+}
+
 mla_status_t mla_check_device_errors(void* stream, uint32_t* code_out) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
-  uint32_t a = 0, b = 0, c = 0, e = 0;
+  uint32_t a = 0, b = 0, c = 0, e = 0, f = 0;
   if (mla::simt_read_clear_error(&a) != cudaSuccess || mla::tc_read_clear_error(&b) != cudaSuccess ||
-      mla::tc128_read_clear_error(&c) != cudaSuccess || mla::mh_read_clear_error(&e) != cudaSuccess)
+      mla::tc128_read_clear_error(&c) != cudaSuccess || mla::mh_read_clear_error(&e) != cudaSuccess ||
+      mla::wrap_read_clear_error(&f) != cudaSuccess)
     return MLA_ERR_CUDA;
-  const uint32_t code = a | b | c | e;
+  const uint32_t code = a | b | c | e | f;
   if (code_out != nullptr) *code_out = code;
   if (code != 0 && !clear_static_workspace()) return MLA_ERR_CUDA;
   if (code & mla::MLA_DEVERR_TIMEOUT) return MLA_ERR_TIMEOUT;

@@ -633,73 +633,91 @@ __device__ __forceinline__ void cluster_combine(const PartialParams& p, const Ct
   cluster_combine_to(p, w, ostage, mst, lst, tid, nthreads, p.partials, p.lse, static_cast<long long>(w.slot));
 }
 
-// Single-launch decode: the final merge of request b's chunk partials (slots lo .. hi-1,
-// normalized, base-2 LSE in lse_src) for columns [col0, col0 + ncols) of every row, into
-// p.out (p.out_dtype) and, with write_lse, p.out_lse. It is the merge kernel's arithmetic in
-// the merge kernel's order (maximum LSE, weights 2^(lse - M) with -inf giving 0, the weight
-// sum and the fused multiply-adds in slot order, one division, one rounding), so the output
-// is the same bits as mla_merge_states on the same partials. The partials were written by
-// other CTAs (ordered before this CTA's ticket by their fences), so they are read through L2.
+// The merge of n partials (slots lo .. lo+n-1, normalized, base-2 LSE) for row r and the four
+// columns [c, c + 4): the merge kernel's arithmetic in the merge kernel's order (the maximum LSE
+// M, weights 2^(lse - M) with -inf giving 0, the weight sum and the fused multiply-adds in slot
+// order, one division per column), so every merge built on it gives the bits mla_merge_states
+// gives. Writes the normalized values (0 when every LSE is -inf), M and the weight sum.
+// Partials and LSE written by other CTAs of the same grid are read through L2 (ld.global.cg).
+__device__ __forceinline__ float4 merge_cols4(const float* partials, const float* lse_src, int lo, int n, int rows,
+                                              int r, int c, bool values, float* M_out, float* den_out) {
+  const long long stride = static_cast<long long>(rows) * kRank;  // one partial slot
+  const float* lrow = lse_src + static_cast<long long>(lo) * rows + r;
+  const float* vcol = partials + static_cast<long long>(lo) * stride + static_cast<long long>(r) * kRank + c;
+  float M = -INFINITY;
+  for (int j = 0; j < n; ++j) M = fmaxf(M, __ldcg(lrow + static_cast<long long>(j) * rows));
+  float den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
+    for (int j0 = 0; j0 < n; j0 += 8) {
+      float lj[8];
+      float4 v[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const bool in = j0 + jj < n;
+        lj[jj] = in ? __ldcg(lrow + static_cast<long long>(j0 + jj) * rows) : -INFINITY;
+        v[jj] = (in && values) ? __ldcg(reinterpret_cast<const float4*>(vcol + (j0 + jj) * stride))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        if (j0 + jj < n) {
+          const float wj = (lj[jj] == -INFINITY) ? 0.f : exp2f(lj[jj] - M);
+          den += wj;
+          acc.x = fmaf(wj, v[jj].x, acc.x);
+          acc.y = fmaf(wj, v[jj].y, acc.y);
+          acc.z = fmaf(wj, v[jj].z, acc.z);
+          acc.w = fmaf(wj, v[jj].w, acc.w);
+        }
+      }
+    }
+    acc = make_float4(acc.x / den, acc.y / den, acc.z / den, acc.w / den);
+  }
+  *M_out = M;
+  *den_out = den;
+  return acc;
+}
+
+// The merged log2 LSE from merge_cols4's maximum and weight sum.
+__device__ __forceinline__ float merged_lse(float M, float den) { return (M == -INFINITY) ? -INFINITY : M + log2f(den); }
+
+// Four values rounded once to the output type (2: fp32, 1: bf16, 0: fp16) at element `off` of `out`.
+__device__ __forceinline__ void store_out4(void* out, int32_t out_dtype, long long off, float4 acc) {
+  if (out_dtype == 2) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + off) = acc;
+    return;
+  }
+  const bool bf = (out_dtype == 1);
+  const float f[4] = {acc.x, acc.y, acc.z, acc.w};
+  uint16_t h[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) h[j] = bf ? f2h<true>(f[j]) : f2h<false>(f[j]);
+  uint2 packed;
+  packed.x = static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16);
+  packed.y = static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[3]) << 16);
+  *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + off) = packed;
+}
+
+// Single-launch decode: the final merge of request b's chunk partials (slots lo .. hi-1) for
+// columns [col0, col0 + ncols) of every row, into p.out (p.out_dtype) and, with write_lse,
+// p.out_lse; the partials were written by other CTAs, ordered before this CTA's ticket by their
+// fences.
 __device__ __forceinline__ void request_merge(const PartialParams& p, int b, int lo, int hi, int col0, int ncols,
                                               bool write_lse, const float* lse_src, int tid, int nthreads) {
   const int rows = p.q_len * p.H;
-  const int n = hi - lo;
   const int n4 = ncols / 4;
   const int items = rows * n4 + (write_lse ? rows : 0);
-  const long long stride = static_cast<long long>(rows) * kRank;  // one partial slot
   for (int idx = tid; idx < items; idx += nthreads) {
     const bool is_lse = idx >= rows * n4;
     const int r = is_lse ? idx - rows * n4 : idx / n4;
     const int c = col0 + (is_lse ? 0 : (idx % n4) * 4);
-    const float* lrow = lse_src + static_cast<long long>(lo) * rows + r;
-    const float* vcol = p.partials + static_cast<long long>(lo) * stride + static_cast<long long>(r) * kRank + c;
-    float M = -INFINITY;
-    for (int j = 0; j < n; ++j) M = fmaxf(M, __ldcg(lrow + static_cast<long long>(j) * rows));
-    float den = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-      for (int j0 = 0; j0 < n; j0 += 8) {
-        float lj[8];
-        float4 v[8];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const bool in = j0 + jj < n;
-          lj[jj] = in ? __ldcg(lrow + static_cast<long long>(j0 + jj) * rows) : -INFINITY;
-          v[jj] = (in && !is_lse) ? __ldcg(reinterpret_cast<const float4*>(vcol + (j0 + jj) * stride))
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          if (j0 + jj < n) {
-            const float wj = (lj[jj] == -INFINITY) ? 0.f : exp2f(lj[jj] - M);
-            den += wj;
-            acc.x = fmaf(wj, v[jj].x, acc.x);
-            acc.y = fmaf(wj, v[jj].y, acc.y);
-            acc.z = fmaf(wj, v[jj].z, acc.z);
-            acc.w = fmaf(wj, v[jj].w, acc.w);
-          }
-        }
-      }
-      acc = make_float4(acc.x / den, acc.y / den, acc.z / den, acc.w / den);
-    }
+    float M, den;
+    const float4 acc = merge_cols4(p.partials, lse_src, lo, hi - lo, rows, r, c, !is_lse, &M, &den);
     const long long br = static_cast<long long>(b) * rows + r;
     if (is_lse) {
-      if (p.out_lse != nullptr) p.out_lse[br] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
-      continue;
-    }
-    const long long o_off = br * kRank + c;
-    if (p.out_dtype == 2) {
-      *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o_off) = acc;
+      if (p.out_lse != nullptr) p.out_lse[br] = merged_lse(M, den);
     } else {
-      const bool bf = (p.out_dtype == 1);
-      const float f[4] = {acc.x, acc.y, acc.z, acc.w};
-      uint16_t h[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) h[j] = bf ? f2h<true>(f[j]) : f2h<false>(f[j]);
-      uint2 packed;
-      packed.x = static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16);
-      packed.y = static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[3]) << 16);
-      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + o_off) = packed;
+      store_out4(p.out, p.out_dtype, br * kRank + c, acc);
     }
   }
 }

@@ -67,6 +67,29 @@ struct MergeParams {
   int32_t out_dtype;
 };
 
+// The cache write of a layer call: token i of request b's q_len new tokens goes to logical
+// position context_lens[b] - q_len + i.
+struct AppendParams {
+  const uint16_t* ckv_new;     // [B, q_len, 512]
+  const uint16_t* kpe_new;     // [B, q_len, 64]
+  const int32_t* block_table;  // [B, max_blocks]
+  const int32_t* context_lens; // [B]
+  uint16_t* ckv;               // [num_blocks, bs, 512]
+  uint16_t* kpe;               // [num_blocks, bs, 64]
+  int32_t B, q_len, bs, max_blocks, num_blocks;
+};
+
+// Merge of each request's partials, then the unembed W_UV^T of each head.
+struct UnembedParams {
+  const float* partials;       // [N, q_len, H, 512]
+  const float* lse;            // [N, q_len, H]
+  const int32_t* o_indptr;     // [B+1]
+  const uint16_t* w_uv_t;      // [H, 512, v_head]
+  void* out;                   // [B, q_len, H, v_head] of out_dtype
+  float* out_lse;              // [B, q_len, H] or null
+  int32_t B, q_len, H, v_head, out_dtype;
+};
+
 // Launchers return cudaSuccess or the launch error. grid.x = cluster of
 // `cluster` CTAs, grid.y = chunks, grid.z = row groups.
 cudaError_t launch_partial_simt(const CUtensorMap& tm_ckv, const CUtensorMap& tm_kpe, const PartialParams& p,
@@ -100,5 +123,9 @@ cudaError_t simt_read_clear_error(uint32_t* out);
 cudaError_t tc_read_clear_error(uint32_t* out);
 cudaError_t tc128_read_clear_error(uint32_t* out);
 cudaError_t mh_read_clear_error(uint32_t* out);
+cudaError_t wrap_read_clear_error(uint32_t* out);
+
+cudaError_t launch_cache_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_merge_unembed(const UnembedParams& p, bool w_bf16, cudaStream_t stream);
 
 }  // namespace mla

@@ -306,6 +306,50 @@ def decompressed_decode(q_nope, q_pe, W_UK, W_UV_T, ckv_rows, kpe_rows, scale):
 
 
 # ---------------------------------------------------------------------------
+# the steps either side of attention: the cache write and the unembed
+# ---------------------------------------------------------------------------
+
+
+def cache_append(ckv, kpe, block_table, context_lens, ckv_new, kpe_new, block_size):
+    """The paged cache after writing each request's newest tokens.
+
+    Token ``i`` of the ``q_len`` new tokens of request ``b`` is logical
+    position ``t = L_b - q_len + i`` (``context_lens`` already counts the new
+    tokens, the convention of the causal window: the window's rows are the
+    last ``q_len`` tokens of the request), stored at the physical row of ``t``
+    ("Wire MLA split-KV decode", *Bench*: the wrapper writes the new token's
+    latent into the paged cache before attention). Positions below 0 are not
+    written. Works on the bit patterns; returns new arrays.
+    """
+    ckv = np.array(ckv, copy=True)
+    kpe = np.array(kpe, copy=True)
+    flat_c = ckv.reshape(-1, ckv.shape[-1])
+    flat_k = kpe.reshape(-1, kpe.shape[-1])
+    B, q_len = ckv_new.shape[0], ckv_new.shape[1]
+    for b in range(B):
+        L = int(context_lens[b])
+        for i in range(q_len):
+            t = L - q_len + i
+            if t < 0:
+                continue
+            row = int(block_table[b][t // block_size]) * block_size + t % block_size
+            flat_c[row] = ckv_new[b, i]
+            flat_k[row] = kpe_new[b, i]
+    return ckv, kpe
+
+
+def merge_unembed(part, lse2, o_indptr, W_UV_T):
+    """Merged latent output taken to the value space: ``merge`` then, per
+    request and row, ``unembed`` (mlxcel PR #995, *What changed*: the output
+    side of the fold, ``W_UV^T [H, r, v_head]``). Returns ``[B, q_len, H, v]``
+    and the merged log2 LSE."""
+    out, out_lse = merge(part, lse2, o_indptr)
+    B, q_len = out.shape[0], out.shape[1]
+    ov = np.stack([np.stack([unembed(out[b, i], W_UV_T) for i in range(q_len)]) for b in range(B)])
+    return ov, out_lse
+
+
+# ---------------------------------------------------------------------------
 # KV-memory accounting (mlxcel PR #995, performance-validation commit)
 # ---------------------------------------------------------------------------
 

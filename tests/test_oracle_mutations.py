@@ -72,6 +72,24 @@ def _indptr_slip(context_lens, parts, block_size):
     return chunks, indptr
 
 
+def _append_one_late(ckv, kpe, block_table, context_lens, ckv_new, kpe_new, block_size):
+    # writes token i at position L - q_len + i + 1 (one past the window's own slot)
+    ckv = np.array(ckv, copy=True)
+    kpe = np.array(kpe, copy=True)
+    fc, fk = ckv.reshape(-1, ckv.shape[-1]), kpe.reshape(-1, kpe.shape[-1])
+    for b in range(ckv_new.shape[0]):
+        for i in range(ckv_new.shape[1]):
+            t = int(context_lens[b]) - ckv_new.shape[1] + i + 1
+            if 0 <= t < len(block_table[b]) * block_size and block_table[b][t // block_size] >= 0:
+                row = int(block_table[b][t // block_size]) * block_size + t % block_size
+                fc[row], fk[row] = ckv_new[b, i], kpe_new[b, i]
+    return ckv, kpe
+
+
+def _unembed_other_side(o_latent, W_UV_T):
+    return np.einsum("hr,hrv->hv", o_latent, W_UV_T[::-1])  # heads' projections swapped
+
+
 MUTATIONS = [
     ("scores", _drop_rope, [pins.test_rope_score_is_additive,
                             lambda: pins.test_matches_torch_sdpa_on_concatenated_keys("f16", 1, False)]),
@@ -86,6 +104,10 @@ MUTATIONS = [
     ("chunk_bounds", _chunks_unaligned, [pins.test_chunk_bounds_examples_and_invariants,
                                          pins.test_plan_chunks_covers_every_token_once_request_major]),
     ("plan_chunks", _indptr_slip, [pins.test_plan_chunks_covers_every_token_once_request_major]),
+    ("cache_append", _append_one_late, [pins.test_cache_append_hand_table,
+                                        pins.test_cache_append_of_the_cached_tail_is_the_identity_and_shifted_rows_are_not]),
+    ("unembed", _unembed_other_side, [pins.test_absorbed_equals_decompressed_and_transposed_fold_does_not,
+                                      pins.test_merge_unembed_is_the_decompressed_decode_of_a_split]),
 ]
 
 

@@ -379,3 +379,71 @@ def test_kv_memory_table_matches_printed_figures():
         == g["printed"]["max_context_tokens_under_16GiB_decompressed"]
     assert orc.max_context_tokens(geo["budget_bytes"], lat, geo["elem_bytes"], st["num_layers"]) \
         == g["printed"]["max_context_tokens_under_16GiB_latent"]
+
+
+# --- the steps either side of attention ----------------------------------------------
+
+def test_cache_append_hand_table():
+    """Two requests, pages of 4 tokens: each new token lands at the hand-computed physical row, nothing else
+    moves, and a position before the start of the context is not written."""
+    ckv = np.zeros((6, 4, 2), dtype=np.uint16)
+    kpe = np.zeros((6, 4, 1), dtype=np.uint16)
+    bt = np.array([[5, 2, -1], [0, 3, 1]], dtype=np.int32)
+    lens = np.array([6, 1], dtype=np.int32)  # request 0: tokens 4, 5 are new; request 1: only token 0 exists
+    new_c = np.array([[[11, 12], [13, 14]], [[21, 22], [23, 24]]], dtype=np.uint16)
+    new_k = np.array([[[1], [2]], [[3], [4]]], dtype=np.uint16)
+    c2, k2 = orc.cache_append(ckv, kpe, bt, lens, new_c, new_k, 4)
+    want_c = ckv.copy()
+    want_k = kpe.copy()
+    want_c[2, 0] = [11, 12]  # b=0, t=4: page 2 (block_table[0][1]), slot 0
+    want_c[2, 1] = [13, 14]  # b=0, t=5: page 2, slot 1
+    want_k[2, 0] = [1]
+    want_k[2, 1] = [2]
+    want_c[0, 0] = [23, 24]  # b=1, i=1 -> t=0: page 0 slot 0; i=0 -> t=-1 is not written
+    want_k[0, 0] = [4]
+    assert np.array_equal(c2, want_c) and np.array_equal(k2, want_k)
+    assert np.array_equal(ckv, np.zeros_like(ckv))  # the inputs are not modified
+
+
+def test_cache_append_of_the_cached_tail_is_the_identity_and_shifted_rows_are_not():
+    case = gen.make_decode_case(17, [77, 130, 31], num_heads=16, q_len=3, block_size=16, dtype="f16")
+    q = 3
+    tail_c = np.stack([case.ckv.reshape(-1, 512)[orc.physical_rows(case.block_table[b], int(L), 16)[-q:]]
+                       for b, L in enumerate(case.context_lens)])
+    tail_k = np.stack([case.kpe.reshape(-1, 64)[orc.physical_rows(case.block_table[b], int(L), 16)[-q:]]
+                       for b, L in enumerate(case.context_lens)])
+    c2, k2 = orc.cache_append(case.ckv, case.kpe, case.block_table, case.context_lens, tail_c, tail_k, 16)
+    assert np.array_equal(c2, case.ckv) and np.array_equal(k2, case.kpe)
+    # the rows one position earlier are different data: writing them there changes the cache
+    prev_c = np.stack([case.ckv.reshape(-1, 512)[orc.physical_rows(case.block_table[b], int(L), 16)[-q - 1:-1]]
+                       for b, L in enumerate(case.context_lens)])
+    c3, _ = orc.cache_append(case.ckv, case.kpe, case.block_table, case.context_lens, prev_c, tail_k, 16)
+    assert not np.array_equal(c3, case.ckv)
+
+
+def test_merge_unembed_is_the_decompressed_decode_of_a_split():
+    """Split the context, merge with the unembed: the decompressed (pre-absorption) decode of the whole
+    context, to 1e-10."""
+    rng = np.random.default_rng(18)
+    H, n, r, v, dr, T = 2, 128, 512, 128, 64, 37
+    q_nope = rng.standard_normal((H, n))
+    q_pe = rng.standard_normal((H, dr))
+    W_UK = rng.standard_normal((H, n, r)) / math.sqrt(r)
+    W_UV_T = rng.standard_normal((H, r, v)) / math.sqrt(r)
+    ckv = rng.standard_normal((T, r))
+    kpe = rng.standard_normal((T, dr))
+    sc = 1 / math.sqrt(192)
+    ref = orc.decompressed_decode(q_nope, q_pe, W_UK, W_UV_T, ckv, kpe, sc)
+    q_abs = orc.absorb_query(q_nope, W_UK)
+    parts, lses = [], []
+    for t0, t1 in [(0, 16), (16, 32), (32, T)]:
+        row = [orc.attend(orc.scores(q_abs[h], q_pe[h], ckv[t0:t1], kpe[t0:t1], sc), ckv[t0:t1]) for h in range(H)]
+        parts.append(np.stack([o for o, _ in row])[None])
+        lses.append(np.array([l for _, l in row])[None])
+    P = np.stack(parts)   # [3, 1, H, r]
+    L = np.stack(lses)    # [3, 1, H]
+    ov, _ = orc.merge_unembed(P, L, [0, 3], W_UV_T)
+    assert np.abs(ov[0, 0] - ref).max() / np.abs(ref).max() < 1e-10
+    # the transposed projection (a shape-valid slip when r == v would not apply; here use the wrong head)
+    bad, _ = orc.merge_unembed(P, L, [0, 3], W_UV_T[::-1])
+    assert np.abs(bad[0, 0] - ref).max() / np.abs(ref).max() > 1e-2
