@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--profile-many-heads", action="store_true",
                     help="profiling case: only --launches plain layer calls of the many-head workload, then exit")
     ap.add_argument("--launches", type=int, default=5)
+    ap.add_argument("--profile-split", default="",
+                    help="profiling case: 'P,C' = a uniform split into P partitions on clusters of C CTAs instead of "
+                         "the planner's plan")
     ap.add_argument("--skip-extra", action="store_true",
                     help="leave out the verify-window and batch-grid timings (reported beside the headline)")
     return ap.parse_args()
@@ -529,17 +532,22 @@ def run_profile_case(args):
     case = make_case(i, L)
     dev = nb.mla_device_query()
     plan = nb.mla_plan([L], H, 1, BS, dev)
+    num_partitions = 1
+    if args.profile_split:  # the library's uniform split instead: P partitions on clusters of C CTAs, one each
+        P, C = (int(x) for x in args.profile_split.split(","))
+        plan = nb.Plan([(0, 0, 0, n) for n in range(P)], [0, P], C, nb.MLA_KERNEL_TC, 1)
+        num_partitions = P
     kernel = {"tc": nb.MLA_KERNEL_TC, "simt": nb.MLA_KERNEL_SIMT}[args.kernel]
     dc = rt.upload(case)
-    chunks_dev = rt.chunks_to_device(plan.chunks)
+    chunks_dev = rt.chunks_to_device(plan.chunks) if not args.profile_split else None
     part, lse = rt.alloc_partials(plan.num_chunks, 1, H)
     ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
     out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
     k = plan.clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
     ws = rt.alloc_decode_workspace(1, plan.num_chunks, k, plan.cluster_ctas, 1, H)
     for _ in range(args.launches):  # the bench's layer call: mla_decode (one launch on the paired kernel)
-        rt.decode(dc, part, lse, ind, out, kernel=kernel, cluster=plan.cluster_ctas, chunks_dev=chunks_dev, subs=k,
-                  workspace=ws, tables_ready=True)
+        rt.decode(dc, part, lse, ind, out, num_partitions=num_partitions, kernel=kernel, cluster=plan.cluster_ctas,
+                  chunks_dev=chunks_dev, subs=k, workspace=ws, tables_ready=True)
     torch.cuda.synchronize()
     st, code = nb.mla_check_device_errors(None)
     print(json.dumps({"profile_ctx": L, "launches": args.launches, "partitions": plan.num_chunks,

@@ -644,8 +644,27 @@ __device__ __forceinline__ float4 merge_cols4(const float* partials, const float
   const long long stride = static_cast<long long>(rows) * kRank;  // one partial slot
   const float* lrow = lse_src + static_cast<long long>(lo) * rows + r;
   const float* vcol = partials + static_cast<long long>(lo) * stride + static_cast<long long>(r) * kRank + c;
+  // the first 8 partials' LSE and values in one round of loads (the values do not depend on the
+  // weights); further LSE in rounds of 8 for the maximum
+  float l0[8];
+  float4 v0[8];
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj) {
+    const bool in = jj < n;
+    l0[jj] = in ? __ldcg(lrow + static_cast<long long>(jj) * rows) : -INFINITY;
+    v0[jj] = (in && values) ? __ldcg(reinterpret_cast<const float4*>(vcol + jj * stride))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float M = -INFINITY;
-  for (int j = 0; j < n; ++j) M = fmaxf(M, __ldcg(lrow + static_cast<long long>(j) * rows));
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj) M = fmaxf(M, l0[jj]);
+  for (int j0 = 8; j0 < n; j0 += 8) {
+    float lj[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) lj[jj] = (j0 + jj < n) ? __ldcg(lrow + static_cast<long long>(j0 + jj) * rows) : -INFINITY;
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) M = fmaxf(M, lj[jj]);
+  }
   float den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
@@ -654,10 +673,15 @@ __device__ __forceinline__ float4 merge_cols4(const float* partials, const float
       float4 v[8];
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
-        const bool in = j0 + jj < n;
-        lj[jj] = in ? __ldcg(lrow + static_cast<long long>(j0 + jj) * rows) : -INFINITY;
-        v[jj] = (in && values) ? __ldcg(reinterpret_cast<const float4*>(vcol + (j0 + jj) * stride))
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j0 == 0) {
+          lj[jj] = l0[jj];
+          v[jj] = v0[jj];
+        } else {
+          const bool in = j0 + jj < n;
+          lj[jj] = in ? __ldcg(lrow + static_cast<long long>(j0 + jj) * rows) : -INFINITY;
+          v[jj] = (in && values) ? __ldcg(reinterpret_cast<const float4*>(vcol + (j0 + jj) * stride))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {

@@ -177,6 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     w = cta_work(p, kNR, kT, pair_index, subs * cluster_pairs, chunk);
     if (warp > kMmaWarp && w.sub1 > w.sub0) load_window(w.sub0 / p.bs);
   }
+  // the tensor-map descriptors are kernel parameters, not data of the preceding kernel: fetch them
+  // now, so the first page loads after the wait do not pay for it
+  if (warp == kMmaWarp + 1 && lane == 0) {
+    tma_prefetch_desc(&tm_pages);
+    tma_prefetch_desc(&tm_kpe_half);
+  }
   pdl_wait();
   pdl_launch_dependents();  // the merge of these partials may be scheduled now; it waits for this grid
   if (!p.tables_ready) w = cta_work(p, kNR, kT, pair_index, subs * cluster_pairs, chunk);
@@ -646,18 +652,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             have ? (sm->red[0][tid] + sm->red[1][tid]) + (sm->red[2][tid] + sm->red[3][tid]) : 0.f;
       }
     }
-    __threadfence();  // this CTA's entry, visible before its ticket
     __syncthreads();
     if (tid == 0) {
+      __threadfence();  // this CTA's entry (ordered before this thread by the barrier), released before its ticket
       uint32_t* ticket = p.ws_tickets + static_cast<long long>(chunk) * 2 + half;
       const uint32_t t = atomicAdd(ticket, 1u);
       const int last = (t == static_cast<uint32_t>(npairs_tot - 1)) ? 1 : 0;
-      if (last) atomicExch(ticket, 0u);
+      if (last) {
+        atomicExch(ticket, 0u);
+        __threadfence();  // the other pairs' entries, acquired before this CTA reads them
+      }
       sm->last_cluster = last;
     }
     __syncthreads();
     if (sm->last_cluster) {
-      __threadfence();
       const float* const ebase = p.ws_partials + static_cast<long long>(chunk) * npairs_tot * rows_total * kRank;
       const float* const mbase = p.ws_lse + static_cast<long long>(chunk) * npairs_tot * 2 * rows_total * 2 +
                               static_cast<long long>(half) * rows_total * 2;
@@ -721,22 +729,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (fused) {
         // the chunk's partial (this half) is written: count it for the request; the CTA that
         // counts the request's last chunk for this half merges the half's columns into the output
-        __threadfence();
         __syncthreads();
         if (tid == 0) {
           __threadfence();
           uint32_t* ticket = p.req_tickets + static_cast<long long>(w.b) * kSliceTickets + half;
           const uint32_t t = atomicAdd(ticket, 1u);
           const int last = (t == static_cast<uint32_t>(req_hi - req_lo - 1)) ? 1 : 0;
-          if (last) atomicExch(ticket, 0u);
+          if (last) {
+            atomicExch(ticket, 0u);
+            __threadfence();
+          }
           sm->last_request = last;
         }
         __syncthreads();
-        if (sm->last_request) {
-          __threadfence();
+        if (sm->last_request)
           request_merge(p, w.b, req_lo, req_hi, kHalfCols * half, kHalfCols, half == 0, half ? p.lse_copy : p.lse,
                         tid, kThreads);
-        }
       }
     }
     cluster_wait_acquire();
@@ -839,7 +847,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  if (fused) __threadfence();  // this CTA's slice of the chunk partial, visible before any ticket below
   cluster_sync();
   if (warp == kMmaWarp) {
     tc_fence_after();
@@ -852,20 +859,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // partials into the output (rank 0's slice also the merged LSE).
     const int dcols = kRank / static_cast<int>(nranks);
     if (tid == 0) {
-      // the other ranks' slices and rank 0's LSE reached this thread through the cluster barrier; this
-      // fence makes them (and this CTA's slice) visible at device scope before the ticket
+      // the cluster's slices and rank 0's LSE are ordered before this thread by the cluster barrier;
+      // this fence releases them at device scope before the ticket (and, for the last, acquires
+      // the other clusters' partials before this CTA's threads read them after the barrier below)
       __threadfence();
       uint32_t* ticket = p.req_tickets + static_cast<long long>(w.b) * kSliceTickets + rank;
       const uint32_t t = atomicAdd(ticket, 1u);
       const int last = (t == static_cast<uint32_t>(req_hi - req_lo - 1)) ? 1 : 0;
-      if (last) atomicExch(ticket, 0u);
+      if (last) {
+        atomicExch(ticket, 0u);
+        __threadfence();
+      }
       sm->last_request = last;
     }
     __syncthreads();
-    if (sm->last_request) {
-      __threadfence();
+    if (sm->last_request)
       request_merge(p, w.b, req_lo, req_hi, static_cast<int>(rank) * dcols, dcols, rank == 0, p.lse, tid, kThreads);
-    }
   }
 }
 
