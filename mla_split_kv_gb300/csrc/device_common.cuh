@@ -487,6 +487,20 @@ __device__ __forceinline__ uint16_t f2h(float v) {
   }
 }
 
+// Ticket for "the last one merges": an add with acquire-release semantics at device scope. It
+// releases what this thread has written, and what other threads wrote before a barrier this
+// thread has passed, before the count moves; the thread that reads the final count acquires
+// what the others released with their own adds.
+__device__ __forceinline__ uint32_t ticket_add_acq_rel(uint32_t* t) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
+  return old;
+}
+// Reset a ticket for the next call: nothing else touches it until this grid has completed.
+__device__ __forceinline__ void ticket_reset(uint32_t* t) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(t) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Work of one CTA: request, chunk bounds, output slot, token sub-range.
 // ---------------------------------------------------------------------------

@@ -654,14 +654,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     if (tid == 0) {
-      __threadfence();  // this CTA's entry (ordered before this thread by the barrier), released before its ticket
+      // releases this CTA's entry (ordered before this thread by the barrier) with the count; the last
+      // acquires the other pairs' entries before this CTA reads them
       uint32_t* ticket = p.ws_tickets + static_cast<long long>(chunk) * 2 + half;
-      const uint32_t t = atomicAdd(ticket, 1u);
+      const uint32_t t = ticket_add_acq_rel(ticket);
       const int last = (t == static_cast<uint32_t>(npairs_tot - 1)) ? 1 : 0;
-      if (last) {
-        atomicExch(ticket, 0u);
-        __threadfence();  // the other pairs' entries, acquired before this CTA reads them
-      }
+      if (last) ticket_reset(ticket);
       sm->last_cluster = last;
     }
     __syncthreads();
@@ -731,14 +729,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // counts the request's last chunk for this half merges the half's columns into the output
         __syncthreads();
         if (tid == 0) {
-          __threadfence();
           uint32_t* ticket = p.req_tickets + static_cast<long long>(w.b) * kSliceTickets + half;
-          const uint32_t t = atomicAdd(ticket, 1u);
+          const uint32_t t = ticket_add_acq_rel(ticket);
           const int last = (t == static_cast<uint32_t>(req_hi - req_lo - 1)) ? 1 : 0;
-          if (last) {
-            atomicExch(ticket, 0u);
-            __threadfence();
-          }
+          if (last) ticket_reset(ticket);
           sm->last_request = last;
         }
         __syncthreads();
@@ -860,16 +854,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int dcols = kRank / static_cast<int>(nranks);
     if (tid == 0) {
       // the cluster's slices and rank 0's LSE are ordered before this thread by the cluster barrier;
-      // this fence releases them at device scope before the ticket (and, for the last, acquires
-      // the other clusters' partials before this CTA's threads read them after the barrier below)
-      __threadfence();
+      // the acquire-release add releases them at device scope with the count (and, for the last,
+      // acquires the other clusters' partials before this CTA's threads read them after the
+      // barrier below)
       uint32_t* ticket = p.req_tickets + static_cast<long long>(w.b) * kSliceTickets + rank;
-      const uint32_t t = atomicAdd(ticket, 1u);
+      const uint32_t t = ticket_add_acq_rel(ticket);
       const int last = (t == static_cast<uint32_t>(req_hi - req_lo - 1)) ? 1 : 0;
-      if (last) {
-        atomicExch(ticket, 0u);
-        __threadfence();
-      }
+      if (last) ticket_reset(ticket);
       sm->last_request = last;
     }
     __syncthreads();
