@@ -3,24 +3,25 @@
 Workload: B=1, H=16, kv_lora_rank 512, rope 64, fp16, block 32, contexts
 32768 / 49152 / 65536 / 81920 / 98304 / 131072 tokens (N(0,1) latents, random
 block permutation), partitions chosen by the planner. One step = one layer
-call at each of the six contexts through mla_decode (with the paired kernel a
-single launch: the partial kernel merges each request's partials itself); the
-six caches live in disjoint memory (528 MB together, > L2), so every call
-streams its latent from HBM.
+call at each of the six contexts through mla_decode (the partial kernel, then
+the merge kernel as a programmatic dependent launch); the six caches live in
+disjoint memory (528 MB together, > L2), so every call streams its latent from
+HBM.
 
 Printed: one JSON line. `value` = mean microseconds per layer call over the
 sweep (device time, inputs resident, each step replayed from one CUDA graph);
 `e2e` = the same through mla_decode with host buffers (queries, block tables
 and plan of the six calls copied in with one copy from one pinned buffer, the
-six outputs copied out with one copy, every step); `roofline` = the kernel's
-algorithmic HBM bytes / its CUDA-event time against the measured copy
+six outputs copied out with one copy, every step); `roofline` = the partial
+kernel's algorithmic HBM bytes / its CUDA-event time against the measured copy
 bandwidth; `cpu_baseline` = the f64 oracle on the host cores. Outside the
-timed region: `two_launch_us` (the same step as partial kernel + merge
-kernel), `per_ctx` (each context alone, its planned split, a single cold call
-after an L2 flush and the host planner's time per call), `trials` (median /
-min / max over five more K-step trials) and `many_heads` (the many-head
-workload). `--impl reference` times the oracle itself on the same workload;
-`--gpus N` without a launcher starts N ranks (one replica per GPU).
+timed region: `single_launch_us` (the same step with each layer call as one
+launch, the merge inside the paired kernel), `per_ctx` (each context alone,
+its planned split, a single cold call after an L2 flush and the host
+planner's time per call), `trials` (median / min / max over five more K-step
+trials), `many_heads` (the many-head workload), `verify_windows` and
+`batch_grid`. `--impl reference` times the oracle itself on the same
+workload; `--gpus N` without a launcher starts N ranks (one replica per GPU).
 """
 from __future__ import annotations
 
@@ -636,13 +637,17 @@ def run_ours(args, rank, world):
             dws = rt.alloc_decode_workspace(1, plan.num_chunks, k, plan.cluster_ctas, 1, H)
             # the tables are uploaded before the step and no kernel of the step writes them
             desc = rt.make_desc(dc, chunks_dev, kernel, plan.cluster_ctas, stream, k, ws, tables_ready=True)
-            fdesc = rt.make_desc(dc, chunks_dev, kernel, plan.cluster_ctas, stream, k, dws, tables_ready=True)
+            sdesc = rt.make_desc(dc, chunks_dev, kernel, plan.cluster_ctas, stream, k, dws, tables_ready=True,
+                                 single_launch=True)
             calls.append(dict(L=L, plan=plan, dc=dc, chunks=chunks_dev, part=part, lse=lse, ind=ind, out=out,
-                              desc=desc, fdesc=fdesc, ws=ws, dws=dws))
+                              desc=desc, sdesc=sdesc, ws=ws, dws=dws))
     torch.cuda.synchronize()
 
-    def layer(c):  # one decode layer call through the library's single entry point
-        rt.decode(c["dc"], c["part"], c["lse"], c["ind"], c["out"], desc=c["fdesc"])
+    def layer(c):  # one decode layer call through mla_decode (its default: partial kernel, then merge kernel)
+        rt.decode(c["dc"], c["part"], c["lse"], c["ind"], c["out"], desc=c["desc"])
+
+    def single(c):  # the same call as one launch (the merge inside the paired kernel)
+        rt.decode(c["dc"], c["part"], c["lse"], c["ind"], c["out"], desc=c["sdesc"])
 
     def partial(c):
         rt.decode_partial(c["dc"], c["part"], c["lse"], desc=c["desc"])
@@ -658,17 +663,16 @@ def run_ours(args, rank, world):
                 layer(c)
                 partial(c)
                 merge(c)
+                single(c)
     stream.synchronize()
     st, code = nb.mla_check_device_errors(stream.cuda_stream)
     if st != nb.MLA_OK:
         raise RuntimeError(f"device error word {code:#x} after warm-up")
-    fused = nb.mla_get_counters()[nb.CTR_DECODE_FUSED] == max(3, args.warmup) * len(calls)
 
-    # One CUDA graph per step (all six layer calls through mla_decode): `value`. With the paired
-    # kernel each call is one launch (the merge runs inside it), so the step graph is that
-    # kernel's launches alone and also gives its average launch duration for the roofline.
-    # Otherwise a graph of the six partial launches alone gives the partial kernel's. Every
-    # graph sweeps the six disjoint caches, so every launch streams its latent from HBM.
+    # One CUDA graph per step (all six layer calls through mla_decode): `value`. A graph of the six
+    # partial launches alone gives the partial kernel's average launch duration for the roofline.
+    # A third graph runs the step with single-launch calls (reported beside it). Every graph sweeps
+    # the six disjoint caches, so every launch streams its latent from HBM.
     g_step, g_part, g_two = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step, stream=stream):
         for c in calls:
@@ -678,8 +682,7 @@ def run_ours(args, rank, world):
             partial(c)
     with torch.cuda.graph(g_two, stream=stream):
         for c in calls:
-            partial(c)
-            merge(c)
+            single(c)
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
             g_step.replay()
@@ -708,22 +711,21 @@ def run_ours(args, rank, world):
             for _ in range(K * reps):
                 g_step.replay()
             ev[1].record(stream)
-            if not fused:
-                for _ in range(K * reps):
-                    g_part.replay()
-                ev[2].record(stream)
+            for _ in range(K * reps):
+                g_part.replay()
+            ev[2].record(stream)
         stream.synchronize()
     if world > 1:
         torch.distributed.barrier()
     total_ms = ev[0].elapsed_time(ev[1]) / reps  # per K steps
-    part_ms_all = total_ms if fused else ev[1].elapsed_time(ev[2]) / reps
+    part_ms_all = ev[1].elapsed_time(ev[2]) / reps
     if world > 1:
         total_ms = max_over_ranks(total_ms, "cuda")
     st, code = nb.mla_check_device_errors(stream.cuda_stream)
     if st != nb.MLA_OK:
         raise RuntimeError(f"device error word {code:#x} in the timed region")
 
-    # the same step as two launches per layer call (partial kernel, then merge kernel), outside the
+    # the same step with single-launch layer calls (the merge inside the paired kernel), outside the
     # timed region, for comparison
     e2 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     with torch.cuda.stream(stream):
@@ -732,22 +734,21 @@ def run_ours(args, rank, world):
             g_two.replay()
         e2[1].record(stream)
     stream.synchronize()
-    two_launch_us = e2[0].elapsed_time(e2[1]) * 1e3 / (K * len(calls))
+    single_launch_us = e2[0].elapsed_time(e2[1]) * 1e3 / (K * len(calls))
 
     # per-context breakdown (not part of the timed region): one graph per call
     per_ctx = []
     kern_bytes_all = 0
     for c in calls:
         pb, mb = algorithmic_bytes(c["L"], c["plan"].num_chunks)
-        kern_bytes_all += (pb + mb if fused else pb) * K
+        kern_bytes_all += pb * K
         g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(g1, stream=stream):
             for _ in range(4):  # the other caches sit between repeats in the sweep; here each repeat re-reads
                 layer(c)
         with torch.cuda.graph(g2, stream=stream):
             for _ in range(4):
-                partial(c)
-                merge(c)
+                single(c)
         e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         with torch.cuda.stream(stream):
             g1.replay()
@@ -762,7 +763,7 @@ def run_ours(args, rank, world):
         tus = e[1].elapsed_time(e[2]) * 1e3 / 4
         per_ctx.append({"ctx": c["L"], "partitions": c["plan"].num_chunks, "cluster": c["plan"].cluster_ctas,
                         "clusters_per_partition": c["desc"].clusters_per_chunk,
-                        "us_per_call": round(us, 3), "two_launch_us": round(tus, 3),
+                        "us_per_call": round(us, 3), "single_launch_us": round(tus, 3),
                         "layer_gbs": round((pb + mb) / (us * 1e-6) / 1e9, 1),
                         "note": "repeats of one cache; caches <= 113 MB may be partly L2-resident"})
 
@@ -842,7 +843,7 @@ def run_ours(args, rank, world):
                             context_lens=dview(lay["lens"], torch.int32), case=dc.case)
         chunks = dview(lay["chunks"], torch.int32)
         desc = rt.make_desc(edc, chunks, kernel, c["plan"].cluster_ctas, stream, c["desc"].clusters_per_chunk,
-                            c["dws"], tables_ready=True)
+                            c["ws"], tables_ready=True)
         e2e_calls.append(dict(dc=edc, desc=desc, ind=dview(lay["ind"], torch.int32), out=dout[j],
                               part=c["part"], lse=c["lse"]))
     h2d = off
@@ -870,9 +871,9 @@ def run_ours(args, rank, world):
     ctr = nb.mla_get_counters()
     expect = (3 + e2e_steps) * len(calls)
     ctr_key = nb.CTR_PARTIAL_SIMT if kernel == nb.MLA_KERNEL_SIMT else nb.CTR_PARTIAL_TC
-    if ctr[ctr_key] != expect or ctr[nb.CTR_DECODE_FUSED if fused else nb.CTR_MERGE] != expect:
+    if ctr[ctr_key] != expect or ctr[nb.CTR_MERGE] != expect or ctr[nb.CTR_DECODE_FUSED] != 0:
         print(f"WARNING: path counters {ctr} disagree with {expect} layer calls on the {args.kernel} kernel "
-              f"({'one launch' if fused else 'two launches'} each)", file=sys.stderr)
+              f"(two launches each)", file=sys.stderr)
 
     many_heads = time_many_heads(nb, rt, torch, stream)
     st, code = nb.mla_check_device_errors(stream.cuda_stream)
@@ -912,13 +913,13 @@ def run_ours(args, rank, world):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "contexts": CONTEXTS, "B": 1, "H": H, "kv_lora_rank": 512, "rope_dim": 64,
                    "block_size": BS, "partitions": "planner", "kernel": args.kernel,
-                   "launches_per_layer_call": 1 if fused else 2,
+                   "launches_per_layer_call": 2,
                    "l2": "inputs larger than L2: each step streams six disjoint caches, 528 MB",
                    "timing": "CUDA graph per step (6 layer calls through mla_decode), CUDA events on the launching "
-                             "stream" + ("" if fused else "; roofline from a graph of the 6 partial launches")},
+                             "stream; roofline from a graph of the 6 partial launches"},
         "per_ctx": per_ctx,
         "trials": trials,
-        "two_launch_us": round(two_launch_us, 3),
+        "single_launch_us": round(single_launch_us, 3),
         "many_heads": many_heads,
         "verify_windows": verify,
         "batch_grid": grid,
@@ -926,11 +927,10 @@ def run_ours(args, rank, world):
                      "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(kname, sum(CONTEXTS) / len(CONTEXTS)),
                      "peak_source": peak_src, "kernel": kname,
-                     "bytes": "latent + block table + queries + partials and LSE written and read back + output"
-                              if fused else "latent + block table + queries + partials and LSE written"},
+                     "bytes": "latent + block table + queries + partials and LSE written"},
         "e2e": {"value": round(e2e_s * 1e6 / (e2e_steps * len(calls)), 3), "unit": "us/layer-call",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": (1 if fused else 3) * n_calls * reps,
+        "gpu_launches": 3 * n_calls * reps,  # step graphs (partial + merge) and partial-only graphs
         "timed_repeats": reps,
         "clocks": clocks.summary(),
     }

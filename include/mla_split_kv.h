@@ -193,6 +193,12 @@ typedef struct {
                                  caches are always read after it. 0 (default):
                                  every input is read after the preceding kernel
                                  has finished. Other values: INVALID_ARG.       */
+  int32_t single_launch;      /* mla_decode only: 1 = merge inside the paired
+                                 16-row kernel's launch (one launch per layer
+                                 call, see mla_decode); 0 (default) = the
+                                 partial kernel and then the merge kernel, a
+                                 programmatic dependent launch. Other values:
+                                 INVALID_ARG. mla_decode_partial ignores it.   */
 } mla_decode_desc_t;
 
 /*
@@ -313,16 +319,23 @@ mla_status_t mla_merge_states(const float* partials, const float* lse, const int
  * mla_merge_states over the request-major offsets o_indptr, with the same
  * arguments and the same results (the chunk partials and LSE in
  * partials / lse, the merged output in out, rounded once to out_dtype, the
- * merged LSE in out_lse when it is not NULL). "[kernel] Wire MLA split-KV
- * decode" (vllm-metal PR #601), *What changed*, avoids a temporary by letting
- * partition 0 write straight into the output; here the reduce itself moves
- * into the partial kernel: with the paired 16-row fp16 kernel (q_len*H <=
- * 16, clusters of 2..16 CTAs) the call is ONE launch. Once a chunk's partial
- * is written, a ticket per (request, column slice) counts it, and the CTA
- * that counts a request's last chunk merges that slice of all the request's
- * partials into `out`, with the merge kernel's arithmetic in its order, so
- * `out` is the same bits as mla_merge_states on the same partials. Other
- * kernels run the two launches on `stream` (no spread plans there).
+ * merged LSE in out_lse when it is not NULL).
+ *
+ * By default (desc->single_launch = 0) it enqueues the two kernels; the merge
+ * is a programmatic dependent launch that is resident before the partial
+ * kernel ends. With desc->single_launch = 1 and the paired 16-row fp16 kernel
+ * (q_len*H <= 16, clusters of 2..16 CTAs) it is ONE launch: "[kernel] Wire
+ * MLA split-KV decode" (vllm-metal PR #601), *What changed*, avoids a
+ * temporary by letting partition 0 write straight into the output; here the
+ * reduce itself moves into the partial kernel. Once a chunk's partial is
+ * written, an acquire-release ticket per (request, column slice) counts it,
+ * and the CTA that counts a request's last chunk merges that slice of all
+ * the request's partials into `out`, with the merge kernel's arithmetic in
+ * its order, so `out` is the same bits as the two launches. On GB300 the two
+ * launches measured faster (the dependent merge kernel is already resident
+ * and released by the grid's completion; the ticket chain adds a device-scope
+ * round trip in the last CTAs), hence the default. Other kernels always run
+ * the two launches.
  *
  * o_indptr : device [B+1] int32, as for mla_merge_states; request b's chunks
  *            must write exactly the slots o_indptr[b] .. o_indptr[b+1]-1 and
@@ -331,15 +344,16 @@ mla_status_t mla_merge_states(const float* partials, const float* lse, const int
  *            Device data: not checked.
  * out      : device [B, q_len, H, 512] of out_dtype (MLA_F16/BF16/F32)
  * out_lse  : device [B, q_len, H] fp32, or NULL
- * desc->workspace (one launch only): DEVICE, >= mla_decode_workspace_bytes(...)
- *            bytes, 16-byte aligned, ZEROED by the caller before its first use;
- *            every completed call leaves it zeroed again (after a device error,
- *            zero it again). It holds the request tickets, a copy of each
- *            chunk's LSE and, for clusters_per_chunk > 1, what
- *            mla_decode_partial's workspace holds. Calls sharing a workspace
- *            must not overlap in time.
- * Returns what mla_decode_partial returns (and MLA_ERR_INVALID_ARG for a
- * NULL or misaligned o_indptr / out / out_lse or a short workspace,
+ * desc->workspace: two launches: what mla_decode_partial needs. One launch:
+ *            DEVICE, >= mla_decode_workspace_bytes(...) bytes, 16-byte aligned,
+ *            ZEROED by the caller before its first use; every completed call
+ *            leaves it zeroed again (after a device error, zero it again). It
+ *            holds the request tickets, a copy of each chunk's LSE and, for
+ *            clusters_per_chunk > 1, what mla_decode_partial's workspace holds.
+ *            Calls sharing a workspace must not overlap in time.
+ * Returns what mla_decode_partial and mla_merge_states return (and
+ * MLA_ERR_INVALID_ARG for a NULL or misaligned o_indptr / out / out_lse, a
+ * short single-launch workspace or a bad single_launch value,
  * MLA_ERR_UNSUPPORTED for another out_dtype). No counterpart on the pages as
  * one call: the pages launch the two kernels.
  */

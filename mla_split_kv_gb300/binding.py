@@ -82,6 +82,7 @@ class mla_decode_desc_t(ctypes.Structure):
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_uint64),
         ("tables_ready", ctypes.c_int32),
+        ("single_launch", ctypes.c_int32),
     ]
 
 

@@ -191,6 +191,7 @@ mla_status_t check_decode(const void* q_absorbed, const void* q_pe, const void* 
   if (d->dtype != MLA_F16 && d->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
   if (d->causal != 0 && d->causal != 1) return MLA_ERR_INVALID_ARG;
   if (d->tables_ready != 0 && d->tables_ready != 1) return MLA_ERR_INVALID_ARG;
+  if (d->single_launch != 0 && d->single_launch != 1) return MLA_ERR_INVALID_ARG;
   if (d->kernel < MLA_KERNEL_AUTO || d->kernel > MLA_KERNEL_TC) return MLA_ERR_INVALID_ARG;
   const int32_t C0 = d->cluster_ctas;
   if (C0 != 0 && C0 != 1 && C0 != 2 && C0 != 4 && C0 != 8 && C0 != 16) return MLA_ERR_INVALID_ARG;
@@ -368,13 +369,18 @@ mla_status_t mla_decode(const void* q_absorbed, const void* q_pe, const void* ck
     return reject(MLA_ERR_INVALID_ARG);
   if (out_dtype != MLA_F16 && out_dtype != MLA_BF16 && out_dtype != MLA_F32) return reject(MLA_ERR_UNSUPPORTED);
   const int rows_total = d->num_heads * d->q_len;
-  const bool fused = d->kernel != MLA_KERNEL_SIMT &&
+  const bool fused = d->single_launch == 1 && d->kernel != MLA_KERNEL_SIMT &&
                      mla::tc128_supports(rows_total, d->dtype == MLA_BF16, launch_cluster(d, N));
   if (!fused) {
-    // kernels without the fused merge: the partial kernel, then the merge kernel, on the same stream
-    if (d->clusters_per_chunk > 1) return reject(MLA_ERR_UNSUPPORTED);  // spread plans are the paired kernel's
+    // the partial kernel, then the merge kernel (a programmatic dependent launch), on the same stream
+    if (d->clusters_per_chunk > 1) {
+      const uint64_t need = mla_workspace_bytes(static_cast<int32_t>(N), d->clusters_per_chunk, d->cluster_ctas,
+                                                d->q_len, d->num_heads);
+      if (d->workspace == nullptr || !aligned(d->workspace, 16) || d->workspace_bytes < need)
+        return reject(MLA_ERR_INVALID_ARG);
+    }
     mla_status_t st = launch_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
-                                    num_partitions, partials, lse, d, N, nullptr, FusedMerge{});
+                                    num_partitions, partials, lse, d, N, d->workspace, FusedMerge{});
     if (st != MLA_OK) return st;
     return mla_merge_states(partials, lse, o_indptr, d->num_requests, d->q_len, d->num_heads, out, out_dtype, out_lse,
                             d->stream);

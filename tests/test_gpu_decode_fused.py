@@ -1,11 +1,12 @@
-"""Single-launch decode (mla_decode) against the two-launch path and the oracle.
+"""Single-launch decode (mla_decode with single_launch) against the two-launch path and the oracle.
 
-mla_decode is mla_decode_partial followed by mla_merge_states; on the paired
-16-row fp16 kernel the merge runs inside the partial kernel (one launch). The
-fused merge uses the merge kernel's arithmetic in its order, so the chunk
-partials, the LSE and the merged output must be the same bits as the two
-launches give, and the merged output must match the f64 oracle within the
-stated tolerance (max-abs 2e-3, rel-L2 1e-3 on fp32 results).
+mla_decode is mla_decode_partial followed by mla_merge_states; with
+single_launch on the paired 16-row fp16 kernel the merge runs inside the
+partial kernel (one launch). The fused merge uses the merge kernel's
+arithmetic in its order, so the chunk partials, the LSE and the merged output
+must be the same bits as the two launches give, and the merged output must
+match the f64 oracle within the stated tolerance (max-abs 2e-3, rel-L2 1e-3 on
+fp32 results).
 """
 import numpy as np
 import pytest
@@ -55,7 +56,7 @@ def both_paths(case, dc, chunks_dev, ind, N, kernel, C, k, out_dtype="f16", tabl
         out_lse = torch.full((B, q, H), float("nan"), device="cuda") if with_lse else None
         if fused:
             ws = ws_fused if ws_fused is not None else rt.alloc_decode_workspace(B, N, k, C, q, H)
-            desc = rt.make_desc(dc, chunks_dev, kernel, C, None, k, ws, tables_ready)
+            desc = rt.make_desc(dc, chunks_dev, kernel, C, None, k, ws, tables_ready, single_launch=True)
             rt.decode(dc, part, lse, ind, out, out_lse, num_partitions=num_partitions, desc=desc)
         else:
             ws = rt.alloc_workspace(N, k, C, q, H)
@@ -92,7 +93,7 @@ def test_single_launch_equals_two_launches_at_every_bench_context(L):
     part, lse = rt.alloc_partials(plan.num_chunks, 1, 16)
     ws = rt.alloc_decode_workspace(1, plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, 16)
     rt.decode(dc, part, lse, ind, out32, kernel=nb.MLA_KERNEL_TC, cluster=plan.cluster_ctas, chunks_dev=chunks,
-              subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True)
+              subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True, single_launch=True)
     heads = [0, 7, 15]
     ref, _ = orc.unsplit(case, heads=heads)
     assert_close(out32.cpu().numpy()[:, :, heads], ref[:, :, heads], f"fused L={L}")
@@ -144,7 +145,7 @@ def test_single_launch_bitwise_reproducible_and_workspace_reused():
         part, lse = rt.alloc_partials(plan.num_chunks, 1, 16)
         out = torch.empty((1, 1, 16, 512), dtype=torch.float16, device="cuda")
         rt.decode(dc, part, lse, ind, out, kernel=nb.MLA_KERNEL_TC, cluster=plan.cluster_ctas, chunks_dev=chunks,
-                  subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True)
+                  subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True, single_launch=True)
         outs.append((part, lse, out))
     for other in outs[1:]:
         assert_same_bits(outs[0], other)
@@ -165,3 +166,28 @@ def test_decode_without_the_fused_merge_is_the_two_launches(H, dtype, kernel):
     ctr = nb.mla_get_counters()
     assert ctr[nb.CTR_DECODE_FUSED] == 0 and ctr[nb.CTR_MERGE] == 2
     assert_same_bits(fused, plain)
+
+
+def test_default_decode_is_two_launches_with_the_same_bits():
+    """Without single_launch, mla_decode enqueues the partial kernel and the merge kernel (the faster path on
+    this part), with the spread workspace of mla_decode_partial; the results are the same bits."""
+    L = 131072
+    case = gen.make_decode_case(35, [L], num_heads=16, block_size=32, dtype="f16")
+    dc = rt.upload(case)
+    plan = nb.mla_plan([L], 16, 1, 32, nb.mla_device_query())
+    chunks = rt.chunks_to_device(plan.chunks)
+    ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
+    res = []
+    for single in (False, True):
+        part, lse = rt.alloc_partials(plan.num_chunks, 1, 16)
+        out = torch.empty((1, 1, 16, 512), dtype=torch.float16, device="cuda")
+        ws = (rt.alloc_decode_workspace(1, plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, 16)
+              if single else rt.alloc_workspace(plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, 16))
+        nb.mla_reset_counters()
+        rt.decode(dc, part, lse, ind, out, kernel=nb.MLA_KERNEL_TC, cluster=plan.cluster_ctas, chunks_dev=chunks,
+                  subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True, single_launch=single)
+        ctr = nb.mla_get_counters()
+        assert ctr[nb.CTR_PARTIAL_TC] == 1 and ctr[nb.CTR_MERGE] == (0 if single else 1)
+        assert ctr[nb.CTR_DECODE_FUSED] == (1 if single else 0)
+        res.append((part, lse, out))
+    assert_same_bits(res[0], res[1])
