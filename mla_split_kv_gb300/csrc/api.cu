@@ -253,7 +253,7 @@ int launch_cluster(const mla_decode_desc_t* d, int64_t N) {
 mla_status_t launch_decode(const void* q_absorbed, const void* q_pe, const void* ckv_cache, const void* kpe_cache,
                            const int32_t* block_table, const int32_t* context_lens, float scale,
                            int32_t num_partitions, float* partials, float* lse, const mla_decode_desc_t* d,
-                           int64_t N, void* spread_ws, const FusedMerge& fm) {
+                           int64_t N, void* spread_ws, const FusedMerge& fm, bool entries_only = false) {
   const int32_t C0 = d->cluster_ctas;
   const uint64_t rows = static_cast<uint64_t>(d->num_blocks) * static_cast<uint64_t>(d->block_size);
   const bool use_simt = (d->kernel == MLA_KERNEL_SIMT);
@@ -300,12 +300,13 @@ mla_status_t launch_decode(const void* q_absorbed, const void* q_pe, const void*
   p.ws_partials = nullptr;
   p.ws_lse = nullptr;
   p.ws_tickets = nullptr;
-  if (subs > 1) {
+  p.entries_only = entries_only ? 1 : 0;
+  if (subs > 1 || entries_only) {
     uint8_t* ws = static_cast<uint8_t*>(spread_ws);
     // tickets (two per chunk), then per chunk its entries, one per CTA pair (subs * cluster_ctas / 2),
     // [rows][512] fp32 each, then per entry two [rows][2] fp32 copies
     const uint64_t tickets = (static_cast<uint64_t>(N) * 2 * 4 + 255) / 256 * 256;
-    const uint64_t entries = static_cast<uint64_t>(N) * subs * static_cast<uint64_t>(C0 / 2);
+    const uint64_t entries = static_cast<uint64_t>(N) * subs * static_cast<uint64_t>(C / 2);
     p.ws_tickets = reinterpret_cast<uint32_t*>(ws);
     p.ws_partials = reinterpret_cast<float*>(ws + tickets);
     p.ws_lse = p.ws_partials + entries * rows_total * mla::kRank;
@@ -332,6 +333,15 @@ mla_status_t launch_decode(const void* q_absorbed, const void* q_pe, const void*
 
 uint64_t round256(uint64_t x) { return (x + 255) / 256 * 256; }
 
+// Workspace of the pair entries (the spread layout, also for one cluster per chunk): the chunk
+// tickets, then N * k * C/2 entries of [rows][512] fp32, then their [2][rows][2] row maxima / sums.
+uint64_t entries_ws_bytes(int64_t N, int32_t k, int32_t C, int32_t q_len, int32_t H) {
+  if (N < 1 || C < 2 || q_len < 1 || H < 1) return 0;
+  const uint64_t rows = static_cast<uint64_t>(q_len) * static_cast<uint64_t>(H);
+  const uint64_t entries = static_cast<uint64_t>(N) * static_cast<uint64_t>(k > 1 ? k : 1) * (C / 2);
+  return round256(static_cast<uint64_t>(N) * 2 * 4) + entries * rows * mla::kRank * 4 + entries * 2 * rows * 2 * 4;
+}
+
 }  // namespace
 
 extern "C" {
@@ -353,7 +363,10 @@ uint64_t mla_decode_workspace_bytes(int32_t num_requests, int32_t num_chunks, in
   if (num_requests < 1 || num_chunks < 1 || q_len < 1 || num_heads < 1) return 0;
   const uint64_t tickets = round256(static_cast<uint64_t>(num_requests) * mla::kSliceTickets * 4);
   const uint64_t lse_copy = round256(static_cast<uint64_t>(num_chunks) * q_len * num_heads * 4);
-  return tickets + lse_copy + mla_workspace_bytes(num_chunks, clusters_per_chunk, cluster_ctas, q_len, num_heads);
+  const uint64_t single = tickets + lse_copy +
+                          mla_workspace_bytes(num_chunks, clusters_per_chunk, cluster_ctas, q_len, num_heads);
+  const uint64_t entries = entries_ws_bytes(num_chunks, clusters_per_chunk, cluster_ctas, q_len, num_heads);
+  return single > entries ? single : entries;
 }
 
 mla_status_t mla_decode(const void* q_absorbed, const void* q_pe, const void* ckv_cache, const void* kpe_cache,
@@ -369,8 +382,39 @@ mla_status_t mla_decode(const void* q_absorbed, const void* q_pe, const void* ck
     return reject(MLA_ERR_INVALID_ARG);
   if (out_dtype != MLA_F16 && out_dtype != MLA_BF16 && out_dtype != MLA_F32) return reject(MLA_ERR_UNSUPPORTED);
   const int rows_total = d->num_heads * d->q_len;
-  const bool fused = d->single_launch == 1 && d->kernel != MLA_KERNEL_SIMT &&
-                     mla::tc128_supports(rows_total, d->dtype == MLA_BF16, launch_cluster(d, N));
+  const bool paired = d->kernel != MLA_KERNEL_SIMT &&
+                      mla::tc128_supports(rows_total, d->dtype == MLA_BF16, launch_cluster(d, N));
+  const bool fused = paired && d->single_launch == 1;
+  if (paired && !fused) {
+    // the paired kernel writes every CTA pair's part to the workspace and exits; the entries merge
+    // kernel, a programmatic dependent launch, combines a request's parts straight into the output
+    const int32_t C = launch_cluster(d, N);
+    const uint64_t need = entries_ws_bytes(N, d->clusters_per_chunk, C, d->q_len, d->num_heads);
+    if (d->workspace == nullptr || !aligned(d->workspace, 16) || d->workspace_bytes < need)
+      return reject(MLA_ERR_INVALID_ARG);
+    mla_status_t st = launch_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
+                                    num_partitions, partials, lse, d, N, d->workspace, FusedMerge{}, true);
+    if (st != MLA_OK) return st;
+    const int32_t k = d->clusters_per_chunk > 1 ? d->clusters_per_chunk : 1;
+    uint8_t* ws = static_cast<uint8_t*>(d->workspace);
+    const uint64_t entries = static_cast<uint64_t>(N) * k * (C / 2);
+    mla::EntryMergeParams mp;
+    mp.ws_partials = reinterpret_cast<const float*>(ws + round256(static_cast<uint64_t>(N) * 2 * 4));
+    mp.ws_lse = mp.ws_partials + entries * rows_total * mla::kRank;
+    mp.o_indptr = o_indptr;
+    mp.out = out;
+    mp.out_lse = out_lse;
+    mp.B = d->num_requests;
+    mp.rows = rows_total;
+    mp.epc = k * (C / 2);
+    mp.out_dtype = out_dtype;
+    if (mla::launch_merge_entries(mp, static_cast<cudaStream_t>(d->stream)) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+    g_counters[MLA_CTR_MERGE].fetch_add(1, std::memory_order_relaxed);
+    return MLA_OK;
+  }
   if (!fused) {
     // the partial kernel, then the merge kernel (a programmatic dependent launch), on the same stream
     if (d->clusters_per_chunk > 1) {

@@ -54,8 +54,23 @@ struct PartialParams {
   int32_t out_dtype;           // MLA_F16 / MLA_BF16 / MLA_F32
   uint32_t* req_tickets;
   float* lse_copy;
+  // the paired kernel writes every CTA pair's part (unnormalized O^T, row maxima and sums) as an
+  // entry of ws_partials / ws_lse and nothing else; the entries merge kernel combines them
+  int32_t entries_only;
 };
 constexpr int kSliceTickets = 16;  // per request: one per column slice (cluster rank) or column half
+
+// The merge of the paired kernel's pair entries (entries_only): request b's entries are
+// [o_indptr[b] * epc, o_indptr[b+1] * epc), epc = entries per chunk.
+struct EntryMergeParams {
+  const float* ws_partials;    // [entries, rows, 512] unnormalized O
+  const float* ws_lse;         // [entries, 2, rows, 2] row maximum and sum (two equal copies)
+  const int32_t* o_indptr;     // [B+1]
+  void* out;                   // [B, rows, 512] of out_dtype
+  float* out_lse;              // [B, rows] or null
+  int32_t B, rows, epc, out_dtype;
+};
+cudaError_t launch_merge_entries(const EntryMergeParams& p, cudaStream_t stream);
 
 struct MergeParams {
   const float* partials;

@@ -106,7 +106,114 @@ __global__ void __launch_bounds__(kWarps * 32) mla_merge_kernel(const MergeParam
     p.out_lse[br] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
 }
 
+// The merge of the paired kernel's pair entries into the output (mla_decode's default path on that
+// kernel). Entry e holds one CTA pair's unnormalized O (its tokens, all 512 columns: each CTA of
+// the pair wrote its 256), its row maximum m_e and its row sum l_e relative to m_e. Per (request,
+// row): M = max_e m_e, w_e = 2^(m_e - M) (0 for m_e = -inf), out = sum_e w_e O_e / sum_e w_e l_e,
+// out_lse = M + log2 sum_e w_e l_e -- the merge of the pages' contract, applied to unnormalized
+// parts. One warp per (request, row, 16 columns): lane = 4 g + q takes column quad q of the
+// entries g, g + 8, g + 16, ... (up to 8 per lane in one round of loads), sums them in entry
+// order, and the warp adds the eight entry groups with a fixed shuffle tree, so the result is
+// the same bits on every call. 256 warps per request row block keep many SMs loading at once.
+constexpr int kEntryWarps = 4;
+
+__global__ void __launch_bounds__(kEntryWarps * 32) mla_merge_entries_kernel(const EntryMergeParams p) {
+  pdl_wait();  // the entries are complete once the partial kernel has
+  pdl_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long gw = static_cast<long long>(blockIdx.x) * kEntryWarps + warp;
+  if (gw >= static_cast<long long>(p.B) * p.rows * 32) return;
+  const int cb = static_cast<int>(gw & 31);   // columns [16 cb, 16 cb + 16)
+  const long long br = gw >> 5;              // b * rows + row
+  const int b = static_cast<int>(br / p.rows), row = static_cast<int>(br % p.rows);
+  const int e0 = p.o_indptr[b] * p.epc, e1 = p.o_indptr[b + 1] * p.epc;
+  const int g = lane >> 2, q = lane & 3;
+  const int col = 16 * cb + 4 * q;
+  const long long ostride = static_cast<long long>(p.rows) * kRank;  // one entry's O
+  const float* const obase = p.ws_partials + static_cast<long long>(row) * kRank + col;
+  const float* const mlbase = p.ws_lse + static_cast<long long>(row) * 2;  // copy 0 of the entry's m, l
+  const long long mlstride = 4LL * p.rows;                                  // one entry's two copies
+  // round 0: the first 64 entries' m, l and values (the values do not depend on the weights)
+  float2 ml0[8];
+  float4 v0[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int e = e0 + g + 8 * j;
+    const bool in = e < e1;
+    ml0[j] = in ? __ldcg(reinterpret_cast<const float2*>(mlbase + e * mlstride)) : make_float2(-INFINITY, 0.f);
+    v0[j] = in ? __ldcg(reinterpret_cast<const float4*>(obase + e * ostride)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) M = fmaxf(M, ml0[j].x);
+  for (int base = e0 + 64; base < e1; base += 64)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = base + g + 8 * j;
+      if (e < e1) M = fmaxf(M, __ldcg(mlbase + e * mlstride));
+    }
+  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
+  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 8));
+  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
+  float den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
+    for (int base = e0; base < e1; base += 64) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int e = base + g + 8 * j;
+        float2 ml;
+        float4 v;
+        if (base == e0) {
+          ml = ml0[j];
+          v = v0[j];
+        } else {
+          const bool in = e < e1;
+          ml = in ? __ldcg(reinterpret_cast<const float2*>(mlbase + e * mlstride)) : make_float2(-INFINITY, 0.f);
+          v = in ? __ldcg(reinterpret_cast<const float4*>(obase + e * ostride)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+        den = fmaf(w, ml.y, den);
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    den += __shfl_xor_sync(0xffffffffu, den, o);
+    acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+    acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+    acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
+    acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
+  }
+  if (g != 0) return;
+  float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) out = make_float4(acc.x / den, acc.y / den, acc.z / den, acc.w / den);
+  store_out4(p.out, p.out_dtype, br * kRank + col, out);
+  if (p.out_lse != nullptr && cb == 0 && q == 0) p.out_lse[br] = merged_lse(M, den);
+}
+
 }  // namespace
+
+cudaError_t launch_merge_entries(const EntryMergeParams& p, cudaStream_t stream) {
+  const long long warps = static_cast<long long>(p.B) * p.rows * 32;
+  const long long blocks = (warps + kEntryWarps - 1) / kEntryWarps;
+  if (blocks <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kEntryWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_merge_entries_kernel, p);
+}
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   const long long warps = static_cast<long long>(p.B) * p.rows * 4;

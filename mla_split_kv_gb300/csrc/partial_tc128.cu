@@ -614,8 +614,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();  // all roles done: the tile slots are free for staging
   const bool have = (ntiles > 0) && !*abort_flag;
-  if (subs > 1) {
-    // A chunk spread over several clusters: no in-cluster combine. Every CTA writes its
+  if (subs > 1 || p.entries_only) {
+    // A chunk spread over several clusters (or any chunk when the merge kernel reads the pairs' parts
+    // itself: entries_only): no in-cluster combine. Every CTA writes its
     // unnormalized O^T (its 256 columns, the rows it holds) and its row maxima and sums as the
     // entry of its pair (entry = chunk * pairs + pair, pairs = subs * pairs per cluster) in the
     // workspace; per chunk and half a ticket counts the CTAs, and the one that takes the last
@@ -655,11 +656,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (tid == 0) {
       // releases this CTA's entry (ordered before this thread by the barrier) with the count; the last
-      // acquires the other pairs' entries before this CTA reads them
-      uint32_t* ticket = p.ws_tickets + static_cast<long long>(chunk) * 2 + half;
-      const uint32_t t = ticket_add_acq_rel(ticket);
-      const int last = (t == static_cast<uint32_t>(npairs_tot - 1)) ? 1 : 0;
-      if (last) ticket_reset(ticket);
+      // acquires the other pairs' entries before this CTA reads them. With entries_only the merge
+      // kernel, a dependent launch, reads the entries after this grid has completed: no ticket.
+      int last = 0;
+      if (!p.entries_only) {
+        uint32_t* ticket = p.ws_tickets + static_cast<long long>(chunk) * 2 + half;
+        const uint32_t t = ticket_add_acq_rel(ticket);
+        last = (t == static_cast<uint32_t>(npairs_tot - 1)) ? 1 : 0;
+        if (last) ticket_reset(ticket);
+      }
       sm->last_cluster = last;
     }
     __syncthreads();

@@ -168,26 +168,64 @@ def test_decode_without_the_fused_merge_is_the_two_launches(H, dtype, kernel):
     assert_same_bits(fused, plain)
 
 
-def test_default_decode_is_two_launches_with_the_same_bits():
-    """Without single_launch, mla_decode enqueues the partial kernel and the merge kernel (the faster path on
-    this part), with the spread workspace of mla_decode_partial; the results are the same bits."""
-    L = 131072
-    case = gen.make_decode_case(35, [L], num_heads=16, block_size=32, dtype="f16")
+def default_decode(case, dc, plan, chunks, ind, out_dtype="f32", ws=None):
+    B = case.num_requests
+    part, lse = rt.alloc_partials(plan.num_chunks, 1, 16)
+    out = torch.empty((B, 1, 16, 512), dtype=TDT[out_dtype], device="cuda")
+    out_lse = torch.empty((B, 1, 16), device="cuda")
+    if ws is None:
+        ws = rt.alloc_decode_workspace(B, plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, 16)
+    rt.decode(dc, part, lse, ind, out, out_lse, kernel=nb.MLA_KERNEL_TC, cluster=plan.cluster_ctas, chunks_dev=chunks,
+              subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True)
+    return out, out_lse
+
+
+@pytest.mark.parametrize("L", [32768, 49152, 65536, 81920, 98304, 131072])
+def test_default_decode_on_the_paired_kernel_every_bench_context(L):
+    """mla_decode's default on the paired kernel: every CTA pair writes its unnormalized part and the entries
+    merge kernel (a dependent launch) combines them; against the oracle on sampled heads, and the same bits on
+    a second call."""
+    case = gen.make_decode_case(2, [L], num_heads=16, block_size=32, dtype="f16")
     dc = rt.upload(case)
     plan = nb.mla_plan([L], 16, 1, 32, nb.mla_device_query())
     chunks = rt.chunks_to_device(plan.chunks)
     ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
-    res = []
-    for single in (False, True):
-        part, lse = rt.alloc_partials(plan.num_chunks, 1, 16)
-        out = torch.empty((1, 1, 16, 512), dtype=torch.float16, device="cuda")
-        ws = (rt.alloc_decode_workspace(1, plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, 16)
-              if single else rt.alloc_workspace(plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, 16))
-        nb.mla_reset_counters()
-        rt.decode(dc, part, lse, ind, out, kernel=nb.MLA_KERNEL_TC, cluster=plan.cluster_ctas, chunks_dev=chunks,
-                  subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True, single_launch=single)
-        ctr = nb.mla_get_counters()
-        assert ctr[nb.CTR_PARTIAL_TC] == 1 and ctr[nb.CTR_MERGE] == (0 if single else 1)
-        assert ctr[nb.CTR_DECODE_FUSED] == (1 if single else 0)
-        res.append((part, lse, out))
-    assert_same_bits(res[0], res[1])
+    nb.mla_reset_counters()
+    out, out_lse = default_decode(case, dc, plan, chunks, ind)
+    ctr = nb.mla_get_counters()
+    assert ctr[nb.CTR_PARTIAL_TC] == 1 and ctr[nb.CTR_MERGE] == 1 and ctr[nb.CTR_DECODE_FUSED] == 0
+    heads = [0, 7, 15]
+    ref, ref_lse = orc.unsplit(case, heads=heads)
+    assert_close(out.cpu().numpy()[:, :, heads], ref[:, :, heads], f"default L={L}")
+    assert np.abs(out_lse.cpu().numpy()[:, :, heads] - ref_lse[:, :, heads]).max() <= MAX_ABS
+    out2, lse2 = default_decode(case, dc, plan, chunks, ind)
+    assert torch.equal(out, out2) and torch.equal(out_lse, lse2)
+
+
+@pytest.mark.parametrize("C,k,bs,out_dtype", [(2, 1, 16, "f32"), (4, 3, 32, "f16"), (16, 1, 64, "bf16"),
+                                              (8, 2, 32, "f32")])
+def test_default_decode_ragged_batch_with_empty_requests(C, k, bs, out_dtype):
+    """Ragged requests on the uniform split (empty, one token, partial pages, several tiles; with and without
+    partitions spread over clusters): the oracle on every head, an empty request merges to zeros, and a
+    16-bit output is the fp32 output rounded once."""
+    lens = [0, 1, 31, 33, 127, 129, 1000, 4133]
+    case = gen.make_decode_case(36, lens, num_heads=16, block_size=bs, dtype="f16")
+    dc = rt.upload(case)
+    P, B = 3, len(lens)
+    ind = rt.uniform_indptr(B, P)
+    res = {}
+    for dt in ("f32", out_dtype):
+        part, lse = rt.alloc_partials(B * P, 1, 16)
+        out = torch.empty((B, 1, 16, 512), dtype=TDT[dt], device="cuda")
+        out_lse = torch.empty((B, 1, 16), device="cuda")
+        ws = rt.alloc_decode_workspace(B, B * P, k, C, 1, 16)
+        rt.decode(dc, part, lse, ind, out, out_lse, num_partitions=P, kernel=nb.MLA_KERNEL_TC, cluster=C, subs=k,
+                  workspace=ws)
+        res[dt] = (out, out_lse)
+    out, out_lse = res["f32"]
+    ref, ref_lse = orc.unsplit(case)
+    got = out.cpu().numpy()
+    assert np.all(got[0] == 0) and np.all(np.isneginf(out_lse.cpu().numpy()[0]))
+    assert_close(got[1:], ref[1:], f"default ragged C={C} k={k} bs={bs}")
+    assert np.abs(out_lse.cpu().numpy()[1:] - ref_lse[1:]).max() <= MAX_ABS
+    assert torch.equal(res[out_dtype][0], out.to(TDT[out_dtype]))
