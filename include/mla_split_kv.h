@@ -196,7 +196,7 @@ typedef struct {
   int32_t single_launch;      /* mla_decode only: 1 = merge inside the paired
                                  16-row kernel's launch (one launch per layer
                                  call, see mla_decode); 0 (default) = the
-                                 partial kernel and then the merge kernel, a
+                                 partial kernel and then a merge kernel, a
                                  programmatic dependent launch. Other values:
                                  INVALID_ARG. mla_decode_partial ignores it.   */
 } mla_decode_desc_t;
@@ -315,56 +315,67 @@ mla_status_t mla_merge_states(const float* partials, const float* lse, const int
                               int32_t out_dtype, float* out_lse, void* stream);
 
 /*
- * mla_decode -- one whole decode layer call: mla_decode_partial and then
- * mla_merge_states over the request-major offsets o_indptr, with the same
- * arguments and the same results (the chunk partials and LSE in
- * partials / lse, the merged output in out, rounded once to out_dtype, the
- * merged LSE in out_lse when it is not NULL).
+ * mla_decode -- one whole decode layer call: the attention of mla_decode_partial
+ * merged as mla_merge_states merges it, over the request-major offsets o_indptr,
+ * into `out` (rounded once to out_dtype) and `out_lse` (NULL allowed).
  *
- * By default (desc->single_launch = 0) it enqueues the two kernels; the merge
- * is a programmatic dependent launch that is resident before the partial
- * kernel ends. With desc->single_launch = 1 and the paired 16-row fp16 kernel
- * (q_len*H <= 16, clusters of 2..16 CTAs) it is ONE launch: "[kernel] Wire
- * MLA split-KV decode" (vllm-metal PR #601), *What changed*, avoids a
- * temporary by letting partition 0 write straight into the output; here the
- * reduce itself moves into the partial kernel. Once a chunk's partial is
- * written, an acquire-release ticket per (request, column slice) counts it,
- * and the CTA that counts a request's last chunk merges that slice of all
- * the request's partials into `out`, with the merge kernel's arithmetic in
- * its order, so `out` is the same bits as the two launches. On GB300 the two
- * launches measured faster (the dependent merge kernel is already resident
- * and released by the grid's completion; the ticket chain adds a device-scope
- * round trip in the last CTAs), hence the default. Other kernels always run
- * the two launches.
+ * Three ways, by kernel and desc->single_launch:
+ *  - the paired 16-row fp16 kernel (q_len*H <= 16, clusters of 2..16 CTAs), the
+ *    default (single_launch = 0): the partial kernel skips its in-cluster combine
+ *    and writes every CTA pair's unnormalized part (O over its tokens, row maxima
+ *    and sums) to the workspace; a merge kernel launched as its programmatic
+ *    dependent combines all the parts of a request straight into `out` (the merge
+ *    of the pages' contract, M = max, weights 2^(m - M), applied to the parts;
+ *    the same bits on every call for the same plan). `partials` and `lse` are
+ *    not written.
+ *  - the paired kernel with single_launch = 1: ONE launch. "[kernel] Wire MLA
+ *    split-KV decode" (vllm-metal PR #601), *What changed*, avoids a temporary by
+ *    letting partition 0 write straight into the output; here the reduce moves
+ *    into the partial kernel: once a chunk's partial is written (to
+ *    partials / lse, as mla_decode_partial writes it), an acquire-release ticket
+ *    per (request, column slice) counts it, and the CTA that counts a request's
+ *    last chunk merges that slice of all the request's partials into `out` with
+ *    the merge kernel's arithmetic in its order: the same bits as
+ *    mla_decode_partial + mla_merge_states. Measured on GB300 it is slower than
+ *    the default (the dependent merge kernel is resident before the partial
+ *    kernel ends and is released by the grid's completion, while the ticket adds
+ *    a device-scope round trip in the last CTAs); kept as an option.
+ *  - other kernels: mla_decode_partial, then mla_merge_states, on `stream`
+ *    (partials / lse written as those calls write them).
  *
- * o_indptr : device [B+1] int32, as for mla_merge_states; request b's chunks
- *            must write exactly the slots o_indptr[b] .. o_indptr[b+1]-1 and
- *            every request needs at least one chunk (mla_plan's tables do;
- *            with desc->chunks == NULL, o_indptr[b] = b * num_partitions).
- *            Device data: not checked.
+ * o_indptr : device [B+1] int32, as for mla_merge_states; the chunks must be
+ *            request-major with chunk n writing slot n, so that request b's
+ *            chunks are exactly o_indptr[b] .. o_indptr[b+1]-1, and every request
+ *            needs at least one chunk (mla_plan's tables do; with
+ *            desc->chunks == NULL, o_indptr[b] = b * num_partitions). Device
+ *            data: not checked.
  * out      : device [B, q_len, H, 512] of out_dtype (MLA_F16/BF16/F32)
  * out_lse  : device [B, q_len, H] fp32, or NULL
- * desc->workspace: two launches: what mla_decode_partial needs. One launch:
- *            DEVICE, >= mla_decode_workspace_bytes(...) bytes, 16-byte aligned,
- *            ZEROED by the caller before its first use; every completed call
- *            leaves it zeroed again (after a device error, zero it again). It
- *            holds the request tickets, a copy of each chunk's LSE and, for
- *            clusters_per_chunk > 1, what mla_decode_partial's workspace holds.
+ * partials, lse: device, as for mla_decode_partial (scratch on the default path
+ *            of the paired kernel)
+ * desc->workspace: on the paired kernel DEVICE, >= mla_decode_workspace_bytes(...)
+ *            bytes, 16-byte aligned, ZEROED by the caller before its first use;
+ *            every completed call leaves its counters zeroed again (after a device
+ *            error, zero it again). Other kernels: what mla_decode_partial needs.
  *            Calls sharing a workspace must not overlap in time.
  * Returns what mla_decode_partial and mla_merge_states return (and
  * MLA_ERR_INVALID_ARG for a NULL or misaligned o_indptr / out / out_lse, a
- * short single-launch workspace or a bad single_launch value,
- * MLA_ERR_UNSUPPORTED for another out_dtype). No counterpart on the pages as
- * one call: the pages launch the two kernels.
+ * short workspace or a bad single_launch value, MLA_ERR_UNSUPPORTED for another
+ * out_dtype). No counterpart on the pages as one call: the pages launch a
+ * partial kernel and a reduce kernel.
  */
 mla_status_t mla_decode(const void* q_absorbed, const void* q_pe, const void* ckv_cache, const void* kpe_cache,
                         const int32_t* block_table, const int32_t* context_lens, float scale, int32_t num_partitions,
                         float* partials, float* lse, const int32_t* o_indptr, void* out, int32_t out_dtype,
                         float* out_lse, const mla_decode_desc_t* desc);
 
-/* Workspace bytes of a single-launch mla_decode: B * 16 uint32 request tickets
- * and num_chunks * q_len * H fp32 LSE copies (each block 256-byte aligned),
- * then mla_workspace_bytes(num_chunks, clusters_per_chunk, cluster_ctas, ...). */
+/* Workspace bytes of mla_decode on the paired kernel: the larger of its two
+ * layouts. Default path: two uint32 tickets per chunk (256-byte block), then
+ * E = num_chunks * max(1, clusters_per_chunk) * cluster_ctas / 2 entries (one
+ * per CTA pair) of [q_len, H, 512] fp32, then E x [2, q_len, H, 2] fp32 row
+ * maxima and sums. Single launch: B * 16 uint32 request tickets and
+ * num_chunks * q_len * H fp32 LSE copies (each block 256-byte aligned), then
+ * mla_workspace_bytes(num_chunks, clusters_per_chunk, cluster_ctas, ...). */
 uint64_t mla_decode_workspace_bytes(int32_t num_requests, int32_t num_chunks, int32_t clusters_per_chunk,
                                     int32_t cluster_ctas, int32_t q_len, int32_t num_heads);
 

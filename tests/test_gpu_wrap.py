@@ -134,8 +134,8 @@ def test_merge_unembed_against_the_oracle_and_the_merge(H, q_len, dtype, v_head)
 
 
 def test_layer_call_append_decode_unembed():
-    """A whole decode layer call on the device: write the new token into its page, single-launch decode over
-    the cache that now holds it, then the merge with the unembed; against the oracle doing the same steps."""
+    """A whole decode layer call on the device: write the new token into its page, the partial decode over the
+    cache that now holds it, then the merge with the unembed; against the oracle doing the same steps."""
     lens = [20000, 7777]
     case = gen.make_decode_case(47, lens, num_heads=16, block_size=32, dtype="f16")
     dc = rt.upload(case)
@@ -147,10 +147,9 @@ def test_layer_call_append_decode_unembed():
     chunks = rt.chunks_to_device(plan.chunks)
     ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
     part, lse = rt.alloc_partials(plan.num_chunks, 1, 16)
-    out = torch.empty((2, 1, 16, 512), dtype=torch.float16, device="cuda")
-    ws = rt.alloc_decode_workspace(2, plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, 16)
-    rt.decode(dc, part, lse, ind, out, kernel=nb.MLA_KERNEL_TC, cluster=plan.cluster_ctas, chunks_dev=chunks,
-              subs=plan.clusters_per_chunk, workspace=ws)
+    ws = rt.alloc_workspace(plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, 16)
+    rt.decode_partial(dc, part, lse, kernel=nb.MLA_KERNEL_TC, cluster=plan.cluster_ctas, chunks_dev=chunks,
+                      subs=plan.clusters_per_chunk, workspace=ws)
     w_bits = unembed_weights(49, 16, 128, "f16")
     w = rt.to_device_16(w_bits, "f16", "cuda")
     ov = torch.empty((2, 1, 16, 128), dtype=torch.float32, device="cuda")
