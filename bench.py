@@ -627,35 +627,46 @@ def run_ours(args, rank, world):
     with torch.cuda.stream(stream):
         for case in cases:
             L = int(case.context_lens[0])
-            plan = nb.mla_plan([L], H, 1, BS, dev)
             dc = rt.upload(case)
-            chunks_dev = rt.chunks_to_device(plan.chunks)
-            part, lse = rt.alloc_partials(plan.num_chunks, 1, H)
-            ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
             out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
-            k = plan.clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
-            ws = rt.alloc_workspace(plan.num_chunks, k, plan.cluster_ctas, 1, H)
-            dws = rt.alloc_decode_workspace(1, plan.num_chunks, k, plan.cluster_ctas, 1, H)
+            c = dict(L=L, dc=dc, out=out)
+            # the timed step (mla_decode's default: pair entries merged by the entries kernel) and the paths
+            # that merge chunk partials (mla_decode_partial + mla_merge_states, the single launch), each
+            # planned for its merge
+            for tag, mp in (("", nb.MLA_MERGE_ENTRIES), ("p", nb.MLA_MERGE_PARTIALS)):
+                plan = nb.mla_plan([L], H, 1, BS, dev, merge_path=mp)
+                chunks_dev = rt.chunks_to_device(plan.chunks)
+                part, lse = rt.alloc_partials(plan.num_chunks, 1, H)
+                k = plan.clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
+                c[tag + "plan"] = plan
+                c[tag + "chunks"] = chunks_dev
+                c[tag + "part"], c[tag + "lse"] = part, lse
+                c[tag + "ind"] = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
+                c[tag + "ws"] = rt.alloc_workspace(plan.num_chunks, k, plan.cluster_ctas, 1, H)
+                c[tag + "dws"] = rt.alloc_decode_workspace(1, plan.num_chunks, k, plan.cluster_ctas, 1, H)
             # the tables are uploaded before the step and no kernel of the step writes them
-            desc = rt.make_desc(dc, chunks_dev, kernel, plan.cluster_ctas, stream, k, ws, tables_ready=True)
-            ldesc = rt.make_desc(dc, chunks_dev, kernel, plan.cluster_ctas, stream, k, dws, tables_ready=True)
-            sdesc = rt.make_desc(dc, chunks_dev, kernel, plan.cluster_ctas, stream, k, dws, tables_ready=True,
-                                 single_launch=True)
-            calls.append(dict(L=L, plan=plan, dc=dc, chunks=chunks_dev, part=part, lse=lse, ind=ind, out=out,
-                              desc=desc, ldesc=ldesc, sdesc=sdesc, ws=ws, dws=dws))
+            c["ldesc"] = rt.make_desc(dc, c["chunks"], kernel, c["plan"].cluster_ctas, stream,
+                                      c["plan"].clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1, c["dws"],
+                                      tables_ready=True)
+            pk = c["pplan"].clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
+            c["desc"] = rt.make_desc(dc, c["pchunks"], kernel, c["pplan"].cluster_ctas, stream, pk, c["pws"],
+                                     tables_ready=True)
+            c["sdesc"] = rt.make_desc(dc, c["pchunks"], kernel, c["pplan"].cluster_ctas, stream, pk, c["pdws"],
+                                      tables_ready=True, single_launch=True)
+            calls.append(c)
     torch.cuda.synchronize()
 
     def layer(c):  # one decode layer call through mla_decode (its default: partial kernel, then merge kernel)
         rt.decode(c["dc"], c["part"], c["lse"], c["ind"], c["out"], desc=c["ldesc"])
 
     def single(c):  # the same call as one launch (the merge inside the paired kernel)
-        rt.decode(c["dc"], c["part"], c["lse"], c["ind"], c["out"], desc=c["sdesc"])
+        rt.decode(c["dc"], c["ppart"], c["plse"], c["pind"], c["out"], desc=c["sdesc"])
 
-    def partial(c):
-        rt.decode_partial(c["dc"], c["part"], c["lse"], desc=c["desc"])
+    def partial(c):  # the ABI's two calls: mla_decode_partial ...
+        rt.decode_partial(c["dc"], c["ppart"], c["plse"], desc=c["desc"])
 
-    def merge(c):
-        rt.merge_states(c["part"], c["lse"], c["ind"], 1, 1, H, "f16", out=c["out"], stream=stream)
+    def merge(c):  # ... and mla_merge_states
+        rt.merge_states(c["ppart"], c["plse"], c["pind"], 1, 1, H, "f16", out=c["out"], stream=stream)
 
     # warm-up through the plain calls (also sets kernel attributes before capture)
     nb.mla_reset_counters()
@@ -765,7 +776,8 @@ def run_ours(args, rank, world):
         us = e[0].elapsed_time(e[1]) * 1e3 / 4
         tus = e[1].elapsed_time(e[2]) * 1e3 / 4
         per_ctx.append({"ctx": c["L"], "partitions": c["plan"].num_chunks, "cluster": c["plan"].cluster_ctas,
-                        "clusters_per_partition": c["desc"].clusters_per_chunk,
+                        "clusters_per_partition": c["ldesc"].clusters_per_chunk,
+                        "partials_plan": [c["pplan"].num_chunks, c["pplan"].cluster_ctas, c["pplan"].clusters_per_chunk],
                         "us_per_call": round(us, 3), "single_launch_us": round(tus, 3),
                         "layer_gbs": round((pb + mb) / (us * 1e-6) / 1e9, 1),
                         "note": "repeats of one cache; caches <= 113 MB may be partly L2-resident"})
@@ -845,7 +857,7 @@ def run_ours(args, rank, world):
                             ckv=dc.ckv, kpe=dc.kpe, block_table=dview(lay["bt"], torch.int32),
                             context_lens=dview(lay["lens"], torch.int32), case=dc.case)
         chunks = dview(lay["chunks"], torch.int32)
-        desc = rt.make_desc(edc, chunks, kernel, c["plan"].cluster_ctas, stream, c["desc"].clusters_per_chunk,
+        desc = rt.make_desc(edc, chunks, kernel, c["plan"].cluster_ctas, stream, c["ldesc"].clusters_per_chunk,
                             c["dws"], tables_ready=True)
         e2e_calls.append(dict(dc=edc, desc=desc, ind=dview(lay["ind"], torch.int32), out=dout[j],
                               part=c["part"], lse=c["lse"]))
@@ -901,7 +913,7 @@ def run_ours(args, rank, world):
     else:
         peak, peak_src = 6800.0, "fallback"
     kname = partial_kernel_name(args.kernel, [c["plan"] for c in calls])
-    part_bytes = sum(algorithmic_bytes(c["L"], c["plan"].num_chunks)[0] for c in calls) * K
+    part_bytes = sum(algorithmic_bytes(c["L"], c["pplan"].num_chunks)[0] for c in calls) * K
     partial_only = {"kernel": kname + " (mla_decode_partial: in-cluster combine, normalized partials)",
                     "us_per_launch": round(part_ms_all * 1e3 / (K * len(calls)), 3),
                     "achieved_gbs": round(part_bytes / (part_ms_all * 1e-3) / 1e9, 1),

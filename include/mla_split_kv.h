@@ -96,6 +96,9 @@ typedef struct {
  */
 mla_status_t mla_device_query(int32_t device, mla_device_info_t* info);
 
+#define MLA_MERGE_ENTRIES 0
+#define MLA_MERGE_PARTIALS 1
+
 /* Planner input/output. The caller sets the inputs and provides the host
  * arrays; mla_plan fills the outputs. */
 typedef struct {
@@ -108,6 +111,13 @@ typedef struct {
   int32_t capacity;         /* entries available in `chunks`                   */
   mla_chunk_t* chunks;      /* host, caller-owned, >= capacity entries         */
   int32_t* o_indptr;        /* host, caller-owned, >= B+1 entries              */
+  int32_t merge_path;       /* how the partitions will be merged, which sets
+                               what spreading a partition over clusters costs:
+                               MLA_MERGE_ENTRIES (0, default: mla_decode on
+                               the paired kernel) or MLA_MERGE_PARTIALS
+                               (mla_decode_partial + mla_merge_states, or
+                               mla_decode's single launch). Other values:
+                               INVALID_ARG.                                     */
   /* outputs */
   int32_t num_chunks;       /* N = sum_b P_b                                   */
   int32_t cluster_ctas;     /* CTAs per cluster (1,2,4,8,16)                    */
@@ -135,7 +145,12 @@ typedef struct {
  * least one 128-token tile); the partition count itself is not raised. For a
  * single long request on that kernel, P, the cluster size and k are chosen
  * by a time model among the plans whose P * k clusters are all co-resident
- * (one wave).
+ * (one wave): ceil(tiles / CTA pairs) x 1.75 us per 128-token tile, plus, for
+ * k > 1, 1.8 us when the parts are merged as pair entries (merge_path
+ * MLA_MERGE_ENTRIES) or 6 us + 0.3 us x 2k / cluster when each chunk's parts
+ * are first merged into its partial (MLA_MERGE_PARTIALS), plus 0.6 us per
+ * further round of 64 entries in the entries merge; constants fitted to
+ * layer-call times measured on GB300.
  *
  * context_lens_host: host [B] int32, each >= 0. dev: from mla_device_query or
  * hand-filled. Returns MLA_ERR_CAPACITY when N > plan->capacity (num_chunks
@@ -369,13 +384,14 @@ mla_status_t mla_decode(const void* q_absorbed, const void* q_pe, const void* ck
                         float* partials, float* lse, const int32_t* o_indptr, void* out, int32_t out_dtype,
                         float* out_lse, const mla_decode_desc_t* desc);
 
-/* Workspace bytes of mla_decode on the paired kernel: the larger of its two
- * layouts. Default path: two uint32 tickets per chunk (256-byte block), then
+/* Workspace bytes of mla_decode on the paired kernel, one layout for both of
+ * its ways: B * 16 uint32 request tickets and num_chunks * q_len * H fp32 LSE
+ * copies (the single launch's; each block 256-byte aligned), then two uint32
+ * tickets per chunk (a 256-byte block; the single launch's spread plans), then
  * E = num_chunks * max(1, clusters_per_chunk) * cluster_ctas / 2 entries (one
- * per CTA pair) of [q_len, H, 512] fp32, then E x [2, q_len, H, 2] fp32 row
- * maxima and sums. Single launch: B * 16 uint32 request tickets and
- * num_chunks * q_len * H fp32 LSE copies (each block 256-byte aligned), then
- * mla_workspace_bytes(num_chunks, clusters_per_chunk, cluster_ctas, ...). */
+ * per CTA pair) of [q_len, H, 512] fp32 and E x [2, q_len, H, 2] fp32 row
+ * maxima and sums. The default way writes only the entries, never a ticket,
+ * so one zeroed workspace serves both ways in any order. */
 uint64_t mla_decode_workspace_bytes(int32_t num_requests, int32_t num_chunks, int32_t clusters_per_chunk,
                                     int32_t cluster_ctas, int32_t q_len, int32_t num_heads);
 

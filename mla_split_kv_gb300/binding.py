@@ -26,6 +26,7 @@ MLA_ERR_CAPACITY = 6
 MLA_F16, MLA_BF16, MLA_F32 = 0, 1, 2
 MLA_STATIC_WORKSPACE_BYTES = 4 * 1024 * 1024
 MLA_KERNEL_AUTO, MLA_KERNEL_SIMT, MLA_KERNEL_TC = 0, 1, 2
+MLA_MERGE_ENTRIES, MLA_MERGE_PARTIALS = 0, 1
 
 CTR_PARTIAL_SIMT, CTR_PARTIAL_TC, CTR_MERGE, CTR_REJECTED, CTR_CTAS, CTR_DECODE_FUSED, CTR_WRAP = range(7)
 NUM_COUNTERS = 7
@@ -56,6 +57,7 @@ class mla_plan_t(ctypes.Structure):
         ("capacity", ctypes.c_int32),
         ("chunks", ctypes.POINTER(mla_chunk_t)),
         ("o_indptr", ctypes.POINTER(ctypes.c_int32)),
+        ("merge_path", ctypes.c_int32),
         ("num_chunks", ctypes.c_int32),
         ("cluster_ctas", ctypes.c_int32),
         ("kernel", ctypes.c_int32),
@@ -188,7 +190,7 @@ class Plan:
 
 def mla_plan(context_lens: Sequence[int], num_heads: int, q_len: int, block_size: int,
              dev: mla_device_info_t, max_partitions: int = 0, min_partitions: int = 0,
-             split_min_tokens: int = 0, dtype: str = "f16") -> Plan:
+             split_min_tokens: int = 0, dtype: str = "f16", merge_path: int = MLA_MERGE_ENTRIES) -> Plan:
     lib = load()
     B = len(context_lens)
     lens = (ctypes.c_int32 * B)(*[int(x) for x in context_lens])
@@ -197,6 +199,7 @@ def mla_plan(context_lens: Sequence[int], num_heads: int, q_len: int, block_size
     plan.min_partitions = min_partitions
     plan.split_min_tokens = split_min_tokens
     plan.dtype = DTYPE_CODES[dtype]
+    plan.merge_path = merge_path
     plan.capacity = 0
     st = lib.mla_plan(lens, B, num_heads, q_len, block_size, ctypes.byref(dev), ctypes.byref(plan))
     if st not in (MLA_OK, MLA_ERR_CAPACITY):

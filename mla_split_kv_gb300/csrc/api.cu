@@ -363,10 +363,9 @@ uint64_t mla_decode_workspace_bytes(int32_t num_requests, int32_t num_chunks, in
   if (num_requests < 1 || num_chunks < 1 || q_len < 1 || num_heads < 1) return 0;
   const uint64_t tickets = round256(static_cast<uint64_t>(num_requests) * mla::kSliceTickets * 4);
   const uint64_t lse_copy = round256(static_cast<uint64_t>(num_chunks) * q_len * num_heads * 4);
-  const uint64_t single = tickets + lse_copy +
-                          mla_workspace_bytes(num_chunks, clusters_per_chunk, cluster_ctas, q_len, num_heads);
-  const uint64_t entries = entries_ws_bytes(num_chunks, clusters_per_chunk, cluster_ctas, q_len, num_heads);
-  return single > entries ? single : entries;
+  // one layout for both ways: the request tickets and LSE copies of the single launch, then the
+  // chunk tickets and pair entries (the default path writes only the entries, never a ticket)
+  return tickets + lse_copy + entries_ws_bytes(num_chunks, clusters_per_chunk, cluster_ctas, q_len, num_heads);
 }
 
 mla_status_t mla_decode(const void* q_absorbed, const void* q_pe, const void* ckv_cache, const void* kpe_cache,
@@ -389,14 +388,16 @@ mla_status_t mla_decode(const void* q_absorbed, const void* q_pe, const void* ck
     // the paired kernel writes every CTA pair's part to the workspace and exits; the entries merge
     // kernel, a programmatic dependent launch, combines a request's parts straight into the output
     const int32_t C = launch_cluster(d, N);
-    const uint64_t need = entries_ws_bytes(N, d->clusters_per_chunk, C, d->q_len, d->num_heads);
+    const uint64_t head = round256(static_cast<uint64_t>(d->num_requests) * mla::kSliceTickets * 4) +
+                          round256(static_cast<uint64_t>(N) * rows_total * 4);  // the single launch's blocks
+    const uint64_t need = head + entries_ws_bytes(N, d->clusters_per_chunk, C, d->q_len, d->num_heads);
     if (d->workspace == nullptr || !aligned(d->workspace, 16) || d->workspace_bytes < need)
       return reject(MLA_ERR_INVALID_ARG);
+    uint8_t* ws = static_cast<uint8_t*>(d->workspace) + head;
     mla_status_t st = launch_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
-                                    num_partitions, partials, lse, d, N, d->workspace, FusedMerge{}, true);
+                                    num_partitions, partials, lse, d, N, ws, FusedMerge{}, true);
     if (st != MLA_OK) return st;
     const int32_t k = d->clusters_per_chunk > 1 ? d->clusters_per_chunk : 1;
-    uint8_t* ws = static_cast<uint8_t*>(d->workspace);
     const uint64_t entries = static_cast<uint64_t>(N) * k * (C / 2);
     mla::EntryMergeParams mp;
     mp.ws_partials = reinterpret_cast<const float*>(ws + round256(static_cast<uint64_t>(N) * 2 * 4));

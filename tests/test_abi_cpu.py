@@ -72,22 +72,38 @@ def check_plan_tiles(plan, lens, bs):
     assert [c[3] for c in plan.chunks] == list(range(plan.num_chunks))
 
 
+@pytest.mark.parametrize("merge_path", [nb.MLA_MERGE_ENTRIES, nb.MLA_MERGE_PARTIALS])
 @pytest.mark.parametrize("L", [32768, 49152, 65536, 81920, 98304, 131072])
-def test_plan_long_context_single_request(lib, L):
-    plan = nb.mla_plan([L], 16, 1, 32, fake_gb300())
+def test_plan_long_context_single_request(lib, L, merge_path):
+    plan = nb.mla_plan([L], 16, 1, 32, fake_gb300(), merge_path=merge_path)
     assert 2 <= plan.num_chunks <= 8
     busy = plan.num_chunks * plan.cluster_ctas * plan.clusters_per_chunk
     assert 100 <= busy <= 152  # most of the 152 SMs busy, with at most 8 partitions
-    if L >= 131072:  # long enough that spreading partitions over clusters pays for its merge tail
-        assert plan.clusters_per_chunk > 1 and busy >= 140
-    if L <= 65536:  # too short for that: one cluster of 16 per partition
-        assert plan.clusters_per_chunk == 1 and plan.cluster_ctas == 16
+    if merge_path == nb.MLA_MERGE_PARTIALS:
+        if L >= 131072:  # long enough that spreading partitions over clusters pays for its merge tail
+            assert plan.clusters_per_chunk > 1 and busy >= 140
+        if L <= 65536:  # too short for that: one cluster of 16 per partition
+            assert plan.clusters_per_chunk == 1 and plan.cluster_ctas == 16
+    else:
+        # the entries merge makes a spread cost about one tile: spread as soon as it saves more than that
+        if L >= 65536:
+            assert plan.clusters_per_chunk > 1 and busy >= 140
+        if L <= 49152:
+            assert plan.clusters_per_chunk == 1 and plan.cluster_ctas == 16
     check_plan_tiles(plan, [L], 32)
     # every CTA pair of every cluster keeps at least one 128-token tile of its partition
     k, C = plan.clusters_per_chunk, plan.cluster_ctas
     assert 1 <= k <= 16
     for (_, t0, t1, _) in plan.chunks:
         assert t1 - t0 >= k * (C // 2) * 128
+
+
+def test_plan_rejects_an_unknown_merge_path(lib):
+    dev = fake_gb300()
+    lens = (ctypes.c_int32 * 1)(65536)
+    plan = nb.mla_plan_t()
+    plan.merge_path = 2
+    assert lib.mla_plan(lens, 1, 16, 1, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_INVALID_ARG
 
 
 def test_plan_spreads_partitions_only_for_the_paired_kernel(lib):
@@ -414,15 +430,14 @@ def test_decode_rejects_before_launch(lib, kw, args, want):
 
 
 def test_decode_workspace_layout():
-    # the larger of the two layouts mla_decode uses on the paired kernel:
-    # single launch: request tickets (16 per request), a copy of each chunk's LSE (each block 256-byte aligned),
-    #   then the spread workspace;
-    # default (pair entries): the chunk tickets, then one [rows][512] fp32 entry per CTA pair (chunks x clusters
-    #   per chunk x cluster / 2) and its [2][rows][2] row maxima / sums
+    # one layout for mla_decode's two ways on the paired kernel: request tickets (16 per request) and a copy of
+    # each chunk's LSE (the single launch's, each block 256-byte aligned), then the chunk tickets and one
+    # [rows][512] fp32 entry per CTA pair (chunks x clusters per chunk x cluster / 2) with its [2][rows][2] row
+    # maxima / sums
     def entries(N, k, C, rows):
         e = N * max(k, 1) * (C // 2)
         return -(-N * 8 // 256) * 256 + e * rows * 512 * 4 + e * 2 * rows * 2 * 4
-    assert nb.mla_decode_workspace_bytes(1, 7, 1, 16, 1, 16) == max(256 + 512, entries(7, 1, 16, 16))
-    assert nb.mla_decode_workspace_bytes(3, 7, 5, 4, 1, 16) == max(256 + 512 + nb.mla_workspace_bytes(7, 5, 4, 1, 16),
-                                                                   entries(7, 5, 4, 16))
+    assert nb.mla_decode_workspace_bytes(1, 7, 1, 16, 1, 16) == 256 + 512 + entries(7, 1, 16, 16)
+    assert nb.mla_decode_workspace_bytes(3, 7, 5, 4, 1, 16) == 256 + 512 + entries(7, 5, 4, 16)
+    assert entries(7, 5, 4, 16) == nb.mla_workspace_bytes(7, 5, 4, 1, 16)  # the spread layout, for k > 1
     assert nb.mla_decode_workspace_bytes(0, 7, 1, 16, 1, 16) == 0

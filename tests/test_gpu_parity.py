@@ -243,7 +243,7 @@ def plan_and_run(case, max_partitions=0, kernel=nb.MLA_KERNEL_TC, dc=None, ws=No
     """The planner's plan as the bench runs it: its cluster size and clusters per partition."""
     dev = nb.mla_device_query()
     plan = nb.mla_plan(case.context_lens.tolist(), case.num_heads, case.q_len, case.block_size, dev,
-                       max_partitions=max_partitions, dtype=case.dtype)
+                       max_partitions=max_partitions, dtype=case.dtype, merge_path=nb.MLA_MERGE_PARTIALS)
     dc = dc or rt.upload(case)
     chunks_dev = rt.chunks_to_device(plan.chunks)
     part, lse = rt.alloc_partials(plan.num_chunks, case.q_len, case.num_heads)
@@ -314,7 +314,7 @@ def test_spread_partitions_bitwise_reproducible_and_workspace_reused():
     case = gen.make_decode_case(6, [131072], num_heads=16, block_size=32, dtype="f16")
     dc = rt.upload(case)
     dev = nb.mla_device_query()
-    plan = nb.mla_plan([131072], 16, 1, 32, dev)
+    plan = nb.mla_plan([131072], 16, 1, 32, dev, merge_path=nb.MLA_MERGE_PARTIALS)
     assert plan.clusters_per_chunk > 1
     ws = rt.alloc_workspace(plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, 16)
     outs = []
