@@ -259,7 +259,8 @@ mla_status_t launch_decode(const void* q_absorbed, const void* q_pe, const void*
   const bool use_simt = (d->kernel == MLA_KERNEL_SIMT);
   const bool bf16 = (d->dtype == MLA_BF16);
   const int rows_total = d->num_heads * d->q_len;
-  // a multiple of 128 rows on the tensor-core path: one CTA pair per 128 rows (a cluster of 2 by default)
+  // more than 16 rows on the tensor-core path: one CTA pair per 128 rows, the last group padded (a cluster
+  // of 2 by default)
   const bool mh = !use_simt && mla::mh_supports(rows_total, C0 ? C0 : 2);
   const int nr = use_simt ? mla::simt_rows_per_cta() : (mh ? 128 : mla::tc_rows_per_cta(rows_total, bf16));
   const int64_t groups = (rows_total + nr - 1) / nr;

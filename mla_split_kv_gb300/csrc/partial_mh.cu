@@ -582,14 +582,16 @@ cudaError_t prepare_mh() {
 
 }  // namespace
 
-bool mh_supports(int total_rows, int cluster) { return total_rows % kRows == 0 && cluster == 2; }
+// More than 16 rows (16 or fewer go to the paired 16-row kernel): groups of 128 rows, the last group
+// padded (its rows past the end have zero queries and are not written back).
+bool mh_supports(int total_rows, int cluster) { return total_rows > 16 && cluster == 2; }
 
 cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe, const PartialParams& p,
                               int num_chunks, bool bf16, cudaStream_t stream) {
   cudaError_t e = bf16 ? prepare_mh<true>() : prepare_mh<false>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * (p.q_len * p.H / kRows), num_chunks, 1);  // one CTA pair per 128-row group
+  cfg.gridDim = dim3(2 * ((p.q_len * p.H + kRows - 1) / kRows), num_chunks, 1);  // one CTA pair per 128-row group
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;

@@ -49,7 +49,7 @@ def close_to(got, ref):
 def planned_call(case, dc, max_partitions=0):
     dev = nb.mla_device_query()
     plan = nb.mla_plan(case.context_lens.tolist(), case.num_heads, case.q_len, case.block_size, dev,
-                       max_partitions=max_partitions, dtype=case.dtype)
+                       max_partitions=max_partitions, dtype=case.dtype, merge_path=nb.MLA_MERGE_PARTIALS)
     chunks = rt.chunks_to_device(plan.chunks)
     ws = rt.alloc_workspace(plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, case.q_len, case.num_heads)
     part, lse = rt.alloc_partials(plan.num_chunks, case.q_len, case.num_heads)
