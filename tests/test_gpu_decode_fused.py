@@ -8,6 +8,8 @@ must be the same bits as the two launches give, and the merged output must
 match the f64 oracle within the stated tolerance (max-abs 2e-3, rel-L2 1e-3 on
 fp32 results).
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -229,3 +231,45 @@ def test_default_decode_ragged_batch_with_empty_requests(C, k, bs, out_dtype):
     assert_close(got[1:], ref[1:], f"default ragged C={C} k={k} bs={bs}")
     assert np.abs(out_lse.cpu().numpy()[1:] - ref_lse[1:]).max() <= MAX_ABS
     assert torch.equal(res[out_dtype][0], out.to(TDT[out_dtype]))
+
+
+@pytest.mark.parametrize("H,dtype", [(16, "f16"), (64, "f16"), (128, "bf16")])
+def test_batch_of_32_requests_through_mla_decode(H, dtype):
+    """The largest batch of the heads x batch grid: 32 requests of 8192 tokens through mla_decode with the
+    planner's plan (16 heads: the paired kernel and the entries merge; 64 and 128 heads: the 128-row kernel and
+    the merge kernel), sampled requests and heads against the oracle."""
+    B, L = 32, 8192
+    bs = 64 if dtype == "bf16" else 32
+    case = gen.make_decode_case(37, [L] * B, num_heads=H, block_size=bs, dtype=dtype,
+                                latent_std=0.5 if dtype == "bf16" else 1.0)
+    dc = rt.upload(case)
+    plan = nb.mla_plan([L] * B, H, 1, bs, nb.mla_device_query(), max_partitions=64, dtype=dtype)
+    chunks = rt.chunks_to_device(plan.chunks)
+    ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
+    part, lse = rt.alloc_partials(plan.num_chunks, 1, H)
+    out = torch.empty((B, 1, H, 512), dtype=torch.float32, device="cuda")
+    ws = rt.alloc_decode_workspace(B, plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, H)
+    rt.decode(dc, part, lse, ind, out, kernel=nb.MLA_KERNEL_TC, cluster=plan.cluster_ctas, chunks_dev=chunks,
+              subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True)
+    reqs, heads = [0, 13, 31], [0, H // 2 + 3, H - 1]
+    sub = dataclasses.replace(case, q_abs=case.q_abs[reqs], q_pe=case.q_pe[reqs],
+                                  block_table=case.block_table[reqs], context_lens=case.context_lens[reqs])
+    ref, _ = orc.unsplit(sub, heads=heads)
+    assert_close(out.cpu().numpy()[reqs][:, :, heads], ref[:, :, heads], f"B=32 H={H} {dtype}")
+
+
+def test_largest_row_count_causal_window_of_32_over_128_heads():
+    """q_len 32 x 128 heads = 4096 rows (32 row groups of the 128-row kernel) with the causal window rule,
+    short and ragged contexts, every row against the oracle."""
+    case = gen.make_decode_case(38, [300, 97], num_heads=128, q_len=32, block_size=16, dtype="bf16", latent_std=0.5,
+                                causal=True)
+    dc = rt.upload(case)
+    P = 2
+    ind = rt.uniform_indptr(2, P)
+    part, lse = rt.alloc_partials(2 * P, 32, 128)
+    out = torch.empty((2, 32, 128, 512), dtype=torch.float32, device="cuda")
+    nb.mla_reset_counters()
+    rt.decode(dc, part, lse, ind, out, num_partitions=P, kernel=nb.MLA_KERNEL_TC, cluster=2)
+    assert nb.mla_get_counters()[nb.CTR_CTAS] == 2 * P * 32 * 2  # 32 row groups of one CTA pair per chunk
+    ref, _ = orc.unsplit(case)
+    assert_close(out.cpu().numpy(), ref, "4096 rows")
