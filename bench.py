@@ -3,26 +3,29 @@
 Workload: B=1, H=16, kv_lora_rank 512, rope 64, fp16, block 32, contexts
 32768 / 49152 / 65536 / 81920 / 98304 / 131072 tokens (N(0,1) latents, random
 block permutation), partitions chosen by the planner. One step = one layer
-call at each of the six contexts through mla_decode (the paired partial
-kernel writing every CTA pair's part, then the entries merge kernel as a
-programmatic dependent launch); the six caches live in
-disjoint memory (528 MB together, > L2), so every call streams its latent from
-HBM.
+call at each of the six contexts through mla_decode's default (the paired
+partial kernel writing every CTA pair's part, the entries merge kernel, its
+programmatic dependent, merging them); the six caches live in disjoint memory (528 MB together, > L2),
+so every call streams its latent from HBM. Each call's tables and the cache
+rows before its window are complete before the step (tables_ready,
+prefix_ready).
 
 Printed: one JSON line. `value` = mean microseconds per layer call over the
 sweep (device time, inputs resident, each step replayed from one CUDA graph);
 `e2e` = the same through mla_decode with host buffers (queries, block tables
 and plan of the six calls copied in with one copy from one pinned buffer, the
-six outputs copied out with one copy, every step); `roofline` = the partial
-layer call's algorithmic HBM bytes / its CUDA-event time in the timed graph
-against the measured copy bandwidth; `cpu_baseline` = the f64 oracle on the host cores. Outside the
-timed region: `single_launch_us` (the same step with each layer call as one
-launch, the merge inside the paired kernel), `per_ctx` (each context alone,
-its planned split, a single cold call after an L2 flush and the host
-planner's time per call), `trials` (median / min / max over five more K-step
-trials), `many_heads` (the many-head workload), `verify_windows` and
-`batch_grid`. `--impl reference` times the oracle itself on the same
-workload; `--gpus N` without a launcher starts N ranks (one replica per GPU).
+six outputs copied out with one copy, every step); `roofline` = the layer
+call's algorithmic HBM bytes / its CUDA-event time in the timed graph against
+the measured copy bandwidth; `cpu_baseline` = the f64 oracle on the host
+cores. Outside the timed region: `without_prefix_ready_us` (every cache read after the preceding kernel has
+finished), `single_launch_us` (one launch per call whose last CTAs merge the
+chunk partials), `partial_kernel_alone` (the ABI's mla_decode_partial),
+`per_ctx` (each context alone, its planned split, a single cold call after an
+L2 flush and the host planner's time per call), `trials` (median / min / max
+over five more K-step trials), `many_heads` (the many-head workload),
+`verify_windows` and `batch_grid`. `--impl reference` times the oracle itself
+on the same workload; `--gpus N` without a launcher starts N ranks (one
+replica per GPU).
 """
 from __future__ import annotations
 
@@ -644,22 +647,27 @@ def run_ours(args, rank, world):
                 c[tag + "ind"] = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
                 c[tag + "ws"] = rt.alloc_workspace(plan.num_chunks, k, plan.cluster_ctas, 1, H)
                 c[tag + "dws"] = rt.alloc_decode_workspace(1, plan.num_chunks, k, plan.cluster_ctas, 1, H)
-            # the tables are uploaded before the step and no kernel of the step writes them
-            c["ldesc"] = rt.make_desc(dc, c["chunks"], kernel, c["plan"].cluster_ctas, stream,
+            # the tables are uploaded before the step and no kernel of the step writes them or the caches:
+            # each call may read its tables and its first cache tiles while the kernel before it finishes
+            for key, early in (("ldesc", True), ("ldesc0", False)):
+                c[key] = rt.make_desc(dc, c["chunks"], kernel, c["plan"].cluster_ctas, stream,
                                       c["plan"].clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1, c["dws"],
-                                      tables_ready=True)
+                                      tables_ready=True, prefix_ready=early)
             pk = c["pplan"].clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
             c["desc"] = rt.make_desc(dc, c["pchunks"], kernel, c["pplan"].cluster_ctas, stream, pk, c["pws"],
                                      tables_ready=True)
             c["sdesc"] = rt.make_desc(dc, c["pchunks"], kernel, c["pplan"].cluster_ctas, stream, pk, c["pdws"],
-                                      tables_ready=True, single_launch=True)
+                                      tables_ready=True, decode_merge=nb.MLA_DECODE_MERGE_TICKETS)
             calls.append(c)
     torch.cuda.synchronize()
 
     def layer(c):  # one decode layer call through mla_decode (its default: partial kernel, then merge kernel)
         rt.decode(c["dc"], c["part"], c["lse"], c["ind"], c["out"], desc=c["ldesc"])
 
-    def single(c):  # the same call as one launch (the merge inside the paired kernel)
+    def layer0(c):  # the same call with every cache read after the preceding kernel has finished
+        rt.decode(c["dc"], c["part"], c["lse"], c["ind"], c["out"], desc=c["ldesc0"])
+
+    def single(c):  # one launch that merges the chunk partials (their last CTAs merge)
         rt.decode(c["dc"], c["ppart"], c["plse"], c["pind"], c["out"], desc=c["sdesc"])
 
     def partial(c):  # the ABI's two calls: mla_decode_partial ...
@@ -674,6 +682,7 @@ def run_ours(args, rank, world):
         for _ in range(max(3, args.warmup)):
             for c in calls:
                 layer(c)
+                layer0(c)
                 partial(c)
                 merge(c)
                 single(c)
@@ -688,9 +697,13 @@ def run_ours(args, rank, world):
     # single-launch calls, are reported beside it. Every graph sweeps the six disjoint caches, so
     # every launch streams its latent from HBM.
     g_step, g_part, g_two = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    g_late = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step, stream=stream):
         for c in calls:
             layer(c)
+    with torch.cuda.graph(g_late, stream=stream):
+        for c in calls:
+            layer0(c)
     with torch.cuda.graph(g_part, stream=stream):
         for c in calls:
             partial(c)
@@ -702,6 +715,7 @@ def run_ours(args, rank, world):
             g_step.replay()
             g_part.replay()
             g_two.replay()
+            g_late.replay()
     stream.synchronize()
 
     K = args.steps
@@ -741,14 +755,18 @@ def run_ours(args, rank, world):
 
     # the same step with single-launch layer calls (the merge inside the paired kernel), outside the
     # timed region, for comparison
-    e2 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    e2 = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     with torch.cuda.stream(stream):
         e2[0].record(stream)
         for _ in range(K):
             g_two.replay()
         e2[1].record(stream)
+        for _ in range(K):
+            g_late.replay()
+        e2[2].record(stream)
     stream.synchronize()
     single_launch_us = e2[0].elapsed_time(e2[1]) * 1e3 / (K * len(calls))
+    late_cache_us = e2[1].elapsed_time(e2[2]) * 1e3 / (K * len(calls))
 
     # per-context breakdown (not part of the timed region): one graph per call
     per_ctx = []
@@ -858,7 +876,7 @@ def run_ours(args, rank, world):
                             context_lens=dview(lay["lens"], torch.int32), case=dc.case)
         chunks = dview(lay["chunks"], torch.int32)
         desc = rt.make_desc(edc, chunks, kernel, c["plan"].cluster_ctas, stream, c["ldesc"].clusters_per_chunk,
-                            c["dws"], tables_ready=True)
+                            c["dws"], tables_ready=True, prefix_ready=True)
         e2e_calls.append(dict(dc=edc, desc=desc, ind=dview(lay["ind"], torch.int32), out=dout[j],
                               part=c["part"], lse=c["lse"]))
     h2d = off
@@ -940,6 +958,7 @@ def run_ours(args, rank, world):
         "per_ctx": per_ctx,
         "trials": trials,
         "single_launch_us": round(single_launch_us, 3),
+        "without_prefix_ready_us": round(late_cache_us, 3),
         "many_heads": many_heads,
         "verify_windows": verify,
         "batch_grid": grid,

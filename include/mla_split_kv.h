@@ -99,6 +99,10 @@ mla_status_t mla_device_query(int32_t device, mla_device_info_t* info);
 #define MLA_MERGE_ENTRIES 0
 #define MLA_MERGE_PARTIALS 1
 
+/* mla_decode_desc_t.decode_merge (see mla_decode) */
+#define MLA_DECODE_MERGE_ENTRIES 0
+#define MLA_DECODE_MERGE_TICKETS 1
+
 /* Planner input/output. The caller sets the inputs and provides the host
  * arrays; mla_plan fills the outputs. */
 typedef struct {
@@ -149,7 +153,7 @@ typedef struct {
  * k > 1, 1.8 us when the parts are merged as pair entries (merge_path
  * MLA_MERGE_ENTRIES) or 6 us + 0.3 us x 2k / cluster when each chunk's parts
  * are first merged into its partial (MLA_MERGE_PARTIALS), plus 0.6 us per
- * further round of 64 entries in the entries merge; constants fitted to
+ * further round of 96 entries in the entries merge; constants fitted to
  * layer-call times measured on GB300.
  *
  * context_lens_host: host [B] int32, each >= 0. dev: from mla_device_query or
@@ -208,12 +212,25 @@ typedef struct {
                                  caches are always read after it. 0 (default):
                                  every input is read after the preceding kernel
                                  has finished. Other values: INVALID_ARG.       */
-  int32_t single_launch;      /* mla_decode only: 1 = merge inside the paired
-                                 16-row kernel's launch (one launch per layer
-                                 call, see mla_decode); 0 (default) = the
-                                 partial kernel and then a merge kernel, a
-                                 programmatic dependent launch. Other values:
-                                 INVALID_ARG. mla_decode_partial ignores it.   */
+  int32_t decode_merge;       /* mla_decode only, how the paired 16-row kernel's
+                                 parts reach `out`: MLA_DECODE_MERGE_ENTRIES
+                                 (0, default) or MLA_DECODE_MERGE_TICKETS (1),
+                                 see mla_decode. Other values: INVALID_ARG.
+                                 mla_decode_partial ignores it.                */
+  int32_t prefix_ready;       /* 1 (needs tables_ready = 1): the cache rows of
+                                 every position before each request's window
+                                 (positions < context_len - q_len) are final
+                                 before the kernel that precedes this call in
+                                 the stream ends (that kernel may write the
+                                 window's rows, as mla_cache_append of this
+                                 call's new tokens does). The paired 16-row
+                                 kernel then loads its first tiles (one per
+                                 tile slot) that lie wholly before the window
+                                 while that kernel finishes; results are the
+                                 same bits. Other kernels ignore it. 0
+                                 (default): caches are read after it. Other
+                                 values, or 1 with tables_ready = 0:
+                                 INVALID_ARG.                                  */
 } mla_decode_desc_t;
 
 /*
@@ -334,27 +351,29 @@ mla_status_t mla_merge_states(const float* partials, const float* lse, const int
  * merged as mla_merge_states merges it, over the request-major offsets o_indptr,
  * into `out` (rounded once to out_dtype) and `out_lse` (NULL allowed).
  *
- * Three ways, by kernel and desc->single_launch:
- *  - the paired 16-row fp16 kernel (q_len*H <= 16, clusters of 2..16 CTAs), the
- *    default (single_launch = 0): the partial kernel skips its in-cluster combine
- *    and writes every CTA pair's unnormalized part (O over its tokens, row maxima
- *    and sums) to the workspace; a merge kernel launched as its programmatic
- *    dependent combines all the parts of a request straight into `out` (the merge
- *    of the pages' contract, M = max, weights 2^(m - M), applied to the parts;
- *    the same bits on every call for the same plan). `partials` and `lse` are
- *    not written.
- *  - the paired kernel with single_launch = 1: ONE launch. "[kernel] Wire MLA
- *    split-KV decode" (vllm-metal PR #601), *What changed*, avoids a temporary by
- *    letting partition 0 write straight into the output; here the reduce moves
- *    into the partial kernel: once a chunk's partial is written (to
- *    partials / lse, as mla_decode_partial writes it), an acquire-release ticket
- *    per (request, column slice) counts it, and the CTA that counts a request's
- *    last chunk merges that slice of all the request's partials into `out` with
- *    the merge kernel's arithmetic in its order: the same bits as
- *    mla_decode_partial + mla_merge_states. Measured on GB300 it is slower than
- *    the default (the dependent merge kernel is resident before the partial
- *    kernel ends and is released by the grid's completion, while the ticket adds
- *    a device-scope round trip in the last CTAs); kept as an option.
+ * The ways, by kernel and desc->decode_merge:
+ *  - the paired 16-row fp16 kernel (q_len*H <= 16, clusters of 2..16 CTAs) with
+ *    MLA_DECODE_MERGE_ENTRIES (default): the partial kernel skips its
+ *    in-cluster combine and writes every CTA pair's unnormalized part (O over
+ *    its tokens, row maxima and sums) to the workspace; a merge kernel launched
+ *    as its programmatic dependent combines all the parts of a request
+ *    straight into `out` (the merge of the pages' contract, M = max, weights
+ *    2^(m - M), applied to the parts; the same bits on every call for the same
+ *    plan). Its CTAs fit on an SM beside the partial kernel's, so it is
+ *    resident before the partial kernel ends; it releases its own dependent at
+ *    once (every kernel of this library waits for the kernel before it to
+ *    complete before reading anything). `partials` and `lse` are not written.
+ *  - the paired kernel with MLA_DECODE_MERGE_TICKETS: ONE launch that writes
+ *    the chunk partials. "[kernel] Wire MLA split-KV decode" (vllm-metal PR
+ *    #601), *What changed*, avoids a temporary by letting partition 0 write
+ *    straight into the output; here the reduce moves into the partial kernel:
+ *    once a chunk's partial is written (to partials / lse, as
+ *    mla_decode_partial writes it), an acquire-release ticket per (request,
+ *    column slice) counts it, and the CTA that counts a request's last chunk
+ *    merges that slice of all the request's partials into `out` with the merge
+ *    kernel's arithmetic in its order: the same bits as mla_decode_partial +
+ *    mla_merge_states. Measured on GB300 it is slower than the default (the
+ *    last CTAs do the whole merge); kept as an option.
  *  - other kernels: mla_decode_partial, then mla_merge_states, on `stream`
  *    (partials / lse written as those calls write them).
  *
@@ -375,7 +394,7 @@ mla_status_t mla_merge_states(const float* partials, const float* lse, const int
  *            Calls sharing a workspace must not overlap in time.
  * Returns what mla_decode_partial and mla_merge_states return (and
  * MLA_ERR_INVALID_ARG for a NULL or misaligned o_indptr / out / out_lse, a
- * short workspace or a bad single_launch value, MLA_ERR_UNSUPPORTED for another
+ * short workspace or a bad decode_merge value, MLA_ERR_UNSUPPORTED for another
  * out_dtype). No counterpart on the pages as one call: the pages launch a
  * partial kernel and a reduce kernel.
  */
@@ -386,8 +405,8 @@ mla_status_t mla_decode(const void* q_absorbed, const void* q_pe, const void* ck
 
 /* Workspace bytes of mla_decode on the paired kernel, one layout for both of
  * its ways: B * 16 uint32 request tickets and num_chunks * q_len * H fp32 LSE
- * copies (the single launch's; each block 256-byte aligned), then two uint32
- * tickets per chunk (a 256-byte block; the single launch's spread plans), then
+ * copies (the TICKETS way's; each block 256-byte aligned), then two uint32
+ * tickets per chunk (a 256-byte block; the TICKETS way's spread plans), then
  * E = num_chunks * max(1, clusters_per_chunk) * cluster_ctas / 2 entries (one
  * per CTA pair) of [q_len, H, 512] fp32 and E x [2, q_len, H, 2] fp32 row
  * maxima and sums. The default way writes only the entries, never a ticket,
@@ -440,7 +459,9 @@ mla_status_t mla_merge_unembed(const float* partials, const float* lse, const in
 
 /*
  * mla_check_device_errors -- synchronize `stream`, read and clear the device
- * error word the kernels set (bounded-wait timeout, out-of-range page id).
+ * error word the kernels set (bit 0: a bounded wait timed out; bit 1: a page
+ * id outside the pool; bit 2: a kernel found its launch unusable -- the
+ * paired kernel's shared memory not 1024-byte aligned -- and did nothing).
  * *code_out (nullable) receives the raw word. When the word was set it also
  * zeroes the current device's mla_decode_partial_static scratch (if set up),
  * since a call that stopped early may have left its tickets counted; a

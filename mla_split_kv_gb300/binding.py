@@ -27,6 +27,7 @@ MLA_F16, MLA_BF16, MLA_F32 = 0, 1, 2
 MLA_STATIC_WORKSPACE_BYTES = 4 * 1024 * 1024
 MLA_KERNEL_AUTO, MLA_KERNEL_SIMT, MLA_KERNEL_TC = 0, 1, 2
 MLA_MERGE_ENTRIES, MLA_MERGE_PARTIALS = 0, 1
+MLA_DECODE_MERGE_ENTRIES, MLA_DECODE_MERGE_TICKETS = 0, 1
 
 CTR_PARTIAL_SIMT, CTR_PARTIAL_TC, CTR_MERGE, CTR_REJECTED, CTR_CTAS, CTR_DECODE_FUSED, CTR_WRAP = range(7)
 NUM_COUNTERS = 7
@@ -84,7 +85,8 @@ class mla_decode_desc_t(ctypes.Structure):
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_uint64),
         ("tables_ready", ctypes.c_int32),
-        ("single_launch", ctypes.c_int32),
+        ("decode_merge", ctypes.c_int32),
+        ("prefix_ready", ctypes.c_int32),
     ]
 
 

@@ -191,7 +191,10 @@ mla_status_t check_decode(const void* q_absorbed, const void* q_pe, const void* 
   if (d->dtype != MLA_F16 && d->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
   if (d->causal != 0 && d->causal != 1) return MLA_ERR_INVALID_ARG;
   if (d->tables_ready != 0 && d->tables_ready != 1) return MLA_ERR_INVALID_ARG;
-  if (d->single_launch != 0 && d->single_launch != 1) return MLA_ERR_INVALID_ARG;
+  if (d->decode_merge != MLA_DECODE_MERGE_ENTRIES && d->decode_merge != MLA_DECODE_MERGE_TICKETS)
+    return MLA_ERR_INVALID_ARG;
+  if (d->prefix_ready != 0 && d->prefix_ready != 1) return MLA_ERR_INVALID_ARG;
+  if (d->prefix_ready == 1 && d->tables_ready != 1) return MLA_ERR_INVALID_ARG;
   if (d->kernel < MLA_KERNEL_AUTO || d->kernel > MLA_KERNEL_TC) return MLA_ERR_INVALID_ARG;
   const int32_t C0 = d->cluster_ctas;
   if (C0 != 0 && C0 != 1 && C0 != 2 && C0 != 4 && C0 != 8 && C0 != 16) return MLA_ERR_INVALID_ARG;
@@ -295,6 +298,7 @@ mla_status_t launch_decode(const void* q_absorbed, const void* q_pe, const void*
   p.num_parts = (d->chunks == nullptr) ? num_partitions : 1;
   p.causal = d->causal;
   p.tables_ready = d->tables_ready;
+  p.prefix_ready = d->prefix_ready;
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
 
   p.subs = subs;
@@ -384,21 +388,22 @@ mla_status_t mla_decode(const void* q_absorbed, const void* q_pe, const void* ck
   const int rows_total = d->num_heads * d->q_len;
   const bool paired = d->kernel != MLA_KERNEL_SIMT &&
                       mla::tc128_supports(rows_total, d->dtype == MLA_BF16, launch_cluster(d, N));
-  const bool fused = paired && d->single_launch == 1;
+  const bool fused = paired && d->decode_merge == MLA_DECODE_MERGE_TICKETS;
   if (paired && !fused) {
     // the paired kernel writes every CTA pair's part to the workspace and exits; the entries merge
-    // kernel, a programmatic dependent launch, combines a request's parts straight into the output
+    // kernel, a programmatic dependent launch resident beside it, combines a request's parts
+    // straight into the output
     const int32_t C = launch_cluster(d, N);
     const uint64_t head = round256(static_cast<uint64_t>(d->num_requests) * mla::kSliceTickets * 4) +
-                          round256(static_cast<uint64_t>(N) * rows_total * 4);  // the single launch's blocks
+                          round256(static_cast<uint64_t>(N) * rows_total * 4);  // the TICKETS way's blocks
     const uint64_t need = head + entries_ws_bytes(N, d->clusters_per_chunk, C, d->q_len, d->num_heads);
     if (d->workspace == nullptr || !aligned(d->workspace, 16) || d->workspace_bytes < need)
       return reject(MLA_ERR_INVALID_ARG);
     uint8_t* ws = static_cast<uint8_t*>(d->workspace) + head;
+    const int32_t k = d->clusters_per_chunk > 1 ? d->clusters_per_chunk : 1;
     mla_status_t st = launch_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
                                     num_partitions, partials, lse, d, N, ws, FusedMerge{}, true);
     if (st != MLA_OK) return st;
-    const int32_t k = d->clusters_per_chunk > 1 ? d->clusters_per_chunk : 1;
     const uint64_t entries = static_cast<uint64_t>(N) * k * (C / 2);
     mla::EntryMergeParams mp;
     mp.ws_partials = reinterpret_cast<const float*>(ws + round256(static_cast<uint64_t>(N) * 2 * 4));

@@ -500,7 +500,6 @@ __device__ __forceinline__ uint32_t ticket_add_acq_rel(uint32_t* t) {
 __device__ __forceinline__ void ticket_reset(uint32_t* t) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(t) : "memory");
 }
-
 // ---------------------------------------------------------------------------
 // Work of one CTA: request, chunk bounds, output slot, token sub-range.
 // ---------------------------------------------------------------------------

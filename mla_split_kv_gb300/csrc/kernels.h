@@ -19,6 +19,7 @@ constexpr int kTileBytes = kBoxesPerTile * kBoxBytes;  // 72 KB
 // Device error bits (the per-file g_device_error words).
 constexpr uint32_t MLA_DEVERR_TIMEOUT = 1u;
 constexpr uint32_t MLA_DEVERR_BAD_PAGE = 2u;
+constexpr uint32_t MLA_DEVERR_CONFIG = 4u;  // a kernel found its launch unusable (shared memory alignment)
 
 struct PartialParams {
   const uint16_t* q_abs;       // [B, q_len, H, 512]
@@ -35,6 +36,7 @@ struct PartialParams {
   int32_t num_parts;           // uniform split when chunks == null
   int32_t causal;
   int32_t tables_ready;        // chunks / context_lens / block_table may be read before the dependency wait
+  int32_t prefix_ready;        // cache rows before each request's window may be read before the dependency wait
   uint64_t timeout_ns;
   // a chunk spread over `subs` clusters (the paired 16-row kernel): grid.y = chunks * subs.
   // One entry per CTA pair of a chunk (subs * cluster / 2 of them): its unnormalized O^T in

@@ -106,24 +106,33 @@ __global__ void __launch_bounds__(kWarps * 32) mla_merge_kernel(const MergeParam
     p.out_lse[br] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
 }
 
-// The merge of the paired kernel's pair entries into the output (mla_decode's default path on that
+// The merge of the paired kernel's pair entries into the output (mla_decode's default on that
 // kernel). Entry e holds one CTA pair's unnormalized O (its tokens, all 512 columns: each CTA of
 // the pair wrote its 256), its row maximum m_e and its row sum l_e relative to m_e. Per (request,
 // row): M = max_e m_e, w_e = 2^(m_e - M) (0 for m_e = -inf), out = sum_e w_e O_e / sum_e w_e l_e,
 // out_lse = M + log2 sum_e w_e l_e -- the merge of the pages' contract, applied to unnormalized
-// parts. One warp per (request, row, 16 columns): lane = 4 g + q takes column quad q of the
-// entries g, g + 8, g + 16, ... (up to 8 per lane in one round of loads), sums them in entry
-// order, and the warp adds the eight entry groups with a fixed shuffle tree, so the result is
-// the same bits on every call. 256 warps per request row block keep many SMs loading at once.
+// parts. One warp per (request, row, 16 columns): lane = 4 g + q takes column quad q of the entries
+// g, g + 8, g + 16, ... (up to 12 per lane, 96 entries, in one round of loads), sums them in entry
+// order, and the warp adds the eight entry groups with a fixed shuffle tree, so the result is the
+// same bits on every call.
+//
+// Residency: a CTA is 128 threads of at most 128 registers and no shared memory, so one fits on an
+// SM beside a CTA of the paired kernel (384 threads x 128 registers, 226 KB). The merge of call n
+// is therefore resident while its partial kernel runs, and it releases its own dependent (the next
+// call's partial kernel) at once: that kernel waits for this one to complete before it reads
+// anything, and its CTAs take each SM as the partial CTA there leaves, beside this merge's CTA.
 constexpr int kEntryWarps = 4;
+constexpr int kEntryGroups = 8;                  // entry groups per warp
+constexpr int kEntriesPerLane = 12;              // per round of loads
+constexpr int kEntryRound = kEntryGroups * kEntriesPerLane;
 
-__global__ void __launch_bounds__(kEntryWarps * 32) mla_merge_entries_kernel(const EntryMergeParams p) {
-  pdl_wait();  // the entries are complete once the partial kernel has
+__global__ void __launch_bounds__(kEntryWarps * 32, 4) mla_merge_entries_kernel(const EntryMergeParams p) {
   pdl_launch_dependents();
+  pdl_wait();  // the entries are complete once the partial kernel has
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long gw = static_cast<long long>(blockIdx.x) * kEntryWarps + warp;
   if (gw >= static_cast<long long>(p.B) * p.rows * 32) return;
-  const int cb = static_cast<int>(gw & 31);   // columns [16 cb, 16 cb + 16)
+  const int cb = static_cast<int>(gw & 31);  // columns [16 cb, 16 cb + 16)
   const long long br = gw >> 5;              // b * rows + row
   const int b = static_cast<int>(br / p.rows), row = static_cast<int>(br % p.rows);
   const int e0 = p.o_indptr[b] * p.epc, e1 = p.o_indptr[b + 1] * p.epc;
@@ -133,23 +142,23 @@ __global__ void __launch_bounds__(kEntryWarps * 32) mla_merge_entries_kernel(con
   const float* const obase = p.ws_partials + static_cast<long long>(row) * kRank + col;
   const float* const mlbase = p.ws_lse + static_cast<long long>(row) * 2;  // copy 0 of the entry's m, l
   const long long mlstride = 4LL * p.rows;                                  // one entry's two copies
-  // round 0: the first 64 entries' m, l and values (the values do not depend on the weights)
-  float2 ml0[8];
-  float4 v0[8];
+  // round 0: the first 96 entries' m, l and values (the values do not depend on the weights)
+  float2 ml0[kEntriesPerLane];
+  float4 v0[kEntriesPerLane];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int e = e0 + g + 8 * j;
+  for (int j = 0; j < kEntriesPerLane; ++j) {
+    const int e = e0 + g + kEntryGroups * j;
     const bool in = e < e1;
     ml0[j] = in ? __ldcg(reinterpret_cast<const float2*>(mlbase + e * mlstride)) : make_float2(-INFINITY, 0.f);
     v0[j] = in ? __ldcg(reinterpret_cast<const float4*>(obase + e * ostride)) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   float M = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) M = fmaxf(M, ml0[j].x);
-  for (int base = e0 + 64; base < e1; base += 64)
+  for (int j = 0; j < kEntriesPerLane; ++j) M = fmaxf(M, ml0[j].x);
+  for (int base = e0 + kEntryRound; base < e1; base += kEntryRound)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = base + g + 8 * j;
+    for (int j = 0; j < kEntriesPerLane; ++j) {
+      const int e = base + g + kEntryGroups * j;
       if (e < e1) M = fmaxf(M, __ldcg(mlbase + e * mlstride));
     }
   M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
@@ -158,10 +167,10 @@ __global__ void __launch_bounds__(kEntryWarps * 32) mla_merge_entries_kernel(con
   float den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
-    for (int base = e0; base < e1; base += 64) {
+    for (int base = e0; base < e1; base += kEntryRound) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int e = base + g + 8 * j;
+      for (int j = 0; j < kEntriesPerLane; ++j) {
+        const int e = base + g + kEntryGroups * j;
         float2 ml;
         float4 v;
         if (base == e0) {

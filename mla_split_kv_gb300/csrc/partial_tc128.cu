@@ -84,7 +84,9 @@ constexpr uint32_t kQChunk = kNR * 128;                     // [16 x 64] fp16, 1
 constexpr uint32_t kQKpe = kNR * kKpeCols * 2;              // [16 x 32] fp16, 64-byte swizzle: 1 KB
 constexpr uint32_t kOffSmall = kOffQ + kHalfBoxes * kQChunk + kQKpe;  // 225 KB
 constexpr uint32_t kSmallBytes = 1024;
-constexpr uint32_t kSmem = kOffSmall + kSmallBytes + 1024;  // + alignment slack
+// no alignment slack: the dynamic shared memory of a CTA starts 1024-byte aligned (checked at run
+// time), and at 226 KB a CTA of the entries merge kernel (no shared memory) still fits on the SM
+constexpr uint32_t kSmem = kOffSmall + kSmallBytes;
 // in the kpe part of a slot, after the tile's score product: the peer's partial S, then P^T
 constexpr uint32_t kXBuf = kNR * kT * 4;                    // [128 tokens][16 rows] fp32: 8 KB
 constexpr uint32_t kPBytes = 2 * kNR * 128;                 // P^T [16 x 128 tokens]: two 64-token atoms
@@ -116,7 +118,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mla_partial_tc128_kernel(const __grid_constant__ CUtensorMap tm_pages, const __grid_constant__ CUtensorMap tm_kpe_half,
                              const PartialParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  // the swizzled tile and Q layouts need a 1024-byte aligned base, and the size leaves no slack to
+  // align it: a launch that breaks this (it does not happen on sm_103a) flags it and does nothing
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) flag_error(MLA_DEVERR_CONFIG);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* qs = smem + kOffQ;
   Small* sm = reinterpret_cast<Small*>(smem + kOffSmall);
   volatile int32_t* abort_flag = &sm->abort_flag;
@@ -173,48 +181,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int npages_req = (w.L + p.bs - 1) / p.bs;
     win_pid = (q < npages_req && q < p.max_blocks) ? checked_page(p, w.b, q) : -1;
   };
+  // producers: warp kMmaWarp + 1 + k0 loads pages k0, k0 + kPageWarps, ... of each tile
+  const int k0 = warp - kMmaWarp - 1;
+  auto page_of = [&](int pg) -> int {  // warp-uniform pg
+    if ((pg & ~31) != win_base) load_window(pg);
+    return __shfl_sync(0xffffffffu, win_pid, pg & 31);
+  };
+  // the physical pages of this warp's share of tile i (block-table reads); returns their number
+  auto tile_pids = [&](int i, int* pids) -> int {
+    const int tok0 = w.sub0 + i * kT;
+    const int pg0 = tok0 / p.bs;
+    const int npg = (min(kT, w.sub1 - tok0) + p.bs - 1) / p.bs;
+    const int mine = (npg > k0) ? (npg - k0 + kPageWarps - 1) / kPageWarps : 0;
+#pragma unroll
+    for (int m = 0; m < kMaxPagesPerWarp; ++m) pids[m] = (m < mine) ? page_of(pg0 + k0 + m * kPageWarps) : -1;
+    return mine;
+  };
+  // the loads of those pages into the slot of tile i (free), counted on its full barrier; lane m
+  // issues page m (TMA issue from several lanes overlaps)
+  auto tile_issue = [&](int i, const int* pids, int mine, uint64_t pol) {
+    const int s = i % kSlots;
+    uint8_t* slot = smem + kOffTile + s * kTileSlot;
+    if (lane == 0) mbar_arrive_expect_tx(&sm->full[s], static_cast<uint32_t>(mine * p.bs * (kHalfCols + kKpeCols) * 2));
+    __syncwarp();
+#pragma unroll
+    for (int m = 0; m < kMaxPagesPerWarp; ++m) {
+      if (lane == m && m < mine) {
+        const int j = k0 + m * kPageWarps;  // page of the tile
+        tma_load_4d(slot + j * p.bs * (kHalfCols * 2), &tm_pages, 0, 0, kHalfBoxes * half, pids[m] * (p.bs / 8),
+                    &sm->full[s], pol);
+        tma_load_2d(slot + kCkvBytes + j * p.bs * (kKpeCols * 2), &tm_kpe_half, kKpeCols * half, pids[m] * p.bs,
+                    &sm->full[s], pol);
+      }
+    }
+  };
+  int issued = -1;  // producers: the last tile whose loads this warp issued
   if (p.tables_ready) {
     w = cta_work(p, kNR, kT, pair_index, subs * cluster_pairs, chunk);
     if (warp > kMmaWarp && w.sub1 > w.sub0) load_window(w.sub0 / p.bs);
   }
   // the tensor-map descriptors are kernel parameters, not data of the preceding kernel: fetch them
-  // now, so the first page loads after the wait do not pay for it
+  // now, so the first page loads do not pay for it
   if (warp == kMmaWarp + 1 && lane == 0) {
     tma_prefetch_desc(&tm_pages);
     tma_prefetch_desc(&tm_kpe_half);
+  }
+  // prefix_ready: the cache rows before each request's window are final before the preceding kernel
+  // ends, so the first tiles (one per slot) whose tokens all lie before the window are loaded while
+  // it finishes; the window's own rows (which that kernel may be writing) only after the wait
+  if (p.prefix_ready && p.tables_ready && warp > kMmaWarp) {
+    const uint64_t pol = l2_policy_evict_first();
+    const int n = (w.sub1 - w.sub0 + kT - 1) / kT;
+    const int before = w.L - p.q_len;  // first position of the window
+    for (int i = 0; i < min(n, kSlots); ++i) {
+      if (min(w.sub0 + (i + 1) * kT, w.sub1) > before) break;
+      int pids[kMaxPagesPerWarp];
+      const int mine = tile_pids(i, pids);
+      tile_issue(i, pids, mine, pol);
+      issued = i;
+    }
   }
   pdl_wait();
   pdl_launch_dependents();  // the merge of these partials may be scheduled now; it waits for this grid
   if (!p.tables_ready) w = cta_work(p, kNR, kT, pair_index, subs * cluster_pairs, chunk);
   const int ntiles = (w.sub1 - w.sub0 + kT - 1) / kT;
   // single-launch decode: request b's chunk slots, whose partials this launch also merges
-  const bool fused = p.out != nullptr;
+  const bool fused = p.out != nullptr;  // the TICKETS way of mla_decode
   int req_lo = 0, req_hi = 0;
-  if (fused) request_slots(p, w.b, &req_lo, &req_hi);
+  if (fused && w.b >= 0 && w.b < p.B) request_slots(p, w.b, &req_lo, &req_hi);
 
   if (warp > kMmaWarp) {
     // ------------------------------------------------------------------ producers
-    const int k0 = warp - kMmaWarp - 1;  // this warp loads pages k0, k0 + kPageWarps, ... of each tile
     const uint64_t pol = l2_policy_evict_first();
-    auto page_of = [&](int pg) -> int {  // warp-uniform pg
-      if ((pg & ~31) != win_base) load_window(pg);
-      return __shfl_sync(0xffffffffu, win_pid, pg & 31);
-    };
-    auto tile_pages = [&](int i, int* pg0, int* npg) {
-      const int tok0 = w.sub0 + i * kT;
-      *pg0 = tok0 / p.bs;
-      *npg = (min(kT, w.sub1 - tok0) + p.bs - 1) / p.bs;
-    };
-    int issued = -1;
-    for (int i = 0; i < ntiles; ++i) {
+    for (int i = issued + 1; i < ntiles; ++i) {
       const int s = i % kSlots;
       // the pages of tile i first: their block-table reads overlap the wait for the slot
-      int pg0, npg;
-      tile_pages(i, &pg0, &npg);
-      const int mine = (npg > k0) ? (npg - k0 + kPageWarps - 1) / kPageWarps : 0;
       int pids[kMaxPagesPerWarp];
-#pragma unroll
-      for (int m = 0; m < kMaxPagesPerWarp; ++m) pids[m] = (m < mine) ? page_of(pg0 + k0 + m * kPageWarps) : -1;
+      const int mine = tile_pids(i, pids);
       if (i >= kSlots) {  // tile i-3 released the slot
         int ok = 1;
         if (lane == 0) {
@@ -223,21 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
-      uint8_t* slot = smem + kOffTile + s * kTileSlot;
-      if (lane == 0)
-        mbar_arrive_expect_tx(&sm->full[s], static_cast<uint32_t>(mine * p.bs * (kHalfCols + kKpeCols) * 2));
-      __syncwarp();
-      // lane m issues this warp's page m (TMA issue from several lanes overlaps)
-#pragma unroll
-      for (int m = 0; m < kMaxPagesPerWarp; ++m) {
-        if (lane == m && m < mine) {
-          const int j = k0 + m * kPageWarps;  // page of the tile
-          tma_load_4d(slot + j * p.bs * (kHalfCols * 2), &tm_pages, 0, 0, kHalfBoxes * half, pids[m] * (p.bs / 8),
-                      &sm->full[s], pol);
-          tma_load_2d(slot + kCkvBytes + j * p.bs * (kKpeCols * 2), &tm_kpe_half, kKpeCols * half, pids[m] * p.bs,
-                      &sm->full[s], pol);
-        }
-      }
+      tile_issue(i, pids, mine, pol);
       issued = i;
     }
     // after an abort, let this warp's loads still in flight (the last three tiles it issued, one per

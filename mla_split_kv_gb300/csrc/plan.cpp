@@ -51,7 +51,7 @@ constexpr int64_t kPairTileTokens = 128;
 // the entries merge kernel (MLA_MERGE_ENTRIES), about one more tile (1.8 us); when each chunk's
 // parts are first merged into the chunk's partial by its last CTA (MLA_MERGE_PARTIALS), a ticket +
 // merge tail of ~6 us plus ~0.3 us per sub-partial for a 2-CTA cluster (the merge work per CTA
-// scales with k / C). The entries merge reads 64 entries per round of loads: 0.6 us per extra round.
+// scales with k / C). The entries merge reads 96 entries per round of loads: 0.6 us per extra round.
 constexpr double kTileUs = 1.75, kSpreadTailUs = 6.0, kMergeUsPerSub = 0.3;
 constexpr double kEntriesSpreadUs = 1.8, kEntriesRoundUs = 0.6;
 
@@ -62,7 +62,7 @@ double paired_cost_us(int64_t L, int64_t P, int64_t k, int C, int32_t merge_path
   double t = static_cast<double>(per_pair) * kTileUs;
   if (merge_path == MLA_MERGE_ENTRIES) {
     if (k > 1) t += kEntriesSpreadUs;
-    t += kEntriesRoundUs * static_cast<double>((pairs + 63) / 64 - 1);
+    t += kEntriesRoundUs * static_cast<double>((pairs + 95) / 96 - 1);
   } else if (k > 1) {
     t += kSpreadTailUs + kMergeUsPerSub * static_cast<double>(k) * 2.0 / static_cast<double>(C);
   }

@@ -55,7 +55,7 @@ def chunks_to_device(chunks: Sequence[Sequence[int]], device="cuda") -> torch.Te
 def make_desc(dc: DeviceCase, chunks_dev: Optional[torch.Tensor], kernel: int, cluster: int,
               stream: Optional[torch.cuda.Stream] = None, subs: int = 1,
               workspace: Optional[torch.Tensor] = None, tables_ready: bool = False,
-              single_launch: bool = False) -> nb.mla_decode_desc_t:
+              decode_merge: int = 0, prefix_ready: bool = False) -> nb.mla_decode_desc_t:
     c = dc.case
     d = nb.mla_decode_desc_t()
     d.num_requests = c.num_requests
@@ -76,7 +76,8 @@ def make_desc(dc: DeviceCase, chunks_dev: Optional[torch.Tensor], kernel: int, c
     d.workspace = workspace.data_ptr() if workspace is not None else None
     d.workspace_bytes = workspace.numel() if workspace is not None else 0
     d.tables_ready = 1 if tables_ready else 0
-    d.single_launch = 1 if single_launch else 0
+    d.decode_merge = decode_merge
+    d.prefix_ready = 1 if prefix_ready else 0
     # the descriptor holds raw device pointers: keep their tensors alive as long as it lives
     d._keep = (chunks_dev, workspace)
     return d
@@ -99,11 +100,12 @@ def alloc_decode_workspace(B: int, num_chunks: int, subs: int, cluster: int, q_l
 def decode(dc: DeviceCase, part: torch.Tensor, lse: torch.Tensor, o_indptr_dev: torch.Tensor, out: torch.Tensor,
            out_lse: Optional[torch.Tensor] = None, num_partitions: int = 1, desc: Optional[nb.mla_decode_desc_t] = None,
            **desc_kw) -> torch.Tensor:
-    """One decode layer call through mla_decode (two launches, or one with single_launch on the paired kernel)."""
+    """One decode layer call through mla_decode (its ways on the paired kernel chosen by decode_merge)."""
     d = desc if desc is not None else make_desc(dc, desc_kw.get("chunks_dev"), desc_kw.get("kernel", nb.MLA_KERNEL_AUTO),
                                                 desc_kw.get("cluster", 0), desc_kw.get("stream"),
                                                 desc_kw.get("subs", 1), desc_kw.get("workspace"),
-                                                desc_kw.get("tables_ready", False), desc_kw.get("single_launch", False))
+                                                desc_kw.get("tables_ready", False), desc_kw.get("decode_merge", 0),
+                                                desc_kw.get("prefix_ready", False))
     out_code = {torch.float32: nb.MLA_F32, torch.float16: nb.MLA_F16, torch.bfloat16: nb.MLA_BF16}[out.dtype]
     nb.mla_decode(dc.q_abs.data_ptr(), dc.q_pe.data_ptr(), dc.ckv.data_ptr(), dc.kpe.data_ptr(),
                   dc.block_table.data_ptr(), dc.context_lens.data_ptr(), float(dc.case.scale), num_partitions,

@@ -274,7 +274,10 @@ def call_partial(lib, d, P=2, ptrs=None):
     (dict(kernel=7), 2, nb.MLA_ERR_INVALID_ARG),
     (dict(causal=2), 2, nb.MLA_ERR_INVALID_ARG),
     (dict(tables_ready=2), 2, nb.MLA_ERR_INVALID_ARG),
-    (dict(single_launch=3), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(decode_merge=3), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(decode_merge=-1), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(prefix_ready=2, tables_ready=1), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(prefix_ready=1), 2, nb.MLA_ERR_INVALID_ARG),  # early cache reads need the tables early too
     (dict(), 0, nb.MLA_ERR_INVALID_ARG),
     (dict(num_requests=40000), 2, nb.MLA_ERR_UNSUPPORTED),
 ])
@@ -414,11 +417,11 @@ def call_decode(lib, d, P=2, o_indptr=FAKE, out=FAKE, out_dtype=nb.MLA_F16, out_
     (dict(cluster_ctas=2), dict(out=FAKE + 8), nb.MLA_ERR_INVALID_ARG),
     (dict(cluster_ctas=2), dict(out_lse=FAKE + 2), nb.MLA_ERR_INVALID_ARG),
     (dict(cluster_ctas=2), dict(out_dtype=7), nb.MLA_ERR_UNSUPPORTED),
-    (dict(cluster_ctas=2, single_launch=2), dict(), nb.MLA_ERR_INVALID_ARG),
-    (dict(cluster_ctas=2, single_launch=1), dict(), nb.MLA_ERR_INVALID_ARG),                  # no workspace
-    (dict(cluster_ctas=2, single_launch=1, workspace=FAKE, workspace_bytes=64), dict(), nb.MLA_ERR_INVALID_ARG),
+    (dict(cluster_ctas=2, decode_merge=5), dict(), nb.MLA_ERR_INVALID_ARG),
+    (dict(cluster_ctas=2, decode_merge=1), dict(), nb.MLA_ERR_INVALID_ARG),                  # no workspace
+    (dict(cluster_ctas=2, decode_merge=1, workspace=FAKE, workspace_bytes=64), dict(), nb.MLA_ERR_INVALID_ARG),
     (dict(cluster_ctas=2, num_heads=24), dict(), nb.MLA_ERR_UNSUPPORTED),
-    (dict(cluster_ctas=4, clusters_per_chunk=4, single_launch=1, workspace=FAKE, workspace_bytes=1024), dict(),
+    (dict(cluster_ctas=4, clusters_per_chunk=4, decode_merge=1, workspace=FAKE, workspace_bytes=1024), dict(),
      nb.MLA_ERR_INVALID_ARG),
     (dict(cluster_ctas=4, clusters_per_chunk=4), dict(), nb.MLA_ERR_INVALID_ARG),              # two launches, no ws
 ])

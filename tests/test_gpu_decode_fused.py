@@ -58,7 +58,7 @@ def both_paths(case, dc, chunks_dev, ind, N, kernel, C, k, out_dtype="f16", tabl
         out_lse = torch.full((B, q, H), float("nan"), device="cuda") if with_lse else None
         if fused:
             ws = ws_fused if ws_fused is not None else rt.alloc_decode_workspace(B, N, k, C, q, H)
-            desc = rt.make_desc(dc, chunks_dev, kernel, C, None, k, ws, tables_ready, single_launch=True)
+            desc = rt.make_desc(dc, chunks_dev, kernel, C, None, k, ws, tables_ready, decode_merge=nb.MLA_DECODE_MERGE_TICKETS)
             rt.decode(dc, part, lse, ind, out, out_lse, num_partitions=num_partitions, desc=desc)
         else:
             ws = rt.alloc_workspace(N, k, C, q, H)
@@ -95,7 +95,7 @@ def test_single_launch_equals_two_launches_at_every_bench_context(L):
     part, lse = rt.alloc_partials(plan.num_chunks, 1, 16)
     ws = rt.alloc_decode_workspace(1, plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, 16)
     rt.decode(dc, part, lse, ind, out32, kernel=nb.MLA_KERNEL_TC, cluster=plan.cluster_ctas, chunks_dev=chunks,
-              subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True, single_launch=True)
+              subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True, decode_merge=nb.MLA_DECODE_MERGE_TICKETS)
     heads = [0, 7, 15]
     ref, _ = orc.unsplit(case, heads=heads)
     assert_close(out32.cpu().numpy()[:, :, heads], ref[:, :, heads], f"fused L={L}")
@@ -147,7 +147,7 @@ def test_single_launch_bitwise_reproducible_and_workspace_reused():
         part, lse = rt.alloc_partials(plan.num_chunks, 1, 16)
         out = torch.empty((1, 1, 16, 512), dtype=torch.float16, device="cuda")
         rt.decode(dc, part, lse, ind, out, kernel=nb.MLA_KERNEL_TC, cluster=plan.cluster_ctas, chunks_dev=chunks,
-                  subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True, single_launch=True)
+                  subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True, decode_merge=nb.MLA_DECODE_MERGE_TICKETS)
         outs.append((part, lse, out))
     for other in outs[1:]:
         assert_same_bits(outs[0], other)
@@ -170,7 +170,7 @@ def test_decode_without_the_fused_merge_is_the_two_launches(H, dtype, kernel):
     assert_same_bits(fused, plain)
 
 
-def default_decode(case, dc, plan, chunks, ind, out_dtype="f32", ws=None):
+def default_decode(case, dc, plan, chunks, ind, out_dtype="f32", ws=None, mode=nb.MLA_DECODE_MERGE_ENTRIES):
     B = case.num_requests
     part, lse = rt.alloc_partials(plan.num_chunks, 1, 16)
     out = torch.empty((B, 1, 16, 512), dtype=TDT[out_dtype], device="cuda")
@@ -178,7 +178,7 @@ def default_decode(case, dc, plan, chunks, ind, out_dtype="f32", ws=None):
     if ws is None:
         ws = rt.alloc_decode_workspace(B, plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, 16)
     rt.decode(dc, part, lse, ind, out, out_lse, kernel=nb.MLA_KERNEL_TC, cluster=plan.cluster_ctas, chunks_dev=chunks,
-              subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True)
+              subs=plan.clusters_per_chunk, workspace=ws, tables_ready=True, decode_merge=mode)
     return out, out_lse
 
 
@@ -202,6 +202,41 @@ def test_default_decode_on_the_paired_kernel_every_bench_context(L):
     assert np.abs(out_lse.cpu().numpy()[:, :, heads] - ref_lse[:, :, heads]).max() <= MAX_ABS
     out2, lse2 = default_decode(case, dc, plan, chunks, ind)
     assert torch.equal(out, out2) and torch.equal(out_lse, lse2)
+
+
+@pytest.mark.parametrize("lens,P,C,k", [([700, 333, 5000], 2, 2, 2), ([1, 64, 65, 9000], 3, 4, 1),
+                                        ([20000] * 2, 3, 16, 1), ([0, 3000], 2, 2, 3), ([100000], 9, 2, 11)])
+def test_default_decode_several_requests_and_many_entries(lens, P, C, k):
+    """Several requests in one call (an empty request merges to zeros), and one request of 99 pair entries
+    (more than one round of the merge's loads): the oracle on every row, and a 16-bit output that is the fp32
+    output rounded once."""
+    case = gen.make_decode_case(35, lens, num_heads=16, block_size=32, dtype="f16")
+    dc = rt.upload(case)
+    B = len(lens)
+    ind = rt.uniform_indptr(B, P)
+    ws = rt.alloc_decode_workspace(B, B * P, k, C, 1, 16)
+    res = {}
+    for dt in ("f32", "f16"):
+        part, lse = rt.alloc_partials(B * P, 1, 16)
+        out = torch.full((B, 1, 16, 512), float("nan"), dtype=TDT[dt], device="cuda")
+        out_lse = torch.full((B, 1, 16), float("nan"), device="cuda")
+        rt.decode(dc, part, lse, ind, out, out_lse, num_partitions=P, kernel=nb.MLA_KERNEL_TC, cluster=C, subs=k,
+                  workspace=ws)
+        res[dt] = (out, out_lse)
+    out, out_lse = res["f32"]
+    assert torch.equal(res["f16"][0], out.to(torch.float16)) and torch.equal(res["f16"][1], out_lse)
+    ref, ref_lse = orc.unsplit(case) if B > 1 else orc.unsplit(case, heads=[0, 5, 15])
+    got = out.cpu().numpy()
+    if B == 1:
+        got = got[:, :, [0, 5, 15]]
+        ref, ref_lse = ref[:, :, [0, 5, 15]], ref_lse[:, :, [0, 5, 15]]
+    lse_got = out_lse.cpu().numpy() if B > 1 else out_lse.cpu().numpy()[:, :, [0, 5, 15]]
+    live = [i for i, L in enumerate(lens) if L > 0]
+    for i, L in enumerate(lens):
+        if L == 0:
+            assert np.all(got[i] == 0) and np.all(np.isneginf(lse_got[i]))
+    assert_close(got[live], ref[live], f"default decode {lens}")
+    assert np.abs(lse_got[live] - ref_lse[live]).max() <= MAX_ABS
 
 
 @pytest.mark.parametrize("C,k,bs,out_dtype", [(2, 1, 16, "f32"), (4, 3, 32, "f16"), (16, 1, 64, "bf16"),
@@ -273,3 +308,83 @@ def test_largest_row_count_causal_window_of_32_over_128_heads():
     assert nb.mla_get_counters()[nb.CTR_CTAS] == 2 * P * 32 * 2  # 32 row groups of one CTA pair per chunk
     ref, _ = orc.unsplit(case)
     assert_close(out.cpu().numpy(), ref, "4096 rows")
+
+
+def prefix_pair(case, dc, plan, chunks, ind, num_partitions=1, C=None, k=None, out_dtype="f32"):
+    """(out, out_lse) of mla_decode twice in a row without and then with prefix_ready (tables_ready on both)."""
+    B, q, H = case.num_requests, case.q_len, case.num_heads
+    N = plan.num_chunks if plan is not None else B * num_partitions
+    C = plan.cluster_ctas if plan is not None else C
+    k = plan.clusters_per_chunk if plan is not None else k
+    res = []
+    for early in (False, True):
+        part, lse = rt.alloc_partials(N, q, H)
+        out = torch.full((B, q, H, 512), float("nan"), dtype=TDT[out_dtype], device="cuda")
+        out_lse = torch.full((B, q, H), float("nan"), device="cuda")
+        ws = rt.alloc_decode_workspace(B, N, k, C, q, H)
+        desc = rt.make_desc(dc, chunks, nb.MLA_KERNEL_TC, C, None, k, ws, True, prefix_ready=early)
+        for _ in range(2):  # the second call follows a kernel of the first: its early loads overlap that kernel
+            rt.decode(dc, part, lse, ind, out, out_lse, num_partitions=num_partitions, desc=desc)
+        res.append((out, out_lse))
+    return res
+
+
+@pytest.mark.parametrize("L", [32768, 131072])
+def test_prefix_ready_gives_the_same_bits(L):
+    """prefix_ready only moves the loads of the first tiles before the dependency wait: the planner's plan at a
+    bench context gives the same bits with and without it, and matches the oracle."""
+    case = gen.make_decode_case(2, [L], num_heads=16, block_size=32, dtype="f16")
+    dc = rt.upload(case)
+    plan = nb.mla_plan([L], 16, 1, 32, nb.mla_device_query())
+    chunks = rt.chunks_to_device(plan.chunks)
+    ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
+    (o0, l0), (o1, l1) = prefix_pair(case, dc, plan, chunks, ind)
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    heads = [0, 9]
+    ref, _ = orc.unsplit(case, heads=heads)
+    assert_close(o1.cpu().numpy()[:, :, heads], ref[:, :, heads], f"prefix_ready L={L}")
+
+
+@pytest.mark.parametrize("q_len,C,k", [(1, 2, 1), (1, 4, 3), (1, 16, 1), (4, 2, 1)])
+def test_prefix_ready_ragged_windows(q_len, C, k):
+    """Ragged requests (contexts shorter than a tile, one tile, a last tile that holds the new token with prefix
+    positions, several tiles) on the paired kernel with and without spread partitions, and a causal window of
+    4 rows (64 rows: the 128-row kernel, which reads every cache row after the wait): the same bits with and
+    without prefix_ready, and the oracle on every row."""
+    lens = [2, 100, 129, 383, 384, 385, 2000]
+    case = gen.make_decode_case(39, lens, num_heads=16, q_len=q_len, block_size=32, dtype="f16", causal=q_len > 1)
+    dc = rt.upload(case)
+    P, B = 2, len(lens)
+    ind = rt.uniform_indptr(B, P)
+    (o0, l0), (o1, l1) = prefix_pair(case, dc, None, None, ind, num_partitions=P, C=C, k=k)
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    ref, _ = orc.unsplit(case)
+    assert_close(o1.cpu().numpy(), ref, f"prefix_ready windows q={q_len} C={C} k={k}")
+
+
+def test_prefix_ready_after_the_cache_write_of_the_window():
+    """The layer call's order: mla_cache_append writes the new tokens' rows, then mla_decode with prefix_ready
+    (the window's rows are read only after the append kernel has finished). Against the oracle on the
+    appended cache, on every row."""
+    lens = [5000, 130, 64]
+    q_len = 1  # 16 rows: the paired kernel, whose early loads stop before the new token's tile
+    case = gen.make_decode_case(40, lens, num_heads=16, q_len=q_len, block_size=32, dtype="f16")
+    dc = rt.upload(case)
+    rng = np.random.default_rng(41)
+    ckv_new = gen.to_bits(rng.standard_normal((3, q_len, 512)), "f16")
+    kpe_new = gen.to_bits(rng.standard_normal((3, q_len, 64)), "f16")
+    cn, kn = rt.to_device_16(ckv_new, "f16", "cuda"), rt.to_device_16(kpe_new, "f16", "cuda")
+    P, B = 2, 3
+    ind = rt.uniform_indptr(B, P)
+    part, lse = rt.alloc_partials(B * P, q_len, 16)
+    out = torch.empty((B, q_len, 16, 512), dtype=torch.float32, device="cuda")
+    ws = rt.alloc_decode_workspace(B, B * P, 1, 2, q_len, 16)
+    desc = rt.make_desc(dc, None, nb.MLA_KERNEL_TC, 2, None, 1, ws, True, prefix_ready=True)
+    rt.decode(dc, part, lse, ind, out, num_partitions=P, desc=desc)  # a kernel before the append
+    nb.mla_cache_append(cn.data_ptr(), kn.data_ptr(), dc.block_table.data_ptr(), dc.context_lens.data_ptr(), B, q_len,
+                        case.block_size, case.num_blocks, case.max_blocks, dc.ckv.data_ptr(), dc.kpe.data_ptr(),
+                        torch.cuda.current_stream().cuda_stream)
+    rt.decode(dc, part, lse, ind, out, num_partitions=P, desc=desc)
+    c2, k2 = orc.cache_append(case.ckv, case.kpe, case.block_table, case.context_lens, ckv_new, kpe_new, 32)
+    ref, _ = orc.unsplit(dataclasses.replace(case, ckv=c2, kpe=k2))
+    assert_close(out.cpu().numpy(), ref, "append then decode with prefix_ready")

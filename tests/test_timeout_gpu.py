@@ -103,3 +103,4 @@ def test_bounded_waits_run_out_then_the_context_is_usable(which):
     assert ok, f"after the timeout: max-abs {e[0]:.3e} rel-L2 {e[1]:.3e}"
     if ws is not None:  # a completed call leaves its tickets at zero
         assert int(ws[: 8 * plan.num_chunks].view(torch.int32).abs().sum()) == 0
+
