@@ -550,9 +550,9 @@ def run_profile_case(args):
     out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
     k = plan.clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
     ws = rt.alloc_decode_workspace(1, plan.num_chunks, k, plan.cluster_ctas, 1, H)
-    for _ in range(args.launches):  # the bench's layer call: mla_decode (one launch on the paired kernel)
+    for _ in range(args.launches):  # the bench's layer call: mla_decode's default (partial kernel + entries merge)
         rt.decode(dc, part, lse, ind, out, num_partitions=num_partitions, kernel=kernel, cluster=plan.cluster_ctas,
-                  chunks_dev=chunks_dev, subs=k, workspace=ws, tables_ready=True)
+                  chunks_dev=chunks_dev, subs=k, workspace=ws, tables_ready=True, prefix_ready=True)
     torch.cuda.synchronize()
     st, code = nb.mla_check_device_errors(None)
     print(json.dumps({"profile_ctx": L, "launches": args.launches, "partitions": plan.num_chunks,

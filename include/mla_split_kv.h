@@ -149,12 +149,14 @@ typedef struct {
  * least one 128-token tile); the partition count itself is not raised. For a
  * single long request on that kernel, P, the cluster size and k are chosen
  * by a time model among the plans whose P * k clusters are all co-resident
- * (one wave): ceil(tiles / CTA pairs) x 1.75 us per 128-token tile, plus, for
- * k > 1, 1.8 us when the parts are merged as pair entries (merge_path
- * MLA_MERGE_ENTRIES) or 6 us + 0.3 us x 2k / cluster when each chunk's parts
- * are first merged into its partial (MLA_MERGE_PARTIALS), plus 0.6 us per
- * further round of 96 entries in the entries merge; constants fitted to
- * layer-call times measured on GB300.
+ * (one wave): 1.75 us per 128-token tile of the busiest CTA pair (a chunk's
+ * tiles split evenly over its k * cluster/2 pairs), plus 0.6 us per further
+ * round of 96 entries in the entries merge when the parts are merged as pair
+ * entries (merge_path MLA_MERGE_ENTRIES: a spread costs nothing more), or,
+ * for k > 1, 6 us + 0.3 us x 2k / cluster when each chunk's parts are first
+ * merged into its partial (MLA_MERGE_PARTIALS); on a tie, more CTA pairs, then
+ * fewer clusters per partition. Constants fitted to steady-state layer-call
+ * times measured on GB300.
  *
  * context_lens_host: host [B] int32, each >= 0. dev: from mla_device_query or
  * hand-filled. Returns MLA_ERR_CAPACITY when N > plan->capacity (num_chunks

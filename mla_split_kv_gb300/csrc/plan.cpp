@@ -45,24 +45,27 @@ struct Candidate {
 
 constexpr int64_t kMaxSubs = 16;       // clusters per partition (the kernel's final merge reads at most 16)
 constexpr int64_t kPairTileTokens = 128;
-// Time model of the paired kernel for one request, fitted to layer-call times measured on GB300 over
-// partition counts, cluster sizes and spreads at 32K-128K tokens: a CTA pair takes ~1.75 us per
-// 128-token tile. Spreading a partition over k > 1 clusters costs, when every pair's part goes to
-// the entries merge kernel (MLA_MERGE_ENTRIES), about one more tile (1.8 us); when each chunk's
-// parts are first merged into the chunk's partial by its last CTA (MLA_MERGE_PARTIALS), a ticket +
+// Time model of the paired kernel for one request, fitted to steady-state layer-call times measured
+// on GB300 (back-to-back calls over caches larger than L2) over partition counts, cluster sizes and
+// spreads at 32K-128K tokens: a call takes about 1.75 us per 128-token tile of its busiest CTA
+// pair (a chunk's tiles are split evenly over its k * C/2 pairs) plus a fixed part common to every
+// plan. With the pairs' parts merged as entries (MLA_MERGE_ENTRIES) a spread costs nothing more,
+// except 0.6 us per further round of 96 entries in the merge; when each chunk's parts are first
+// merged into the chunk's partial by its last CTA (MLA_MERGE_PARTIALS), a spread adds a ticket +
 // merge tail of ~6 us plus ~0.3 us per sub-partial for a 2-CTA cluster (the merge work per CTA
-// scales with k / C). The entries merge reads 96 entries per round of loads: 0.6 us per extra round.
+// scales with k / C).
 constexpr double kTileUs = 1.75, kSpreadTailUs = 6.0, kMergeUsPerSub = 0.3;
-constexpr double kEntriesSpreadUs = 1.8, kEntriesRoundUs = 0.6;
+constexpr double kEntriesRoundUs = 0.6;
+constexpr int64_t kEntriesPerRound = 96;
 
-double paired_cost_us(int64_t L, int64_t P, int64_t k, int C, int32_t merge_path) {
-  const int64_t pairs = P * k * (C / 2);
-  const int64_t tiles = (L + kPairTileTokens - 1) / kPairTileTokens;
-  const int64_t per_pair = (tiles + pairs - 1) / pairs;
+double paired_cost_us(int64_t L, int64_t P, int64_t k, int C, int32_t merge_path, int64_t bs) {
+  const int64_t pairs_per_chunk = k * (C / 2);
+  const int64_t chunk_tiles = (chunk_len(L, P, bs) + kPairTileTokens - 1) / kPairTileTokens;
+  const int64_t per_pair = (chunk_tiles + pairs_per_chunk - 1) / pairs_per_chunk;
   double t = static_cast<double>(per_pair) * kTileUs;
   if (merge_path == MLA_MERGE_ENTRIES) {
-    if (k > 1) t += kEntriesSpreadUs;
-    t += kEntriesRoundUs * static_cast<double>((pairs + 95) / 96 - 1);
+    const int64_t entries = P * pairs_per_chunk;
+    t += kEntriesRoundUs * static_cast<double>((entries + kEntriesPerRound - 1) / kEntriesPerRound - 1);
   } else if (k > 1) {
     t += kSpreadTailUs + kMergeUsPerSub * static_cast<double>(k) * 2.0 / static_cast<double>(C);
   }
@@ -172,16 +175,18 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
       cand.subs = largest_k(cand.parts, N);
       if (paired_single) {
         // one long request: among the allowed partition counts and spreads take the fastest by the
-        // time model (ties: fewer clusters per partition)
+        // time model (ties: more CTA pairs busy, then fewer clusters per partition)
         const int64_t L = context_lens_host[0];
-        double best_cost = paired_cost_us(L, N, cand.subs, C, merge_path);
+        double best_cost = paired_cost_us(L, N, cand.subs, C, merge_path, block_size);
         std::vector<int64_t> parts1(1);
         for (int64_t P1 = minP; P1 <= maxP; ++P1) {
           parts1[0] = no_empty_chunks(L, P1, block_size);
           if (parts1[0] != P1 || P1 * row_groups > slots) continue;
           for (int64_t k1 = largest_k(parts1, P1); k1 >= 1; --k1) {
-            const double c1 = paired_cost_us(L, P1, k1, C, merge_path);
-            if (c1 < best_cost - 1e-9 || (c1 < best_cost + 1e-9 && k1 < cand.subs)) {
+            const double c1 = paired_cost_us(L, P1, k1, C, merge_path, block_size);
+            const int64_t pairs1 = P1 * k1, pairs0 = cand.parts[0] * cand.subs;
+            const bool tie = c1 < best_cost + 1e-9 && c1 > best_cost - 1e-9;
+            if (c1 < best_cost - 1e-9 || (tie && (pairs1 > pairs0 || (pairs1 == pairs0 && k1 < cand.subs)))) {
               best_cost = c1;
               cand.parts[0] = P1;
               cand.subs = k1;
@@ -194,7 +199,7 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
     // the time model assumes one wave: a launch whose clusters cannot all be co-resident (the
     // partition floor exceeding the device's clusters of this size) is not a candidate
     if (paired_single && N * cand.subs * row_groups > slots) continue;
-    if (paired_single) cand.cost_us = paired_cost_us(context_lens_host[0], N, cand.subs, C, merge_path);
+    if (paired_single) cand.cost_us = paired_cost_us(context_lens_host[0], N, cand.subs, C, merge_path, block_size);
     cand.active = std::min<int64_t>(N * row_groups * cand.subs, slots) * C;
     if (paired_single) {
       // the modelled fastest; on a tie the smaller cluster (visited first)

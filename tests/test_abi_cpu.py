@@ -85,11 +85,16 @@ def test_plan_long_context_single_request(lib, L, merge_path):
         if L <= 65536:  # too short for that: one cluster of 16 per partition
             assert plan.clusters_per_chunk == 1 and plan.cluster_ctas == 16
     else:
-        # the entries merge makes a spread cost about one tile: spread as soon as it saves more than that
-        if L >= 65536:
-            assert plan.clusters_per_chunk > 1 and busy >= 140
-        if L <= 49152:
-            assert plan.clusters_per_chunk == 1 and plan.cluster_ctas == 16
+        # with the pairs' parts merged as entries a spread costs nothing more: CTA pairs over the whole GPU,
+        # and no plan of up to 8 partitions on the 76 co-resident pairs gives its busiest pair fewer tiles
+        assert plan.cluster_ctas == 2 and plan.clusters_per_chunk > 1 and busy >= 140
+
+        def busiest(P, k):  # 128-token tiles of the busiest pair: a chunk's tiles split evenly over its k pairs
+            longest = max(t1 - t0 for t0, t1 in orc.chunk_bounds(L, P, 32))
+            return -(-(-(-longest // 128)) // k)
+
+        best = min(busiest(P, k) for P in range(2, 9) for k in range(1, 17) if P * k <= 76)
+        assert busiest(plan.num_chunks, plan.clusters_per_chunk) == best
     check_plan_tiles(plan, [L], 32)
     # every CTA pair of every cluster keeps at least one 128-token tile of its partition
     k, C = plan.clusters_per_chunk, plan.cluster_ctas
