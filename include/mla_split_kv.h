@@ -204,16 +204,19 @@ typedef struct {
                                  again). Calls sharing a workspace must not
                                  overlap in time. Unused when k <= 1.           */
   uint64_t workspace_bytes;   /* size of `workspace`                          */
-  int32_t tables_ready;       /* 1: `chunks`, context_lens and block_table are
-                                 complete before the kernel that precedes this
-                                 call in the stream starts (for instance copied
-                                 from the host before the decode step); the
-                                 paired 16-row kernel, a programmatic dependent
-                                 launch, then reads them while that kernel
-                                 finishes instead of after it. Queries and
-                                 caches are always read after it. 0 (default):
-                                 every input is read after the preceding kernel
-                                 has finished. Other values: INVALID_ARG.       */
+  int32_t tables_ready;       /* 1: `chunks`, context_lens and block_table
+                                 (and mla_decode's o_indptr) are complete
+                                 before the kernel that precedes this call in
+                                 the stream starts (for instance copied from
+                                 the host before the decode step); the paired
+                                 16-row kernel and the entries merge kernel,
+                                 programmatic dependent launches, then read
+                                 them while the kernel before them finishes
+                                 instead of after it. Queries are always read
+                                 after it, caches too unless prefix_ready. 0
+                                 (default): every input is read after the
+                                 preceding kernel has finished. Other values:
+                                 INVALID_ARG.                                  */
   int32_t decode_merge;       /* mla_decode only, how the paired 16-row kernel's
                                  parts reach `out`: MLA_DECODE_MERGE_ENTRIES
                                  (0, default) or MLA_DECODE_MERGE_TICKETS (1),

@@ -415,6 +415,7 @@ mla_status_t mla_decode(const void* q_absorbed, const void* q_pe, const void* ck
     mp.rows = rows_total;
     mp.epc = k * (C / 2);
     mp.out_dtype = out_dtype;
+    mp.tables_ready = d->tables_ready;
     if (mla::launch_merge_entries(mp, static_cast<cudaStream_t>(d->stream)) != cudaSuccess) {
       cudaGetLastError();
       return MLA_ERR_CUDA;

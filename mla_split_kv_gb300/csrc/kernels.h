@@ -71,6 +71,7 @@ struct EntryMergeParams {
   void* out;                   // [B, rows, 512] of out_dtype
   float* out_lse;              // [B, rows] or null
   int32_t B, rows, epc, out_dtype;
+  int32_t tables_ready;        // o_indptr complete before the partial kernel started: read before the wait
 };
 cudaError_t launch_merge_entries(const EntryMergeParams& p, cudaStream_t stream);
 

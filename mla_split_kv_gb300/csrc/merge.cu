@@ -128,14 +128,25 @@ constexpr int kEntryRound = kEntryGroups * kEntriesPerLane;
 
 __global__ void __launch_bounds__(kEntryWarps * 32, 4) mla_merge_entries_kernel(const EntryMergeParams p) {
   pdl_launch_dependents();
-  pdl_wait();  // the entries are complete once the partial kernel has
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long gw = static_cast<long long>(blockIdx.x) * kEntryWarps + warp;
-  if (gw >= static_cast<long long>(p.B) * p.rows * 32) return;
+  const bool active = gw < static_cast<long long>(p.B) * p.rows * 32;
   const int cb = static_cast<int>(gw & 31);  // columns [16 cb, 16 cb + 16)
   const long long br = gw >> 5;              // b * rows + row
   const int b = static_cast<int>(br / p.rows), row = static_cast<int>(br % p.rows);
-  const int e0 = p.o_indptr[b] * p.epc, e1 = p.o_indptr[b + 1] * p.epc;
+  // the offsets are an input of the call, not data of the partial kernel: with tables_ready (complete
+  // before that kernel started) they are read before the wait, so the entries' loads follow it at once
+  int e0 = 0, e1 = 0;
+  if (active && p.tables_ready) {
+    e0 = __ldg(p.o_indptr + b) * p.epc;
+    e1 = __ldg(p.o_indptr + b + 1) * p.epc;
+  }
+  pdl_wait();  // the entries are complete once the partial kernel has
+  if (!active) return;
+  if (!p.tables_ready) {
+    e0 = p.o_indptr[b] * p.epc;
+    e1 = p.o_indptr[b + 1] * p.epc;
+  }
   const int g = lane >> 2, q = lane & 3;
   const int col = 16 * cb + 4 * q;
   const long long ostride = static_cast<long long>(p.rows) * kRank;  // one entry's O

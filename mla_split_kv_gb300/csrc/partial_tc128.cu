@@ -413,19 +413,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("" : "+f"(scale_log2), "+l"(tmo));
     // Q^T: this CTA's 256 latent columns (4 chunks, 128-byte swizzle), then its 32 kpe columns
     // (one chunk, 64-byte swizzle); 16 rows, K-major
+    // (every thread's loads are issued before its shared-memory stores: one round trip, not three)
     constexpr int kQPieces = (kHalfCols + kKpeCols) / 8;  // 16-byte pieces per row
-    for (int idx = tid; idx < kNR * kQPieces; idx += kSoftmaxThreads) {
+    constexpr int kQIters = (kNR * kQPieces + kSoftmaxThreads - 1) / kSoftmaxThreads;
+    uint4 qv[kQIters];
+#pragma unroll
+    for (int it = 0; it < kQIters; ++it) {
+      const int idx = tid + it * kSoftmaxThreads;
       const int r = idx / kQPieces, k = (idx % kQPieces) * 8;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (r < w.nrows) {
+      qv[it] = make_uint4(0u, 0u, 0u, 0u);
+      if (idx < kNR * kQPieces && r < w.nrows) {
         const long long row = static_cast<long long>(w.b) * rows_total + w.row0 + r;
-        v = (k < kHalfCols)
-                ? *reinterpret_cast<const uint4*>(p.q_abs + row * kRank + kHalfCols * half + k)
-                : *reinterpret_cast<const uint4*>(p.q_pe + row * kRope + kKpeCols * half + (k - kHalfCols));
+        qv[it] = (k < kHalfCols)
+                     ? __ldcg(reinterpret_cast<const uint4*>(p.q_abs + row * kRank + kHalfCols * half + k))
+                     : __ldcg(reinterpret_cast<const uint4*>(p.q_pe + row * kRope + kKpeCols * half + (k - kHalfCols)));
       }
+    }
+#pragma unroll
+    for (int it = 0; it < kQIters; ++it) {
+      const int idx = tid + it * kSoftmaxThreads;
+      if (idx >= kNR * kQPieces) break;
+      const int r = idx / kQPieces, k = (idx % kQPieces) * 8;
       uint8_t* dst = (k < kHalfCols) ? qs + (k / kBoxCols) * kQChunk + sw128_offset(r, k % kBoxCols)
                                      : qs + kHalfBoxes * kQChunk + sw64_offset(r, k - kHalfCols);
-      *reinterpret_cast<uint4*>(dst) = v;
+      *reinterpret_cast<uint4*>(dst) = qv[it];
     }
     fence_proxy_async_smem();
     named_bar_arrive(2, kSoftmaxThreads + 32);
