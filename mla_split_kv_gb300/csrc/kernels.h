@@ -128,7 +128,7 @@ int tc128_max_active_clusters(int cluster);
 // 64-token-tile tensor-core kernel for groups of 128 rows (q_len * H > 16, the last group
 // padded), fp16 or bf16, each group on a cluster of one CTA pair that split the latent columns.
 bool mh_supports(int total_rows, int cluster);
-cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe, const PartialParams& p,
+cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe_half, const PartialParams& p,
                               int num_chunks, bool bf16, cudaStream_t stream);
 
 // Query rows per CTA for q_len x H rows (SIMT: always 16).

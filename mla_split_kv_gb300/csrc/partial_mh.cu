@@ -15,9 +15,9 @@
 // CTAs of a cluster pair split the latent columns: CTA `half` holds ckv
 // columns [256 half, 256 half + 256) (and the kpe box, of whose 4 16-column
 // K steps it uses 2) and accumulates O for those columns. Each computes S
-// over its columns, stages it (128 x 64 fp32, 32 KB) in its shared memory
-// and sends it into the peer's with one bulk copy completing on the peer's
-// mbarrier (one copy instead of 2048 16-byte remote stores), and adds the
+// over its columns (128 x 64 fp32), sends it from registers into the peer's
+// shared memory with asynchronous 16-byte remote stores completing on the
+// peer's mbarrier (no staging copy in its own shared memory), and adds the
 // peer's part in a fixed order, so both hold the same scores and take the
 // same decisions.
 //
@@ -28,11 +28,13 @@
 // the same shared-memory tile read N-major. With bf16 inputs P is carried as
 // two bf16 terms (hi + lo, two MMAs per step), as in the other kernels.
 //
-// TMEM: O 256 columns, S 2 x 64, P 2 x (32 + 32) = 512. Shared memory: Q (5
-// swizzled [128 x 64] chunks, 80 KB), two 64-token tile slots of 40 KB (the
-// ckv half as one 4D TMA box per page: row groups of four [8 x 64] atoms,
-// group g and block c at 4096 g + 1024 c; the kpe box), this CTA's and the
-// peer's partial S (32 KB each): 226 KB.
+// TMEM: O 256 columns, S 2 x 64, P 2 x (32 + 32) = 512. Shared memory: Q (4
+// swizzled [128 x 64] chunks of this CTA's latent columns and its 32 rope
+// columns with the 64-byte swizzle, 72 KB), three 64-token tile slots of 36 KB
+// (the ckv half as one 4D TMA box per page: row groups of four [8 x 64] atoms,
+// group g and block c at 4096 g + 1024 c; this CTA's 32 kpe columns, 64-byte
+// swizzle), so tiles i+1 and i+2 load while tile i is computed, and the peer's
+// partial S (32 KB): 215 KB.
 //
 // Warp roles (384 threads): warps 0-7 softmax and epilogue (thread = row r =
 // TMEM lane 32 (w % 4) + lane; warps w and w + 4 share the rows and take the
@@ -51,9 +53,12 @@ constexpr int kHalfBoxes = 4;                     // ckv column blocks per CTA: 
 constexpr int kHalfCols = kHalfBoxes * kBoxCols;  // 256
 constexpr int kGroupBytes = 8 * kHalfCols * 2;    // 4 KB: one 8-token group of the four blocks
 constexpr int kCkvBytes = kT * kHalfCols * 2;     // 32 KB
-constexpr int kKpeBytes = kT * 128;               // 8 KB
-constexpr int kTileSlot = kCkvBytes + kKpeBytes;  // 40 KB
+constexpr int kKpeCols = kRope / 2;               // 32 rope columns per CTA
+constexpr int kKpeBytes = kT * kKpeCols * 2;      // 4 KB: [64 tokens x 32 columns], 64-byte swizzle
+constexpr int kTileSlot = kCkvBytes + kKpeBytes;  // 36 KB
+constexpr int kSlots = 3;
 constexpr int kQChunk = kRows * 128;              // 16 KB: [128 rows x 64 columns], swizzled
+constexpr int kQKpe = kRows * kKpeCols * 2;       // 8 KB: [128 rows x 32 rope columns], 64-byte swizzle
 constexpr int kPageWarps = 3;
 constexpr int kSoftmaxWarps = 8;                  // two per TMEM lane quadrant: each takes half of a tile's tokens
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
@@ -62,13 +67,14 @@ constexpr int kThreads = (kSoftmaxWarps + 1 + kPageWarps) * 32;  // 384: three w
 constexpr int kHalfT = kT / 2;                    // tokens of a tile per softmax thread
 constexpr float kRescaleTau = 8.0f;
 
-constexpr uint32_t kOffQ = 0;                             // 80 KB
-constexpr uint32_t kOffTile = 5 * kQChunk;                // 80 KB: 2 tile slots
-constexpr uint32_t kOffX = kOffTile + 2 * kTileSlot;      // 160 KB: the peer's partial S
+constexpr uint32_t kOffQ = 0;                             // 64 KB: latent columns
+constexpr uint32_t kOffQKpe = 4 * kQChunk;                // 8 KB: rope columns
+constexpr uint32_t kOffTile = kOffQKpe + kQKpe;           // 72 KB: 3 tile slots
+constexpr uint32_t kOffX = kOffTile + kSlots * kTileSlot; // 180 KB: the peer's partial S
 constexpr uint32_t kXBytes = kRows * kT * 4;              // [128 rows][64 tokens] fp32: 32 KB
-constexpr uint32_t kOffXS = kOffX + kXBytes;              // 192 KB: this CTA's partial S, sent as one copy
-constexpr uint32_t kOffSmall = kOffXS + kXBytes;          // 224 KB
+constexpr uint32_t kOffSmall = kOffX + kXBytes;           // 212 KB
 constexpr uint32_t kSmem = kOffSmall + 2048 + 1024;       // + alignment slack
+static_assert(kTileSlot % 1024 == 0 && kOffTile % 1024 == 0, "swizzle atoms stay aligned");
 static_assert(kSmem <= 232448, "shared memory per CTA");
 
 constexpr uint32_t kTmemO = 0;      // O [128 x 256] fp32
@@ -77,7 +83,7 @@ constexpr uint32_t kTmemP = 384;    // P [128 x 64] 16-bit, hi and lo (32 column
 constexpr uint32_t kTmemCols = 512;
 
 struct Small {
-  uint64_t full[2], empty[2], sfull[2], sfree[2], ppfull[2], pvdone[2], xfull, xempty, drain;
+  uint64_t full[kSlots], empty[kSlots], sfull[2], sfree[2], ppfull[2], pvdone[2], xfull, xempty, drain;
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t peer_abort;        // set by the peer CTA (remote store) when it gave up
@@ -102,14 +108,13 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { retur
 
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    mla_partial_mh_kernel(const __grid_constant__ CUtensorMap tm_pages, const __grid_constant__ CUtensorMap tm_kpe,
+    mla_partial_mh_kernel(const __grid_constant__ CUtensorMap tm_pages, const __grid_constant__ CUtensorMap tm_kpe_half,
                           const PartialParams p) {
   extern __shared__ uint8_t smem_raw[];
   pdl_launch_dependents();  // the merge of these partials may be scheduled now; it waits for this grid
   uint8_t* smem = align1024(smem_raw);
   uint8_t* qs = smem + kOffQ;
   float* xs = reinterpret_cast<float*>(smem + kOffX);
-  float* xsend = reinterpret_cast<float*>(smem + kOffXS);
   Small* sm = reinterpret_cast<Small*>(smem + kOffSmall);
   volatile int32_t* abort_flag = &sm->abort_flag;
 
@@ -119,9 +124,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rows_total = p.q_len * p.H;
 
   if (tid == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&sm->full[s], kPageWarps);  // one expect_tx arrival per producer warp
+      mbar_init(&sm->empty[s], 1);
+    }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&sm->full[t], kPageWarps);  // one expect_tx arrival per producer warp
-      mbar_init(&sm->empty[t], 1);
       mbar_init(&sm->sfull[t], 1);
       mbar_init(&sm->sfree[t], kSoftmaxWarps);
       mbar_init(&sm->ppfull[t], kSoftmaxWarps);
@@ -174,11 +181,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int issued = -1;
     for (int i = 0; i < ntiles; ++i) {
-      const int t = i & 1;
-      if (i >= 2) {  // PV(i-2) released the slot
+      const int s = i % kSlots;
+      if (i >= kSlots) {  // PV(i-3) released the slot
         int ok = 1;
         if (lane == 0) {
-          ok = mbar_wait(&sm->empty[t], ((i >> 1) - 1) & 1, tmo) && !*abort_flag;
+          ok = mbar_wait(&sm->empty[s], ((i / kSlots) - 1) & 1, tmo) && !*abort_flag;
           if (!ok) *abort_flag = 1;
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -189,8 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int pids[2];
 #pragma unroll
       for (int m = 0; m < 2; ++m) pids[m] = (m < mine) ? page_of(pg0 + k0 + m * kPageWarps) : -1;
-      uint8_t* slot = smem + kOffTile + t * kTileSlot;
-      if (lane == 0) mbar_arrive_expect_tx(&sm->full[t], static_cast<uint32_t>(mine * p.bs * (kHalfCols * 2 + 128)));
+      uint8_t* slot = smem + kOffTile + s * kTileSlot;
+      if (lane == 0)
+        mbar_arrive_expect_tx(&sm->full[s], static_cast<uint32_t>(mine * p.bs * (kHalfCols + kKpeCols) * 2));
       __syncwarp();
       // lane m issues this warp's page m (TMA issue from several lanes overlaps)
 #pragma unroll
@@ -198,14 +206,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == m && m < mine) {
           const int j = k0 + m * kPageWarps;
           tma_load_4d(slot + j * p.bs * (kHalfCols * 2), &tm_pages, 0, 0, kHalfBoxes * half, pids[m] * (p.bs / 8),
-                      &sm->full[t], pol);
-          tma_load_2d(slot + kCkvBytes + j * p.bs * 128, &tm_kpe, 0, pids[m] * p.bs, &sm->full[t], pol);
+                      &sm->full[s], pol);
+          tma_load_2d(slot + kCkvBytes + j * p.bs * (kKpeCols * 2), &tm_kpe_half, kKpeCols * half, pids[m] * p.bs,
+                      &sm->full[s], pol);
         }
       }
       issued = i;
-      if (i + 2 < ntiles) {  // the same page of tile i+2 into L2: ckv by the even CTA, kpe by the odd one
+      if (i + kSlots < ntiles) {  // the same page of tile i+3 into L2: ckv by the even CTA, kpe by the odd one
         int qg0, qn;
-        tile_pages(i + 2, &qg0, &qn);
+        tile_pages(i + kSlots, &qg0, &qn);
         for (int j = k0; j < qn; j += kPageWarps) {
           const int qpid = page_of(qg0 + j);
           if (lane == 0 && qpid >= 0) {
@@ -218,10 +227,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    // after an abort, let this warp's loads still in flight (the last two tiles it issued) land before
+    // after an abort, let this warp's loads still in flight (the last three tiles it issued) land before
     // shared memory is released
     if (lane == 0 && *abort_flag)
-      for (int t = max(0, issued - 1); t <= issued; ++t) mbar_wait(&sm->full[t & 1], (t >> 1) & 1, kDrainTimeoutNs);
+      for (int t = max(0, issued - (kSlots - 1)); t <= issued; ++t)
+        mbar_wait(&sm->full[t % kSlots], (t / kSlots) & 1, kDrainTimeoutNs);
     cluster_wait_acquire();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
@@ -231,21 +241,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tile_base = smem_u32(smem + kOffTile);
     uint64_t tmo = p.timeout_ns;
     asm volatile("" : "+l"(tmo));
-    auto wait_lane0 = [&](uint64_t* bar, uint32_t parity) -> bool {
-      int ok = 1;
-      if (lane == 0) {
-        ok = mbar_wait(bar, parity, tmo) && !*abort_flag;
-        if (!ok) *abort_flag = 1;
-      }
-      return __shfl_sync(0xffffffffu, ok, 0) != 0;
-    };
-    auto score = [&](int i) -> bool {
+    // score product of tile i (slot i % 3) into S buffer i & 1: this CTA's 4 latent column blocks, then
+    // its 32 rope columns (two K steps of the 64-byte-swizzled box)
+    auto score = [&](int i) {
       const int t = i & 1;
-      if (i >= 2 && !wait_lane0(&sm->sfree[t], ((i >> 1) - 1) & 1)) return false;
-      if (!wait_lane0(&sm->full[t], (i >> 1) & 1)) return false;
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t slot = tile_base + t * kTileSlot;
+        const uint32_t slot = tile_base + (i % kSlots) * kTileSlot;
         const uint32_t d = tmem + kTmemS + t * kT;
 #pragma unroll
         for (int c = 0; c < kHalfBoxes; ++c) {
@@ -255,17 +257,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 4; ++kk)
             umma_f16_ss(d, desc_add(qd, kk * 32), desc_add(kd, kk * 32), idesc_s, (c == 0 && kk == 0) ? 0u : 1u);
         }
-        const uint64_t qd = smem_desc_sw128(q_base + kHalfBoxes * kQChunk, 16, 1024);
-        const uint64_t kd = smem_desc_sw128(slot + kCkvBytes, 16, 1024);
+        const uint64_t qd = smem_desc_sw64(q_base + kOffQKpe, 512);
+        const uint64_t kd = smem_desc_sw64(slot + kCkvBytes, 512);
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const uint32_t ks = 2 * half + kk;  // 16-column step of the kpe box
-          umma_f16_ss(d, desc_add(qd, ks * 32), desc_add(kd, ks * 32), idesc_s, 1u);
-        }
+        for (int kk = 0; kk < 2; ++kk) umma_f16_ss(d, desc_add(qd, kk * 32), desc_add(kd, kk * 32), idesc_s, 1u);
         umma_commit(&sm->sfull[t]);
       }
       __syncwarp();
-      return true;
     };
     // rows [nvalid, nend) of the ckv part of a slot: zeroed so the V operand stays finite
     auto zero_rows = [&](uint8_t* ckv, int nvalid, int nend) {
@@ -275,19 +273,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             make_uint4(0u, 0u, 0u, 0u);
       }
     };
-    auto pv = [&](int i) -> bool {
-      const int t = i & 1;
+    auto pv = [&](int i) {
+      const int t = i & 1, s = i % kSlots;
       const int nvalid = min(kT, w.sub1 - (w.sub0 + i * kT));
-      if (!wait_lane0(&sm->ppfull[t], (i >> 1) & 1)) return false;
       const int ksteps = (nvalid + 15) >> 4;
       if (nvalid < (ksteps << 4)) {
-        zero_rows(smem + kOffTile + t * kTileSlot, nvalid, ksteps << 4);
+        zero_rows(smem + kOffTile + s * kTileSlot, nvalid, ksteps << 4);
         fence_proxy_async_smem();
         __syncwarp();
       }
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t slot = tile_base + t * kTileSlot;
+        const uint32_t slot = tile_base + s * kTileSlot;
         const uint32_t pa = tmem + kTmemP + t * 64;
         for (int ks = 0; ks < ksteps; ++ks) {
           const uint64_t vd = smem_desc_sw128(slot + ks * 2 * kGroupBytes, 1024, kGroupBytes);
@@ -297,18 +294,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_f16_ts(tmem + kTmemO, pk, vd, idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
           if (BF16) umma_f16_ts(tmem + kTmemO, pk + 16, vd, idesc_o, 1u);
         }
-        umma_commit(&sm->empty[t]);
+        umma_commit(&sm->empty[s]);
         umma_commit(&sm->pvdone[t]);
       }
       __syncwarp();
-      return true;
     };
     named_bar_sync(2, kSoftmaxThreads + 32);  // Q staged by the softmax warps
-    bool alive = true;
-    for (int i0 = 0; i0 < ntiles && alive; i0 += 2) {
-      const int i1 = min(i0 + 2, ntiles);
-      for (int i = i0; i < i1 && alive; ++i) alive = score(i);
-      for (int i = i0; i < i1 && alive; ++i) alive = pv(i);
+    // Issue as the inputs get ready, each product in tile order: PV(np) once its probabilities are in
+    // TMEM (first: it releases a slot for the next load), else S(ns) once tile ns has landed and its S
+    // buffer is free. Nothing ready for longer than the wait limit (or an abort elsewhere) ends it.
+    int ns = 0, np = 0;
+    bool idle = false;
+    uint64_t idle_t0 = 0;
+    while (np < ntiles) {
+      int act = 0;
+      if (lane == 0) {
+        if (np < ns && mbar_test(&sm->ppfull[np & 1], (np >> 1) & 1)) {
+          act = 2;
+        } else if (ns < ntiles && (ns < 2 || mbar_test(&sm->sfree[ns & 1], ((ns >> 1) - 1) & 1)) &&
+                   mbar_test(&sm->full[ns % kSlots], (ns / kSlots) & 1)) {
+          act = 1;
+        } else if (*abort_flag) {
+          act = -1;
+        } else {
+          const uint64_t now = globaltimer_ns();
+          if (!idle) {
+            idle = true;
+            idle_t0 = now;
+          } else if (now - idle_t0 > tmo) {
+            act = -1;
+            *abort_flag = 1;
+            flag_error(MLA_DEVERR_TIMEOUT);
+          }
+        }
+        if (act > 0) idle = false;
+      }
+      act = __shfl_sync(0xffffffffu, act, 0);
+      if (act == 2) {
+        pv(np);
+        ++np;
+      } else if (act == 1) {
+        score(ns);
+        ++ns;
+      } else if (act < 0) {
+        break;
+      }
     }
     if (lane == 0) {  // every MMA issued so far has completed before TMEM is read or freed
       umma_commit(&sm->drain);
@@ -318,15 +348,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_wait_acquire();
   } else {
     // ------------------------------------------------------------------ softmax (warps 0-3): thread = row
-    // Q: this CTA's 256 latent columns, then the 64 kpe columns; 128 rows, K-major, 5 swizzled chunks
-    // (all the 16-byte copies in flight at once; rows past the request's zero-filled)
-    for (int idx = tid; idx < kRows * 40; idx += kSoftmaxThreads) {
-      const int r = idx / 40, k = (idx % 40) * 8;
+    // Q: this CTA's 256 latent columns (4 chunks, 128-byte swizzle), then its 32 rope columns (64-byte
+    // swizzle); 128 rows, K-major (all the 16-byte copies in flight at once; rows past the request's
+    // zero-filled)
+    constexpr int kQPieces = (kHalfCols + kKpeCols) / 8;  // 16-byte pieces per row
+    for (int idx = tid; idx < kRows * kQPieces; idx += kSoftmaxThreads) {
+      const int r = idx / kQPieces, k = (idx % kQPieces) * 8;
       const bool in = r < w.nrows;
       const long long row = static_cast<long long>(w.b) * rows_total + w.row0 + (in ? r : 0);
       const uint16_t* src = (k < kHalfCols) ? p.q_abs + row * kRank + kHalfCols * half + k
-                                            : p.q_pe + row * kRope + (k - kHalfCols);
-      cp_async16(qs + (k / kBoxCols) * kQChunk + sw128_offset(r, k % kBoxCols), src, in ? 16u : 0u);
+                                            : p.q_pe + row * kRope + kKpeCols * half + (k - kHalfCols);
+      uint8_t* dst = (k < kHalfCols) ? qs + (k / kBoxCols) * kQChunk + sw128_offset(r, k % kBoxCols)
+                                     : qs + kOffQKpe + sw64_offset(r, k - kHalfCols);
+      cp_async16(dst, src, in ? 16u : 0u);
     }
     cp_async_wait_all();
     fence_proxy_async_smem();
@@ -348,9 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t peer_xfull = dsmem_addr(&sm->xfull, peer);
     const uint32_t peer_xempty = dsmem_addr(&sm->xempty, peer);
     const float4* xrow = reinterpret_cast<const float4*>(xs + r * kT);
-    float4* srow = reinterpret_cast<float4*>(xsend + r * kT);
+    const uint32_t peer_xrow = peer_x + static_cast<uint32_t>(r * kT * 4);
     float m_r = -INFINITY, l_r = 0.f;
-    const float4* srow_c = srow;
+    float own[kHalfT];  // this CTA's partial scores of the current tile, kept for B
     // C(j): probabilities of tile j (its scaled scores wait in its P buffer) -> the same buffer (hi, and lo
     // for bf16), 32 tokens at a time; then PV(j) may run
     auto probabilities = [&](int j) {
@@ -389,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&sm->ppfull[j & 1]);
     };
     // Software pipeline over tiles: iteration i sends tile i's partial scores (A), computes the
-    // probabilities of tile i-1 while that copy is in flight (C), then finishes tile i's scores (B).
+    // probabilities of tile i-1 while those stores are in flight (C), then finishes tile i's scores (B).
     // Between B(i) and C(i) the scaled scores of tile i wait in tile i's P buffer in tensor memory
     // (64 fp32 columns), which C(i) then overwrites with the packed probabilities.
     for (int i = 0; i <= ntiles; ++i) {
@@ -407,35 +441,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           c_done = true;
         }
       }
-      // ---- A(i): this CTA's partial S of tile i -> send buffer -> one copy into the peer
+      // ---- A(i): this CTA's partial S of tile i -> the peer's shared memory (16-byte asynchronous
+      // remote stores from registers, completing on the peer's xfull)
       if (cur) {
         if (lane == 0) ok = mbar_wait(&sm->sfull[buf], (i >> 1) & 1, tmo);
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        float x[kHalfT];
         if (ok) {
           tc_fence_after();
-          tmem_ld16(tmem + lane_base + kTmemS + buf * kT + 32 * hf, x);
-          tmem_ld16(tmem + lane_base + kTmemS + buf * kT + 32 * hf + 16, x + 16);
+          tmem_ld16(tmem + lane_base + kTmemS + buf * kT + 32 * hf, own);
+          tmem_ld16(tmem + lane_base + kTmemS + buf * kT + 32 * hf + 16, own + 16);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm->sfree[buf]);
-          // the peer has read tile i-1's scores (so the copy out of the send buffer is finished too)
+          // the peer has read tile i-1's scores out of its buffer
           if (i >= 1) ok = mbar_wait_cluster(&sm->xempty, (i - 1) & 1, tmo);
         }
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
 #pragma unroll
           for (int c = 0; c < kHalfT / 4; ++c)
-            srow[(8 * hf + c) ^ xsw] = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
-          fence_proxy_async_smem();
+            dsmem_st_async_f32x4(peer_xrow + (((8 * hf + c) ^ xsw) << 4),
+                                 make_float4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]), peer_xfull);
         }
       }
       if (named_bar_sync_or(1, kSoftmaxThreads, !ok || *abort_flag != 0)) {
         *abort_flag = 1;
         break;
       }
-      if (cur && tid == 0) dsmem_bulk_copy(peer_x, xsend, kXBytes, peer_xfull);
       // ---- C(i-1), when tile i's scores are not ready yet (so it cannot wait on them)
       if (!c_done) {
         probabilities(i - 1);
@@ -451,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
 #pragma unroll
         for (int c = 0; c < kHalfT / 4; ++c) {
-          const float4 o = srow_c[(8 * hf + c) ^ xsw];
+          const float4 o = make_float4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]);
           const float4 y = xrow[(8 * hf + c) ^ xsw];
           // rank-0 part + rank-1 part, the same sum in both CTAs
           x[4 * c] = half ? (y.x + o.x) : (o.x + y.x);
@@ -558,9 +591,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // a CTA that gave up tells its peer before the last cluster barrier: the bulk copies of partial
-  // scores that either CTA issued may then still be in flight (reading the sender's shared memory,
-  // writing the receiver's), so after an abort on either side both stay until they have landed
+  // a CTA that gave up tells its peer before the last cluster barrier: the remote stores of partial
+  // scores that either CTA issued may then still be in flight (writing the receiver's shared memory),
+  // so after an abort on either side both stay until they have landed
   if (tid == 0 && *abort_flag) dsmem_st_u32(dsmem_addr(&sm->peer_abort, peer), 1u);
   cluster_sync();  // the peer is done with this CTA's shared memory
   if (*abort_flag || *reinterpret_cast<volatile int32_t*>(&sm->peer_abort)) settle_in_flight(20000ull);
@@ -586,7 +619,7 @@ cudaError_t prepare_mh() {
 // padded (its rows past the end have zero queries and are not written back).
 bool mh_supports(int total_rows, int cluster) { return total_rows > 16 && cluster == 2; }
 
-cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe, const PartialParams& p,
+cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe_half, const PartialParams& p,
                               int num_chunks, bool bf16, cudaStream_t stream) {
   cudaError_t e = bf16 ? prepare_mh<true>() : prepare_mh<false>();
   if (e != cudaSuccess) return e;
@@ -604,8 +637,8 @@ cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return bf16 ? cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<true>, tm_pages, tm_kpe, p)
-              : cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<false>, tm_pages, tm_kpe, p);
+  return bf16 ? cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<true>, tm_pages, tm_kpe_half, p)
+              : cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<false>, tm_pages, tm_kpe_half, p);
 }
 
 cudaError_t mh_read_clear_error(uint32_t* out) {
