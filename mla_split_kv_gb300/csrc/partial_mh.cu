@@ -465,10 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  make_float4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]), peer_xfull);
         }
       }
-      if (named_bar_sync_or(1, kSoftmaxThreads, !ok || *abort_flag != 0)) {
-        *abort_flag = 1;
-        break;
-      }
+      // (no barrier here: each warp goes on to C(i-1) as soon as its own stores are issued; a failure
+      // in A ends the loop at B's barrier, in every warp)
+      const bool a_ok = ok != 0;
       // ---- C(i-1), when tile i's scores are not ready yet (so it cannot wait on them)
       if (!c_done) {
         probabilities(i - 1);
@@ -477,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!cur) break;
       // ---- B(i): add the peer's part, scale and mask, lazy rescale, scores -> tile i's P buffer
       const int tok0 = w.sub0 + i * kT;
-      ok = mbar_wait_cluster(&sm->xfull, i & 1, tmo);
+      ok = a_ok ? mbar_wait_cluster(&sm->xfull, i & 1, tmo) : 0;
       ok = __all_sync(0xffffffffu, ok);
       float x[kHalfT];
       float mx = -INFINITY;
