@@ -61,6 +61,8 @@ def parse():
                     help="profiling case: only --launches plain layer calls at this context (of the sweep), then exit")
     ap.add_argument("--profile-many-heads", action="store_true",
                     help="profiling case: only --launches plain layer calls of the many-head workload, then exit")
+    ap.add_argument("--profile-verify", type=int, default=0,
+                    help="profiling case: only --launches plain verify-window calls of this q_len, then exit")
     ap.add_argument("--launches", type=int, default=5)
     ap.add_argument("--profile-split", default="",
                     help="profiling case: 'P,C' = a uniform split into P partitions on clusters of C CTAs instead of "
@@ -198,31 +200,41 @@ def window_work(seg):
     return flops, tokens * LATENT_BYTES_PER_TOKEN + pages * 4 + B * q * Hh * (576 * 2 + 512 * 2)
 
 
-def time_verify_windows(nb, rt, torch, stream, peaks, reps=5):
+def verify_window_call(nb, rt, torch, stream, full, dc_base, q):
+    """One verify-window layer call of q_len q over the segmented prefix: one partial launch per segment and
+    one merge. Returns (call, the window's view of the case, the number of partial launches)."""
     from mla_split_kv_gb300 import inputs as gen
 
     dev = nb.mla_device_query()
+    seg = gen.window_view(full, q)
+    sp = rt.plan_segments(seg, dev, max_partitions=64)  # as the many-head timing: enough pairs to fill the GPU
+    part, lse = rt.alloc_partials(sp.num_slots, q, H)
+    out = torch.empty((VW_B, q, H, 512), dtype=torch.float16, device="cuda")
+    launches = []
+    for s, table, plan in zip(seg.segments, sp.chunk_tables, sp.plans):
+        dc = rt.upload(s, ckv=dc_base.ckv, kpe=dc_base.kpe)
+        ws = rt.alloc_workspace(plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, q, H)
+        desc = rt.make_desc(dc, table, nb.MLA_KERNEL_TC, plan.cluster_ctas, stream, plan.clusters_per_chunk, ws,
+                            tables_ready=True)
+        launches.append((dc, desc))
+
+    def call():
+        for dc, desc in launches:
+            rt.decode_partial(dc, part, lse, desc=desc)
+        rt.merge_states(part, lse, sp.o_indptr, VW_B, q, H, "f16", out=out, stream=stream)
+
+    call.plans = sp.plans
+    return call, seg, len(launches)
+
+
+def time_verify_windows(nb, rt, torch, stream, peaks, reps=5):
+    from mla_split_kv_gb300 import inputs as gen
+
     full = gen.make_segmented_case(VW_SEED, B=VW_B, q_len=max(VW_QLENS), num_heads=H, block_size=BS)
     dc_base = rt.upload(full.base)  # the cache pool, shared by every window length
     rows = []
     for q in VW_QLENS:
-        seg = gen.window_view(full, q)
-        sp = rt.plan_segments(seg, dev, max_partitions=64)  # as the many-head timing: enough pairs to fill the GPU
-        part, lse = rt.alloc_partials(sp.num_slots, q, H)
-        out = torch.empty((VW_B, q, H, 512), dtype=torch.float16, device="cuda")
-        launches = []
-        for s, table, plan in zip(seg.segments, sp.chunk_tables, sp.plans):
-            dc = rt.upload(s, ckv=dc_base.ckv, kpe=dc_base.kpe)
-            ws = rt.alloc_workspace(plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, q, H)
-            desc = rt.make_desc(dc, table, nb.MLA_KERNEL_TC, plan.cluster_ctas, stream, plan.clusters_per_chunk, ws,
-                                tables_ready=True)
-            launches.append((dc, desc))
-
-        def call():
-            for dc, desc in launches:
-                rt.decode_partial(dc, part, lse, desc=desc)
-            rt.merge_states(part, lse, sp.o_indptr, VW_B, q, H, "f16", out=out, stream=stream)
-
+        call, seg, nlaunch = verify_window_call(nb, rt, torch, stream, full, dc_base, q)
         with torch.cuda.stream(stream):
             for _ in range(3):
                 call()
@@ -248,8 +260,8 @@ def time_verify_windows(nb, rt, torch, stream, peaks, reps=5):
                      "bound": "tensor" if flops / nbytes > peaks["tensor_tflops"] * 1e3 / peaks["hbm_gbs"] else "hbm",
                      "frac_tensor": round(frac_t, 4), "frac_hbm": round(frac_h, 4),
                      "flop_per_byte": round(flops / nbytes, 1),
-                     "partitions_per_segment": [p.num_chunks for p in sp.plans],
-                     "launches": len(launches) + 1})
+                     "partitions_per_segment": [p.num_chunks for p in call.plans],
+                     "launches": nlaunch + 1})
     return {"workload": VERIFY, "per_q_len": rows,
             "peaks": {"tensor_tflops": peaks["tensor_tflops"], "hbm_gbs": peaks["hbm_gbs"],
                       "source": peaks["source"]},
@@ -558,6 +570,36 @@ def run_profile_case(args):
     print(json.dumps({"profile_ctx": L, "launches": args.launches, "partitions": plan.num_chunks,
                       "cluster": plan.cluster_ctas, "clusters_per_partition": k,
                       "kernel": partial_kernel_name(args.kernel, [plan]),
+                      "device_status": st, "device_error": code}))
+    if st != nb.MLA_OK:
+        raise SystemExit(1)
+
+
+def run_profile_verify(args):
+    """A few plain verify-window calls of q_len args.profile_verify: the workload of the ncu capture of the
+    window kernels' DRAM traffic in profiles/."""
+    import torch
+
+    from mla_split_kv_gb300 import binding as nb
+    from mla_split_kv_gb300 import build as nbuild
+    from mla_split_kv_gb300 import inputs as gen
+    from mla_split_kv_gb300 import runtime as rt
+
+    nbuild.build()
+    nb.load()
+    q = args.profile_verify
+    full = gen.make_segmented_case(VW_SEED, B=VW_B, q_len=max(VW_QLENS), num_heads=H, block_size=BS)
+    dc_base = rt.upload(full.base)
+    stream = torch.cuda.current_stream()
+    call, seg, nlaunch = verify_window_call(nb, rt, torch, stream, full, dc_base, q)
+    for _ in range(args.launches):
+        call()
+    torch.cuda.synchronize()
+    st, code = nb.mla_check_device_errors(None)
+    flops, nbytes = window_work(seg)
+    print(json.dumps({"profile": VERIFY, "q_len": q, "calls": args.launches, "partial_launches_per_call": nlaunch,
+                      "algorithmic_bytes_per_call": nbytes, "algorithmic_flops_per_call": flops,
+                      "partitions_per_segment": [p.num_chunks for p in call.plans],
                       "device_status": st, "device_error": code}))
     if st != nb.MLA_OK:
         raise SystemExit(1)
@@ -1018,6 +1060,9 @@ def main():
         return
     if args.profile_many_heads:
         run_profile_many_heads(args)
+        return
+    if args.profile_verify:
+        run_profile_verify(args)
         return
     if "WORLD_SIZE" not in os.environ and args.gpus > 1:
         # no launcher around this process: start one rank per GPU (this file again, same arguments)
