@@ -188,6 +188,9 @@ __device__ __forceinline__ void cluster_arrive_release() {
   asm volatile("barrier.cluster.arrive.release;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait_acquire() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+// Arrival with no memory ordering: for a barrier that only has to keep a CTA until its peers have
+// reached a point (their shared-memory traffic to it already observed complete on mbarriers).
+__device__ __forceinline__ void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory"); }
 // Address of the same shared variable in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
   uint32_t out;
