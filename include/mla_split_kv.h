@@ -120,7 +120,8 @@ typedef struct {
                                MLA_MERGE_ENTRIES (0, default: mla_decode on
                                the paired kernel) or MLA_MERGE_PARTIALS
                                (mla_decode_partial + mla_merge_states, or
-                               mla_decode's single launch). Other values:
+                               mla_decode's MLA_DECODE_MERGE_TICKETS way).
+                               Other values:
                                INVALID_ARG.                                     */
   /* outputs */
   int32_t num_chunks;       /* N = sum_b P_b                                   */

@@ -92,7 +92,8 @@ def alloc_workspace(num_chunks: int, subs: int, cluster: int, q_len: int, H: int
 
 def alloc_decode_workspace(B: int, num_chunks: int, subs: int, cluster: int, q_len: int, H: int,
                            device="cuda") -> torch.Tensor:
-    """Zeroed workspace of a single-launch mla_decode (request tickets, LSE copies, the spread workspace)."""
+    """Zeroed workspace of mla_decode on the paired kernel (request tickets and LSE copies of its single-launch
+    way, then the chunk tickets and the pair entries)."""
     n = nb.mla_decode_workspace_bytes(B, num_chunks, subs, cluster, q_len, H)
     return torch.zeros(n, dtype=torch.uint8, device=device)
 

@@ -1,12 +1,13 @@
-"""Single-launch decode (mla_decode with single_launch) against the two-launch path and the oracle.
+"""mla_decode's ways on the paired 16-row kernel against the two ABI calls and the oracle.
 
-mla_decode is mla_decode_partial followed by mla_merge_states; with
-single_launch on the paired 16-row fp16 kernel the merge runs inside the
-partial kernel (one launch). The fused merge uses the merge kernel's
-arithmetic in its order, so the chunk partials, the LSE and the merged output
-must be the same bits as the two launches give, and the merged output must
-match the f64 oracle within the stated tolerance (max-abs 2e-3, rel-L2 1e-3 on
-fp32 results).
+The default: every CTA pair writes its unnormalized part and the entries merge
+kernel combines them; against the f64 oracle within the stated tolerance
+(max-abs 2e-3, rel-L2 1e-3 on fp32 results), the same bits on a repeat, and
+with prefix_ready the same bits as without it. The single launch
+(decode_merge = MLA_DECODE_MERGE_TICKETS): the merge runs inside the partial
+kernel with the merge kernel's arithmetic in its order, so the chunk partials,
+the LSE and the merged output must be the same bits as mla_decode_partial +
+mla_merge_states give.
 """
 import dataclasses
 
