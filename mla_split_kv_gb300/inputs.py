@@ -10,6 +10,9 @@ Conventions (shared by every consumer):
 * 16-bit tensors are stored as ``numpy.uint16`` bit patterns together with a
   dtype tag ``"f16"`` (IEEE binary16) or ``"bf16"`` (bfloat16). f64 draws are
   rounded once, to nearest-even, into the tagged type.
+* dtype ``"e4m3"``: the caches are ``numpy.uint8`` 8-bit E4M3 patterns drawn
+  directly as bits (random sign, exponent field, mantissa; no NaN pattern),
+  read with a power-of-two ``cache_scale``; the queries are fp16.
 * ``ckv``  : ``[num_blocks, block_size, 512]`` -- compressed latent, one row per
   cached token (the key *and* the value of absorbed attention).
 * ``kpe``  : ``[num_blocks, block_size, 64]`` -- rotary key part.
@@ -70,6 +73,7 @@ class DecodeCase:
     kpe: np.ndarray  # uint16 [num_blocks, bs, 64]
     block_table: np.ndarray  # int32 [B, max_blocks]
     context_lens: np.ndarray  # int32 [B]
+    cache_scale: float = 1.0  # e4m3 caches: the value of pattern x is e4m3(x) * cache_scale
 
     @property
     def num_requests(self) -> int:
@@ -85,15 +89,29 @@ class DecodeCase:
 
     def latent_bytes(self) -> int:
         """Bytes of ckv+kpe a single pass over every request's context touches."""
-        return int(self.context_lens.astype(np.int64).sum()) * (KV_LORA_RANK + ROPE_DIM) * 2
+        per = 1 if self.dtype == "e4m3" else 2
+        return int(self.context_lens.astype(np.int64).sum()) * (KV_LORA_RANK + ROPE_DIM) * per
 
 
 def pages_for(n_tokens: int, block_size: int) -> int:
     return (int(n_tokens) + block_size - 1) // block_size
 
 
+def e4m3_bits(rng: np.random.Generator, shape) -> np.ndarray:
+    """Random 8-bit E4M3 patterns: random sign and mantissa, exponent field 4..9 (values 0.125 to 7.5 in
+    magnitude) for 15 of 16 entries, and field 0 (zero and subnormals) for the rest; never the NaN pattern."""
+    sign = rng.integers(0, 2, size=shape, dtype=np.uint8) << 7
+    exp = rng.integers(4, 10, size=shape, dtype=np.uint8)
+    exp = np.where(rng.integers(0, 16, size=shape) == 0, 0, exp).astype(np.uint8)
+    mant = rng.integers(0, 8, size=shape, dtype=np.uint8)
+    return (sign | (exp << 3) | mant).astype(np.uint8)
+
+
 def _latent_pool(rng: np.random.Generator, num_blocks: int, block_size: int,
                  dtype: str, std: float):
+    if dtype == "e4m3":
+        return (e4m3_bits(rng, (num_blocks, block_size, KV_LORA_RANK)),
+                e4m3_bits(rng, (num_blocks, block_size, ROPE_DIM)))
     ckv = to_bits(rng.standard_normal((num_blocks, block_size, KV_LORA_RANK)) * std, dtype)
     kpe = to_bits(rng.standard_normal((num_blocks, block_size, ROPE_DIM)) * std, dtype)
     return ckv, kpe
@@ -117,7 +135,7 @@ def make_decode_case(seed: int, context_lens: Sequence[int], num_heads: int = 16
                      q_len: int = 1, block_size: int = 32, dtype: str = "f16",
                      scale: Optional[float] = None, latent_std: float = 1.0,
                      pool_blocks: Optional[int] = None, causal: bool = False,
-                     shuffle: bool = True) -> DecodeCase:
+                     shuffle: bool = True, cache_scale: float = 0.25) -> DecodeCase:
     """A batch whose requests own disjoint pages of one shared, shuffled pool.
 
     The pool holds ``pool_blocks`` pages (default: twice the pages needed, so
@@ -136,13 +154,14 @@ def make_decode_case(seed: int, context_lens: Sequence[int], num_heads: int = 16
     for n in need:
         pages.append(perm[off: off + n].tolist())
         off += n
-    q_abs, q_pe = _queries(rng, len(lens), q_len, num_heads, dtype)
+    q_abs, q_pe = _queries(rng, len(lens), q_len, num_heads, "f16" if dtype == "e4m3" else dtype)
     ckv, kpe = _latent_pool(rng, nb, block_size, dtype, latent_std)
     return DecodeCase(dtype=dtype, num_heads=num_heads, q_len=q_len, block_size=block_size,
                       scale=scale if scale is not None else 1.0 / math.sqrt(192.0),
                       causal=causal, q_abs=q_abs, q_pe=q_pe, ckv=ckv, kpe=kpe,
                       block_table=_tables_from_pages(pages),
-                      context_lens=np.asarray(lens, dtype=np.int32))
+                      context_lens=np.asarray(lens, dtype=np.int32),
+                      cache_scale=cache_scale if dtype == "e4m3" else 1.0)
 
 
 @dataclasses.dataclass

@@ -60,6 +60,39 @@ def decode16(bits: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(dtype)
 
 
+def decode_e4m3(bits: np.ndarray) -> np.ndarray:
+    """Exact f64 value of 8-bit E4M3 floating-point patterns (uint8).
+
+    The pages leave caches other than 16-bit out ("Paged-backed and non-FP16
+    latent caches, both declined", mlxcel PR #995, *Left out*); the format is
+    taken as the OCP 8-bit E4M3 one: sign bit, 4 exponent bits with bias 7, 3
+    mantissa bits; exponent field 0 is subnormal (mantissa x 2^-9); the one
+    pattern S.1111.111 is NaN; there are no infinities (largest finite 448).
+    """
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    normal = (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0)
+    sub = m * 2.0 ** -9
+    val = sign * np.where(e == 0, sub, normal)
+    return np.where((e == 15) & ((b & 0x7) == 7), np.nan, val)
+
+
+def decode_cache(bits: np.ndarray, case) -> np.ndarray:
+    """Exact f64 value of cache entries: 16-bit patterns, or E4M3 patterns times the case's cache scale
+    (a scalar folded into the dequantized value, as mlxcel PR #995, *What changed*, folds a global scale:
+    ``(x @ W^T) * s == x @ (W * s)^T``)."""
+    if case.dtype == "e4m3":
+        return decode_e4m3(bits) * float(case.cache_scale)
+    return decode16(bits, case.dtype)
+
+
+def query_dtype(case) -> str:
+    """The queries' 16-bit type: the case's dtype, fp16 beside an E4M3 cache."""
+    return "f16" if case.dtype == "e4m3" else case.dtype
+
+
 # ---------------------------------------------------------------------------
 # paged cache addressing
 # ---------------------------------------------------------------------------
@@ -137,10 +170,10 @@ def _request_rows(case, b: int):
     rows = physical_rows(case.block_table[b], L, bs)
     ckv = case.ckv.reshape(-1, case.ckv.shape[-1])
     kpe = case.kpe.reshape(-1, case.kpe.shape[-1])
-    ckv_rows = decode16(ckv[rows], case.dtype)
-    kpe_rows = decode16(kpe[rows], case.dtype)
-    qa = decode16(case.q_abs[b], case.dtype)  # [q_len, H, r]
-    qp = decode16(case.q_pe[b], case.dtype)  # [q_len, H, d_r]
+    ckv_rows = decode_cache(ckv[rows], case)
+    kpe_rows = decode_cache(kpe[rows], case)
+    qa = decode16(case.q_abs[b], query_dtype(case))  # [q_len, H, r]
+    qp = decode16(case.q_pe[b], query_dtype(case))  # [q_len, H, d_r]
     return L, ckv_rows, kpe_rows, qa, qp
 
 

@@ -87,3 +87,18 @@ def test_concatenated_segments_are_the_segments_in_order():
     for i in range(len(used)):
         for j in range(i + 1, len(used)):
             assert not used[i] & used[j]
+
+
+def test_e4m3_cache_bits_and_case():
+    """E4M3 caches are uint8 patterns with no NaN, magnitudes 0.125 .. 7.5 or zero/subnormal, fp16 queries and a
+    power-of-two cache scale; the byte count of a pass is half the 16-bit one."""
+    c = gen.make_decode_case(3, [500, 77], num_heads=16, block_size=32, dtype="e4m3", cache_scale=0.25)
+    assert c.ckv.dtype == np.uint8 and c.kpe.dtype == np.uint8 and c.q_abs.dtype == np.uint16
+    for x in (c.ckv, c.kpe):
+        assert not np.any((x & 0x7F) == 0x7F)  # no NaN pattern
+        e = (x >> 3) & 0xF
+        assert set(np.unique(e).tolist()) <= {0, 4, 5, 6, 7, 8, 9}
+        assert 0.04 < np.mean(e == 0) < 0.09  # about one entry in 16 is zero or subnormal
+    assert c.cache_scale == 0.25
+    f = gen.make_decode_case(3, [500, 77], num_heads=16, block_size=32, dtype="f16")
+    assert 2 * c.latent_bytes() == f.latent_bytes()

@@ -86,6 +86,17 @@ def _append_one_late(ckv, kpe, block_table, context_lens, ckv_new, kpe_new, bloc
     return ckv, kpe
 
 
+def _e4m3_bias_eight(bits):
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    e, m = (b >> 3) & 0xF, (b & 7).astype(np.float64)
+    val = np.where(e == 0, m * 2.0 ** -10, (1 + m / 8) * np.exp2(e - 8.0))  # exponent bias 8 instead of 7
+    return np.where(b & 0x80, -val, val)
+
+
+def _cache_scale_dropped(bits, case):
+    return orc.decode_e4m3(bits) if case.dtype == "e4m3" else orc.decode16(bits, case.dtype)
+
+
 def _unembed_other_side(o_latent, W_UV_T):
     return np.einsum("hr,hrv->hv", o_latent, W_UV_T[::-1])  # heads' projections swapped
 
@@ -106,6 +117,9 @@ MUTATIONS = [
     ("plan_chunks", _indptr_slip, [pins.test_plan_chunks_covers_every_token_once_request_major]),
     ("cache_append", _append_one_late, [pins.test_cache_append_hand_table,
                                         pins.test_cache_append_of_the_cached_tail_is_the_identity_and_shifted_rows_are_not]),
+    ("decode_e4m3", _e4m3_bias_eight, [pins.test_decode_e4m3_known_bit_patterns,
+                                       pins.test_decode_e4m3_matches_torch_float8_on_every_pattern]),
+    ("decode_cache", _cache_scale_dropped, [pins.test_e4m3_cache_matches_torch_sdpa_with_its_scale]),
     ("unembed", _unembed_other_side, [pins.test_absorbed_equals_decompressed_and_transposed_fold_does_not,
                                       pins.test_merge_unembed_is_the_decompressed_decode_of_a_split]),
 ]

@@ -35,6 +35,50 @@ def test_decode16_known_bit_patterns():
     assert orc.decode16(bf, "bf16").tolist() == [1.0, 3.140625, -0.5, 2.0 ** -126]
 
 
+def test_decode_e4m3_known_bit_patterns():
+    """E4M3 patterns against the format's table (bias 7, subnormals at exponent field 0, 448 the largest)."""
+    bits = np.array([0x00, 0x01, 0x07, 0x08, 0x38, 0x3F, 0x40, 0x7E, 0xB8, 0xFE, 0x5A], dtype=np.uint8)
+    want = [0.0, 2.0 ** -9, 7 * 2.0 ** -9, 2.0 ** -6, 1.0, 1.875, 2.0, 448.0, -1.0, -448.0, 20.0]
+    assert orc.decode_e4m3(bits).tolist() == want
+    neg_zero = orc.decode_e4m3(np.array([0x80], dtype=np.uint8))[0]
+    assert neg_zero == 0.0 and math.copysign(1.0, neg_zero) == -1.0
+    assert np.isnan(orc.decode_e4m3(np.array([0x7F, 0xFF], dtype=np.uint8))).all()
+
+
+def test_decode_e4m3_matches_torch_float8_on_every_pattern():
+    """All 256 patterns against torch's own float8_e4m3fn type (a library decode)."""
+    bits = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(bits).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = orc.decode_e4m3(bits)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok]) and np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+
+def test_e4m3_cache_matches_torch_sdpa_with_its_scale():
+    """An E4M3 cache read as torch float8 values times the cache scale, fp16 queries: textbook SDPA."""
+    case = gen.make_decode_case(8, [40, 11], num_heads=3, block_size=8, dtype="e4m3", cache_scale=0.125)
+    out, lse = orc.unsplit(case)
+    f8 = lambda x: torch.from_numpy(np.ascontiguousarray(x)).view(torch.float8_e4m3fn).to(torch.float64) * 0.125
+    for b in range(2):
+        L = int(case.context_lens[b])
+        K, V = [], []
+        for t in range(L):
+            page = int(case.block_table[b][t // case.block_size])
+            slot = t % case.block_size
+            ck, kp = f8(case.ckv[page, slot]), f8(case.kpe[page, slot])
+            K.append(torch.cat([ck, kp]))
+            V.append(ck)
+        K, V = torch.stack(K), torch.stack(V)
+        Q = torch.tensor(np.concatenate([orc.decode16(case.q_abs[b], "f16"), orc.decode16(case.q_pe[b], "f16")],
+                                        axis=-1)).permute(1, 0, 2)
+        ref = torch.nn.functional.scaled_dot_product_attention(Q, K.expand(3, L, 576), V.expand(3, L, 512),
+                                                               scale=case.scale)
+        np.testing.assert_allclose(out[b], ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+        lse_ref = torch.logsumexp(case.scale * (Q @ K.T), dim=-1) / math.log(2)
+        np.testing.assert_allclose(lse[b], lse_ref.permute(1, 0).numpy(), rtol=0, atol=1e-12)
+
+
 # --- paged addressing and causal rule -----------------------------------------
 
 def test_physical_rows_hand_table():
