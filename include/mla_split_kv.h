@@ -67,7 +67,10 @@ typedef enum {
   MLA_ERR_CAPACITY = 6      /* caller-provided plan arrays are too small       */
 } mla_status_t;
 
-typedef enum { MLA_F16 = 0, MLA_BF16 = 1, MLA_F32 = 2 } mla_dtype_t;
+/* MLA_E4M3: 8-bit E4M3 latent caches (sign, 4 exponent bits with bias 7, 3
+ * mantissa bits; exponent field 0 subnormal; S.1111.111 NaN, no infinities)
+ * read with a power-of-two cache scale, beside fp16 queries. */
+typedef enum { MLA_F16 = 0, MLA_BF16 = 1, MLA_F32 = 2, MLA_E4M3 = 3 } mla_dtype_t;
 
 /* Which partial-decode kernel runs. AUTO picks the tensor-core kernel. */
 typedef enum {
@@ -111,7 +114,9 @@ typedef struct {
   int32_t min_partitions;   /* floor for a request that is split; 0 = 2       */
   int32_t split_min_tokens; /* contexts shorter than this are not split;
                                0 = 4096                                        */
-  int32_t dtype;            /* MLA_F16 or MLA_BF16 (sets rows per CTA)         */
+  int32_t dtype;            /* MLA_F16, MLA_BF16 or MLA_E4M3 (sets rows per CTA;
+                               E4M3 caches need clusters of 2 or more and
+                               q_len * num_heads <= 16, else UNSUPPORTED)      */
   int32_t capacity;         /* entries available in `chunks`                   */
   mla_chunk_t* chunks;      /* host, caller-owned, >= capacity entries         */
   int32_t* o_indptr;        /* host, caller-owned, >= B+1 entries              */
@@ -176,7 +181,11 @@ typedef struct {
   int32_t block_size;         /* tokens per page: 16, 32 or 64                */
   int32_t num_blocks;         /* pages in the cache pool                      */
   int32_t max_blocks_per_req; /* row stride of block_table, in entries        */
-  int32_t dtype;              /* MLA_F16 or MLA_BF16 (q, ckv, kpe)            */
+  int32_t dtype;              /* MLA_F16 or MLA_BF16 (q, ckv, kpe), or MLA_E4M3:
+                                 ckv and kpe 8-bit E4M3 (576 bytes a token),
+                                 q fp16; E4M3 runs on the paired 16-row kernel
+                                 only (q_len * H <= 16, clusters of 2..16 CTAs,
+                                 not MLA_KERNEL_SIMT), else UNSUPPORTED        */
   int32_t causal;             /* 1: the q_len rows are the last q_len tokens
                                  of each request; row i sees t <= L-q_len+i    */
   const mla_chunk_t* chunks;  /* DEVICE array of num_chunks records, or NULL
@@ -237,6 +246,13 @@ typedef struct {
                                  (default): caches are read after it. Other
                                  values, or 1 with tables_ready = 0:
                                  INVALID_ARG.                                  */
+  float cache_scale;          /* MLA_E4M3 caches: the value of a cache byte x is
+                                 e4m3(x) * cache_scale, a power of two in
+                                 [2^-24, 2^24] (so the scores and the output
+                                 take it without rounding; the scalar folded
+                                 in as mlxcel PR #995, *What changed*, folds
+                                 a global scale). Other dtypes: ignored.
+                                 Anything else with E4M3: INVALID_ARG.         */
 } mla_decode_desc_t;
 
 /*
@@ -305,10 +321,14 @@ mla_status_t mla_decode_partial_static(const void* q_absorbed, const void* q_pe,
  * lse = -inf. The token t of request b lives in cache row
  * block_table[b, t / bs] * bs + t % bs.
  *
- * q_absorbed : device [B, q_len, H, 512] dtype, 16-byte aligned
- * q_pe       : device [B, q_len, H, 64]  dtype, 16-byte aligned
- * ckv_cache  : device [num_blocks, bs, 512] dtype, 16-byte aligned
- * kpe_cache  : device [num_blocks, bs, 64]  dtype, 16-byte aligned
+ * q_absorbed : device [B, q_len, H, 512] dtype (fp16 for MLA_E4M3), 16-byte
+ *              aligned
+ * q_pe       : device [B, q_len, H, 64]  dtype (fp16 for MLA_E4M3), 16-byte
+ *              aligned
+ * ckv_cache  : device [num_blocks, bs, 512] dtype (bytes for MLA_E4M3),
+ *              16-byte aligned
+ * kpe_cache  : device [num_blocks, bs, 64]  dtype (bytes for MLA_E4M3),
+ *              16-byte aligned
  * block_table: device [B, max_blocks_per_req] int32; entries past a request's
  *              last page are never read. An entry outside [0, num_blocks)
  *              reads zeros and raises MLA_ERR_DEVICE_CHECK at the next

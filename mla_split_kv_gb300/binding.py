@@ -23,7 +23,7 @@ MLA_ERR_TIMEOUT = 4
 MLA_ERR_DEVICE_CHECK = 5
 MLA_ERR_CAPACITY = 6
 
-MLA_F16, MLA_BF16, MLA_F32 = 0, 1, 2
+MLA_F16, MLA_BF16, MLA_F32, MLA_E4M3 = 0, 1, 2, 3
 MLA_STATIC_WORKSPACE_BYTES = 4 * 1024 * 1024
 MLA_KERNEL_AUTO, MLA_KERNEL_SIMT, MLA_KERNEL_TC = 0, 1, 2
 MLA_MERGE_ENTRIES, MLA_MERGE_PARTIALS = 0, 1
@@ -32,7 +32,7 @@ MLA_DECODE_MERGE_ENTRIES, MLA_DECODE_MERGE_TICKETS = 0, 1
 CTR_PARTIAL_SIMT, CTR_PARTIAL_TC, CTR_MERGE, CTR_REJECTED, CTR_CTAS, CTR_DECODE_FUSED, CTR_WRAP = range(7)
 NUM_COUNTERS = 7
 
-DTYPE_CODES = {"f16": MLA_F16, "bf16": MLA_BF16, "f32": MLA_F32}
+DTYPE_CODES = {"f16": MLA_F16, "bf16": MLA_BF16, "f32": MLA_F32, "e4m3": MLA_E4M3}
 
 
 class MlaError(RuntimeError):
@@ -87,6 +87,7 @@ class mla_decode_desc_t(ctypes.Structure):
         ("tables_ready", ctypes.c_int32),
         ("decode_merge", ctypes.c_int32),
         ("prefix_ready", ctypes.c_int32),
+        ("cache_scale", ctypes.c_float),
     ]
 
 

@@ -44,7 +44,8 @@ struct MapKey {
   uint32_t box_rows;
   int dtype;
   int device;
-  int kind;  // 0: the 2D map; 1: the page map of the ckv cache (see page_map); 2: the kpe half map
+  int kind;  // 0: the 2D map; 1: the page map of the ckv cache (see page_map); 2: the kpe half map;
+             // 3 / 4: the ckv / kpe half maps of an E4M3 cache (bytes, no swizzle)
 };
 struct MapEntry {
   MapKey key;
@@ -80,6 +81,13 @@ bool page_map(CUtensorMap* out, const void* base, uint64_t rows, uint32_t box_ro
 // 2D map over the [rows, 64] kpe cache with boxes of 32 columns x box_rows rows
 // and the 64-byte swizzle: one half of the rope columns of a page, rows of 64
 // bytes (two K=16 steps of a K-major tensor-core operand).
+// The maps of an E4M3 cache: a CTA's half of each row (ckv 256 of 512 columns, kpe 32 of 64), bytes.
+bool fp8_half_map(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, int kind) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  return encode_map(out, MapKey{base, rows, cols, box_rows, MLA_E4M3, dev, kind});
+}
+
 bool kpe_half_map(CUtensorMap* out, const void* base, uint64_t rows, uint32_t box_rows, int dtype) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
@@ -100,7 +108,17 @@ bool encode_map(CUtensorMap* out, const MapKey& key) {
   const CUtensorMapDataType dt =
       key.dtype == MLA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUresult r;
-  if (key.kind == 0) {
+  if (key.kind == 3 || key.kind == 4) {
+    // E4M3 bytes: [rows][cols] with one byte an element; a box is one CTA's half of the row's columns
+    // (256 of the 512 latent, 32 of the 64 rope) for box_rows rows, landing unswizzled
+    cuuint64_t dims[2] = {key.cols, key.rows};
+    cuuint64_t strides[1] = {key.cols};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(key.cols / 2), key.box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(key.base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else if (key.kind == 0) {
     cuuint64_t dims[2] = {key.cols, key.rows};
     cuuint64_t strides[1] = {key.cols * 2};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(mla::kBoxCols), key.box_rows};
@@ -188,7 +206,15 @@ mla_status_t check_decode(const void* q_absorbed, const void* q_pe, const void* 
   if (d->num_requests < 1 || d->num_blocks < 1 || d->max_blocks_per_req < 1) return MLA_ERR_INVALID_ARG;
   if (!valid_heads(d->num_heads) || d->q_len < 1 || d->q_len > MLA_MAX_Q_LEN) return MLA_ERR_UNSUPPORTED;
   if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64) return MLA_ERR_UNSUPPORTED;
-  if (d->dtype != MLA_F16 && d->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (d->dtype != MLA_F16 && d->dtype != MLA_BF16 && d->dtype != MLA_E4M3) return MLA_ERR_UNSUPPORTED;
+  if (d->dtype == MLA_E4M3) {
+    // E4M3 caches: the paired 16-row kernel only, and a power-of-two scale
+    if (d->kernel == MLA_KERNEL_SIMT || d->num_heads * d->q_len > 16 || d->cluster_ctas == 1)
+      return MLA_ERR_UNSUPPORTED;
+    int e = 0;
+    const float f = std::frexp(d->cache_scale, &e);
+    if (!std::isfinite(d->cache_scale) || f != 0.5f || e < -23 || e > 25) return MLA_ERR_INVALID_ARG;
+  }
   if (d->causal != 0 && d->causal != 1) return MLA_ERR_INVALID_ARG;
   if (d->tables_ready != 0 && d->tables_ready != 1) return MLA_ERR_INVALID_ARG;
   if (d->decode_merge != MLA_DECODE_MERGE_ENTRIES && d->decode_merge != MLA_DECODE_MERGE_TICKETS)
@@ -248,7 +274,8 @@ int launch_cluster(const mla_decode_desc_t* d, int64_t N) {
   const int nr = use_simt ? mla::simt_rows_per_cta()
                           : (mh ? 128 : mla::tc_rows_per_cta(rows_total, d->dtype == MLA_BF16));
   const int64_t groups = (rows_total + nr - 1) / nr;
-  return d->cluster_ctas ? d->cluster_ctas : (mh ? 2 : default_cluster(N * groups));
+  const int C = d->cluster_ctas ? d->cluster_ctas : (mh ? 2 : default_cluster(N * groups));
+  return (d->dtype == MLA_E4M3 && C < 2) ? 2 : C;  // E4M3 runs on CTA pairs
 }
 
 // One launch of the partial kernel the descriptor selects (arguments already checked; N chunks;
@@ -271,12 +298,21 @@ mla_status_t launch_decode(const void* q_absorbed, const void* q_pe, const void*
   const int C = launch_cluster(d, N);
 
   CUtensorMap tm_ckv, tm_kpe, tm_pages, tm_kpe_half;
-  if (!tensor_map(&tm_ckv, ckv_cache, rows, mla::kRank, d->block_size, d->dtype) ||
-      !tensor_map(&tm_kpe, kpe_cache, rows, mla::kRope, d->block_size, d->dtype) ||
-      !page_map(&tm_pages, ckv_cache, rows, d->block_size, d->dtype) ||
-      !kpe_half_map(&tm_kpe_half, kpe_cache, rows, d->block_size, d->dtype)) {
+  const bool fp8 = (d->dtype == MLA_E4M3);
+  if (fp8) {
+    // the paired kernel takes the E4M3 half maps where it takes the 16-bit page and kpe half maps
+    std::memset(&tm_ckv, 0, sizeof(tm_ckv));
+    std::memset(&tm_kpe, 0, sizeof(tm_kpe));
+    if (!fp8_half_map(&tm_pages, ckv_cache, rows, mla::kRank, d->block_size, 3) ||
+        !fp8_half_map(&tm_kpe_half, kpe_cache, rows, mla::kRope, d->block_size, 4))
+      return reject(MLA_ERR_CUDA);
+  } else if (!tensor_map(&tm_ckv, ckv_cache, rows, mla::kRank, d->block_size, d->dtype) ||
+             !tensor_map(&tm_kpe, kpe_cache, rows, mla::kRope, d->block_size, d->dtype) ||
+             !page_map(&tm_pages, ckv_cache, rows, d->block_size, d->dtype) ||
+             !kpe_half_map(&tm_kpe_half, kpe_cache, rows, d->block_size, d->dtype)) {
     return reject(MLA_ERR_CUDA);
   }
+  if (fp8 && (use_simt || !mla::tc128_supports(rows_total, false, C))) return reject(MLA_ERR_UNSUPPORTED);
 
   mla::PartialParams p;
   p.q_abs = static_cast<const uint16_t*>(q_absorbed);
@@ -288,7 +324,10 @@ mla_status_t launch_decode(const void* q_absorbed, const void* q_pe, const void*
   p.chunks = d->chunks;
   p.partials = partials;
   p.lse = lse;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  // an E4M3 cache's scale (a power of two) multiplies every score: folded into the score scale
+  p.scale_log2 = scale * 1.4426950408889634f * (fp8 ? d->cache_scale : 1.0f);
+  p.fp8 = fp8 ? 1 : 0;
+  p.cache_scale = fp8 ? d->cache_scale : 1.0f;
   p.B = d->num_requests;
   p.H = d->num_heads;
   p.q_len = d->q_len;

@@ -36,6 +36,8 @@ struct PartialParams {
   int32_t num_parts;           // uniform split when chunks == null
   int32_t causal;
   int32_t tables_ready;        // chunks / context_lens / block_table may be read before the dependency wait
+  int32_t fp8;                 // E4M3 caches (the paired kernel): loaded as bytes, converted to fp16 in the slot
+  float cache_scale;           // E4M3: the value of byte x is e4m3(x) * cache_scale (folded into scale_log2 and O)
   int32_t prefix_ready;        // cache rows before each request's window may be read before the dependency wait
   uint64_t timeout_ns;
   // a chunk spread over `subs` clusters (the paired 16-row kernel): grid.y = chunks * subs.

@@ -53,6 +53,8 @@
 // tile's pages measured slower over a sweep of caches larger than L2, so
 // there is none. The kernel is a programmatic dependent launch: its set-up overlaps the
 // end of the previous kernel in the stream.
+#include <cuda_fp8.h>
+
 #include "device_common.cuh"
 
 namespace mla {
@@ -77,6 +79,12 @@ constexpr int kThreads = (kSoftmaxWarps + 1 + kPageWarps) * 32;  // 384: three w
 constexpr int kRH = kNR / 2;                     // rows per softmax thread
 constexpr int kMaxPagesPerWarp = (kT / 16 + kPageWarps - 1) / kPageWarps;  // pages of 16 tokens or more
 constexpr float kRescaleTau = 8.0f;
+// E4M3 caches: a tile's bytes land unswizzled in the upper half of its slot (staged rows of 256
+// bytes: ckv tokens 0-127, then the kpe, 8 tokens a row) and are widened to fp16 in place.
+constexpr int kStage = kTileSlot - kT * (kHalfCols + kKpeCols);  // 36 KB
+constexpr int kStageRows = kT * (kHalfCols + kKpeCols) / kHalfCols;  // 144
+static_assert(kStage == 9 * kGroupBytes && kStageRows == 144 && kCkvBytes == kStage + 112 * kHalfCols,
+              "the widening order below assumes this geometry");
 
 constexpr uint32_t kOffTile = 0;                            // 3 tile slots
 constexpr uint32_t kOffQ = kSlots * kTileSlot;              // 216 KB: Q^T
@@ -102,6 +110,9 @@ struct Small {
   // tile is done: its kpe part is free for this CTA's partial S); pvdone per tile parity
   uint64_t full[kSlots], empty[kSlots], sfull[2], sfree[2], ppfull[kSlots], pvdone[2], xfull[kSlots],
       xready[kSlots], drain;
+  // E4M3 caches: the bytes of a tile landed in its slot (TMA), and the producer warps' meeting point
+  // inside each tile's in-place conversion (one phase per tile)
+  uint64_t landed[kSlots], conv;
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t last_cluster;  // this CTA took the last ticket of its chunk half (spread plans)
@@ -111,6 +122,19 @@ struct Small {
   float alpha[kNR];
 };
 static_assert(sizeof(Small) <= kSmallBytes, "small smem region");
+
+// eight E4M3 values (bytes in column order) -> eight fp16 values; exact (every E4M3 value, its
+// subnormals included, is an fp16 value)
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 v) {
+  uint32_t o[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t w = (k < 2) ? v.x : v.y;
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> (16 * (k & 1))), __NV_E4M3);
+    o[k] = static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
 
 __device__ __forceinline__ uint32_t tmem_lane_base(int warp) { return static_cast<uint32_t>(32 * (warp & 3)) << 16; }
 
@@ -146,7 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm->ppfull[s], kSoftmaxWarps);
       mbar_init(&sm->xfull[s], 1);   // local expect_tx arrival + the peer's st.async bytes
       mbar_init(&sm->xready[s], 1);  // the peer's MMA commit
+      mbar_init(&sm->landed[s], kPageWarps);
     }
+    mbar_init(&sm->conv, kPageWarps);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm->sfull[t], 1);
       mbar_init(&sm->sfree[t], kSoftmaxWarps);
@@ -202,6 +228,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tile_issue = [&](int i, const int* pids, int mine, uint64_t pol) {
     const int s = i % kSlots;
     uint8_t* slot = smem + kOffTile + s * kTileSlot;
+    if (p.fp8) {
+      // E4M3 bytes, unswizzled, into the upper half of the slot: ckv rows of 256 bytes, then kpe rows of 32
+      if (lane == 0) mbar_arrive_expect_tx(&sm->landed[s], static_cast<uint32_t>(mine * p.bs * (kHalfCols + kKpeCols)));
+      __syncwarp();
+#pragma unroll
+      for (int m = 0; m < kMaxPagesPerWarp; ++m) {
+        if (lane == m && m < mine) {
+          const int j = k0 + m * kPageWarps;  // page of the tile
+          tma_load_2d(slot + kStage + j * p.bs * kHalfCols, &tm_pages, kHalfCols * half, pids[m] * p.bs,
+                      &sm->landed[s], pol);
+          tma_load_2d(slot + kStage + kT * kHalfCols + j * p.bs * kKpeCols, &tm_kpe_half, kKpeCols * half,
+                      pids[m] * p.bs, &sm->landed[s], pol);
+        }
+      }
+      return;
+    }
     if (lane == 0) mbar_arrive_expect_tx(&sm->full[s], static_cast<uint32_t>(mine * p.bs * (kHalfCols + kKpeCols) * 2));
     __syncwarp();
 #pragma unroll
@@ -214,6 +256,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                     &sm->full[s], pol);
       }
     }
+  };
+  // E4M3 caches: tile i's staged bytes become the 16-bit tile in place, in the layouts the 16-bit loads
+  // give (ckv: 128-byte-swizzled [8 x 64] atoms, a 4 KB row group per 8 tokens; kpe: 64-byte
+  // swizzle), by the three producer warps, a staged row per warp and step, 8 bytes a lane. The 16-bit
+  // rows of ckv tokens 0-71 lie below the staging; those of tokens 8g..8g+7 (g >= 9) overwrite staged
+  // rows 16(g-9)..16(g-9)+15, and the 16-bit kpe staged rows 112-143. So, with the three warps
+  // meeting between the steps: tokens 0-71 | tokens 72-103 | tokens 104-119, then the staged rows
+  // 120-143 into registers | tokens 120-127 and the kpe from those registers. Every staged row is read
+  // before a step that overwrites it. Lane 0 of each warp then counts it on the slot's full barrier.
+  const int cb = lane >> 3, c8 = lane & 7;  // ckv: a lane's 64-column block and 8-column piece
+  auto ckv_dst = [&](uint8_t* slot, int t) -> uint8_t* {
+    return slot + (t >> 3) * kGroupBytes + cb * 1024 + (t & 7) * 128 + ((c8 ^ (t & 7)) << 4);
+  };
+  auto widen_rows = [&](uint8_t* slot, int t0, int t1, int first) {  // ckv tokens [t0, t1)
+#pragma unroll 4
+    for (int t = t0 + first; t < t1; t += kPageWarps)
+      *reinterpret_cast<uint4*>(ckv_dst(slot, t)) =
+          e4m3x8_to_f16x8(*reinterpret_cast<const uint2*>(slot + kStage + t * kHalfCols + lane * 8));
+  };
+  auto meet = [&](int phase) -> bool {  // the three producer warps; three phases per tile
+    __syncwarp();
+    int ok = 1;
+    if (lane == 0) {
+      mbar_arrive(&sm->conv);
+      ok = mbar_wait(&sm->conv, phase & 1, p.timeout_ns);
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+  };
+  auto convert = [&](int i) -> bool {
+    const int s = i % kSlots;
+    uint8_t* slot = smem + kOffTile + s * kTileSlot;
+    if (!__all_sync(0xffffffffu, mbar_wait(&sm->landed[s], (i / kSlots) & 1, p.timeout_ns))) return false;
+    widen_rows(slot, 0, 72, k0);
+    if (!meet(3 * i)) return false;
+    widen_rows(slot, 72, 104, k0);
+    if (!meet(3 * i + 1)) return false;
+    widen_rows(slot, 104, 120, (k0 + 1) % kPageWarps);  // rotated: 48 rows per warp over the tile
+    uint2 held[8];  // staged rows 120 + k0 + 3m: ckv tokens 120-127, then the kpe rows
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+      held[m] = *reinterpret_cast<const uint2*>(slot + kStage + (120 + k0 + kPageWarps * m) * kHalfCols + lane * 8);
+    if (!meet(3 * i + 2)) return false;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int r = k0 + kPageWarps * m;
+      uint8_t* dst;
+      if (r < 8) {
+        dst = ckv_dst(slot, 120 + r);
+      } else {  // kpe tokens 8(r-8) .. 8(r-8)+7: 32 bytes each, four pieces
+        const int t = (r - 8) * 8 + (lane >> 2), c = lane & 3;
+        dst = slot + kCkvBytes + t * (kKpeCols * 2) + ((c ^ (t >> 1)) & 3) * 16;
+      }
+      *reinterpret_cast<uint4*>(dst) = e4m3x8_to_f16x8(held[m]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm->full[s]);
+    return true;
   };
   int issued = -1;  // producers: the last tile whose loads this warp issued
   if (p.tables_ready) {
@@ -253,7 +355,57 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp > kMmaWarp) {
     // ------------------------------------------------------------------ producers
     const uint64_t pol = l2_policy_evict_first();
-    for (int i = issued + 1; i < ntiles; ++i) {
+    if (p.fp8) {
+      // Issue and widening interleave: the next tile's loads as soon as its slot is free, else the
+      // widening of the oldest landed tile; nothing to do for longer than the wait limit (or an abort
+      // elsewhere) ends it
+      int ni = issued + 1, nc = 0;
+      bool idle = false;
+      uint64_t idle_t0 = 0;
+      while (nc < ntiles) {
+        int act = 0;
+        if (lane == 0) {
+          if (ni < ntiles && ni < nc + kSlots &&
+              (ni < kSlots || mbar_test(&sm->empty[ni % kSlots], ((ni / kSlots) - 1) & 1))) {
+            act = 1;
+          } else if (nc < ni && mbar_test(&sm->landed[nc % kSlots], (nc / kSlots) & 1)) {
+            act = 2;
+          } else if (*abort_flag) {
+            act = -1;
+          } else {
+            const uint64_t now = globaltimer_ns();
+            if (!idle) {
+              idle = true;
+              idle_t0 = now;
+            } else if (now - idle_t0 > p.timeout_ns) {
+              act = -1;
+              *abort_flag = 1;
+              flag_error(MLA_DEVERR_TIMEOUT);
+            }
+          }
+          if (act > 0) idle = false;
+        }
+        act = __shfl_sync(0xffffffffu, act, 0);
+        if (act == 1) {
+          int pids[kMaxPagesPerWarp];
+          const int mine = tile_pids(ni, pids);
+          tile_issue(ni, pids, mine, pol);
+          issued = ni++;
+        } else if (act == 2) {
+          if (!convert(nc)) {
+            if (lane == 0) {
+              *abort_flag = 1;
+              flag_error(MLA_DEVERR_TIMEOUT);
+            }
+            break;
+          }
+          ++nc;
+        } else if (act < 0) {
+          break;
+        }
+      }
+    }
+    for (int i = p.fp8 ? ntiles : issued + 1; i < ntiles; ++i) {
       const int s = i % kSlots;
       // the pages of tile i first: their block-table reads overlap the wait for the slot
       int pids[kMaxPagesPerWarp];
@@ -273,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // slot) land before shared memory is released
     if (lane == 0 && *abort_flag)
       for (int t = max(0, issued - (kSlots - 1)); t <= issued; ++t)
-        mbar_wait(&sm->full[t % kSlots], (t / kSlots) & 1, kDrainTimeoutNs);
+        mbar_wait(p.fp8 ? &sm->landed[t % kSlots] : &sm->full[t % kSlots], (t / kSlots) & 1, kDrainTimeoutNs);
     cluster_wait_acquire();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
@@ -673,6 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* const eml = p.ws_lse + (entry * 2 + half) * rows_total * 2;               // [rows][m, l]
     if (warp < kSoftmaxWarps) {
       const int q4 = warp & 3, h = warp >> 2;
+      const float cs = p.cache_scale;  // an E4M3 cache's scale (1 for 16-bit caches): exact, a power of two
       if (have) tc_fence_after();
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
@@ -680,6 +833,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (have) {
           tmem_ld8(tmem + tmem_lane_base(q4) + 2 * kNR + blk * kNR + kRH * h, v);
           tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < kRH; ++k) v[k] *= cs;
         } else {
 #pragma unroll
           for (int k = 0; k < kRH; ++k) v[k] = 0.f;
@@ -813,7 +968,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         const int d = blk * 128 + q4 * 32 + lane;
 #pragma unroll
-        for (int k = 0; k < kRH; ++k) ostage[(kRH * h + k) * kHalfCols + d] = v[k];
+        for (int k = 0; k < kRH; ++k) ostage[(kRH * h + k) * kHalfCols + d] = v[k] * p.cache_scale;
       }
     } else {
       for (int idx = tid; idx < kNR * kHalfCols; idx += kSoftmaxThreads) ostage[idx] = 0.f;

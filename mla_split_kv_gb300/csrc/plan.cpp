@@ -81,7 +81,7 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
   if (num_heads != 16 && num_heads != 64 && num_heads != 128) return MLA_ERR_UNSUPPORTED;
   if (q_len < 1 || q_len > MLA_MAX_Q_LEN) return MLA_ERR_UNSUPPORTED;
   if (block_size != 16 && block_size != 32 && block_size != 64) return MLA_ERR_UNSUPPORTED;
-  if (plan->dtype != MLA_F16 && plan->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (plan->dtype != MLA_F16 && plan->dtype != MLA_BF16 && plan->dtype != MLA_E4M3) return MLA_ERR_UNSUPPORTED;
   if (plan->capacity < 0 || plan->max_partitions < 0 || plan->min_partitions < 0 || plan->split_min_tokens < 0)
     return MLA_ERR_INVALID_ARG;
   if (plan->merge_path != MLA_MERGE_ENTRIES && plan->merge_path != MLA_MERGE_PARTIALS) return MLA_ERR_INVALID_ARG;
@@ -96,6 +96,7 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
   if (maxP < 1 || maxP > 1024) return MLA_ERR_INVALID_ARG;
 
   const int rows = num_heads * q_len;
+  if (plan->dtype == MLA_E4M3 && rows > 16) return MLA_ERR_UNSUPPORTED;  // E4M3: the paired 16-row kernel only
   // more than 16 rows: one CTA pair (a cluster of 2) per 128 rows, the last group padded
   const bool many_rows = mla::mh_supports(rows, 2);
   const int nr = many_rows ? 128 : mla::tc_rows_per_cta(rows, plan->dtype == MLA_BF16);
@@ -116,6 +117,7 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
     const int64_t slots = dev->max_clusters[k];
     if (slots <= 0) continue;
     if (paired_single && C == 1) continue;  // the paired kernel needs a pair of CTAs
+    if (plan->dtype == MLA_E4M3 && C == 1) continue;  // so do E4M3 caches, always
     if (many_rows && C != 2) continue;      // the 128-row kernel runs on CTA pairs
     Candidate cand;
     cand.cluster = C;

@@ -34,13 +34,26 @@ class DeviceCase:
     case: DecodeCase
 
 
+def to_device_cache(bits: np.ndarray, dtype: str, device) -> torch.Tensor:
+    """Cache patterns -> device: 16-bit floats (bit-exact), or E4M3 bytes as uint8."""
+    if dtype == "e4m3":
+        return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint8)).to(device)
+    return to_device_16(bits, dtype, device)
+
+
+def query_dtype(dtype: str) -> str:
+    """The queries' 16-bit type beside a cache of `dtype`: fp16 beside E4M3."""
+    return "f16" if dtype == "e4m3" else dtype
+
+
 def upload(case: DecodeCase, device="cuda", ckv: torch.Tensor = None, kpe: torch.Tensor = None) -> DeviceCase:
     """Copy a case to the device. A resident cache (ckv/kpe) can be shared."""
+    qdt = query_dtype(case.dtype)
     return DeviceCase(
-        q_abs=to_device_16(case.q_abs, case.dtype, device),
-        q_pe=to_device_16(case.q_pe, case.dtype, device),
-        ckv=ckv if ckv is not None else to_device_16(case.ckv, case.dtype, device),
-        kpe=kpe if kpe is not None else to_device_16(case.kpe, case.dtype, device),
+        q_abs=to_device_16(case.q_abs, qdt, device),
+        q_pe=to_device_16(case.q_pe, qdt, device),
+        ckv=ckv if ckv is not None else to_device_cache(case.ckv, case.dtype, device),
+        kpe=kpe if kpe is not None else to_device_cache(case.kpe, case.dtype, device),
         block_table=torch.from_numpy(np.ascontiguousarray(case.block_table)).to(device),
         context_lens=torch.from_numpy(np.ascontiguousarray(case.context_lens)).to(device),
         case=case,
@@ -78,6 +91,7 @@ def make_desc(dc: DeviceCase, chunks_dev: Optional[torch.Tensor], kernel: int, c
     d.tables_ready = 1 if tables_ready else 0
     d.decode_merge = decode_merge
     d.prefix_ready = 1 if prefix_ready else 0
+    d.cache_scale = float(c.cache_scale)
     # the descriptor holds raw device pointers: keep their tensors alive as long as it lives
     d._keep = (chunks_dev, workspace)
     return d

@@ -127,6 +127,19 @@ def test_plan_spreads_partitions_only_for_the_paired_kernel(lib):
             assert t1 - t0 >= k * (C // 2) * 128
 
 
+@pytest.mark.parametrize("lens", [[131072], [700], [4096] * 8, [32768, 100, 9000, 0], [20000] * 64])
+def test_plan_for_e4m3_caches_keeps_pairs(lib, lens):
+    # E4M3 caches run on CTA pairs only: every plan uses clusters of 2 or more, and otherwise splits the
+    # contexts as for fp16 caches whenever the fp16 plan already uses pairs
+    pe = nb.mla_plan(lens, 16, 1, 32, fake_gb300(), dtype="e4m3")
+    pf = nb.mla_plan(lens, 16, 1, 32, fake_gb300(), dtype="f16")
+    assert pe.cluster_ctas >= 2
+    check_plan_tiles(pe, lens, 32)
+    if pf.cluster_ctas >= 2:
+        assert (pe.chunks, pe.o_indptr, pe.cluster_ctas, pe.clusters_per_chunk) == \
+            (pf.chunks, pf.o_indptr, pf.cluster_ctas, pf.clusters_per_chunk)
+
+
 def test_workspace_bytes(lib):
     assert nb.mla_workspace_bytes(8, 1, 4, 1, 16) == 0
     assert nb.mla_workspace_bytes(8, 4, 1, 1, 16) == 0
@@ -242,6 +255,9 @@ def test_plan_capacity_and_argument_errors(lib):
     assert lib.mla_plan(lens, 0, 16, 1, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_INVALID_ARG
     plan.dtype = 2
     assert lib.mla_plan(lens, 1, 16, 1, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_UNSUPPORTED
+    plan.dtype = nb.MLA_E4M3  # E4M3 caches run on the paired 16-row kernel only
+    assert lib.mla_plan(lens, 1, 64, 1, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_UNSUPPORTED
+    assert lib.mla_plan(lens, 1, 16, 2, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_UNSUPPORTED
     plan.dtype = 0
     neg = (ctypes.c_int32 * 1)(-5)
     assert lib.mla_plan(neg, 1, 16, 1, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_INVALID_ARG
@@ -285,6 +301,20 @@ def call_partial(lib, d, P=2, ptrs=None):
     (dict(prefix_ready=1), 2, nb.MLA_ERR_INVALID_ARG),  # early cache reads need the tables early too
     (dict(), 0, nb.MLA_ERR_INVALID_ARG),
     (dict(num_requests=40000), 2, nb.MLA_ERR_UNSUPPORTED),
+    (dict(dtype=4, cluster_ctas=2), 2, nb.MLA_ERR_UNSUPPORTED),
+    # E4M3 caches: the paired 16-row kernel only, and a power-of-two cache scale in [2^-24, 2^24]
+    (dict(dtype=nb.MLA_E4M3, cache_scale=1.0), 2, nb.MLA_ERR_UNSUPPORTED),  # clusters of 1
+    (dict(dtype=nb.MLA_E4M3, cluster_ctas=2, kernel=nb.MLA_KERNEL_SIMT, cache_scale=1.0), 2,
+     nb.MLA_ERR_UNSUPPORTED),
+    (dict(dtype=nb.MLA_E4M3, cluster_ctas=2, num_heads=64, cache_scale=1.0), 2, nb.MLA_ERR_UNSUPPORTED),
+    (dict(dtype=nb.MLA_E4M3, cluster_ctas=2, q_len=2, cache_scale=1.0), 2, nb.MLA_ERR_UNSUPPORTED),
+    (dict(dtype=nb.MLA_E4M3, cluster_ctas=2), 2, nb.MLA_ERR_INVALID_ARG),  # cache_scale left 0
+    (dict(dtype=nb.MLA_E4M3, cluster_ctas=2, cache_scale=0.3), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(dtype=nb.MLA_E4M3, cluster_ctas=2, cache_scale=-0.25), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(dtype=nb.MLA_E4M3, cluster_ctas=2, cache_scale=2.0 ** -25), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(dtype=nb.MLA_E4M3, cluster_ctas=2, cache_scale=2.0 ** 25), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(dtype=nb.MLA_E4M3, cluster_ctas=2, cache_scale=float("inf")), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(dtype=nb.MLA_E4M3, cluster_ctas=2, cache_scale=float("nan")), 2, nb.MLA_ERR_INVALID_ARG),
 ])
 def test_decode_partial_rejects_before_launch(lib, kw, P, want):
     nb.mla_reset_counters()
@@ -357,7 +387,8 @@ def test_descriptor_keeps_its_tensors_alive():
     import weakref
     import torch
     from mla_split_kv_gb300 import runtime as rt
-    case = types.SimpleNamespace(num_requests=1, num_heads=16, q_len=1, block_size=32, dtype="f16", causal=False)
+    case = types.SimpleNamespace(num_requests=1, num_heads=16, q_len=1, block_size=32, dtype="f16", causal=False,
+                                 cache_scale=1.0)
     dc = types.SimpleNamespace(case=case, ckv=torch.zeros(4, 1), block_table=torch.zeros(1, 4, dtype=torch.int32))
     chunks = torch.zeros(3, 4, dtype=torch.int32)
     ws = torch.zeros(256, dtype=torch.uint8)
