@@ -23,7 +23,8 @@ chunk partials), `partial_kernel_alone` (the ABI's mla_decode_partial),
 `per_ctx` (each context alone, its planned split, a single cold call after an
 L2 flush and the host planner's time per call), `trials` (median / min / max
 over five more K-step trials), `many_heads` (the many-head workload),
-`verify_windows` and `batch_grid`. `--impl reference` times the oracle itself
+`verify_windows`, `batch_grid` and `e4m3_caches` (the same sweep on 8-bit E4M3
+caches). `--impl reference` times the oracle itself
 on the same workload; `--gpus N` without a launcher starts N ranks (one
 replica per GPU).
 """
@@ -64,6 +65,8 @@ def parse():
     ap.add_argument("--profile-verify", type=int, default=0,
                     help="profiling case: only --launches plain verify-window calls of this q_len, then exit")
     ap.add_argument("--launches", type=int, default=5)
+    ap.add_argument("--profile-cache", default="f16", choices=["f16", "e4m3"],
+                    help="profiling case at --profile-ctx: the cache type (e4m3: 8-bit caches, scale 1/4)")
     ap.add_argument("--profile-split", default="",
                     help="profiling case: 'P,C' = a uniform split into P partitions on clusters of C CTAs instead of "
                          "the planner's plan")
@@ -135,13 +138,14 @@ class OraclePool:
         self.pool.join()
 
 
-def make_case(i, L):
-    """Context i of the sweep: seeded latents, a pool 25% larger than needed, random page order."""
+def make_case(i, L, dtype=DTYPE):
+    """Context i of the sweep: seeded latents, a pool 25% larger than needed, random page order (E4M3 caches:
+    cache scale 1/4)."""
     from mla_split_kv_gb300 import inputs as gen
 
     pages = gen.pages_for(L, BS)
-    return gen.make_decode_case(SEED * 100 + i, [L], num_heads=H, block_size=BS, dtype=DTYPE,
-                                pool_blocks=pages + pages // 4)
+    return gen.make_decode_case(SEED * 100 + i, [L], num_heads=H, block_size=BS, dtype=dtype,
+                                pool_blocks=pages + pages // 4, cache_scale=0.25)
 
 
 def make_cases():
@@ -427,10 +431,10 @@ def planner_host_us(nb, lens, dev, batches=5, reps=400):
     return statistics.median(per)
 
 
-def algorithmic_bytes(L, n_chunks):
+def algorithmic_bytes(L, n_chunks, latent_per_token=LATENT_BYTES_PER_TOKEN):
     """(partial kernel bytes, merge kernel bytes) one layer call must move."""
     pages = (L + BS - 1) // BS
-    latent = L * LATENT_BYTES_PER_TOKEN
+    latent = L * latent_per_token
     table = pages * 4
     queries = H * 576 * 2
     partial_io = n_chunks * H * 513 * 4  # partials + lse written
@@ -546,9 +550,9 @@ def run_profile_case(args):
     nb.load()
     L = args.profile_ctx
     i = CONTEXTS.index(L) if L in CONTEXTS else 0
-    case = make_case(i, L)
+    case = make_case(i, L, args.profile_cache)
     dev = nb.mla_device_query()
-    plan = nb.mla_plan([L], H, 1, BS, dev)
+    plan = nb.mla_plan([L], H, 1, BS, dev, dtype=args.profile_cache)
     num_partitions = 1
     if args.profile_split:  # the library's uniform split instead: P partitions on clusters of C CTAs, one each
         P, C = (int(x) for x in args.profile_split.split(","))
@@ -567,7 +571,8 @@ def run_profile_case(args):
                   chunks_dev=chunks_dev, subs=k, workspace=ws, tables_ready=True, prefix_ready=True)
     torch.cuda.synchronize()
     st, code = nb.mla_check_device_errors(None)
-    print(json.dumps({"profile_ctx": L, "launches": args.launches, "partitions": plan.num_chunks,
+    print(json.dumps({"profile_ctx": L, "cache": args.profile_cache, "launches": args.launches,
+                      "partitions": plan.num_chunks,
                       "cluster": plan.cluster_ctas, "clusters_per_partition": k,
                       "kernel": partial_kernel_name(args.kernel, [plan]),
                       "device_status": st, "device_error": code}))
@@ -649,6 +654,66 @@ def time_many_heads(nb, rt, torch, stream, reps=20):
             "cluster": plan.cluster_ctas, "tokens": tokens, "tflops": round(flops / (us * 1e-6) / 1e12, 1),
             "hbm_gbs": round(tokens * LATENT_BYTES_PER_TOKEN / (us * 1e-6) / 1e9, 1),
             "note": "a parity workload timed beside the headline one; repeats of one cache (323 MB, > L2)"}
+
+
+# the headline sweep with 8-bit E4M3 caches (576 bytes a token, power-of-two cache scale 1/4) beside fp16
+# queries: the same contexts, seeds and pools, planned for E4M3 caches
+E4M3_SWEEP = "mla_decode_ctx_sweep_B1_H16_e4m3_cache_fp16_q_bs32"
+
+
+def time_e4m3_sweep(nb, rt, torch, stream, dev, peak, reps=20):
+    calls, per_ctx = [], []
+    with torch.cuda.stream(stream):
+        for i, L in enumerate(CONTEXTS):
+            case = make_case(i, L, "e4m3")
+            plan = nb.mla_plan([L], H, 1, BS, dev, dtype="e4m3")
+            dc = rt.upload(case)
+            chunks = rt.chunks_to_device(plan.chunks)
+            part, lse = rt.alloc_partials(plan.num_chunks, 1, H)
+            ws = rt.alloc_decode_workspace(1, plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, H)
+            desc = rt.make_desc(dc, chunks, nb.MLA_KERNEL_TC, plan.cluster_ctas, stream, plan.clusters_per_chunk, ws,
+                                tables_ready=True, prefix_ready=True)
+            out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
+            ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
+            calls.append(dict(L=L, plan=plan, dc=dc, part=part, lse=lse, ind=ind, out=out, desc=desc))
+        for _ in range(3):
+            for c in calls:
+                rt.decode(c["dc"], c["part"], c["lse"], c["ind"], c["out"], desc=c["desc"])
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for c in calls:
+            rt.decode(c["dc"], c["part"], c["lse"], c["ind"], c["out"], desc=c["desc"])
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(stream):
+        g.replay()
+        e[0].record(stream)
+        for _ in range(reps):
+            g.replay()
+        e[1].record(stream)
+    stream.synchronize()
+    us = e[0].elapsed_time(e[1]) * 1e3 / (reps * len(calls))
+    nbytes = sum(sum(algorithmic_bytes(c["L"], c["plan"].num_chunks, 576)) for c in calls) / len(calls)
+    for c in calls:  # each context alone: a graph of four calls on its cache
+        g1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1, stream=stream):
+            for _ in range(4):
+                rt.decode(c["dc"], c["part"], c["lse"], c["ind"], c["out"], desc=c["desc"])
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        with torch.cuda.stream(stream):
+            g1.replay()
+            e1[0].record(stream)
+            g1.replay()
+            e1[1].record(stream)
+        stream.synchronize()
+        per_ctx.append({"ctx": c["L"], "us_per_call": round(e1[0].elapsed_time(e1[1]) * 1e3 / 4, 3),
+                        "partitions": c["plan"].num_chunks, "cluster": c["plan"].cluster_ctas,
+                        "clusters_per_partition": c["plan"].clusters_per_chunk})
+    achieved = nbytes / (us * 1e-6) / 1e9
+    return {"workload": E4M3_SWEEP, "us_per_call": round(us, 3), "bytes_per_token": 576, "cache_scale": 0.25,
+            "achieved_gbs": round(achieved, 1), "frac": round(achieved / peak, 4), "per_ctx": per_ctx,
+            "note": "timed like the headline step (a graph of the six layer calls through mla_decode, tables and "
+                    "first tiles read early); caches 354 MB in all, > L2"}
 
 
 def run_ours(args, rank, world):
@@ -961,6 +1026,7 @@ def run_ours(args, rank, world):
         if peaks and peaks.get("hbm_gbs") and peaks.get("bf16_tflops") else \
         {"hbm_gbs": 6800.0, "tensor_tflops": 1900.0, "source": "fallback"}
     verify = time_verify_windows(nb, rt, torch, stream, tpk) if not args.skip_extra else None
+    e4m3 = time_e4m3_sweep(nb, rt, torch, stream, dev, tpk["hbm_gbs"]) if not args.skip_extra else None
     grid = time_batch_grid(nb, rt, torch, stream) if not args.skip_extra else None
     st, code = nb.mla_check_device_errors(stream.cuda_stream)
     if st != nb.MLA_OK:
@@ -1006,6 +1072,7 @@ def run_ours(args, rank, world):
         "many_heads": many_heads,
         "verify_windows": verify,
         "batch_grid": grid,
+        "e4m3_caches": e4m3,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(kname, sum(CONTEXTS) / len(CONTEXTS)),

@@ -53,8 +53,6 @@
 // tile's pages measured slower over a sweep of caches larger than L2, so
 // there is none. The kernel is a programmatic dependent launch: its set-up overlaps the
 // end of the previous kernel in the stream.
-#include <cuda_fp8.h>
-
 #include "device_common.cuh"
 
 namespace mla {
@@ -123,21 +121,64 @@ struct Small {
 };
 static_assert(sizeof(Small) <= kSmallBytes, "small smem region");
 
-// eight E4M3 values (bytes in column order) -> eight fp16 values; exact (every E4M3 value, its
-// subnormals included, is an fp16 value)
-__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 v) {
-  uint32_t o[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t w = (k < 2) ? v.x : v.y;
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> (16 * (k & 1))), __NV_E4M3);
-    o[k] = static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// four E4M3 values (the bytes of w, lowest first) -> four fp16 values (two f16x2 words, lowest first);
+// exact: every E4M3 value, its subnormals included, is an fp16 value
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  // volatile: kept between its step's load and stores, so the widening holds few values at a time
+  asm volatile("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// Shared-memory loads and stores of the in-place widening, as volatile asm without a memory clobber:
+// kept in the order written (so a step's load can be issued ahead of earlier steps' stores, which the
+// compiler could not prove independent), and ordered against the barrier operations around them
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, const uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+}
+
+// 16 E4M3 bytes -> two 16-byte pieces of fp16 (bytes 0-7, bytes 8-15), stored at d0 and d1
+__device__ __forceinline__ void widen16(const uint4 v, uint32_t d0, uint32_t d1) {
+  uint4 a, b;
+  e4m3x4_to_f16x4(v.x, a.x, a.y);
+  e4m3x4_to_f16x4(v.y, a.z, a.w);
+  e4m3x4_to_f16x4(v.z, b.x, b.y);
+  e4m3x4_to_f16x4(v.w, b.z, b.w);
+  sts128(d0, a);
+  sts128(d1, b);
+}
+
+// One warp's steps of a widening part: ckv tokens t + 6 m (+ r2), m < n, staged at
+// stage_src + (t + 6 m) * 256; each step's load is issued three steps ahead of its conversion
+__device__ __forceinline__ void widen_ckv_steps(uint32_t slot, uint32_t stage_src, int t, int n, int r2, int cbl,
+                                                int kk) {
+  if (n <= 0) return;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  uint4 b0 = lds128(stage_src + t * 256), b1 = z, b2 = z;
+  if (n > 1) b1 = lds128(stage_src + (t + 6) * 256);
+  if (n > 2) b2 = lds128(stage_src + (t + 12) * 256);
+#pragma unroll 1
+  for (int m = 0; m < n; ++m, t += 6) {
+    const uint4 v = b0;
+    b0 = b1;
+    b1 = b2;
+    if (m + 3 < n) b2 = lds128(stage_src + (t + 18) * 256);
+    const int r = (t & 7) + r2;
+    const uint32_t row = slot + (t >> 3) * 4096 + cbl * 1024 + r * 128;
+    widen16(v, row + (((2 * kk) ^ r) << 4), row + (((2 * kk + 1) ^ r) << 4));
   }
-  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __device__ __forceinline__ uint32_t tmem_lane_base(int warp) { return static_cast<uint32_t>(32 * (warp & 3)) << 16; }
 
+// kFp8: E4M3 caches (byte loads, widened in the slot, cache scale on the output); one instance each
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_partial_tc128_kernel(const __grid_constant__ CUtensorMap tm_pages, const __grid_constant__ CUtensorMap tm_kpe_half,
                              const PartialParams p) {
@@ -228,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tile_issue = [&](int i, const int* pids, int mine, uint64_t pol) {
     const int s = i % kSlots;
     uint8_t* slot = smem + kOffTile + s * kTileSlot;
-    if (p.fp8) {
+    if (kFp8) {
       // E4M3 bytes, unswizzled, into the upper half of the slot: ckv rows of 256 bytes, then kpe rows of 32
       if (lane == 0) mbar_arrive_expect_tx(&sm->landed[s], static_cast<uint32_t>(mine * p.bs * (kHalfCols + kKpeCols)));
       __syncwarp();
@@ -259,28 +300,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // E4M3 caches: tile i's staged bytes become the 16-bit tile in place, in the layouts the 16-bit loads
   // give (ckv: 128-byte-swizzled [8 x 64] atoms, a 4 KB row group per 8 tokens; kpe: 64-byte
-  // swizzle), by the three producer warps, a staged row per warp and step, 8 bytes a lane. The 16-bit
-  // rows of ckv tokens 0-71 lie below the staging; those of tokens 8g..8g+7 (g >= 9) overwrite staged
-  // rows 16(g-9)..16(g-9)+15, and the 16-bit kpe staged rows 112-143. So, with the three warps
-  // meeting between the steps: tokens 0-71 | tokens 72-103 | tokens 104-119, then the staged rows
-  // 120-143 into registers | tokens 120-127 and the kpe from those registers. Every staged row is read
-  // before a step that overwrites it. Lane 0 of each warp then counts it on the slot's full barrier.
-  const int cb = lane >> 3, c8 = lane & 7;  // ckv: a lane's 64-column block and 8-column piece
-  auto ckv_dst = [&](uint8_t* slot, int t) -> uint8_t* {
-    return slot + (t >> 3) * kGroupBytes + cb * 1024 + (t & 7) * 128 + ((c8 ^ (t & 7)) << 4);
+  // swizzle), by the three producer warps. A warp step takes two staged rows (512 bytes, 16 a lane):
+  // ckv tokens t, t+1 (t even), or 16 kpe tokens. The 16-bit rows of ckv tokens 0-71 lie below the
+  // staging; those of tokens 8g..8g+7 (g >= 9) overwrite staged rows 16(g-9)..16(g-9)+15, and the
+  // 16-bit kpe staged rows 112-143. So, with the three warps meeting between the parts: tokens 0-71 |
+  // tokens 72-103, then staged rows 104-143 into registers | those rows (tokens 104-127, the kpe) from
+  // the registers. Every staged row is read before a part that overwrites it. Lane 0 of each warp
+  // then counts it on the slot's full barrier.
+  // ckv lanes: quarter q and half r2 of it take token t + r2, column block q ^ r2, 16 columns 16 (lane
+  // & 3) .. +15 (8-column pieces 2 (lane & 3), +1): the 8 lanes of a quarter read 8 different 16-byte
+  // bank groups and, the two halves writing rows of opposite parity, write 8 different ones
+  const int r2 = (lane >> 2) & 1, cbl = (lane >> 3) ^ r2, kk = lane & 3;
+  const int src_ckv = r2 * kHalfCols + cbl * 64 + kk * 16;  // in the two staged rows of a step
+  // kpe lanes: token 16 j + lane / 2 of step j, fp8 columns 16 (lane & 1) .. +15
+  const int tk_l = lane >> 1, hk = lane & 1;
+  auto ckv_store = [&](uint32_t slot, int t, const uint4 v) {  // ckv tokens t + r2 (t even)
+    const int r = (t & 7) + r2;
+    const uint32_t row = slot + (t >> 3) * kGroupBytes + cbl * 1024 + r * 128;
+    widen16(v, row + (((2 * kk) ^ r) << 4), row + (((2 * kk + 1) ^ r) << 4));
   };
-  auto widen_rows = [&](uint8_t* slot, int t0, int t1, int first) {  // ckv tokens [t0, t1)
-#pragma unroll 4
-    for (int t = t0 + first; t < t1; t += kPageWarps)
-      *reinterpret_cast<uint4*>(ckv_dst(slot, t)) =
-          e4m3x8_to_f16x8(*reinterpret_cast<const uint2*>(slot + kStage + t * kHalfCols + lane * 8));
+  auto kpe_store = [&](uint32_t slot, int j, const uint4 v) {  // kpe step j: tokens 16 j .. 16 j + 15
+    const int tk = 16 * j + tk_l;
+    const uint32_t row = slot + kCkvBytes + tk * (kKpeCols * 2);
+    widen16(v, row + ((((2 * hk) ^ (tk >> 1)) & 3) << 4), row + ((((2 * hk + 1) ^ (tk >> 1)) & 3) << 4));
   };
-  auto meet = [&](int phase) -> bool {  // the three producer warps; three phases per tile
+  // the three producer warps meet (two phases per tile); the wait spins rather than suspends, the
+  // others being at most a few hundred cycles away
+  auto meet = [&](int phase) -> bool {
     __syncwarp();
     int ok = 1;
     if (lane == 0) {
       mbar_arrive(&sm->conv);
-      ok = mbar_wait(&sm->conv, phase & 1, p.timeout_ns);
+      if (!mbar_test(&sm->conv, phase & 1)) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_test(&sm->conv, phase & 1)) {
+          if (globaltimer_ns() - t0 > p.timeout_ns) {
+            flag_error(MLA_DEVERR_TIMEOUT);
+            ok = 0;
+            break;
+          }
+        }
+      }
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     __syncwarp();
@@ -288,29 +348,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto convert = [&](int i) -> bool {
     const int s = i % kSlots;
-    uint8_t* slot = smem + kOffTile + s * kTileSlot;
+    const uint32_t slot = smem_u32(smem + kOffTile + s * kTileSlot);
+    const uint32_t stage_src = slot + kStage + src_ckv;
     if (!__all_sync(0xffffffffu, mbar_wait(&sm->landed[s], (i / kSlots) & 1, p.timeout_ns))) return false;
-    widen_rows(slot, 0, 72, k0);
-    if (!meet(3 * i)) return false;
-    widen_rows(slot, 72, 104, k0);
-    if (!meet(3 * i + 1)) return false;
-    widen_rows(slot, 104, 120, (k0 + 1) % kPageWarps);  // rotated: 48 rows per warp over the tile
-    uint2 held[8];  // staged rows 120 + k0 + 3m: ckv tokens 120-127, then the kpe rows
+    widen_ckv_steps(slot, stage_src, 2 * k0, 12, r2, cbl, kk);  // tokens 0-71: 36 steps, 12 a warp
+    if (!meet(2 * i)) return false;
+    widen_ckv_steps(slot, stage_src, 72 + 2 * k0, k0 == 0 ? 6 : 5, r2, cbl, kk);  // 72-103: 6, 5, 5
+    // staged rows 104-143 in 20 steps (7, 7, 6): steps 0-11 ckv tokens 104-127, steps 12-19 the kpe
+    constexpr int kHeld = 7;
+    uint4 held[kHeld];
 #pragma unroll
-    for (int m = 0; m < 8; ++m)
-      held[m] = *reinterpret_cast<const uint2*>(slot + kStage + (120 + k0 + kPageWarps * m) * kHalfCols + lane * 8);
-    if (!meet(3 * i + 2)) return false;
+    for (int m = 0; m < kHeld; ++m) {
+      const int j = k0 + kPageWarps * m;
+      if (j < 20) held[m] = lds128(slot + kStage + (104 + 2 * j) * kHalfCols + (j < 12 ? src_ckv : lane * 16));
+    }
+    if (!meet(2 * i + 1)) return false;
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const int r = k0 + kPageWarps * m;
-      uint8_t* dst;
-      if (r < 8) {
-        dst = ckv_dst(slot, 120 + r);
-      } else {  // kpe tokens 8(r-8) .. 8(r-8)+7: 32 bytes each, four pieces
-        const int t = (r - 8) * 8 + (lane >> 2), c = lane & 3;
-        dst = slot + kCkvBytes + t * (kKpeCols * 2) + ((c ^ (t >> 1)) & 3) * 16;
-      }
-      *reinterpret_cast<uint4*>(dst) = e4m3x8_to_f16x8(held[m]);
+    for (int m = 0; m < kHeld; ++m) {
+      const int j = k0 + kPageWarps * m;
+      if (j < 12)
+        ckv_store(slot, 104 + 2 * j, held[m]);
+      else if (j < 20)
+        kpe_store(slot, j - 12, held[m]);
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -355,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp > kMmaWarp) {
     // ------------------------------------------------------------------ producers
     const uint64_t pol = l2_policy_evict_first();
-    if (p.fp8) {
+    if (kFp8) {
       // Issue and widening interleave: the next tile's loads as soon as its slot is free, else the
       // widening of the oldest landed tile; nothing to do for longer than the wait limit (or an abort
       // elsewhere) ends it
@@ -405,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    for (int i = p.fp8 ? ntiles : issued + 1; i < ntiles; ++i) {
+    for (int i = kFp8 ? ntiles : issued + 1; i < ntiles; ++i) {
       const int s = i % kSlots;
       // the pages of tile i first: their block-table reads overlap the wait for the slot
       int pids[kMaxPagesPerWarp];
@@ -425,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // slot) land before shared memory is released
     if (lane == 0 && *abort_flag)
       for (int t = max(0, issued - (kSlots - 1)); t <= issued; ++t)
-        mbar_wait(p.fp8 ? &sm->landed[t % kSlots] : &sm->full[t % kSlots], (t / kSlots) & 1, kDrainTimeoutNs);
+        mbar_wait(kFp8 ? &sm->landed[t % kSlots] : &sm->full[t % kSlots], (t / kSlots) & 1, kDrainTimeoutNs);
     cluster_wait_acquire();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
@@ -825,7 +884,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* const eml = p.ws_lse + (entry * 2 + half) * rows_total * 2;               // [rows][m, l]
     if (warp < kSoftmaxWarps) {
       const int q4 = warp & 3, h = warp >> 2;
-      const float cs = p.cache_scale;  // an E4M3 cache's scale (1 for 16-bit caches): exact, a power of two
+      const float cs = p.cache_scale;  // an E4M3 cache's scale: exact, a power of two
       if (have) tc_fence_after();
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
@@ -833,8 +892,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (have) {
           tmem_ld8(tmem + tmem_lane_base(q4) + 2 * kNR + blk * kNR + kRH * h, v);
           tmem_wait_ld();
+          if (kFp8)
 #pragma unroll
-          for (int k = 0; k < kRH; ++k) v[k] *= cs;
+            for (int k = 0; k < kRH; ++k) v[k] *= cs;
         } else {
 #pragma unroll
           for (int k = 0; k < kRH; ++k) v[k] = 0.f;
@@ -968,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         const int d = blk * 128 + q4 * 32 + lane;
 #pragma unroll
-        for (int k = 0; k < kRH; ++k) ostage[(kRH * h + k) * kHalfCols + d] = v[k] * p.cache_scale;
+        for (int k = 0; k < kRH; ++k) ostage[(kRH * h + k) * kHalfCols + d] = kFp8 ? v[k] * p.cache_scale : v[k];
       }
     } else {
       for (int idx = tid; idx < kNR * kHalfCols; idx += kSoftmaxThreads) ostage[idx] = 0.f;
@@ -1071,9 +1131,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <bool kFp8>
 cudaError_t prepare(int cluster) {
   static bool smem_set = false, np_set = false;
-  const void* fn = reinterpret_cast<const void*>(&mla_partial_tc128_kernel);
+  const void* fn = reinterpret_cast<const void*>(&mla_partial_tc128_kernel<kFp8>);
   cudaError_t e = cudaSuccess;
   if (!smem_set) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
@@ -1096,7 +1157,7 @@ bool tc128_supports(int total_rows, bool bf16, int cluster) {
 
 cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe_half, const PartialParams& p,
                                  int num_chunks, int cluster, cudaStream_t stream) {
-  cudaError_t e = prepare(cluster);
+  cudaError_t e = p.fp8 ? prepare<true>(cluster) : prepare<false>(cluster);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster, num_chunks * (p.subs > 1 ? p.subs : 1), 1);
@@ -1112,11 +1173,13 @@ cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap&
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, mla_partial_tc128_kernel, tm_pages, tm_kpe_half, p);
+  return p.fp8 ? cudaLaunchKernelEx(&cfg, mla_partial_tc128_kernel<true>, tm_pages, tm_kpe_half, p)
+               : cudaLaunchKernelEx(&cfg, mla_partial_tc128_kernel<false>, tm_pages, tm_kpe_half, p);
 }
 
 int tc128_max_active_clusters(int cluster) {
-  if (prepare(cluster) != cudaSuccess) {
+  // both instances take the same threads, shared memory and (at most) registers
+  if (prepare<false>(cluster) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1132,7 +1195,7 @@ int tc128_max_active_clusters(int cluster) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(&mla_partial_tc128_kernel), &cfg) !=
+  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(&mla_partial_tc128_kernel<false>), &cfg) !=
       cudaSuccess) {
     cudaGetLastError();
     return 0;
