@@ -69,7 +69,7 @@ typedef enum {
 
 /* MLA_E4M3: 8-bit E4M3 latent caches (sign, 4 exponent bits with bias 7, 3
  * mantissa bits; exponent field 0 subnormal; S.1111.111 NaN, no infinities)
- * read with a power-of-two cache scale, beside fp16 queries. */
+ * read with a scalar cache scale, beside fp16 queries. */
 typedef enum { MLA_F16 = 0, MLA_BF16 = 1, MLA_F32 = 2, MLA_E4M3 = 3 } mla_dtype_t;
 
 /* Which partial-decode kernel runs. AUTO picks the tensor-core kernel. */
@@ -247,12 +247,14 @@ typedef struct {
                                  values, or 1 with tables_ready = 0:
                                  INVALID_ARG.                                  */
   float cache_scale;          /* MLA_E4M3 caches: the value of a cache byte x is
-                                 e4m3(x) * cache_scale, a power of two in
-                                 [2^-24, 2^24] (so the scores and the output
-                                 take it without rounding; the scalar folded
-                                 in as mlxcel PR #995, *What changed*, folds
-                                 a global scale). Other dtypes: ignored.
-                                 Anything else with E4M3: INVALID_ARG.         */
+                                 e4m3(x) * cache_scale, cache_scale in
+                                 [2^-24, 2^24] (the scalar folded in as mlxcel
+                                 PR #995, *What changed*, folds a global
+                                 scale). It multiplies the score scale and the
+                                 output: one fp32 rounding each, none for a
+                                 power of two. Other dtypes: ignored. Anything
+                                 else (0, negative, NaN, out of range) with
+                                 E4M3: INVALID_ARG.                            */
 } mla_decode_desc_t;
 
 /*

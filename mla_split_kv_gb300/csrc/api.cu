@@ -208,12 +208,11 @@ mla_status_t check_decode(const void* q_absorbed, const void* q_pe, const void* 
   if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64) return MLA_ERR_UNSUPPORTED;
   if (d->dtype != MLA_F16 && d->dtype != MLA_BF16 && d->dtype != MLA_E4M3) return MLA_ERR_UNSUPPORTED;
   if (d->dtype == MLA_E4M3) {
-    // E4M3 caches: the paired 16-row kernel only, and a power-of-two scale
+    // E4M3 caches: the paired 16-row kernel only, and a scale in [2^-24, 2^24]
     if (d->kernel == MLA_KERNEL_SIMT || d->num_heads * d->q_len > 16 || d->cluster_ctas == 1)
       return MLA_ERR_UNSUPPORTED;
-    int e = 0;
-    const float f = std::frexp(d->cache_scale, &e);
-    if (!std::isfinite(d->cache_scale) || f != 0.5f || e < -23 || e > 25) return MLA_ERR_INVALID_ARG;
+    const float cs = d->cache_scale;
+    if (!(cs >= 0x1p-24f && cs <= 0x1p24f)) return MLA_ERR_INVALID_ARG;  // also NaN
   }
   if (d->causal != 0 && d->causal != 1) return MLA_ERR_INVALID_ARG;
   if (d->tables_ready != 0 && d->tables_ready != 1) return MLA_ERR_INVALID_ARG;
@@ -324,7 +323,8 @@ mla_status_t launch_decode(const void* q_absorbed, const void* q_pe, const void*
   p.chunks = d->chunks;
   p.partials = partials;
   p.lse = lse;
-  // an E4M3 cache's scale (a power of two) multiplies every score: folded into the score scale
+  // an E4M3 cache's scale multiplies every score: folded into the score scale (one rounding; none
+  // for a power of two)
   p.scale_log2 = scale * 1.4426950408889634f * (fp8 ? d->cache_scale : 1.0f);
   p.fp8 = fp8 ? 1 : 0;
   p.cache_scale = fp8 ? d->cache_scale : 1.0f;

@@ -818,30 +818,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&sm->ppfull[s]);
       return true;
     };
-    // Tiles in pairs, as the MMA warp issues them (S(i) S(i+1) PV(i) PV(i+1)): when tile i+1's scores
-    // are already there, they are loaded (and, if the peer's buffer is already free, sent) before
-    // tile i is finished, so the exchange of one overlaps the work on the other; otherwise tile i is
-    // finished first, so PV(i) is not held back. Each warp decides for itself, so no warp may wait
-    // on the peer between the two: the peer's warps that would release it may be held at their own
-    // barrier in B(i) by their warps that are waiting on this CTA the same way.
-    for (int i0 = 0; i0 < ntiles && ok_all; i0 += 2) {
-      const bool two = i0 + 1 < ntiles;
-      float x0[kRH], x1[kRH];
-      const bool sent0 = prep(i0, x0) && push(i0, x0);
-      bool prepped1 = false, sent1 = false;
-      if (two && sent0) {
-        int ready = 0;
-        if (lane == 0) ready = mbar_test(&sm->sfull[(i0 + 1) & 1], ((i0 + 1) >> 1) & 1) ? 1 : 0;
-        if (__shfl_sync(0xffffffffu, ready, 0) != 0) {
-          prepped1 = prep(i0 + 1, x1);
-          if (prepped1 && peer_free(i0 + 1)) sent1 = push(i0 + 1, x1);
+    // Tile by tile, one ahead: when tile i+1's scores are already there, they are loaded (and, if the
+    // peer's buffer is already free, sent) before tile i is finished, so the exchange of one overlaps
+    // the work on the other; otherwise tile i is finished first, so PV(i) is not held back. Each warp
+    // decides for itself, so no warp may wait on the peer between the two: the peer's warps that
+    // would release it may be held at their own barrier in B(i) by their warps that are waiting on
+    // this CTA the same way.
+    {
+      float xc[kRH], xn[kRH];  // tile i's scores; tile i+1's, when loaded early
+      bool c_prepped = false, c_sent = false;
+      for (int i = 0; i < ntiles && ok_all; ++i) {
+        if (!c_prepped) c_prepped = prep(i, xc);
+        if (c_prepped && !c_sent) c_sent = push(i, xc);
+        bool n_prepped = false, n_sent = false;
+        if (c_sent && i + 1 < ntiles) {
+          int ready = 0;
+          if (lane == 0) ready = mbar_test(&sm->sfull[(i + 1) & 1], ((i + 1) >> 1) & 1) ? 1 : 0;
+          if (__shfl_sync(0xffffffffu, ready, 0) != 0) {
+            n_prepped = prep(i + 1, xn);
+            if (n_prepped && peer_free(i + 1)) n_sent = push(i + 1, xn);
+          }
         }
-      }
-      ok_all = finish(i0, x0, sent0);
-      if (ok_all && two) {
-        if (!prepped1) prepped1 = sent0 && prep(i0 + 1, x1);
-        if (prepped1 && !sent1) sent1 = push(i0 + 1, x1);
-        ok_all = finish(i0 + 1, x1, sent1);
+        ok_all = finish(i, xc, c_sent);
+#pragma unroll
+        for (int k = 0; k < kRH; ++k) xc[k] = xn[k];
+        c_prepped = n_prepped;
+        c_sent = n_sent;
       }
     }
     if (!ok_all && lane == 0) *abort_flag = 1;
@@ -884,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* const eml = p.ws_lse + (entry * 2 + half) * rows_total * 2;               // [rows][m, l]
     if (warp < kSoftmaxWarps) {
       const int q4 = warp & 3, h = warp >> 2;
-      const float cs = p.cache_scale;  // an E4M3 cache's scale: exact, a power of two
+      const float cs = p.cache_scale;  // an E4M3 cache's scale (one rounding; exact for a power of two)
       if (have) tc_fence_after();
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {

@@ -12,7 +12,7 @@ Conventions (shared by every consumer):
   rounded once, to nearest-even, into the tagged type.
 * dtype ``"e4m3"``: the caches are ``numpy.uint8`` 8-bit E4M3 patterns drawn
   directly as bits (random sign, exponent field, mantissa; no NaN pattern),
-  read with a power-of-two ``cache_scale``; the queries are fp16.
+  read with a scalar ``cache_scale``; the queries are fp16.
 * ``ckv``  : ``[num_blocks, block_size, 512]`` -- compressed latent, one row per
   cached token (the key *and* the value of absorbed attention).
 * ``kpe``  : ``[num_blocks, block_size, 64]`` -- rotary key part.

@@ -1,14 +1,15 @@
 """GPU parity for 8-bit E4M3 latent caches on the paired 16-row kernel.
 
 The oracle reads each cache byte as its exact E4M3 value times the cache
-scale (a power of two). The kernel loads the bytes, widens them to fp16 in
-shared memory (exact: every E4M3 value is an fp16 value) and folds the scale
-into the score scale and the output. From the widening on, the arithmetic is
-the fp16 path's, so the tolerance is the one stated for 16-bit inputs with
-fp32 accumulation: max-abs 2e-3 and rel-L2 1e-3 on fp32 results, max-abs 2e-3
-on every finite log2 LSE. And since scaling by a power of two commutes with
-every rounding, the same bytes widened on the host into an fp16 cache holding
-value * scale must give the fp16 path's results bit for bit.
+scale. The kernel loads the bytes, widens them to fp16 in shared memory
+(exact: every E4M3 value is an fp16 value) and folds the scale into the score
+scale and the output. From the widening on, the arithmetic is the fp16 path's
+(plus one rounding of each folded product), so the tolerance is the one stated
+for 16-bit inputs with fp32 accumulation: max-abs 2e-3 and rel-L2 1e-3 on fp32
+results, max-abs 2e-3 on every finite log2 LSE. And since scaling by a power
+of two commutes with every rounding, for such a scale the same bytes widened
+on the host into an fp16 cache holding value * scale must give the fp16 path's
+results bit for bit.
 """
 import dataclasses
 
@@ -84,6 +85,7 @@ def uniform(case, P, C, dc=None, subs=1):
     ([5000, 300, 0], 64, 3, 4, 2.0 ** -6),        # an empty request
     ([20000], 32, 4, 8, 0.125),
     ([777, 4133], 16, 2, 16, 0.25),
+    ([3000, 129], 32, 2, 2, 0.3),                 # a scale that is not a power of two
 ])
 def test_e4m3_partials_and_merge_against_the_oracle(lens, bs, P, C, cs):
     case = gen.make_decode_case(61, lens, num_heads=16, block_size=bs, dtype="e4m3", cache_scale=cs)
