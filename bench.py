@@ -14,7 +14,9 @@ Printed: one JSON line. `value` = mean microseconds per layer call over the
 sweep (device time, inputs resident, each step replayed from one CUDA graph);
 `e2e` = the same through mla_decode with host buffers (queries, block tables
 and plan of the six calls copied in with one copy from one pinned buffer, the
-six outputs copied out with one copy, every step); `roofline` = the layer
+six outputs copied out with one copy, every step; the step replayed from a
+CUDA graph captured through those calls, host wall clock with a synchronize
+per step; `eager_us` launches them one by one); `roofline` = the layer
 call's algorithmic HBM bytes / its CUDA-event time in the timed graph against
 the measured copy bandwidth; `cpu_baseline` = the f64 oracle on the host
 cores. Outside the timed region: `without_prefix_ready_us` (every cache read after the preceding kernel has
@@ -56,7 +58,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--kernel", default="tc", choices=["tc", "simt"])
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-ctx", type=int, default=0,
                     help="profiling case: only --launches plain layer calls at this context (of the sweep), then exit")
@@ -1003,7 +1005,7 @@ def run_ours(args, rank, world):
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         e2e_step()
-    e2e_s = time.perf_counter() - t0
+    e2e_eager_s = time.perf_counter() - t0
     # the results of the last step are the graph's results (same inputs)
     for j, c in enumerate(calls):
         if not torch.equal(hout[j], c["out"].cpu()):
@@ -1016,6 +1018,30 @@ def run_ours(args, rank, world):
         print(f"WARNING: path counters {ctr} disagree with {expect} layer calls on the {args.kernel} kernel",
               file=sys.stderr)
     launches_per_call = (ctr[ctr_key] + ctr[nb.CTR_MERGE]) / max(expect, 1)
+    # the same step captured once through the same calls into a CUDA graph (the upload from the pinned
+    # buffer, the six layer calls, the download), then replayed and waited for every step: how a decode
+    # loop would run it; the copies still move every step's inputs and outputs
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_e2e, stream=stream):
+        dbuf.copy_(hbuf, non_blocking=True)
+        for e in e2e_calls:
+            rt.decode(e["dc"], e["part"], e["lse"], e["ind"], e["out"], desc=e["desc"])
+        hout.copy_(dout, non_blocking=True)
+    # (outputs cleared on both sides first, so the check below sees what the replays computed)
+    with torch.cuda.stream(stream):
+        dout.zero_()
+        hout.zero_()
+        for _ in range(3):
+            g_e2e.replay()
+            stream.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            g_e2e.replay()
+            stream.synchronize()
+        e2e_s = time.perf_counter() - t0
+    for j, c in enumerate(calls):
+        if not torch.equal(hout[j], c["out"].cpu()):
+            raise RuntimeError(f"graphed end-to-end output of call {j} differs from the timed graph's")
 
     many_heads = time_many_heads(nb, rt, torch, stream)
     st, code = nb.mla_check_device_errors(stream.cuda_stream)
@@ -1082,7 +1108,11 @@ def run_ours(args, rank, world):
                      "time": "the timed step graph: every launch of both kernels and the gaps between them"},
         "partial_kernel_alone": partial_only,
         "e2e": {"value": round(e2e_s * 1e6 / (e2e_steps * len(calls)), 3), "unit": "us/layer-call",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "eager_us": round(e2e_eager_s * 1e6 / (e2e_steps * len(calls)), 3),
+                "how": "host wall clock per step: the pinned upload, the six mla_decode calls and the download, "
+                       "replayed from one CUDA graph captured through those calls, then a stream synchronize; "
+                       "eager_us: the same calls launched one by one every step"},
         # the step graphs (launches_per_call each layer call) and the partial-only graphs (one each)
         "gpu_launches": int(round((launches_per_call + 1) * n_calls * reps)),
         "timed_repeats": reps,
