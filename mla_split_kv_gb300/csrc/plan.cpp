@@ -110,13 +110,17 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
     }
 
   Candidate best;
+  // 16 fp16 rows (or E4M3 caches) run on the paired kernel whenever the device has CTA pairs: a
+  // partition's tiles stream through three slots on two SMs, several times the 64-token kernel's
+  // rate, so clusters of one are not candidates then (for a batch they would tie on busy CTAs)
+  const bool paired_ok = mla::tc128_supports(rows, plan->dtype == MLA_BF16, 2) && dev->max_clusters[1] > 0;
   // one long request on the paired kernel: candidates compared by the time model
-  const bool paired_single = (B == 1 && n_split == 1 && mla::tc128_supports(rows, plan->dtype == MLA_BF16, 2));
+  const bool paired_single = (B == 1 && n_split == 1 && paired_ok);
   for (int k = 0; k < 5; ++k) {
     const int C = 1 << k;
     const int64_t slots = dev->max_clusters[k];
     if (slots <= 0) continue;
-    if (paired_single && C == 1) continue;  // the paired kernel needs a pair of CTAs
+    if (paired_ok && C == 1) continue;  // the paired kernel needs a pair of CTAs
     if (plan->dtype == MLA_E4M3 && C == 1) continue;  // so do E4M3 caches, always
     if (many_rows && C != 2) continue;      // the 128-row kernel runs on CTA pairs
     Candidate cand;

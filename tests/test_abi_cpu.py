@@ -140,6 +140,21 @@ def test_plan_for_e4m3_caches_keeps_pairs(lib, lens):
             (pf.chunks, pf.o_indptr, pf.cluster_ctas, pf.clusters_per_chunk)
 
 
+@pytest.mark.parametrize("lens", [[8192] * 8, [8192] * 32, [1000] * 8, [40000, 3000, 0, 129]])
+def test_batch_plans_of_sixteen_fp16_rows_use_cta_pairs(lib, lens):
+    # a batch at H=16 fp16 runs on the paired kernel (clusters of 2 or more) whenever the device has pairs
+    plan = nb.mla_plan(lens, 16, 1, 32, fake_gb300())
+    assert plan.cluster_ctas >= 2
+    check_plan_tiles(plan, lens, 32)
+    assert plan.num_chunks * plan.clusters_per_chunk <= 76  # one wave of the device's 76 pairs
+    # without pairs on the device: one CTA per partition
+    plan1 = nb.mla_plan(lens, 16, 1, 32, fake_device(152, [152, 0, 0, 0, 0]))
+    assert plan1.cluster_ctas == 1
+    # bf16 keeps the 64-token kernel's choice (the paired kernel is fp16 only)
+    pb = nb.mla_plan(lens, 16, 1, 32, fake_gb300(), dtype="bf16")
+    assert pb.clusters_per_chunk == 1
+
+
 def test_workspace_bytes(lib):
     assert nb.mla_workspace_bytes(8, 1, 4, 1, 16) == 0
     assert nb.mla_workspace_bytes(8, 4, 1, 1, 16) == 0
