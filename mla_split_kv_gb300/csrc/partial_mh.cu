@@ -137,7 +137,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm->xfull, 1);   // local expect_tx arrival + the peer's st.async bytes
     mbar_init(&sm->xempty, kSoftmaxWarps);  // one remote arrival per peer softmax warp
     mbar_init(&sm->drain, 1);
-    mbar_arrive_expect_tx(&sm->xfull, kXBytes);  // tile 0
     sm->abort_flag = 0;
     sm->peer_abort = 0;
     fence_mbar_init();
@@ -156,6 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // and the later reads are served by L2)
   const CtaWork w = cta_work(p, kRows, kT, 0, 1, -1, static_cast<int32_t>(blockIdx.x >> 1));
   const int ntiles = (w.sub1 - w.sub0 + kT - 1) / kT;
+  // only the group's real rows exchange their partial scores (a group of 64 rows, H=64, sends half);
+  // the peer's bytes of tile 0 may land before this expectation: its arrival completes the phase
+  const uint32_t xbytes = static_cast<uint32_t>(min(w.nrows, kRows)) * kT * 4;
+  if (tid == 0) mbar_arrive_expect_tx(&sm->xfull, xbytes);  // tile 0
 
   if (warp > kMmaWarp) {
     // ------------------------------------------------------------------ producers
@@ -458,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i >= 1) ok = mbar_wait_cluster(&sm->xempty, (i - 1) & 1, tmo);
         }
         ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
+        if (ok && r < w.nrows) {
 #pragma unroll
           for (int c = 0; c < kHalfT / 4; ++c)
             dsmem_st_async_f32x4(peer_xrow + (((8 * hf + c) ^ xsw) << 4),
@@ -484,7 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kHalfT / 4; ++c) {
           const float4 o = make_float4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]);
-          const float4 y = xrow[(8 * hf + c) ^ xsw];
+          // (a padding row past the group's rows takes no peer part: its scores are never used)
+          const float4 y = (r < w.nrows) ? xrow[(8 * hf + c) ^ xsw] : make_float4(0.f, 0.f, 0.f, 0.f);
           // rank-0 part + rank-1 part, the same sum in both CTAs
           x[4 * c] = half ? (y.x + o.x) : (o.x + y.x);
           x[4 * c + 1] = half ? (y.y + o.y) : (o.y + y.y);
@@ -495,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           // expect the peer's next tile before letting it send, then free the buffer (the values are
           // consumed above; a plain signal)
-          if (tid == 0) mbar_arrive_expect_tx(&sm->xfull, kXBytes);
+          if (tid == 0) mbar_arrive_expect_tx(&sm->xfull, xbytes);
           mbar_remote_arrive_relaxed(peer_xempty);
         }
         const int nvis = min(kT, tlim - tok0) - kHalfT * hf;  // tokens of this half the row can see
