@@ -167,8 +167,9 @@ def make_many_heads_case():
     return gen.make_decode_case(MH_SEED, lens, num_heads=MH_H, block_size=MH_BS, dtype="bf16", latent_std=0.5)
 
 
-def many_heads_call(nb, rt, torch, stream=None):
-    """Upload the many-head case, plan it, and return a closure doing one layer call (partial + merge kernels)."""
+def many_heads_call(nb, rt, torch, stream=None, exchange=0):
+    """Upload the many-head case, plan it, and return a closure doing one layer call (partial + merge kernels);
+    `exchange`: the 128-row kernel's partial-score exchange (0: fp32, the default; 1: fp16)."""
     case = make_many_heads_case()
     dev = nb.mla_device_query()
     plan = nb.mla_plan(case.context_lens.tolist(), MH_H, 1, MH_BS, dev, max_partitions=64, dtype="bf16")
@@ -177,7 +178,7 @@ def many_heads_call(nb, rt, torch, stream=None):
     part, lse = rt.alloc_partials(plan.num_chunks, 1, MH_H)
     ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
     out = torch.empty((MH_B, 1, MH_H, 512), dtype=torch.bfloat16, device="cuda")
-    desc = rt.make_desc(dc, chunks_dev, nb.MLA_KERNEL_TC, plan.cluster_ctas, stream)
+    desc = rt.make_desc(dc, chunks_dev, nb.MLA_KERNEL_TC, plan.cluster_ctas, stream, score_exchange=exchange)
 
     def call():  # mla_decode: the 128-row kernel, then the merge kernel
         rt.decode(dc, part, lse, ind, out, desc=desc)
@@ -633,29 +634,37 @@ def run_profile_many_heads(args):
 
 
 def time_many_heads(nb, rt, torch, stream, reps=20):
-    """Device time of one many-head layer call (graph of `reps` calls, CUDA events), and its flop rate."""
-    with torch.cuda.stream(stream):
-        call, plan, tokens = many_heads_call(nb, rt, torch, stream)
-        for _ in range(3):
-            call()
-    stream.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for _ in range(reps):
-            call()
-    e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    with torch.cuda.stream(stream):
-        g.replay()
-        e[0].record(stream)
-        g.replay()
-        e[1].record(stream)
-    stream.synchronize()
-    us = e[0].elapsed_time(e[1]) * 1e3 / reps
+    """Device time of one many-head layer call (graph of `reps` calls, CUDA events), and its flop rate; beside
+    it the same call with the partial scores exchanged as fp16 (an opt-in of the ABI)."""
+    def timed(exchange):
+        with torch.cuda.stream(stream):
+            call, plan, tokens = many_heads_call(nb, rt, torch, stream, exchange)
+            for _ in range(3):
+                call()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                call()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        with torch.cuda.stream(stream):
+            g.replay()
+            e[0].record(stream)
+            g.replay()
+            e[1].record(stream)
+        stream.synchronize()
+        return e[0].elapsed_time(e[1]) * 1e3 / reps, plan, tokens
+
+    us, plan, tokens = timed(0)
+    us16, _, _ = timed(1)
     flops = tokens * MH_H * 2 * (576 + 512)
     return {"workload": MANY_HEADS, "us_per_call": round(us, 3), "partitions": plan.num_chunks,
             "cluster": plan.cluster_ctas, "tokens": tokens, "tflops": round(flops / (us * 1e-6) / 1e12, 1),
             "hbm_gbs": round(tokens * LATENT_BYTES_PER_TOKEN / (us * 1e-6) / 1e9, 1),
-            "note": "a parity workload timed beside the headline one; repeats of one cache (323 MB, > L2)"}
+            "fp16_exchange_us": round(us16, 3),
+            "fp16_exchange_tflops": round(flops / (us16 * 1e-6) / 1e12, 1),
+            "note": "a parity workload timed beside the headline one; repeats of one cache (323 MB, > L2); "
+                    "fp16_exchange: score_exchange = MLA_SCORE_EXCHANGE_F16"}
 
 
 # the headline sweep with 8-bit E4M3 caches (576 bytes a token, power-of-two cache scale 1/4) beside fp16

@@ -219,6 +219,8 @@ mla_status_t check_decode(const void* q_absorbed, const void* q_pe, const void* 
   if (d->decode_merge != MLA_DECODE_MERGE_ENTRIES && d->decode_merge != MLA_DECODE_MERGE_TICKETS)
     return MLA_ERR_INVALID_ARG;
   if (d->prefix_ready != 0 && d->prefix_ready != 1) return MLA_ERR_INVALID_ARG;
+  if (d->score_exchange != MLA_SCORE_EXCHANGE_F32 && d->score_exchange != MLA_SCORE_EXCHANGE_F16)
+    return MLA_ERR_INVALID_ARG;
   if (d->prefix_ready == 1 && d->tables_ready != 1) return MLA_ERR_INVALID_ARG;
   if (d->kernel < MLA_KERNEL_AUTO || d->kernel > MLA_KERNEL_TC) return MLA_ERR_INVALID_ARG;
   const int32_t C0 = d->cluster_ctas;
@@ -338,6 +340,7 @@ mla_status_t launch_decode(const void* q_absorbed, const void* q_pe, const void*
   p.causal = d->causal;
   p.tables_ready = d->tables_ready;
   p.prefix_ready = d->prefix_ready;
+  p.xchg16 = (d->score_exchange == MLA_SCORE_EXCHANGE_F16) ? 1 : 0;
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
 
   p.subs = subs;

@@ -39,6 +39,7 @@ struct PartialParams {
   int32_t fp8;                 // E4M3 caches (the paired kernel): loaded as bytes, converted to fp16 in the slot
   float cache_scale;           // E4M3: the value of byte x is e4m3(x) * cache_scale (folded into scale_log2 and O)
   int32_t prefix_ready;        // cache rows before each request's window may be read before the dependency wait
+  int32_t xchg16;              // the 128-row kernel: partial scores cross the pair as fp16
   uint64_t timeout_ns;
   // a chunk spread over `subs` clusters (the paired 16-row kernel): grid.y = chunks * subs.
   // One entry per CTA pair of a chunk (subs * cluster / 2 of them): its unnormalized O^T in

@@ -106,7 +106,8 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 }
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
-template <bool BF16>
+// X16: the pair's partial scores cross as fp16 (an instance each, no run-time branch in the loop)
+template <bool BF16, bool X16>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_partial_mh_kernel(const __grid_constant__ CUtensorMap tm_pages, const __grid_constant__ CUtensorMap tm_kpe_half,
                           const PartialParams p) {
@@ -155,9 +156,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // and the later reads are served by L2)
   const CtaWork w = cta_work(p, kRows, kT, 0, 1, -1, static_cast<int32_t>(blockIdx.x >> 1));
   const int ntiles = (w.sub1 - w.sub0 + kT - 1) / kT;
-  // only the group's real rows exchange their partial scores (a group of 64 rows, H=64, sends half);
-  // the peer's bytes of tile 0 may land before this expectation: its arrival completes the phase
-  const uint32_t xbytes = static_cast<uint32_t>(min(w.nrows, kRows)) * kT * 4;
+  // only the group's real rows exchange their partial scores (a group of 64 rows, H=64, sends half),
+  // 4 bytes a score, or 2 with the fp16 exchange; the peer's bytes of tile 0 may land before this
+  // expectation: its arrival completes the phase
+  constexpr bool x16 = X16;
+  const uint32_t xbytes = static_cast<uint32_t>(min(w.nrows, kRows)) * kT * (x16 ? 2 : 4);
   if (tid == 0) mbar_arrive_expect_tx(&sm->xfull, xbytes);  // tile 0
 
   if (warp > kMmaWarp) {
@@ -384,8 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t peer_x = dsmem_addr(xs, peer);
     const uint32_t peer_xfull = dsmem_addr(&sm->xfull, peer);
     const uint32_t peer_xempty = dsmem_addr(&sm->xempty, peer);
+    // row r of the receive buffer: 64 fp32 scores (16-byte chunk c at position c ^ (r & 15)), or with
+    // the fp16 exchange 64 fp16 scores in the first half of the row's 256 bytes (c ^ (r & 7))
     const float4* xrow = reinterpret_cast<const float4*>(xs + r * kT);
     const uint32_t peer_xrow = peer_x + static_cast<uint32_t>(r * kT * 4);
+    const uint32_t xsw8 = static_cast<uint32_t>(r & 7);
     float m_r = -INFINITY, l_r = 0.f;
     float own[kHalfT];  // this CTA's partial scores of the current tile, kept for B
     // C(j): probabilities of tile j (its scaled scores wait in its P buffer) -> the same buffer (hi, and lo
@@ -461,11 +467,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i >= 1) ok = mbar_wait_cluster(&sm->xempty, (i - 1) & 1, tmo);
         }
         ok = __all_sync(0xffffffffu, ok);
-        if (ok && r < w.nrows) {
+        if constexpr (X16) {  // both CTAs add the two parts rounded to fp16: the same values on both sides
 #pragma unroll
-          for (int c = 0; c < kHalfT / 4; ++c)
-            dsmem_st_async_f32x4(peer_xrow + (((8 * hf + c) ^ xsw) << 4),
-                                 make_float4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]), peer_xfull);
+          for (int t = 0; t < kHalfT; ++t) own[t] = h2f<false>(f2h<false>(own[t]));
+        }
+        if (ok && r < w.nrows) {
+          if constexpr (X16) {
+#pragma unroll
+            for (int c = 0; c < kHalfT / 8; ++c) {
+              float4 v;
+              v.x = __uint_as_float(pack2<false>(own[8 * c], own[8 * c + 1]));
+              v.y = __uint_as_float(pack2<false>(own[8 * c + 2], own[8 * c + 3]));
+              v.z = __uint_as_float(pack2<false>(own[8 * c + 4], own[8 * c + 5]));
+              v.w = __uint_as_float(pack2<false>(own[8 * c + 6], own[8 * c + 7]));
+              dsmem_st_async_f32x4(peer_xrow + (((4 * hf + c) ^ xsw8) << 4), v, peer_xfull);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < kHalfT / 4; ++c)
+              dsmem_st_async_f32x4(peer_xrow + (((8 * hf + c) ^ xsw) << 4),
+                                   make_float4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]), peer_xfull);
+          }
         }
       }
       // (no barrier here: each warp goes on to C(i-1) as soon as its own stores are issued; a failure
@@ -488,7 +510,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kHalfT / 4; ++c) {
           const float4 o = make_float4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]);
           // (a padding row past the group's rows takes no peer part: its scores are never used)
-          const float4 y = (r < w.nrows) ? xrow[(8 * hf + c) ^ xsw] : make_float4(0.f, 0.f, 0.f, 0.f);
+          float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (r < w.nrows) {
+            if constexpr (X16) {
+              const uint4 q = reinterpret_cast<const uint4*>(xrow)[(4 * hf + (c >> 1)) ^ xsw8];
+              const uint32_t a = (c & 1) ? q.z : q.x, b = (c & 1) ? q.w : q.y;
+              y = make_float4(h2f<false>(static_cast<uint16_t>(a & 0xffffu)), h2f<false>(static_cast<uint16_t>(a >> 16)),
+                              h2f<false>(static_cast<uint16_t>(b & 0xffffu)), h2f<false>(static_cast<uint16_t>(b >> 16)));
+            } else {
+              y = xrow[(8 * hf + c) ^ xsw];
+            }
+          }
           // rank-0 part + rank-1 part, the same sum in both CTAs
           x[4 * c] = half ? (y.x + o.x) : (o.x + y.x);
           x[4 * c + 1] = half ? (y.y + o.y) : (o.y + y.y);
@@ -606,11 +638,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool BF16>
+template <bool BF16, bool X16>
 cudaError_t prepare_mh() {
   static bool done = false;
   if (done) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&mla_partial_mh_kernel<BF16>),
+  const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&mla_partial_mh_kernel<BF16, X16>),
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e == cudaSuccess) done = true;
   return e;
@@ -624,7 +656,9 @@ bool mh_supports(int total_rows, int cluster) { return total_rows > 16 && cluste
 
 cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe_half, const PartialParams& p,
                               int num_chunks, bool bf16, cudaStream_t stream) {
-  cudaError_t e = bf16 ? prepare_mh<true>() : prepare_mh<false>();
+  const bool x16 = p.xchg16 != 0;
+  cudaError_t e = bf16 ? (x16 ? prepare_mh<true, true>() : prepare_mh<true, false>())
+                       : (x16 ? prepare_mh<false, true>() : prepare_mh<false, false>());
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * ((p.q_len * p.H + kRows - 1) / kRows), num_chunks, 1);  // one CTA pair per 128-row group
@@ -640,8 +674,11 @@ cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return bf16 ? cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<true>, tm_pages, tm_kpe_half, p)
-              : cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<false>, tm_pages, tm_kpe_half, p);
+  if (bf16)
+    return x16 ? cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<true, true>, tm_pages, tm_kpe_half, p)
+               : cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<true, false>, tm_pages, tm_kpe_half, p);
+  return x16 ? cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<false, true>, tm_pages, tm_kpe_half, p)
+             : cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<false, false>, tm_pages, tm_kpe_half, p);
 }
 
 cudaError_t mh_read_clear_error(uint32_t* out) {

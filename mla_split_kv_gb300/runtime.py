@@ -68,7 +68,8 @@ def chunks_to_device(chunks: Sequence[Sequence[int]], device="cuda") -> torch.Te
 def make_desc(dc: DeviceCase, chunks_dev: Optional[torch.Tensor], kernel: int, cluster: int,
               stream: Optional[torch.cuda.Stream] = None, subs: int = 1,
               workspace: Optional[torch.Tensor] = None, tables_ready: bool = False,
-              decode_merge: int = 0, prefix_ready: bool = False) -> nb.mla_decode_desc_t:
+              decode_merge: int = 0, prefix_ready: bool = False,
+              score_exchange: int = 0) -> nb.mla_decode_desc_t:
     c = dc.case
     d = nb.mla_decode_desc_t()
     d.num_requests = c.num_requests
@@ -92,6 +93,7 @@ def make_desc(dc: DeviceCase, chunks_dev: Optional[torch.Tensor], kernel: int, c
     d.decode_merge = decode_merge
     d.prefix_ready = 1 if prefix_ready else 0
     d.cache_scale = float(c.cache_scale)
+    d.score_exchange = score_exchange
     # the descriptor holds raw device pointers: keep their tensors alive as long as it lives
     d._keep = (chunks_dev, workspace)
     return d
@@ -120,7 +122,8 @@ def decode(dc: DeviceCase, part: torch.Tensor, lse: torch.Tensor, o_indptr_dev: 
                                                 desc_kw.get("cluster", 0), desc_kw.get("stream"),
                                                 desc_kw.get("subs", 1), desc_kw.get("workspace"),
                                                 desc_kw.get("tables_ready", False), desc_kw.get("decode_merge", 0),
-                                                desc_kw.get("prefix_ready", False))
+                                                desc_kw.get("prefix_ready", False),
+                                                desc_kw.get("score_exchange", 0))
     out_code = {torch.float32: nb.MLA_F32, torch.float16: nb.MLA_F16, torch.bfloat16: nb.MLA_BF16}[out.dtype]
     nb.mla_decode(dc.q_abs.data_ptr(), dc.q_pe.data_ptr(), dc.ckv.data_ptr(), dc.kpe.data_ptr(),
                   dc.block_table.data_ptr(), dc.context_lens.data_ptr(), float(dc.case.scale), num_partitions,
