@@ -67,6 +67,8 @@ def parse():
     ap.add_argument("--profile-verify", type=int, default=0,
                     help="profiling case: only --launches plain verify-window calls of this q_len, then exit")
     ap.add_argument("--launches", type=int, default=5)
+    ap.add_argument("--profile-exchange", default="f32", choices=["f32", "f16"],
+                    help="profiling case of the many-head workload: the 128-row kernel's partial-score exchange")
     ap.add_argument("--profile-cache", default="f16", choices=["f16", "e4m3"],
                     help="profiling case at --profile-ctx: the cache type (e4m3: 8-bit caches, scale 1/4)")
     ap.add_argument("--profile-split", default="",
@@ -622,7 +624,7 @@ def run_profile_many_heads(args):
 
     nbuild.build()
     nb.load()
-    call, plan, tokens = many_heads_call(nb, rt, torch)
+    call, plan, tokens = many_heads_call(nb, rt, torch, exchange=1 if args.profile_exchange == "f16" else 0)
     for _ in range(args.launches):
         call()
     torch.cuda.synchronize()
