@@ -152,7 +152,9 @@ typedef struct {
  * otherwise P_b is proportional to L_b so that all partitions fill one wave
  * of the device's co-resident clusters, clamped to [min, max] partitions and
  * so that no chunk is empty. cluster_ctas is the cluster size that keeps the
- * most CTAs busy in that wave with at least one 64-token tile per CTA. When
+ * most CTAs busy in that wave with at least one 64-token tile per CTA; when
+ * the paired 16-row kernel applies (q_len*H <= 16, fp16 or E4M3) and the
+ * device has CTA pairs, clusters of one are not considered. When
  * the paired 16-row kernel applies (q_len*H <= 16, fp16, clusters of >= 2)
  * and one wave holds more clusters than partitions, each partition is spread
  * over clusters_per_chunk = k clusters (k <= 16, every CTA pair keeping at
