@@ -141,9 +141,10 @@ def alloc_partials(num_slots: int, q_len: int, H: int, device="cuda"):
 def decode_partial(dc: DeviceCase, part: torch.Tensor, lse: torch.Tensor, num_partitions: int = 1,
                    chunks_dev: Optional[torch.Tensor] = None, kernel: int = nb.MLA_KERNEL_AUTO,
                    cluster: int = 0, stream=None, desc: Optional[nb.mla_decode_desc_t] = None, subs: int = 1,
-                   workspace: Optional[torch.Tensor] = None, tables_ready: bool = False) -> None:
+                   workspace: Optional[torch.Tensor] = None, tables_ready: bool = False,
+                   score_exchange: int = 0) -> None:
     d = desc if desc is not None else make_desc(dc, chunks_dev, kernel, cluster, stream, subs, workspace,
-                                                tables_ready)
+                                                tables_ready, score_exchange=score_exchange)
     nb.mla_decode_partial(dc.q_abs.data_ptr(), dc.q_pe.data_ptr(), dc.ckv.data_ptr(), dc.kpe.data_ptr(),
                           dc.block_table.data_ptr(), dc.context_lens.data_ptr(), float(dc.case.scale),
                           num_partitions, part.data_ptr(), lse.data_ptr(), d)

@@ -46,7 +46,7 @@ def close_to(got, ref):
     return err <= MAX_ABS and rel <= REL_L2, (err, rel)
 
 
-def planned_call(case, dc, max_partitions=0):
+def planned_call(case, dc, max_partitions=0, score_exchange=0):
     dev = nb.mla_device_query()
     plan = nb.mla_plan(case.context_lens.tolist(), case.num_heads, case.q_len, case.block_size, dev,
                        max_partitions=max_partitions, dtype=case.dtype, merge_path=nb.MLA_MERGE_PARTIALS)
@@ -57,13 +57,13 @@ def planned_call(case, dc, max_partitions=0):
 
     def call():
         rt.decode_partial(dc, part, lse, chunks_dev=chunks, kernel=nb.MLA_KERNEL_TC, cluster=plan.cluster_ctas,
-                          subs=plan.clusters_per_chunk, workspace=ws)
+                          subs=plan.clusters_per_chunk, workspace=ws, score_exchange=score_exchange)
         return rt.merge_states(part, lse, ind, case.num_requests, case.q_len, case.num_heads, "f32")
 
     return plan, ws, call
 
 
-@pytest.mark.parametrize("which", ["pair_spread", "pair_cluster", "many_rows"])
+@pytest.mark.parametrize("which", ["pair_spread", "pair_cluster", "many_rows", "e4m3_pair", "many_rows_fp16_exchange"])
 def test_bounded_waits_run_out_then_the_context_is_usable(which):
     if which == "pair_spread":      # 16 fp16 rows, 131072 tokens: partitions spread over clusters (tickets)
         case = gen.make_decode_case(21, [131072], num_heads=16, block_size=32, dtype="f16")
@@ -71,16 +71,20 @@ def test_bounded_waits_run_out_then_the_context_is_usable(which):
     elif which == "pair_cluster":   # 16 fp16 rows, 65536 tokens: partitions on clusters of 16 CTAs
         case = gen.make_decode_case(22, [65536], num_heads=16, block_size=32, dtype="f16")
         heads = [3, 12]
+    elif which == "e4m3_pair":      # E4M3 caches on the pairs: the widening's meetings and loads give up too
+        case = gen.make_decode_case(24, [131072], num_heads=16, block_size=32, dtype="e4m3")
+        heads = [1, 14]
     else:                           # 128 bf16 rows on a CTA pair (the many-head kernel)
         case = gen.make_decode_case(23, [65536, 40000], num_heads=128, block_size=64, dtype="bf16", latent_std=0.5)
         heads = [0, 77, 127]
     dc = rt.upload(case)
-    plan, ws, call = planned_call(case, dc, max_partitions=64 if case.num_heads == 128 else 0)
+    plan, ws, call = planned_call(case, dc, max_partitions=64 if case.num_heads == 128 else 0,
+                                  score_exchange=1 if which == "many_rows_fp16_exchange" else 0)
     if which == "pair_spread":
         assert plan.clusters_per_chunk > 1
     if which == "pair_cluster":
         assert plan.clusters_per_chunk == 1 and plan.cluster_ctas >= 4
-    if which == "many_rows":
+    if which.startswith("many_rows"):
         assert plan.cluster_ctas == 2
     nb.mla_check_device_errors(None)
     nb.mla_reset_counters()
