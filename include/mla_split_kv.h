@@ -119,8 +119,7 @@ typedef struct {
   int32_t split_min_tokens; /* contexts shorter than this are not split;
                                0 = 4096                                        */
   int32_t dtype;            /* MLA_F16, MLA_BF16 or MLA_E4M3 (sets rows per CTA;
-                               E4M3 caches need clusters of 2 or more and
-                               q_len * num_heads <= 16, else UNSUPPORTED)      */
+                               E4M3 caches need clusters of 2 or more)         */
   int32_t capacity;         /* entries available in `chunks`                   */
   mla_chunk_t* chunks;      /* host, caller-owned, >= capacity entries         */
   int32_t* o_indptr;        /* host, caller-owned, >= B+1 entries              */
@@ -189,9 +188,10 @@ typedef struct {
   int32_t max_blocks_per_req; /* row stride of block_table, in entries        */
   int32_t dtype;              /* MLA_F16 or MLA_BF16 (q, ckv, kpe), or MLA_E4M3:
                                  ckv and kpe 8-bit E4M3 (576 bytes a token),
-                                 q fp16; E4M3 runs on the paired 16-row kernel
-                                 only (q_len * H <= 16, clusters of 2..16 CTAs,
-                                 not MLA_KERNEL_SIMT), else UNSUPPORTED        */
+                                 q fp16; E4M3 runs on the CTA-pair kernels
+                                 only (q_len * H <= 16: clusters of 2..16 CTAs;
+                                 more rows: clusters of 2 (or 0 = auto); not
+                                 MLA_KERNEL_SIMT), else UNSUPPORTED            */
   int32_t causal;             /* 1: the q_len rows are the last q_len tokens
                                  of each request; row i sees t <= L-q_len+i    */
   const mla_chunk_t* chunks;  /* DEVICE array of num_chunks records, or NULL

@@ -208,9 +208,10 @@ mla_status_t check_decode(const void* q_absorbed, const void* q_pe, const void* 
   if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64) return MLA_ERR_UNSUPPORTED;
   if (d->dtype != MLA_F16 && d->dtype != MLA_BF16 && d->dtype != MLA_E4M3) return MLA_ERR_UNSUPPORTED;
   if (d->dtype == MLA_E4M3) {
-    // E4M3 caches: the paired 16-row kernel only, and a scale in [2^-24, 2^24]
-    if (d->kernel == MLA_KERNEL_SIMT || d->num_heads * d->q_len > 16 || d->cluster_ctas == 1)
-      return MLA_ERR_UNSUPPORTED;
+    // E4M3 caches: the two CTA-pair kernels only (16 rows: clusters of 2 or more; more rows: the 128-row
+    // kernel's pairs), and a scale in [2^-24, 2^24]
+    if (d->kernel == MLA_KERNEL_SIMT || d->cluster_ctas == 1) return MLA_ERR_UNSUPPORTED;
+    if (d->num_heads * d->q_len > 16 && d->cluster_ctas != 0 && d->cluster_ctas != 2) return MLA_ERR_UNSUPPORTED;
     const float cs = d->cache_scale;
     if (!(cs >= 0x1p-24f && cs <= 0x1p24f)) return MLA_ERR_INVALID_ARG;  // also NaN
   }
@@ -313,7 +314,7 @@ mla_status_t launch_decode(const void* q_absorbed, const void* q_pe, const void*
              !kpe_half_map(&tm_kpe_half, kpe_cache, rows, d->block_size, d->dtype)) {
     return reject(MLA_ERR_CUDA);
   }
-  if (fp8 && (use_simt || !mla::tc128_supports(rows_total, false, C))) return reject(MLA_ERR_UNSUPPORTED);
+  if (fp8 && (use_simt || !(mh || mla::tc128_supports(rows_total, false, C)))) return reject(MLA_ERR_UNSUPPORTED);
 
   mla::PartialParams p;
   p.q_abs = static_cast<const uint16_t*>(q_absorbed);

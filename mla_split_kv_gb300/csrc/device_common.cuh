@@ -762,6 +762,66 @@ __device__ __forceinline__ void request_merge(const PartialParams& p, int b, int
   }
 }
 
+// ---------------------------------------------------------------------------
+// E4M3 caches: widening 8-bit tiles to fp16 in shared memory (the paired and
+// the 128-row kernels)
+// ---------------------------------------------------------------------------
+// four E4M3 values (the bytes of w, lowest first) -> four fp16 values (two f16x2 words, lowest first);
+// exact: every E4M3 value, its subnormals included, is an fp16 value
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  // volatile: kept between its step's load and stores, so the widening holds few values at a time
+  asm volatile("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// Shared-memory loads and stores of the in-place widening, as volatile asm without a memory clobber:
+// kept in the order written (so a step's load can be issued ahead of earlier steps' stores, which the
+// compiler could not prove independent), and ordered against the barrier operations around them
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, const uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+}
+
+// 16 E4M3 bytes -> two 16-byte pieces of fp16 (bytes 0-7, bytes 8-15), stored at d0 and d1
+__device__ __forceinline__ void widen16(const uint4 v, uint32_t d0, uint32_t d1) {
+  uint4 a, b;
+  e4m3x4_to_f16x4(v.x, a.x, a.y);
+  e4m3x4_to_f16x4(v.y, a.z, a.w);
+  e4m3x4_to_f16x4(v.z, b.x, b.y);
+  e4m3x4_to_f16x4(v.w, b.z, b.w);
+  sts128(d0, a);
+  sts128(d1, b);
+}
+
+// One warp's steps of a widening part (three warps, two staged rows of 256 bytes a step: the CTA's half
+// of the ckv columns of tokens t + 6 m and t + 6 m + 1, m < n), staged at stage_src + (t + 6 m) * 256;
+// written to the 16-bit tile layout whose 8-token row groups of four swizzled [8 x 64] atoms are 4 KB
+// apart. Each step's load is issued three steps ahead of its conversion.
+__device__ __forceinline__ void widen_ckv_steps(uint32_t slot, uint32_t stage_src, int t, int n, int r2, int cbl,
+                                                int kk) {
+  if (n <= 0) return;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  uint4 b0 = lds128(stage_src + t * 256), b1 = z, b2 = z;
+  if (n > 1) b1 = lds128(stage_src + (t + 6) * 256);
+  if (n > 2) b2 = lds128(stage_src + (t + 12) * 256);
+#pragma unroll 1
+  for (int m = 0; m < n; ++m, t += 6) {
+    const uint4 v = b0;
+    b0 = b1;
+    b1 = b2;
+    if (m + 3 < n) b2 = lds128(stage_src + (t + 18) * 256);
+    const int r = (t & 7) + r2;
+    const uint32_t row = slot + (t >> 3) * 4096 + cbl * 1024 + r * 128;
+    widen16(v, row + (((2 * kk) ^ r) << 4), row + (((2 * kk + 1) ^ r) << 4));
+  }
+}
+
 // Request b's chunk slots [lo, hi): from the offsets, or the uniform split.
 __device__ __forceinline__ void request_slots(const PartialParams& p, int b, int* lo, int* hi) {
   if (p.o_indptr != nullptr) {

@@ -77,6 +77,12 @@ constexpr uint32_t kSmem = kOffSmall + 2048 + 1024;       // + alignment slack
 static_assert(kTileSlot % 1024 == 0 && kOffTile % 1024 == 0, "swizzle atoms stay aligned");
 static_assert(kSmem <= 232448, "shared memory per CTA");
 
+// E4M3 caches: a tile's bytes land unswizzled in the upper half of its slot (staged rows of 256 bytes:
+// ckv tokens 0-63, then the kpe, 8 tokens a row) and are widened to fp16 in place
+constexpr int kStage = kTileSlot - kT * (kHalfCols + kKpeCols);  // 18 KB
+static_assert(kStage == 18432 && kCkvBytes == kStage + 56 * kHalfCols && kGroupBytes == 4096,
+              "the widening order below assumes this geometry");
+
 constexpr uint32_t kTmemO = 0;      // O [128 x 256] fp32
 constexpr uint32_t kTmemS = 256;    // S [128 x 64] fp32, 2 buffers
 constexpr uint32_t kTmemP = 384;    // P [128 x 64] 16-bit, hi and lo (32 columns each), 2 buffers
@@ -84,6 +90,7 @@ constexpr uint32_t kTmemCols = 512;
 
 struct Small {
   uint64_t full[kSlots], empty[kSlots], sfull[2], sfree[2], ppfull[2], pvdone[2], xfull, xempty, drain;
+  uint64_t landed[kSlots], conv;  // E4M3 caches: a tile's bytes landed; the producer warps' meeting point
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t peer_abort;        // set by the peer CTA (remote store) when it gave up
@@ -106,8 +113,9 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 }
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
-// X16: the pair's partial scores cross as fp16 (an instance each, no run-time branch in the loop)
-template <bool BF16, bool X16>
+// X16: the pair's partial scores cross as fp16 (an instance each, no run-time branch in the loop);
+// FP8: E4M3 caches beside fp16 queries (BF16 false), widened in the tile slots, scaled on the output
+template <bool BF16, bool X16, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_partial_mh_kernel(const __grid_constant__ CUtensorMap tm_pages, const __grid_constant__ CUtensorMap tm_kpe_half,
                           const PartialParams p) {
@@ -128,7 +136,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&sm->full[s], kPageWarps);  // one expect_tx arrival per producer warp
       mbar_init(&sm->empty[s], 1);
+      mbar_init(&sm->landed[s], kPageWarps);
     }
+    mbar_init(&sm->conv, kPageWarps);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm->sfull[t], 1);
       mbar_init(&sm->sfree[t], kSoftmaxWarps);
@@ -185,17 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       *pg0 = tok0 / p.bs;
       *npg = (min(kT, w.sub1 - tok0) + p.bs - 1) / p.bs;
     };
-    int issued = -1;
-    for (int i = 0; i < ntiles; ++i) {
+    int issued = -1;  // the last tile whose loads this warp issued
+    // the loads of this warp's pages of tile i into its slot (free), then an L2 prefetch of the same
+    // pages of tile i+3: ckv by the even CTA, kpe by the odd one
+    auto issue_tile = [&](int i) {
       const int s = i % kSlots;
-      if (i >= kSlots) {  // PV(i-3) released the slot
-        int ok = 1;
-        if (lane == 0) {
-          ok = mbar_wait(&sm->empty[s], ((i / kSlots) - 1) & 1, tmo) && !*abort_flag;
-          if (!ok) *abort_flag = 1;
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      }
       int pg0, npg;
       tile_pages(i, &pg0, &npg);
       const int mine = (npg > k0) ? (npg - k0 + kPageWarps - 1) / kPageWarps : 0;  // at most 2 (bs >= 16)
@@ -203,22 +207,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int m = 0; m < 2; ++m) pids[m] = (m < mine) ? page_of(pg0 + k0 + m * kPageWarps) : -1;
       uint8_t* slot = smem + kOffTile + s * kTileSlot;
-      if (lane == 0)
-        mbar_arrive_expect_tx(&sm->full[s], static_cast<uint32_t>(mine * p.bs * (kHalfCols + kKpeCols) * 2));
+      constexpr int kElem = FP8 ? 1 : 2;  // bytes a cached value
+      uint64_t* bar = FP8 ? &sm->landed[s] : &sm->full[s];
+      if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(mine * p.bs * (kHalfCols + kKpeCols) * kElem));
       __syncwarp();
       // lane m issues this warp's page m (TMA issue from several lanes overlaps)
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         if (lane == m && m < mine) {
           const int j = k0 + m * kPageWarps;
-          tma_load_4d(slot + j * p.bs * (kHalfCols * 2), &tm_pages, 0, 0, kHalfBoxes * half, pids[m] * (p.bs / 8),
-                      &sm->full[s], pol);
-          tma_load_2d(slot + kCkvBytes + j * p.bs * (kKpeCols * 2), &tm_kpe_half, kKpeCols * half, pids[m] * p.bs,
-                      &sm->full[s], pol);
+          if constexpr (FP8) {  // bytes, unswizzled, into the upper part of the slot
+            tma_load_2d(slot + kStage + j * p.bs * kHalfCols, &tm_pages, kHalfCols * half, pids[m] * p.bs, bar, pol);
+            tma_load_2d(slot + kStage + kT * kHalfCols + j * p.bs * kKpeCols, &tm_kpe_half, kKpeCols * half,
+                        pids[m] * p.bs, bar, pol);
+          } else {
+            tma_load_4d(slot + j * p.bs * (kHalfCols * 2), &tm_pages, 0, 0, kHalfBoxes * half, pids[m] * (p.bs / 8),
+                        bar, pol);
+            tma_load_2d(slot + kCkvBytes + j * p.bs * (kKpeCols * 2), &tm_kpe_half, kKpeCols * half, pids[m] * p.bs,
+                        bar, pol);
+          }
         }
       }
       issued = i;
-      if (i + kSlots < ntiles) {  // the same page of tile i+3 into L2: ckv by the even CTA, kpe by the odd one
+      if (i + kSlots < ntiles) {
         int qg0, qn;
         tile_pages(i + kSlots, &qg0, &qn);
         for (int j = k0; j < qn; j += kPageWarps) {
@@ -226,18 +237,142 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0 && qpid >= 0) {
             const long long row = static_cast<long long>(qpid) * p.bs;
             if (half == 0)
-              bulk_prefetch_l2(p.ckv + row * (kRank * 2), static_cast<uint32_t>(p.bs * kRank * 2));
+              bulk_prefetch_l2(p.ckv + row * (kRank * kElem), static_cast<uint32_t>(p.bs * kRank * kElem));
             else
-              bulk_prefetch_l2(p.kpe + row * (kRope * 2), static_cast<uint32_t>(p.bs * kRope * 2));
+              bulk_prefetch_l2(p.kpe + row * (kRope * kElem), static_cast<uint32_t>(p.bs * kRope * kElem));
           }
         }
+      }
+    };
+    if constexpr (FP8) {
+      // E4M3 caches: tile i's staged bytes become the 16-bit tile in place by the three producer warps,
+      // a warp step taking two staged rows (512 bytes, 16 a lane). The 16-bit rows of ckv tokens 0-31 lie
+      // below the staging; those of tokens 8g..8g+7 (g >= 4) overwrite staged rows 16g-72..16g-57 (from
+      // row 0), and the 16-bit kpe staged rows 56-71. So, with the three warps meeting between the parts:
+      // tokens 0-31 | tokens 32-47, then staged rows 48-71 into registers | those rows (tokens 48-63, the
+      // kpe) from the registers. Lane 0 of each warp then counts it on the slot's full barrier. Lanes as
+      // in the paired kernel: every quarter warp reads and writes 8 different 16-byte bank groups.
+      const int r2 = (lane >> 2) & 1, cbl = (lane >> 3) ^ r2, kk = lane & 3;
+      const int src_ckv = r2 * kHalfCols + cbl * 64 + kk * 16;
+      const int tk_l = lane >> 1, hk = lane & 1;
+      auto meet = [&](int phase) -> bool {  // two phases per tile; spins, the others being close
+        __syncwarp();
+        int ok = 1;
+        if (lane == 0) {
+          mbar_arrive(&sm->conv);
+          if (!mbar_test(&sm->conv, phase & 1)) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_test(&sm->conv, phase & 1)) {
+              if (globaltimer_ns() - t0 > tmo) {
+                flag_error(MLA_DEVERR_TIMEOUT);
+                ok = 0;
+                break;
+              }
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();
+        return ok != 0;
+      };
+      auto convert = [&](int i) -> bool {
+        const int s = i % kSlots;
+        const uint32_t slot = smem_u32(smem + kOffTile + s * kTileSlot);
+        const uint32_t stage_src = slot + kStage + src_ckv;
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm->landed[s], (i / kSlots) & 1, tmo))) return false;
+        widen_ckv_steps(slot, stage_src, 2 * k0, k0 == 0 ? 6 : 5, r2, cbl, kk);  // tokens 0-31: 16 steps
+        if (!meet(2 * i)) return false;
+        const int fb = (k0 + 2) % kPageWarps;  // rotated: 12 steps per warp over the tile
+        widen_ckv_steps(slot, stage_src, 32 + 2 * fb, fb == 2 ? 2 : 3, r2, cbl, kk);  // tokens 32-47: 8 steps
+        uint4 held[4];  // staged rows 48 + 2j, j = k0 + 3m: ckv tokens 48-63 (j < 8), then the kpe
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int j = k0 + kPageWarps * m;
+          held[m] = lds128(slot + kStage + (48 + 2 * j) * kHalfCols + (j < 8 ? src_ckv : lane * 16));
+        }
+        if (!meet(2 * i + 1)) return false;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int j = k0 + kPageWarps * m;
+          if (j < 8) {
+            const int t = 48 + 2 * j, r = (t & 7) + r2;
+            const uint32_t row = slot + (t >> 3) * kGroupBytes + cbl * 1024 + r * 128;
+            widen16(held[m], row + (((2 * kk) ^ r) << 4), row + (((2 * kk + 1) ^ r) << 4));
+          } else {  // kpe tokens 16 (j-8) .. +15: 32 bytes each, two 16-byte fp16 pieces per lane
+            const int tk = 16 * (j - 8) + tk_l;
+            const uint32_t row = slot + kCkvBytes + tk * (kKpeCols * 2);
+            widen16(held[m], row + ((((2 * hk) ^ (tk >> 1)) & 3) << 4), row + ((((2 * hk + 1) ^ (tk >> 1)) & 3) << 4));
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->full[s]);
+        return true;
+      };
+      // issue and widening interleave: the next tile's loads as soon as its slot is free, else the
+      // widening of the oldest landed tile; nothing to do for longer than the wait limit (or an abort
+      // elsewhere) ends it
+      int ni = 0, nc = 0;
+      bool idle = false;
+      uint64_t idle_t0 = 0;
+      while (nc < ntiles) {
+        int act = 0;
+        if (lane == 0) {
+          if (ni < ntiles && ni < nc + kSlots &&
+              (ni < kSlots || mbar_test(&sm->empty[ni % kSlots], ((ni / kSlots) - 1) & 1))) {
+            act = 1;
+          } else if (nc < ni && mbar_test(&sm->landed[nc % kSlots], (nc / kSlots) & 1)) {
+            act = 2;
+          } else if (*abort_flag) {
+            act = -1;
+          } else {
+            const uint64_t now = globaltimer_ns();
+            if (!idle) {
+              idle = true;
+              idle_t0 = now;
+            } else if (now - idle_t0 > tmo) {
+              act = -1;
+              *abort_flag = 1;
+              flag_error(MLA_DEVERR_TIMEOUT);
+            }
+          }
+          if (act > 0) idle = false;
+        }
+        act = __shfl_sync(0xffffffffu, act, 0);
+        if (act == 1) {
+          issue_tile(ni++);
+        } else if (act == 2) {
+          if (!convert(nc)) {
+            if (lane == 0) {
+              *abort_flag = 1;
+              flag_error(MLA_DEVERR_TIMEOUT);
+            }
+            break;
+          }
+          ++nc;
+        } else if (act < 0) {
+          break;
+        }
+      }
+    } else {
+      for (int i = 0; i < ntiles; ++i) {
+        const int s = i % kSlots;
+        if (i >= kSlots) {  // PV(i-3) released the slot
+          int ok = 1;
+          if (lane == 0) {
+            ok = mbar_wait(&sm->empty[s], ((i / kSlots) - 1) & 1, tmo) && !*abort_flag;
+            if (!ok) *abort_flag = 1;
+          }
+          if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        }
+        issue_tile(i);
       }
     }
     // after an abort, let this warp's loads still in flight (the last three tiles it issued) land before
     // shared memory is released
     if (lane == 0 && *abort_flag)
       for (int t = max(0, issued - (kSlots - 1)); t <= issued; ++t)
-        mbar_wait(&sm->full[t % kSlots], (t / kSlots) & 1, kDrainTimeoutNs);
+        mbar_wait(FP8 ? &sm->landed[t % kSlots] : &sm->full[t % kSlots], (t / kSlots) & 1, kDrainTimeoutNs);
     cluster_wait_acquire();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
@@ -604,7 +739,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue: the normalized partial of this row over this thread's half of the CTA's 256 columns,
     // and the LSE (rank 0)
     const bool has_mass = read_o && (r < w.nrows) && (m_r != -INFINITY) && (l_row > 0.f);
-    const float inv = has_mass ? 1.f / l_row : 0.f;
+    // (an E4M3 cache's scale multiplies the output: folded into the normalisation)
+    const float inv = has_mass ? (FP8 ? (1.f / l_row) * p.cache_scale : 1.f / l_row) : 0.f;
     const long long orow = static_cast<long long>(w.slot) * rows_total + w.row0 + r;
     if (read_o) tc_fence_after();
     for (int q = 0; q < kHalfCols / 32; ++q) {
@@ -638,11 +774,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool BF16, bool X16>
+template <bool BF16, bool X16, bool FP8>
 cudaError_t prepare_mh() {
   static bool done = false;
   if (done) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&mla_partial_mh_kernel<BF16, X16>),
+  const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&mla_partial_mh_kernel<BF16, X16, FP8>),
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e == cudaSuccess) done = true;
   return e;
@@ -657,8 +793,10 @@ bool mh_supports(int total_rows, int cluster) { return total_rows > 16 && cluste
 cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe_half, const PartialParams& p,
                               int num_chunks, bool bf16, cudaStream_t stream) {
   const bool x16 = p.xchg16 != 0;
-  cudaError_t e = bf16 ? (x16 ? prepare_mh<true, true>() : prepare_mh<true, false>())
-                       : (x16 ? prepare_mh<false, true>() : prepare_mh<false, false>());
+  if (p.fp8 && bf16) return cudaErrorInvalidValue;  // E4M3 caches go with fp16 queries
+  cudaError_t e = p.fp8 ? (x16 ? prepare_mh<false, true, true>() : prepare_mh<false, false, true>())
+                  : bf16 ? (x16 ? prepare_mh<true, true, false>() : prepare_mh<true, false, false>())
+                         : (x16 ? prepare_mh<false, true, false>() : prepare_mh<false, false, false>());
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * ((p.q_len * p.H + kRows - 1) / kRows), num_chunks, 1);  // one CTA pair per 128-row group
@@ -674,11 +812,14 @@ cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (p.fp8)
+    return x16 ? cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<false, true, true>, tm_pages, tm_kpe_half, p)
+               : cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<false, false, true>, tm_pages, tm_kpe_half, p);
   if (bf16)
-    return x16 ? cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<true, true>, tm_pages, tm_kpe_half, p)
-               : cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<true, false>, tm_pages, tm_kpe_half, p);
-  return x16 ? cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<false, true>, tm_pages, tm_kpe_half, p)
-             : cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<false, false>, tm_pages, tm_kpe_half, p);
+    return x16 ? cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<true, true, false>, tm_pages, tm_kpe_half, p)
+               : cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<true, false, false>, tm_pages, tm_kpe_half, p);
+  return x16 ? cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<false, true, false>, tm_pages, tm_kpe_half, p)
+             : cudaLaunchKernelEx(&cfg, mla_partial_mh_kernel<false, false, false>, tm_pages, tm_kpe_half, p);
 }
 
 cudaError_t mh_read_clear_error(uint32_t* out) {

@@ -96,7 +96,6 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
   if (maxP < 1 || maxP > 1024) return MLA_ERR_INVALID_ARG;
 
   const int rows = num_heads * q_len;
-  if (plan->dtype == MLA_E4M3 && rows > 16) return MLA_ERR_UNSUPPORTED;  // E4M3: the paired 16-row kernel only
   // more than 16 rows: one CTA pair (a cluster of 2) per 128 rows, the last group padded
   const bool many_rows = mla::mh_supports(rows, 2);
   const int nr = many_rows ? 128 : mla::tc_rows_per_cta(rows, plan->dtype == MLA_BF16);

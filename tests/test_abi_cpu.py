@@ -270,9 +270,9 @@ def test_plan_capacity_and_argument_errors(lib):
     assert lib.mla_plan(lens, 0, 16, 1, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_INVALID_ARG
     plan.dtype = 2
     assert lib.mla_plan(lens, 1, 16, 1, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_UNSUPPORTED
-    plan.dtype = nb.MLA_E4M3  # E4M3 caches run on the paired 16-row kernel only
-    assert lib.mla_plan(lens, 1, 64, 1, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_UNSUPPORTED
-    assert lib.mla_plan(lens, 1, 16, 2, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_UNSUPPORTED
+    plan.dtype = nb.MLA_E4M3  # E4M3 caches run on CTA pairs: 128-row groups on clusters of 2
+    assert lib.mla_plan(lens, 1, 64, 1, 32, ctypes.byref(dev), ctypes.byref(plan)) in (nb.MLA_OK, nb.MLA_ERR_CAPACITY)
+    assert plan.cluster_ctas == 2
     plan.dtype = 0
     neg = (ctypes.c_int32 * 1)(-5)
     assert lib.mla_plan(neg, 1, 16, 1, 32, ctypes.byref(dev), ctypes.byref(plan)) == nb.MLA_ERR_INVALID_ARG
@@ -323,8 +323,8 @@ def call_partial(lib, d, P=2, ptrs=None):
     (dict(dtype=nb.MLA_E4M3, cache_scale=1.0), 2, nb.MLA_ERR_UNSUPPORTED),  # clusters of 1
     (dict(dtype=nb.MLA_E4M3, cluster_ctas=2, kernel=nb.MLA_KERNEL_SIMT, cache_scale=1.0), 2,
      nb.MLA_ERR_UNSUPPORTED),
-    (dict(dtype=nb.MLA_E4M3, cluster_ctas=2, num_heads=64, cache_scale=1.0), 2, nb.MLA_ERR_UNSUPPORTED),
-    (dict(dtype=nb.MLA_E4M3, cluster_ctas=2, q_len=2, cache_scale=1.0), 2, nb.MLA_ERR_UNSUPPORTED),
+    (dict(dtype=nb.MLA_E4M3, cluster_ctas=4, num_heads=64, cache_scale=1.0), 2, nb.MLA_ERR_UNSUPPORTED),
+    (dict(dtype=nb.MLA_E4M3, cluster_ctas=8, q_len=2, cache_scale=1.0), 2, nb.MLA_ERR_UNSUPPORTED),
     (dict(dtype=nb.MLA_E4M3, cluster_ctas=2), 2, nb.MLA_ERR_INVALID_ARG),  # cache_scale left 0
     (dict(dtype=nb.MLA_E4M3, cluster_ctas=2, cache_scale=-0.25), 2, nb.MLA_ERR_INVALID_ARG),
     (dict(dtype=nb.MLA_E4M3, cluster_ctas=2, cache_scale=2.0 ** -25), 2, nb.MLA_ERR_INVALID_ARG),

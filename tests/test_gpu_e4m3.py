@@ -67,13 +67,14 @@ def widened_f16(case):
     return dataclasses.replace(case, dtype="f16", ckv=ckv, kpe=kpe, cache_scale=1.0)
 
 
-def uniform(case, P, C, dc=None, subs=1):
+def uniform(case, P, C, dc=None, subs=1, exchange=0):
     dc = dc or rt.upload(case)
     B, q, H = case.num_requests, case.q_len, case.num_heads
     part, lse = rt.alloc_partials(B * P, q, H)
     part.fill_(float("nan"))
     ws = rt.alloc_workspace(B * P, subs, C, q, H) if subs > 1 else None
-    rt.decode_partial(dc, part, lse, num_partitions=P, kernel=nb.MLA_KERNEL_TC, cluster=C, subs=subs, workspace=ws)
+    rt.decode_partial(dc, part, lse, num_partitions=P, kernel=nb.MLA_KERNEL_TC, cluster=C, subs=subs, workspace=ws,
+                      score_exchange=exchange)
     ind = rt.uniform_indptr(B, P)
     out = rt.merge_states(part, lse, ind, B, q, H, "f32")
     return part, lse, out
@@ -182,3 +183,31 @@ def test_e4m3_out_of_range_page_reads_zeros_and_is_flagged():
     fixed.block_table[0, 2] = spare
     ref, _ = orc.unsplit(fixed)
     assert_close(out.cpu().numpy(), ref, "e4m3 bad page")
+
+
+@pytest.mark.parametrize("H,q_len,bs,lens,cs,exchange,heads", [
+    (128, 1, 64, [9000, 2500, 130], 0.25, 0, [0, 45, 90, 127]),   # the many-head shape on E4M3 caches
+    (64, 1, 32, [5000, 777], 2.0 ** -4, 0, None),                  # a 64-row group
+    (16, 4, 32, [4000, 2000], 0.25, 0, None),                      # a verify window: 64 rows, causal
+    (16, 16, 16, [3000, 1000], 0.5, 0, [0, 8, 15]),                # 256 rows: two 128-row groups, causal
+    (128, 1, 64, [6000, 1000], 0.25, 1, [3, 64, 126]),             # with the fp16 score exchange
+])
+def test_e4m3_many_rows_against_the_oracle_and_the_fp16_path(H, q_len, bs, lens, cs, exchange, heads):
+    """More than 16 rows: the 128-row kernel's pairs widen the tiles in place as the 16-row kernel does. Against
+    the oracle, and (power-of-two scales) the fp16 path's bits on the host-widened cache."""
+    case = gen.make_decode_case(66, lens, num_heads=H, q_len=q_len, block_size=bs, dtype="e4m3", cache_scale=cs,
+                                causal=q_len > 1)
+    nb.mla_reset_counters()
+    got = uniform(case, 2, 2, exchange=exchange)
+    assert nb.mla_get_counters()[nb.CTR_PARTIAL_TC] == 1
+    hs = heads if heads is not None else list(range(H))
+    chunks, _ = orc.plan_chunks(case.context_lens, [2] * case.num_requests, bs)
+    if heads is None:
+        ref_part, ref_lse = orc.partials(case, chunks)
+        assert_close(got[0].cpu().numpy(), ref_part, f"e4m3 many-row partials H={H} q_len={q_len}")
+        assert_lse_close(got[1].cpu().numpy(), ref_lse, "e4m3 many-row lse")
+    ref, _ = orc.unsplit(case, heads=hs)
+    assert_close(got[2].cpu().numpy()[:, :, hs], ref[:, :, hs], f"e4m3 many-row merged H={H} q_len={q_len}")
+    want = uniform(widened_f16(case), 2, 2, exchange=exchange)
+    for g, w in zip(got, want):
+        assert torch.equal(g, w)
