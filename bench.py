@@ -162,24 +162,27 @@ MH_B, MH_H, MH_BS, MH_SEED = 8, 128, 64, 4
 MANY_HEADS = "mla_decode_B8_H128_bf16_bs64_ctx_U4K_64K"
 
 
-def make_many_heads_case():
+def make_many_heads_case(dtype="bf16"):
+    """The many-head workload; dtype "e4m3": the same lengths and pages over an E4M3 cache (scale 1/4) beside
+    fp16 queries."""
     from mla_split_kv_gb300 import inputs as gen
 
     lens = gen.uniform_lengths(MH_SEED, MH_B, 4096, 65536)
-    return gen.make_decode_case(MH_SEED, lens, num_heads=MH_H, block_size=MH_BS, dtype="bf16", latent_std=0.5)
+    return gen.make_decode_case(MH_SEED, lens, num_heads=MH_H, block_size=MH_BS, dtype=dtype, latent_std=0.5,
+                                cache_scale=0.25)
 
 
-def many_heads_call(nb, rt, torch, stream=None, exchange=0):
+def many_heads_call(nb, rt, torch, stream=None, exchange=0, dtype="bf16"):
     """Upload the many-head case, plan it, and return a closure doing one layer call (partial + merge kernels);
     `exchange`: the 128-row kernel's partial-score exchange (0: fp32, the default; 1: fp16)."""
-    case = make_many_heads_case()
+    case = make_many_heads_case(dtype)
     dev = nb.mla_device_query()
-    plan = nb.mla_plan(case.context_lens.tolist(), MH_H, 1, MH_BS, dev, max_partitions=64, dtype="bf16")
+    plan = nb.mla_plan(case.context_lens.tolist(), MH_H, 1, MH_BS, dev, max_partitions=64, dtype=dtype)
     dc = rt.upload(case)
     chunks_dev = rt.chunks_to_device(plan.chunks)
     part, lse = rt.alloc_partials(plan.num_chunks, 1, MH_H)
     ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
-    out = torch.empty((MH_B, 1, MH_H, 512), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((MH_B, 1, MH_H, 512), dtype=torch.bfloat16 if dtype == "bf16" else torch.float16, device="cuda")
     desc = rt.make_desc(dc, chunks_dev, nb.MLA_KERNEL_TC, plan.cluster_ctas, stream, score_exchange=exchange)
 
     def call():  # mla_decode: the 128-row kernel, then the merge kernel
@@ -638,9 +641,9 @@ def run_profile_many_heads(args):
 def time_many_heads(nb, rt, torch, stream, reps=20):
     """Device time of one many-head layer call (graph of `reps` calls, CUDA events), and its flop rate; beside
     it the same call with the partial scores exchanged as fp16 (an opt-in of the ABI)."""
-    def timed(exchange):
+    def timed(exchange, dtype="bf16"):
         with torch.cuda.stream(stream):
-            call, plan, tokens = many_heads_call(nb, rt, torch, stream, exchange)
+            call, plan, tokens = many_heads_call(nb, rt, torch, stream, exchange, dtype)
             for _ in range(3):
                 call()
         stream.synchronize()
@@ -659,14 +662,17 @@ def time_many_heads(nb, rt, torch, stream, reps=20):
 
     us, plan, tokens = timed(0)
     us16, _, _ = timed(1)
+    us8, _, _ = timed(0, "e4m3")
     flops = tokens * MH_H * 2 * (576 + 512)
     return {"workload": MANY_HEADS, "us_per_call": round(us, 3), "partitions": plan.num_chunks,
             "cluster": plan.cluster_ctas, "tokens": tokens, "tflops": round(flops / (us * 1e-6) / 1e12, 1),
             "hbm_gbs": round(tokens * LATENT_BYTES_PER_TOKEN / (us * 1e-6) / 1e9, 1),
             "fp16_exchange_us": round(us16, 3),
             "fp16_exchange_tflops": round(flops / (us16 * 1e-6) / 1e12, 1),
+            "e4m3_cache_us": round(us8, 3),
             "note": "a parity workload timed beside the headline one; repeats of one cache (323 MB, > L2); "
-                    "fp16_exchange: score_exchange = MLA_SCORE_EXCHANGE_F16"}
+                    "fp16_exchange: score_exchange = MLA_SCORE_EXCHANGE_F16; e4m3_cache: the same lengths over an "
+                    "E4M3 cache (scale 1/4) beside fp16 queries"}
 
 
 # the headline sweep with 8-bit E4M3 caches (576 bytes a token, power-of-two cache scale 1/4) beside fp16

@@ -63,7 +63,8 @@ def planned_call(case, dc, max_partitions=0, score_exchange=0):
     return plan, ws, call
 
 
-@pytest.mark.parametrize("which", ["pair_spread", "pair_cluster", "many_rows", "e4m3_pair", "many_rows_fp16_exchange"])
+@pytest.mark.parametrize("which", ["pair_spread", "pair_cluster", "many_rows", "e4m3_pair", "many_rows_fp16_exchange",
+                                   "e4m3_many_rows"])
 def test_bounded_waits_run_out_then_the_context_is_usable(which):
     if which == "pair_spread":      # 16 fp16 rows, 131072 tokens: partitions spread over clusters (tickets)
         case = gen.make_decode_case(21, [131072], num_heads=16, block_size=32, dtype="f16")
@@ -74,6 +75,9 @@ def test_bounded_waits_run_out_then_the_context_is_usable(which):
     elif which == "e4m3_pair":      # E4M3 caches on the pairs: the widening's meetings and loads give up too
         case = gen.make_decode_case(24, [131072], num_heads=16, block_size=32, dtype="e4m3")
         heads = [1, 14]
+    elif which == "e4m3_many_rows":  # E4M3 caches on the 128-row kernel
+        case = gen.make_decode_case(25, [65536, 40000], num_heads=128, block_size=64, dtype="e4m3")
+        heads = [0, 77, 127]
     else:                           # 128 bf16 rows on a CTA pair (the many-head kernel)
         case = gen.make_decode_case(23, [65536, 40000], num_heads=128, block_size=64, dtype="bf16", latent_std=0.5)
         heads = [0, 77, 127]
@@ -84,7 +88,7 @@ def test_bounded_waits_run_out_then_the_context_is_usable(which):
         assert plan.clusters_per_chunk > 1
     if which == "pair_cluster":
         assert plan.clusters_per_chunk == 1 and plan.cluster_ctas >= 4
-    if which.startswith("many_rows"):
+    if which.startswith("many_rows") or which == "e4m3_many_rows":
         assert plan.cluster_ctas == 2
     nb.mla_check_device_errors(None)
     nb.mla_reset_counters()
