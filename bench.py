@@ -25,8 +25,8 @@ chunk partials), `partial_kernel_alone` (the ABI's mla_decode_partial),
 `per_ctx` (each context alone, its planned split, a single cold call after an
 L2 flush and the host planner's time per call), `trials` (median / min / max
 over five more K-step trials), `many_heads` (the many-head workload),
-`verify_windows`, `batch_grid` and `e4m3_caches` (the same sweep on 8-bit E4M3
-caches). `--impl reference` times the oracle itself
+`verify_windows`, `batch_grid`, `e4m3_caches` (the same sweep on 8-bit E4M3
+caches) and `bf16` (the same sweep in bf16). `--impl reference` times the oracle itself
 on the same workload; `--gpus N` without a launcher starts N ranks (one
 replica per GPU).
 """
@@ -678,21 +678,24 @@ def time_many_heads(nb, rt, torch, stream, reps=20):
 # the headline sweep with 8-bit E4M3 caches (576 bytes a token, power-of-two cache scale 1/4) beside fp16
 # queries: the same contexts, seeds and pools, planned for E4M3 caches
 E4M3_SWEEP = "mla_decode_ctx_sweep_B1_H16_e4m3_cache_fp16_q_bs32"
+BF16_SWEEP = "mla_decode_ctx_sweep_B1_H16_r512_rope64_bf16_bs32"
 
 
-def time_e4m3_sweep(nb, rt, torch, stream, dev, peak, reps=20):
+def time_e4m3_sweep(nb, rt, torch, stream, dev, peak, reps=20, dtype="e4m3"):
+    """The headline sweep on another cache type (E4M3 caches with fp16 queries, or bf16 throughout)."""
     calls, per_ctx = [], []
     with torch.cuda.stream(stream):
         for i, L in enumerate(CONTEXTS):
-            case = make_case(i, L, "e4m3")
-            plan = nb.mla_plan([L], H, 1, BS, dev, dtype="e4m3")
+            case = make_case(i, L, dtype)
+            plan = nb.mla_plan([L], H, 1, BS, dev, dtype=dtype)
             dc = rt.upload(case)
             chunks = rt.chunks_to_device(plan.chunks)
             part, lse = rt.alloc_partials(plan.num_chunks, 1, H)
             ws = rt.alloc_decode_workspace(1, plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, H)
             desc = rt.make_desc(dc, chunks, nb.MLA_KERNEL_TC, plan.cluster_ctas, stream, plan.clusters_per_chunk, ws,
                                 tables_ready=True, prefix_ready=True)
-            out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
+            out = torch.empty((1, 1, H, 512), dtype=torch.bfloat16 if dtype == "bf16" else torch.float16,
+                              device="cuda")
             ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
             calls.append(dict(L=L, plan=plan, dc=dc, part=part, lse=lse, ind=ind, out=out, desc=desc))
         for _ in range(3):
@@ -712,7 +715,8 @@ def time_e4m3_sweep(nb, rt, torch, stream, dev, peak, reps=20):
         e[1].record(stream)
     stream.synchronize()
     us = e[0].elapsed_time(e[1]) * 1e3 / (reps * len(calls))
-    nbytes = sum(sum(algorithmic_bytes(c["L"], c["plan"].num_chunks, 576)) for c in calls) / len(calls)
+    per_token = 576 if dtype == "e4m3" else LATENT_BYTES_PER_TOKEN
+    nbytes = sum(sum(algorithmic_bytes(c["L"], c["plan"].num_chunks, per_token)) for c in calls) / len(calls)
     for c in calls:  # each context alone: a graph of four calls on its cache
         g1 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g1, stream=stream):
@@ -729,6 +733,10 @@ def time_e4m3_sweep(nb, rt, torch, stream, dev, peak, reps=20):
                         "partitions": c["plan"].num_chunks, "cluster": c["plan"].cluster_ctas,
                         "clusters_per_partition": c["plan"].clusters_per_chunk})
     achieved = nbytes / (us * 1e-6) / 1e9
+    if dtype != "e4m3":
+        return {"workload": BF16_SWEEP, "us_per_call": round(us, 3), "bytes_per_token": per_token,
+                "achieved_gbs": round(achieved, 1), "frac": round(achieved / peak, 4), "per_ctx": per_ctx,
+                "note": "timed like the headline step; the same seeds and pools drawn in bf16"}
     return {"workload": E4M3_SWEEP, "us_per_call": round(us, 3), "bytes_per_token": 576, "cache_scale": 0.25,
             "achieved_gbs": round(achieved, 1), "frac": round(achieved / peak, 4), "per_ctx": per_ctx,
             "note": "timed like the headline step (a graph of the six layer calls through mla_decode, tables and "
@@ -1070,6 +1078,7 @@ def run_ours(args, rank, world):
         {"hbm_gbs": 6800.0, "tensor_tflops": 1900.0, "source": "fallback"}
     verify = time_verify_windows(nb, rt, torch, stream, tpk) if not args.skip_extra else None
     e4m3 = time_e4m3_sweep(nb, rt, torch, stream, dev, tpk["hbm_gbs"]) if not args.skip_extra else None
+    bf16 = time_e4m3_sweep(nb, rt, torch, stream, dev, tpk["hbm_gbs"], dtype="bf16") if not args.skip_extra else None
     grid = time_batch_grid(nb, rt, torch, stream) if not args.skip_extra else None
     st, code = nb.mla_check_device_errors(stream.cuda_stream)
     if st != nb.MLA_OK:
@@ -1116,6 +1125,7 @@ def run_ours(args, rank, world):
         "verify_windows": verify,
         "batch_grid": grid,
         "e4m3_caches": e4m3,
+        "bf16": bf16,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(kname, sum(CONTEXTS) / len(CONTEXTS)),

@@ -152,9 +152,9 @@ typedef struct {
  * of the device's co-resident clusters, clamped to [min, max] partitions and
  * so that no chunk is empty. cluster_ctas is the cluster size that keeps the
  * most CTAs busy in that wave with at least one 64-token tile per CTA; when
- * the paired 16-row kernel applies (q_len*H <= 16, fp16 or E4M3) and the
- * device has CTA pairs, clusters of one are not considered. When
- * the paired 16-row kernel applies (q_len*H <= 16, fp16, clusters of >= 2)
+ * the paired 16-row kernel applies (q_len*H <= 16) and the device has CTA
+ * pairs, clusters of one are not considered. When the paired 16-row kernel
+ * applies (q_len*H <= 16, clusters of >= 2)
  * and one wave holds more clusters than partitions, each partition is spread
  * over clusters_per_chunk = k clusters (k <= 16, every CTA pair keeping at
  * least one 128-token tile); the partition count itself is not raised. For a
@@ -206,7 +206,7 @@ typedef struct {
                                  (unnormalized O, row maxima and sums) to the
                                  workspace and the CTA that finishes last
                                  merges them in index order into the
-                                 partition's slot. Only for the 16-row fp16
+                                 partition's slot. Only for the 16-row
                                  tensor-core kernel whose CTAs share tiles in
                                  pairs (q_len*H <= 16, cluster_ctas set to
                                  2..16, not 0 = auto);
@@ -399,7 +399,7 @@ mla_status_t mla_merge_states(const float* partials, const float* lse, const int
  * into `out` (rounded once to out_dtype) and `out_lse` (NULL allowed).
  *
  * The ways, by kernel and desc->decode_merge:
- *  - the paired 16-row fp16 kernel (q_len*H <= 16, clusters of 2..16 CTAs) with
+ *  - the paired 16-row kernel (q_len*H <= 16, clusters of 2..16 CTAs) with
  *    MLA_DECODE_MERGE_ENTRIES (default): the partial kernel skips its
  *    in-cluster combine and writes every CTA pair's unnormalized part (O over
  *    its tokens, row maxima and sums) to the workspace; a merge kernel launched

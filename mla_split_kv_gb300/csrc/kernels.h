@@ -121,12 +121,12 @@ cudaError_t launch_partial_tc(const CUtensorMap& tm_ckv, const CUtensorMap& tm_k
                               const CUtensorMap& tm_kpe_half, const PartialParams& p, int num_chunks, int cluster,
                               bool bf16, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
-// 128-token-tile tensor-core kernel for CTAs of at most 16 rows (fp16 only),
+// 128-token-tile tensor-core kernel for CTAs of at most 16 rows (fp16, bf16, or E4M3 caches),
 // CTAs in pairs that split the latent columns (cluster of 2..16 CTAs).
 // tm_kpe_half: kpe boxes of 32 columns with the 64-byte swizzle.
 bool tc128_supports(int total_rows, bool bf16, int cluster);
 cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe_half, const PartialParams& p,
-                                 int num_chunks, int cluster, cudaStream_t stream);
+                                 int num_chunks, int cluster, bool bf16, cudaStream_t stream);
 int tc128_max_active_clusters(int cluster);
 // 64-token-tile tensor-core kernel for groups of 128 rows (q_len * H > 16, the last group
 // padded), fp16 or bf16, each group on a cluster of one CTA pair that split the latent columns.

@@ -1,5 +1,5 @@
-// Tensor-core partial-decode kernel for CTAs of 16 query rows (fp16) working
-// in pairs, sm_103a.
+// Tensor-core partial-decode kernel for CTAs of 16 query rows (fp16 or bf16)
+// working in pairs, sm_103a.
 //
 // The operation is the one of the other partial kernels ("feat(core):
 // matrix-absorbed MLA decode over a compressed-latent KV cache", *What
@@ -96,9 +96,10 @@ constexpr uint32_t kSmem = kOffSmall + kSmallBytes;
 // in the kpe part of a slot, after the tile's score product: the peer's partial S, then P^T
 constexpr uint32_t kXBuf = kNR * kT * 4;                    // [128 tokens][16 rows] fp32: 8 KB
 constexpr uint32_t kPBytes = 2 * kNR * 128;                 // P^T [16 x 128 tokens]: two 64-token atoms
+// (bf16: P^T as two bf16 terms, hi then lo, 2 x kPBytes: the whole kpe part of the slot)
 constexpr uint32_t kTmemCols = 64;                          // S^T 2 x 16 + O^T 2 x 16
 static_assert(kSmem <= 232448, "shared memory per CTA");
-static_assert(kXBuf <= kKpeBytes && kPBytes <= kKpeBytes, "exchange and P^T fit the kpe part of a slot");
+static_assert(kXBuf <= kKpeBytes && 2 * kPBytes <= kKpeBytes, "exchange and P^T (hi, lo) fit the kpe part of a slot");
 static_assert(kCkvBytes % 1024 == 0 && kTileSlot % 1024 == 0, "swizzle atoms stay aligned");
 static_assert(kNR * kHalfCols * 4 + 2 * kNR * 4 <= kSlots * kTileSlot, "epilogue staging fits the tile slots");
 
@@ -123,8 +124,9 @@ static_assert(sizeof(Small) <= kSmallBytes, "small smem region");
 
 __device__ __forceinline__ uint32_t tmem_lane_base(int warp) { return static_cast<uint32_t>(32 * (warp & 3)) << 16; }
 
-// kFp8: E4M3 caches (byte loads, widened in the slot, cache scale on the output); one instance each
-template <bool kFp8>
+// kFp8: E4M3 caches (byte loads, widened in the slot, cache scale on the output); kBf16: bf16 queries and
+// caches (the probabilities carried as two bf16 terms, two PV products a step); one instance each
+template <bool kFp8, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_partial_tc128_kernel(const __grid_constant__ CUtensorMap tm_pages, const __grid_constant__ CUtensorMap tm_kpe_half,
                              const PartialParams p) {
@@ -434,8 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_wait_acquire();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
-    const uint32_t idesc_s = idesc_f16_f32(128, kNR, false, false, false);
-    const uint32_t idesc_o = idesc_f16_f32(128, kNR, false, true, false);
+    const uint32_t idesc_s = idesc_f16_f32(128, kNR, kBf16, false, false);
+    const uint32_t idesc_o = idesc_f16_f32(128, kNR, kBf16, true, false);
     const Desc2 qd = desc2(smem_desc_sw128(smem_u32(qs), 16, 1024));
     const Desc2 qk = desc2(smem_desc_sw64(smem_u32(qs + kHalfBoxes * kQChunk), 512));
     const uint32_t tile_base = smem_u32(smem + kOffTile);
@@ -501,13 +503,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d = tmem + 2 * kNR + blk * kNR;
           if (ksteps == kT / 16) {
 #pragma unroll
-            for (int ks = 0; ks < kT / 16; ++ks)
+            for (int ks = 0; ks < kT / 16; ++ks) {
               umma_ss(d, a0, (ks * 2 * kGroupBytes) >> 4, pb, ((ks >> 2) * (kNR * 128) + (ks & 3) * 32) >> 4, idesc_o,
                       ks > 0 ? 1u : acc0);
+              if (kBf16)  // the lo term of the probabilities, kPBytes further
+                umma_ss(d, a0, (ks * 2 * kGroupBytes) >> 4, pb,
+                        (kPBytes + (ks >> 2) * (kNR * 128) + (ks & 3) * 32) >> 4, idesc_o, 1u);
+            }
           } else {
-            for (int ks = 0; ks < ksteps; ++ks)
+            for (int ks = 0; ks < ksteps; ++ks) {
               umma_ss(d, a0, (ks * 2 * kGroupBytes) >> 4, pb, ((ks >> 2) * (kNR * 128) + (ks & 3) * 32) >> 4, idesc_o,
                       ks > 0 ? 1u : acc0);
+              if (kBf16)
+                umma_ss(d, a0, (ks * 2 * kGroupBytes) >> 4, pb,
+                        (kPBytes + (ks >> 2) * (kNR * 128) + (ks & 3) * 32) >> 4, idesc_o, 1u);
+            }
           }
         }
         umma_commit(&sm->empty[s]);
@@ -746,16 +756,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < kRH; ++k) lsum[k] *= sm->alpha[kRH * h + k];
       }
-      {  // probabilities -> P^T (fp16, K-major, two swizzled 64-token atoms) and row sums, over the
-         // peer's partial S (every softmax warp has read its part: the barrier above)
+      {  // probabilities -> P^T (16-bit, K-major, two swizzled 64-token atoms; bf16: a second P^T of the
+         // rounding remainders kPBytes further) and row sums, over the peer's partial S (every softmax
+         // warp has read its part: the barrier above)
         uint8_t* pb = region + (tl >> 6) * (kNR * 128);
 #pragma unroll
         for (int k = 0; k < kRH; ++k) {
           // masked scores (-inf) give 0; a row with no visible token yet subtracts a finite stand-in
           const float pr = fast_exp2(x[k] - ((mr[k] == -INFINITY) ? 0.f : mr[k]));
-          const uint16_t hv = f2h<false>(pr);
-          lsum[k] += h2f<false>(hv);
-          *reinterpret_cast<uint16_t*>(pb + sw128_offset(kRH * h + k, tl & 63)) = hv;
+          const uint16_t hv = f2h<kBf16>(pr);
+          const uint32_t off = sw128_offset(kRH * h + k, tl & 63);
+          *reinterpret_cast<uint16_t*>(pb + off) = hv;
+          if (kBf16) {
+            const float hf = h2f<true>(hv);
+            const uint16_t lv = f2h<true>(pr - hf);
+            lsum[k] += hf + h2f<true>(lv);
+            *reinterpret_cast<uint16_t*>(pb + kPBytes + off) = lv;
+          } else {
+            lsum[k] += h2f<false>(hv);
+          }
         }
         fence_proxy_async_smem();
       }
@@ -1079,10 +1098,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kBf16>
 cudaError_t prepare(int cluster) {
   static bool smem_set = false, np_set = false;
-  const void* fn = reinterpret_cast<const void*>(&mla_partial_tc128_kernel<kFp8>);
+  const void* fn = reinterpret_cast<const void*>(&mla_partial_tc128_kernel<kFp8, kBf16>);
   cudaError_t e = cudaSuccess;
   if (!smem_set) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
@@ -1099,13 +1118,15 @@ cudaError_t prepare(int cluster) {
 
 }  // namespace
 
-bool tc128_supports(int total_rows, bool bf16, int cluster) {
-  return total_rows <= kNR && !bf16 && cluster >= 2 && cluster <= 16 && (cluster & (cluster - 1)) == 0;
+bool tc128_supports(int total_rows, bool, int cluster) {
+  return total_rows <= kNR && cluster >= 2 && cluster <= 16 && (cluster & (cluster - 1)) == 0;
 }
 
 cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe_half, const PartialParams& p,
-                                 int num_chunks, int cluster, cudaStream_t stream) {
-  cudaError_t e = p.fp8 ? prepare<true>(cluster) : prepare<false>(cluster);
+                                 int num_chunks, int cluster, bool bf16, cudaStream_t stream) {
+  if (p.fp8 && bf16) return cudaErrorInvalidValue;  // E4M3 caches go with fp16 queries
+  cudaError_t e = p.fp8 ? prepare<true, false>(cluster)
+                  : bf16 ? prepare<false, true>(cluster) : prepare<false, false>(cluster);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster, num_chunks * (p.subs > 1 ? p.subs : 1), 1);
@@ -1121,13 +1142,14 @@ cudaError_t launch_partial_tc128(const CUtensorMap& tm_pages, const CUtensorMap&
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return p.fp8 ? cudaLaunchKernelEx(&cfg, mla_partial_tc128_kernel<true>, tm_pages, tm_kpe_half, p)
-               : cudaLaunchKernelEx(&cfg, mla_partial_tc128_kernel<false>, tm_pages, tm_kpe_half, p);
+  if (p.fp8) return cudaLaunchKernelEx(&cfg, mla_partial_tc128_kernel<true, false>, tm_pages, tm_kpe_half, p);
+  return bf16 ? cudaLaunchKernelEx(&cfg, mla_partial_tc128_kernel<false, true>, tm_pages, tm_kpe_half, p)
+              : cudaLaunchKernelEx(&cfg, mla_partial_tc128_kernel<false, false>, tm_pages, tm_kpe_half, p);
 }
 
 int tc128_max_active_clusters(int cluster) {
-  // both instances take the same threads, shared memory and (at most) registers
-  if (prepare<false>(cluster) != cudaSuccess) {
+  // every instance takes the same threads, shared memory and (at most) registers
+  if (prepare<false, false>(cluster) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1143,7 +1165,7 @@ int tc128_max_active_clusters(int cluster) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(&mla_partial_tc128_kernel<false>), &cfg) !=
+  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(&mla_partial_tc128_kernel<false, false>), &cfg) !=
       cudaSuccess) {
     cudaGetLastError();
     return 0;

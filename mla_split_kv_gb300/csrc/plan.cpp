@@ -109,7 +109,7 @@ extern "C" mla_status_t mla_plan(const int32_t* context_lens_host, int32_t B, in
     }
 
   Candidate best;
-  // 16 fp16 rows (or E4M3 caches) run on the paired kernel whenever the device has CTA pairs: a
+  // 16 rows run on the paired kernel whenever the device has CTA pairs: a
   // partition's tiles stream through three slots on two SMs, several times the 64-token kernel's
   // rate, so clusters of one are not candidates then (for a batch they would tie on busy CTAs)
   const bool paired_ok = mla::tc128_supports(rows, plan->dtype == MLA_BF16, 2) && dev->max_clusters[1] > 0;

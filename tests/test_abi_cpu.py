@@ -112,11 +112,11 @@ def test_plan_rejects_an_unknown_merge_path(lib):
 
 
 def test_plan_spreads_partitions_only_for_the_paired_kernel(lib):
-    # the paired kernel runs for 16 fp16 rows per CTA only: bf16 or 128 heads keep one cluster per partition
+    # the paired kernel runs for 16 rows per CTA (fp16 or bf16): 128 heads keep one cluster per partition
     p16 = nb.mla_plan([131072], 16, 1, 32, fake_gb300())
     assert p16.clusters_per_chunk > 1 and p16.cluster_ctas >= 2
     pb = nb.mla_plan([131072], 16, 1, 32, fake_gb300(), dtype="bf16")
-    assert pb.clusters_per_chunk == 1
+    assert (pb.chunks, pb.cluster_ctas, pb.clusters_per_chunk) == (p16.chunks, p16.cluster_ctas, p16.clusters_per_chunk)
     p128 = nb.mla_plan([131072], 128, 1, 32, fake_gb300())
     assert p128.clusters_per_chunk == 1
     # a short request in the batch caps k so that, when a partition is spread, every pair still gets a tile
@@ -141,8 +141,8 @@ def test_plan_for_e4m3_caches_keeps_pairs(lib, lens):
 
 
 @pytest.mark.parametrize("lens", [[8192] * 8, [8192] * 32, [1000] * 8, [40000, 3000, 0, 129]])
-def test_batch_plans_of_sixteen_fp16_rows_use_cta_pairs(lib, lens):
-    # a batch at H=16 fp16 runs on the paired kernel (clusters of 2 or more) whenever the device has pairs
+def test_batch_plans_of_sixteen_rows_use_cta_pairs(lib, lens):
+    # a batch at H=16 runs on the paired kernel (clusters of 2 or more) whenever the device has pairs
     plan = nb.mla_plan(lens, 16, 1, 32, fake_gb300())
     assert plan.cluster_ctas >= 2
     check_plan_tiles(plan, lens, 32)
@@ -150,9 +150,9 @@ def test_batch_plans_of_sixteen_fp16_rows_use_cta_pairs(lib, lens):
     # without pairs on the device: one CTA per partition
     plan1 = nb.mla_plan(lens, 16, 1, 32, fake_device(152, [152, 0, 0, 0, 0]))
     assert plan1.cluster_ctas == 1
-    # bf16 keeps the 64-token kernel's choice (the paired kernel is fp16 only)
+    # bf16 runs on the same pairs
     pb = nb.mla_plan(lens, 16, 1, 32, fake_gb300(), dtype="bf16")
-    assert pb.clusters_per_chunk == 1
+    assert pb.cluster_ctas >= 2
 
 
 def test_workspace_bytes(lib):
@@ -350,8 +350,6 @@ BIG = 1 << 40
     (dict(clusters_per_chunk=4, cluster_ctas=2, workspace=FAKE + 8, workspace_bytes=BIG), nb.MLA_ERR_INVALID_ARG),
     (dict(clusters_per_chunk=4, cluster_ctas=0, workspace=FAKE, workspace_bytes=BIG), nb.MLA_ERR_INVALID_ARG),
     (dict(clusters_per_chunk=4, cluster_ctas=1, workspace=FAKE, workspace_bytes=BIG), nb.MLA_ERR_UNSUPPORTED),
-    (dict(clusters_per_chunk=4, cluster_ctas=2, dtype=nb.MLA_BF16, workspace=FAKE, workspace_bytes=BIG),
-     nb.MLA_ERR_UNSUPPORTED),
     (dict(clusters_per_chunk=4, cluster_ctas=2, num_heads=64, workspace=FAKE, workspace_bytes=BIG),
      nb.MLA_ERR_UNSUPPORTED),
     (dict(clusters_per_chunk=4, cluster_ctas=2, kernel=nb.MLA_KERNEL_SIMT, workspace=FAKE, workspace_bytes=BIG),
@@ -428,7 +426,6 @@ def call_static(lib, d, P=2, ptrs=None):
 @pytest.mark.parametrize("kw,P", [
     (dict(clusters_per_chunk=4, cluster_ctas=0), 2),
     (dict(clusters_per_chunk=4, cluster_ctas=1), 2),
-    (dict(clusters_per_chunk=4, cluster_ctas=2, dtype=nb.MLA_BF16), 2),
     (dict(clusters_per_chunk=4, cluster_ctas=2, num_heads=64), 2),
     (dict(clusters_per_chunk=4, cluster_ctas=2, kernel=nb.MLA_KERNEL_SIMT), 2),
     (dict(clusters_per_chunk=17, cluster_ctas=2), 2),

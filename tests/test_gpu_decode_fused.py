@@ -103,12 +103,14 @@ def test_single_launch_equals_two_launches_at_every_bench_context(L):
     assert torch.equal(out32.to(torch.float16), fused[2])
 
 
-@pytest.mark.parametrize("C,bs,out_dtype", [(2, 16, "f32"), (4, 32, "f16"), (8, 64, "bf16"), (16, 32, "f32")])
-def test_single_launch_ragged_batch_with_empty_requests(C, bs, out_dtype):
+@pytest.mark.parametrize("C,bs,out_dtype,dtype", [(2, 16, "f32", "f16"), (4, 32, "f16", "f16"), (8, 64, "bf16", "f16"),
+                                                  (16, 32, "f32", "f16"), (2, 32, "f32", "bf16"), (4, 64, "bf16", "bf16")])
+def test_single_launch_ragged_batch_with_empty_requests(C, bs, out_dtype, dtype):
     """A batch of ragged requests (empty, one token, partial pages, several tiles) on the uniform split: the
     same bits as the two launches, the oracle on every head, an empty request merges to zeros."""
     lens = [0, 1, 31, 33, 127, 129, 1000, 4133]
-    case = gen.make_decode_case(31, lens, num_heads=16, block_size=bs, dtype="f16")
+    case = gen.make_decode_case(31, lens, num_heads=16, block_size=bs, dtype=dtype,
+                                latent_std=0.5 if dtype == "bf16" else 1.0)
     dc = rt.upload(case)
     P, B = 3, len(lens)
     ind = rt.uniform_indptr(B, P)
@@ -157,7 +159,7 @@ def test_single_launch_bitwise_reproducible_and_workspace_reused():
 
 
 @pytest.mark.parametrize("H,dtype,kernel", [(128, "bf16", nb.MLA_KERNEL_TC), (16, "f16", nb.MLA_KERNEL_SIMT),
-                                            (16, "bf16", nb.MLA_KERNEL_TC)])
+                                            (64, "f16", nb.MLA_KERNEL_TC)])
 def test_decode_without_the_fused_merge_is_the_two_launches(H, dtype, kernel):
     """Kernels without the fused merge: mla_decode enqueues the partial kernel and the merge kernel."""
     case = gen.make_decode_case(34, [3000, 700], num_heads=H, block_size=64 if dtype == "bf16" else 32, dtype=dtype,
@@ -389,3 +391,26 @@ def test_prefix_ready_after_the_cache_write_of_the_window():
     c2, k2 = orc.cache_append(case.ckv, case.kpe, case.block_table, case.context_lens, ckv_new, kpe_new, 32)
     ref, _ = orc.unsplit(dataclasses.replace(case, ckv=c2, kpe=k2))
     assert_close(out.cpu().numpy(), ref, "append then decode with prefix_ready")
+
+
+@pytest.mark.parametrize("L", [32768, 131072])
+def test_bf16_on_the_paired_kernel_planner_plan(L):
+    """bf16 at 16 rows runs on the paired kernel (probabilities as two bf16 terms): the planner's plan through
+    mla_decode's default and its single launch, against the oracle on sampled heads, the single launch the
+    same bits as the two ABI calls."""
+    case = gen.make_decode_case(41, [L], num_heads=16, block_size=32, dtype="bf16", latent_std=0.5)
+    dc = rt.upload(case)
+    plan = nb.mla_plan([L], 16, 1, 32, nb.mla_device_query(), dtype="bf16")
+    assert plan.cluster_ctas >= 2
+    chunks = rt.chunks_to_device(plan.chunks)
+    ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
+    nb.mla_reset_counters()
+    out, out_lse = default_decode(case, dc, plan, chunks, ind)
+    assert nb.mla_get_counters()[nb.CTR_PARTIAL_TC] == 1
+    heads = [0, 6, 15]
+    ref, ref_lse = orc.unsplit(case, heads=heads)
+    assert_close(out.cpu().numpy()[:, :, heads], ref[:, :, heads], f"bf16 pairs L={L}")
+    assert np.abs(out_lse.cpu().numpy()[:, :, heads] - ref_lse[:, :, heads]).max() <= MAX_ABS
+    fused, plain = both_paths(case, dc, chunks, ind, plan.num_chunks, nb.MLA_KERNEL_TC, plan.cluster_ctas,
+                              plan.clusters_per_chunk, "bf16", tables_ready=True)
+    assert_same_bits(fused, plain)
