@@ -26,7 +26,9 @@ chunk partials), `partial_kernel_alone` (the ABI's mla_decode_partial),
 L2 flush and the host planner's time per call), `trials` (median / min / max
 over five more K-step trials), `many_heads` (the many-head workload),
 `verify_windows`, `batch_grid`, `e4m3_caches` (the same sweep on 8-bit E4M3
-caches) and `bf16` (the same sweep in bf16). `--impl reference` times the oracle itself
+caches), `bf16` (the same sweep in bf16) and `layer_with_append_and_unembed`
+(the new token's cache write, the partial decode and the merge with the
+W_UV^T unembed at 32K and 131K). `--impl reference` times the oracle itself
 on the same workload; `--gpus N` without a launcher starts N ranks (one
 replica per GPU).
 """
@@ -743,6 +745,77 @@ def time_e4m3_sweep(nb, rt, torch, stream, dev, peak, reps=20, dtype="e4m3"):
                     "first tiles read early); caches 354 MB in all, > L2"}
 
 
+# the steps either side of attention: one new token written into its page (mla_cache_append), the
+# partial decode over the cache that now holds it (mla_decode_partial, the planner's plan for chunk
+# partials), then the merge with the W_UV^T unembed (mla_merge_unembed, v_head 128, fp16 weights)
+WRAP = "mla_layer_append_decode_unembed_B1_H16_fp16_bs32_vhead128"
+
+
+def time_wrap(nb, rt, torch, stream, dev, reps=20):
+    import numpy as np
+
+    from mla_split_kv_gb300 import inputs as gen
+
+    rows = []
+    for i, L in ((0, CONTEXTS[0]), (len(CONTEXTS) - 1, CONTEXTS[-1])):
+        case = make_case(i, L)
+        rng = np.random.default_rng(SEED + 77)
+        with torch.cuda.stream(stream):
+            dc = rt.upload(case)
+            new_c = rt.to_device_16(gen.to_bits(rng.standard_normal((1, 1, 512)), "f16"), "f16", "cuda")
+            new_k = rt.to_device_16(gen.to_bits(rng.standard_normal((1, 1, 64)), "f16"), "f16", "cuda")
+            w = rt.to_device_16(gen.to_bits(rng.standard_normal((H, 512, 128)) / 512 ** 0.5, "f16"), "f16", "cuda")
+            plan = nb.mla_plan([L], H, 1, BS, dev, merge_path=nb.MLA_MERGE_PARTIALS)
+            chunks = rt.chunks_to_device(plan.chunks)
+            ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
+            part, lse = rt.alloc_partials(plan.num_chunks, 1, H)
+            ws = rt.alloc_workspace(plan.num_chunks, plan.clusters_per_chunk, plan.cluster_ctas, 1, H)
+            desc = rt.make_desc(dc, chunks, nb.MLA_KERNEL_TC, plan.cluster_ctas, stream, plan.clusters_per_chunk, ws,
+                                tables_ready=True)
+            out = torch.empty((1, 1, H, 128), dtype=torch.float16, device="cuda")
+        s = stream.cuda_stream
+
+        def append():
+            nb.mla_cache_append(new_c.data_ptr(), new_k.data_ptr(), dc.block_table.data_ptr(),
+                                dc.context_lens.data_ptr(), 1, 1, BS, case.num_blocks, case.max_blocks, dc.ckv.data_ptr(),
+                                dc.kpe.data_ptr(), s)
+
+        def unembed():
+            nb.mla_merge_unembed(part.data_ptr(), lse.data_ptr(), ind.data_ptr(), 1, 1, H, w.data_ptr(), nb.MLA_F16,
+                                 128, out.data_ptr(), nb.MLA_F16, None, s)
+
+        def layer():
+            append()
+            rt.decode_partial(dc, part, lse, desc=desc)
+            unembed()
+
+        def timed(fn):
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    fn()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(reps):
+                    fn()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            with torch.cuda.stream(stream):
+                g.replay()
+                e[0].record(stream)
+                g.replay()
+                e[1].record(stream)
+            stream.synchronize()
+            return e[0].elapsed_time(e[1]) * 1e3 / reps
+
+        rows.append({"ctx": L, "us_per_call": round(timed(layer), 3), "append_us": round(timed(append), 3),
+                     "merge_unembed_us": round(timed(unembed), 3),
+                     "partials_plan": [plan.num_chunks, plan.cluster_ctas, plan.clusters_per_chunk]})
+        del dc
+    return {"workload": WRAP, "per_ctx": rows,
+            "note": "append_us and merge_unembed_us: each call alone, repeated in a graph (latency-bound: one "
+                    "token's 1152 bytes; 2 MB of W_UV^T and the partials)"}
+
+
 def run_ours(args, rank, world):
     import numpy as np
     import torch
@@ -1079,6 +1152,7 @@ def run_ours(args, rank, world):
     verify = time_verify_windows(nb, rt, torch, stream, tpk) if not args.skip_extra else None
     e4m3 = time_e4m3_sweep(nb, rt, torch, stream, dev, tpk["hbm_gbs"]) if not args.skip_extra else None
     bf16 = time_e4m3_sweep(nb, rt, torch, stream, dev, tpk["hbm_gbs"], dtype="bf16") if not args.skip_extra else None
+    wrap = time_wrap(nb, rt, torch, stream, dev) if not args.skip_extra else None
     grid = time_batch_grid(nb, rt, torch, stream) if not args.skip_extra else None
     st, code = nb.mla_check_device_errors(stream.cuda_stream)
     if st != nb.MLA_OK:
@@ -1126,6 +1200,7 @@ def run_ours(args, rank, world):
         "batch_grid": grid,
         "e4m3_caches": e4m3,
         "bf16": bf16,
+        "layer_with_append_and_unembed": wrap,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(kname, sum(CONTEXTS) / len(CONTEXTS)),

@@ -490,15 +490,18 @@ mla_status_t mla_cache_append(const void* ckv_new, const void* kpe_new, const in
  * "[kernel] Wire MLA split-KV decode", *Bench*: the wrapper's unembed):
  *   out_v[b, i, h, :] = merged[b, i, h, :] @ W_UV^T[h]
  * where merged is what mla_merge_states computes in fp32 (the same bits; it
- * is never rounded here), the product accumulates in fp32 over d = 0 .. 511
- * in that order, and the result is rounded once to out_dtype. out_lse (NULL
- * allowed) receives the merged LSE.
+ * is never rounded here), the product accumulates in fp32 in a fixed order
+ * (d in eight chunks of 64, each in order, the chunk sums added in order),
+ * and the result is rounded once to out_dtype. out_lse (NULL allowed)
+ * receives the merged LSE.
  *
  * w_uv_t : device [H, 512, v_head] of w_dtype (MLA_F16 / MLA_BF16), 16-byte
  *          aligned; v_head a multiple of 32, at most 512
  * out    : device [B, q_len, H, v_head] of out_dtype (MLA_F16 / BF16 / F32)
  * partials, lse, o_indptr: as for mla_merge_states
- * A programmatic dependent launch, like mla_merge_states.
+ * A programmatic dependent launch, like mla_merge_states; w_uv_t (a weight) is
+ * read while the kernel before it in the stream finishes, so that kernel must
+ * not write it.
  */
 mla_status_t mla_merge_unembed(const float* partials, const float* lse, const int32_t* o_indptr, int32_t B,
                                int32_t q_len, int32_t num_heads, const void* w_uv_t, int32_t w_dtype, int32_t v_head,

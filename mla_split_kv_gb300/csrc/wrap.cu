@@ -11,11 +11,19 @@
 //    64 rope values (1152 bytes, 16-byte pieces) to the token's physical cache
 //    row. A pure copy: HBM-bound, 2 x 1152 bytes per token.
 //  - mla_merge_unembed_kernel: per (head, 32 value columns, 16 rows of that
-//    head) one CTA merges the rows' partials over all 512 latent columns (the
-//    merge kernel's arithmetic, so the fp32 latent is the bits mla_merge_states
-//    would give, never rounded), stages them and the head's W_UV^T slice
-//    [512 x 32] in shared memory, and takes the product in fp32 in a fixed
-//    order (d = 0 .. 511), rounded once to the output type.
+//    head) one CTA merges the rows' partials over all 512 latent columns in the
+//    merge kernel's arithmetic (so the fp32 latent is the bits
+//    mla_merge_states would give, never rounded): each warp takes the LSE
+//    maximum, the weights and their sum of two rows, the weights go to shared
+//    memory in pieces of 128 partials, and each thread sums its two latent
+//    columns over the partials in order with 32 loads in flight (the first
+//    round issued before the maxima are known). The head's W_UV^T slice
+//    [512 x 32] is staged while the preceding kernel finishes, each warp
+//    keeping its 64 rows of it in registers; the product runs in fp32 in a
+//    fixed order (eight chunks of 64 d, each in order, one per warp, then the
+//    chunk sums in order) over the real rows only, rounded once to the output
+//    type. A single-token decode call is latency-bound here: a few dependent
+//    L2 round trips, not bytes.
 #include "device_common.cuh"
 
 namespace mla {
@@ -49,66 +57,208 @@ __global__ void __launch_bounds__(kAppendWarps * 32) mla_cache_append_kernel(con
 constexpr int kUnThreads = 256;
 constexpr int kUnRows = 16;  // rows of one head per CTA
 constexpr int kUnCols = 32;  // value columns per CTA
-constexpr uint32_t kUnSmem = kUnRows * kRank * 4 + kRank * kUnCols * 2;  // latent rows + W slice: 64 KB
+constexpr int kUnChunks = kUnThreads / 32;  // the d range in 8 chunks of 64, one per warp
+constexpr int kUnDper = kRank / kUnChunks;  // d values per chunk
+constexpr uint32_t kUnPartOff = kUnRows * kRank * 4 + kRank * kUnCols * 2;  // after the latent rows + W slice
+constexpr int kUnPiece = 128;  // partial weights held in shared memory at a time, per row
+constexpr int kUnDepth = 32;   // partial values a thread has in flight
+constexpr uint32_t kUnWgtOff = kUnPartOff + kUnChunks * kUnRows * kUnCols * 4;  // after the chunk sums
+constexpr uint32_t kUnRowOff = kUnWgtOff + kUnRows * kUnPiece * 4;             // after the weights
+constexpr uint32_t kUnSmem = kUnRowOff + 5 * kUnRows * 4;  // + each row's range, slot row, sum, maximum: 88.3 KB
+static_assert(kRank / 2 == kUnThreads, "one thread per pair of latent columns");
+static_assert(kUnPiece % 32 == 0, "whole warps of weights");
+static_assert(kRank * 4 % kUnThreads == 0, "whole 16-byte pieces of the W slice per thread");
 
 template <bool BF16>
 __global__ void __launch_bounds__(kUnThreads) mla_merge_unembed_kernel(const UnembedParams p) {
   extern __shared__ uint8_t smem_raw[];
   float* lat = reinterpret_cast<float*>(smem_raw);                          // [16][512] fp32
   uint16_t* wsl = reinterpret_cast<uint16_t*>(smem_raw + kUnRows * kRank * 4);  // [512][32] 16-bit
-  pdl_wait();  // a programmatic dependent of the partial kernel: its partials are complete after this
-  pdl_launch_dependents();
   const int tid = threadIdx.x;
   const int h = blockIdx.x, vblk = blockIdx.y;
   const int rows_total = p.q_len * p.H;
   const int R = p.B * p.q_len;  // rows of head h
   const int rr0 = blockIdx.z * kUnRows;
   const int nrows = min(kUnRows, R - rr0);
-  // this head's W_UV^T columns [32 vblk, 32 vblk + 32): 512 rows of 64 bytes
+  // this head's W_UV^T columns [32 vblk, 32 vblk + 32): 512 rows of 64 bytes. The weights are no output
+  // of the preceding kernel: they are staged while it finishes, all of a thread's loads in flight at once
   const uint16_t* wsrc = p.w_uv_t + (static_cast<long long>(h) * kRank) * p.v_head + vblk * kUnCols;
-  for (int x = tid; x < kRank * 4; x += kUnThreads) {
-    const int d = x >> 2, q = x & 3;
-    reinterpret_cast<uint4*>(wsl + d * kUnCols)[q] =
-        *reinterpret_cast<const uint4*>(wsrc + static_cast<long long>(d) * p.v_head + q * 8);
-  }
-  // the merged latent of each row (row rr of head h = query row i of request b)
-  for (int x = tid; x < kUnRows * (kRank / 4) + kUnRows; x += kUnThreads) {
-    const bool is_lse = x >= kUnRows * (kRank / 4);
-    const int k = is_lse ? x - kUnRows * (kRank / 4) : x / (kRank / 4);
-    const int c = is_lse ? 0 : (x % (kRank / 4)) * 4;
-    if (k >= nrows) {
-      if (!is_lse) *reinterpret_cast<float4*>(lat + k * kRank + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-      continue;
+  {
+    constexpr int kPer = kRank * 4 / kUnThreads;  // 16-byte pieces per thread: 8
+    uint4 wv[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int x = tid + u * kUnThreads, d = x >> 2, q = x & 3;
+      wv[u] = *reinterpret_cast<const uint4*>(wsrc + static_cast<long long>(d) * p.v_head + q * 8);
     }
-    const int rr = rr0 + k, b = rr / p.q_len, i = rr % p.q_len;
-    const int lo = __ldg(p.o_indptr + b), hi = __ldg(p.o_indptr + b + 1);
-    float M, den;
-    const float4 acc = merge_cols4(p.partials, p.lse, lo, hi - lo, rows_total, i * p.H + h, c, !is_lse, &M, &den);
-    if (is_lse) {
-      if (p.out_lse != nullptr && vblk == 0) p.out_lse[static_cast<long long>(b) * rows_total + i * p.H + h] =
-          merged_lse(M, den);
-    } else {
-      *reinterpret_cast<float4*>(lat + k * kRank + c) = acc;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int x = tid + u * kUnThreads, d = x >> 2, q = x & 3;
+      reinterpret_cast<uint4*>(wsl + d * kUnCols)[q] = wv[u];
     }
   }
   __syncthreads();
-  // out_v[row][col] = sum_d lat[row][d] * W[d][col], d in order; warp w takes rows w and w + 8
   const int lane = tid & 31, w = tid >> 5;
-  float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 8
-  for (int d = 0; d < kRank; ++d) {
-    const float wv = h2f<BF16>(wsl[d * kUnCols + lane]);
-    acc0 = fmaf(lat[w * kRank + d], wv, acc0);
-    acc1 = fmaf(lat[(w + 8) * kRank + d], wv, acc1);
-  }
-  const int col = vblk * kUnCols + lane;
+  float wreg[kUnDper];  // W[64 w + dd][32 vblk + lane]
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int k = w + 8 * u;
-    if (k >= nrows) continue;
+  for (int dd = 0; dd < kUnDper; ++dd) wreg[dd] = h2f<BF16>(wsl[(w * kUnDper + dd) * kUnCols + lane]);
+  pdl_wait();  // a programmatic dependent of the partial kernel: its partials are complete after this
+  pdl_launch_dependents();
+  // the merged latent of each row (row rr of head h = query row i of request b), in the merge kernel's
+  // arithmetic: the maximum M of the row's partial LSE, weights 2^(lse_j - M) in partial order, the weighted
+  // values summed per column in partial order and divided by the weight sum. Thread tid owns latent columns
+  // 2 tid, 2 tid + 1 of every row; warp w takes rows w, w + 8 for the maxima, the weights and their sum.
+  int* row_lo = reinterpret_cast<int*>(smem_raw + kUnRowOff);
+  int* row_n = row_lo + kUnRows;
+  int* row_r = row_n + kUnRows;
+  float* row_den = reinterpret_cast<float*>(row_r + kUnRows);
+  float* row_m = row_den + kUnRows;
+  float* wgt = reinterpret_cast<float*>(smem_raw + kUnWgtOff);  // [16 rows][kUnPiece partials]
+  if (tid < nrows) {
+    const int rr = rr0 + tid, b = rr / p.q_len, i = rr % p.q_len;
+    const int lo = __ldg(p.o_indptr + b);
+    row_lo[tid] = lo;
+    row_n[tid] = __ldg(p.o_indptr + b + 1) - lo;
+    row_r[tid] = i * p.H + h;
+  }
+  __syncthreads();
+  const long long stride = static_cast<long long>(rows_total) * kRank;  // one partial slot
+  int nmax = 0;
+  for (int k = 0; k < nrows; ++k) nmax = max(nmax, row_n[k]);
+  float2 v[kUnDepth];
+  // values of partials k, j0 .. j0 + kUnDepth - 1 for this thread's columns, all loads in flight at once
+  auto load_values = [&](int k, int j0) {
+    const float* src = p.partials + static_cast<long long>(row_lo[k]) * stride +
+                       static_cast<long long>(row_r[k]) * kRank + 2 * tid;
+#pragma unroll
+    for (int jj = 0; jj < kUnDepth; ++jj)
+      v[jj] = (j0 + jj < row_n[k]) ? __ldcg(reinterpret_cast<const float2*>(src + (j0 + jj) * stride))
+                                   : make_float2(0.f, 0.f);
+  };
+  if (nrows > 0) load_values(0, 0);  // the first round goes out before the maxima are known
+  float m_of[2] = {-INFINITY, -INFINITY}, den_of[2] = {0.f, 0.f};  // rows w, w + 8
+  {
+    float l[2][kUnPiece / 32];
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int k = w + 8 * s;
+#pragma unroll
+      for (int t = 0; t < kUnPiece / 32; ++t) {
+        const int j = lane + 32 * t;
+        l[s][t] = (k < nrows && j < row_n[k])
+                      ? __ldcg(p.lse + static_cast<long long>(row_lo[k] + j) * rows_total + row_r[k])
+                      : -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int k = w + 8 * s;
+      if (k >= nrows) continue;
+      float m = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < kUnPiece / 32; ++t) m = fmaxf(m, l[s][t]);
+      for (int j = kUnPiece + lane; j < row_n[k]; j += 32)  // more partials than one piece holds
+        m = fmaxf(m, __ldcg(p.lse + static_cast<long long>(row_lo[k] + j) * rows_total + row_r[k]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      m_of[s] = m;
+#pragma unroll
+      for (int t = 0; t < kUnPiece / 32; ++t)
+        wgt[k * kUnPiece + lane + 32 * t] = (l[s][t] == -INFINITY) ? 0.f : exp2f(l[s][t] - m);
+    }
+  }
+  float2* lat2 = reinterpret_cast<float2*>(lat);
+  for (int j0 = 0; j0 < nmax; j0 += kUnPiece) {  // partials in pieces of kUnPiece weights
+    if (j0 > 0) {
+      __syncthreads();  // the previous piece's weights are no longer read
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        const int k = w + 8 * s;
+        if (k >= nrows) continue;
+#pragma unroll
+        for (int t = 0; t < kUnPiece / 32; ++t) {
+          const int j = j0 + lane + 32 * t;
+          const float lj = (j < row_n[k])
+                               ? __ldcg(p.lse + static_cast<long long>(row_lo[k] + j) * rows_total + row_r[k])
+                               : -INFINITY;
+          wgt[k * kUnPiece + lane + 32 * t] = (lj == -INFINITY) ? 0.f : exp2f(lj - m_of[s]);
+        }
+      }
+    }
+    __syncthreads();
+    for (int k = 0; k < nrows; ++k) {
+      const int cnt = min(kUnPiece, row_n[k] - j0);
+      if (cnt <= 0) continue;
+      float2 acc = (j0 == 0) ? make_float2(0.f, 0.f) : lat2[k * (kRank / 2) + tid];
+      for (int s0 = 0; s0 < cnt; s0 += kUnDepth) {
+        if (k != 0 || j0 != 0 || s0 != 0) load_values(k, j0 + s0);
+#pragma unroll
+        for (int jj = 0; jj < kUnDepth; ++jj) {
+          if (s0 + jj < cnt) {
+            const float wj = wgt[k * kUnPiece + s0 + jj];
+            acc.x = fmaf(wj, v[jj].x, acc.x);
+            acc.y = fmaf(wj, v[jj].y, acc.y);
+          }
+        }
+      }
+      lat2[k * (kRank / 2) + tid] = acc;
+    }
+    if (lane == 0) {  // the weight sums, in partial order
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        const int k = w + 8 * s;
+        if (k >= nrows) continue;
+        const int cnt = min(kUnPiece, row_n[k] - j0);
+        for (int j = 0; j < cnt; ++j) den_of[s] += wgt[k * kUnPiece + j];
+      }
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int k = w + 8 * s;
+      if (k >= nrows) continue;
+      row_den[k] = den_of[s];
+      row_m[k] = m_of[s];
+      if (p.out_lse != nullptr && vblk == 0) {
+        const int rr = rr0 + k, b = rr / p.q_len;
+        p.out_lse[static_cast<long long>(b) * rows_total + row_r[k]] = merged_lse(m_of[s], den_of[s]);
+      }
+    }
+  }
+  __syncthreads();
+  for (int k = 0; k < nrows; ++k) {
+    const float2 acc = lat2[k * (kRank / 2) + tid];
+    const float den = row_den[k];
+    lat2[k * (kRank / 2) + tid] =
+        (row_m[k] == -INFINITY) ? make_float2(0.f, 0.f) : make_float2(acc.x / den, acc.y / den);
+  }
+  __syncthreads();
+  // out_v[row][col] = sum_d lat[row][d] * W[d][col]: warp w sums d in [64 w, 64 w + 64) in order for each
+  // real row of the group (lane = column, its 64 weights in registers), into its chunk sums; the eight
+  // chunk sums are then added in chunk order.
+  float* part = reinterpret_cast<float*>(smem_raw + kUnPartOff);  // [8 chunks][16 rows][32 columns]
+  for (int k = 0; k < nrows; ++k) {
+    const float4* lrow = reinterpret_cast<const float4*>(lat + k * kRank + w * kUnDper);
+    float acc = 0.f;
+#pragma unroll
+    for (int q = 0; q < kUnDper / 4; ++q) {
+      const float4 l4 = lrow[q];
+      acc = fmaf(l4.x, wreg[4 * q + 0], acc);
+      acc = fmaf(l4.y, wreg[4 * q + 1], acc);
+      acc = fmaf(l4.z, wreg[4 * q + 2], acc);
+      acc = fmaf(l4.w, wreg[4 * q + 3], acc);
+    }
+    part[(w * kUnRows + k) * kUnCols + lane] = acc;
+  }
+  __syncthreads();
+  const int col = vblk * kUnCols + lane;
+  for (int k = w; k < nrows; k += kUnChunks) {  // warp w writes rows w, w + 8
+    float v = 0.f;
+#pragma unroll
+    for (int c = 0; c < kUnChunks; ++c) v += part[(c * kUnRows + k) * kUnCols + lane];
     const int rr = rr0 + k, b = rr / p.q_len, i = rr % p.q_len;
     const long long o = ((static_cast<long long>(b) * p.q_len + i) * p.H + h) * p.v_head + col;
-    const float v = u ? acc1 : acc0;
     if (p.out_dtype == 2)
       static_cast<float*>(p.out)[o] = v;
     else

@@ -160,3 +160,44 @@ def test_layer_call_append_decode_unembed():
     W = orc.decode16(w_bits, "f16")
     ref = np.stack([np.stack([orc.unembed(lat[b, 0][heads], W[heads])]) for b in range(2)])
     assert_close(ov.cpu().numpy()[:, :, heads], ref, "layer call")
+
+
+@pytest.mark.parametrize("counts,q_len,H", [
+    ([300, 0, 129, 1], 1, 16),   # more partials than one piece of weights, an empty request, a single partial
+    ([5, 140, 0, 64, 2] * 4, 2, 64),  # 40 rows of a head: two full row groups and a ragged one
+])
+def test_merge_unembed_many_partials(counts, q_len, H):
+    """Partials written straight into the buffers (no attention call): some requests with more than 128
+    partials, requests with none, and rows whose every partial is empty (LSE -inf)."""
+    rng = np.random.default_rng(50)
+    B, S = len(counts), sum(counts)
+    indptr = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    part_np = rng.standard_normal((S, q_len, H, 512)).astype(np.float32)
+    lse_np = (rng.standard_normal((S, q_len, H)) * 4.0).astype(np.float32)
+    lse_np[rng.random((S, q_len, H)) < 0.2] = -np.inf  # empty partials
+    lse_np[int(indptr[3]):int(indptr[4]), :, 1] = -np.inf  # request 3, head 1: every partial empty
+    part_np[np.isinf(lse_np)] = 0.0
+    part = torch.from_numpy(part_np).cuda()
+    lse = torch.from_numpy(lse_np).cuda()
+    ind = torch.from_numpy(indptr).cuda()
+    w_bits = unembed_weights(51, H, 64, "bf16")
+    w = rt.to_device_16(w_bits, "bf16", "cuda")
+    out = torch.empty((B, q_len, H, 64), dtype=torch.float32, device="cuda")
+    out_lse = torch.empty((B, q_len, H), dtype=torch.float32, device="cuda")
+    nb.mla_merge_unembed(part.data_ptr(), lse.data_ptr(), ind.data_ptr(), B, q_len, H, w.data_ptr(), nb.MLA_BF16,
+                         64, out.data_ptr(), nb.MLA_F32, out_lse.data_ptr(), None)
+    W = orc.decode16(w_bits, "bf16")
+    ref, ref_lse = orc.merge_unembed(part_np.astype(np.float64), lse_np.astype(np.float64), indptr, W)
+    assert_close(out.cpu().numpy(), ref, f"many partials B={B} q={q_len} H={H}")
+    got_lse = out_lse.cpu().numpy()
+    assert np.array_equal(np.isinf(got_lse), np.isinf(ref_lse))
+    fin = np.isfinite(ref_lse)
+    assert np.abs(got_lse[fin] - ref_lse[fin]).max() <= 1e-5 * max(1.0, np.abs(ref_lse[fin]).max())
+    # the merge kernel's own latent times W, and its LSE bit for bit
+    lat_lse = torch.empty_like(out_lse)
+    lat = rt.merge_states(part, lse, ind, B, q_len, H, "f32", out_lse=lat_lse).cpu().double().numpy()
+    prod = np.einsum("biHr,Hrv->biHv", lat, W)
+    assert np.abs(out.cpu().double().numpy() - prod).max() <= 1e-5 * max(1.0, np.abs(prod).max())
+    assert torch.equal(out_lse, lat_lse)
+    empty = [b for b in range(B) if counts[b] == 0]
+    assert empty and not out[empty].any() and not out[3, :, 1].any()  # no partials, or only empty ones: zero
