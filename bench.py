@@ -745,9 +745,9 @@ def time_e4m3_sweep(nb, rt, torch, stream, dev, peak, reps=20, dtype="e4m3"):
                     "first tiles read early); caches 354 MB in all, > L2"}
 
 
-# the steps either side of attention: one new token written into its page (mla_cache_append), the
-# partial decode over the cache that now holds it (mla_decode_partial, the planner's plan for chunk
-# partials), then the merge with the W_UV^T unembed (mla_merge_unembed, v_head 128, fp16 weights)
+# the steps either side of attention: one new token written into its page (mla_cache_append), then the
+# decode over the cache that now holds it with the W_UV^T unembed after it (mla_decode_unembed, v_head
+# 128, fp16 weights); beside it the same through chunk partials (mla_decode_partial + mla_merge_unembed)
 WRAP = "mla_layer_append_decode_unembed_B1_H16_fp16_bs32_vhead128"
 
 
@@ -773,6 +773,14 @@ def time_wrap(nb, rt, torch, stream, dev, reps=20):
             desc = rt.make_desc(dc, chunks, nb.MLA_KERNEL_TC, plan.cluster_ctas, stream, plan.clusters_per_chunk, ws,
                                 tables_ready=True)
             out = torch.empty((1, 1, H, 128), dtype=torch.float16, device="cuda")
+            # the default plan: pair entries merged and unembedded by one dependent launch
+            plan_d = nb.mla_plan([L], H, 1, BS, dev)
+            chunks_d = rt.chunks_to_device(plan_d.chunks)
+            ind_d = torch.tensor(plan_d.o_indptr, dtype=torch.int32, device="cuda")
+            part_d, lse_d = rt.alloc_partials(plan_d.num_chunks, 1, H)
+            ws_d = rt.alloc_decode_workspace(1, plan_d.num_chunks, plan_d.clusters_per_chunk, plan_d.cluster_ctas, 1, H)
+            desc_d = rt.make_desc(dc, chunks_d, nb.MLA_KERNEL_TC, plan_d.cluster_ctas, stream,
+                                  plan_d.clusters_per_chunk, ws_d, tables_ready=True, prefix_ready=True)
         s = stream.cuda_stream
 
         def append():
@@ -784,10 +792,14 @@ def time_wrap(nb, rt, torch, stream, dev, reps=20):
             nb.mla_merge_unembed(part.data_ptr(), lse.data_ptr(), ind.data_ptr(), 1, 1, H, w.data_ptr(), nb.MLA_F16,
                                  128, out.data_ptr(), nb.MLA_F16, None, s)
 
-        def layer():
+        def layer_partials():
             append()
             rt.decode_partial(dc, part, lse, desc=desc)
             unembed()
+
+        def layer():
+            append()
+            rt.decode_unembed(dc, part_d, lse_d, ind_d, w, out, desc=desc_d)
 
         def timed(fn):
             with torch.cuda.stream(stream):
@@ -807,12 +819,17 @@ def time_wrap(nb, rt, torch, stream, dev, reps=20):
             stream.synchronize()
             return e[0].elapsed_time(e[1]) * 1e3 / reps
 
-        rows.append({"ctx": L, "us_per_call": round(timed(layer), 3), "append_us": round(timed(append), 3),
-                     "merge_unembed_us": round(timed(unembed), 3),
+        rows.append({"ctx": L, "us_per_call": round(timed(layer), 3),
+                     "plan": [plan_d.num_chunks, plan_d.cluster_ctas, plan_d.clusters_per_chunk],
+                     "us_per_call_chunk_partials": round(timed(layer_partials), 3),
+                     "append_us": round(timed(append), 3), "merge_unembed_us": round(timed(unembed), 3),
                      "partials_plan": [plan.num_chunks, plan.cluster_ctas, plan.clusters_per_chunk]})
         del dc
     return {"workload": WRAP, "per_ctx": rows,
-            "note": "append_us and merge_unembed_us: each call alone, repeated in a graph (latency-bound: one "
+            "note": "us_per_call: mla_cache_append + mla_decode_unembed (the planner's default plan, pair entries "
+                    "merged and unembedded by one dependent launch, prefix_ready); us_per_call_chunk_partials: "
+                    "mla_cache_append + mla_decode_partial (a plan for chunk partials) + mla_merge_unembed; "
+                    "append_us and merge_unembed_us: each call alone, repeated in a graph (latency-bound: one "
                     "token's 1152 bytes; 2 MB of W_UV^T and the partials)"}
 
 

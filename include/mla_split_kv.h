@@ -476,7 +476,11 @@ uint64_t mla_decode_workspace_bytes(int32_t num_requests, int32_t num_chunks, in
  * kpe_new  : device [B, q_len, 64]  16-bit, 16-byte aligned
  * block_table, context_lens: as for mla_decode_partial
  * ckv_cache, kpe_cache: device, as for mla_decode_partial (written)
- * Returns MLA_OK once the copy kernel is enqueued.
+ * Returns MLA_OK once the copy kernel is enqueued. A programmatic dependent
+ * launch: it waits for the kernel before it in the stream to complete before
+ * reading anything, and lets the kernel after it start at once (every kernel
+ * of this library waits for it before reading what it writes; with
+ * prefix_ready the decode reads only rows before the window early).
  */
 mla_status_t mla_cache_append(const void* ckv_new, const void* kpe_new, const int32_t* block_table,
                               const int32_t* context_lens, int32_t B, int32_t q_len, int32_t block_size,
@@ -506,6 +510,33 @@ mla_status_t mla_cache_append(const void* ckv_new, const void* kpe_new, const in
 mla_status_t mla_merge_unembed(const float* partials, const float* lse, const int32_t* o_indptr, int32_t B,
                                int32_t q_len, int32_t num_heads, const void* w_uv_t, int32_t w_dtype, int32_t v_head,
                                void* out, int32_t out_dtype, float* out_lse, void* stream);
+
+/*
+ * mla_decode_unembed -- a layer call's attention with the unembed after it:
+ * mla_decode's merged latent taken to the value space,
+ *   out_v[b, i, h, :] = merged[b, i, h, :] @ W_UV^T[h]
+ * ("feat(core): matrix-absorbed MLA decode over a compressed-latent KV cache",
+ * *What changed*: the output side of the fold, W_UV^T [1, H, r, v_head];
+ * "[kernel] Wire MLA split-KV decode", *Bench*: the wrapper unembeds the
+ * attention output).
+ *  - the paired kernel: every CTA pair writes its part to desc->workspace as
+ *    mla_decode does, then ONE programmatic dependent launch merges a
+ *    request's parts in the entries merge's arithmetic and order (its fp32
+ *    latent is the bits mla_decode writes with MLA_F32, never rounded here)
+ *    and takes the product with W_UV^T as mla_merge_unembed does. Only the
+ *    default way: MLA_ERR_UNSUPPORTED for MLA_DECODE_MERGE_TICKETS.
+ *  - other kernels: mla_decode_partial, then mla_merge_unembed.
+ * Arguments: those of mla_decode (o_indptr, partials, lse and desc alike,
+ * desc->workspace included), with w_uv_t, w_dtype, v_head, out_v and
+ * out_dtype as for mla_merge_unembed (out_v: device [B, q_len, H, v_head]);
+ * out_lse (NULL allowed) receives the merged LSE. Returns what mla_decode and
+ * mla_merge_unembed return for the same arguments.
+ */
+mla_status_t mla_decode_unembed(const void* q_absorbed, const void* q_pe, const void* ckv_cache, const void* kpe_cache,
+                                const int32_t* block_table, const int32_t* context_lens, float scale,
+                                int32_t num_partitions, float* partials, float* lse, const int32_t* o_indptr,
+                                const void* w_uv_t, int32_t w_dtype, int32_t v_head, void* out_v, int32_t out_dtype,
+                                float* out_lse, const mla_decode_desc_t* desc);
 
 /*
  * mla_check_device_errors -- synchronize `stream`, read and clear the device
@@ -554,7 +585,7 @@ mla_status_t mla_selfcheck(float* max_abs_err);
 #define MLA_CTR_REJECTED 3
 #define MLA_CTR_CTAS 4 /* CTAs launched by partial kernels */
 #define MLA_CTR_DECODE_FUSED 5 /* mla_decode calls that ran as one launch */
-#define MLA_CTR_WRAP 6 /* mla_cache_append and mla_merge_unembed launches */
+#define MLA_CTR_WRAP 6 /* mla_cache_append, mla_merge_unembed and mla_decode_unembed unembed launches */
 #define MLA_NUM_COUNTERS 7
 /* mla_get_counters -- copy min(n, MLA_NUM_COUNTERS) counters to out (host). */
 void mla_get_counters(uint64_t* out, int32_t n);

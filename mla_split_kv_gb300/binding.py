@@ -24,6 +24,7 @@ MLA_ERR_DEVICE_CHECK = 5
 MLA_ERR_CAPACITY = 6
 
 MLA_F16, MLA_BF16, MLA_F32, MLA_E4M3 = 0, 1, 2, 3
+MLA_MAX_Q_LEN = 32  # rows of a verify window per request, at most
 MLA_STATIC_WORKSPACE_BYTES = 4 * 1024 * 1024
 MLA_KERNEL_AUTO, MLA_KERNEL_SIMT, MLA_KERNEL_TC = 0, 1, 2
 MLA_MERGE_ENTRIES, MLA_MERGE_PARTIALS = 0, 1
@@ -125,6 +126,9 @@ def load() -> ctypes.CDLL:
     lib.mla_cache_append.restype = i32
     lib.mla_merge_unembed.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32, i32, vp, i32, vp, vp]
     lib.mla_merge_unembed.restype = i32
+    lib.mla_decode_unembed.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, i32, vp, vp, vp, vp, i32, i32, vp, i32,
+                                       vp, ctypes.POINTER(mla_decode_desc_t)]
+    lib.mla_decode_unembed.restype = i32
     lib.mla_merge_states.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32, vp, vp]
     lib.mla_merge_states.restype = i32
     lib.mla_check_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -242,6 +246,16 @@ def mla_decode(q_absorbed: int, q_pe: int, ckv_cache: int, kpe_cache: int, block
     _check(load().mla_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, ctypes.c_float(scale),
                              num_partitions, partials, lse, o_indptr, out, out_dtype, out_lse or None,
                              ctypes.byref(desc)), "mla_decode")
+
+
+def mla_decode_unembed(q_absorbed: int, q_pe: int, ckv_cache: int, kpe_cache: int, block_table: int,
+                       context_lens: int, scale: float, num_partitions: int, partials: int, lse: int, o_indptr: int,
+                       w_uv_t: int, w_dtype: int, v_head: int, out_v: int, out_dtype: int, out_lse: Optional[int],
+                       desc: mla_decode_desc_t) -> None:
+    _check(load().mla_decode_unembed(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens,
+                                     ctypes.c_float(scale), num_partitions, partials, lse, o_indptr, w_uv_t, w_dtype,
+                                     v_head, out_v, out_dtype, out_lse or None, ctypes.byref(desc)),
+           "mla_decode_unembed")
 
 
 def mla_decode_workspace_bytes(num_requests: int, num_chunks: int, clusters_per_chunk: int, cluster_ctas: int,

@@ -416,6 +416,45 @@ uint64_t mla_decode_workspace_bytes(int32_t num_requests, int32_t num_chunks, in
   return tickets + lse_copy + entries_ws_bytes(num_chunks, clusters_per_chunk, cluster_ctas, q_len, num_heads);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The paired kernel's default way: every CTA pair writes its unnormalized part (O, row maxima and
+// sums) to an entry of the workspace, laid out as mla_decode_workspace_bytes describes.
+struct PairEntries {
+  const float* o;   // [E, q_len, H, 512]
+  const float* ml;  // [E, 2, q_len, H, 2]
+  int32_t epc;      // entries per chunk
+};
+
+mla_status_t launch_pair_entries(const void* q_absorbed, const void* q_pe, const void* ckv_cache, const void* kpe_cache,
+                                 const int32_t* block_table, const int32_t* context_lens, float scale,
+                                 int32_t num_partitions, float* partials, float* lse, const mla_decode_desc_t* d,
+                                 int64_t N, PairEntries* out) {
+  const int rows_total = d->num_heads * d->q_len;
+  const int32_t C = launch_cluster(d, N);
+  const uint64_t head = round256(static_cast<uint64_t>(d->num_requests) * mla::kSliceTickets * 4) +
+                        round256(static_cast<uint64_t>(N) * rows_total * 4);  // the TICKETS way's blocks
+  const uint64_t need = head + entries_ws_bytes(N, d->clusters_per_chunk, C, d->q_len, d->num_heads);
+  if (d->workspace == nullptr || !aligned(d->workspace, 16) || d->workspace_bytes < need)
+    return reject(MLA_ERR_INVALID_ARG);
+  uint8_t* ws = static_cast<uint8_t*>(d->workspace) + head;
+  const int32_t k = d->clusters_per_chunk > 1 ? d->clusters_per_chunk : 1;
+  mla_status_t st = launch_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
+                                  num_partitions, partials, lse, d, N, ws, FusedMerge{}, true);
+  if (st != MLA_OK) return st;
+  const uint64_t entries = static_cast<uint64_t>(N) * k * (C / 2);
+  out->o = reinterpret_cast<const float*>(ws + round256(static_cast<uint64_t>(N) * 2 * 4));
+  out->ml = out->o + entries * rows_total * mla::kRank;
+  out->epc = k * (C / 2);
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 mla_status_t mla_decode(const void* q_absorbed, const void* q_pe, const void* ckv_cache, const void* kpe_cache,
                         const int32_t* block_table, const int32_t* context_lens, float scale, int32_t num_partitions,
                         float* partials, float* lse, const int32_t* o_indptr, void* out, int32_t out_dtype,
@@ -436,27 +475,19 @@ mla_status_t mla_decode(const void* q_absorbed, const void* q_pe, const void* ck
     // the paired kernel writes every CTA pair's part to the workspace and exits; the entries merge
     // kernel, a programmatic dependent launch resident beside it, combines a request's parts
     // straight into the output
-    const int32_t C = launch_cluster(d, N);
-    const uint64_t head = round256(static_cast<uint64_t>(d->num_requests) * mla::kSliceTickets * 4) +
-                          round256(static_cast<uint64_t>(N) * rows_total * 4);  // the TICKETS way's blocks
-    const uint64_t need = head + entries_ws_bytes(N, d->clusters_per_chunk, C, d->q_len, d->num_heads);
-    if (d->workspace == nullptr || !aligned(d->workspace, 16) || d->workspace_bytes < need)
-      return reject(MLA_ERR_INVALID_ARG);
-    uint8_t* ws = static_cast<uint8_t*>(d->workspace) + head;
-    const int32_t k = d->clusters_per_chunk > 1 ? d->clusters_per_chunk : 1;
-    mla_status_t st = launch_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
-                                    num_partitions, partials, lse, d, N, ws, FusedMerge{}, true);
+    PairEntries pe;
+    mla_status_t st = launch_pair_entries(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
+                                          num_partitions, partials, lse, d, N, &pe);
     if (st != MLA_OK) return st;
-    const uint64_t entries = static_cast<uint64_t>(N) * k * (C / 2);
     mla::EntryMergeParams mp;
-    mp.ws_partials = reinterpret_cast<const float*>(ws + round256(static_cast<uint64_t>(N) * 2 * 4));
-    mp.ws_lse = mp.ws_partials + entries * rows_total * mla::kRank;
+    mp.ws_partials = pe.o;
+    mp.ws_lse = pe.ml;
     mp.o_indptr = o_indptr;
     mp.out = out;
     mp.out_lse = out_lse;
     mp.B = d->num_requests;
     mp.rows = rows_total;
-    mp.epc = k * (C / 2);
+    mp.epc = pe.epc;
     mp.out_dtype = out_dtype;
     mp.tables_ready = d->tables_ready;
     if (mla::launch_merge_entries(mp, static_cast<cudaStream_t>(d->stream)) != cudaSuccess) {
@@ -496,6 +527,71 @@ mla_status_t mla_decode(const void* q_absorbed, const void* q_pe, const void* ck
   void* spread_ws = ws + tickets + round256(static_cast<uint64_t>(N) * rows_total * 4);
   return launch_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale, num_partitions,
                        partials, lse, d, N, spread_ws, fm);
+}
+
+mla_status_t mla_decode_unembed(const void* q_absorbed, const void* q_pe, const void* ckv_cache, const void* kpe_cache,
+                                const int32_t* block_table, const int32_t* context_lens, float scale,
+                                int32_t num_partitions, float* partials, float* lse, const int32_t* o_indptr,
+                                const void* w_uv_t, int32_t w_dtype, int32_t v_head, void* out_v, int32_t out_dtype,
+                                float* out_lse, const mla_decode_desc_t* d) {
+  int64_t N = 0;
+  const mla_status_t chk = check_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
+                                        num_partitions, partials, lse, d, false, &N);
+  if (chk != MLA_OK) return reject(chk);
+  if (o_indptr == nullptr || out_v == nullptr || w_uv_t == nullptr || !aligned(o_indptr, 4) || !aligned(out_v, 4) ||
+      !aligned(w_uv_t, 16) || (out_lse != nullptr && !aligned(out_lse, 4)))
+    return reject(MLA_ERR_INVALID_ARG);
+  if (v_head < 32 || v_head > 512 || v_head % 32 != 0) return reject(MLA_ERR_UNSUPPORTED);
+  if (w_dtype != MLA_F16 && w_dtype != MLA_BF16) return reject(MLA_ERR_UNSUPPORTED);
+  if (out_dtype != MLA_F16 && out_dtype != MLA_BF16 && out_dtype != MLA_F32) return reject(MLA_ERR_UNSUPPORTED);
+  if (static_cast<int64_t>(d->num_requests) * d->q_len > 65535LL * 16) return reject(MLA_ERR_UNSUPPORTED);
+  const int rows_total = d->num_heads * d->q_len;
+  const bool paired = d->kernel != MLA_KERNEL_SIMT &&
+                      mla::tc128_supports(rows_total, d->dtype == MLA_BF16, launch_cluster(d, N));
+  if (paired && d->decode_merge == MLA_DECODE_MERGE_TICKETS) return reject(MLA_ERR_UNSUPPORTED);
+  mla::UnembedParams up;
+  up.o_indptr = o_indptr;
+  up.w_uv_t = static_cast<const uint16_t*>(w_uv_t);
+  up.out = out_v;
+  up.out_lse = out_lse;
+  up.B = d->num_requests;
+  up.q_len = d->q_len;
+  up.H = d->num_heads;
+  up.v_head = v_head;
+  up.out_dtype = out_dtype;
+  up.tables_ready = d->tables_ready;
+  if (paired) {
+    // the paired kernel's pair entries, merged and unembedded by one programmatic dependent launch
+    PairEntries pe;
+    mla_status_t st = launch_pair_entries(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
+                                          num_partitions, partials, lse, d, N, &pe);
+    if (st != MLA_OK) return st;
+    up.partials = pe.o;
+    up.lse = pe.ml;
+    up.entries = 1;
+    up.epc = pe.epc;
+  } else {
+    // chunk partials, then their merge with the unembed
+    if (d->clusters_per_chunk > 1) {
+      const uint64_t need = mla_workspace_bytes(static_cast<int32_t>(N), d->clusters_per_chunk, d->cluster_ctas,
+                                                d->q_len, d->num_heads);
+      if (d->workspace == nullptr || !aligned(d->workspace, 16) || d->workspace_bytes < need)
+        return reject(MLA_ERR_INVALID_ARG);
+    }
+    mla_status_t st = launch_decode(q_absorbed, q_pe, ckv_cache, kpe_cache, block_table, context_lens, scale,
+                                    num_partitions, partials, lse, d, N, d->workspace, FusedMerge{});
+    if (st != MLA_OK) return st;
+    up.partials = partials;
+    up.lse = lse;
+    up.entries = 0;
+    up.epc = 1;
+  }
+  if (mla::launch_merge_unembed(up, w_dtype == MLA_BF16, static_cast<cudaStream_t>(d->stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  g_counters[MLA_CTR_WRAP].fetch_add(1, std::memory_order_relaxed);
+  return MLA_OK;
 }
 
 }  // extern "C"
@@ -668,6 +764,9 @@ mla_status_t mla_merge_unembed(const float* partials, const float* lse, const in
   p.H = num_heads;
   p.v_head = v_head;
   p.out_dtype = out_dtype;
+  p.entries = 0;
+  p.epc = 1;
+  p.tables_ready = 0;
   if (mla::launch_merge_unembed(p, w_dtype == MLA_BF16, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;

@@ -102,13 +102,16 @@ struct AppendParams {
 
 // Merge of each request's partials, then the unembed W_UV^T of each head.
 struct UnembedParams {
-  const float* partials;       // [N, q_len, H, 512]
-  const float* lse;            // [N, q_len, H]
+  const float* partials;       // [N, q_len, H, 512] normalized O, or [E, q_len, H, 512] pair entries' O
+  const float* lse;            // [N, q_len, H] log2 LSE, or [E, 2, q_len, H, 2] entries' (m, l)
   const int32_t* o_indptr;     // [B+1]
   const uint16_t* w_uv_t;      // [H, 512, v_head]
   void* out;                   // [B, q_len, H, v_head] of out_dtype
   float* out_lse;              // [B, q_len, H] or null
   int32_t B, q_len, H, v_head, out_dtype;
+  int32_t entries;             // 1: pair entries (epc per chunk), 0: chunk partials (epc 1)
+  int32_t epc;
+  int32_t tables_ready;        // o_indptr complete before the preceding kernel started: read before the wait
 };
 
 // Launchers return cudaSuccess or the launch error. grid.x = cluster of

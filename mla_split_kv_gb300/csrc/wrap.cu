@@ -33,6 +33,11 @@ namespace {
 constexpr int kAppendWarps = 4;
 
 __global__ void __launch_bounds__(kAppendWarps * 32) mla_cache_append_kernel(const AppendParams p) {
+  // the kernel after it (the layer call's decode) may start at once: it reads nothing this kernel writes
+  // before waiting for it to complete. This kernel waits for the one before it (which may produce the new
+  // tokens) before reading anything.
+  pdl_launch_dependents();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long tok = static_cast<long long>(blockIdx.x) * kAppendWarps + warp;  // b * q_len + i
   if (tok >= static_cast<long long>(p.B) * p.q_len) return;
@@ -63,23 +68,47 @@ constexpr uint32_t kUnPartOff = kUnRows * kRank * 4 + kRank * kUnCols * 2;  // a
 constexpr int kUnPiece = 128;  // partial weights held in shared memory at a time, per row
 constexpr int kUnDepth = 32;   // partial values a thread has in flight
 constexpr uint32_t kUnWgtOff = kUnPartOff + kUnChunks * kUnRows * kUnCols * 4;  // after the chunk sums
-constexpr uint32_t kUnRowOff = kUnWgtOff + kUnRows * kUnPiece * 4;             // after the weights
-constexpr uint32_t kUnSmem = kUnRowOff + 5 * kUnRows * 4;  // + each row's range, slot row, sum, maximum: 88.3 KB
+constexpr uint32_t kUnRowOff = kUnWgtOff + 2 * kUnRows * kUnPiece * 4;  // after the weights and sums l
+constexpr uint32_t kUnSmem = kUnRowOff + 5 * kUnRows * 4;  // + each row's range, slot row, sum, maximum: 96.3 KB
 static_assert(kRank / 2 == kUnThreads, "one thread per pair of latent columns");
 static_assert(kUnPiece % 32 == 0, "whole warps of weights");
 static_assert(kRank * 4 % kUnThreads == 0, "whole 16-byte pieces of the W slice per thread");
 
-template <bool BF16>
-__global__ void __launch_bounds__(kUnThreads) mla_merge_unembed_kernel(const UnembedParams p) {
+// Two sources of a row's parts: chunk partials (normalized O with its log2 LSE; the merge is
+// mla_merge_states' arithmetic, one chain per column in partial order) or the paired kernel's pair
+// entries (unnormalized O with the pair's row maximum m and sum l relative to m; the merge is the
+// entries merge's arithmetic: eight groups of entries, entry e in group (e - first) mod 8, each group
+// summed in order, then the groups added as ((0+1)+(2+3))+((4+5)+(6+7))). Either way the fp32
+// latent is the bits the stand-alone merge writes.
+template <bool BF16, bool kEntries>
+__global__ void __launch_bounds__(kUnThreads, 1) mla_merge_unembed_kernel(const UnembedParams p) {
   extern __shared__ uint8_t smem_raw[];
   float* lat = reinterpret_cast<float*>(smem_raw);                          // [16][512] fp32
   uint16_t* wsl = reinterpret_cast<uint16_t*>(smem_raw + kUnRows * kRank * 4);  // [512][32] 16-bit
-  const int tid = threadIdx.x;
+  int* row_lo = reinterpret_cast<int*>(smem_raw + kUnRowOff);
+  int* row_n = row_lo + kUnRows;
+  int* row_r = row_n + kUnRows;
+  float* row_den = reinterpret_cast<float*>(row_r + kUnRows);
+  float* row_m = row_den + kUnRows;
+  float* wgt = reinterpret_cast<float*>(smem_raw + kUnWgtOff);  // [16 rows][kUnPiece] weights
+  float* lsum = wgt + kUnRows * kUnPiece;                        // [16 rows][kUnPiece] entries' sums l
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int h = blockIdx.x, vblk = blockIdx.y;
   const int rows_total = p.q_len * p.H;
   const int R = p.B * p.q_len;  // rows of head h
   const int rr0 = blockIdx.z * kUnRows;
   const int nrows = min(kUnRows, R - rr0);
+  // each row's parts: slots lo .. lo + n - 1 (row rr of head h = query row i of request b)
+  auto row_ranges = [&]() {
+    if (tid < nrows) {
+      const int rr = rr0 + tid, b = rr / p.q_len, i = rr % p.q_len;
+      const int lo = __ldg(p.o_indptr + b) * p.epc;
+      row_lo[tid] = lo;
+      row_n[tid] = __ldg(p.o_indptr + b + 1) * p.epc - lo;
+      row_r[tid] = i * p.H + h;
+    }
+  };
+  if (p.tables_ready) row_ranges();  // the offsets were complete before the preceding kernel started
   // this head's W_UV^T columns [32 vblk, 32 vblk + 32): 512 rows of 64 bytes. The weights are no output
   // of the preceding kernel: they are staged while it finishes, all of a thread's loads in flight at once
   const uint16_t* wsrc = p.w_uv_t + (static_cast<long long>(h) * kRank) * p.v_head + vblk * kUnCols;
@@ -98,35 +127,25 @@ __global__ void __launch_bounds__(kUnThreads) mla_merge_unembed_kernel(const Une
     }
   }
   __syncthreads();
-  const int lane = tid & 31, w = tid >> 5;
   float wreg[kUnDper];  // W[64 w + dd][32 vblk + lane]
 #pragma unroll
   for (int dd = 0; dd < kUnDper; ++dd) wreg[dd] = h2f<BF16>(wsl[(w * kUnDper + dd) * kUnCols + lane]);
-  pdl_wait();  // a programmatic dependent of the partial kernel: its partials are complete after this
+  pdl_wait();  // a programmatic dependent of the partial kernel: its parts are complete after this
   pdl_launch_dependents();
-  // the merged latent of each row (row rr of head h = query row i of request b), in the merge kernel's
-  // arithmetic: the maximum M of the row's partial LSE, weights 2^(lse_j - M) in partial order, the weighted
-  // values summed per column in partial order and divided by the weight sum. Thread tid owns latent columns
-  // 2 tid, 2 tid + 1 of every row; warp w takes rows w, w + 8 for the maxima, the weights and their sum.
-  int* row_lo = reinterpret_cast<int*>(smem_raw + kUnRowOff);
-  int* row_n = row_lo + kUnRows;
-  int* row_r = row_n + kUnRows;
-  float* row_den = reinterpret_cast<float*>(row_r + kUnRows);
-  float* row_m = row_den + kUnRows;
-  float* wgt = reinterpret_cast<float*>(smem_raw + kUnWgtOff);  // [16 rows][kUnPiece partials]
-  if (tid < nrows) {
-    const int rr = rr0 + tid, b = rr / p.q_len, i = rr % p.q_len;
-    const int lo = __ldg(p.o_indptr + b);
-    row_lo[tid] = lo;
-    row_n[tid] = __ldg(p.o_indptr + b + 1) - lo;
-    row_r[tid] = i * p.H + h;
-  }
+  if (!p.tables_ready) row_ranges();
   __syncthreads();
-  const long long stride = static_cast<long long>(rows_total) * kRank;  // one partial slot
-  int nmax = 0;
-  for (int k = 0; k < nrows; ++k) nmax = max(nmax, row_n[k]);
+  // the merged latent: thread tid owns latent columns 2 tid, 2 tid + 1 of every row; warp w takes rows
+  // w, w + 8 for the maxima, the weights and their sum
+  const long long stride = static_cast<long long>(rows_total) * kRank;  // one slot's values
+  // a part's (LSE, 0) or (m, l)
+  auto part_ml = [&](int k, int j) -> float2 {
+    if (kEntries)
+      return __ldcg(reinterpret_cast<const float2*>(p.lse + static_cast<long long>(row_lo[k] + j) * 4 * rows_total +
+                                                    row_r[k] * 2));
+    return make_float2(__ldcg(p.lse + static_cast<long long>(row_lo[k] + j) * rows_total + row_r[k]), 0.f);
+  };
   float2 v[kUnDepth];
-  // values of partials k, j0 .. j0 + kUnDepth - 1 for this thread's columns, all loads in flight at once
+  // values of parts k, j0 .. j0 + kUnDepth - 1 for this thread's columns, all loads in flight at once
   auto load_values = [&](int k, int j0) {
     const float* src = p.partials + static_cast<long long>(row_lo[k]) * stride +
                        static_cast<long long>(row_r[k]) * kRank + 2 * tid;
@@ -136,18 +155,39 @@ __global__ void __launch_bounds__(kUnThreads) mla_merge_unembed_kernel(const Une
                                    : make_float2(0.f, 0.f);
   };
   if (nrows > 0) load_values(0, 0);  // the first round goes out before the maxima are known
-  float m_of[2] = {-INFINITY, -INFINITY}, den_of[2] = {0.f, 0.f};  // rows w, w + 8
+  // the weights (and the entries' sums) of parts j0 .. j0 + kUnPiece - 1 of row k, by one warp
+  auto put_weights = [&](int k, int j0, float m, const float2* ml) {
+#pragma unroll
+    for (int t = 0; t < kUnPiece / 32; ++t) {
+      const int jj = lane + 32 * t;
+      const float2 x = (ml != nullptr) ? ml[t] : ((j0 + jj < row_n[k]) ? part_ml(k, j0 + jj) : make_float2(-INFINITY, 0.f));
+      wgt[k * kUnPiece + jj] = (x.x == -INFINITY) ? 0.f : exp2f(x.x - m);
+      if (kEntries) lsum[k * kUnPiece + jj] = (j0 + jj < row_n[k]) ? x.y : 0.f;
+    }
+  };
+  // the weight sum over parts j0 .. j0 + cnt - 1 of row k, continuing `den` (eight group sums for entries)
+  auto add_den = [&](int k, int cnt, float* den) {
+    for (int j0 = 0; j0 < cnt; j0 += 8) {
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        if (j0 + g < cnt) {
+          if (kEntries)
+            den[g] = fmaf(wgt[k * kUnPiece + j0 + g], lsum[k * kUnPiece + j0 + g], den[g]);
+          else
+            den[0] += wgt[k * kUnPiece + j0 + g];
+        }
+      }
+    }
+  };
   {
-    float l[2][kUnPiece / 32];
+    float2 ml[2][kUnPiece / 32];
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const int k = w + 8 * s;
 #pragma unroll
       for (int t = 0; t < kUnPiece / 32; ++t) {
         const int j = lane + 32 * t;
-        l[s][t] = (k < nrows && j < row_n[k])
-                      ? __ldcg(p.lse + static_cast<long long>(row_lo[k] + j) * rows_total + row_r[k])
-                      : -INFINITY;
+        ml[s][t] = (k < nrows && j < row_n[k]) ? part_ml(k, j) : make_float2(-INFINITY, 0.f);
       }
     }
 #pragma unroll
@@ -156,82 +196,64 @@ __global__ void __launch_bounds__(kUnThreads) mla_merge_unembed_kernel(const Une
       if (k >= nrows) continue;
       float m = -INFINITY;
 #pragma unroll
-      for (int t = 0; t < kUnPiece / 32; ++t) m = fmaxf(m, l[s][t]);
-      for (int j = kUnPiece + lane; j < row_n[k]; j += 32)  // more partials than one piece holds
-        m = fmaxf(m, __ldcg(p.lse + static_cast<long long>(row_lo[k] + j) * rows_total + row_r[k]));
+      for (int t = 0; t < kUnPiece / 32; ++t) m = fmaxf(m, ml[s][t].x);
+      for (int j = kUnPiece + lane; j < row_n[k]; j += 32) m = fmaxf(m, part_ml(k, j).x);  // more than a piece
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      m_of[s] = m;
-#pragma unroll
-      for (int t = 0; t < kUnPiece / 32; ++t)
-        wgt[k * kUnPiece + lane + 32 * t] = (l[s][t] == -INFINITY) ? 0.f : exp2f(l[s][t] - m);
+      put_weights(k, 0, m, ml[s]);
+      if (lane == 0) row_m[k] = m;
     }
   }
+  __syncthreads();
   float2* lat2 = reinterpret_cast<float2*>(lat);
-  for (int j0 = 0; j0 < nmax; j0 += kUnPiece) {  // partials in pieces of kUnPiece weights
-    if (j0 > 0) {
-      __syncthreads();  // the previous piece's weights are no longer read
+  for (int k = 0; k < nrows; ++k) {
+    const int n = row_n[k];
+    float2 acc[kEntries ? 8 : 1];
 #pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        const int k = w + 8 * s;
-        if (k >= nrows) continue;
+    for (int g = 0; g < (kEntries ? 8 : 1); ++g) acc[g] = make_float2(0.f, 0.f);
+    float den[kEntries ? 8 : 1];
 #pragma unroll
-        for (int t = 0; t < kUnPiece / 32; ++t) {
-          const int j = j0 + lane + 32 * t;
-          const float lj = (j < row_n[k])
-                               ? __ldcg(p.lse + static_cast<long long>(row_lo[k] + j) * rows_total + row_r[k])
-                               : -INFINITY;
-          wgt[k * kUnPiece + lane + 32 * t] = (lj == -INFINITY) ? 0.f : exp2f(lj - m_of[s]);
-        }
+    for (int g = 0; g < (kEntries ? 8 : 1); ++g) den[g] = 0.f;
+    for (int j0 = 0; j0 < n; j0 += kUnPiece) {
+      if (j0 > 0) {  // a row with more parts than a piece: its next weights, by warp 0
+        __syncthreads();  // the row's previous weights are read
+        if (w == 0) put_weights(k, j0, row_m[k], nullptr);
+        __syncthreads();
       }
-    }
-    __syncthreads();
-    for (int k = 0; k < nrows; ++k) {
-      const int cnt = min(kUnPiece, row_n[k] - j0);
-      if (cnt <= 0) continue;
-      float2 acc = (j0 == 0) ? make_float2(0.f, 0.f) : lat2[k * (kRank / 2) + tid];
+      const int cnt = min(kUnPiece, n - j0);
       for (int s0 = 0; s0 < cnt; s0 += kUnDepth) {
         if (k != 0 || j0 != 0 || s0 != 0) load_values(k, j0 + s0);
 #pragma unroll
         for (int jj = 0; jj < kUnDepth; ++jj) {
           if (s0 + jj < cnt) {
             const float wj = wgt[k * kUnPiece + s0 + jj];
-            acc.x = fmaf(wj, v[jj].x, acc.x);
-            acc.y = fmaf(wj, v[jj].y, acc.y);
+            float2& a = acc[kEntries ? (jj & 7) : 0];
+            a.x = fmaf(wj, v[jj].x, a.x);
+            a.y = fmaf(wj, v[jj].y, a.y);
           }
         }
       }
-      lat2[k * (kRank / 2) + tid] = acc;
+      if (tid == 0) add_den(k, cnt, den);  // after this thread's loads are out
     }
-    if (lane == 0) {  // the weight sums, in partial order
-#pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        const int k = w + 8 * s;
-        if (k >= nrows) continue;
-        const int cnt = min(kUnPiece, row_n[k] - j0);
-        for (int j = 0; j < cnt; ++j) den_of[s] += wgt[k * kUnPiece + j];
-      }
+    float2 tot = acc[0];
+    float dtot = den[0];
+    if (kEntries) {
+      tot = make_float2(((acc[0].x + acc[1].x) + (acc[2].x + acc[3].x)) + ((acc[4].x + acc[5].x) + (acc[6].x + acc[7].x)),
+                        ((acc[0].y + acc[1].y) + (acc[2].y + acc[3].y)) + ((acc[4].y + acc[5].y) + (acc[6].y + acc[7].y)));
+      dtot = ((den[0] + den[1]) + (den[2] + den[3])) + ((den[4] + den[5]) + (den[6] + den[7]));
     }
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      const int k = w + 8 * s;
-      if (k >= nrows) continue;
-      row_den[k] = den_of[s];
-      row_m[k] = m_of[s];
-      if (p.out_lse != nullptr && vblk == 0) {
-        const int rr = rr0 + k, b = rr / p.q_len;
-        p.out_lse[static_cast<long long>(b) * rows_total + row_r[k]] = merged_lse(m_of[s], den_of[s]);
-      }
-    }
+    lat2[k * (kRank / 2) + tid] = tot;
+    if (tid == 0) row_den[k] = dtot;
   }
   __syncthreads();
+  if (tid < nrows && p.out_lse != nullptr && vblk == 0) {
+    const int rr = rr0 + tid, b = rr / p.q_len;
+    p.out_lse[static_cast<long long>(b) * rows_total + row_r[tid]] = merged_lse(row_m[tid], row_den[tid]);
+  }
   for (int k = 0; k < nrows; ++k) {
-    const float2 acc = lat2[k * (kRank / 2) + tid];
+    const float2 a = lat2[k * (kRank / 2) + tid];
     const float den = row_den[k];
-    lat2[k * (kRank / 2) + tid] =
-        (row_m[k] == -INFINITY) ? make_float2(0.f, 0.f) : make_float2(acc.x / den, acc.y / den);
+    lat2[k * (kRank / 2) + tid] = (row_m[k] == -INFINITY) ? make_float2(0.f, 0.f) : make_float2(a.x / den, a.y / den);
   }
   __syncthreads();
   // out_v[row][col] = sum_d lat[row][d] * W[d][col]: warp w sums d in [64 w, 64 w + 64) in order for each
@@ -272,18 +294,30 @@ cudaError_t launch_cache_append(const AppendParams& p, cudaStream_t stream) {
   const long long toks = static_cast<long long>(p.B) * p.q_len;
   const long long blocks = (toks + kAppendWarps - 1) / kAppendWarps;
   if (blocks <= 0) return cudaSuccess;
-  mla_cache_append_kernel<<<static_cast<unsigned>(blocks), kAppendWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kAppendWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_cache_append_kernel, p);
 }
 
 cudaError_t launch_merge_unembed(const UnembedParams& p, bool w_bf16, cudaStream_t stream) {
-  static bool smem_set[2] = {false, false};
-  const void* fn = w_bf16 ? reinterpret_cast<const void*>(&mla_merge_unembed_kernel<true>)
-                          : reinterpret_cast<const void*>(&mla_merge_unembed_kernel<false>);
-  if (!smem_set[w_bf16 ? 1 : 0]) {
-    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kUnSmem);
+  static bool smem_set[4] = {false, false, false, false};
+  const int inst = (w_bf16 ? 1 : 0) + (p.entries ? 2 : 0);
+  const void* fns[4] = {reinterpret_cast<const void*>(&mla_merge_unembed_kernel<false, false>),
+                        reinterpret_cast<const void*>(&mla_merge_unembed_kernel<true, false>),
+                        reinterpret_cast<const void*>(&mla_merge_unembed_kernel<false, true>),
+                        reinterpret_cast<const void*>(&mla_merge_unembed_kernel<true, true>)};
+  if (!smem_set[inst]) {
+    const cudaError_t e = cudaFuncSetAttribute(fns[inst], cudaFuncAttributeMaxDynamicSharedMemorySize, kUnSmem);
     if (e != cudaSuccess) return e;
-    smem_set[w_bf16 ? 1 : 0] = true;
+    smem_set[inst] = true;
   }
   const long long R = static_cast<long long>(p.B) * p.q_len;
   cudaLaunchConfig_t cfg = {};
@@ -297,8 +331,12 @@ cudaError_t launch_merge_unembed(const UnembedParams& p, bool w_bf16, cudaStream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return w_bf16 ? cudaLaunchKernelEx(&cfg, mla_merge_unembed_kernel<true>, p)
-                : cudaLaunchKernelEx(&cfg, mla_merge_unembed_kernel<false>, p);
+  switch (inst) {
+    case 0: return cudaLaunchKernelEx(&cfg, mla_merge_unembed_kernel<false, false>, p);
+    case 1: return cudaLaunchKernelEx(&cfg, mla_merge_unembed_kernel<true, false>, p);
+    case 2: return cudaLaunchKernelEx(&cfg, mla_merge_unembed_kernel<false, true>, p);
+    default: return cudaLaunchKernelEx(&cfg, mla_merge_unembed_kernel<true, true>, p);
+  }
 }
 
 cudaError_t wrap_read_clear_error(uint32_t* out) {

@@ -132,6 +132,25 @@ def decode(dc: DeviceCase, part: torch.Tensor, lse: torch.Tensor, o_indptr_dev: 
     return out
 
 
+def decode_unembed(dc: DeviceCase, part: torch.Tensor, lse: torch.Tensor, o_indptr_dev: torch.Tensor,
+                   w_uv_t: torch.Tensor, out_v: torch.Tensor, out_lse: Optional[torch.Tensor] = None,
+                   num_partitions: int = 1, desc: Optional[nb.mla_decode_desc_t] = None, **desc_kw) -> torch.Tensor:
+    """One decode layer call through mla_decode_unembed: attention, then W_UV^T [H, 512, v_head] per head."""
+    d = desc if desc is not None else make_desc(dc, desc_kw.get("chunks_dev"), desc_kw.get("kernel", nb.MLA_KERNEL_AUTO),
+                                                desc_kw.get("cluster", 0), desc_kw.get("stream"),
+                                                desc_kw.get("subs", 1), desc_kw.get("workspace"),
+                                                desc_kw.get("tables_ready", False), desc_kw.get("decode_merge", 0),
+                                                desc_kw.get("prefix_ready", False),
+                                                desc_kw.get("score_exchange", 0))
+    codes = {torch.float32: nb.MLA_F32, torch.float16: nb.MLA_F16, torch.bfloat16: nb.MLA_BF16}
+    nb.mla_decode_unembed(dc.q_abs.data_ptr(), dc.q_pe.data_ptr(), dc.ckv.data_ptr(), dc.kpe.data_ptr(),
+                          dc.block_table.data_ptr(), dc.context_lens.data_ptr(), float(dc.case.scale), num_partitions,
+                          part.data_ptr(), lse.data_ptr(), o_indptr_dev.data_ptr(), w_uv_t.data_ptr(),
+                          codes[w_uv_t.dtype], int(w_uv_t.shape[-1]), out_v.data_ptr(), codes[out_v.dtype],
+                          out_lse.data_ptr() if out_lse is not None else None, d)
+    return out_v
+
+
 def alloc_partials(num_slots: int, q_len: int, H: int, device="cuda"):
     part = torch.empty((num_slots, q_len, H, 512), dtype=torch.float32, device=device)
     lse = torch.empty((num_slots, q_len, H), dtype=torch.float32, device=device)

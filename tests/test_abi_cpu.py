@@ -493,3 +493,83 @@ def test_decode_workspace_layout():
     assert nb.mla_decode_workspace_bytes(3, 7, 5, 4, 1, 16) == 256 + 512 + entries(7, 5, 4, 16)
     assert entries(7, 5, 4, 16) == nb.mla_workspace_bytes(7, 5, 4, 1, 16)  # the spread layout, for k > 1
     assert nb.mla_decode_workspace_bytes(0, 7, 1, 16, 1, 16) == 0
+
+
+def call_decode_unembed(lib, d, P=2, o_indptr=FAKE, w=FAKE, w_dtype=nb.MLA_F16, v_head=128, out_v=FAKE,
+                        out_dtype=nb.MLA_F16, out_lse=None):
+    p = [FAKE] * 8
+    return lib.mla_decode_unembed(p[0], p[1], p[2], p[3], p[4], p[5], ctypes.c_float(0.07), P, p[6], p[7], o_indptr,
+                                  w, w_dtype, v_head, out_v, out_dtype, out_lse, ctypes.byref(d))
+
+
+@pytest.mark.parametrize("kw,args,want", [
+    (dict(cluster_ctas=2), dict(o_indptr=None), nb.MLA_ERR_INVALID_ARG),
+    (dict(cluster_ctas=2), dict(w=None), nb.MLA_ERR_INVALID_ARG),
+    (dict(cluster_ctas=2), dict(w=FAKE + 8), nb.MLA_ERR_INVALID_ARG),  # W_UV^T not 16-byte aligned
+    (dict(cluster_ctas=2), dict(out_v=None), nb.MLA_ERR_INVALID_ARG),
+    (dict(cluster_ctas=2), dict(out_v=FAKE + 2), nb.MLA_ERR_INVALID_ARG),
+    (dict(cluster_ctas=2), dict(out_lse=FAKE + 2), nb.MLA_ERR_INVALID_ARG),
+    (dict(cluster_ctas=2), dict(v_head=48), nb.MLA_ERR_UNSUPPORTED),
+    (dict(cluster_ctas=2), dict(v_head=544), nb.MLA_ERR_UNSUPPORTED),
+    (dict(cluster_ctas=2), dict(w_dtype=nb.MLA_F32), nb.MLA_ERR_UNSUPPORTED),
+    (dict(cluster_ctas=2), dict(out_dtype=7), nb.MLA_ERR_UNSUPPORTED),
+    (dict(cluster_ctas=2, num_heads=24), dict(), nb.MLA_ERR_UNSUPPORTED),
+    (dict(cluster_ctas=2), dict(), nb.MLA_ERR_INVALID_ARG),  # the paired kernel's entries need a workspace
+    (dict(cluster_ctas=2, decode_merge=1, workspace=FAKE, workspace_bytes=BIG), dict(), nb.MLA_ERR_UNSUPPORTED),
+    (dict(cluster_ctas=4, clusters_per_chunk=4), dict(), nb.MLA_ERR_INVALID_ARG),  # two launches, no workspace
+])
+def test_decode_unembed_rejects_before_launch(lib, kw, args, want):
+    nb.mla_reset_counters()
+    assert call_decode_unembed(lib, desc(**kw), 2, **args) == want
+    ctr = nb.mla_get_counters()
+    assert ctr[nb.CTR_REJECTED] == 1 and ctr[nb.CTR_PARTIAL_TC] == 0 and ctr[nb.CTR_PARTIAL_SIMT] == 0
+    assert ctr[nb.CTR_WRAP] == 0
+
+
+def call_merge_unembed(lib, partials=FAKE, B=2, q_len=1, H=16, w=FAKE, w_dtype=nb.MLA_F16, v_head=128, out=FAKE,
+                       out_dtype=nb.MLA_F16, out_lse=None):
+    return lib.mla_merge_unembed(partials, FAKE, FAKE, B, q_len, H, w, w_dtype, v_head, out, out_dtype, out_lse, None)
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(partials=None), nb.MLA_ERR_INVALID_ARG),
+    (dict(partials=FAKE + 4), nb.MLA_ERR_INVALID_ARG),
+    (dict(w=FAKE + 8), nb.MLA_ERR_INVALID_ARG),
+    (dict(out=FAKE + 2), nb.MLA_ERR_INVALID_ARG),
+    (dict(out_lse=FAKE + 1), nb.MLA_ERR_INVALID_ARG),
+    (dict(B=0), nb.MLA_ERR_INVALID_ARG),
+    (dict(H=24), nb.MLA_ERR_UNSUPPORTED),
+    (dict(q_len=nb.MLA_MAX_Q_LEN + 1), nb.MLA_ERR_UNSUPPORTED),
+    (dict(v_head=40), nb.MLA_ERR_UNSUPPORTED),
+    (dict(v_head=0), nb.MLA_ERR_UNSUPPORTED),
+    (dict(w_dtype=nb.MLA_E4M3), nb.MLA_ERR_UNSUPPORTED),
+    (dict(out_dtype=9), nb.MLA_ERR_UNSUPPORTED),
+    (dict(B=65535 * 16 + 1), nb.MLA_ERR_UNSUPPORTED),  # more row groups than a grid's z dimension holds
+])
+def test_merge_unembed_rejects_before_launch(lib, args, want):
+    nb.mla_reset_counters()
+    assert call_merge_unembed(lib, **args) == want
+    ctr = nb.mla_get_counters()
+    assert ctr[nb.CTR_REJECTED] == 1 and ctr[nb.CTR_WRAP] == 0
+
+
+def call_cache_append(lib, ckv_new=FAKE, B=2, q_len=1, bs=32, num_blocks=8, max_blocks=4, ckv=FAKE):
+    return lib.mla_cache_append(ckv_new, FAKE, FAKE, FAKE, B, q_len, bs, num_blocks, max_blocks, ckv, FAKE, None)
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(ckv_new=None), nb.MLA_ERR_INVALID_ARG),
+    (dict(ckv_new=FAKE + 8), nb.MLA_ERR_INVALID_ARG),
+    (dict(ckv=None), nb.MLA_ERR_INVALID_ARG),
+    (dict(B=0), nb.MLA_ERR_INVALID_ARG),
+    (dict(num_blocks=0), nb.MLA_ERR_INVALID_ARG),
+    (dict(max_blocks=0), nb.MLA_ERR_INVALID_ARG),
+    (dict(q_len=0), nb.MLA_ERR_UNSUPPORTED),
+    (dict(q_len=nb.MLA_MAX_Q_LEN + 1), nb.MLA_ERR_UNSUPPORTED),
+    (dict(bs=48), nb.MLA_ERR_UNSUPPORTED),
+])
+def test_cache_append_rejects_before_launch(lib, args, want):
+    nb.mla_reset_counters()
+    assert call_cache_append(lib, **args) == want
+    ctr = nb.mla_get_counters()
+    assert ctr[nb.CTR_REJECTED] == 1 and ctr[nb.CTR_WRAP] == 0

@@ -201,3 +201,68 @@ def test_merge_unembed_many_partials(counts, q_len, H):
     assert torch.equal(out_lse, lat_lse)
     empty = [b for b in range(B) if counts[b] == 0]
     assert empty and not out[empty].any() and not out[3, :, 1].any()  # no partials, or only empty ones: zero
+
+
+TDT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+@pytest.mark.parametrize("lens,H,dtype,v_head,P,C,k", [
+    ([32768], 16, "f16", 128, None, None, None),      # the planner's plan on the paired kernel (pair entries)
+    ([131072], 16, "bf16", 64, None, None, None),
+    ([700, 0, 5000, 64], 16, "f16", 256, 2, 2, 2),    # several requests, an empty one, spread partitions
+    ([200000], 16, "f16", 32, 16, 2, 9),              # 144 entries: more than one piece of weights
+    ([3000, 1200], 128, "bf16", 128, None, None, None),  # the 128-row kernel: chunk partials, then the merge
+])
+def test_decode_unembed_against_the_oracle_and_mla_decode(lens, H, dtype, v_head, P, C, k):
+    """mla_decode_unembed: the oracle's unembed of the exact attention on sampled heads; mla_decode's own fp32
+    latent times W to fp32 rounding, its LSE bit for bit; a 16-bit output that is the fp32 one rounded once."""
+    case = gen.make_decode_case(52, lens, num_heads=H, block_size=32, dtype=dtype, latent_std=0.5)
+    dc = rt.upload(case)
+    B = len(lens)
+    if P is None:
+        plan = nb.mla_plan(lens, H, 1, 32, nb.mla_device_query(), dtype=dtype)
+        N, C, k = plan.num_chunks, plan.cluster_ctas, plan.clusters_per_chunk
+        kw = dict(chunks_dev=rt.chunks_to_device(plan.chunks), cluster=C, subs=k)
+        ind = torch.tensor(plan.o_indptr, dtype=torch.int32, device="cuda")
+        nparts = 1
+    else:
+        N, nparts = B * P, P
+        kw = dict(cluster=C, subs=k)
+        ind = rt.uniform_indptr(B, P)
+    ws = rt.alloc_decode_workspace(B, N, k, C, 1, H)
+    kw.update(kernel=nb.MLA_KERNEL_TC, workspace=ws, tables_ready=True)
+    w_bits = unembed_weights(53, H, v_head, dtype)
+    w = rt.to_device_16(w_bits, dtype, "cuda")
+    W = orc.decode16(w_bits, dtype)
+    res = {}
+    for dt in ("f32", dtype):
+        part, lse = rt.alloc_partials(N, 1, H)
+        out_v = torch.full((B, 1, H, v_head), float("nan"), dtype=TDT[dt], device="cuda")
+        out_lse = torch.full((B, 1, H), float("nan"), device="cuda")
+        nb.mla_reset_counters()
+        rt.decode_unembed(dc, part, lse, ind, w, out_v, out_lse, num_partitions=nparts, **kw)
+        ctr = nb.mla_get_counters()
+        assert ctr[nb.CTR_PARTIAL_TC] == 1 and ctr[nb.CTR_WRAP] == 1 and ctr[nb.CTR_MERGE] == 0
+        res[dt] = (out_v, out_lse)
+    out_v, out_lse = res["f32"]
+    assert torch.equal(res[dtype][0], out_v.to(TDT[dtype])) and torch.equal(res[dtype][1], out_lse)
+    # mla_decode's fp32 latent on the same plan, times W
+    part, lse = rt.alloc_partials(N, 1, H)
+    lat = torch.empty((B, 1, H, 512), dtype=torch.float32, device="cuda")
+    lat_lse = torch.empty((B, 1, H), dtype=torch.float32, device="cuda")
+    rt.decode(dc, part, lse, ind, lat, lat_lse, num_partitions=nparts, **kw)
+    prod = np.einsum("biHr,Hrv->biHv", lat.cpu().double().numpy(), W)
+    assert np.abs(out_v.cpu().double().numpy() - prod).max() <= 1e-5 * max(1.0, np.abs(prod).max())
+    assert torch.equal(out_lse, lat_lse)
+    # the oracle on sampled heads
+    heads = [0, H // 2 - 1, H - 1]
+    ref_lat, ref_lse = orc.unsplit(case, heads=heads)
+    ref = np.stack([np.stack([orc.unembed(ref_lat[b, 0][heads], W[heads])]) for b in range(B)])
+    got = out_v.cpu().numpy()[:, :, heads]
+    live = [b for b, L in enumerate(lens) if L > 0]
+    assert_close(got[live], ref[live], f"decode+unembed {lens} H={H} {dtype}")
+    got_lse = out_lse.cpu().numpy()[:, :, heads]
+    assert np.abs(got_lse[live] - ref_lse[:, :, heads][live]).max() <= MAX_ABS
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert not out_v[b].any() and torch.all(torch.isneginf(out_lse[b]))
