@@ -73,6 +73,9 @@ def parse():
                     help="profiling case of the many-head workload: the 128-row kernel's partial-score exchange")
     ap.add_argument("--profile-cache", default="f16", choices=["f16", "e4m3"],
                     help="profiling case at --profile-ctx: the cache type (e4m3: 8-bit caches, scale 1/4)")
+    ap.add_argument("--profile-layer", action="store_true",
+                    help="profiling case at --profile-ctx: each call is the layer call with the cache write and the "
+                         "unembed (mla_cache_append + mla_decode_unembed, v_head 128)")
     ap.add_argument("--profile-split", default="",
                     help="profiling case: 'P,C' = a uniform split into P partitions on clusters of C CTAs instead of "
                          "the planner's plan")
@@ -576,13 +579,31 @@ def run_profile_case(args):
     out = torch.empty((1, 1, H, 512), dtype=torch.float16, device="cuda")
     k = plan.clusters_per_chunk if kernel != nb.MLA_KERNEL_SIMT else 1
     ws = rt.alloc_decode_workspace(1, plan.num_chunks, k, plan.cluster_ctas, 1, H)
+    if args.profile_layer:  # the layer call with its ends: cache write, decode, merge with the unembed
+        import numpy as np
+
+        from mla_split_kv_gb300 import inputs as gen
+
+        rng = np.random.default_rng(SEED + 77)
+        new_c = rt.to_device_16(gen.to_bits(rng.standard_normal((1, 1, 512)), "f16"), "f16", "cuda")
+        new_k = rt.to_device_16(gen.to_bits(rng.standard_normal((1, 1, 64)), "f16"), "f16", "cuda")
+        w = rt.to_device_16(gen.to_bits(rng.standard_normal((H, 512, 128)) / 512 ** 0.5, "f16"), "f16", "cuda")
+        out_v = torch.empty((1, 1, H, 128), dtype=torch.float16, device="cuda")
     for _ in range(args.launches):  # the bench's layer call: mla_decode's default (partial kernel + entries merge)
+        if args.profile_layer:
+            nb.mla_cache_append(new_c.data_ptr(), new_k.data_ptr(), dc.block_table.data_ptr(),
+                                dc.context_lens.data_ptr(), 1, 1, BS, case.num_blocks, case.max_blocks,
+                                dc.ckv.data_ptr(), dc.kpe.data_ptr(), None)
+            rt.decode_unembed(dc, part, lse, ind, w, out_v, num_partitions=num_partitions, kernel=kernel,
+                              cluster=plan.cluster_ctas, chunks_dev=chunks_dev, subs=k, workspace=ws,
+                              tables_ready=True, prefix_ready=True)
+            continue
         rt.decode(dc, part, lse, ind, out, num_partitions=num_partitions, kernel=kernel, cluster=plan.cluster_ctas,
                   chunks_dev=chunks_dev, subs=k, workspace=ws, tables_ready=True, prefix_ready=True)
     torch.cuda.synchronize()
     st, code = nb.mla_check_device_errors(None)
     print(json.dumps({"profile_ctx": L, "cache": args.profile_cache, "launches": args.launches,
-                      "partitions": plan.num_chunks,
+                      "layer_with_append_and_unembed": args.profile_layer, "partitions": plan.num_chunks,
                       "cluster": plan.cluster_ctas, "clusters_per_partition": k,
                       "kernel": partial_kernel_name(args.kernel, [plan]),
                       "device_status": st, "device_error": code}))
