@@ -212,6 +212,8 @@ TDT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
     ([700, 0, 5000, 64], 16, "f16", 256, 2, 2, 2),    # several requests, an empty one, spread partitions
     ([200000], 16, "f16", 32, 16, 2, 9),              # 144 entries: more than one piece of weights
     ([3000, 1200], 128, "bf16", 128, None, None, None),  # the 128-row kernel: chunk partials, then the merge
+    ([2000, 900], 64, "f16", 512, None, None, None),   # the largest v_head (16 blocks of 32 columns)
+    ([300 + 97 * b for b in range(20)], 16, "f16", 96, None, None, None),  # 20 rows a head: two row groups
 ])
 def test_decode_unembed_against_the_oracle_and_mla_decode(lens, H, dtype, v_head, P, C, k):
     """mla_decode_unembed: the oracle's unembed of the exact attention on sampled heads; mla_decode's own fp32
