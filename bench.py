@@ -69,7 +69,7 @@ def parse():
     ap.add_argument("--profile-verify", type=int, default=0,
                     help="profiling case: only --launches plain verify-window calls of this q_len, then exit")
     ap.add_argument("--launches", type=int, default=5)
-    ap.add_argument("--profile-exchange", default="f32", choices=["f32", "f16"],
+    ap.add_argument("--profile-exchange", default="f32", choices=["f32", "f16", "none", "exact"],
                     help="profiling case of the many-head workload: the 128-row kernel's partial-score exchange")
     ap.add_argument("--profile-cache", default="f16", choices=["f16", "e4m3"],
                     help="profiling case at --profile-ctx: the cache type (e4m3: 8-bit caches, scale 1/4)")
@@ -179,7 +179,8 @@ def make_many_heads_case(dtype="bf16"):
 
 def many_heads_call(nb, rt, torch, stream=None, exchange=0, dtype="bf16"):
     """Upload the many-head case, plan it, and return a closure doing one layer call (partial + merge kernels);
-    `exchange`: the 128-row kernel's partial-score exchange (0: fp32, the default; 1: fp16)."""
+    `exchange`: the 128-row kernel's score exchange (0: the exact default, no exchange on 16-bit caches; 1: fp16;
+    2: none; 3: fp32)."""
     case = make_many_heads_case(dtype)
     dev = nb.mla_device_query()
     plan = nb.mla_plan(case.context_lens.tolist(), MH_H, 1, MH_BS, dev, max_partitions=64, dtype=dtype)
@@ -650,7 +651,7 @@ def run_profile_many_heads(args):
 
     nbuild.build()
     nb.load()
-    call, plan, tokens = many_heads_call(nb, rt, torch, exchange=1 if args.profile_exchange == "f16" else 0)
+    call, plan, tokens = many_heads_call(nb, rt, torch, exchange={"exact": 0, "f16": 1, "none": 2, "f32": 3}[args.profile_exchange])
     for _ in range(args.launches):
         call()
     torch.cuda.synchronize()
@@ -683,19 +684,23 @@ def time_many_heads(nb, rt, torch, stream, reps=20):
         stream.synchronize()
         return e[0].elapsed_time(e[1]) * 1e3 / reps, plan, tokens
 
-    us, plan, tokens = timed(0)
+    us, plan, tokens = timed(0)  # the exact default: on 16-bit caches no partial scores cross the pair
     us16, _, _ = timed(1)
+    us32, _, _ = timed(3)
     us8, _, _ = timed(0, "e4m3")
     flops = tokens * MH_H * 2 * (576 + 512)
     return {"workload": MANY_HEADS, "us_per_call": round(us, 3), "partitions": plan.num_chunks,
             "cluster": plan.cluster_ctas, "tokens": tokens, "tflops": round(flops / (us * 1e-6) / 1e12, 1),
             "hbm_gbs": round(tokens * LATENT_BYTES_PER_TOKEN / (us * 1e-6) / 1e9, 1),
+            "fp32_exchange_us": round(us32, 3),
             "fp16_exchange_us": round(us16, 3),
             "fp16_exchange_tflops": round(flops / (us16 * 1e-6) / 1e12, 1),
             "e4m3_cache_us": round(us8, 3),
             "note": "a parity workload timed beside the headline one; repeats of one cache (323 MB, > L2); "
-                    "fp16_exchange: score_exchange = MLA_SCORE_EXCHANGE_F16; e4m3_cache: the same lengths over an "
-                    "E4M3 cache (scale 1/4) beside fp16 queries"}
+                    "us_per_call: the exact default (each CTA of a pair computes the full scores, nothing crosses "
+                    "the pair); fp32_exchange: score_exchange = MLA_SCORE_EXCHANGE_F32 (half the columns a CTA, "
+                    "fp32 partial scores exchanged); fp16_exchange: MLA_SCORE_EXCHANGE_F16; e4m3_cache: the same "
+                    "lengths over an E4M3 cache (scale 1/4) beside fp16 queries"}
 
 
 # the headline sweep with 8-bit E4M3 caches (576 bytes a token, power-of-two cache scale 1/4) beside fp16

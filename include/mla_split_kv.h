@@ -103,8 +103,10 @@ mla_status_t mla_device_query(int32_t device, mla_device_info_t* info);
 #define MLA_MERGE_PARTIALS 1
 
 /* mla_decode_desc_t.score_exchange */
-#define MLA_SCORE_EXCHANGE_F32 0
+#define MLA_SCORE_EXCHANGE_EXACT 0
 #define MLA_SCORE_EXCHANGE_F16 1
+#define MLA_SCORE_EXCHANGE_NONE 2
+#define MLA_SCORE_EXCHANGE_F32 3
 
 /* mla_decode_desc_t.decode_merge (see mla_decode) */
 #define MLA_DECODE_MERGE_ENTRIES 0
@@ -261,19 +263,30 @@ typedef struct {
                                  power of two. Other dtypes: ignored. Anything
                                  else (0, negative, NaN, out of range) with
                                  E4M3: INVALID_ARG.                            */
-  int32_t score_exchange;     /* the 128-row kernel (more than 16 rows): how the
-                                 two CTAs of a pair send each other their
-                                 partial scores. MLA_SCORE_EXCHANGE_F32 (0,
-                                 default): fp32, exact. MLA_SCORE_EXCHANGE_F16
-                                 (1): each CTA's partial dot product of a tile
-                                 is rounded once to fp16 (both CTAs add the
-                                 same rounded values, so they still agree),
-                                 halving the bytes that cross distributed
-                                 shared memory; the error this adds grows with
-                                 the scores' magnitude (|s| x 2^-12 per half,
-                                 before the softmax scale), so it is a caller's
-                                 choice. Other kernels ignore it. Other values:
-                                 INVALID_ARG.                                  */
+  int32_t score_exchange;     /* the 128-row kernel (more than 16 rows): what
+                                 the two CTAs of a pair send each other of
+                                 their scores. MLA_SCORE_EXCHANGE_EXACT (0,
+                                 default): exact; on 16-bit caches with at
+                                 least 128 rows nothing crosses (as NONE),
+                                 otherwise (64 rows, E4M3 caches) fp32
+                                 partial scores of the real rows (as F32).
+                                 MLA_SCORE_EXCHANGE_F16 (1): each CTA's partial
+                                 dot product of a tile is rounded once to fp16
+                                 (both CTAs add the same rounded values, so
+                                 they still agree), halving the bytes that
+                                 cross distributed shared memory; the error
+                                 this adds grows with the scores' magnitude
+                                 (|s| x 2^-12 per half, before the softmax
+                                 scale), so it is a caller's choice.
+                                 MLA_SCORE_EXCHANGE_NONE (2, 16-bit caches;
+                                 E4M3: UNSUPPORTED): each CTA computes the full
+                                 scores itself (part of the queries held in
+                                 tensor memory, two full-width tile slots).
+                                 MLA_SCORE_EXCHANGE_F32 (3): each CTA computes
+                                 the scores over its half of the columns and
+                                 the fp32 partial scores cross. The exact ways
+                                 differ only in the order of fp32 sums. Other
+                                 kernels ignore it. Other values: INVALID_ARG. */
 } mla_decode_desc_t;
 
 /*

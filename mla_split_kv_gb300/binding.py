@@ -29,7 +29,7 @@ MLA_STATIC_WORKSPACE_BYTES = 4 * 1024 * 1024
 MLA_KERNEL_AUTO, MLA_KERNEL_SIMT, MLA_KERNEL_TC = 0, 1, 2
 MLA_MERGE_ENTRIES, MLA_MERGE_PARTIALS = 0, 1
 MLA_DECODE_MERGE_ENTRIES, MLA_DECODE_MERGE_TICKETS = 0, 1
-MLA_SCORE_EXCHANGE_F32, MLA_SCORE_EXCHANGE_F16 = 0, 1
+MLA_SCORE_EXCHANGE_EXACT, MLA_SCORE_EXCHANGE_F16, MLA_SCORE_EXCHANGE_NONE, MLA_SCORE_EXCHANGE_F32 = 0, 1, 2, 3
 
 CTR_PARTIAL_SIMT, CTR_PARTIAL_TC, CTR_MERGE, CTR_REJECTED, CTR_CTAS, CTR_DECODE_FUSED, CTR_WRAP = range(7)
 NUM_COUNTERS = 7

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libmla_split_kv.so")
-SOURCES = ["api.cu", "merge.cu", "partial_simt.cu", "partial_tc.cu", "partial_tc128.cu", "partial_mh.cu", "plan.cpp", "selfcheck.cu", "wrap.cu"]
+SOURCES = ["api.cu", "merge.cu", "partial_simt.cu", "partial_tc.cu", "partial_tc128.cu", "partial_mh.cu", "partial_mh_nx.cu", "plan.cpp", "selfcheck.cu", "wrap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

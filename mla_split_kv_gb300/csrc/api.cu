@@ -214,13 +214,14 @@ mla_status_t check_decode(const void* q_absorbed, const void* q_pe, const void* 
     if (d->num_heads * d->q_len > 16 && d->cluster_ctas != 0 && d->cluster_ctas != 2) return MLA_ERR_UNSUPPORTED;
     const float cs = d->cache_scale;
     if (!(cs >= 0x1p-24f && cs <= 0x1p24f)) return MLA_ERR_INVALID_ARG;  // also NaN
+    if (d->score_exchange == MLA_SCORE_EXCHANGE_NONE) return MLA_ERR_UNSUPPORTED;  // 16-bit caches only
   }
   if (d->causal != 0 && d->causal != 1) return MLA_ERR_INVALID_ARG;
   if (d->tables_ready != 0 && d->tables_ready != 1) return MLA_ERR_INVALID_ARG;
   if (d->decode_merge != MLA_DECODE_MERGE_ENTRIES && d->decode_merge != MLA_DECODE_MERGE_TICKETS)
     return MLA_ERR_INVALID_ARG;
   if (d->prefix_ready != 0 && d->prefix_ready != 1) return MLA_ERR_INVALID_ARG;
-  if (d->score_exchange != MLA_SCORE_EXCHANGE_F32 && d->score_exchange != MLA_SCORE_EXCHANGE_F16)
+  if (d->score_exchange < MLA_SCORE_EXCHANGE_EXACT || d->score_exchange > MLA_SCORE_EXCHANGE_F32)
     return MLA_ERR_INVALID_ARG;
   if (d->prefix_ready == 1 && d->tables_ready != 1) return MLA_ERR_INVALID_ARG;
   if (d->kernel < MLA_KERNEL_AUTO || d->kernel > MLA_KERNEL_TC) return MLA_ERR_INVALID_ARG;
@@ -341,7 +342,15 @@ mla_status_t launch_decode(const void* q_absorbed, const void* q_pe, const void*
   p.causal = d->causal;
   p.tables_ready = d->tables_ready;
   p.prefix_ready = d->prefix_ready;
-  p.xchg16 = (d->score_exchange == MLA_SCORE_EXCHANGE_F16) ? 1 : 0;
+  // the 128-row kernel's pair: 0 fp32 partial scores cross, 1 fp16 ones, 2 none (each CTA computes the full
+  // scores). The exact default: none on 16-bit caches with a full group of 128 rows; with fewer rows (a
+  // 64-row group: half of each score product is padding) the fp32 exchange of the real rows' scores
+  // measured faster, and E4M3 caches have only that way
+  const bool full_group = d->num_heads * d->q_len >= 128;
+  p.xchg16 = (d->score_exchange == MLA_SCORE_EXCHANGE_F16)  ? 1
+             : (d->score_exchange == MLA_SCORE_EXCHANGE_F32) ? 0
+             : (d->score_exchange == MLA_SCORE_EXCHANGE_NONE) ? 2
+                                                              : ((d->dtype != MLA_E4M3 && full_group) ? 2 : 0);
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
 
   p.subs = subs;
@@ -777,12 +786,12 @@ mla_status_t mla_merge_unembed(const float* partials, const float* lse, const in
 
 mla_status_t mla_check_device_errors(void* stream, uint32_t* code_out) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
-  uint32_t a = 0, b = 0, c = 0, e = 0, f = 0;
+  uint32_t a = 0, b = 0, c = 0, e = 0, f = 0, g = 0;
   if (mla::simt_read_clear_error(&a) != cudaSuccess || mla::tc_read_clear_error(&b) != cudaSuccess ||
       mla::tc128_read_clear_error(&c) != cudaSuccess || mla::mh_read_clear_error(&e) != cudaSuccess ||
-      mla::wrap_read_clear_error(&f) != cudaSuccess)
+      mla::wrap_read_clear_error(&f) != cudaSuccess || mla::mh_nx_read_clear_error(&g) != cudaSuccess)
     return MLA_ERR_CUDA;
-  const uint32_t code = a | b | c | e | f;
+  const uint32_t code = a | b | c | e | f | g;
   if (code_out != nullptr) *code_out = code;
   if (code != 0 && !clear_static_workspace()) return MLA_ERR_CUDA;
   if (code & mla::MLA_DEVERR_TIMEOUT) return MLA_ERR_TIMEOUT;

@@ -39,7 +39,7 @@ struct PartialParams {
   int32_t fp8;                 // E4M3 caches (the paired kernel): loaded as bytes, converted to fp16 in the slot
   float cache_scale;           // E4M3: the value of byte x is e4m3(x) * cache_scale (folded into scale_log2 and O)
   int32_t prefix_ready;        // cache rows before each request's window may be read before the dependency wait
-  int32_t xchg16;              // the 128-row kernel: partial scores cross the pair as fp16
+  int32_t xchg16;              // the 128-row kernel: 1 partial scores cross the pair as fp16, 2 none cross
   uint64_t timeout_ns;
   // a chunk spread over `subs` clusters (the paired 16-row kernel): grid.y = chunks * subs.
   // One entry per CTA pair of a chunk (subs * cluster / 2 of them): its unnormalized O^T in
@@ -134,6 +134,10 @@ int tc128_max_active_clusters(int cluster);
 // 64-token-tile tensor-core kernel for groups of 128 rows (q_len * H > 16, the last group
 // padded), fp16 or bf16, each group on a cluster of one CTA pair that split the latent columns.
 bool mh_supports(int total_rows, int cluster);
+// The 128-row groups without a score exchange (xchg16 == 2): every CTA of a pair computes the full scores.
+cudaError_t launch_partial_mh_nx(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe_half, const PartialParams& p,
+                                 int num_chunks, bool bf16, cudaStream_t stream);
+cudaError_t mh_nx_read_clear_error(uint32_t* out);
 cudaError_t launch_partial_mh(const CUtensorMap& tm_pages, const CUtensorMap& tm_kpe_half, const PartialParams& p,
                               int num_chunks, bool bf16, cudaStream_t stream);
 

@@ -520,7 +520,9 @@ cudaError_t launch_partial_tc(const CUtensorMap& tm_ckv, const CUtensorMap& tm_k
   const int rows = p.q_len * p.H;
   if (tc128_supports(rows, bf16, cluster))
     return launch_partial_tc128(tm_pages, tm_kpe_half, p, num_chunks, cluster, bf16, stream);
-  if (mh_supports(rows, cluster)) return launch_partial_mh(tm_pages, tm_kpe_half, p, num_chunks, bf16, stream);
+  if (mh_supports(rows, cluster))
+    return (p.xchg16 == 2) ? launch_partial_mh_nx(tm_pages, tm_kpe_half, p, num_chunks, bf16, stream)
+                           : launch_partial_mh(tm_pages, tm_kpe_half, p, num_chunks, bf16, stream);
   const int nr = tc_rows_per_cta(rows, bf16);
   const void* fn = tc_kernel_ptr(nr, bf16);
   cudaError_t e = prepare(fn, nr, bf16, cluster);

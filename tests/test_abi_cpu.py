@@ -317,8 +317,9 @@ def call_partial(lib, d, P=2, ptrs=None):
     (dict(), 0, nb.MLA_ERR_INVALID_ARG),
     (dict(num_requests=40000), 2, nb.MLA_ERR_UNSUPPORTED),
     (dict(dtype=4, cluster_ctas=2), 2, nb.MLA_ERR_UNSUPPORTED),
-    (dict(score_exchange=2), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(score_exchange=4), 2, nb.MLA_ERR_INVALID_ARG),
     (dict(score_exchange=-1), 2, nb.MLA_ERR_INVALID_ARG),
+    (dict(score_exchange=2, dtype=nb.MLA_E4M3, cluster_ctas=2, cache_scale=1.0), 2, nb.MLA_ERR_UNSUPPORTED),
     # E4M3 caches: the paired 16-row kernel only, and a cache scale in [2^-24, 2^24]
     (dict(dtype=nb.MLA_E4M3, cache_scale=1.0), 2, nb.MLA_ERR_UNSUPPORTED),  # clusters of 1
     (dict(dtype=nb.MLA_E4M3, cluster_ctas=2, kernel=nb.MLA_KERNEL_SIMT, cache_scale=1.0), 2,

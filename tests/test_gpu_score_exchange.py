@@ -1,4 +1,6 @@
-"""The 128-row kernel with its partial scores exchanged as fp16 (score_exchange = MLA_SCORE_EXCHANGE_F16).
+"""The 128-row kernel's score exchange options: partial scores exchanged as fp16
+(score_exchange = MLA_SCORE_EXCHANGE_F16), and none exchanged (MLA_SCORE_EXCHANGE_NONE: each CTA of a
+pair computes the full scores, part of the queries in tensor memory).
 
 Each CTA of a pair rounds its partial dot product of a tile to fp16 once and
 both add the same rounded values, so they still take the same decisions. The
@@ -81,6 +83,37 @@ def test_fp16_exchange_against_the_oracle(H, q_len, dtype, bs, std, heads):
 def test_fp16_exchange_bitwise_repeatable():
     case = gen.make_decode_case(82, [7000, 2049], num_heads=128, block_size=64, dtype="bf16", latent_std=0.5)
     runs = [planned(case, nb.MLA_SCORE_EXCHANGE_F16) for _ in range(3)]
+    for other in runs[1:]:
+        for a, b in zip(runs[0], other):
+            assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("H,q_len,dtype,bs,std,heads,lens", [
+    (128, 1, "bf16", 64, 0.5, [0, 37, 64, 127], [9000, 2500, 130]),  # the many-head decode's shape
+    (128, 1, "f16", 16, 1.0, [0, 77, 127], [4099, 1, 2222]),          # block 16, a one-token request
+    (64, 1, "f16", 32, 1.0, [0, 21, 42, 63], [9000, 2500, 130]),      # a 64-row group: half its rows padding
+    (64, 2, "bf16", 32, 0.5, [0, 40, 63], [3000, 65]),                 # two window rows per request, causal
+    (16, 16, "f16", 32, 1.0, [0, 7, 15], [9000, 2500, 130]),           # a verify window of 16, causal
+    (16, 32, "f16", 64, 1.0, [0, 15], [6000, 777]),                    # 512 rows: four groups, causal
+])
+def test_no_exchange_against_the_oracle(H, q_len, dtype, bs, std, heads, lens):
+    """No exchange: exact (within the stated tolerance of the oracle, like the fp32 exchange) and within
+    fp32 rounding of the fp32 exchange's results (only the order of the 576-term sums differs)."""
+    case = gen.make_decode_case(83, lens, num_heads=H, q_len=q_len, block_size=bs, dtype=dtype, latent_std=std,
+                                causal=q_len > 1)
+    part, lse, out = planned(case, nb.MLA_SCORE_EXCHANGE_NONE)
+    ref, ref_lse = orc.unsplit(case, heads=heads)
+    assert_close(out.cpu().numpy()[:, :, heads], ref[:, :, heads], f"no exchange H={H} q_len={q_len} {dtype}")
+    # the two exact ways differ only by the order of fp32 sums: well inside the stated tolerance (a quarter)
+    part32, lse32, out32 = planned(case, nb.MLA_SCORE_EXCHANGE_F32)
+    assert (out - out32).abs().max().item() <= MAX_ABS / 4
+    live = torch.isfinite(lse32)
+    assert torch.equal(torch.isfinite(lse), live) and (lse - lse32)[live].abs().max().item() <= MAX_ABS / 4
+
+
+def test_no_exchange_bitwise_repeatable():
+    case = gen.make_decode_case(84, [7000, 2049], num_heads=128, block_size=64, dtype="bf16", latent_std=0.5)
+    runs = [planned(case, nb.MLA_SCORE_EXCHANGE_NONE) for _ in range(3)]
     for other in runs[1:]:
         for a, b in zip(runs[0], other):
             assert torch.equal(a, b)

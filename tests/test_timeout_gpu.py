@@ -64,7 +64,7 @@ def planned_call(case, dc, max_partitions=0, score_exchange=0):
 
 
 @pytest.mark.parametrize("which", ["pair_spread", "pair_cluster", "many_rows", "e4m3_pair", "many_rows_fp16_exchange",
-                                   "e4m3_many_rows"])
+                                   "many_rows_f32_exchange", "e4m3_many_rows"])
 def test_bounded_waits_run_out_then_the_context_is_usable(which):
     if which == "pair_spread":      # 16 fp16 rows, 131072 tokens: partitions spread over clusters (tickets)
         case = gen.make_decode_case(21, [131072], num_heads=16, block_size=32, dtype="f16")
@@ -83,7 +83,8 @@ def test_bounded_waits_run_out_then_the_context_is_usable(which):
         heads = [0, 77, 127]
     dc = rt.upload(case)
     plan, ws, call = planned_call(case, dc, max_partitions=64 if case.num_heads == 128 else 0,
-                                  score_exchange=1 if which == "many_rows_fp16_exchange" else 0)
+                                  score_exchange={"many_rows_fp16_exchange": nb.MLA_SCORE_EXCHANGE_F16,
+                                                  "many_rows_f32_exchange": nb.MLA_SCORE_EXCHANGE_F32}.get(which, 0))
     if which == "pair_spread":
         assert plan.clusters_per_chunk > 1
     if which == "pair_cluster":
