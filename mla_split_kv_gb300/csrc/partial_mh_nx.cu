@@ -24,7 +24,11 @@
 // column) = 512. Shared memory: Q (4 swizzled [128 x 64] chunks and two
 // [128 x 32] rope boxes with the 64-byte swizzle, 80 KB) and two full-width
 // 64-token tile slots of 72 KB (both halves of ckv as one 4D TMA box per page
-// each, and both 32-column kpe boxes): 227 KB with the barriers.
+// each, and both 32-column kpe boxes): 227 KB with the barriers. A slot is
+// two parts with barriers of their own: this CTA's ckv half (the V operand,
+// free once PV is done) and the other half with the kpe (read by the score
+// product only, free once it is done), so the next tile's larger part loads
+// while PV still runs.
 //
 // Warp roles (384 threads): warps 0-7 softmax and epilogue (thread = row r =
 // TMEM lane 32 (w % 4) + lane; warps w and w + 4 share the rows and take the
@@ -71,7 +75,9 @@ constexpr uint32_t kTmemQ = 384;    // Q latent columns 0-255, 16-bit, two a col
 constexpr uint32_t kTmemCols = 512;
 
 struct Small {
-  uint64_t full[kSlots], empty[kSlots], sfull[2], ppfull[2], pvdone[2], drain;
+  // a slot in two parts: this CTA's ckv half (the V operand, free once PV is done) and the other ckv half
+  // with both kpe boxes (read by the score product only, free once it is done)
+  uint64_t full[kSlots], empty[kSlots], fullb[kSlots], emptyb[kSlots], sfull[2], ppfull[2], pvdone[2], drain;
   uint32_t tmem_base;
   int32_t abort_flag;
   float half_val[2][kRows];  // per row, the two token halves' tile maximum (then their sums)
@@ -111,6 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&sm->full[s], kPageWarps);  // one expect_tx arrival per producer warp
       mbar_init(&sm->empty[s], 1);
+      mbar_init(&sm->fullb[s], kPageWarps);
+      mbar_init(&sm->emptyb[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm->sfull[t], 1);
@@ -150,17 +158,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return __shfl_sync(0xffffffffu, win_pid, pg & 31);
     };
-    int issued = -1;
+    int issued_b = -1, issued_a = -1;  // the last tile whose score-only part, V half this warp issued
     for (int i = 0; i < ntiles; ++i) {
       const int s = i % kSlots;
-      if (i >= kSlots) {  // PV(i-2) released the slot
-        int ok = 1;
-        if (lane == 0) {
-          ok = mbar_wait(&sm->empty[s], ((i / kSlots) - 1) & 1, tmo) && !*abort_flag;
-          if (!ok) *abort_flag = 1;
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      }
       const int tok0 = w.sub0 + i * kT;
       const int pg0 = tok0 / p.bs;
       const int npg = (min(kT, w.sub1 - tok0) + p.bs - 1) / p.bs;
@@ -169,24 +169,52 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int m = 0; m < 2; ++m) pids[m] = (m < mine) ? page_of(pg0 + k0 + m * kPageWarps) : -1;
       uint8_t* slot = smem + kOffTile + s * kTileSlot;
+      const int other = half ^ 1;
+      // the score-only part first (the other ckv half, both kpe boxes): free once S(i-2) is done
+      if (i >= kSlots) {
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait(&sm->emptyb[s], ((i / kSlots) - 1) & 1, tmo) && !*abort_flag;
+          if (!ok) *abort_flag = 1;
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
       if (lane == 0)
-        mbar_arrive_expect_tx(&sm->full[s], static_cast<uint32_t>(mine * p.bs * (2 * kHalfCols + 2 * kKpeCols) * 2));
+        mbar_arrive_expect_tx(&sm->fullb[s], static_cast<uint32_t>(mine * p.bs * (kHalfCols + 2 * kKpeCols) * 2));
       __syncwarp();
-      // lane m issues this warp's page m: both ckv halves and both kpe boxes
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         if (lane == m && m < mine) {
           const int j = k0 + m * kPageWarps;
+          tma_load_4d(slot + other * kCkvBytes + j * p.bs * (kHalfCols * 2), &tm_pages, 0, 0, kHalfBoxes * other,
+                      pids[m] * (p.bs / 8), &sm->fullb[s], pol);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tma_load_4d(slot + h * kCkvBytes + j * p.bs * (kHalfCols * 2), &tm_pages, 0, 0, kHalfBoxes * h,
-                        pids[m] * (p.bs / 8), &sm->full[s], pol);
+          for (int h = 0; h < 2; ++h)
             tma_load_2d(slot + 2 * kCkvBytes + h * kKpeBytes + j * p.bs * (kKpeCols * 2), &tm_kpe_half, kKpeCols * h,
-                        pids[m] * p.bs, &sm->full[s], pol);
-          }
+                        pids[m] * p.bs, &sm->fullb[s], pol);
         }
       }
-      issued = i;
+      issued_b = i;
+      // then this CTA's ckv half (the V operand): free once PV(i-2) is done
+      if (i >= kSlots) {
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait(&sm->empty[s], ((i / kSlots) - 1) & 1, tmo) && !*abort_flag;
+          if (!ok) *abort_flag = 1;
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&sm->full[s], static_cast<uint32_t>(mine * p.bs * kHalfCols * 2));
+      __syncwarp();
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        if (lane == m && m < mine) {
+          const int j = k0 + m * kPageWarps;
+          tma_load_4d(slot + half * kCkvBytes + j * p.bs * (kHalfCols * 2), &tm_pages, 0, 0, kHalfBoxes * half,
+                      pids[m] * (p.bs / 8), &sm->full[s], pol);
+        }
+      }
+      issued_a = i;
       // an L2 prefetch of tile i + kPrefetch's pages (latent rows by the even CTA, rope rows by the odd one),
       // so that its slot load, which waits for PV(i + kPrefetch - 2) to free the slot, reads L2
       if (i + kPrefetch < ntiles) {
@@ -206,9 +234,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // after an abort, let this warp's loads still in flight land before shared memory is released
-    if (lane == 0 && *abort_flag)
-      for (int t = max(0, issued - (kSlots - 1)); t <= issued; ++t)
+    if (lane == 0 && *abort_flag) {
+      for (int t = max(0, issued_b - (kSlots - 1)); t <= issued_b; ++t)
+        mbar_wait(&sm->fullb[t % kSlots], (t / kSlots) & 1, kDrainTimeoutNs);
+      for (int t = max(0, issued_a - (kSlots - 1)); t <= issued_a; ++t)
         mbar_wait(&sm->full[t % kSlots], (t / kSlots) & 1, kDrainTimeoutNs);
+    }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     const uint32_t idesc_s = idesc_f16_f32(kRows, kT, BF16, false, false);         // A = Q, B = K tile
@@ -249,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 2; ++kk) umma_f16_ss(d, desc_add(qd, kk * 32), desc_add(kd, kk * 32), idesc_s, 1u);
         }
         umma_commit(&sm->sfull[t]);
+        umma_commit(&sm->emptyb[i % kSlots]);  // the score-only part of the slot is free
       }
       __syncwarp();
     };
@@ -299,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (np < ns && mbar_test(&sm->ppfull[np & 1], (np >> 1) & 1)) {
           act = 2;
         } else if (ns < ntiles && (ns < 2 || mbar_test(&sm->pvdone[ns & 1], ((ns >> 1) - 1) & 1)) &&
-                   mbar_test(&sm->full[ns % kSlots], (ns / kSlots) & 1)) {
+                   mbar_test(&sm->full[ns % kSlots], (ns / kSlots) & 1) &&
+                   mbar_test(&sm->fullb[ns % kSlots], (ns / kSlots) & 1)) {
           act = 1;
         } else if (*abort_flag) {
           act = -1;
